@@ -1,0 +1,132 @@
+"""AdaComp CPU oracle — TEST INFRASTRUCTURE ONLY.
+
+ctypes binding over ``adacomp_oracle.c``: a plain single-threaded C restatement of
+AdaComp's per-layer compressor (Algorithm 2 as restated in the "AdaComp (Adaptive
+Residual Gradient Compression)" entry, Claims > Mechanism
+#r629-local-bin-soft-threshold-and-mean-gmax-quantization) and of the K-learner
+decoder. Only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may import this package; the CUDA product path never does, and the two
+share no code.
+
+All arrays are numpy; residue is updated in place like the CUDA entry point does.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "adacomp_oracle.c")
+_LIB = os.path.join(_HERE, "libadacomp_oracle.so")
+_lib = None
+
+OK, ERR_ARG, ERR_CAPACITY, ERR_BAD_MESSAGE = 0, 1, 2, 3
+
+
+def build(force: bool = False) -> str:
+    """Compile the oracle with gcc: -O2, no FMA contraction, no fast-math."""
+    if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
+        tmp = _LIB + f".tmp{os.getpid()}"
+        subprocess.check_call(
+            ["gcc", "-std=c99", "-O2", "-ffp-contract=off", "-fno-fast-math", "-fPIC",
+             "-shared", "-Wall", "-o", tmp, _SRC, "-lm"])
+        os.replace(tmp, _LIB)
+    return _LIB
+
+
+class Oracle:
+    """ctypes view of one compiled oracle library (the default one, or a test's copy)."""
+
+    def __init__(self, path: str):
+        lib = ctypes.CDLL(path)
+        i64, i32, u64 = ctypes.c_int64, ctypes.c_int32, ctypes.c_uint64
+        vp = ctypes.c_void_p
+        lib.adacomp_oracle_max_msg_bytes.argtypes = [i64, i32]
+        lib.adacomp_oracle_max_msg_bytes.restype = i64
+        lib.adacomp_oracle_exact_sum_f32.argtypes = [vp, i64]
+        lib.adacomp_oracle_exact_sum_f32.restype = ctypes.c_double
+        lib.adacomp_oracle_compress.argtypes = [i64, i32, ctypes.c_int, vp, vp, vp, u64,
+                                                ctypes.POINTER(u64), vp, vp, vp, ctypes.c_int]
+        lib.adacomp_oracle_compress.restype = ctypes.c_int
+        lib.adacomp_oracle_decode_accumulate.argtypes = [i64, i32, vp, i32, vp]
+        lib.adacomp_oracle_decode_accumulate.restype = ctypes.c_int
+        self.lib = lib
+
+
+def _load():
+    global _lib
+    if _lib is None:
+        build()
+        _lib = Oracle(_LIB).lib
+    return _lib
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def max_msg_bytes(n: int, bin_len: int, lib=None) -> int:
+    return int((lib or _load()).adacomp_oracle_max_msg_bytes(n, bin_len))
+
+
+def exact_sum_f32(x: np.ndarray, lib=None) -> float:
+    """Exact sum of non-negative fp32 values, correctly rounded to fp64."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    return float((lib or _load()).adacomp_oracle_exact_sum_f32(_ptr(x), x.size))
+
+
+class CompressResult:
+    __slots__ = ("msg", "s", "gmax", "sel")
+
+    def __init__(self, msg, s, gmax, sel):
+        self.msg, self.s, self.gmax, self.sel = msg, s, gmax, sel
+
+
+def compress(residue: np.ndarray, dw: np.ndarray, bin_len: int,
+             literal_zero_select: bool = False, lib=None) -> CompressResult:
+    """One step for one layer. ``residue`` (fp32, contiguous) is updated in place.
+
+    ``dw`` is fp32, or uint16 holding bf16 bit patterns. Returns the message bytes,
+    s, g_max per bin and the 0/1 selection mask.
+    """
+    lib = lib or _load()
+    assert residue.dtype == np.float32 and residue.flags.c_contiguous
+    if dw.dtype == np.float32:
+        bf16 = 0
+    elif dw.dtype == np.uint16:
+        bf16 = 1
+    else:
+        raise TypeError("dw must be float32 or uint16 (bf16 bits)")
+    dw = np.ascontiguousarray(dw)
+    n = residue.size
+    assert dw.size == n and n >= 1
+    cap = max_msg_bytes(n, bin_len, lib)
+    if cap < 0:
+        raise ValueError("bad n / bin_len")
+    nb = -(-n // bin_len)
+    msg = np.zeros(cap, dtype=np.uint8)
+    gmax = np.zeros(nb, dtype=np.float32)
+    sel = np.zeros(n, dtype=np.uint8)
+    s = np.zeros(1, dtype=np.float32)
+    mlen = ctypes.c_uint64(0)
+    rc = lib.adacomp_oracle_compress(n, bin_len, bf16, _ptr(residue), _ptr(dw), _ptr(msg), cap,
+                                     ctypes.byref(mlen), _ptr(s), _ptr(gmax), _ptr(sel),
+                                     int(literal_zero_select))
+    if rc != OK:
+        raise RuntimeError(f"oracle compress failed: {rc}")
+    return CompressResult(msg[: mlen.value].copy(), s[0], gmax, sel.astype(bool))
+
+
+def decode_accumulate(n: int, bin_len: int, msgs, dense: np.ndarray, lib=None) -> int:
+    """Adds every message's sign*s_k into ``dense`` (fp32, in place), k in order.
+
+    Returns the oracle status (0 = OK, 3 = a malformed message, nothing added).
+    """
+    lib = lib or _load()
+    assert dense.dtype == np.float32 and dense.flags.c_contiguous and dense.size == n
+    bufs = [np.ascontiguousarray(m, dtype=np.uint8) for m in msgs]
+    arr = (ctypes.c_void_p * len(bufs))(*[b.ctypes.data for b in bufs])
+    return int(lib.adacomp_oracle_decode_accumulate(n, bin_len, arr, len(bufs), _ptr(dense)))
