@@ -1,0 +1,597 @@
+#!/usr/bin/env python3
+"""Benchmark of the AdaComp hot path on GB300: compress + decode-accumulate.
+
+One step = one pass of the whole path over one batch of synthetic gradients: every
+layer of the workload is compressed (fused streaming kernel + sparse fix-up) and
+the step's messages are decoded and accumulated into dense gradients. The default
+workload is the ResNet-50 gradient set (53 conv tensors at L_T = 50 with 8-bit
+codes and the 2048x1000 FC at L_T = 500 with 16-bit codes, 25.5M fp32 elements,
+carried residue), compressed by one grouped launch, with the single learner's
+messages decoded (K = 1). ``--workload flat100m`` runs 16 learners over a 10^8
+element layer and decodes all 16 messages.
+
+The JSON line reports gradient elements/s (value), algorithmic HBM GB/s and their
+fraction of the measured copy bandwidth, the dominant kernel's roofline, an
+end-to-end figure through the C ABI with host buffers, and the oracle timed on
+host cores. ``--impl reference`` times the oracle alone (this build's reference
+arm). With torchrun and N > 1 every rank runs an independent replica.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from residual_gradient_compression_gb300 import workloads as wl  # noqa: E402
+
+METRIC = "gradient elements/s and HBM GB/s (% of GB300 roofline) for compress+decode"
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    p = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--impl", choices=["adacomp", "reference"], default="adacomp")
+    p.add_argument("--workload", default="resnet50",
+                   choices=["resnet50", "fc400k", "lstm_fc", "gpt1p3b", "flat100m"])
+    p.add_argument("--bin-len", type=int, default=500, help="L_T for gpt1p3b")
+    p.add_argument("--learners", type=int, default=16, help="K for flat100m")
+    p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--min-timed-seconds", type=float, default=1.5,
+                   help="repeat the K timed steps until the clock sampler has covered this long")
+    return p.parse_args()
+
+
+# ---------------------------------------------------------------- distributed (replicas)
+def dist_init():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value over all ranks (the slowest replica sets the job's time)."""
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ---------------------------------------------------------------- workloads
+def workload_layers(args):
+    if args.workload == "gpt1p3b":
+        return wl.layers("gpt1p3b", args.bin_len)
+    return wl.layers(args.workload)
+
+
+def learners(args):
+    return args.learners if args.workload == "flat100m" else 1
+
+
+def chunks(seq, size):
+    return [seq[i:i + size] for i in range(0, len(seq), size)]
+
+
+def algorithmic_bytes(layers, nnz):
+    """Minimum bytes one compress of each layer must move, and one decode of it.
+
+    compress: read residue (4 B) and dW (2 or 4 B), write residue (4 B) per element;
+    write the message (8 + 2B + w*nnz); fix-up reads the counts (2B) and the codes
+    (w*nnz) and rewrites each sent residue (4 B read + 4 B write).
+    decode: read and write the dense element (8 B); read the message; the count scan
+    reads the counts once more (2B).
+    Returns (k1 bytes, fix-up bytes, decode bytes) summed over layers.
+    """
+    k1 = fix = dec = 0
+    for ly, z in zip(layers, nnz):
+        d = 2 if ly.dw_dtype == "bf16" else 4
+        B = -(-ly.numel // ly.bin_len)
+        w = 1 if ly.bin_len < 64 else 2
+        msg = 8 + 2 * B + w * z
+        k1 += ly.numel * (8 + d) + msg
+        fix += 2 * B + w * z + 8 * z
+        dec += 8 * ly.numel + msg + 2 * B
+    return k1, fix, dec
+
+
+def source_hash():
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(os.path.join(ROOT, "residual_gradient_compression_gb300", "csrc"))):
+        with open(os.path.join(ROOT, "residual_gradient_compression_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_hbm_gbs():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on the
+    current kernel sources; None otherwise."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+    except Exception:
+        return None
+    if rec.get("source_sha") != source_hash():
+        return None
+    return rec.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{gpu_index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}", "--format=csv,noheader",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.15)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        if not rows:
+            return None
+
+        def mhz(v):
+            try:
+                return float(v.split()[0])
+            except Exception:
+                return float("nan")
+        sm = [mhz(r[1]) for r in rows]
+        mx = [mhz(r[2]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i].lower() == "active"})
+        good = [x for x in sm if not math.isnan(x)]
+        return {"sm_mhz": statistics.median(good) if good else None,
+                "sm_max_mhz": max(x for x in mx if not math.isnan(x)) if mx else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+def _flat_views(total_numels, dtype, device, fill=None, pinned=False):
+    """One buffer holding several tensors, each starting on a 16-byte boundary."""
+    esz = torch.empty(0, dtype=dtype).element_size()
+    per = max(1, 16 // esz)
+    offs, cur = [], 0
+    for n in total_numels:
+        offs.append(cur)
+        cur += -(-n // per) * per
+    if pinned:
+        buf = torch.empty(max(cur, 1), dtype=dtype, pin_memory=True)
+    else:
+        buf = torch.zeros(max(cur, 1), dtype=dtype, device=device)
+    return buf, [buf[o:o + n] for o, n in zip(offs, total_numels)]
+
+
+class DeviceRun:
+    """All device buffers and prepared C-ABI calls of one replica."""
+
+    def __init__(self, args, layers, dev):
+        import ctypes
+        import residual_gradient_compression_gb300 as ac
+        from residual_gradient_compression_gb300 import build
+        build.build()
+        self.ac, self.ct, self.L = ac, ctypes, ac.lib()
+        self.args, self.layers, self.dev = args, layers, dev
+        self.K = learners(args)
+        self.sets = 4 if args.workload in ("resnet50", "fc400k", "lstm_fc") else 2
+        names = [l.name for l in wl.layers(args.workload, args.bin_len if args.workload == "gpt1p3b" else None)]
+        self.gidx = chunks(list(range(len(layers))), ac.MAX_GROUP)
+        self.h = [ac.adacomp_init_group([layers[i].numel for i in g], [layers[i].bin_len for i in g],
+                                        [ac.BF16 if layers[i].dw_dtype == "bf16" else ac.F32 for i in g])
+                  for g in self.gidx]
+        numels = [l.numel for l in layers]
+        bf16 = layers[0].dw_dtype == "bf16"
+        self.dw_dtype = torch.bfloat16 if bf16 else torch.float32
+        # residue per learner, dense per layer, dW sets per learner
+        self.res = [_flat_views(numels, torch.float32, dev) for _ in range(self.K)]
+        self.dense = _flat_views(numels, torch.float32, dev)
+        self.dw = []
+        for k in range(self.K):
+            per_set = []
+            for s in range(self.sets):
+                buf, views = _flat_views(numels, self.dw_dtype, dev)
+                for i, ly in enumerate(layers):
+                    views[i].copy_(wl.gen_dw(args.workload, names.index(ly.name), ly, s, learner=k, device=dev))
+                per_set.append((buf, views))
+            self.dw.append(per_set)
+        maxmsg = [m for h in self.h for m in h.max_msg_bytes]
+        self.msg = [_flat_views(maxmsg, torch.uint8, dev) for _ in range(self.K)]
+        self.dws_bytes = [h.decode_ws_bytes(self.K) for h in self.h]
+        self.dec_ws = [torch.zeros(b, dtype=torch.uint8, device=dev) for b in self.dws_bytes]
+        self.ring = max(1, args.steps)
+        self.ws = [[[torch.zeros(h.compress_ws_bytes, dtype=torch.uint8, device=dev) for h in self.h]
+                    for _ in range(self.K)] for _ in range(self.ring)]
+        self._prepare()
+
+    def _prepare(self):
+        ct, VP = self.ct, self.ct.c_void_p
+        self.c_res, self.c_msg, self.c_cap, self.c_dw = [], [], [], []
+        for k in range(self.K):
+            r, m, c = [], [], []
+            for g in self.gidx:
+                r.append((VP * len(g))(*[self.res[k][1][i].data_ptr() for i in g]))
+                m.append((VP * len(g))(*[self.msg[k][1][i].data_ptr() for i in g]))
+                c.append((ct.c_size_t * len(g))(*[self.msg[k][1][i].numel() for i in g]))
+            self.c_res.append(r)
+            self.c_msg.append(m)
+            self.c_cap.append(c)
+            self.c_dw.append([[(VP * len(g))(*[self.dw[k][s][1][i].data_ptr() for i in g]) for g in self.gidx]
+                              for s in range(self.sets)])
+        self.c_dec_msgs = [(VP * (len(g) * self.K))(*[self.msg[k][1][i].data_ptr() for i in g
+                                                        for k in range(self.K)]) for g in self.gidx]
+        self.c_dense = [(VP * len(g))(*[self.dense[1][i].data_ptr() for i in g]) for g in self.gidx]
+
+    def launches_per_step(self):
+        return self.K * len(self.gidx) * 2 + len(self.gidx) * 3
+
+    def step(self, i, stream_ptr, k1_events=None, dec_events=None):
+        """Enqueues one step: every learner's compress, then the decode of the step's messages."""
+        L, s = self.L, i % self.sets
+        for k in range(self.K):
+            for gi, h in enumerate(self.h):
+                if k1_events is not None:
+                    e = k1_events[k * len(self.h) + gi]
+                    L.adacomp_set_timing_events(h.ptr, self.ct.c_void_p(e[0].cuda_event),
+                                                self.ct.c_void_p(e[1].cuda_event),
+                                                self.ct.c_void_p(e[2].cuda_event))
+                ws = self.ws[i % self.ring][k][gi]
+                st = L.adacomp_compress_group(h.ptr, self.c_res[k][gi], self.c_dw[k][s][gi], self.c_msg[k][gi],
+                                              self.c_cap[k][gi], ws.data_ptr(), ws.numel(), stream_ptr)
+                if st:
+                    raise RuntimeError(f"adacomp_compress_group: {st}")
+        if dec_events is not None:
+            dec_events[0].record()
+        for gi, h in enumerate(self.h):
+            st = L.adacomp_decode_accumulate_group(h.ptr, self.c_dec_msgs[gi], self.K, self.c_dense[gi],
+                                                   self.dec_ws[gi].data_ptr(), self.dec_ws[gi].numel(),
+                                                   stream_ptr)
+            if st:
+                raise RuntimeError(f"adacomp_decode_accumulate_group: {st}")
+        if dec_events is not None:
+            dec_events[1].record()
+
+    def clear_timing(self):
+        for h in self.h:
+            self.L.adacomp_set_timing_events(h.ptr, None, None, None)
+
+    def step_results(self, i):
+        """[(nnz, msg_bytes, status)] per learner per layer for ring slot i."""
+        out = []
+        for k in range(self.K):
+            for gi, (h, g) in enumerate(zip(self.h, self.gidx)):
+                ws = self.ws[i % self.ring][k][gi]
+                blk = ws[64:64 + 2112 * len(g)].cpu().numpy()
+                for j in range(len(g)):
+                    o = 2112 * j + 2064
+                    status = int(blk[o + 4:o + 8].view(np.uint32)[0])
+                    nnz = int(blk[o + 8:o + 16].view(np.uint64)[0])
+                    mb = int(blk[o + 16:o + 24].view(np.uint64)[0])
+                    out.append((nnz, mb, status))
+        return out
+
+
+def _new_events(n):
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(n)]
+    for e in evs:
+        e.record()  # creates the underlying CUDA event
+    return evs
+
+
+def run_device(args, rank, world):
+    dev = torch.device("cuda", torch.cuda.current_device())
+    layers = workload_layers(args)
+    run = DeviceRun(args, layers, dev)
+    stream = torch.cuda.current_stream()
+    sp = run.ct.c_void_p(stream.cuda_stream)
+    n_elems = sum(l.numel for l in layers) * run.K
+
+    for i in range(args.warmup):
+        run.step(i, sp)
+    torch.cuda.synchronize()
+    for i in range(args.warmup):  # warm-up results must be clean
+        for nnz, mb, st in run.step_results(i):
+            if st != 0:
+                raise RuntimeError(f"device status {st} during warm-up")
+
+    ncalls = run.K * len(run.h)
+    k1_events = [[_new_events(3) for _ in range(ncalls)] for _ in range(args.steps)]
+    dec_events = [_new_events(2) for _ in range(args.steps)]
+    start, end = _new_events(2)
+    sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
+    if sampler:
+        sampler.start()
+    reps, t0 = [], time.perf_counter()
+    step_no = args.warmup
+    while True:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(args.steps):
+            run.step(step_no + i, sp, k1_events[i], dec_events[i])
+        end.record()
+        torch.cuda.synchronize()
+        barrier(world)
+        ms = start.elapsed_time(end)
+        k1 = [e[0].elapsed_time(e[1]) for st in k1_events for e in st]
+        fx = [e[1].elapsed_time(e[2]) for st in k1_events for e in st]
+        dec = [e[0].elapsed_time(e[1]) for e in dec_events]
+        res = [run.step_results(step_no + i) for i in range(args.steps)]
+        reps.append((ms, k1, fx, dec, res))
+        step_no += args.steps
+        if time.perf_counter() - t0 >= args.min_timed_seconds or len(reps) >= 500:
+            break
+    clocks = sampler.stop() if sampler else None
+    run.clear_timing()
+
+    # the median repetition is reported
+    order = sorted(range(len(reps)), key=lambda r: reps[r][0])
+    ms, k1, fx, dec, res = reps[order[len(order) // 2]]
+    ms = max_over_ranks(ms, world)
+    for step_res in res:
+        for nnz, mb, st in step_res:
+            if st != 0:
+                raise RuntimeError(f"device status {st} in the timed region")
+    lay_k = [ly for _ in range(run.K) for ly in layers]
+    per_step = [algorithmic_bytes(lay_k, [r[0] for r in step_res]) for step_res in res]
+    k1_bytes = sum(p[0] for p in per_step)
+    fix_bytes = sum(p[1] for p in per_step)
+    dec_bytes = sum(p[2] for p in per_step) / run.K  # one decode per layer per step
+    total_bytes = k1_bytes + fix_bytes + dec_bytes
+    msg_bytes = sum(r[1] for step_res in res for r in step_res)
+    nnz_total = sum(r[0] for step_res in res for r in step_res)
+    bins_total = sum(-(-ly.numel // ly.bin_len) for ly in lay_k) * args.steps
+
+    peak, peak_kind = measured_hbm_gbs()
+    k1_ms_per_launch = statistics.mean(k1)
+    k1_bytes_per_launch = k1_bytes / len(k1)
+    achieved = k1_bytes_per_launch / (k1_ms_per_launch * 1e-3) / 1e9
+    step_gbs = total_bytes / (ms * 1e-3) / 1e9
+    value = n_elems * args.steps * world / (ms * 1e-3)
+
+    out = {
+        "metric": METRIC, "value": value, "unit": "elements/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32" if run.dw_dtype == torch.float32 else "bf16+f32",
+        "data": "synthetic",
+        "config": {"workload": args.workload, "layers": len(layers), "elements_per_learner": n_elems // run.K,
+                   "learners": run.K, "bin_len": sorted({l.bin_len for l in layers}),
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": "inputs larger than L2 (dW rotates over %d sets)" % run.sets,
+                   "timed_repetitions": len(reps)},
+        "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+        "compress_ms_per_step": (sum(k1) + sum(fx)) / args.steps, "decode_ms_per_step": statistics.mean(dec),
+        "fixup_ms_per_launch": statistics.mean(fx), "compression_ratio": 4.0 * n_elems * args.steps / msg_bytes,
+        "sent_per_bin": nnz_total / bins_total,
+        "roofline": {"kernel": "compress_kernel", "bound": "hbm", "achieved": achieved, "peak": peak,
+                     "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                     "traffic": profiled_traffic("compress_kernel", args.workload),
+                     "bytes_per_launch": k1_bytes_per_launch, "ms_per_launch": k1_ms_per_launch},
+        "gpu_launches": run.launches_per_step() * args.steps,
+        "clocks": clocks,
+    }
+    if not args.no_e2e:
+        out["e2e"] = run_e2e(args, run, layers, sp, world)
+    return out, run
+
+
+def run_e2e(args, run, layers, sp, world):
+    """Same steps through the C ABI with host buffers: each step copies its dW from
+    pinned host memory, runs the path, reads every message length and copies the
+    messages back to pinned host memory."""
+    numels = [l.numel for l in layers]
+    host_dw = []
+    for k in range(run.K):
+        buf, views = _flat_views(numels, run.dw_dtype, "cpu", pinned=True)
+        buf.copy_(run.dw[k][0][0][:buf.numel()])
+        host_dw.append(buf)
+    host_msg = [torch.empty(run.msg[k][0].numel(), dtype=torch.uint8, pin_memory=True) for k in range(run.K)]
+    msg_offs = [[v.data_ptr() - run.msg[k][0].data_ptr() for v in run.msg[k][1]] for k in range(run.K)]
+    steps = args.steps
+    h2d = d2h = 0
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        slot = i % run.sets
+        for k in range(run.K):
+            dst = run.dw[k][slot][0]
+            dst[:host_dw[k].numel()].copy_(host_dw[k], non_blocking=True)
+            h2d += host_dw[k].numel() * host_dw[k].element_size()
+        run.step(i, sp)
+        res = run.step_results(i)  # synchronises: message lengths are on the device
+        d2h += sum(len(g) for g in run.gidx) * 2112 * run.K
+        j = 0
+        for k in range(run.K):
+            for li in range(len(layers)):
+                mb = res[j][1]
+                o = msg_offs[k][li]
+                host_msg[k][o:o + mb].copy_(run.msg[k][0][o:o + mb], non_blocking=True)
+                d2h += mb
+                j += 1
+    torch.cuda.synchronize()
+    secs = max_over_ranks(time.perf_counter() - t0, world)
+    n_elems = sum(numels) * run.K
+    return {"value": n_elems * steps * world / secs, "unit": "elements/s",
+            "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
+            "ms_per_step": secs * 1e3 / steps}
+
+
+# ---------------------------------------------------------------- oracle legs
+def oracle_sample_layers(args):
+    """The layers one oracle step covers: the whole workload when it is small,
+    otherwise a fixed slice of it (said in the JSON's `sample`)."""
+    layers = workload_layers(args)
+    if args.workload in ("resnet50", "fc400k", "flat100m"):
+        return layers, "all layers"
+    if args.workload == "lstm_fc":
+        return [layers[0], layers[4]], "one LSTM tensor + one FC tensor (25.2M elements)"
+    sub = [l for l in layers if l.name.startswith("h0.")]
+    return sub, "all tensors of one decoder block (50.4M elements)"
+
+
+def oracle_run(args, steps=None, budget_s=None, warmup=0):
+    """Runs the oracle on host cores: compress of every sampled layer (one learner,
+    carried residue) and decode of the step's messages. Returns (elements, seconds,
+    steps, sample text); input generation is outside the timed part."""
+    import oracle
+    oracle.build()
+    layers, sample = oracle_sample_layers(args)
+    names = [l.name for l in workload_layers(args)]
+    res = [np.zeros(l.numel, np.float32) for l in layers]
+    dense = [np.zeros(l.numel, np.float32) for l in layers]
+    elems = secs = 0.0
+    done = 0
+    i = 0
+    while True:
+        dws = []
+        for ly in layers:
+            t = wl.gen_dw(args.workload, names.index(ly.name), ly, i, device="cpu")
+            dws.append(t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy())
+        t0 = time.perf_counter()
+        for ly, r, d, dn in zip(layers, res, dws, dense):
+            out = oracle.compress(r, d, ly.bin_len)
+            oracle.decode_accumulate(ly.numel, ly.bin_len, [out.msg], dn)
+        dt = time.perf_counter() - t0
+        i += 1
+        if i <= warmup:
+            continue
+        secs += dt
+        elems += sum(l.numel for l in layers)
+        done += 1
+        if steps is not None and done >= steps:
+            break
+        if budget_s is not None and secs >= budget_s:
+            break
+    what = f"{args.workload}: {sample}, {done} step(s) of oracle compress + K=1 decode, carried residue"
+    return elems, secs, done, what
+
+
+def oracle_baseline(args):
+    elems, secs, done, what = oracle_run(args, budget_s=args.cpu_seconds, steps=max(args.steps, 1))
+    return {"value": elems / secs, "unit": "elements/s", "cores": 1, "kind": "oracle", "sample": what,
+            "seconds": secs, "host": _host()}
+
+
+def _host():
+    try:
+        model = ""
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith(("model name", "cpu part")):
+                    model = line.split(":", 1)[1].strip()
+                    break
+        return {"nproc": os.cpu_count(), "cpu": model, "arch": os.uname().machine}
+    except Exception:
+        return {"nproc": os.cpu_count()}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return None
+    elems, secs, done, what = oracle_run(args, steps=max(args.steps, 1), warmup=args.warmup)
+    v = elems / secs
+    layers = workload_layers(args)
+    return {
+        "metric": METRIC, "value": v, "unit": "elements/s", "n_gpus": int(os.environ.get("WORLD_SIZE", "1")),
+        "steps": done, "warmup": args.warmup, "ms_per_step": secs * 1e3 / done, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32" if layers[0].dw_dtype == "bf16" else "f32",
+        "data": "synthetic", "impl": "reference",
+        "config": {"workload": args.workload, "layers": len(layers), "learners": 1,
+                   "bin_len": sorted({l.bin_len for l in layers})},
+        "cpu_baseline": {"value": v, "unit": "elements/s", "cores": 1, "kind": "oracle", "sample": what,
+                         "host": _host()},
+        "e2e": {"value": v, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        out = run_reference(args)
+        if out is not None:
+            print(json.dumps(out), flush=True)
+        return 0
+    rank, world = dist_init()
+    out, run = run_device(args, rank, world)
+    del run
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        out["cpu_baseline"] = oracle_baseline(args)
+    if rank == 0:
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -1,0 +1,202 @@
+/*
+ * adacomp.h — C ABI of the GB300 (sm_103a) AdaComp library, libadacomp.so.
+ *
+ * AdaComp ("AdaComp (Adaptive Residual Gradient Compression)", summary paragraph and
+ * Claims > Mechanism #r629-local-bin-soft-threshold-and-mean-gmax-quantization) is a
+ * per-layer residual gradient compressor for data-parallel training. For one layer
+ * with residue r and gradient dW (N elements):
+ *     G = r + dW,  H = G + dW,  bins of length L_T over G,
+ *     g_max(i) = max |G| over bin i,  s = (1/B) sum_i g_max(i),
+ *     send every element with |H| >= g_max(i) as sign(G) * s,
+ *     r = G - sign(G) * s for sent elements, r = G for the rest.
+ * Codes are 8 bits when L_T < 64 and 16 bits otherwise (Claims > Application
+ * #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers; Curated
+ * Limitations). The pages leave open the points below; this library reads them so:
+ *   - a partial last bin is a bin; its g_max covers its own elements;
+ *   - only G != 0 is sent (sign(0) has no code); the tie |H| == g_max is sent;
+ *   - H = fl32(G + dW) after G is rounded; IEEE fp32 adds, no contraction;
+ *   - s = fl32( fl64(exact sum of the g_max) / B ), independent of summation order;
+ *   - decoding adds sign * s_k into a dense fp32 buffer learner by learner,
+ *     k = 0..K-1, with no averaging.
+ *
+ * Message format (little-endian, no padding), produced by adacomp_compress:
+ *     offset 0      float32  s
+ *     offset 4      uint32   B = ceil(N / L_T)
+ *     offset 8      uint16   count[B]          codes sent from each bin
+ *     offset 8+2B   codes, bin by bin, ascending offset within a bin;
+ *                   code = (offset_in_bin << 1) | (G < 0); uint8 if L_T < 64 else uint16
+ * Its length is 8 + 2B + w * nnz bytes (w = code bytes, nnz = elements sent); it never
+ * exceeds max_msg_bytes = 8 + 2B + w * N.
+ *
+ * Conventions shared by every call:
+ *   - Pointers named "device" are CUDA device pointers (e.g. torch tensor data_ptr());
+ *     the caller owns every buffer. The library never allocates device memory.
+ *   - residue, dW, dense and msg must be 16-byte aligned (ADACOMP_ERR_ALIGNMENT).
+ *   - Work is enqueued on `stream` and returns before it runs; results, the message
+ *     length and the device-side status are read back with adacomp_query /
+ *     adacomp_decode_status. Every call is deterministic: same inputs, same bits.
+ *   - Argument errors are reported synchronously before anything is enqueued.
+ *     ADACOMP_ERR_CUDA reports a failed launch (cudaGetLastError).
+ *   - Workspaces: a compress workspace must be zero-filled before its first use
+ *     (e.g. torch.zeros); every completed compress call leaves it zero-filled again
+ *     except for its result area, so it can be reused by later calls and by other
+ *     handles that fit in it. Calls that share a workspace must not overlap on the
+ *     GPU (use one stream, or order the streams). After any device-side error
+ *     status, zero the workspace again before reusing it.
+ *   - Device-side waits (the look-back between tiles) are bounded by a timeout
+ *     (default 2 s, adacomp_set_timeout_ns); on expiry the kernel records
+ *     ADACOMP_ERR_TIMEOUT in the workspace and returns. Nothing traps.
+ *   - L_T (bin_len) is limited to 1..8192 by this implementation (the format itself
+ *     would allow offsets up to 32767).
+ */
+#ifndef ADACOMP_H
+#define ADACOMP_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    ADACOMP_OK = 0,
+    ADACOMP_ERR_INVALID_ARG = 1,  /* n < 1, bin_len outside 1..8192, B >= 2^32, K outside 1..256 ... */
+    ADACOMP_ERR_ALIGNMENT = 2,    /* a buffer is not 16-byte aligned */
+    ADACOMP_ERR_WORKSPACE = 3,    /* ws is NULL or smaller than the size init returned */
+    ADACOMP_ERR_CAPACITY = 4,     /* msg_capacity < max_msg_bytes */
+    ADACOMP_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
+    ADACOMP_ERR_TIMEOUT = 6,      /* device: a bounded wait between tiles ran out */
+    ADACOMP_ERR_BAD_MESSAGE = 7   /* device: a message's B, counts or offsets do not fit this layer */
+} adacomp_status;
+
+typedef enum { ADACOMP_F32 = 0, ADACOMP_BF16 = 1 } adacomp_dtype;
+
+/* Opaque host-side handle: layer sizes, bin length, dW dtype and tile geometry. It
+ * holds no device memory and may be used from one host thread at a time. */
+typedef struct adacomp_layer* adacomp_layer_t;
+
+/*
+ * Describes one layer of n elements compressed with bins of bin_len elements and a
+ * dW of type dw_dtype ("AdaComp ...", Claims > Mechanism #r629-local-bin-...: one
+ * compressor per layer, with its own residue).
+ * Out (each may be NULL):
+ *   max_msg_bytes                 bytes a message buffer needs (8 + 2B + w*n)
+ *   compress_ws_bytes             bytes of compress workspace
+ *   decode_ws_bytes_per_learner   decode workspace = ADACOMP_DECODE_WS_FIXED + K * this
+ * Host only: makes no CUDA call. Errors: ADACOMP_ERR_INVALID_ARG.
+ */
+adacomp_status adacomp_init_layer(adacomp_layer_t* out, int64_t n, int32_t bin_len,
+                                  adacomp_dtype dw_dtype, size_t* max_msg_bytes,
+                                  size_t* compress_ws_bytes,
+                                  size_t* decode_ws_bytes_per_learner);
+
+/*
+ * A group of num_layers layers (1..ADACOMP_MAX_GROUP) compressed by one launch
+ * sequence: layer l has n[l] elements, bin length bin_len[l] and dW type
+ * dw_dtype[l]. Each layer keeps its own bins, s and message, exactly as if it were
+ * compressed alone; grouping only removes per-layer launches. max_msg_bytes is an
+ * array of num_layers entries (or NULL). Host only.
+ */
+adacomp_status adacomp_init_group(adacomp_layer_t* out, int32_t num_layers, const int64_t* n,
+                                  const int32_t* bin_len, const int32_t* dw_dtype,
+                                  size_t* max_msg_bytes, size_t* compress_ws_bytes,
+                                  size_t* decode_ws_bytes_per_learner);
+
+#define ADACOMP_MAX_GROUP 128
+#define ADACOMP_MAX_LEARNERS 256
+#define ADACOMP_DECODE_WS_FIXED 2048
+
+/*
+ * One AdaComp step for one layer (Algorithm 2 as restated in Claims > Mechanism
+ * #r629-local-bin-soft-threshold-and-mean-gmax-quantization).
+ *   residue   device fp32[n], in/out: the carried residue, updated in place
+ *             (zeros before the first step)
+ *   dW        device fp32[n] or bf16[n] (the dtype given at init), read only
+ *   msg       device buffer of msg_capacity >= max_msg_bytes bytes; receives the
+ *             message (format above)
+ *   ws        device compress workspace of ws_bytes >= compress_ws_bytes (see
+ *             Workspaces above)
+ * residue and dW must not overlap msg or ws. Errors: INVALID_ARG (NULL handle or
+ * pointer), ALIGNMENT, CAPACITY, WORKSPACE, CUDA. Device-side status via
+ * adacomp_query.
+ */
+adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* dW, void* msg,
+                                size_t msg_capacity, void* ws, size_t ws_bytes,
+                                cudaStream_t stream);
+
+/* adacomp_compress for every layer of a group: arrays of num_layers device pointers
+ * (host arrays) and capacities; one workspace for the whole group. */
+adacomp_status adacomp_compress_group(adacomp_layer_t h, float* const* residue,
+                                      const void* const* dW, void* const* msg,
+                                      const size_t* msg_capacity, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream);
+
+/*
+ * Sums K learners' messages into a dense gradient: for k = 0..K-1 in order, every
+ * code of msgs[k] adds sign * s_k to dense[bin * L_T + offset] (one fp32 add each).
+ * The pages only say that learners' quantised gradients are combined in
+ * data-parallel training (abstract; summary paragraph); the plain sum is this
+ * library's reading, and the caller zeroes dense for a fresh sum.
+ *   msgs   host array of K device pointers, each a message of this layer starting
+ *          on a 4-byte boundary
+ *   dense  device fp32[n], in/out
+ *   ws     device decode workspace, ws_bytes >= ADACOMP_DECODE_WS_FIXED
+ *          + K * decode_ws_bytes_per_learner; needs no initialisation
+ * One CTA owns each range of bins, so no two threads ever add to one element and
+ * no float atomics are used. A message whose header B, counts or code offsets do
+ * not fit the layer is skipped entirely and ADACOMP_ERR_BAD_MESSAGE is recorded
+ * (adacomp_decode_status); a code whose offset lies outside its bin is ignored and
+ * also recorded. Errors: INVALID_ARG (K outside 1..256, NULL pointers), ALIGNMENT
+ * (dense not 16-byte or a message not 4-byte aligned), WORKSPACE, CUDA.
+ */
+adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs, int32_t K,
+                                         float* dense, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream);
+
+/* Decode for every layer of a group: msgs is a host array of num_layers * K device
+ * pointers, layer-major (msgs[l * K + k]); dense a host array of num_layers device
+ * pointers. K <= ADACOMP_MAX_LEARNERS and K * num_layers <= 1024. */
+adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* const* msgs,
+                                               int32_t K, float* const* dense, void* ws,
+                                               size_t ws_bytes, cudaStream_t stream);
+
+/*
+ * Waits for `stream` and reads the result of the last compress call that used `ws`
+ * for layer `layer` (0 for a single layer): the message length in bytes, s, and the
+ * device status (ADACOMP_OK, ADACOMP_ERR_TIMEOUT). Any output may be NULL.
+ */
+adacomp_status adacomp_query(adacomp_layer_t h, const void* ws, int32_t layer,
+                             cudaStream_t stream, uint64_t* msg_bytes, float* s,
+                             int32_t* device_status);
+
+/* Waits for `stream` and reads the device status of the last decode call that used
+ * `ws` (ADACOMP_OK or ADACOMP_ERR_BAD_MESSAGE). */
+adacomp_status adacomp_decode_status(adacomp_layer_t h, const void* ws, cudaStream_t stream,
+                                     int32_t* device_status);
+
+/*
+ * Measurement hook (not part of the method): when set, every later compress call
+ * on this handle records `before` on its stream before the streaming kernel, `mid`
+ * between the streaming and the fix-up kernel, and `after` once both are enqueued,
+ * so cudaEventElapsedTime gives each kernel's duration. The events are created and
+ * owned by the caller; pass NULLs to stop recording.
+ */
+adacomp_status adacomp_set_timing_events(adacomp_layer_t h, cudaEvent_t before, cudaEvent_t mid,
+                                         cudaEvent_t after);
+
+/* Bound on each device-side wait, in nanoseconds (default 2e9). */
+adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns);
+
+/* Releases the handle. adacomp_free(NULL) does nothing. */
+void adacomp_free(adacomp_layer_t h);
+
+/* Static text for a status code. */
+const char* adacomp_status_string(adacomp_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ADACOMP_H */

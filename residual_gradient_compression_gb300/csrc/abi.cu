@@ -1,0 +1,266 @@
+// C ABI of libadacomp.so (declared in include/adacomp.h): handles, argument
+// checks, workspace sizing and launches. The library allocates no device memory;
+// every buffer and stream comes from the caller.
+#include "adacomp_internal.cuh"
+
+#include <cstddef>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "../../include/adacomp.h"
+
+struct adacomp_layer {
+    std::vector<adacomp::KLayer> layers;  // device pointers are filled in per call
+    uint32_t total_tiles = 0;
+    uint32_t tile_cap = 0;
+    uint16_t max_bins = 0;
+    uint16_t d_size = 2;
+    uint64_t timeout_ns = 2000000000ull;
+    size_t compress_ws = 0;
+    size_t decode_per_learner = 0;
+    cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // optional timing events
+};
+
+namespace {
+
+using adacomp::KGroup;
+using adacomp::KLayer;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+size_t max_msg_bytes(const KLayer& l) { return 8 + 2 * (size_t)l.nbins + (size_t)l.code_bytes * (size_t)l.n; }
+
+adacomp_status make_group(adacomp_layer_t* out, int32_t num_layers, const int64_t* n, const int32_t* bin_len,
+                          const int32_t* dtype, size_t* max_msg, size_t* cws, size_t* dws)
+{
+    if (!out) return ADACOMP_ERR_INVALID_ARG;
+    *out = nullptr;
+    if (num_layers < 1 || num_layers > ADACOMP_MAX_GROUP || !n || !bin_len || !dtype)
+        return ADACOMP_ERR_INVALID_ARG;
+    adacomp_layer* h = new (std::nothrow) adacomp_layer;
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    uint64_t tiles = 0;
+    for (int32_t i = 0; i < num_layers; ++i) {
+        const int64_t N = n[i];
+        const int32_t L = bin_len[i];
+        if (N < 1 || L < 1 || L > adacomp::kMaxBinLen || (dtype[i] != ADACOMP_F32 && dtype[i] != ADACOMP_BF16)) {
+            delete h;
+            return ADACOMP_ERR_INVALID_ARG;
+        }
+        const int64_t B = (N + L - 1) / L;
+        if (B >= (int64_t)1 << 32) { delete h; return ADACOMP_ERR_INVALID_ARG; }
+        KLayer k;
+        std::memset(&k, 0, sizeof k);
+        k.n = N;
+        k.nbins = (uint32_t)B;
+        k.bin_len = L;
+        int64_t bpt = adacomp::kTileTarget / L;
+        if (bpt < 1) bpt = 1;
+        if (bpt > adacomp::kMaxBinsPerTile) bpt = adacomp::kMaxBinsPerTile;
+        if (bpt > B) bpt = B;
+        k.bins_per_tile = (uint32_t)bpt;
+        k.num_tiles = (uint32_t)((B + bpt - 1) / bpt);
+        k.tile_begin = (uint32_t)tiles;
+        tiles += k.num_tiles;
+        k.dw_bf16 = dtype[i] == ADACOMP_BF16 ? 1 : 0;
+        k.code_bytes = L < 64 ? 1 : 2;
+        k.vec = (L % 4 == 0) ? 4 : (L % 2 == 0) ? 2 : 1;
+        if (!k.dw_bf16) h->d_size = 4;
+        const uint64_t te = (uint64_t)bpt * (uint64_t)L;
+        if (te > h->tile_cap) h->tile_cap = (uint32_t)te;
+        if (bpt > h->max_bins) h->max_bins = (uint16_t)bpt;
+        h->layers.push_back(k);
+        if (max_msg) max_msg[i] = max_msg_bytes(k);
+    }
+    if (tiles >= (1ull << 31)) { delete h; return ADACOMP_ERR_INVALID_ARG; }
+    h->total_tiles = (uint32_t)tiles;
+    h->compress_ws = adacomp::compress_ws_bytes(num_layers, tiles);
+    h->decode_per_learner = adacomp::decode_per_learner(tiles);
+    if (cws) *cws = h->compress_ws;
+    if (dws) *dws = h->decode_per_learner;
+    *out = h;
+    return ADACOMP_OK;
+}
+
+void fill_group(const adacomp_layer* h, KGroup* g)
+{
+    g->num_layers = (int32_t)h->layers.size();
+    g->total_tiles = h->total_tiles;
+    g->tile_cap = h->tile_cap;
+    g->max_bins = h->max_bins;
+    g->d_size = h->d_size;
+    g->timeout_ns = h->timeout_ns;
+    for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];
+}
+
+adacomp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ADACOMP_OK : ADACOMP_ERR_CUDA; }
+
+}  // namespace
+
+extern "C" {
+
+adacomp_status adacomp_init_layer(adacomp_layer_t* out, int64_t n, int32_t bin_len, adacomp_dtype dw_dtype,
+                                  size_t* max_msg_bytes, size_t* compress_ws_bytes,
+                                  size_t* decode_ws_bytes_per_learner)
+{
+    const int32_t dt = (int32_t)dw_dtype;
+    return make_group(out, 1, &n, &bin_len, &dt, max_msg_bytes, compress_ws_bytes, decode_ws_bytes_per_learner);
+}
+
+adacomp_status adacomp_init_group(adacomp_layer_t* out, int32_t num_layers, const int64_t* n,
+                                  const int32_t* bin_len, const int32_t* dw_dtype, size_t* max_msg_bytes,
+                                  size_t* compress_ws_bytes, size_t* decode_ws_bytes_per_learner)
+{
+    return make_group(out, num_layers, n, bin_len, dw_dtype, max_msg_bytes, compress_ws_bytes,
+                      decode_ws_bytes_per_learner);
+}
+
+adacomp_status adacomp_compress_group(adacomp_layer_t h, float* const* residue, const void* const* dW,
+                                      void* const* msg, const size_t* msg_capacity, void* ws, size_t ws_bytes,
+                                      cudaStream_t stream)
+{
+    if (!h || !residue || !dW || !msg || !msg_capacity || !ws) return ADACOMP_ERR_INVALID_ARG;
+    if (!aligned(ws, 16)) return ADACOMP_ERR_ALIGNMENT;
+    if (ws_bytes < h->compress_ws) return ADACOMP_ERR_WORKSPACE;
+    KGroup* g = new (std::nothrow) KGroup;
+    if (!g) return ADACOMP_ERR_INVALID_ARG;
+    std::memset(g, 0, sizeof *g);
+    fill_group(h, g);
+    for (size_t i = 0; i < h->layers.size(); ++i) {
+        if (!residue[i] || !dW[i] || !msg[i]) { delete g; return ADACOMP_ERR_INVALID_ARG; }
+        if (!aligned(residue[i], 16) || !aligned(dW[i], 16) || !aligned(msg[i], 16)) {
+            delete g;
+            return ADACOMP_ERR_ALIGNMENT;
+        }
+        if (msg_capacity[i] < max_msg_bytes(h->layers[i])) { delete g; return ADACOMP_ERR_CAPACITY; }
+        g->layer[i].residue = residue[i];
+        g->layer[i].dw = dW[i];
+        g->layer[i].msg = static_cast<uint8_t*>(msg[i]);
+    }
+    const cudaError_t e = adacomp::launch_compress(*g, ws, stream, h->ev[0], h->ev[1], h->ev[2]);
+    delete g;
+    return cuda_status(e);
+}
+
+adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* dW, void* msg, size_t msg_capacity,
+                                void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
+    return adacomp_compress_group(h, &residue, &dW, &msg, &msg_capacity, ws, ws_bytes, stream);
+}
+
+adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
+                                               float* const* dense, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!h || !msgs || !dense || !ws) return ADACOMP_ERR_INVALID_ARG;
+    const int64_t L = (int64_t)h->layers.size();
+    if (K < 1 || K > ADACOMP_MAX_LEARNERS || (int64_t)K * L > adacomp::kMaxDecodePairs)
+        return ADACOMP_ERR_INVALID_ARG;
+    if (!aligned(ws, 16)) return ADACOMP_ERR_ALIGNMENT;
+    if (ws_bytes < adacomp::kDecodeFixed + (size_t)K * h->decode_per_learner) return ADACOMP_ERR_WORKSPACE;
+    KGroup* g = new (std::nothrow) KGroup;
+    adacomp::DecodeParams* p = new (std::nothrow) adacomp::DecodeParams;
+    if (!g || !p) { delete g; delete p; return ADACOMP_ERR_INVALID_ARG; }
+    std::memset(g, 0, sizeof *g);
+    std::memset(p, 0, sizeof *p);
+    fill_group(h, g);
+    p->K = K;
+    adacomp_status st = ADACOMP_OK;
+    for (int64_t l = 0; l < L && st == ADACOMP_OK; ++l) {
+        if (!dense[l]) st = ADACOMP_ERR_INVALID_ARG;
+        else if (!aligned(dense[l], 16)) st = ADACOMP_ERR_ALIGNMENT;
+        p->dense[l] = dense[l];
+        for (int32_t k = 0; k < K && st == ADACOMP_OK; ++k) {
+            const void* m = msgs[l * K + k];
+            if (!m) st = ADACOMP_ERR_INVALID_ARG;
+            else if (!aligned(m, 4)) st = ADACOMP_ERR_ALIGNMENT;
+            p->msg[l * K + k] = static_cast<const uint8_t*>(m);
+        }
+    }
+    if (st == ADACOMP_OK) st = cuda_status(adacomp::launch_decode(*g, *p, ws, stream));
+    delete g;
+    delete p;
+    return st;
+}
+
+adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs, int32_t K, float* dense,
+                                         void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
+    return adacomp_decode_accumulate_group(h, msgs, K, &dense, ws, ws_bytes, stream);
+}
+
+adacomp_status adacomp_query(adacomp_layer_t h, const void* ws, int32_t layer, cudaStream_t stream,
+                             uint64_t* msg_bytes, float* s, int32_t* device_status)
+{
+    if (!h || !ws || layer < 0 || layer >= (int32_t)h->layers.size()) return ADACOMP_ERR_INVALID_ARG;
+    adacomp::Result r;
+    const uint8_t* src = static_cast<const uint8_t*>(ws) + adacomp::ws_layer_offset(layer) +
+                         offsetof(adacomp::LayerWs, result);
+    cudaError_t e = cudaMemcpyAsync(&r, src, sizeof r, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return ADACOMP_ERR_CUDA;
+    if (msg_bytes) *msg_bytes = r.msg_bytes;
+    if (s) *s = r.s;
+    if (device_status) *device_status = (int32_t)r.status;
+    return ADACOMP_OK;
+}
+
+adacomp_status adacomp_decode_status(adacomp_layer_t h, const void* ws, cudaStream_t stream,
+                                     int32_t* device_status)
+{
+    if (!h || !ws) return ADACOMP_ERR_INVALID_ARG;
+    uint8_t fixed[adacomp::kDecodeFixed];
+    cudaError_t e = cudaMemcpyAsync(fixed, ws, sizeof fixed, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return ADACOMP_ERR_CUDA;
+    uint32_t K, L;
+    std::memcpy(&K, fixed, 4);
+    std::memcpy(&L, fixed + 4, 4);
+    int32_t st = ADACOMP_OK;
+    if ((uint64_t)K * L > (uint64_t)adacomp::kMaxDecodePairs) st = ADACOMP_ERR_BAD_MESSAGE;
+    else
+        for (uint32_t i = 0; i < K * L; ++i)
+            if (fixed[16 + i]) st = ADACOMP_ERR_BAD_MESSAGE;
+    if (device_status) *device_status = st;
+    return ADACOMP_OK;
+}
+
+adacomp_status adacomp_set_timing_events(adacomp_layer_t h, cudaEvent_t before, cudaEvent_t mid,
+                                         cudaEvent_t after)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    h->ev[0] = before;
+    h->ev[1] = mid;
+    h->ev[2] = after;
+    return ADACOMP_OK;
+}
+
+adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns)
+{
+    if (!h || timeout_ns == 0) return ADACOMP_ERR_INVALID_ARG;
+    h->timeout_ns = timeout_ns;
+    return ADACOMP_OK;
+}
+
+void adacomp_free(adacomp_layer_t h) { delete h; }
+
+const char* adacomp_status_string(adacomp_status s)
+{
+    switch (s) {
+    case ADACOMP_OK: return "ok";
+    case ADACOMP_ERR_INVALID_ARG: return "invalid argument";
+    case ADACOMP_ERR_ALIGNMENT: return "buffer not aligned";
+    case ADACOMP_ERR_WORKSPACE: return "workspace too small";
+    case ADACOMP_ERR_CAPACITY: return "message buffer too small";
+    case ADACOMP_ERR_CUDA: return "CUDA error";
+    case ADACOMP_ERR_TIMEOUT: return "device wait timed out";
+    case ADACOMP_ERR_BAD_MESSAGE: return "malformed message";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,228 @@
+// Internal definitions shared by the AdaComp kernels and the C ABI host code:
+// per-layer launch descriptors, workspace layout, tile geometry and inline-PTX
+// helpers (mbarrier, bulk async copies, proxy fences) for sm_103a.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace adacomp {
+
+// ---------------------------------------------------------------- limits
+constexpr int kMaxBinLen = 8192;       // bins are processed whole inside one CTA
+constexpr int kMaxGroup = 128;         // layers per launch (by-value kernel parameter)
+constexpr int kMaxBinsPerTile = 1024;  // per-tile bin arrays in shared memory
+constexpr int kTileTarget = 4096;      // elements per tile (whole bins)
+constexpr int kThreads = 256;          // compress CTA size
+constexpr int kWarps = kThreads / 32;
+constexpr int kRounds = 4;             // lane-vectors per chunk: chunk <= 32*VEC*kRounds elements
+
+// ---------------------------------------------------------------- descriptors
+// One layer of a launch. Tiles of all layers are numbered consecutively in layer
+// order; tile t of layer l covers bins [ (t - tile_begin) * bins_per_tile, ... ).
+struct KLayer {
+    float* residue;          // fp32[n], in/out
+    const void* dw;          // fp32[n] or bf16[n]
+    uint8_t* msg;            // message buffer
+    int64_t n;               // elements
+    uint32_t nbins;          // B = ceil(n / bin_len)
+    int32_t bin_len;         // L_T
+    uint32_t tile_begin;     // first global tile index of the layer
+    uint32_t num_tiles;
+    uint32_t bins_per_tile;
+    uint8_t dw_bf16;
+    uint8_t code_bytes;      // 1 if L_T < 64 else 2
+    uint8_t vec;             // 4, 2 or 1: largest of these dividing L_T
+    uint8_t pad0;
+    uint32_t pad1;
+};
+static_assert(sizeof(KLayer) == 64, "KLayer layout");
+
+struct KGroup {
+    KLayer layer[kMaxGroup];
+    int32_t num_layers;
+    uint32_t total_tiles;
+    uint32_t tile_cap;       // max tile elements over the group (shared memory sizing)
+    uint16_t max_bins;       // max bins per tile over the group
+    uint16_t d_size;         // 4 if any layer has fp32 dW, else 2
+    uint64_t timeout_ns;
+};
+
+// Dynamic shared memory of the compress kernel (bytes), laid out in this order:
+// 2 stages x {residue slice, dW slice}, code staging, g_max, counts, exponent
+// histogram, 2 mbarriers, per-warp scalars.
+struct SmemPlan {
+    uint32_t r_bytes, d_bytes, stg_bytes, bin_bytes, total;
+};
+__host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size, uint32_t max_bins)
+{
+    SmemPlan p;
+    p.r_bytes = ((tile_cap + 8) * 4 + 127) & ~127u;
+    p.d_bytes = ((tile_cap + 16) * d_size + 127) & ~127u;
+    p.stg_bytes = (tile_cap * 2 + 127) & ~127u;
+    p.bin_bytes = (max_bins * 4 + 127) & ~127u;
+    p.total = 2 * (p.r_bytes + p.d_bytes) + p.stg_bytes + 2 * p.bin_bytes + 2048 + 16 + 256;
+    return p;
+}
+
+// ---------------------------------------------------------------- compress workspace
+// [Ctl 64 B][LayerWs x num_layers][desc u64 x T][tile_excl u64 x T]
+struct Ctl {
+    uint32_t ticket;         // next tile to hand out; reset to 0 by the fix-up kernel
+    uint32_t pad[15];
+};
+
+struct Result {              // written by each call, kept for adacomp_query
+    float s;
+    uint32_t status;
+    uint64_t nnz;
+    uint64_t msg_bytes;
+    uint64_t pad;
+};
+
+struct LayerWs {
+    unsigned long long acc[256];  // exact sum of g_max: integer mantissas per fp32 exponent
+    uint32_t done;                // tiles finished; the last one finalises the layer
+    uint32_t err;                 // device-side error bits of this call
+    uint32_t pad[2];
+    Result result;
+    uint32_t pad2[4];
+};
+static_assert(sizeof(LayerWs) % 64 == 0, "LayerWs alignment");
+
+__host__ __device__ inline size_t ws_layer_offset(int l) { return sizeof(Ctl) + (size_t)l * sizeof(LayerWs); }
+__host__ __device__ inline size_t ws_desc_offset(int num_layers) { return sizeof(Ctl) + (size_t)num_layers * sizeof(LayerWs); }
+__host__ __device__ inline size_t compress_ws_bytes(int num_layers, uint64_t total_tiles)
+{
+    return ws_desc_offset(num_layers) + 16 * (size_t)total_tiles;
+}
+
+// Look-back descriptor: flag in bits 62..63, value in bits 0..61.
+constexpr uint64_t kFlagAgg = 1ull << 62;
+constexpr uint64_t kFlagIncl = 2ull << 62;
+constexpr uint64_t kFlagErr = 3ull << 62;
+constexpr uint64_t kValueMask = (1ull << 62) - 1;
+
+// ---------------------------------------------------------------- decode workspace
+// [fixed 2048 B: u32 K, u32 num_layers, u32 pad[2], u8 bad[num_layers * K]]
+// [per learner k: tile_off u64 x T]
+// bad[l*K+k] and tile_off are written by every decode call before they are read, so
+// the decode workspace needs no initialisation. tile_off = kBadOffset marks a
+// (layer, learner) message that is skipped.
+constexpr size_t kDecodeFixed = 2048;
+constexpr int kMaxDecodePairs = 1024;  // num_layers * K per launch
+constexpr uint64_t kBadOffset = ~0ull;
+__host__ __device__ inline size_t decode_per_learner(uint64_t total_tiles) { return 8 * (size_t)total_tiles; }
+
+constexpr uint32_t kErrTimeout = 1;
+
+struct DecodeParams {
+    const uint8_t* msg[kMaxDecodePairs];  // [layer * K + k]
+    float* dense[kMaxGroup];
+    int32_t K;
+    int32_t pad;
+};
+
+// ---------------------------------------------------------------- host-side launchers
+cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cudaEvent_t ev_before = nullptr,
+                            cudaEvent_t ev_mid = nullptr, cudaEvent_t ev_after = nullptr);
+cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cudaStream_t stream);
+
+}  // namespace adacomp
+
+// ---------------------------------------------------------------- device helpers
+#ifdef __CUDACC__
+namespace adacomp {
+namespace ptx {
+
+__device__ __forceinline__ uint32_t smem_addr(const void* p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+// Makes mbarrier initialisation visible to the async proxy (bulk copies).
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+// Returns true once the phase with the given parity has completed.
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Global -> shared bulk copy (non-tensor TMA), completion counted on an mbarrier.
+// dst, src and bytes must be multiples of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// Shared -> global bulk copy, tracked by the issuing thread's bulk group.
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes)
+{
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_addr(src)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until every committed bulk store has finished reading shared memory.
+__device__ __forceinline__ void bulk_wait_read0() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// Waits until every committed bulk store has completed.
+__device__ __forceinline__ void bulk_wait0() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads.
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t ld_relaxed(const uint64_t* p)
+{
+    uint64_t v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_relaxed(uint64_t* p, uint64_t v)
+{
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ uint64_t globaltimer()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+}  // namespace ptx
+}  // namespace adacomp
+#endif

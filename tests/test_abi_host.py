@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI (no GPU needed).
+
+The library builds for sm_103a, loads, exports every function declared in
+include/adacomp.h, sizes buffers as the header states, and rejects bad arguments
+synchronously before any CUDA call is made.
+"""
+import ctypes
+import os
+import re
+
+import pytest
+
+import residual_gradient_compression_gb300 as ac
+from residual_gradient_compression_gb300 import build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    build.build()
+    ac.lib()
+
+
+def _declared():
+    text = open(os.path.join(ROOT, "include", "adacomp.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return set(re.findall(r"\b(adacomp_\w+)\s*\(", text))
+
+
+def test_every_declared_symbol_is_exported():
+    names = _declared()
+    assert {"adacomp_init_layer", "adacomp_compress", "adacomp_decode_accumulate", "adacomp_free"} <= names
+    for name in names:
+        assert hasattr(ac.lib(), name), name
+
+
+def test_sizes_follow_the_message_format():
+    for n, L, w in ((10, 4, 1), (400_000, 500, 2), (1003, 63, 1), (1003, 64, 2), (1, 1, 1)):
+        h = ac.adacomp_init_layer(n, L, ac.F32)
+        B = -(-n // L)
+        assert h.max_msg_bytes == [8 + 2 * B + w * n]
+        assert h.compress_ws_bytes > 0 and h.decode_ws_bytes_per_learner > 0
+        ac.adacomp_free(h)
+
+
+@pytest.mark.parametrize("n,L,dt", [(0, 4, 0), (-5, 4, 0), (10, 0, 0), (10, 8193, 0), (10, 4, 2)])
+def test_init_rejects_bad_arguments(n, L, dt):
+    with pytest.raises(ac.AdacompError) as e:
+        ac.adacomp_init_layer(n, L, dt)
+    assert e.value.status == ac.ERR_INVALID_ARG
+
+
+def test_group_limits():
+    with pytest.raises(ac.AdacompError):
+        ac.adacomp_init_group([], [], [])
+    with pytest.raises(ac.AdacompError):
+        ac.adacomp_init_group([10] * 129, [4] * 129, [0] * 129)
+    h = ac.adacomp_init_group([10, 20, 30], [4, 64, 500], [0, 1, 0])
+    assert len(h.max_msg_bytes) == 3
+    ac.adacomp_free(h)
+
+
+def _raw_compress(h, residue, dw, msg, cap, ws, wsb):
+    return ac.lib().adacomp_compress(h.ptr if h else None, residue, dw, msg, cap, ws, wsb, None)
+
+
+def test_compress_argument_checks_return_before_launch():
+    h = ac.adacomp_init_layer(1000, 50, ac.F32)
+    cap, wsb = h.max_msg_bytes[0], h.compress_ws_bytes
+    A = 1 << 20  # a 16-byte-aligned stand-in address; no call below reaches the GPU
+    assert _raw_compress(None, A, A, A, cap, A, wsb) == ac.ERR_INVALID_ARG
+    assert _raw_compress(h, None, A, A, cap, A, wsb) == ac.ERR_INVALID_ARG
+    assert _raw_compress(h, A + 4, A, A, cap, A, wsb) == ac.ERR_ALIGNMENT
+    assert _raw_compress(h, A, A + 2, A, cap, A, wsb) == ac.ERR_ALIGNMENT
+    assert _raw_compress(h, A, A, A + 8, cap, A, wsb) == ac.ERR_ALIGNMENT
+    assert _raw_compress(h, A, A, A, cap - 1, A, wsb) == ac.ERR_CAPACITY
+    assert _raw_compress(h, A, A, A, cap, A, wsb - 1) == ac.ERR_WORKSPACE
+    assert _raw_compress(h, A, A, A, cap, None, wsb) == ac.ERR_INVALID_ARG
+    ac.adacomp_free(h)
+
+
+def test_decode_argument_checks_return_before_launch():
+    h = ac.adacomp_init_layer(1000, 50, ac.F32)
+    A = 1 << 20
+    L = ac.lib()
+    one = (ctypes.c_void_p * 1)(A)
+    wsb = h.decode_ws_bytes(1)
+    assert L.adacomp_decode_accumulate(h.ptr, one, 0, A, A, wsb, None) == ac.ERR_INVALID_ARG
+    assert L.adacomp_decode_accumulate(h.ptr, one, 257, A, A, 1 << 30, None) == ac.ERR_INVALID_ARG
+    assert L.adacomp_decode_accumulate(h.ptr, one, 1, A + 4, A, wsb, None) == ac.ERR_ALIGNMENT
+    bad = (ctypes.c_void_p * 1)(A + 2)
+    assert L.adacomp_decode_accumulate(h.ptr, bad, 1, A, A, wsb, None) == ac.ERR_ALIGNMENT
+    assert L.adacomp_decode_accumulate(h.ptr, one, 1, A, A, wsb - 1, None) == ac.ERR_WORKSPACE
+    null = (ctypes.c_void_p * 1)(None)
+    assert L.adacomp_decode_accumulate(h.ptr, null, 1, A, A, wsb, None) == ac.ERR_INVALID_ARG
+    ac.adacomp_free(h)
+
+
+def test_status_strings_and_free_null():
+    for s in range(8):
+        assert ac.adacomp_status_string(s) not in ("", "unknown status")
+    ac.lib().adacomp_free(None)
+    assert ac.lib().adacomp_set_timeout_ns(None, 5) == ac.ERR_INVALID_ARG

@@ -1,0 +1,141 @@
+"""CUDA decode-and-accumulate vs the oracle (GPU).
+
+The pages only say that the learners' quantised gradients are combined in
+data-parallel training ("AdaComp (Adaptive Residual Gradient Compression)",
+abstract and summary paragraph); the library reads this as a plain fp32 sum in
+learner order. The bar is bit-exact against the oracle's decoder on the same
+message bytes.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import residual_gradient_compression_gb300 as ac
+from residual_gradient_compression_gb300 import workloads as wl
+from _gpu import GpuLayer, dw_host, ensure_built, workspace
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    ensure_built()
+
+
+def _learner_msgs(n, L, K, seed, bf16=False):
+    """K learners' messages from the CUDA compressor (itself checked against the
+    oracle elsewhere), each with a few steps of carried residue behind it."""
+    msgs = []
+    layer = GpuLayer(n, L, ac.BF16 if bf16 else ac.F32)
+    for k in range(K):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed + 1000 * k)
+        res = torch.randn(n, generator=g, device="cuda") * 1e-3
+        dw = torch.randn(n, generator=g, device="cuda") * 1e-3
+        if bf16:
+            dw = dw.to(torch.bfloat16)
+        ac.adacomp_compress(layer.h, res, dw, layer.msg, layer.ws)
+        mb, _, st = ac.adacomp_query(layer.h, layer.ws)
+        assert st == ac.OK
+        buf = torch.zeros(((mb + 15) // 16) * 16, dtype=torch.uint8, device="cuda")
+        buf[:mb] = layer.msg[:mb]
+        msgs.append((buf, mb))
+    return msgs
+
+
+def _gpu_decode(h, msgs, dense0):
+    dense = dense0.clone()
+    ws = workspace(h.decode_ws_bytes(len(msgs)))
+    ac.adacomp_decode_accumulate(h, [m for m, _ in msgs], dense, ws)
+    return dense.cpu().numpy(), ac.adacomp_decode_status(h, ws)
+
+
+@pytest.mark.parametrize("n,L,K", [(10, 4, 1), (1, 1, 2), (100_003, 50, 1), (100_003, 50, 3),
+                                   (1_000_001, 500, 16), (300_007, 5000, 5), (77_777, 7, 4),
+                                   (65_537, 64, 2)])
+def test_decode_matches_oracle(n, L, K):
+    msgs = _learner_msgs(n, L, K, seed=n + L)
+    h = ac.adacomp_init_layer(n, L, ac.F32)
+    dense0 = torch.randn(n, device="cuda") * 1e-3
+    got, st = _gpu_decode(h, msgs, dense0)
+    assert st == ac.OK
+    ref = dense0.cpu().numpy()
+    assert oracle.decode_accumulate(n, L, [m[:mb].cpu().numpy() for m, mb in msgs], ref) == oracle.OK
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+
+
+def test_decode_group_matches_per_layer():
+    lys = wl.layers("resnet50")[:12]
+    K = 3
+    h = ac.adacomp_init_group([l.numel for l in lys], [l.bin_len for l in lys], [ac.F32] * len(lys))
+    per_layer = [_learner_msgs(l.numel, l.bin_len, K, seed=i) for i, l in enumerate(lys)]
+    dense = [torch.zeros(l.numel, device="cuda") for l in lys]
+    ws = workspace(h.decode_ws_bytes(K))
+    ac.adacomp_decode_accumulate_group(h, [[m for m, _ in pl] for pl in per_layer], dense, ws)
+    assert ac.adacomp_decode_status(h, ws) == ac.OK
+    for l, pl, d in zip(lys, per_layer, dense):
+        ref = np.zeros(l.numel, np.float32)
+        oracle.decode_accumulate(l.numel, l.bin_len, [m[:mb].cpu().numpy() for m, mb in pl], ref)
+        assert np.array_equal(d.cpu().numpy().view(np.uint32), ref.view(np.uint32)), l.name
+
+
+def test_flat100m_four_learners_end_to_end():
+    """Full-size flat layer (10^8 elements, L_T = 500): 4 learners compress their own
+    N(0, 1e-3) dW, then one decode sums the 4 messages."""
+    (ly,) = wl.layers("flat100m")
+    n, L, K = ly.numel, ly.bin_len, 4
+    layer = GpuLayer(n, L, ac.F32)
+    msgs, host_msgs = [], []
+    for k in range(K):
+        res = torch.zeros(n, device="cuda")
+        dw = wl.gen_dw("flat100m", 0, ly, 0, learner=k)
+        ac.adacomp_compress(layer.h, res, dw, layer.msg, layer.ws)
+        mb, s, st = ac.adacomp_query(layer.h, layer.ws)
+        assert st == ac.OK
+        ref = oracle.compress(np.zeros(n, np.float32), dw_host(dw), L)
+        got = layer.msg[:mb].cpu().numpy()
+        assert np.array_equal(got, ref.msg), f"learner {k} message"
+        msgs.append(layer.msg[:((mb + 15) // 16) * 16].clone())
+        host_msgs.append(ref.msg)
+        del dw, res
+    dense = torch.zeros(n, device="cuda")
+    ws = workspace(layer.h.decode_ws_bytes(K))
+    ac.adacomp_decode_accumulate(layer.h, msgs, dense, ws)
+    assert ac.adacomp_decode_status(layer.h, ws) == ac.OK
+    ref_dense = np.zeros(n, np.float32)
+    oracle.decode_accumulate(n, L, host_msgs, ref_dense)
+    assert np.array_equal(dense.cpu().numpy().view(np.uint32), ref_dense.view(np.uint32))
+
+
+def test_malformed_messages_are_skipped_and_reported():
+    n, L = 50_000, 50
+    msgs = _learner_msgs(n, L, 2, seed=3)
+    h = ac.adacomp_init_layer(n, L, ac.F32)
+    good = msgs[0][0][:msgs[0][1]].cpu().numpy()
+    dense0 = torch.zeros(n, device="cuda")
+    expect = np.zeros(n, np.float32)
+    oracle.decode_accumulate(n, L, [good], expect)
+    for mutate in ("B", "count"):
+        bad, mb = msgs[1][0].clone(), msgs[1][1]
+        if mutate == "B":
+            bad[4] = (int(bad[4]) + 1) % 256
+        else:
+            bad[8] = 60  # bin 0 holds 50 elements
+            bad[9] = 0
+        got, st = _gpu_decode(h, [msgs[0], (bad, mb)], dense0)
+        assert st == ac.ERR_BAD_MESSAGE, mutate
+        assert np.array_equal(got.view(np.uint32), expect.view(np.uint32)), mutate
+    # a clean call afterwards reports OK again with the same workspace
+    got, st = _gpu_decode(h, msgs, dense0)
+    assert st == ac.OK
+
+
+def test_decode_is_deterministic():
+    n, L, K = 2_000_000, 500, 8
+    msgs = _learner_msgs(n, L, K, seed=11)
+    h = ac.adacomp_init_layer(n, L, ac.F32)
+    dense0 = torch.randn(n, device="cuda") * 1e-3
+    a, _ = _gpu_decode(h, msgs, dense0)
+    b, _ = _gpu_decode(h, msgs, dense0)
+    assert a.tobytes() == b.tobytes()
