@@ -126,6 +126,33 @@ adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* d
                                 size_t msg_capacity, void* ws, size_t ws_bytes,
                                 cudaStream_t stream);
 
+/*
+ * adacomp_compress for callers that cannot allocate device memory: plugins and
+ * hooks of communication or training frameworks that are handed only their
+ * gradient and message buffers, and that run where allocating is not allowed (the
+ * host application's allocator owns all device memory, or a fixed memory budget
+ * leaves no room for a separate workspace). The paper has no counterpart; this is
+ * an interface convenience of this library.
+ *
+ * Same arguments, checks and results as adacomp_compress, but the compress
+ * workspace is a 1 MiB array inside the library (a file-scope __device__ array that
+ * every GPU loading the library keeps until the process exits). It therefore
+ * takes single-layer handles whose compress_ws_bytes is at most 1 MiB (about
+ * 260M elements at L_T = 50 or 500); larger layers get ADACOMP_ERR_WORKSPACE.
+ * The call allocates nothing: it zeroes the part of the array it uses
+ * (cudaMemsetAsync) and runs the same kernels on `stream`.
+ *   result_out  optional device buffer of 32 bytes, 8-byte aligned, that receives
+ *               {float s; uint32 status; uint64 nnz; uint64 msg_bytes; uint64 pad}
+ *               (the values adacomp_query reports for adacomp_compress); NULL skips it.
+ * The first call on each device looks up the array's device address with that
+ * device current; make that first call before capturing any stream. All calls
+ * share the one array, so calls that overlap on a GPU (different streams, or
+ * several host threads) race and corrupt each other's results: serialise them.
+ */
+adacomp_status adacomp_compress_static_ws(adacomp_layer_t h, float* residue, const void* dW,
+                                          void* msg, size_t msg_capacity, void* result_out,
+                                          cudaStream_t stream);
+
 /* adacomp_compress for every layer of a group: arrays of num_layers device pointers
  * (host arrays) and capacities; one workspace for the whole group. */
 adacomp_status adacomp_compress_group(adacomp_layer_t h, float* const* residue,

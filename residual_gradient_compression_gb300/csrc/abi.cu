@@ -264,3 +264,28 @@ const char* adacomp_status_string(adacomp_status s)
 }
 
 }  // extern "C"
+
+namespace adacomp {
+
+// Argument checks and launch descriptor for one single-layer compress call, for
+// entry points that supply their own workspace. Same checks as adacomp_compress
+// apart from the workspace; *ws_needed receives the workspace size the call uses.
+int prepare_single_compress(const adacomp_layer* h, float* residue, const void* dW, void* msg,
+                            size_t msg_capacity, KGroup* g, size_t* ws_needed)
+{
+    if (!h || h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
+    *ws_needed = h->compress_ws;
+    if (!residue || !dW || !msg) return ADACOMP_ERR_INVALID_ARG;
+    if (!aligned(residue, 16) || !aligned(dW, 16) || !aligned(msg, 16)) return ADACOMP_ERR_ALIGNMENT;
+    if (msg_capacity < max_msg_bytes(h->layers[0])) return ADACOMP_ERR_CAPACITY;
+    std::memset(g, 0, sizeof *g);
+    fill_group(h, g);
+    g->layer[0].residue = residue;
+    g->layer[0].dw = dW;
+    g->layer[0].msg = static_cast<uint8_t*>(msg);
+    return ADACOMP_OK;
+}
+
+size_t compress_ws_of(const adacomp_layer* h) { return h ? h->compress_ws : 0; }
+
+}  // namespace adacomp

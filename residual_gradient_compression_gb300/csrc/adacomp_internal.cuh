@@ -127,6 +127,13 @@ struct DecodeParams {
 cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cudaEvent_t ev_before = nullptr,
                             cudaEvent_t ev_mid = nullptr, cudaEvent_t ev_after = nullptr);
 cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cudaStream_t stream);
+}  // namespace adacomp
+
+struct adacomp_layer;
+namespace adacomp {
+int prepare_single_compress(const adacomp_layer* h, float* residue, const void* dW, void* msg,
+                            size_t msg_capacity, KGroup* g, size_t* ws_needed);
+size_t compress_ws_of(const adacomp_layer* h);
 
 }  // namespace adacomp
 

@@ -812,3 +812,54 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
 }
 
 }  // namespace adacomp
+
+// ---------------------------------------------------------------- compress without a caller workspace
+// For callers that cannot allocate device memory (see adacomp_compress_static_ws in
+// include/adacomp.h). The workspace lives in this file-scope array, which every GPU
+// that loads the library holds until the process exits.
+#include <atomic>
+#include <cstddef>
+
+#include "../../include/adacomp.h"
+
+namespace {
+constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
+// Device address of g_static_scratch, looked up once per device (index = device id).
+std::atomic<void*> g_static_scratch_addr[64];
+}  // namespace
+
+extern "C" adacomp_status adacomp_compress_static_ws(adacomp_layer_t h, float* residue, const void* dW,
+                                                     void* msg, size_t msg_capacity, void* result_out,
+                                                     cudaStream_t stream)
+{
+    using namespace adacomp;
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    if (compress_ws_of(h) > kStaticScratchBytes) return ADACOMP_ERR_WORKSPACE;  // layer too large
+    KGroup g;  // on the host stack: nothing is allocated
+    size_t ws_needed = 0;
+    const int chk = prepare_single_compress(h, residue, dW, msg, msg_capacity, &g, &ws_needed);
+    if (chk != ADACOMP_OK) return (adacomp_status)chk;
+    if (result_out && (reinterpret_cast<uintptr_t>(result_out) & 7u)) return ADACOMP_ERR_ALIGNMENT;
+
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return ADACOMP_ERR_CUDA;
+    void* scratch = g_static_scratch_addr[dev].load(std::memory_order_acquire);
+    if (!scratch) {
+        // First call on this device (which is current): host code only has a stand-in
+        // for the array's name, so fetch its device address.
+        if (cudaGetSymbolAddress(&scratch, g_static_scratch) != cudaSuccess || !scratch) return ADACOMP_ERR_CUDA;
+        g_static_scratch_addr[dev].store(scratch, std::memory_order_release);
+    }
+    // The array keeps the previous call's contents: zero the control word, the
+    // layer's accumulators and the look-back descriptors this call relies on.
+    const size_t zero_bytes = ws_desc_offset(1) + 8 * (size_t)g.total_tiles;
+    if (cudaMemsetAsync(scratch, 0, zero_bytes, stream) != cudaSuccess) return ADACOMP_ERR_CUDA;
+    if (launch_compress(g, scratch, stream) != cudaSuccess) return ADACOMP_ERR_CUDA;
+    if (result_out) {
+        const uint8_t* res = static_cast<const uint8_t*>(scratch) + ws_layer_offset(0) + offsetof(LayerWs, result);
+        if (cudaMemcpyAsync(result_out, res, sizeof(Result), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
+            return ADACOMP_ERR_CUDA;
+    }
+    return ADACOMP_OK;
+}
