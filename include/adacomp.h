@@ -213,6 +213,16 @@ adacomp_status adacomp_decode_status(adacomp_layer_t h, const void* ws, cudaStre
 adacomp_status adacomp_set_timing_events(adacomp_layer_t h, cudaEvent_t before, cudaEvent_t mid,
                                          cudaEvent_t after);
 
+/*
+ * Fault injection for tests of the device-side timeout (not part of the method):
+ * when skip_tile is a valid tile index of this handle's next compress calls, that
+ * tile never publishes its look-back descriptor, so the tiles after it in its layer
+ * wait for it until the timeout and the layer reports ADACOMP_ERR_TIMEOUT. Nothing
+ * faults or hangs. Pass 0xFFFFFFFF to switch it off (the default). After such a
+ * call, zero the workspace before reusing it.
+ */
+adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile);
+
 /* Bound on each device-side wait, in nanoseconds (default 2e9). */
 adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns);
 

@@ -56,6 +56,7 @@ def lib() -> ctypes.CDLL:
         L.adacomp_decode_status.argtypes = [vp, vp, vp, P(i32)]
         L.adacomp_set_timeout_ns.argtypes = [vp, u64]
         L.adacomp_set_timing_events.argtypes = [vp, vp, vp, vp]
+        L.adacomp_set_fault_injection.argtypes = [vp, ctypes.c_uint32]
         L.adacomp_free.argtypes = [vp]
         L.adacomp_free.restype = None
         L.adacomp_status_string.argtypes = [ctypes.c_int]
@@ -63,7 +64,8 @@ def lib() -> ctypes.CDLL:
         for name in ("adacomp_init_layer", "adacomp_init_group", "adacomp_compress",
                      "adacomp_compress_group", "adacomp_decode_accumulate",
                      "adacomp_decode_accumulate_group", "adacomp_query", "adacomp_decode_status",
-                     "adacomp_set_timeout_ns", "adacomp_set_timing_events"):
+                     "adacomp_set_timeout_ns", "adacomp_set_timing_events",
+                     "adacomp_set_fault_injection"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -189,6 +191,11 @@ def adacomp_set_timing_events(h: Handle, before=None, mid=None, after=None):
         return None if ev is None else ctypes.c_void_p(ev.cuda_event)
     _check(lib().adacomp_set_timing_events(h.ptr, raw(before), raw(mid), raw(after)),
            "adacomp_set_timing_events")
+
+
+def adacomp_set_fault_injection(h: Handle, skip_tile: int = 0xFFFFFFFF):
+    """Test hook: the given tile never publishes, so its successors time out."""
+    _check(lib().adacomp_set_fault_injection(h.ptr, skip_tile), "adacomp_set_fault_injection")
 
 
 def adacomp_free(h: Handle):

@@ -8,7 +8,7 @@
 #include <new>
 #include <vector>
 
-#include "../../include/adacomp.h"
+#include "adacomp.h"
 
 struct adacomp_layer {
     std::vector<adacomp::KLayer> layers;  // device pointers are filled in per call
@@ -20,6 +20,7 @@ struct adacomp_layer {
     size_t compress_ws = 0;
     size_t decode_per_learner = 0;
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // optional timing events
+    uint32_t inject_skip_tile = 0xffffffffu;           // test-only fault injection
 };
 
 namespace {
@@ -66,6 +67,7 @@ adacomp_status make_group(adacomp_layer_t* out, int32_t num_layers, const int64_
         k.dw_bf16 = dtype[i] == ADACOMP_BF16 ? 1 : 0;
         k.code_bytes = L < 64 ? 1 : 2;
         k.vec = (L % 4 == 0) ? 4 : (L % 2 == 0) ? 2 : 1;
+        k.inv_len = (uint32_t)(((1ull << 32) + (uint64_t)L - 1) / (uint64_t)L);
         if (!k.dw_bf16) h->d_size = 4;
         const uint64_t te = (uint64_t)bpt * (uint64_t)L;
         if (te > h->tile_cap) h->tile_cap = (uint32_t)te;
@@ -91,6 +93,7 @@ void fill_group(const adacomp_layer* h, KGroup* g)
     g->max_bins = h->max_bins;
     g->d_size = h->d_size;
     g->timeout_ns = h->timeout_ns;
+    g->inject_skip_tile = h->inject_skip_tile;
     for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];
 }
 
@@ -236,6 +239,13 @@ adacomp_status adacomp_set_timing_events(adacomp_layer_t h, cudaEvent_t before, 
     h->ev[0] = before;
     h->ev[1] = mid;
     h->ev[2] = after;
+    return ADACOMP_OK;
+}
+
+adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    h->inject_skip_tile = skip_tile;
     return ADACOMP_OK;
 }
 

@@ -34,7 +34,7 @@ struct KLayer {
     uint8_t code_bytes;      // 1 if L_T < 64 else 2
     uint8_t vec;             // 4, 2 or 1: largest of these dividing L_T
     uint8_t pad0;
-    uint32_t pad1;
+    uint32_t inv_len;        // ceil(2^32 / L_T): x / L_T == umulhi(x, inv_len) for x < 2^16
 };
 static_assert(sizeof(KLayer) == 64, "KLayer layout");
 
@@ -46,30 +46,39 @@ struct KGroup {
     uint16_t max_bins;       // max bins per tile over the group
     uint16_t d_size;         // 4 if any layer has fp32 dW, else 2
     uint64_t timeout_ns;
+    uint32_t inject_skip_tile;  // fault injection for tests: this tile never publishes (~0u: none)
+    uint32_t pad2;
 };
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:
-// 2 stages x {residue slice, dW slice}, code staging, g_max, counts, exponent
-// histogram, 2 mbarriers, per-warp scalars.
+// 2 stages x {residue slice, dW slice}, layer table, G buffer, 2 code staging buffers, g_max, counts,
+// exponent buckets, per-stage tile geometry, 2 mbarriers, hand-off slots, scalars.
 struct SmemPlan {
-    uint32_t r_bytes, d_bytes, stg_bytes, bin_bytes, total;
+    uint32_t r_bytes, d_bytes, layer_bytes, stg_bytes, bin_bytes, total;
 };
-__host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size, uint32_t max_bins)
+__host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size, uint32_t max_bins,
+                                              uint32_t num_layers)
 {
     SmemPlan p;
-    p.r_bytes = ((tile_cap + 8) * 4 + 127) & ~127u;
-    p.d_bytes = ((tile_cap + 16) * d_size + 127) & ~127u;
+    // slack past the tile: the phase slots (< 4 fp32, < 8 bf16) plus segments that
+    // run up to 15 slots beyond the last element
+    p.r_bytes = ((tile_cap + 32) * 4 + 127) & ~127u;
+    p.d_bytes = ((tile_cap + 48) * d_size + 127) & ~127u;
     p.stg_bytes = (tile_cap * 2 + 127) & ~127u;
-    p.bin_bytes = (max_bins * 4 + 127) & ~127u;
-    p.total = 2 * (p.r_bytes + p.d_bytes) + p.stg_bytes + 2 * p.bin_bytes + 2048 + 16 + 256;
+    p.bin_bytes = (2 * (max_bins + 1) * 4 + 127) & ~127u;  // two buffers
+    p.layer_bytes = num_layers * 64u;                        // copy of the layer table
+    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.r_bytes + 2 * p.stg_bytes + 2 * p.bin_bytes + 4096 +
+              2048 + 32 + 512;
     return p;
 }
 
 // ---------------------------------------------------------------- compress workspace
 // [Ctl 64 B][LayerWs x num_layers][desc u64 x T][tile_excl u64 x T]
+// desc (the look-back descriptors) and each layer's accumulators are zero between
+// calls: the finalise kernel clears the accumulators, the fix-up kernel the
+// descriptors.
 struct Ctl {
-    uint32_t ticket;         // next tile to hand out; reset to 0 by the fix-up kernel
-    uint32_t pad[15];
+    uint32_t reserved[16];
 };
 
 struct Result {              // written by each call, kept for adacomp_query
@@ -156,6 +165,11 @@ __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count)
 __device__ __forceinline__ void fence_mbar_init()
 {
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar)
+{
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_addr(bar)) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes)

@@ -120,7 +120,9 @@ __device__ __forceinline__ void load_d(const void* sd, int id, float (&d)[VEC])
 
 // One tile's geometry and shared-memory slices.
 struct Tile {
-    float* sr;      // residue slice; element i at sr[pr + i]; phase A overwrites it with G
+    float* gres;    // global residue at the element held in shared slot 0 (tile start - pr)
+    const float* sr;  // residue slice; element i at sr[pr + i]
+    float* gs;        // G, same slot layout as sr (a buffer the bulk copies never target)
     const void* sd; // dW slice; element i at sd[pd + i]
     int pr, pd;
     int tl;         // elements in the tile
@@ -128,6 +130,7 @@ struct Tile {
     int bins;       // bins in the tile (last bin may be partial)
     int cpb;        // chunks per bin
     int ch;         // chunk length (elements, multiple of VEC)
+    uint32_t inv_len;  // ceil(2^32 / L)
 };
 
 struct ChunkRange {
@@ -163,7 +166,7 @@ __device__ __forceinline__ void phase_a(const Tile& T, int c_begin, int c_end, u
                 load_rd<VEC, BF16>(T.sr, T.sd, T.pr + i, T.pd + i, r, d);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) g[k] = __fadd_rn(r[k], d[k]);
-                store_g<VEC>(T.sr, T.pr + i, g);
+                store_g<VEC>(T.gs, T.pr + i, g);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k)
                     if (VEC == 1 || i + k < cr.e1) m = max(m, __float_as_uint(fabsf(g[k])));
@@ -199,7 +202,7 @@ __device__ __forceinline__ uint32_t phase_c(const Tile& T, int c_begin, int c_en
             uint32_t code[VEC];
             if (i < cr.e1) {
                 float g[VEC], d[VEC];
-                load_g<VEC>(T.sr, T.pr + i, g);
+                load_g<VEC>(T.gs, T.pr + i, g);
                 load_d<VEC, BF16>(T.sd, T.pd + i, d);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) {
@@ -230,6 +233,251 @@ __device__ __forceinline__ uint32_t phase_c(const Tile& T, int c_begin, int c_en
         }
     }
     return run;
+}
+
+// ---------------------------------------------------------------- segment path (L_T >= 16)
+// Each thread owns 16-element segments of the tile, aligned in shared memory:
+// segment s holds slots [16 s, 16 s + 16) of the residue slice, i.e. tile elements
+// e0 + idx with e0 = 16 s - pr. Since L_T >= 16 a segment spans at most two bins;
+// slots idx < split belong to bin_lo, the rest to bin_lo + 1. Per segment the bin
+// maxima and counts take at most two shared-memory atomics.
+//
+// The four 16-byte chunks of a segment are visited in the order q = k ^ rot, with
+// rot = ((t >> 1) ^ (t >> 3)) & 3, which makes both the fp32 128-bit accesses
+// (8 lanes per wavefront) and the bf16 64-bit accesses (16 lanes per wavefront)
+// free of bank conflicts.
+//
+// Slots that hold no element of the tile (the alignment slots before it, the slots
+// past its end) get G = 0 in phase A, so they never raise a maximum and are never
+// selected; only the (rare) edge segments pay for that masking.
+constexpr int kSeg = 16;
+
+struct SegGeo {
+    int e0;          // tile element of slot 0 (negative for the phase slots of segment 0)
+    uint32_t valid;  // bit idx set when slot idx holds an element of this tile
+    int bin_lo;      // bin of the first valid slot
+    int split;       // first slot of bin_lo + 1 (may exceed 15)
+    int off_lo;      // e0 - first element of bin_lo
+};
+
+__device__ __forceinline__ SegGeo seg_geo(const Tile& T, int s)
+{
+    SegGeo G;
+    G.e0 = s * kSeg - T.pr;
+    const int lo = max(0, -G.e0), hi = min(kSeg, T.tl - G.e0);
+    G.valid = hi > lo ? (((1u << (hi - lo)) - 1u) << lo) : 0u;
+    const int bin = (int)__umulhi((uint32_t)max(G.e0, 0), T.inv_len);
+    G.bin_lo = bin;
+    G.off_lo = G.e0 - bin * T.L;
+    G.split = T.L - G.off_lo;
+    return G;
+}
+
+__device__ __forceinline__ int seg_rot(int tid) { return ((tid >> 1) ^ (tid >> 3)) & 3; }
+
+// dW of slots 4q..4q+3 of segment s.
+template <bool BF16>
+__device__ __forceinline__ void seg_load_d(const Tile& T, int s, int q, float (&d)[4])
+{
+    if constexpr (BF16) {
+        const uint16_t* p = static_cast<const uint16_t*>(T.sd) + (T.pd - T.pr) + s * kSeg + 4 * q;
+        const uint2 u = *reinterpret_cast<const uint2*>(p);
+        d[0] = bf16_lo(u.x); d[1] = bf16_hi(u.x); d[2] = bf16_lo(u.y); d[3] = bf16_hi(u.y);
+    } else {
+        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(T.sd) + s * kSeg + 4 * q);
+        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+    }
+}
+
+// Phase A, segment path: G = residue + dW over the slots, written to the G buffer
+// (for phase C) and to the residue in global memory; bin maxima. *mine gets
+// the geometry of segment `tid` (the thread's only segment when the tile fits one
+// round).
+template <bool BF16>
+__device__ __forceinline__ void phase_a_seg(const Tile& T, uint32_t* gmax_s, int tid, SegGeo* mine)
+{
+    const int nseg = (T.pr + T.tl + kSeg - 1) / kSeg;
+    const int rot = seg_rot(tid);
+    for (int s = tid; s < nseg; s += kThreads) {
+        const SegGeo G = seg_geo(T, s);
+        if (s == tid) *mine = G;
+        const bool edge = G.valid != 0xffffu;
+        const float* rs = T.sr + s * kSeg;
+        float* gsp = T.gs + s * kSeg;
+        float m_lo = 0.0f, m_hi = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q = k ^ rot;
+            const int q0 = 4 * q;
+            const float4 r = *reinterpret_cast<const float4*>(rs + q0);
+            float d[4];
+            seg_load_d<BF16>(T, s, q, d);
+            float g[4];
+            g[0] = __fadd_rn(r.x, d[0]);
+            g[1] = __fadd_rn(r.y, d[1]);
+            g[2] = __fadd_rn(r.z, d[2]);
+            g[3] = __fadd_rn(r.w, d[3]);
+            const uint32_t vq = (G.valid >> q0) & 0xfu;
+            if (edge) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (!((vq >> i) & 1u)) g[i] = 0.0f;
+            }
+            *reinterpret_cast<float4*>(gsp + q0) = make_float4(g[0], g[1], g[2], g[3]);
+            // residue := G in global memory (sent elements are corrected by the fix-up kernel)
+            float* gp = T.gres + s * kSeg + q0;
+            if (vq == 0xfu) {
+                *reinterpret_cast<float4*>(gp) = make_float4(g[0], g[1], g[2], g[3]);
+            } else if (vq) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if ((vq >> i) & 1u) gp[i] = g[i];
+            }
+            if (q0 + 4 <= G.split) {
+                m_lo = fmaxf(m_lo, fmaxf(fmaxf(fabsf(g[0]), fabsf(g[1])), fmaxf(fabsf(g[2]), fabsf(g[3]))));
+            } else if (q0 >= G.split) {
+                m_hi = fmaxf(m_hi, fmaxf(fmaxf(fabsf(g[0]), fabsf(g[1])), fmaxf(fabsf(g[2]), fabsf(g[3]))));
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (q0 + i < G.split) m_lo = fmaxf(m_lo, fabsf(g[i]));
+                    else m_hi = fmaxf(m_hi, fabsf(g[i]));
+                }
+            }
+        }
+        if (m_lo > 0.0f) atomicMax(&gmax_s[G.bin_lo], __float_as_uint(m_lo));
+        if (m_hi > 0.0f) atomicMax(&gmax_s[G.bin_lo + 1], __float_as_uint(m_hi));
+    }
+}
+
+// Flags of one segment's 16 slots (bit idx): G != 0 && |fl32(G + dW)| >= g_max.
+template <bool BF16>
+__device__ __forceinline__ uint32_t seg_flags(const Tile& T, const SegGeo& G, int s, int rot, float gm_lo,
+                                              float gm_hi)
+{
+    const float* rs = T.gs + s * kSeg;
+    uint32_t f = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int q = k ^ rot;
+        const int q0 = 4 * q;
+        const float4 gv = *reinterpret_cast<const float4*>(rs + q0);
+        const float g[4] = {gv.x, gv.y, gv.z, gv.w};
+        float d[4];
+        seg_load_d<BF16>(T, s, q, d);
+        uint32_t nib = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float h = __fadd_rn(g[i], d[i]);
+            const float gm = q0 + i < G.split ? gm_lo : gm_hi;
+            nib |= (g[i] != 0.0f && fabsf(h) >= gm) ? (1u << i) : 0u;
+        }
+        f |= nib << q0;
+    }
+    return f;
+}
+
+// Phase C, segment path: flags and codes per slot, per-bin counts, and a block-wide
+// exclusive scan of the per-segment counts (in element order) that places every
+// code at stg[rank]. For tiles of several rounds. Runs on the 256 compute threads
+// (named barrier 1). Returns the tile's code count (same value in every thread).
+template <bool BF16>
+__device__ __forceinline__ uint32_t phase_c_seg(const Tile& T, const uint32_t* gmax_s, uint32_t* cnt_s,
+                                                uint16_t* stg, uint32_t* wsum, int tid)
+{
+    const int nseg = (T.pr + T.tl + kSeg - 1) / kSeg;
+    const int rot = seg_rot(tid);
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t carry = 0;
+    for (int base = 0; base < nseg; base += kThreads) {
+        const int s = base + tid;
+        uint32_t f = 0;
+        SegGeo G;
+        G.valid = 0; G.bin_lo = 0; G.split = kSeg; G.off_lo = 0; G.e0 = 0;
+        if (s < nseg) {
+            G = seg_geo(T, s);
+            const float gm_lo = __uint_as_float(gmax_s[G.bin_lo]);
+            const float gm_hi = G.split < kSeg ? __uint_as_float(gmax_s[G.bin_lo + 1]) : 0.0f;
+            f = seg_flags<BF16>(T, G, s, rot, gm_lo, gm_hi);
+            const uint32_t lomask = G.split >= kSeg ? 0xffffu : ((1u << max(G.split, 0)) - 1u);
+            const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
+            if (c_lo) atomicAdd(&cnt_s[G.bin_lo], c_lo);
+            if (c_hi) atomicAdd(&cnt_s[G.bin_lo + 1], c_hi);
+        }
+        // block-wide exclusive scan of the per-thread counts
+        const uint32_t c = __popc(f);
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (lane == 31) wsum[warp] = incl;
+        asm volatile("bar.sync %0, %1;" ::"n"(1), "n"(kThreads) : "memory");
+        uint32_t woff = 0, tot = 0;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) {
+            const uint32_t v = wsum[w];
+            woff += w < warp ? v : 0u;
+            tot += v;
+        }
+        uint32_t pos = carry + woff + incl - c;
+        const float* rs = T.gs + s * kSeg;
+        while (f) {
+            const int idx = __ffs(f) - 1;
+            f &= f - 1;
+            const int off = G.off_lo + idx - (idx < G.split ? 0 : T.L);
+            stg[pos++] = (uint16_t)(((uint32_t)off << 1) | (rs[idx] < 0.0f ? 1u : 0u));
+        }
+        carry += tot;
+        asm volatile("bar.sync %0, %1;" ::"n"(1), "n"(kThreads) : "memory");  // wsum reuse
+    }
+    return carry;
+}
+
+// Phase C, segment path, for tiles of one round (at most 256 segments, one per
+// thread, whose geometry phase A computed): flags per slot and per-bin counts; each
+// warp then ranks its own codes (shuffle scan of the per-thread counts) and stages
+// them at stg[wbase + rank], wbase being the first tile element of the warp's
+// segments (a warp never has more codes than elements, so the warps' ranges stay
+// disjoint). Only the sent slots are visited when the codes are written. Returns
+// the warp's code count.
+template <bool BF16>
+__device__ __forceinline__ uint32_t phase_c_seg_warp(const Tile& T, const SegGeo& G, const uint32_t* gmax_s,
+                                                     uint32_t* cnt_s, uint16_t* stg, int tid, int* wbase_out)
+{
+    const int nseg = (T.pr + T.tl + kSeg - 1) / kSeg;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int s = tid;
+    uint32_t f = 0;
+    if (s < nseg) {
+        const float gm_lo = __uint_as_float(gmax_s[G.bin_lo]);
+        const float gm_hi = G.split < kSeg ? __uint_as_float(gmax_s[G.bin_lo + 1]) : 0.0f;
+        f = seg_flags<BF16>(T, G, s, seg_rot(tid), gm_lo, gm_hi);
+        const uint32_t lomask = G.split >= kSeg ? 0xffffu : ((1u << max(G.split, 0)) - 1u);
+        const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
+        if (c_lo) atomicAdd(&cnt_s[G.bin_lo], c_lo);
+        if (c_hi) atomicAdd(&cnt_s[G.bin_lo + 1], c_hi);
+    }
+    const uint32_t c = __popc(f);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    const int wbase = max(kSeg * 32 * warp - T.pr, 0);
+    uint32_t pos = (uint32_t)wbase + incl - c;
+    const float* rs = T.gs + s * kSeg;
+    while (f) {
+        const int idx = __ffs(f) - 1;
+        f &= f - 1;
+        const int off = G.off_lo + idx - (idx < G.split ? 0 : T.L);
+        stg[pos++] = (uint16_t)(((uint32_t)off << 1) | (rs[idx] < 0.0f ? 1u : 0u));
+    }
+    *wbase_out = wbase;
+    return total;
 }
 
 // ---------------------------------------------------------------- exact scale sum
@@ -290,41 +538,71 @@ __device__ double exact_sum_from_buckets(const unsigned long long* acc)
 
 // ---------------------------------------------------------------- look-back
 // Warp-cooperative exclusive prefix of tile t's code count over the tiles of its
-// layer. Publishes AGGREGATE(total), walks back 32 descriptors at a time until an
-// INCLUSIVE one, then publishes INCLUSIVE(prefix + total). Every wait is bounded by
-// timeout_ns of global time; on expiry (or a predecessor's error) the tile is
-// published as ERROR and the function returns false.
-__device__ bool lookback(uint64_t* desc, uint32_t t, uint32_t tile_begin, uint32_t total, uint64_t timeout_ns,
-                         int lane, uint64_t* excl_out)
+// layer (single-pass scan with decoupled look-back, Merrill & Garland 2016). The
+// tile's AGGREGATE (or, for a layer's first tile, its INCLUSIVE value) has already
+// been published by the compute warps. Each round reads 128 predecessor
+// descriptors (4 per lane, nearest first) and stops at the nearest INCLUSIVE one;
+// then INCLUSIVE(prefix + total) is published. Every wait is bounded by timeout_ns
+// of global time; on expiry (or a predecessor's error) the tile is published as
+// ERROR and the function returns false.
+constexpr int kLbPerLane = 4;
+
+__device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin, uint32_t total,
+                                 uint64_t timeout_ns, int lane, bool publish, uint64_t* excl_out)
 {
     if (t == tile_begin) {
-        if (lane == 0) ptx::st_relaxed(&desc[t], kFlagIncl | total);
         *excl_out = 0;
         return true;
     }
-    if (lane == 0) ptx::st_relaxed(&desc[t], kFlagAgg | total);
     uint64_t excl = 0;
     int64_t j = (int64_t)t - 1;
     uint64_t start = 0;
-    uint32_t sleep_ns = 32;
+    uint32_t sleep_ns = 64;
     bool ok = true;
     for (;;) {
-        const int64_t idx = j - lane;
-        const uint64_t dv = idx >= (int64_t)tile_begin ? ptx::ld_relaxed(&desc[idx]) : kFlagIncl;
-        const uint32_t flag = (uint32_t)(dv >> 62);
-        const uint32_t incl = __ballot_sync(kFull, flag >= 2u);
-        const uint32_t lim = incl ? (uint32_t)(__ffs(incl) - 1) : 31u;
-        const uint32_t needed = (2u << lim) - 1u;
-        const uint32_t pending = __ballot_sync(kFull, flag == 0u) & needed;
-        if (pending == 0u) {
-            if (__ballot_sync(kFull, flag == 3u) & needed) { ok = false; break; }
-            unsigned long long v = ((uint32_t)lane <= lim) ? (dv & kValueMask) : 0ull;
+        uint64_t dv[kLbPerLane];
+#pragma unroll
+        for (int m = 0; m < kLbPerLane; ++m) {
+            const int64_t idx = j - (m * 32 + lane);
+            dv[m] = idx >= (int64_t)tile_begin ? ptx::ld_relaxed(&desc[idx]) : kFlagIncl;
+        }
+        int mstar = kLbPerLane;
+        uint32_t lim = 31;
+        bool pending = false, error = false;
+        uint32_t needed[kLbPerLane];
+#pragma unroll
+        for (int m = 0; m < kLbPerLane; ++m) {
+            const uint32_t f = (uint32_t)(dv[m] >> 62);
+            const uint32_t incl = __ballot_sync(kFull, f >= 2u);
+            const uint32_t pend = __ballot_sync(kFull, f == 0u);
+            const uint32_t err = __ballot_sync(kFull, f == 3u);
+            uint32_t need = 0u;
+            if (mstar == kLbPerLane) {
+                if (incl) {
+                    mstar = m;
+                    lim = (uint32_t)(__ffs(incl) - 1);
+                    need = (2u << lim) - 1u;
+                } else {
+                    need = kFull;
+                }
+            }
+            needed[m] = need;
+            pending |= (pend & need) != 0u;
+            error |= (err & need) != 0u;
+        }
+        if (!pending) {
+            if (error) { ok = false; break; }
+            unsigned long long v = 0;
+#pragma unroll
+            for (int m = 0; m < kLbPerLane; ++m)
+                if ((needed[m] >> lane) & 1u) v += dv[m] & kValueMask;
 #pragma unroll
             for (int o = 16; o; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
             excl += v;
-            if (incl) break;
-            j -= 32;
+            if (mstar < kLbPerLane) break;
+            j -= 32 * kLbPerLane;
             start = 0;
+            sleep_ns = 64;
             continue;
         }
         uint64_t now = 0;
@@ -333,9 +611,9 @@ __device__ bool lookback(uint64_t* desc, uint32_t t, uint32_t tile_begin, uint32
         if (start == 0) start = now;
         else if (now - start > timeout_ns) { ok = false; break; }
         __nanosleep(sleep_ns);
-        if (sleep_ns < 1024) sleep_ns <<= 1;
+        if (sleep_ns < 512) sleep_ns <<= 1;
     }
-    if (lane == 0) ptx::st_relaxed(&desc[t], ok ? (kFlagIncl | (excl + total)) : kFlagErr);
+    if (lane == 0 && publish) ptx::st_relaxed(&desc[t], ok ? (kFlagIncl | (excl + total)) : kFlagErr);
     *excl_out = excl;
     return ok;
 }
@@ -375,17 +653,6 @@ __device__ void finalize_layer(const KLayer& ly, LayerWs* lw, const uint64_t* de
     __syncwarp();
 }
 
-__device__ __forceinline__ int find_layer(const KGroup& g, uint32_t t)
-{
-    int lo = 0, hi = g.num_layers - 1;
-    while (lo < hi) {
-        int mid = (lo + hi + 1) >> 1;
-        if (g.layer[mid].tile_begin <= t) lo = mid;
-        else hi = mid - 1;
-    }
-    return lo;
-}
-
 // ---------------------------------------------------------------- tile geometry
 struct TileGeo {
     int layer;
@@ -395,39 +662,6 @@ struct TileGeo {
     int bins;
 };
 
-__device__ __forceinline__ TileGeo tile_geo(const KGroup& g, uint32_t t)
-{
-    TileGeo G;
-    G.layer = find_layer(g, t);
-    const KLayer& ly = g.layer[G.layer];
-    G.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
-    G.bins = (int)min(ly.bins_per_tile, ly.nbins - G.first_bin);
-    G.ts = (int64_t)G.first_bin * ly.bin_len;
-    G.tl = (int)min((int64_t)G.bins * ly.bin_len, ly.n - G.ts);
-    return G;
-}
-
-// Issues the bulk copies of tile t's residue and dW slices into one stage. Each copy
-// covers the slice's 16-byte-aligned span that starts at or before the tile; the
-// last few elements past the final 16-byte boundary are loaded with plain loads
-// after the wait, so nothing outside the arrays is read.
-__device__ void issue_load(const KGroup& g, uint32_t t, float* sr, void* sd, uint64_t* bar)
-{
-    const TileGeo G = tile_geo(g, t);
-    const KLayer& ly = g.layer[G.layer];
-    const int64_t a0 = G.ts & ~3ll, a1 = (G.ts + G.tl) & ~3ll;
-    const uint32_t rb = a1 > a0 ? (uint32_t)(a1 - a0) * 4u : 0u;
-    int64_t b0 = a0;
-    uint32_t db = rb;
-    if (ly.dw_bf16) {
-        b0 = G.ts & ~7ll;
-        const int64_t b1 = (G.ts + G.tl) & ~7ll;
-        db = b1 > b0 ? (uint32_t)(b1 - b0) * 2u : 0u;
-    }
-    ptx::mbar_arrive_expect_tx(bar, rb + db);
-    if (rb) ptx::bulk_g2s(sr, ly.residue + a0, rb, bar);
-    if (db) ptx::bulk_g2s(sd, static_cast<const uint8_t*>(ly.dw) + b0 * (ly.dw_bf16 ? 2 : 4), db, bar);
-}
 
 // Bounded wait on a stage's mbarrier phase; true when the data has landed.
 __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint64_t timeout_ns)
@@ -452,14 +686,231 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint6
     }
 
 // ---------------------------------------------------------------- compress kernel
-// Persistent: each CTA takes tiles from a ticket counter in increasing order, so
-// every tile's predecessors are already running or done and the look-back cannot
-// deadlock. Two stages: the next tile's bulk copies are in flight while the
-// current one is processed.
-__global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
+// Persistent, cooperative (all CTAs co-resident) and warp-specialised. CTA c takes
+// tiles c, c + grid, c + 2*grid, ... in order, so its next tile is known while the
+// current one is processed (its bulk copies are already in flight) and the order
+// holds nothing back: every tile's predecessors are processed by co-resident CTAs
+// that never wait on a later tile, so the look-back cannot deadlock.
+// Eight compute warps stream a tile through phases A and C (three barriers per
+// tile), publish its code count and hand the staged codes to one of two look-back
+// warps (one per staging buffer), which resolves the tile's prefix and copies the
+// codes into the message while the compute warps go on. Hand-off uses named
+// barriers FULL[b] (compute -> look-back warp b) and EMPTY[b] (back).
+// Bin maxima accumulate per CTA in exponent buckets and are flushed to the layer's
+// accumulator when the CTA moves to another layer; s is formed afterwards by the
+// finalise kernel.
+constexpr int kLookbackWarps = 2;  // one per staging buffer
+constexpr int kProducerWarp = kWarps + kLookbackWarps;
+constexpr int kCtaThreads = kThreads + 32 * (kLookbackWarps + 1);
+constexpr int kBarCompute = 1;
+constexpr int kBarFull = 2;   // + buffer
+constexpr int kBarEmpty = 4;  // + buffer
+constexpr uint32_t kEndTile = 0xffffffffu;
+
+struct Slot {
+    uint32_t t, total, layer, nrun;
+    uint32_t first_bin, bins, pad0, pad1;
+    uint32_t src[kWarps], dst[kWarps], cnt[kWarps];
+};
+
+template <int ID, int N>
+__device__ __forceinline__ void bar_sync() { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
+template <int ID, int N>
+__device__ __forceinline__ void bar_arrive() { asm volatile("bar.arrive %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
+// Named barriers of the buffer-indexed pairs (the compute warps and the look-back
+// warp that owns buffer b), with the index known only at run time.
+constexpr int kPair = kThreads + 32;
+__device__ __forceinline__ void full_sync(int b) { if (b) bar_sync<kBarFull + 1, kPair>(); else bar_sync<kBarFull, kPair>(); }
+__device__ __forceinline__ void full_arrive(int b) { if (b) bar_arrive<kBarFull + 1, kPair>(); else bar_arrive<kBarFull, kPair>(); }
+__device__ __forceinline__ void empty_sync(int b) { if (b) bar_sync<kBarEmpty + 1, kPair>(); else bar_sync<kBarEmpty, kPair>(); }
+__device__ __forceinline__ void empty_arrive(int b) { if (b) bar_arrive<kBarEmpty + 1, kPair>(); else bar_arrive<kBarEmpty, kPair>(); }
+__device__ __forceinline__ void compute_sync() { bar_sync<kBarCompute, kThreads>(); }
+
+
+// Barrier among the compute threads that also ANDs a predicate over them.
+__device__ __forceinline__ bool compute_and(bool p)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred a, b;\n\t"
+        "setp.ne.u32 a, %1, 0;\n\t"
+        "bar.red.and.pred b, %2, %3, a;\n\t"
+        "selp.u32 %0, 1, 0, b;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)p), "n"(kBarCompute), "n"(kThreads)
+        : "memory");
+    return r != 0;
+}
+
+// Layer of tile t, searching from layer `lo` (tiles of a CTA only move forward).
+// `lays` is the CTA's shared-memory copy of the layer table: kernel parameters
+// indexed at run time would be served by the small constant cache, and a miss
+// costs an L2 round trip.
+__device__ __forceinline__ int layer_from(const KLayer* lays, int num_layers, uint32_t t, int lo)
+{
+    int hi = num_layers - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (lays[mid].tile_begin <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Starts tile t's data into a stage: bulk copies of the 16-byte-aligned spans that
+// cover its residue and dW slices (plain loads for the few elements past the last
+// 16-byte boundary of a layer's array), and the tile's geometry for the threads
+// that will process it.
+__device__ void issue_tile(const KLayer* lays, uint32_t t, int layer, float* sr, void* sd, uint64_t* bar,
+                           TileGeo* info)
+{
+    TileGeo G;
+    G.layer = layer;
+    const KLayer& ly = lays[layer];
+    G.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+    G.bins = (int)min(ly.bins_per_tile, ly.nbins - G.first_bin);
+    G.ts = (int64_t)G.first_bin * ly.bin_len;
+    G.tl = (int)min((int64_t)G.bins * ly.bin_len, ly.n - G.ts);
+    *info = G;
+    const int64_t te = G.ts + G.tl;
+    // The copies start at the 16-byte boundary at or before the tile and end at the
+    // one at or after it (reading into the next tile, whose elements are ignored);
+    // only at the end of the layer's array do they stop at the boundary before it.
+    const int64_t a0 = G.ts & ~(int64_t)3;
+    int64_t a1 = (te + 3) & ~(int64_t)3;
+    if (a1 > ly.n) a1 = te & ~(int64_t)3;
+    const uint32_t rb = a1 > a0 ? (uint32_t)(a1 - a0) * 4u : 0u;
+    int64_t b0 = a0, b1 = a1;
+    uint32_t db = rb;
+    if (ly.dw_bf16) {
+        b0 = G.ts & ~(int64_t)7;
+        b1 = (te + 7) & ~(int64_t)7;
+        if (b1 > ly.n) b1 = te & ~(int64_t)7;
+        db = b1 > b0 ? (uint32_t)(b1 - b0) * 2u : 0u;
+    }
+    ptx::mbar_arrive_expect_tx(bar, rb + db);
+    if (rb) ptx::bulk_g2s(sr, ly.residue + a0, rb, bar);
+    if (db) ptx::bulk_g2s(sd, static_cast<const uint8_t*>(ly.dw) + b0 * (ly.dw_bf16 ? 2 : 4), db, bar);
+    const int pr = (int)(G.ts - a0), pd = (int)(G.ts - b0);
+    if (a1 < te || b1 < te) {
+        for (int64_t j = max(a1, G.ts); j < te; ++j) sr[pr + (j - G.ts)] = ly.residue[j];
+        if (ly.dw_bf16) {
+            for (int64_t j = max(b1, G.ts); j < te; ++j)
+                static_cast<uint16_t*>(sd)[pd + (j - G.ts)] = static_cast<const uint16_t*>(ly.dw)[j];
+        } else {
+            for (int64_t j = max(b1, G.ts); j < te; ++j)
+                static_cast<float*>(sd)[pd + (j - G.ts)] = static_cast<const float*>(ly.dw)[j];
+        }
+        ptx::fence_proxy_async_smem();  // before later bulk copies refill these bytes
+    }
+}
+
+// Exponent buckets of the bin maxima: warp `w` of `nw` handles the groups of 32
+// bins b0 = 32 w, 32 (w + nw), ... A group of 32 maxima mostly has the largest
+// exponent present or the one below it: both are summed with one warp reduction
+// each (at most 32 x 2^24 < 2^32); any other exponent is summed in a loop. Lane 0
+// adds each sum to the CTA's shared buckets with a 64-bit shared atomic.
+__device__ __forceinline__ void bucket_bins(const uint32_t* gmax_s, int bins, unsigned long long* hist, int lane,
+                                            int w, int nw)
+{
+    for (int b0 = 32 * w; b0 < bins; b0 += 32 * nw) {
+        const int b = b0 + lane;
+        const uint32_t u = b < bins ? gmax_s[b] : 0u;
+        const uint32_t E = u >> 23;
+        const uint32_t M = E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
+        if (__ballot_sync(kFull, u != 0u) == 0u) continue;
+        const uint32_t Eh = __reduce_max_sync(kFull, u ? E : 0u);
+        const uint32_t s_hi = __reduce_add_sync(kFull, (u && E == Eh) ? M : 0u);
+        const uint32_t s_lo = __reduce_add_sync(kFull, (u && Eh > 0 && E == Eh - 1) ? M : 0u);
+        if (lane == 0) {
+            if (s_hi) atomicAdd(&hist[Eh], (unsigned long long)s_hi);
+            if (s_lo) atomicAdd(&hist[Eh - 1], (unsigned long long)s_lo);
+        }
+        uint32_t left = __ballot_sync(kFull, u != 0u && E + 1 < Eh);
+        while (left) {
+            const uint32_t Ek = __shfl_sync(kFull, E, __ffs(left) - 1);
+            const bool mine = ((left >> lane) & 1u) && E == Ek;
+            const uint32_t sum = __reduce_add_sync(kFull, mine ? M : 0u);
+            if (lane == 0) atomicAdd(&hist[Ek], (unsigned long long)sum);
+            left &= ~__ballot_sync(kFull, mine);
+        }
+        __syncwarp();
+    }
+}
+
+// Adds a warp's shared buckets to layer lw's accumulator and clears them.
+__device__ __forceinline__ void flush_buckets(unsigned long long* hist, LayerWs* lw, int lane)
+{
+    __syncwarp();
+    for (int e = lane; e < 256; e += 32) {
+        const unsigned long long v = hist[e];
+        if (v) {
+            atomicAdd(&lw->acc[e], v);
+            hist[e] = 0ull;
+        }
+    }
+    __syncwarp();
+}
+
+// Look-back warp that owns staging buffer b, i.e. every other tile of the CTA.
+// For each such tile, in order: it writes the per-bin counts into the message and
+// clears the bin arrays; then it resolves the tile's prefix with the look-back (by
+// now the predecessors have had time to publish) and copies the staged codes into
+// the message.
+struct LookbackCtx {
+    uint16_t* stg;
+    uint32_t* gmax;
+    uint32_t* cnt;
+    uint32_t bin_len;  // entries of gmax / cnt to clear
+};
+
+__device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, const Slot* slots, const LookbackCtx& C,
+                              int b, int lane)
+{
+    uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
+    uint64_t* texcl = desc + g.total_tiles;
+    for (;;) {
+        full_sync(b);
+        const Slot& sl = slots[b];
+        const uint32_t t = sl.t;
+        if (t == kEndTile) break;
+        const int l = (int)sl.layer;
+        const KLayer& ly = lays[l];
+        const int bins = (int)sl.bins;
+        uint16_t* cdst = reinterpret_cast<uint16_t*>(ly.msg + 8) + sl.first_bin;
+        for (int bb = lane; bb < bins; bb += 32) cdst[bb] = (uint16_t)C.cnt[bb];
+        __syncwarp();
+        for (uint32_t bb = lane; bb < C.bin_len; bb += 32) { C.gmax[bb] = 0u; C.cnt[bb] = 0u; }
+        uint64_t excl = 0;
+        const bool ok = lookback_resolve(desc, t, ly.tile_begin, sl.total, g.timeout_ns, lane,
+                                         t != g.inject_skip_tile, &excl);
+        if (ok) {
+            if (lane == 0) texcl[t] = excl;
+            uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
+            for (uint32_t r = 0; r < sl.nrun; ++r) {
+                const uint32_t n = sl.cnt[r];
+                const uint16_t* sp = C.stg + sl.src[r];
+                const unsigned long long base = excl + sl.dst[r];
+                if (ly.code_bytes == 1) {
+                    for (uint32_t k = lane; k < n; k += 32) codes[base + k] = (uint8_t)sp[k];
+                } else {
+                    uint16_t* c16 = reinterpret_cast<uint16_t*>(codes);
+                    for (uint32_t k = lane; k < n; k += 32) c16[base + k] = sp[k];
+                }
+            }
+        } else if (lane == 0) {
+            atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
+        }
+        __syncwarp();
+        empty_arrive(b);
+    }
+}
+
+__global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_constant__ KGroup g,
+                                                                  uint8_t* __restrict__ ws)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins);
+    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers);
     uint8_t* p = smem;
     float* sr[2];
     void* sd[2];
@@ -467,246 +918,263 @@ __global__ void __launch_bounds__(kThreads) compress_kernel(const __grid_constan
     sd[0] = p; p += P.d_bytes;
     sr[1] = reinterpret_cast<float*>(p); p += P.r_bytes;
     sd[1] = p; p += P.d_bytes;
-    uint16_t* stg = reinterpret_cast<uint16_t*>(p); p += P.stg_bytes;
-    uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;
-    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;
-    unsigned long long* hist = reinterpret_cast<unsigned long long*>(p); p += 2048;
+    KLayer* lays = reinterpret_cast<KLayer*>(p); p += P.layer_bytes;
+    float* gbuf = reinterpret_cast<float*>(p); p += P.r_bytes;  // G of the tile being processed
+    uint16_t* stg0 = reinterpret_cast<uint16_t*>(p); p += 2 * P.stg_bytes;
+    const uint32_t stg_stride = P.stg_bytes / 2;
+    uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;  // 2 buffers of bin_stride
+    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;   // 2 buffers of bin_stride
+    const uint32_t bin_stride = P.bin_bytes / 8;
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(p); p += 4096;  // [256] exponent buckets + spare
+    TileGeo* info = reinterpret_cast<TileGeo*>(p); p += 2048;  // [2]: geometry of the tile in each stage
     uint64_t* bar = reinterpret_cast<uint64_t*>(p); p += 16;
-    uint32_t* wtot = reinterpret_cast<uint32_t*>(p);         // [8] codes per warp
-    uint32_t* wexcl = wtot + 8;                              // [8] warp prefix
-    int32_t* wbase = reinterpret_cast<int32_t*>(wtot + 16);  // [8] staging base per warp
-    uint32_t* tk = wtot + 24;                                // [2] held tickets
-    uint32_t* flags = wtot + 26;                             // [0] layer+1 to finalise, [1] prefix ok
-    unsigned long long* bexcl = reinterpret_cast<unsigned long long*>(wtot + 28);
+    uint64_t* freebar = reinterpret_cast<uint64_t*>(p); p += 16;  // stage s read for the last time
+    Slot* slots = reinterpret_cast<Slot*>(p); p += 2 * sizeof(Slot);
+    uint32_t* wsum = reinterpret_cast<uint32_t*>(p);         // [8]
+    uint32_t* wtot = wsum + 8;                               // [8]
+    int32_t* wbase = reinterpret_cast<int32_t*>(wsum + 16);  // [8]
 
-    Ctl* ctl = reinterpret_cast<Ctl*>(ws);
     uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
-    uint64_t* texcl = desc + g.total_tiles;
     const uint32_t T = g.total_tiles;
+    const uint32_t G0 = blockIdx.x, GS = gridDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    for (int e = tid; e < 256; e += kThreads) hist[e] = 0ull;
-    if (tid == 0) {
+    for (int e = tid; e < 512; e += kCtaThreads) hist[e] = 0ull;
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(&g.layer[0]);
+        uint4* dst = reinterpret_cast<uint4*>(lays);
+        for (int e = tid; e < g.num_layers * (int)(sizeof(KLayer) / 16); e += kCtaThreads) dst[e] = src[e];
+    }
+    __syncthreads();
+    for (uint32_t e = tid; e < 2 * bin_stride; e += kCtaThreads) { gmax_s[e] = 0u; cnt_s[e] = 0u; }
+    int issue_layer = 0;  // layer of the last tile issued (thread 64)
+    if (tid == 64) {
         ptx::mbar_init(&bar[0], 1);
         ptx::mbar_init(&bar[1], 1);
+        ptx::mbar_init(&freebar[0], 1);
+        ptx::mbar_init(&freebar[1], 1);
         ptx::fence_mbar_init();
-    }
-    __syncthreads();
-    if (tid == 0) {
-        uint32_t t0 = atomicAdd(&ctl->ticket, 1u), t1 = T;
-        if (t0 < T) {
-            issue_load(g, t0, sr[0], sd[0], &bar[0]);
-            t1 = atomicAdd(&ctl->ticket, 1u);
-            if (t1 < T) issue_load(g, t1, sr[1], sd[1], &bar[1]);
-            else t1 = T;
-        } else {
-            t0 = T;
-        }
-        tk[0] = t0;
-        tk[1] = t1;
-    }
-    __syncthreads();
-
-    uint32_t it = 0;
-    bool poisoned = false;
-    for (;;) {
-        const uint32_t t = tk[0];
-        if (t >= T) break;
-        const int s = it & 1;
-        const uint32_t parity = (it >> 1) & 1u;
-        const TileGeo G = tile_geo(g, t);
-        const KLayer& ly = g.layer[G.layer];
-        LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(G.layer));
-
-        if (!__syncthreads_and(wait_stage(&bar[s], parity, g.timeout_ns))) { poisoned = true; break; }
-
-        // tail elements past the last 16-byte boundary; clear per-bin arrays
-        const int pr = (int)(G.ts & 3), pd = ly.dw_bf16 ? (int)(G.ts & 7) : pr;
-        float* r_s = sr[s];
-        void* d_s = sd[s];
-        const int64_t te = G.ts + G.tl;
-        for (int64_t j = max((int64_t)(te & ~(int64_t)3), G.ts) + tid; j < te; j += kThreads) r_s[pr + (j - G.ts)] = ly.residue[j];
-        if (ly.dw_bf16) {
-            for (int64_t j = max((int64_t)(te & ~(int64_t)7), G.ts) + tid; j < te; j += kThreads)
-                static_cast<uint16_t*>(d_s)[pd + (j - G.ts)] = static_cast<const uint16_t*>(ly.dw)[j];
-        } else {
-            for (int64_t j = max((int64_t)(te & ~(int64_t)3), G.ts) + tid; j < te; j += kThreads)
-                static_cast<float*>(d_s)[pd + (j - G.ts)] = static_cast<const float*>(ly.dw)[j];
-        }
-        for (int b = tid; b < G.bins; b += kThreads) { gmax_s[b] = 0u; cnt_s[b] = 0u; }
-        __syncthreads();
-
-        Tile Tl;
-        Tl.sr = r_s; Tl.sd = d_s; Tl.pr = pr; Tl.pd = pd; Tl.tl = G.tl; Tl.L = ly.bin_len; Tl.bins = G.bins;
-        Tl.ch = min(ly.bin_len, 32 * (int)ly.vec * kRounds);
-        Tl.cpb = (ly.bin_len + Tl.ch - 1) / Tl.ch;
-        const int nchunks = G.bins * Tl.cpb;
-        const int cpw = (nchunks + kWarps - 1) / kWarps;
-        const int c_begin = min(nchunks, warp * cpw), c_end = min(nchunks, c_begin + cpw);
-
-        // phase A: G and bin maxima
-        ADACOMP_DISPATCH(ly.vec, ly.dw_bf16, (phase_a<VEC, BF16>(Tl, c_begin, c_end, gmax_s, lane)))
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-
-        // residue := G for the whole tile (sent elements are corrected by the fix-up kernel)
-        {
-            const int64_t c0 = (G.ts + 3) & ~3ll, c1 = te & ~3ll;
-            if (c1 > c0) {
-                if (tid == 0) {
-                    ptx::bulk_s2g(ly.residue + c0, r_s + pr + (c0 - G.ts), (uint32_t)(c1 - c0) * 4u);
-                    ptx::bulk_commit();
-                }
-                for (int64_t j = G.ts + tid; j < c0; j += kThreads) ly.residue[j] = r_s[pr + (j - G.ts)];
-                for (int64_t j = c1 + tid; j < te; j += kThreads) ly.residue[j] = r_s[pr + (j - G.ts)];
-            } else {
-                for (int64_t j = G.ts + tid; j < te; j += kThreads) ly.residue[j] = r_s[pr + (j - G.ts)];
-            }
-        }
-
-        // phase C: selection, per-bin counts, codes staged in element order
-        const int stg_base = c_begin < c_end ? chunk_at(Tl, c_begin).e0 : 0;
-        uint32_t wt = 0;
-        ADACOMP_DISPATCH(ly.vec, ly.dw_bf16,
-                         (wt = phase_c<VEC, BF16>(Tl, c_begin, c_end, gmax_s, cnt_s, stg, stg_base, lane)))
-        if (lane == 0) { wtot[warp] = wt; wbase[warp] = stg_base; }
-        __syncthreads();
-
-        if (warp == 0) {
-            // block scan over warps, then the look-back across tiles
-            const uint32_t v = lane < kWarps ? wtot[lane] : 0u;
-            uint32_t incl = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane < kWarps) wexcl[lane] = incl - v;
-            const uint32_t total = __shfl_sync(kFull, incl, 31);
-            uint64_t ex = 0;
-            const bool okl = lookback(desc, t, ly.tile_begin, total, g.timeout_ns, lane, &ex);
-            if (lane == 0) {
-                *bexcl = ex;
-                flags[1] = okl ? 1u : 0u;
-                if (okl) texcl[t] = ex;
-                else atomicOr(&lw->err, kErrTimeout);
-            }
-        } else if (warp == 1) {
-            // exact sum of the tile's bin maxima, bucketed by exponent
-            for (int b0 = 0; b0 < G.bins; b0 += 32) {
-                const int b = b0 + lane;
-                const uint32_t u = b < G.bins ? gmax_s[b] : 0u;
-                const uint32_t E = u >> 23;
-                const uint32_t M = E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
-                const uint32_t key = u ? E : 0x100u;
-                const uint32_t peers = __match_any_sync(kFull, key);
-                const uint32_t sum = __reduce_add_sync(peers, M);
-                if (key != 0x100u && lane == __ffs(peers) - 1) hist[E] += sum;
-                __syncwarp();
-            }
-            for (int e = lane; e < 256; e += 32) {
-                const unsigned long long v = hist[e];
-                if (v) {
-                    atomicAdd(&lw->acc[e], v);
-                    hist[e] = 0ull;
-                }
-            }
-            __threadfence();
-        } else {
-            uint16_t* cdst = reinterpret_cast<uint16_t*>(ly.msg + 8) + G.first_bin;
-            for (int b = tid - 64; b < G.bins; b += kThreads - 64) cdst[b] = (uint16_t)cnt_s[b];
-        }
-        __syncthreads();
-
-        if (tid == 0) {
-            __threadfence();
-            const uint32_t old = atomicAdd(&lw->done, 1u);
-            flags[0] = (old + 1u == ly.num_tiles) ? (uint32_t)G.layer + 1u : 0u;
-        }
-        if (flags[1]) {
-            const uint32_t nw = wtot[warp];
-            const unsigned long long base = *bexcl + wexcl[warp];
-            const int sb = wbase[warp];
-            uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
-            if (ly.code_bytes == 1) {
-                for (uint32_t k = lane; k < nw; k += 32) codes[base + k] = (uint8_t)stg[sb + k];
-            } else {
-                uint16_t* c16 = reinterpret_cast<uint16_t*>(codes);
-                for (uint32_t k = lane; k < nw; k += 32) c16[base + k] = stg[sb + k];
-            }
-        }
-        if (tid == 0) {
-            ptx::bulk_wait_read0();  // stage s is free once its G store has been read
-            const uint32_t nxt = tk[1];
-            uint32_t nn = T;
-            if (nxt < T) {
-                nn = atomicAdd(&ctl->ticket, 1u);
-                if (nn < T) issue_load(g, nn, sr[s], sd[s], &bar[s]);
-                else nn = T;
-            }
-            tk[0] = nxt;
-            tk[1] = nn;
-        }
-        __syncthreads();
-        if (flags[0]) {
-            const int l = (int)flags[0] - 1;
-            if (warp == 0)
-                finalize_layer(g.layer[l], reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l)), desc, hist, lane);
-            __syncthreads();
-        }
-        ++it;
-    }
-
-    if (poisoned) {
-        // A bulk copy never completed: retire the held tiles as errors so their
-        // layers still finalise, then give the copies one more bounded wait before
-        // the CTA's shared memory is released.
-        for (int h = 0; h < 2; ++h) {
-            const uint32_t t = tk[h];
+        for (int k = 0; k < 2; ++k) {
+            const uint32_t t = G0 + k * GS;
             if (t < T) {
-                const int l = find_layer(g, t);
-                LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l));
-                if (tid == 0) {
-                    ptx::st_relaxed(&desc[t], kFlagErr);
-                    atomicOr(&lw->err, kErrTimeout);
-                    __threadfence();
-                    const uint32_t old = atomicAdd(&lw->done, 1u);
-                    flags[0] = (old + 1u == g.layer[l].num_tiles) ? 1u : 0u;
-                }
-                __syncthreads();
-                if (flags[0] && warp == 0) finalize_layer(g.layer[l], lw, desc, hist, lane);
-                __syncthreads();
+                issue_layer = layer_from(lays, g.num_layers, t, issue_layer);
+                issue_tile(lays, t, issue_layer, sr[k], sd[k], &bar[k], &info[k]);
             }
         }
-        wait_stage(&bar[it & 1], (it >> 1) & 1u, g.timeout_ns);
-        if (tk[1] < T) wait_stage(&bar[(it + 1) & 1], ((it + 1) >> 1) & 1u, g.timeout_ns);
-        __syncthreads();
     }
-    if (tid == 0) ptx::bulk_wait0();
+    __syncthreads();
+
+    bool poisoned = false;
+    uint32_t it = 0;
+    if (warp >= kWarps && warp < kProducerWarp) {
+        const int b = warp - kWarps;  // look-back warp of staging buffer b
+        LookbackCtx C;
+        C.stg = stg0 + b * stg_stride;
+        C.gmax = gmax_s + b * bin_stride;
+        C.cnt = cnt_s + b * bin_stride;
+        C.bin_len = bin_stride;
+        lookback_warp(g, lays, ws, slots, C, b, lane);
+    } else if (warp == kProducerWarp) {
+        // Producer: once the compute warps have read stage s for the last time
+        // (tile k-2, signalled on freebar[s]), start the CTA's tile k into it.
+        const uint32_t n = G0 < T ? (T - 1 - G0) / GS + 1 : 0;  // this CTA's tiles
+        int issue_layer = 0;
+        if (lane == 0) {
+            for (uint32_t k = 2; k < n; ++k) {
+                const int s = k & 1;
+                if (!wait_stage(&freebar[s], ((k - 2) >> 1) & 1u, g.timeout_ns)) break;  // compute stopped
+                const uint32_t t = G0 + k * GS;
+                issue_layer = layer_from(lays, g.num_layers, t, issue_layer);
+                issue_tile(lays, t, issue_layer, sr[s], sd[s], &bar[s], &info[s]);
+            }
+        }
+        __syncwarp();
+    } else {
+        int hist_layer = -1;
+        for (;; ++it) {
+            const uint32_t t = G0 + it * GS;
+            if (t >= T) break;
+            const int s = it & 1;  // stage, staging buffer and bin-array buffer
+            const uint32_t parity = (it >> 1) & 1u;
+            if (!compute_and(wait_stage(&bar[s], parity, g.timeout_ns))) {
+                poisoned = true;
+                break;
+            }
+            // the look-back warp of this parity has finished tile it-2: the staging
+            // buffer and bin arrays of parity s are free and cleared
+            if (it >= 2) empty_sync(s);
+            const TileGeo G = info[s];
+            const KLayer& ly = lays[G.layer];
+            if (G.layer != hist_layer) {  // new layer: hand the buckets to the previous one
+                if (warp == 1 && hist_layer >= 0)
+                    flush_buckets(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+                hist_layer = G.layer;
+            }
+            uint32_t* gmax_c = gmax_s + s * bin_stride;
+            uint32_t* cnt_c = cnt_s + s * bin_stride;
+            const int pr = (int)(G.ts & 3), pd = ly.dw_bf16 ? (int)(G.ts & 7) : pr;
+            float* r_s = sr[s];
+            void* d_s = sd[s];
+            const int64_t te = G.ts + G.tl;
+
+            Tile Tl;
+            Tl.gres = ly.residue + (G.ts - pr);
+            Tl.sr = r_s; Tl.gs = gbuf; Tl.sd = d_s; Tl.pr = pr; Tl.pd = pd; Tl.tl = G.tl; Tl.L = ly.bin_len; Tl.bins = G.bins;
+            Tl.ch = min(ly.bin_len, 32 * (int)ly.vec * kRounds);
+            Tl.cpb = (ly.bin_len + Tl.ch - 1) / Tl.ch;
+            Tl.inv_len = ly.inv_len;
+            const bool seg = ly.bin_len >= kSeg;
+            const bool one_round = seg && pr + G.tl <= kThreads * kSeg;
+            const int nchunks = G.bins * Tl.cpb;
+            const int cpw = (nchunks + kWarps - 1) / kWarps;
+            const int c_begin = min(nchunks, warp * cpw), c_end = min(nchunks, c_begin + cpw);
+
+            // phase A: G (to shared and global memory) and bin maxima
+            SegGeo mine;
+            mine.valid = 0; mine.bin_lo = 0; mine.split = kSeg; mine.off_lo = 0; mine.e0 = 0;
+            if (seg) {
+                if (ly.dw_bf16) phase_a_seg<true>(Tl, gmax_c, tid, &mine);
+                else phase_a_seg<false>(Tl, gmax_c, tid, &mine);
+            } else {
+                ADACOMP_DISPATCH(ly.vec, ly.dw_bf16, (phase_a<VEC, BF16>(Tl, c_begin, c_end, gmax_c, lane)))
+            }
+            compute_sync();
+            if (!seg)  // short bins: residue := G from the shared slice
+                for (int64_t j = G.ts + tid; j < te; j += kThreads) ly.residue[j] = gbuf[pr + (j - G.ts)];
+
+            // phase C: selection, per-bin counts, codes staged in element order
+            uint16_t* stg = stg0 + s * stg_stride;
+            Slot& sl = slots[s];
+            if (one_round || !seg) {
+                int wb = 0;
+                uint32_t wt = 0;
+                if (one_round) {
+                    if (ly.dw_bf16) wt = phase_c_seg_warp<true>(Tl, mine, gmax_c, cnt_c, stg, tid, &wb);
+                    else wt = phase_c_seg_warp<false>(Tl, mine, gmax_c, cnt_c, stg, tid, &wb);
+                } else {
+                    wb = c_begin < c_end ? chunk_at(Tl, c_begin).e0 : 0;
+                    ADACOMP_DISPATCH(ly.vec, ly.dw_bf16,
+                                     (wt = phase_c<VEC, BF16>(Tl, c_begin, c_end, gmax_c, cnt_c, stg, wb, lane)))
+                }
+                if (lane == 0) { wtot[warp] = wt; wbase[warp] = wb; }
+                compute_sync();
+            } else {
+                uint32_t total;
+                if (ly.dw_bf16) total = phase_c_seg<true>(Tl, gmax_c, cnt_c, stg, wsum, tid);
+                else total = phase_c_seg<false>(Tl, gmax_c, cnt_c, stg, wsum, tid);
+                if (tid == 0) {
+                    sl.total = total;
+                    sl.nrun = 1;
+                    sl.src[0] = 0; sl.dst[0] = 0; sl.cnt[0] = total;
+                }
+            }
+
+            if (tid == 0) ptx::mbar_arrive(&freebar[s]);  // phase C was the last reader of stage s
+            if (warp == 0) {
+                if (one_round || !seg) {
+                    const uint32_t v = lane < kWarps ? wtot[lane] : 0u;
+                    uint32_t incl = v;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+                        if (lane >= o) incl += y;
+                    }
+                    if (lane < kWarps) {
+                        sl.src[lane] = (uint32_t)wbase[lane];
+                        sl.dst[lane] = incl - v;
+                        sl.cnt[lane] = v;
+                    }
+                    const uint32_t tot = __shfl_sync(kFull, incl, 31);
+                    if (lane == 0) {
+                        sl.total = tot;
+                        sl.nrun = kWarps;
+                    }
+                }
+                if (lane == 0) {
+                    sl.t = t;
+                    sl.layer = (uint32_t)G.layer;
+                    sl.first_bin = G.first_bin;
+                    sl.bins = (uint32_t)G.bins;
+                    if (t != g.inject_skip_tile)
+                        ptx::st_relaxed(&desc[t], (t == ly.tile_begin ? kFlagIncl : kFlagAgg) | sl.total);
+                }
+            } else {
+                bucket_bins(gmax_c, G.bins, hist, lane, warp - 1, kWarps - 1);
+            }
+            full_arrive(s);
+        }
+        compute_sync();  // every warp's additions to the buckets are in
+        if (warp == 1 && hist_layer >= 0)
+            flush_buckets(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+        // hand each look-back warp the end marker once it has released its buffer:
+        // buffer b carried the tiles it' < it with it' % 2 == b
+        for (int b = 0; b < 2; ++b) {
+            if ((it + 1 - b) / 2 >= 1) empty_sync(b);
+            if (tid == 0) slots[b].t = kEndTile;
+            full_arrive(b);
+        }
+    }
+    __syncthreads();
+
+    if (poisoned && tid == 0) {
+        // A bulk copy never completed: mark this CTA's remaining tiles as errors so
+        // no other tile waits on them, then give the outstanding copies one more
+        // bounded wait before the CTA's shared memory is released.
+        int l = 0;
+        for (uint32_t t = G0 + it * GS; t < T; t += GS) {
+            l = layer_from(lays, g.num_layers, t, l);
+            ptx::st_relaxed(&desc[t], kFlagErr);
+            atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
+        }
+    }
+    if (poisoned && warp < kWarps) {
+        wait_stage(&bar[it & 1], (it >> 1) & 1u, g.timeout_ns);
+        if (G0 + (it + 1) * GS < T) wait_stage(&bar[(it + 1) & 1], ((it + 1) >> 1) & 1u, g.timeout_ns);
+    }
+}
+
+// One warp per layer, after the compress kernel: s from the layer's exact sum,
+// header, result area; the accumulators are left zeroed for the next call.
+__global__ void __launch_bounds__(32) finalize_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
+{
+    __shared__ unsigned long long tmp[256];
+    const int l = blockIdx.x;
+    for (int e = threadIdx.x; e < 256; e += 32) tmp[e] = 0ull;
+    __syncwarp();
+    const uint64_t* desc = reinterpret_cast<const uint64_t*>(ws + ws_desc_offset(g.num_layers));
+    finalize_layer(g.layer[l], reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l)), desc, tmp, threadIdx.x);
 }
 
 // ---------------------------------------------------------------- fix-up kernel
 // For every sent element: residue = fl32(G - s) if G > 0, fl32(G + s) if G < 0
-// (the residue still holds G). Tiles are visited in reverse ticket order, so the
-// most recently written residue lines are the likeliest to still be in L2. Also
-// returns the look-back state to zero for the next call.
+// (the residue still holds G). Tiles are visited in reverse order, so the most
+// recently written residue lines are the likeliest to still be in L2. Also returns
+// the look-back descriptors to zero for the next call.
 constexpr int kFixThreads = 256;
 
 __global__ void __launch_bounds__(kFixThreads) fixup_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
 {
     __shared__ uint32_t pre[kMaxBinsPerTile + 1];
     __shared__ uint32_t wsum[kFixThreads / 32];
-    Ctl* ctl = reinterpret_cast<Ctl*>(ws);
+    extern __shared__ uint4 fix_dyn[];
+    KLayer* lays = reinterpret_cast<KLayer*>(fix_dyn);  // shared copy of the layer table
+    for (int e = threadIdx.x; e < g.num_layers * (int)(sizeof(KLayer) / 16); e += kFixThreads)
+        fix_dyn[e] = reinterpret_cast<const uint4*>(&g.layer[0])[e];
+    __syncthreads();
     uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
     const uint64_t* texcl = desc + g.total_tiles;
     const uint32_t T = g.total_tiles;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (blockIdx.x == 0 && tid == 0) ctl->ticket = 0u;
 
     for (uint32_t q = blockIdx.x; q < T; q += gridDim.x) {
         const uint32_t t = T - 1u - q;
-        const TileGeo G = tile_geo(g, t);
-        const KLayer& ly = g.layer[G.layer];
+        TileGeo G;
+        G.layer = layer_from(lays, g.num_layers, t, 0);
+        const KLayer& ly = lays[G.layer];
+        G.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+        G.bins = (int)min(ly.bins_per_tile, ly.nbins - G.first_bin);
+        G.ts = (int64_t)G.first_bin * ly.bin_len;
+        G.tl = (int)min((int64_t)G.bins * ly.bin_len, ly.n - G.ts);
         const LayerWs* lw = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(G.layer));
         if (lw->result.status == 0u) {
             // exclusive prefix of this tile's per-bin counts (4 bins per thread)
@@ -785,26 +1253,41 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
         e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins);
+    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers);
     if (P.total > di.smem_set) {
         e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
         if (e != cudaSuccess) return e;
         di.smem_set = P.total;
     }
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_kernel, kThreads, P.total);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_kernel, kCtaThreads, P.total);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const long long cap = (long long)di.sms * occ;
     const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
     if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess) return e;
-    compress_kernel<<<grid, kThreads, P.total, stream>>>(g, static_cast<uint8_t*>(ws));
+    {
+        // all CTAs must be resident together: the look-back waits on other CTAs' tiles
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(kCtaThreads);
+        cfg.dynamicSmemBytes = P.total;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeCooperative;
+        attr[0].val.cooperative = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        e = cudaLaunchKernelEx(&cfg, compress_kernel, g, static_cast<uint8_t*>(ws));
+        if (e != cudaSuccess) return e;
+    }
+    if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
+    finalize_kernel<<<g.num_layers, 32, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
     const long long fcap = (long long)di.sms * 8;
     const uint32_t fgrid = (uint32_t)((long long)g.total_tiles < fcap ? (long long)g.total_tiles : fcap);
-    fixup_kernel<<<fgrid, kFixThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    fixup_kernel<<<fgrid, kFixThreads, g.num_layers * sizeof(KLayer), stream>>>(g, static_cast<uint8_t*>(ws));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev_after) e = cudaEventRecord(ev_after, stream);
@@ -820,7 +1303,7 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
 #include <atomic>
 #include <cstddef>
 
-#include "../../include/adacomp.h"
+#include "adacomp.h"
 
 namespace {
 constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB

@@ -144,9 +144,9 @@ def test_deterministic_and_workspace_left_clean():
         msg, s = layer.step(r, dw)
         outs.append((msg.tobytes(), s, r.cpu().numpy().tobytes()))
         ws = layer.ws.cpu().numpy()
-        # the control word, the layer's exact-sum buckets and counters, and every
-        # look-back descriptor are zero again; only the result area and the per-tile
-        # offsets (rewritten by every call) keep data
+        # the layer's exact-sum buckets and counters and every look-back descriptor
+        # are zero again; only the result area and the per-tile offsets (rewritten by
+        # every call) keep data
         hdr = 64
         assert not ws[:hdr].any()
         lw = ws[hdr:hdr + 2112]
@@ -178,23 +178,20 @@ def test_checkpoint_resume_is_bit_identical(tmp_path):
 
 
 def test_lookback_wait_times_out_with_a_status():
-    """A tile whose predecessor never publishes: the bounded wait ends, the layer
-    reports ADACOMP_ERR_TIMEOUT, and the context stays usable."""
+    """A tile that never publishes its look-back descriptor: the bounded waits of the
+    tiles after it end, the layer reports ADACOMP_ERR_TIMEOUT, and the context stays
+    usable for a normal call afterwards."""
     n, L = 400_000, 500
     layer = GpuLayer(n, L, ac.F32)
     ac.adacomp_set_timeout_ns(layer.h, 20_000_000)  # 20 ms
-    # Fault injection in the workspace: the tile ticket starts at 1, so tile 0 never
-    # runs and tile 1's look-back waits on a descriptor nothing writes; the layer's
-    # done counter (after the 64-byte control block and 256 exponent buckets) is
-    # pre-set to 1 so the remaining tiles still complete and finalise the layer.
-    layer.ws[0:4] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8)
-    layer.ws[64 + 2048:64 + 2052] = torch.tensor([1, 0, 0, 0], dtype=torch.uint8)
+    ac.adacomp_set_fault_injection(layer.h, 3)      # tile 3 never publishes
     res_t = torch.zeros(n, device="cuda")
     dw = _dw(n, 0, 9, False)
     ac.adacomp_compress(layer.h, res_t, dw, layer.msg, layer.ws)
     mb, s, st = ac.adacomp_query(layer.h, layer.ws)
     assert st == ac.ERR_TIMEOUT
-    # recover: zero the workspace, run again, match the oracle
+    # recover: switch the injection off, zero the workspace, run again, match the oracle
+    ac.adacomp_set_fault_injection(layer.h)
     layer.ws.zero_()
     res_t.zero_()
     msg, s = layer.step(res_t, dw)
