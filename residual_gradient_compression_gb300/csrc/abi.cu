@@ -94,6 +94,9 @@ void fill_group(const adacomp_layer* h, KGroup* g)
     g->d_size = h->d_size;
     g->timeout_ns = h->timeout_ns;
     g->inject_skip_tile = h->inject_skip_tile;
+    g->needs_gbuf = 0;
+    for (const KLayer& k : h->layers)
+        if (k.bin_len < 16 || (uint64_t)k.bins_per_tile * k.bin_len + 3 > 4096) g->needs_gbuf = 1;
     for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];
 }
 

@@ -47,17 +47,17 @@ struct KGroup {
     uint16_t d_size;         // 4 if any layer has fp32 dW, else 2
     uint64_t timeout_ns;
     uint32_t inject_skip_tile;  // fault injection for tests: this tile never publishes (~0u: none)
-    uint32_t pad2;
+    uint32_t needs_gbuf;        // some tile is processed through shared memory (short bins or > 4096 slots)
 };
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:
 // 2 stages x {residue slice, dW slice}, layer table, G buffer, 2 code staging buffers, g_max, counts,
 // exponent buckets, per-stage tile geometry, 2 mbarriers, hand-off slots, scalars.
 struct SmemPlan {
-    uint32_t r_bytes, d_bytes, layer_bytes, stg_bytes, bin_bytes, total;
+    uint32_t r_bytes, d_bytes, layer_bytes, g_bytes, stg_bytes, bin_bytes, total;
 };
 __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size, uint32_t max_bins,
-                                              uint32_t num_layers)
+                                              uint32_t num_layers, uint32_t needs_gbuf)
 {
     SmemPlan p;
     // slack past the tile: the phase slots (< 4 fp32, < 8 bf16) plus segments that
@@ -67,7 +67,8 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
     p.stg_bytes = (tile_cap * 2 + 127) & ~127u;
     p.bin_bytes = (2 * (max_bins + 1) * 4 + 127) & ~127u;  // two buffers
     p.layer_bytes = num_layers * 64u;                        // copy of the layer table
-    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.r_bytes + 2 * p.stg_bytes + 2 * p.bin_bytes + 4096 +
+    p.g_bytes = needs_gbuf ? p.r_bytes : 0u;
+    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + 2 * p.stg_bytes + 2 * p.bin_bytes + 4096 +
               2048 + 32 + 512;
     return p;
 }

@@ -700,8 +700,7 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint6
 // accumulator when the CTA moves to another layer; s is formed afterwards by the
 // finalise kernel.
 constexpr int kLookbackWarps = 2;  // one per staging buffer
-constexpr int kProducerWarp = kWarps + kLookbackWarps;
-constexpr int kCtaThreads = kThreads + 32 * (kLookbackWarps + 1);
+constexpr int kCtaThreads = kThreads + 32 * kLookbackWarps;
 constexpr int kBarCompute = 1;
 constexpr int kBarFull = 2;   // + buffer
 constexpr int kBarEmpty = 4;  // + buffer
@@ -906,11 +905,126 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
     }
 }
 
+// One-round segment tile held in registers (at most 256 segments, one per thread):
+// phase A computes G, residue := G, the bin maxima and, per slot, |H| = |fl32(G + dW)|
+// and the masks of G != 0 and G < 0 (all phase C needs); after a barrier the stage
+// is no longer read and thread 0 refills it with the CTA's tile after next; phase C
+// then runs from the registers (flags, per-bin counts, codes ranked per warp and
+// staged at stg[wbase + rank]). Returns the warp's code count.
+template <bool BF16, class Refill>
+__device__ __forceinline__ uint32_t tile_in_registers(const Tile& T, uint32_t* gmax_s, uint32_t* cnt_s,
+                                                      uint16_t* stg, int tid, int* wbase_out, Refill&& refill)
+{
+    const int nseg = (T.pr + T.tl + kSeg - 1) / kSeg;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int s = tid;
+    const int rot = seg_rot(tid);
+    const bool active = s < nseg;
+    SegGeo G;
+    G.valid = 0; G.bin_lo = 0; G.split = kSeg; G.off_lo = 0; G.e0 = 0;
+    float ah[4][4];          // |H| per slot
+    uint32_t nz = 0, ng = 0;  // G != 0, G < 0 per slot
+    if (active) {
+        G = seg_geo(T, s);
+        const bool edge = G.valid != 0xffffu;
+        const float* rs = T.sr + s * kSeg;
+        float m_lo = 0.0f, m_hi = 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q0 = 4 * (k ^ rot);
+            const float4 r = *reinterpret_cast<const float4*>(rs + q0);
+            float d[4], g[4];
+            seg_load_d<BF16>(T, s, q0 >> 2, d);
+            g[0] = __fadd_rn(r.x, d[0]);
+            g[1] = __fadd_rn(r.y, d[1]);
+            g[2] = __fadd_rn(r.z, d[2]);
+            g[3] = __fadd_rn(r.w, d[3]);
+            const uint32_t vq = (G.valid >> q0) & 0xfu;
+            if (edge) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (!((vq >> i) & 1u)) g[i] = 0.0f;
+            }
+            uint32_t nzq = 0, ngq = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                ah[k][i] = fabsf(__fadd_rn(g[i], d[i]));
+                nzq |= g[i] != 0.0f ? (1u << i) : 0u;
+                ngq |= g[i] < 0.0f ? (1u << i) : 0u;
+            }
+            nz |= nzq << q0;
+            ng |= ngq << q0;
+            // residue := G in global memory (sent elements are corrected by the fix-up kernel)
+            float* gp = T.gres + s * kSeg + q0;
+            if (vq == 0xfu) {
+                *reinterpret_cast<float4*>(gp) = make_float4(g[0], g[1], g[2], g[3]);
+            } else if (vq) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if ((vq >> i) & 1u) gp[i] = g[i];
+            }
+            const float cm = fmaxf(fmaxf(fabsf(g[0]), fabsf(g[1])), fmaxf(fabsf(g[2]), fabsf(g[3])));
+            if (q0 + 4 <= G.split) {
+                m_lo = fmaxf(m_lo, cm);
+            } else if (q0 >= G.split) {
+                m_hi = fmaxf(m_hi, cm);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (q0 + i < G.split) m_lo = fmaxf(m_lo, fabsf(g[i]));
+                    else m_hi = fmaxf(m_hi, fabsf(g[i]));
+                }
+            }
+        }
+        if (m_lo > 0.0f) atomicMax(&gmax_s[G.bin_lo], __float_as_uint(m_lo));
+        if (m_hi > 0.0f) atomicMax(&gmax_s[G.bin_lo + 1], __float_as_uint(m_hi));
+    }
+    compute_sync();  // all bin maxima are in; the stage is not read again
+    if (tid == 0) refill();
+    uint32_t f = 0;
+    if (active) {
+        const float gm_lo = __uint_as_float(gmax_s[G.bin_lo]);
+        const float gm_hi = G.split < kSeg ? __uint_as_float(gmax_s[G.bin_lo + 1]) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q0 = 4 * (k ^ rot);
+            uint32_t nib = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                nib |= ah[k][i] >= (q0 + i < G.split ? gm_lo : gm_hi) ? (1u << i) : 0u;
+            f |= nib << q0;
+        }
+        f &= nz;
+        const uint32_t lomask = G.split >= kSeg ? 0xffffu : ((1u << max(G.split, 0)) - 1u);
+        const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
+        if (c_lo) atomicAdd(&cnt_s[G.bin_lo], c_lo);
+        if (c_hi) atomicAdd(&cnt_s[G.bin_lo + 1], c_hi);
+    }
+    const uint32_t c = __popc(f);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    const int wbase = max(kSeg * 32 * warp - T.pr, 0);
+    uint32_t pos = (uint32_t)wbase + incl - c;
+    while (f) {
+        const int idx = __ffs(f) - 1;
+        f &= f - 1;
+        const int off = G.off_lo + idx - (idx < G.split ? 0 : T.L);
+        stg[pos++] = (uint16_t)(((uint32_t)off << 1) | ((ng >> idx) & 1u));
+    }
+    *wbase_out = wbase;
+    return total;
+}
+
 __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_constant__ KGroup g,
                                                                   uint8_t* __restrict__ ws)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers);
+    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf);
     uint8_t* p = smem;
     float* sr[2];
     void* sd[2];
@@ -919,7 +1033,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
     sr[1] = reinterpret_cast<float*>(p); p += P.r_bytes;
     sd[1] = p; p += P.d_bytes;
     KLayer* lays = reinterpret_cast<KLayer*>(p); p += P.layer_bytes;
-    float* gbuf = reinterpret_cast<float*>(p); p += P.r_bytes;  // G of the tile being processed
+    float* gbuf = reinterpret_cast<float*>(p); p += P.g_bytes;  // G, for tiles not held in registers
     uint16_t* stg0 = reinterpret_cast<uint16_t*>(p); p += 2 * P.stg_bytes;
     const uint32_t stg_stride = P.stg_bytes / 2;
     uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;  // 2 buffers of bin_stride
@@ -928,7 +1042,6 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
     unsigned long long* hist = reinterpret_cast<unsigned long long*>(p); p += 4096;  // [256] exponent buckets + spare
     TileGeo* info = reinterpret_cast<TileGeo*>(p); p += 2048;  // [2]: geometry of the tile in each stage
     uint64_t* bar = reinterpret_cast<uint64_t*>(p); p += 16;
-    uint64_t* freebar = reinterpret_cast<uint64_t*>(p); p += 16;  // stage s read for the last time
     Slot* slots = reinterpret_cast<Slot*>(p); p += 2 * sizeof(Slot);
     uint32_t* wsum = reinterpret_cast<uint32_t*>(p);         // [8]
     uint32_t* wtot = wsum + 8;                               // [8]
@@ -947,12 +1060,10 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
     }
     __syncthreads();
     for (uint32_t e = tid; e < 2 * bin_stride; e += kCtaThreads) { gmax_s[e] = 0u; cnt_s[e] = 0u; }
-    int issue_layer = 0;  // layer of the last tile issued (thread 64)
-    if (tid == 64) {
+    int issue_layer = 0;  // layer of the last tile issued (thread 0 issues every tile)
+    if (tid == 0) {
         ptx::mbar_init(&bar[0], 1);
         ptx::mbar_init(&bar[1], 1);
-        ptx::mbar_init(&freebar[0], 1);
-        ptx::mbar_init(&freebar[1], 1);
         ptx::fence_mbar_init();
         for (int k = 0; k < 2; ++k) {
             const uint32_t t = G0 + k * GS;
@@ -966,7 +1077,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
 
     bool poisoned = false;
     uint32_t it = 0;
-    if (warp >= kWarps && warp < kProducerWarp) {
+    if (warp >= kWarps) {
         const int b = warp - kWarps;  // look-back warp of staging buffer b
         LookbackCtx C;
         C.stg = stg0 + b * stg_stride;
@@ -974,21 +1085,6 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
         C.cnt = cnt_s + b * bin_stride;
         C.bin_len = bin_stride;
         lookback_warp(g, lays, ws, slots, C, b, lane);
-    } else if (warp == kProducerWarp) {
-        // Producer: once the compute warps have read stage s for the last time
-        // (tile k-2, signalled on freebar[s]), start the CTA's tile k into it.
-        const uint32_t n = G0 < T ? (T - 1 - G0) / GS + 1 : 0;  // this CTA's tiles
-        int issue_layer = 0;
-        if (lane == 0) {
-            for (uint32_t k = 2; k < n; ++k) {
-                const int s = k & 1;
-                if (!wait_stage(&freebar[s], ((k - 2) >> 1) & 1u, g.timeout_ns)) break;  // compute stopped
-                const uint32_t t = G0 + k * GS;
-                issue_layer = layer_from(lays, g.num_layers, t, issue_layer);
-                issue_tile(lays, t, issue_layer, sr[s], sd[s], &bar[s], &info[s]);
-            }
-        }
-        __syncwarp();
     } else {
         int hist_layer = -1;
         for (;; ++it) {
@@ -1029,47 +1125,55 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
             const int cpw = (nchunks + kWarps - 1) / kWarps;
             const int c_begin = min(nchunks, warp * cpw), c_end = min(nchunks, c_begin + cpw);
 
-            // phase A: G (to shared and global memory) and bin maxima
-            SegGeo mine;
-            mine.valid = 0; mine.bin_lo = 0; mine.split = kSeg; mine.off_lo = 0; mine.e0 = 0;
-            if (seg) {
-                if (ly.dw_bf16) phase_a_seg<true>(Tl, gmax_c, tid, &mine);
-                else phase_a_seg<false>(Tl, gmax_c, tid, &mine);
-            } else {
-                ADACOMP_DISPATCH(ly.vec, ly.dw_bf16, (phase_a<VEC, BF16>(Tl, c_begin, c_end, gmax_c, lane)))
-            }
-            compute_sync();
-            if (!seg)  // short bins: residue := G from the shared slice
-                for (int64_t j = G.ts + tid; j < te; j += kThreads) ly.residue[j] = gbuf[pr + (j - G.ts)];
-
-            // phase C: selection, per-bin counts, codes staged in element order
             uint16_t* stg = stg0 + s * stg_stride;
             Slot& sl = slots[s];
-            if (one_round || !seg) {
-                int wb = 0;
-                uint32_t wt = 0;
-                if (one_round) {
-                    if (ly.dw_bf16) wt = phase_c_seg_warp<true>(Tl, mine, gmax_c, cnt_c, stg, tid, &wb);
-                    else wt = phase_c_seg_warp<false>(Tl, mine, gmax_c, cnt_c, stg, tid, &wb);
-                } else {
-                    wb = c_begin < c_end ? chunk_at(Tl, c_begin).e0 : 0;
-                    ADACOMP_DISPATCH(ly.vec, ly.dw_bf16,
-                                     (wt = phase_c<VEC, BF16>(Tl, c_begin, c_end, gmax_c, cnt_c, stg, wb, lane)))
+            const uint32_t t_next = t + 2 * GS;
+            // thread 0: start the CTA's tile after next into stage s once it is free
+            auto refill = [&]() {
+                if (t_next < T) {
+                    issue_layer = layer_from(lays, g.num_layers, t_next, issue_layer);
+                    issue_tile(lays, t_next, issue_layer, sr[s], sd[s], &bar[s], &info[s]);
                 }
+            };
+            if (one_round) {
+                // phases A and C with G and dW in registers; the stage is refilled in between
+                int wb = 0;
+                uint32_t wt;
+                if (ly.dw_bf16) wt = tile_in_registers<true>(Tl, gmax_c, cnt_c, stg, tid, &wb, refill);
+                else wt = tile_in_registers<false>(Tl, gmax_c, cnt_c, stg, tid, &wb, refill);
                 if (lane == 0) { wtot[warp] = wt; wbase[warp] = wb; }
                 compute_sync();
             } else {
-                uint32_t total;
-                if (ly.dw_bf16) total = phase_c_seg<true>(Tl, gmax_c, cnt_c, stg, wsum, tid);
-                else total = phase_c_seg<false>(Tl, gmax_c, cnt_c, stg, wsum, tid);
-                if (tid == 0) {
-                    sl.total = total;
-                    sl.nrun = 1;
-                    sl.src[0] = 0; sl.dst[0] = 0; sl.cnt[0] = total;
+                // phase A: G (to the G buffer and global memory) and bin maxima
+                SegGeo mine;
+                if (seg) {
+                    if (ly.dw_bf16) phase_a_seg<true>(Tl, gmax_c, tid, &mine);
+                    else phase_a_seg<false>(Tl, gmax_c, tid, &mine);
+                } else {
+                    ADACOMP_DISPATCH(ly.vec, ly.dw_bf16, (phase_a<VEC, BF16>(Tl, c_begin, c_end, gmax_c, lane)))
                 }
+                compute_sync();
+                if (!seg) {  // short bins: residue := G from the G buffer, then phase C per warp
+                    for (int64_t j = G.ts + tid; j < te; j += kThreads) ly.residue[j] = gbuf[pr + (j - G.ts)];
+                    const int wb = c_begin < c_end ? chunk_at(Tl, c_begin).e0 : 0;
+                    uint32_t wt = 0;
+                    ADACOMP_DISPATCH(ly.vec, ly.dw_bf16,
+                                     (wt = phase_c<VEC, BF16>(Tl, c_begin, c_end, gmax_c, cnt_c, stg, wb, lane)))
+                    if (lane == 0) { wtot[warp] = wt; wbase[warp] = wb; }
+                    compute_sync();
+                } else {  // several rounds: block-wide scan (ends with a barrier)
+                    uint32_t total;
+                    if (ly.dw_bf16) total = phase_c_seg<true>(Tl, gmax_c, cnt_c, stg, wsum, tid);
+                    else total = phase_c_seg<false>(Tl, gmax_c, cnt_c, stg, wsum, tid);
+                    if (tid == 0) {
+                        sl.total = total;
+                        sl.nrun = 1;
+                        sl.src[0] = 0; sl.dst[0] = 0; sl.cnt[0] = total;
+                    }
+                }
+                if (tid == 0) refill();  // phase C was the last reader of stage s
             }
 
-            if (tid == 0) ptx::mbar_arrive(&freebar[s]);  // phase C was the last reader of stage s
             if (warp == 0) {
                 if (one_round || !seg) {
                     const uint32_t v = lane < kWarps ? wtot[lane] : 0u;
@@ -1253,7 +1357,7 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
         e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers);
+    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf);
     if (P.total > di.smem_set) {
         e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
         if (e != cudaSuccess) return e;
