@@ -289,7 +289,8 @@ class DeviceRun:
         self.c_dense = [(VP * len(g))(*[self.dense[1][i].data_ptr() for i in g]) for g in self.gidx]
 
     def launches_per_step(self):
-        return self.K * len(self.gidx) * 2 + len(self.gidx) * 3
+        # compress: streaming kernel, finalise, fix-up; decode: tile sums, scan, accumulate
+        return self.K * len(self.gidx) * 3 + len(self.gidx) * 3
 
     def step(self, i, stream_ptr, k1_events=None, dec_events=None):
         """Enqueues one step: every learner's compress, then the decode of the step's messages."""

@@ -56,10 +56,14 @@ adacomp_status make_group(adacomp_layer_t* out, int32_t num_layers, const int64_
         k.n = N;
         k.nbins = (uint32_t)B;
         k.bin_len = L;
-        int64_t bpt = adacomp::kTileTarget / L;
+        // warp-sliced tiles: eight warp slices of floor(509 / L_T) whole bins each;
+        // otherwise about kTileTarget elements of whole bins
+        const int bpw = (L >= 16 && L <= adacomp::kWarpSliceMax) ? adacomp::kWarpSliceMax / L : 0;
+        int64_t bpt = bpw ? (int64_t)adacomp::kWarps * bpw : adacomp::kTileTarget / L;
         if (bpt < 1) bpt = 1;
         if (bpt > adacomp::kMaxBinsPerTile) bpt = adacomp::kMaxBinsPerTile;
         if (bpt > B) bpt = B;
+        k.bpw = (uint8_t)bpw;
         k.bins_per_tile = (uint32_t)bpt;
         k.num_tiles = (uint32_t)((B + bpt - 1) / bpt);
         k.tile_begin = (uint32_t)tiles;

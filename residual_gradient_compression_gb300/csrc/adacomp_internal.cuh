@@ -16,6 +16,10 @@ constexpr int kTileTarget = 4096;      // elements per tile (whole bins)
 constexpr int kThreads = 256;          // compress CTA size
 constexpr int kWarps = kThreads / 32;
 constexpr int kRounds = 4;             // lane-vectors per chunk: chunk <= 32*VEC*kRounds elements
+constexpr int kWarpSliceMax = 509;     // warp-sliced tiles: a warp slice plus its alignment slots fits 512 slots
+constexpr int kWarpScratch = 36;       // per-warp g_max / count scratch entries (bins per slice <= 31)
+constexpr uint32_t kHistBytes = kWarps * 256 * 8;                   // per-warp exponent buckets
+constexpr uint32_t kWarpScratchBytes = kWarps * 2 * kWarpScratch * 4;
 
 // ---------------------------------------------------------------- descriptors
 // One layer of a launch. Tiles of all layers are numbered consecutively in layer
@@ -33,7 +37,7 @@ struct KLayer {
     uint8_t dw_bf16;
     uint8_t code_bytes;      // 1 if L_T < 64 else 2
     uint8_t vec;             // 4, 2 or 1: largest of these dividing L_T
-    uint8_t pad0;
+    uint8_t bpw;             // warp-sliced tiles: bins per warp slice, floor(509 / L_T); 0: block-wide tiles
     uint32_t inv_len;        // ceil(2^32 / L_T): x / L_T == umulhi(x, inv_len) for x < 2^16
 };
 static_assert(sizeof(KLayer) == 64, "KLayer layout");
@@ -52,7 +56,8 @@ struct KGroup {
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:
 // 2 stages x {residue slice, dW slice}, layer table, G buffer, 2 code staging buffers, g_max, counts,
-// exponent buckets, per-stage tile geometry, 2 mbarriers, hand-off slots, scalars.
+// per-warp exponent buckets, per-warp bin scratch, per-stage tile geometry, control block (mbarriers,
+// counters, hand-off slots).
 struct SmemPlan {
     uint32_t r_bytes, d_bytes, layer_bytes, g_bytes, stg_bytes, bin_bytes, total;
 };
@@ -68,8 +73,8 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
     p.bin_bytes = (2 * (max_bins + 1) * 4 + 127) & ~127u;  // two buffers
     p.layer_bytes = num_layers * 64u;                        // copy of the layer table
     p.g_bytes = needs_gbuf ? p.r_bytes : 0u;
-    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + 2 * p.stg_bytes + 2 * p.bin_bytes + 4096 +
-              2048 + 32 + 512;
+    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + 2 * p.stg_bytes + 2 * p.bin_bytes +
+              kHistBytes + kWarpScratchBytes + 2048 + 512;
     return p;
 }
 

@@ -486,54 +486,86 @@ __device__ __forceinline__ uint32_t phase_c_seg_warp(const Tile& T, const SegGeo
 // M * 2^(max(E,1) - 150). The exact sum is rebuilt as a 384-bit integer in units of
 // 2^-149 and rounded once to the nearest fp64 (ties to even), so s does not depend
 // on the order in which tiles finished.
-__device__ double exact_sum_from_buckets(const unsigned long long* acc)
+//
+// Warp-parallel: lane l shifts buckets 8l .. 8l+7 into place; their 32-bit pieces
+// land in at most five consecutive words, which are added into `words` (twelve
+// 64-bit partial sums in shared memory, zero on entry) with shared atomics. Lane 0
+// then propagates the carries and rounds. Every lane returns the sum.
+constexpr int kSumWords = 12;
+
+__device__ double exact_sum_warp(const unsigned long long* acc, unsigned long long* words, int lane)
 {
-    constexpr int W = 12;
-    uint32_t w[W];
-#pragma unroll
-    for (int i = 0; i < W; ++i) w[i] = 0;
     if (acc[255] != 0ull) return __longlong_as_double(0x7ff0000000000000ll);  // non-finite input
-    for (int e = 0; e < 255; ++e) {
-        const unsigned long long v = acc[e];
-        if (v == 0ull) continue;
+    const int e_first = lane * 8;
+    const int q0 = (e_first ? e_first - 1 : 0) >> 5;
+    unsigned long long loc[5] = {0ull, 0ull, 0ull, 0ull, 0ull};
+#pragma unroll
+    for (int j = 0; j < 8; ++j) {
+        const int e = e_first + j;
+        const unsigned long long v = e < 255 ? acc[e] : 0ull;
         const int sh = e ? e - 1 : 0;
-        const int q = sh >> 5, b = sh & 31;
+        const int dq = (sh >> 5) - q0;  // 0 or 1
+        const int b = sh & 31;
         const unsigned long long lo = v << b;
         const unsigned long long hi = b ? (v >> (64 - b)) : 0ull;
-        const uint32_t part[4] = {(uint32_t)lo, (uint32_t)(lo >> 32), (uint32_t)hi, (uint32_t)(hi >> 32)};
+        const unsigned long long p0 = lo & 0xffffffffull, p1 = lo >> 32, p2 = hi & 0xffffffffull, p3 = hi >> 32;
+        if (dq == 0) { loc[0] += p0; loc[1] += p1; loc[2] += p2; loc[3] += p3; }
+        else { loc[1] += p0; loc[2] += p1; loc[3] += p2; loc[4] += p3; }
+    }
+#pragma unroll
+    for (int i = 0; i < 5; ++i)
+        if (loc[i] && q0 + i < kSumWords) atomicAdd(&words[q0 + i], loc[i]);
+    __syncwarp();
+    double S = 0.0;
+    if (lane == 0) {
+        uint32_t w[kSumWords];
         unsigned long long carry = 0;
-        for (int i = 0; q + i < W; ++i) {
-            unsigned long long t = (unsigned long long)w[q + i] + (i < 4 ? part[i] : 0u) + carry;
-            w[q + i] = (uint32_t)t;
+#pragma unroll
+        for (int i = 0; i < kSumWords; ++i) {
+            const unsigned long long t = words[i] + carry;
+            w[i] = (uint32_t)t;
             carry = t >> 32;
-            if (i >= 3 && carry == 0) break;
+        }
+        int top = -1;
+#pragma unroll
+        for (int i = kSumWords - 1; i >= 0; --i)
+            if (top < 0 && w[i]) top = i * 32 + 31 - __clz(w[i]);
+        if (top >= 0) {
+            const int lo = top - 52;  // weight of the last kept bit
+            unsigned long long mant;
+            int scale;
+            if (lo <= 0) {
+                mant = ((unsigned long long)w[1] << 32) | w[0];  // exact: fewer than 54 bits
+                scale = -149;
+            } else {
+                const int q = lo >> 5, off = lo & 31;
+                unsigned long long x = 0, x2 = 0;
+#pragma unroll
+                for (int i = 0; i < kSumWords; ++i) {
+                    if (i == q) x |= w[i];
+                    if (i == q + 1) x |= (unsigned long long)w[i] << 32;
+                    if (i == q + 2) x2 = w[i];
+                }
+                mant = off ? ((x >> off) | (x2 << (64 - off))) : x;
+                mant &= (1ull << 53) - 1;
+                const int rb = lo - 1;  // round bit; the sticky bits lie below it
+                uint32_t round = 0, sticky = 0;
+#pragma unroll
+                for (int i = 0; i < kSumWords; ++i) {
+                    const int base = i * 32;
+                    if (rb >= base && rb < base + 32) round = (w[i] >> (rb - base)) & 1u;
+                    if (base + 32 <= rb) sticky |= w[i];
+                    else if (base < rb) sticky |= w[i] & ((1u << (rb - base)) - 1u);
+                }
+                if (round && (sticky || (mant & 1ull))) ++mant;  // may carry to 2^53: still exact
+                scale = lo - 149;
+            }
+            // mant * 2^scale, both exact in fp64 (scale lies well inside the normal range)
+            S = __dmul_rn((double)mant, __longlong_as_double((long long)(scale + 1023) << 52));
         }
     }
-    int top = -1;
-    for (int i = W - 1; i >= 0; --i)
-        if (w[i]) { top = i * 32 + 31 - __clz(w[i]); break; }
-    if (top < 0) return 0.0;
-    const int lo = top - 52;
-    if (lo <= 0) {
-        unsigned long long m = ((unsigned long long)w[1] << 32) | w[0];
-        return ldexp((double)m, -149);
-    }
-    const int q = lo >> 5, off = lo & 31;
-    const unsigned long long x = (unsigned long long)w[q] | ((unsigned long long)(q + 1 < W ? w[q + 1] : 0u) << 32);
-    const unsigned long long x2 = q + 2 < W ? w[q + 2] : 0u;
-    unsigned long long mant = off ? ((x >> off) | (x2 << (64 - off))) : x;
-    mant &= (1ull << 53) - 1;
-    const int rb = lo - 1;
-    const uint32_t round = (w[rb >> 5] >> (rb & 31)) & 1u;
-    uint32_t sticky = 0;
-    if (rb > 0) {
-        const int sq = (rb - 1) >> 5;
-        for (int i = 0; i < sq; ++i) sticky |= w[i];
-        const int nb = ((rb - 1) & 31) + 1;  // bits 0 .. rb-1 of word sq
-        sticky |= w[sq] & (nb == 32 ? 0xffffffffu : ((1u << nb) - 1u));
-    }
-    if (round && (sticky || (mant & 1ull))) ++mant;
-    return ldexp((double)mant, lo - 149);
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, S, 0);
 }
 
 // ---------------------------------------------------------------- look-back
@@ -619,18 +651,18 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
 }
 
 // ---------------------------------------------------------------- layer finalisation
-// Run by one warp of the CTA whose tile completed the layer: s from the exact sum,
+// Run by one warp per layer after the compress kernel: s from the exact sum,
 // header, result area; the accumulator and counters are left zeroed for the next
-// call. `tmp` is a zeroed 256-entry shared buffer; it is zeroed again on return.
+// call. `tmp` (256 entries) and `words` (kSumWords entries) are shared scratch;
+// `words` must be zero on entry.
 __device__ void finalize_layer(const KLayer& ly, LayerWs* lw, const uint64_t* desc, unsigned long long* tmp,
-                               int lane)
+                               unsigned long long* words, int lane)
 {
-    __threadfence();
     for (int e = lane; e < 256; e += 32)
         tmp[e] = ptx::ld_relaxed(reinterpret_cast<const uint64_t*>(&lw->acc[e]));
     __syncwarp();
+    const double S = exact_sum_warp(tmp, words, lane);
     if (lane == 0) {
-        const double S = exact_sum_from_buckets(tmp);
         const float s = __double2float_rn(__ddiv_rn(S, (double)ly.nbins));
         const uint32_t err = *reinterpret_cast<volatile uint32_t*>(&lw->err);
         const uint64_t last = ptx::ld_relaxed(&desc[ly.tile_begin + ly.num_tiles - 1]);
@@ -645,12 +677,7 @@ __device__ void finalize_layer(const KLayer& ly, LayerWs* lw, const uint64_t* de
         lw->done = 0;
         lw->err = 0;
     }
-    __syncwarp();
-    for (int e = lane; e < 256; e += 32) {
-        lw->acc[e] = 0ull;
-        tmp[e] = 0ull;
-    }
-    __syncwarp();
+    for (int e = lane; e < 256; e += 32) lw->acc[e] = 0ull;
 }
 
 // ---------------------------------------------------------------- tile geometry
@@ -691,54 +718,67 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint6
 // current one is processed (its bulk copies are already in flight) and the order
 // holds nothing back: every tile's predecessors are processed by co-resident CTAs
 // that never wait on a later tile, so the look-back cannot deadlock.
-// Eight compute warps stream a tile through phases A and C (three barriers per
-// tile), publish its code count and hand the staged codes to one of two look-back
-// warps (one per staging buffer), which resolves the tile's prefix and copies the
-// codes into the message while the compute warps go on. Hand-off uses named
-// barriers FULL[b] (compute -> look-back warp b) and EMPTY[b] (back).
-// Bin maxima accumulate per CTA in exponent buckets and are flushed to the layer's
-// accumulator when the CTA moves to another layer; s is formed afterwards by the
+//
+// Eight compute warps stream each tile; two look-back warps (one per staging
+// buffer, so every other tile) publish the tile's code count, resolve its prefix
+// and copy its codes into the message while the compute warps go on. Hand-off uses
+// mbarriers: FULL[b] (each compute warp arrives once per tile) and EMPTY[b] (the
+// look-back warp arrives when buffer b is free again), so a compute warp never
+// waits for the other compute warps on the warp-sliced path.
+// A stage is refilled as soon as every compute warp has taken what it needs from
+// it: each warp bumps the stage's reader count, and the warp that completes it
+// issues the bulk copies of the CTA's tile after next into the stage.
+//
+// Warp-sliced tiles (16 <= L_T <= 509): a tile is eight slices of
+// bpw = floor(509 / L_T) whole bins, warp w owning slice w, so bin maxima, counts
+// and code ranks are all warp-local and the compute warps never wait for one
+// another inside a tile. Other bin lengths use block-wide phases (see above).
+// Bin maxima accumulate per warp in exponent buckets and are flushed to the
+// layer's accumulator when the warp moves to another layer; s is formed by the
 // finalise kernel.
 constexpr int kLookbackWarps = 2;  // one per staging buffer
 constexpr int kCtaThreads = kThreads + 32 * kLookbackWarps;
 constexpr int kBarCompute = 1;
-constexpr int kBarFull = 2;   // + buffer
-constexpr int kBarEmpty = 4;  // + buffer
 constexpr uint32_t kEndTile = 0xffffffffu;
 
 struct Slot {
-    uint32_t t, total, layer, nrun;
-    uint32_t first_bin, bins, pad0, pad1;
-    uint32_t src[kWarps], dst[kWarps], cnt[kWarps];
+    uint32_t t, layer, first_bin, bins;
+    uint32_t nrun, pad0, pad1, pad2;
+    uint32_t src[kWarps], cnt[kWarps];  // code runs: staging offset and length, in message order
+};
+
+// Shared-memory control block of the compress kernel.
+struct Ctrl {
+    uint64_t stage_full[2];   // bulk copies of the tile in each stage have landed
+    uint64_t buf_full[2];     // compute warps -> look-back warp of buffer b (count kWarps)
+    uint64_t buf_empty[2];    // look-back warp of buffer b -> compute warps (count 1)
+    uint32_t users[2];        // compute warps done reading each stage
+    uint32_t issued[2];       // tiles issued into each stage
+    int32_t issue_layer;      // layer of the last tile issued
+    uint32_t poisoned;        // a wait ran out: later tiles publish errors only
+    uint32_t wsum[kWarps];    // block scan scratch
+    Slot slot[2];
 };
 
 template <int ID, int N>
 __device__ __forceinline__ void bar_sync() { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
-template <int ID, int N>
-__device__ __forceinline__ void bar_arrive() { asm volatile("bar.arrive %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
-// Named barriers of the buffer-indexed pairs (the compute warps and the look-back
-// warp that owns buffer b), with the index known only at run time.
-constexpr int kPair = kThreads + 32;
-__device__ __forceinline__ void full_sync(int b) { if (b) bar_sync<kBarFull + 1, kPair>(); else bar_sync<kBarFull, kPair>(); }
-__device__ __forceinline__ void full_arrive(int b) { if (b) bar_arrive<kBarFull + 1, kPair>(); else bar_arrive<kBarFull, kPair>(); }
-__device__ __forceinline__ void empty_sync(int b) { if (b) bar_sync<kBarEmpty + 1, kPair>(); else bar_sync<kBarEmpty, kPair>(); }
-__device__ __forceinline__ void empty_arrive(int b) { if (b) bar_arrive<kBarEmpty + 1, kPair>(); else bar_arrive<kBarEmpty, kPair>(); }
 __device__ __forceinline__ void compute_sync() { bar_sync<kBarCompute, kThreads>(); }
 
-
-// Barrier among the compute threads that also ANDs a predicate over them.
-__device__ __forceinline__ bool compute_and(bool p)
+// Bounded wait on an mbarrier phase; skipped (reported as failed) once the CTA is
+// poisoned, so that a lost copy or hand-off costs at most one timeout per CTA.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, uint32_t* poisoned)
 {
-    uint32_t r;
-    asm volatile(
-        "{\n\t.reg .pred a, b;\n\t"
-        "setp.ne.u32 a, %1, 0;\n\t"
-        "bar.red.and.pred b, %2, %3, a;\n\t"
-        "selp.u32 %0, 1, 0, b;\n\t}"
-        : "=r"(r)
-        : "r"((uint32_t)p), "n"(kBarCompute), "n"(kThreads)
-        : "memory");
-    return r != 0;
+    if (*reinterpret_cast<volatile uint32_t*>(poisoned)) return false;
+    uint64_t start = 0;
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        const uint64_t now = ptx::globaltimer();
+        if (start == 0) start = now;
+        else if (now - start > timeout_ns) {
+            *reinterpret_cast<volatile uint32_t*>(poisoned) = 1u;
+            return false;
+        }
+    }
+    return true;
 }
 
 // Layer of tile t, searching from layer `lo` (tiles of a CTA only move forward).
@@ -787,9 +827,6 @@ __device__ void issue_tile(const KLayer* lays, uint32_t t, int layer, float* sr,
         if (b1 > ly.n) b1 = te & ~(int64_t)7;
         db = b1 > b0 ? (uint32_t)(b1 - b0) * 2u : 0u;
     }
-    ptx::mbar_arrive_expect_tx(bar, rb + db);
-    if (rb) ptx::bulk_g2s(sr, ly.residue + a0, rb, bar);
-    if (db) ptx::bulk_g2s(sd, static_cast<const uint8_t*>(ly.dw) + b0 * (ly.dw_bf16 ? 2 : 4), db, bar);
     const int pr = (int)(G.ts - a0), pd = (int)(G.ts - b0);
     if (a1 < te || b1 < te) {
         for (int64_t j = max(a1, G.ts); j < te; ++j) sr[pr + (j - G.ts)] = ly.residue[j];
@@ -802,42 +839,39 @@ __device__ void issue_tile(const KLayer* lays, uint32_t t, int layer, float* sr,
         }
         ptx::fence_proxy_async_smem();  // before later bulk copies refill these bytes
     }
+    ptx::mbar_arrive_expect_tx(bar, rb + db);
+    if (rb) ptx::bulk_g2s(sr, ly.residue + a0, rb, bar);
+    if (db) ptx::bulk_g2s(sd, static_cast<const uint8_t*>(ly.dw) + b0 * (ly.dw_bf16 ? 2 : 4), db, bar);
 }
 
-// Exponent buckets of the bin maxima: warp `w` of `nw` handles the groups of 32
-// bins b0 = 32 w, 32 (w + nw), ... A group of 32 maxima mostly has the largest
-// exponent present or the one below it: both are summed with one warp reduction
-// each (at most 32 x 2^24 < 2^32); any other exponent is summed in a loop. Lane 0
-// adds each sum to the CTA's shared buckets with a 64-bit shared atomic.
-__device__ __forceinline__ void bucket_bins(const uint32_t* gmax_s, int bins, unsigned long long* hist, int lane,
-                                            int w, int nw)
+// Exponent buckets of 32 bin maxima (one per lane, 0 for none): the largest
+// exponent present and the one below it are summed with one warp reduction each
+// (at most 32 x 2^24 < 2^32); any other exponent is summed in a loop. Lane 0 adds
+// each sum to the warp's shared buckets.
+__device__ __forceinline__ void bucket_group(uint32_t u, unsigned long long* hist, int lane)
 {
-    for (int b0 = 32 * w; b0 < bins; b0 += 32 * nw) {
-        const int b = b0 + lane;
-        const uint32_t u = b < bins ? gmax_s[b] : 0u;
-        const uint32_t E = u >> 23;
-        const uint32_t M = E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
-        if (__ballot_sync(kFull, u != 0u) == 0u) continue;
-        const uint32_t Eh = __reduce_max_sync(kFull, u ? E : 0u);
-        const uint32_t s_hi = __reduce_add_sync(kFull, (u && E == Eh) ? M : 0u);
-        const uint32_t s_lo = __reduce_add_sync(kFull, (u && Eh > 0 && E == Eh - 1) ? M : 0u);
-        if (lane == 0) {
-            if (s_hi) atomicAdd(&hist[Eh], (unsigned long long)s_hi);
-            if (s_lo) atomicAdd(&hist[Eh - 1], (unsigned long long)s_lo);
-        }
-        uint32_t left = __ballot_sync(kFull, u != 0u && E + 1 < Eh);
-        while (left) {
-            const uint32_t Ek = __shfl_sync(kFull, E, __ffs(left) - 1);
-            const bool mine = ((left >> lane) & 1u) && E == Ek;
-            const uint32_t sum = __reduce_add_sync(kFull, mine ? M : 0u);
-            if (lane == 0) atomicAdd(&hist[Ek], (unsigned long long)sum);
-            left &= ~__ballot_sync(kFull, mine);
-        }
-        __syncwarp();
+    if (__ballot_sync(kFull, u != 0u) == 0u) return;
+    const uint32_t E = u >> 23;
+    const uint32_t M = E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
+    const uint32_t Eh = __reduce_max_sync(kFull, u ? E : 0u);
+    const uint32_t s_hi = __reduce_add_sync(kFull, (u && E == Eh) ? M : 0u);
+    const uint32_t s_lo = __reduce_add_sync(kFull, (u && Eh > 0 && E == Eh - 1) ? M : 0u);
+    if (lane == 0) {
+        if (s_hi) hist[Eh] += (unsigned long long)s_hi;
+        if (s_lo) hist[Eh - 1] += (unsigned long long)s_lo;
     }
+    uint32_t left = __ballot_sync(kFull, u != 0u && E + 1 < Eh);
+    while (left) {
+        const uint32_t Ek = __shfl_sync(kFull, E, __ffs(left) - 1);
+        const bool mine = ((left >> lane) & 1u) && E == Ek;
+        const uint32_t sum = __reduce_add_sync(kFull, mine ? M : 0u);
+        if (lane == 0) hist[Ek] += (unsigned long long)sum;
+        left &= ~__ballot_sync(kFull, mine);
+    }
+    __syncwarp();
 }
 
-// Adds a warp's shared buckets to layer lw's accumulator and clears them.
+// Adds a warp's buckets to layer lw's accumulator and clears them.
 __device__ __forceinline__ void flush_buckets(unsigned long long* hist, LayerWs* lw, int lane)
 {
     __syncwarp();
@@ -852,10 +886,10 @@ __device__ __forceinline__ void flush_buckets(unsigned long long* hist, LayerWs*
 }
 
 // Look-back warp that owns staging buffer b, i.e. every other tile of the CTA.
-// For each such tile, in order: it writes the per-bin counts into the message and
-// clears the bin arrays; then it resolves the tile's prefix with the look-back (by
-// now the predecessors have had time to publish) and copies the staged codes into
-// the message.
+// For each such tile, in order: it sums the code runs, publishes the tile's
+// AGGREGATE (INCLUSIVE for a layer's first tile), writes the per-bin counts into
+// the message and clears the bin arrays; then it resolves the tile's prefix with
+// the look-back and copies the staged codes into the message.
 struct LookbackCtx {
     uint16_t* stg;
     uint32_t* gmax;
@@ -863,33 +897,72 @@ struct LookbackCtx {
     uint32_t bin_len;  // entries of gmax / cnt to clear
 };
 
-__device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, const Slot* slots, const LookbackCtx& C,
+__device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, Ctrl* ctl, const LookbackCtx& C,
                               int b, int lane)
 {
     uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
     uint64_t* texcl = desc + g.total_tiles;
-    for (;;) {
-        full_sync(b);
-        const Slot& sl = slots[b];
+    for (uint32_t j = 0;; ++j) {
+        const bool got = wait_phase(&ctl->buf_full[b], j & 1u, g.timeout_ns, &ctl->poisoned);
+        const Slot& sl = ctl->slot[b];
         const uint32_t t = sl.t;
         if (t == kEndTile) break;
+        if (!got || *reinterpret_cast<volatile uint32_t*>(&ctl->poisoned)) {
+            // The CTA is poisoned: the tile's data or hand-off may be incomplete, so
+            // only an error is published, for this tile and every later one of the
+            // CTA's (the compute warps keep handing them over, or stop).
+            if (!got) {
+                const uint32_t T = g.total_tiles;
+                int l = 0;
+                for (uint32_t u = (uint32_t)blockIdx.x + (2 * j + b) * gridDim.x; u < T; u += 2 * gridDim.x) {
+                    l = layer_from(lays, g.num_layers, u, l);
+                    if (lane == 0) {
+                        ptx::st_relaxed(&desc[u], kFlagErr);
+                        atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
+                    }
+                }
+                break;
+            }
+            const int l = layer_from(lays, g.num_layers, t, 0);
+            if (lane == 0) {
+                ptx::st_relaxed(&desc[t], kFlagErr);
+                atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&ctl->buf_empty[b]);
+            continue;
+        }
         const int l = (int)sl.layer;
         const KLayer& ly = lays[l];
         const int bins = (int)sl.bins;
+        // code runs: exclusive offsets and the tile's total
+        const uint32_t nrun = sl.nrun;
+        const uint32_t v = lane < (int)nrun ? sl.cnt[lane] : 0u;
+        uint32_t incl = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t total = __shfl_sync(kFull, incl, 31);
+        const uint32_t my_dst = incl - v;
+        const uint32_t my_src = lane < (int)nrun ? sl.src[lane] : 0u;
+        if (lane == 0 && t != g.inject_skip_tile)
+            ptx::st_relaxed(&desc[t], (t == ly.tile_begin ? kFlagIncl : kFlagAgg) | total);
         uint16_t* cdst = reinterpret_cast<uint16_t*>(ly.msg + 8) + sl.first_bin;
         for (int bb = lane; bb < bins; bb += 32) cdst[bb] = (uint16_t)C.cnt[bb];
         __syncwarp();
         for (uint32_t bb = lane; bb < C.bin_len; bb += 32) { C.gmax[bb] = 0u; C.cnt[bb] = 0u; }
         uint64_t excl = 0;
-        const bool ok = lookback_resolve(desc, t, ly.tile_begin, sl.total, g.timeout_ns, lane,
+        const bool ok = lookback_resolve(desc, t, ly.tile_begin, total, g.timeout_ns, lane,
                                          t != g.inject_skip_tile, &excl);
         if (ok) {
             if (lane == 0) texcl[t] = excl;
             uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
-            for (uint32_t r = 0; r < sl.nrun; ++r) {
-                const uint32_t n = sl.cnt[r];
-                const uint16_t* sp = C.stg + sl.src[r];
-                const unsigned long long base = excl + sl.dst[r];
+            for (uint32_t r = 0; r < nrun; ++r) {
+                const uint32_t n = __shfl_sync(kFull, v, r);
+                const unsigned long long base = excl + __shfl_sync(kFull, my_dst, r);
+                const uint16_t* sp = C.stg + __shfl_sync(kFull, my_src, r);
                 if (ly.code_bytes == 1) {
                     for (uint32_t k = lane; k < n; k += 32) codes[base + k] = (uint8_t)sp[k];
                 } else {
@@ -901,19 +974,160 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
             atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
         }
         __syncwarp();
-        empty_arrive(b);
+        if (lane == 0) ptx::mbar_arrive(&ctl->buf_empty[b]);
     }
+}
+
+// Warp-sliced tile: warp `warp` owns bins [wb0, wb1) of the tile, at most 509
+// elements, held as up to 512 slots of 16 per lane (slot 0 of the warp is the
+// 16-byte boundary at or before its first element). Per lane: G = residue + dW,
+// residue := G in global memory, and |H| = |fl32(G + dW)| with the masks of G != 0
+// and G < 0 kept in registers; `release` then gives the stage back. Bin maxima and
+// counts go through the warp's scratch (wg, wc: zero on entry and on return), the
+// counts into the tile's count array, the maxima into the warp's exponent buckets,
+// and the codes, ranked with a warp scan, to stg[we0 + rank], we0 being the warp's
+// first tile element. Returns the warp's code count; *src gets we0.
+template <bool BF16, class Release>
+__device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G, int pr, int pd, const float* sr,
+                                              const void* sd, uint32_t* wg, uint32_t* wc, uint32_t* cnt_tile,
+                                              uint16_t* stg, unsigned long long* hist, int warp, int lane,
+                                              uint32_t* src, Release&& release)
+{
+    const int L = ly.bin_len;
+    const int bpw = ly.bpw;
+    const int wb0 = min(G.bins, warp * bpw), wb1 = min(G.bins, wb0 + bpw);
+    const int we0 = wb0 * L, we1 = min(wb1 * L, G.tl);
+    const int e_first = (((pr + we0) & ~3) - pr) + kSeg * lane;  // tile element of the lane's slot 0
+    const bool active = we1 > we0 && e_first + kSeg > we0 && e_first < we1;
+    const int vlo = max(0, we0 - e_first), vhi = min(kSeg, we1 - e_first);
+    const uint32_t valid = (active && vhi > vlo) ? (((1u << (vhi - vlo)) - 1u) << vlo) : 0u;
+    const int rel0 = max(e_first, we0) - we0;
+    const int bin_lo = active ? (int)__umulhi((uint32_t)rel0, ly.inv_len) : 0;  // warp-relative bin
+    const int split = (bin_lo + 1) * L - (e_first - we0);  // first slot of bin_lo + 1
+    const int rot = seg_rot(lane);
+    float ah[4][4];
+    uint32_t nz = 0, ng = 0;
+    float m_lo = 0.0f, m_hi = 0.0f;
+    if (active) {
+        const bool edge = valid != 0xffffu;
+        const float* rs = sr + pr + e_first;
+        float* gres = ly.residue + G.ts + e_first;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q0 = 4 * (k ^ rot);
+            const float4 r = *reinterpret_cast<const float4*>(rs + q0);
+            float d[4], gv[4];
+            if constexpr (BF16) {
+                const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(sd) + pd + e_first + q0);
+                d[0] = bf16_lo(u.x); d[1] = bf16_hi(u.x); d[2] = bf16_lo(u.y); d[3] = bf16_hi(u.y);
+            } else {
+                const float4 w = *reinterpret_cast<const float4*>(static_cast<const float*>(sd) + pd + e_first + q0);
+                d[0] = w.x; d[1] = w.y; d[2] = w.z; d[3] = w.w;
+            }
+            gv[0] = __fadd_rn(r.x, d[0]);
+            gv[1] = __fadd_rn(r.y, d[1]);
+            gv[2] = __fadd_rn(r.z, d[2]);
+            gv[3] = __fadd_rn(r.w, d[3]);
+            const uint32_t vq = (valid >> q0) & 0xfu;
+            if (edge) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if (!((vq >> i) & 1u)) gv[i] = 0.0f;
+            }
+            uint32_t nzq = 0, ngq = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                ah[k][i] = fabsf(__fadd_rn(gv[i], d[i]));
+                nzq |= gv[i] != 0.0f ? (1u << i) : 0u;
+                ngq |= gv[i] < 0.0f ? (1u << i) : 0u;
+            }
+            nz |= nzq << q0;
+            ng |= ngq << q0;
+            // residue := G (sent elements are corrected by the fix-up kernel)
+            float* gp = gres + q0;
+            if (vq == 0xfu) {
+                *reinterpret_cast<float4*>(gp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+            } else if (vq) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if ((vq >> i) & 1u) gp[i] = gv[i];
+            }
+            const float cm = fmaxf(fmaxf(fabsf(gv[0]), fabsf(gv[1])), fmaxf(fabsf(gv[2]), fabsf(gv[3])));
+            if (q0 + 4 <= split) {
+                m_lo = fmaxf(m_lo, cm);
+            } else if (q0 >= split) {
+                m_hi = fmaxf(m_hi, cm);
+            } else {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if (q0 + i < split) m_lo = fmaxf(m_lo, fabsf(gv[i]));
+                    else m_hi = fmaxf(m_hi, fabsf(gv[i]));
+                }
+            }
+        }
+    }
+    __syncwarp();
+    release();  // the stage is not read again by this warp
+    if (m_lo > 0.0f) atomicMax(&wg[bin_lo], __float_as_uint(m_lo));
+    if (m_hi > 0.0f) atomicMax(&wg[bin_lo + 1], __float_as_uint(m_hi));
+    __syncwarp();
+    uint32_t f = 0;
+    if (active) {
+        const float gm_lo = __uint_as_float(wg[bin_lo]);
+        const float gm_hi = split < kSeg ? __uint_as_float(wg[bin_lo + 1]) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q0 = 4 * (k ^ rot);
+            uint32_t nib = 0;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                nib |= ah[k][i] >= (q0 + i < split ? gm_lo : gm_hi) ? (1u << i) : 0u;
+            f |= nib << q0;
+        }
+        f &= nz;
+        const uint32_t lomask = split >= kSeg ? 0xffffu : ((1u << max(split, 0)) - 1u);
+        const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
+        if (c_lo) atomicAdd(&wc[bin_lo], c_lo);
+        if (c_hi) atomicAdd(&wc[bin_lo + 1], c_hi);
+    }
+    __syncwarp();
+    {
+        // per bin of the slice: count to the tile's array, maximum to the buckets; scratch back to zero
+        const int nb = wb1 - wb0;
+        const uint32_t u = lane < nb ? wg[lane] : 0u;
+        if (lane < nb) cnt_tile[wb0 + lane] = wc[lane];
+        wg[lane] = 0u;
+        wc[lane] = 0u;
+        bucket_group(u, hist, lane);
+    }
+    const uint32_t c = __popc(f);
+    uint32_t incl = c;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    const uint32_t total = __shfl_sync(kFull, incl, 31);
+    uint32_t pos = (uint32_t)we0 + incl - c;
+    while (f) {
+        const int idx = __ffs(f) - 1;
+        f &= f - 1;
+        const int off = (e_first + idx - we0) - bin_lo * L - (idx < split ? 0 : L);
+        stg[pos++] = (uint16_t)(((uint32_t)off << 1) | ((ng >> idx) & 1u));
+    }
+    *src = (uint32_t)we0;
+    return total;
 }
 
 // One-round segment tile held in registers (at most 256 segments, one per thread):
 // phase A computes G, residue := G, the bin maxima and, per slot, |H| = |fl32(G + dW)|
 // and the masks of G != 0 and G < 0 (all phase C needs); after a barrier the stage
-// is no longer read and thread 0 refills it with the CTA's tile after next; phase C
-// then runs from the registers (flags, per-bin counts, codes ranked per warp and
-// staged at stg[wbase + rank]). Returns the warp's code count.
-template <bool BF16, class Refill>
+// is no longer read and is released; phase C then runs from the registers (flags,
+// per-bin counts, codes ranked per warp and staged at stg[wbase + rank]). Returns
+// the warp's code count.
+template <bool BF16, class Release>
 __device__ __forceinline__ uint32_t tile_in_registers(const Tile& T, uint32_t* gmax_s, uint32_t* cnt_s,
-                                                      uint16_t* stg, int tid, int* wbase_out, Refill&& refill)
+                                                      uint16_t* stg, int tid, int* wbase_out, Release&& release)
 {
     const int nseg = (T.pr + T.tl + kSeg - 1) / kSeg;
     const int lane = tid & 31, warp = tid >> 5;
@@ -980,7 +1194,7 @@ __device__ __forceinline__ uint32_t tile_in_registers(const Tile& T, uint32_t* g
         if (m_hi > 0.0f) atomicMax(&gmax_s[G.bin_lo + 1], __float_as_uint(m_hi));
     }
     compute_sync();  // all bin maxima are in; the stage is not read again
-    if (tid == 0) refill();
+    release();
     uint32_t f = 0;
     if (active) {
         const float gm_lo = __uint_as_float(gmax_s[G.bin_lo]);
@@ -1020,39 +1234,112 @@ __device__ __forceinline__ uint32_t tile_in_registers(const Tile& T, uint32_t* g
     return total;
 }
 
+// Block-wide tile (bin lengths outside the warp-sliced range): phases A and C
+// with barriers among the compute warps, kept out of line so that the
+// warp-sliced path's register allocation does not pay for it.
+template <class Release>
+__device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int pr, int pd, float* sr_s, void* sd_s,
+                                        float* gbuf, uint32_t* gmax_c, uint32_t* cnt_c, uint16_t* stg, Slot& sl,
+                                        uint32_t* wsum, unsigned long long* hist, int tid, Release* release_p)
+{
+    Release& release = *release_p;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int64_t te = G.ts + G.tl;
+    Tile Tl;
+    Tl.gres = ly.residue + (G.ts - pr);
+    Tl.sr = sr_s; Tl.gs = gbuf; Tl.sd = sd_s; Tl.pr = pr; Tl.pd = pd; Tl.tl = G.tl; Tl.L = ly.bin_len;
+    Tl.bins = G.bins;
+    Tl.ch = min(ly.bin_len, 32 * (int)ly.vec * kRounds);
+    Tl.cpb = (ly.bin_len + Tl.ch - 1) / Tl.ch;
+    Tl.inv_len = ly.inv_len;
+    const bool seg = ly.bin_len >= kSeg;
+    const bool one_round = seg && pr + G.tl <= kThreads * kSeg;
+    const int nchunks = G.bins * Tl.cpb;
+    const int cpw = (nchunks + kWarps - 1) / kWarps;
+    const int c_begin = min(nchunks, warp * cpw), c_end = min(nchunks, c_begin + cpw);
+    compute_sync();  // every compute warp is past its waits for this tile
+    if (one_round) {
+        // phases A and C with G and dW in registers; the stage is released in between
+        int wb = 0;
+        uint32_t wt;
+        if (ly.dw_bf16) wt = tile_in_registers<true>(Tl, gmax_c, cnt_c, stg, tid, &wb, release);
+        else wt = tile_in_registers<false>(Tl, gmax_c, cnt_c, stg, tid, &wb, release);
+        if (lane == 0) {
+            sl.src[warp] = (uint32_t)wb;
+            sl.cnt[warp] = wt;
+            if (warp == 0) sl.nrun = kWarps;
+        }
+    } else {
+        // phase A: G (to the G buffer and global memory) and bin maxima
+        SegGeo mine;
+        if (seg) {
+            if (ly.dw_bf16) phase_a_seg<true>(Tl, gmax_c, tid, &mine);
+            else phase_a_seg<false>(Tl, gmax_c, tid, &mine);
+        } else {
+            ADACOMP_DISPATCH(ly.vec, ly.dw_bf16, (phase_a<VEC, BF16>(Tl, c_begin, c_end, gmax_c, lane)))
+        }
+        compute_sync();
+        if (!seg) {  // short bins: residue := G from the G buffer, then phase C per warp
+            for (int64_t j = G.ts + tid; j < te; j += kThreads) ly.residue[j] = gbuf[pr + (j - G.ts)];
+            const int wb = c_begin < c_end ? chunk_at(Tl, c_begin).e0 : 0;
+            uint32_t wt = 0;
+            ADACOMP_DISPATCH(ly.vec, ly.dw_bf16,
+                             (wt = phase_c<VEC, BF16>(Tl, c_begin, c_end, gmax_c, cnt_c, stg, wb, lane)))
+            if (lane == 0) {
+                sl.src[warp] = (uint32_t)wb;
+                sl.cnt[warp] = wt;
+                if (warp == 0) sl.nrun = kWarps;
+            }
+        } else {  // several rounds: block-wide scan (ends with a barrier)
+            uint32_t total;
+            if (ly.dw_bf16) total = phase_c_seg<true>(Tl, gmax_c, cnt_c, stg, wsum, tid);
+            else total = phase_c_seg<false>(Tl, gmax_c, cnt_c, stg, wsum, tid);
+            if (tid == 0) {
+                sl.nrun = 1;
+                sl.src[0] = 0;
+                sl.cnt[0] = total;
+            }
+        }
+        compute_sync();  // phase C was the last reader of the stage
+        release();
+    }
+    compute_sync();  // every warp's bin maxima are in gmax_c
+    for (int b0 = 32 * warp; b0 < G.bins; b0 += 32 * kWarps)
+        bucket_group(b0 + lane < G.bins ? gmax_c[b0 + lane] : 0u, hist, lane);
+}
+
+// kPaths: 1 = every layer of the launch is warp-sliced, 2 = none is, 3 = mixed.
+// The single-path instantiations keep the warp-sliced path's registers free of
+// the block-wide path's needs.
+template <int kPaths>
 __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_constant__ KGroup g,
                                                                   uint8_t* __restrict__ ws)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf);
-    uint8_t* p = smem;
-    float* sr[2];
-    void* sd[2];
-    sr[0] = reinterpret_cast<float*>(p); p += P.r_bytes;
-    sd[0] = p; p += P.d_bytes;
-    sr[1] = reinterpret_cast<float*>(p); p += P.r_bytes;
-    sd[1] = p; p += P.d_bytes;
+    // stage s: residue slice at smem + s * stage_bytes, dW slice r_bytes after it
+    const uint32_t stage_bytes = P.r_bytes + P.d_bytes;
+    auto stage_r = [&](int s) { return reinterpret_cast<float*>(smem + s * stage_bytes); };
+    auto stage_d = [&](int s) { return static_cast<void*>(smem + s * stage_bytes + P.r_bytes); };
+    uint8_t* p = smem + 2 * stage_bytes;
     KLayer* lays = reinterpret_cast<KLayer*>(p); p += P.layer_bytes;
-    float* gbuf = reinterpret_cast<float*>(p); p += P.g_bytes;  // G, for tiles not held in registers
+    float* gbuf = reinterpret_cast<float*>(p); p += P.g_bytes;  // G, for tiles processed through shared memory
     uint16_t* stg0 = reinterpret_cast<uint16_t*>(p); p += 2 * P.stg_bytes;
     const uint32_t stg_stride = P.stg_bytes / 2;
     uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;  // 2 buffers of bin_stride
     uint32_t* cnt_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;   // 2 buffers of bin_stride
     const uint32_t bin_stride = P.bin_bytes / 8;
-    unsigned long long* hist = reinterpret_cast<unsigned long long*>(p); p += 4096;  // [256] exponent buckets + spare
+    unsigned long long* hist0 = reinterpret_cast<unsigned long long*>(p); p += kHistBytes;  // [warp][256] buckets
+    uint32_t* wscr0 = reinterpret_cast<uint32_t*>(p); p += kWarpScratchBytes;  // [warp][2][kWarpScratch]
     TileGeo* info = reinterpret_cast<TileGeo*>(p); p += 2048;  // [2]: geometry of the tile in each stage
-    uint64_t* bar = reinterpret_cast<uint64_t*>(p); p += 16;
-    Slot* slots = reinterpret_cast<Slot*>(p); p += 2 * sizeof(Slot);
-    uint32_t* wsum = reinterpret_cast<uint32_t*>(p);         // [8]
-    uint32_t* wtot = wsum + 8;                               // [8]
-    int32_t* wbase = reinterpret_cast<int32_t*>(wsum + 16);  // [8]
+    Ctrl* ctl = reinterpret_cast<Ctrl*>(p);
 
-    uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
     const uint32_t T = g.total_tiles;
     const uint32_t G0 = blockIdx.x, GS = gridDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    for (int e = tid; e < 512; e += kCtaThreads) hist[e] = 0ull;
+    for (int e = tid; e < kHistBytes / 8; e += kCtaThreads) hist0[e] = 0ull;
+    for (int e = tid; e < kWarpScratchBytes / 4; e += kCtaThreads) wscr0[e] = 0u;
     {
         const uint4* src = reinterpret_cast<const uint4*>(&g.layer[0]);
         uint4* dst = reinterpret_cast<uint4*>(lays);
@@ -1060,22 +1347,29 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
     }
     __syncthreads();
     for (uint32_t e = tid; e < 2 * bin_stride; e += kCtaThreads) { gmax_s[e] = 0u; cnt_s[e] = 0u; }
-    int issue_layer = 0;  // layer of the last tile issued (thread 0 issues every tile)
     if (tid == 0) {
-        ptx::mbar_init(&bar[0], 1);
-        ptx::mbar_init(&bar[1], 1);
+        ctl->users[0] = ctl->users[1] = 0u;
+        ctl->issued[0] = ctl->issued[1] = 0u;
+        ctl->poisoned = 0u;
+        for (int k = 0; k < 2; ++k) {
+            ptx::mbar_init(&ctl->stage_full[k], 1);
+            ptx::mbar_init(&ctl->buf_full[k], kWarps);
+            ptx::mbar_init(&ctl->buf_empty[k], 1);
+        }
         ptx::fence_mbar_init();
+        int il = 0;
         for (int k = 0; k < 2; ++k) {
             const uint32_t t = G0 + k * GS;
             if (t < T) {
-                issue_layer = layer_from(lays, g.num_layers, t, issue_layer);
-                issue_tile(lays, t, issue_layer, sr[k], sd[k], &bar[k], &info[k]);
+                il = layer_from(lays, g.num_layers, t, il);
+                issue_tile(lays, t, il, stage_r(k), stage_d(k), &ctl->stage_full[k], &info[k]);
+                ctl->issued[k] = 1u;
             }
         }
+        ctl->issue_layer = il;
     }
     __syncthreads();
 
-    bool poisoned = false;
     uint32_t it = 0;
     if (warp >= kWarps) {
         const int b = warp - kWarps;  // look-back warp of staging buffer b
@@ -1084,156 +1378,124 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
         C.gmax = gmax_s + b * bin_stride;
         C.cnt = cnt_s + b * bin_stride;
         C.bin_len = bin_stride;
-        lookback_warp(g, lays, ws, slots, C, b, lane);
+        lookback_warp(g, lays, ws, ctl, C, b, lane);
     } else {
+        unsigned long long* hist = hist0 + warp * 256;
+        uint32_t* wg = wscr0 + warp * 2 * kWarpScratch;
+        uint32_t* wc = wg + kWarpScratch;
         int hist_layer = -1;
         for (;; ++it) {
             const uint32_t t = G0 + it * GS;
             if (t >= T) break;
             const int s = it & 1;  // stage, staging buffer and bin-array buffer
-            const uint32_t parity = (it >> 1) & 1u;
-            if (!compute_and(wait_stage(&bar[s], parity, g.timeout_ns))) {
-                poisoned = true;
-                break;
-            }
+            // Bounded waits. A copy or hand-off that never completes poisons the CTA:
+            // no further copies are issued, and the look-back warps publish only
+            // errors from then on; the compute warps still run every tile (from
+            // whatever the buffers hold: every index stays inside its buffer) so
+            // that the hand-off protocol ends normally.
+            wait_phase(&ctl->stage_full[s], (it >> 1) & 1u, g.timeout_ns, &ctl->poisoned);
             // the look-back warp of this parity has finished tile it-2: the staging
             // buffer and bin arrays of parity s are free and cleared
-            if (it >= 2) empty_sync(s);
+            if (it >= 2) wait_phase(&ctl->buf_empty[s], ((it >> 1) & 1u) ^ 1u, g.timeout_ns, &ctl->poisoned);
+            __syncwarp();
             const TileGeo G = info[s];
             const KLayer& ly = lays[G.layer];
             if (G.layer != hist_layer) {  // new layer: hand the buckets to the previous one
-                if (warp == 1 && hist_layer >= 0)
+                if (hist_layer >= 0)
                     flush_buckets(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
                 hist_layer = G.layer;
             }
             uint32_t* gmax_c = gmax_s + s * bin_stride;
             uint32_t* cnt_c = cnt_s + s * bin_stride;
             const int pr = (int)(G.ts & 3), pd = ly.dw_bf16 ? (int)(G.ts & 7) : pr;
-            float* r_s = sr[s];
-            void* d_s = sd[s];
             const int64_t te = G.ts + G.tl;
-
-            Tile Tl;
-            Tl.gres = ly.residue + (G.ts - pr);
-            Tl.sr = r_s; Tl.gs = gbuf; Tl.sd = d_s; Tl.pr = pr; Tl.pd = pd; Tl.tl = G.tl; Tl.L = ly.bin_len; Tl.bins = G.bins;
-            Tl.ch = min(ly.bin_len, 32 * (int)ly.vec * kRounds);
-            Tl.cpb = (ly.bin_len + Tl.ch - 1) / Tl.ch;
-            Tl.inv_len = ly.inv_len;
-            const bool seg = ly.bin_len >= kSeg;
-            const bool one_round = seg && pr + G.tl <= kThreads * kSeg;
-            const int nchunks = G.bins * Tl.cpb;
-            const int cpw = (nchunks + kWarps - 1) / kWarps;
-            const int c_begin = min(nchunks, warp * cpw), c_end = min(nchunks, c_begin + cpw);
-
             uint16_t* stg = stg0 + s * stg_stride;
-            Slot& sl = slots[s];
+            Slot& sl = ctl->slot[s];
             const uint32_t t_next = t + 2 * GS;
-            // thread 0: start the CTA's tile after next into stage s once it is free
-            auto refill = [&]() {
-                if (t_next < T) {
-                    issue_layer = layer_from(lays, g.num_layers, t_next, issue_layer);
-                    issue_tile(lays, t_next, issue_layer, sr[s], sd[s], &bar[s], &info[s]);
-                }
-            };
-            if (one_round) {
-                // phases A and C with G and dW in registers; the stage is refilled in between
-                int wb = 0;
-                uint32_t wt;
-                if (ly.dw_bf16) wt = tile_in_registers<true>(Tl, gmax_c, cnt_c, stg, tid, &wb, refill);
-                else wt = tile_in_registers<false>(Tl, gmax_c, cnt_c, stg, tid, &wb, refill);
-                if (lane == 0) { wtot[warp] = wt; wbase[warp] = wb; }
-                compute_sync();
-            } else {
-                // phase A: G (to the G buffer and global memory) and bin maxima
-                SegGeo mine;
-                if (seg) {
-                    if (ly.dw_bf16) phase_a_seg<true>(Tl, gmax_c, tid, &mine);
-                    else phase_a_seg<false>(Tl, gmax_c, tid, &mine);
-                } else {
-                    ADACOMP_DISPATCH(ly.vec, ly.dw_bf16, (phase_a<VEC, BF16>(Tl, c_begin, c_end, gmax_c, lane)))
-                }
-                compute_sync();
-                if (!seg) {  // short bins: residue := G from the G buffer, then phase C per warp
-                    for (int64_t j = G.ts + tid; j < te; j += kThreads) ly.residue[j] = gbuf[pr + (j - G.ts)];
-                    const int wb = c_begin < c_end ? chunk_at(Tl, c_begin).e0 : 0;
-                    uint32_t wt = 0;
-                    ADACOMP_DISPATCH(ly.vec, ly.dw_bf16,
-                                     (wt = phase_c<VEC, BF16>(Tl, c_begin, c_end, gmax_c, cnt_c, stg, wb, lane)))
-                    if (lane == 0) { wtot[warp] = wt; wbase[warp] = wb; }
-                    compute_sync();
-                } else {  // several rounds: block-wide scan (ends with a barrier)
-                    uint32_t total;
-                    if (ly.dw_bf16) total = phase_c_seg<true>(Tl, gmax_c, cnt_c, stg, wsum, tid);
-                    else total = phase_c_seg<false>(Tl, gmax_c, cnt_c, stg, wsum, tid);
-                    if (tid == 0) {
-                        sl.total = total;
-                        sl.nrun = 1;
-                        sl.src[0] = 0; sl.dst[0] = 0; sl.cnt[0] = total;
-                    }
-                }
-                if (tid == 0) refill();  // phase C was the last reader of stage s
-            }
-
-            if (warp == 0) {
-                if (one_round || !seg) {
-                    const uint32_t v = lane < kWarps ? wtot[lane] : 0u;
-                    uint32_t incl = v;
-#pragma unroll
-                    for (int o = 1; o < 32; o <<= 1) {
-                        const uint32_t y = __shfl_up_sync(kFull, incl, o);
-                        if (lane >= o) incl += y;
-                    }
-                    if (lane < kWarps) {
-                        sl.src[lane] = (uint32_t)wbase[lane];
-                        sl.dst[lane] = incl - v;
-                        sl.cnt[lane] = v;
-                    }
-                    const uint32_t tot = __shfl_sync(kFull, incl, 31);
-                    if (lane == 0) {
-                        sl.total = tot;
-                        sl.nrun = kWarps;
-                    }
-                }
+            // every compute warp calls this once per tile when it no longer reads the
+            // stage; the last one starts the CTA's tile after next into it
+            auto release = [&]() {
                 if (lane == 0) {
-                    sl.t = t;
-                    sl.layer = (uint32_t)G.layer;
-                    sl.first_bin = G.first_bin;
-                    sl.bins = (uint32_t)G.bins;
-                    if (t != g.inject_skip_tile)
-                        ptx::st_relaxed(&desc[t], (t == ly.tile_begin ? kFlagIncl : kFlagAgg) | sl.total);
+                    __threadfence_block();
+                    const uint32_t prev = atomicAdd(&ctl->users[s], 1u);
+                    if (prev == kWarps - 1) {
+                        ctl->users[s] = 0u;
+                        __threadfence_block();
+                        if (t_next < T && !*reinterpret_cast<volatile uint32_t*>(&ctl->poisoned)) {
+                            const int il = layer_from(lays, g.num_layers, t_next, ctl->issue_layer);
+                            ctl->issue_layer = il;
+                            issue_tile(lays, t_next, il, stage_r(s), stage_d(s), &ctl->stage_full[s], &info[s]);
+                            ctl->issued[s] += 1u;
+                        }
+                    }
+                }
+                __syncwarp();
+            };
+
+            bool sliced;
+            if constexpr (kPaths == 1) sliced = true;
+            else if constexpr (kPaths == 2) sliced = false;
+            else sliced = ly.bpw != 0;
+            if (sliced) {
+                if constexpr (kPaths & 1) {
+                // warp-sliced tile: no barrier among the compute warps
+                uint32_t src = 0, cnt;
+                if (ly.dw_bf16)
+                    cnt = warp_tile<true>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, hist, warp, lane, &src,
+                                          release);
+                else
+                    cnt = warp_tile<false>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, hist, warp, lane, &src,
+                                           release);
+                if (lane == 0) {
+                    sl.src[warp] = src;
+                    sl.cnt[warp] = cnt;
+                    if (warp == 0) sl.nrun = kWarps;
+                }
                 }
             } else {
-                bucket_bins(gmax_c, G.bins, hist, lane, warp - 1, kWarps - 1);
+                if constexpr ((kPaths & 2) != 0)
+                    block_tile(ly, G, pr, pd, stage_r(s), stage_d(s), gbuf, gmax_c, cnt_c, stg, sl, ctl->wsum, hist, tid,
+                               &release);
             }
-            full_arrive(s);
+            if (tid == 0) {
+                sl.t = t;
+                sl.layer = (uint32_t)G.layer;
+                sl.first_bin = G.first_bin;
+                sl.bins = (uint32_t)G.bins;
+            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(&ctl->buf_full[s]);
         }
-        compute_sync();  // every warp's additions to the buckets are in
-        if (warp == 1 && hist_layer >= 0)
-            flush_buckets(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+        if (hist_layer >= 0) flush_buckets(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
         // hand each look-back warp the end marker once it has released its buffer:
-        // buffer b carried the tiles it' < it with it' % 2 == b
+        // buffer b carried the tiles it' < it with it' % 2 == b. Every warp waits for
+        // that release before it arrives: an arrival is not tied to a phase, so one
+        // made early would count towards the last tile's hand-off.
         for (int b = 0; b < 2; ++b) {
-            if ((it + 1 - b) / 2 >= 1) empty_sync(b);
-            if (tid == 0) slots[b].t = kEndTile;
-            full_arrive(b);
+            const uint32_t uses = (it + 1 - b) / 2;  // tiles handed over on buffer b
+            if (lane == 0) {
+                if (uses >= 1) wait_phase(&ctl->buf_empty[b], (uses - 1) & 1u, g.timeout_ns, &ctl->poisoned);
+                if (warp == 0) ctl->slot[b].t = kEndTile;
+                ptx::mbar_arrive(&ctl->buf_full[b]);
+            }
+            __syncwarp();
         }
     }
     __syncthreads();
 
-    if (poisoned && tid == 0) {
-        // A bulk copy never completed: mark this CTA's remaining tiles as errors so
-        // no other tile waits on them, then give the outstanding copies one more
-        // bounded wait before the CTA's shared memory is released.
-        int l = 0;
-        for (uint32_t t = G0 + it * GS; t < T; t += GS) {
-            l = layer_from(lays, g.num_layers, t, l);
-            ptx::st_relaxed(&desc[t], kFlagErr);
-            atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
+    if (tid == 0 && *reinterpret_cast<volatile uint32_t*>(&ctl->poisoned)) {
+        // Give the copies that may still be in flight one more bounded wait before
+        // the CTA's shared memory is released.
+        for (int k = 0; k < 2; ++k) {
+            if (ctl->issued[k] == 0u) continue;
+            const uint32_t par = (ctl->issued[k] - 1u) & 1u;
+            uint64_t start = 0;
+            while (!ptx::mbar_try_wait(&ctl->stage_full[k], par)) {
+                const uint64_t now = ptx::globaltimer();
+                if (start == 0) start = now;
+                else if (now - start > g.timeout_ns) break;
+            }
         }
-    }
-    if (poisoned && warp < kWarps) {
-        wait_stage(&bar[it & 1], (it >> 1) & 1u, g.timeout_ns);
-        if (G0 + (it + 1) * GS < T) wait_stage(&bar[(it + 1) & 1], ((it + 1) >> 1) & 1u, g.timeout_ns);
     }
 }
 
@@ -1242,95 +1504,117 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
 __global__ void __launch_bounds__(32) finalize_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
 {
     __shared__ unsigned long long tmp[256];
+    __shared__ unsigned long long words[kSumWords];
     const int l = blockIdx.x;
-    for (int e = threadIdx.x; e < 256; e += 32) tmp[e] = 0ull;
+    if (threadIdx.x < kSumWords) words[threadIdx.x] = 0ull;
     __syncwarp();
     const uint64_t* desc = reinterpret_cast<const uint64_t*>(ws + ws_desc_offset(g.num_layers));
-    finalize_layer(g.layer[l], reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l)), desc, tmp, threadIdx.x);
+    finalize_layer(g.layer[l], reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l)), desc, tmp, words, threadIdx.x);
 }
 
 // ---------------------------------------------------------------- fix-up kernel
 // For every sent element: residue = fl32(G - s) if G > 0, fl32(G + s) if G < 0
-// (the residue still holds G). Tiles are visited in reverse order, so the most
-// recently written residue lines are the likeliest to still be in L2. Also returns
-// the look-back descriptors to zero for the next call.
+// (the residue still holds G). One warp per tile, tiles in reverse order so the
+// most recently written residue lines are the likeliest to still be in L2. The
+// warp turns the tile's per-bin counts into an exclusive prefix (shared memory,
+// one array per warp); each lane then takes a contiguous run of the tile's codes,
+// finds the bin of its first code by binary search and walks forward, gathering
+// kFixBatch residues before it writes them back. Also returns the look-back
+// descriptors to zero for the next call.
 constexpr int kFixThreads = 256;
+constexpr int kFixWarps = kFixThreads / 32;
+constexpr int kFixBatch = 4;
+
+__host__ __device__ inline uint32_t fix_smem_bytes(uint32_t num_layers, uint32_t max_bins)
+{
+    return num_layers * (uint32_t)sizeof(KLayer) + kFixWarps * (max_bins + 2) * 4;
+}
 
 __global__ void __launch_bounds__(kFixThreads) fixup_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
 {
-    __shared__ uint32_t pre[kMaxBinsPerTile + 1];
-    __shared__ uint32_t wsum[kFixThreads / 32];
     extern __shared__ uint4 fix_dyn[];
     KLayer* lays = reinterpret_cast<KLayer*>(fix_dyn);  // shared copy of the layer table
     for (int e = threadIdx.x; e < g.num_layers * (int)(sizeof(KLayer) / 16); e += kFixThreads)
         fix_dyn[e] = reinterpret_cast<const uint4*>(&g.layer[0])[e];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t* pre = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(fix_dyn) + g.num_layers * sizeof(KLayer)) +
+                    warp * (g.max_bins + 2);
     __syncthreads();
     uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
     const uint64_t* texcl = desc + g.total_tiles;
     const uint32_t T = g.total_tiles;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t nw = gridDim.x * kFixWarps;
 
-    for (uint32_t q = blockIdx.x; q < T; q += gridDim.x) {
+    for (uint32_t q = blockIdx.x * kFixWarps + warp; q < T; q += nw) {
         const uint32_t t = T - 1u - q;
-        TileGeo G;
-        G.layer = layer_from(lays, g.num_layers, t, 0);
-        const KLayer& ly = lays[G.layer];
-        G.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
-        G.bins = (int)min(ly.bins_per_tile, ly.nbins - G.first_bin);
-        G.ts = (int64_t)G.first_bin * ly.bin_len;
-        G.tl = (int)min((int64_t)G.bins * ly.bin_len, ly.n - G.ts);
-        const LayerWs* lw = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(G.layer));
+        const int l = layer_from(lays, g.num_layers, t, 0);
+        const KLayer& ly = lays[l];
+        const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+        const int bins = (int)min(ly.bins_per_tile, ly.nbins - first_bin);
+        const int64_t ts = (int64_t)first_bin * ly.bin_len;
+        const int tl = (int)min((int64_t)bins * ly.bin_len, ly.n - ts);
+        const LayerWs* lw = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l));
         if (lw->result.status == 0u) {
-            // exclusive prefix of this tile's per-bin counts (4 bins per thread)
-            const uint16_t* cnt = reinterpret_cast<const uint16_t*>(ly.msg + 8) + G.first_bin;
-            uint32_t c[4], loc = 0;
+            const uint16_t* cnt = reinterpret_cast<const uint16_t*>(ly.msg + 8) + first_bin;
+            uint32_t run = 0;
+            for (int b0 = 0; b0 < bins; b0 += 32) {
+                const int b = b0 + lane;
+                const uint32_t c = b < bins ? cnt[b] : 0u;
+                uint32_t incl = c;
 #pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int b = tid * 4 + k;
-                c[k] = b < G.bins ? cnt[b] : 0u;
-                loc += c[k];
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(kFull, incl, o);
+                    if (lane >= o) incl += y;
+                }
+                if (b < bins) pre[b] = run + incl - c;
+                run += __shfl_sync(kFull, incl, 31);
             }
-            uint32_t incl = loc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane == 31) wsum[warp] = incl;
-            __syncthreads();
-            uint32_t woff = 0, total = 0;
-            for (int w = 0; w < kFixThreads / 32; ++w) {
-                if (w < warp) woff += wsum[w];
-                total += wsum[w];
-            }
-            uint32_t run = woff + incl - loc;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int b = tid * 4 + k;
-                if (b < G.bins) pre[b] = run;
-                run += c[k];
-            }
-            __syncthreads();
-            const float s = lw->result.s;
-            const uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * texcl[t];
-            float* res = ly.residue + G.ts;
-            for (uint32_t i = tid; i < total; i += kFixThreads) {
-                int lo = 0, hi = G.bins - 1;  // last bin whose prefix is <= i
+            if (lane == 0) pre[bins] = run;
+            __syncwarp();
+            const uint32_t total = run;
+            const uint32_t per = (total + 31) / 32;
+            uint32_t i = min(total, lane * per);
+            const uint32_t iend = min(total, i + per);
+            if (i < iend) {
+                const float s = lw->result.s;
+                const uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * texcl[t];
+                float* res = ly.residue + ts;
+                int lo = 0, hi = bins - 1;  // last bin whose prefix is <= i
                 while (lo < hi) {
                     const int mid = (lo + hi + 1) >> 1;
                     if (pre[mid] <= i) lo = mid;
                     else hi = mid - 1;
                 }
-                const uint32_t code = ly.code_bytes == 1 ? codes[i] : reinterpret_cast<const uint16_t*>(codes)[i];
-                const int64_t off = (int64_t)lo * ly.bin_len + (code >> 1);
-                if (off < G.tl) {  // always true for codes this call produced
-                    float* r = res + off;
-                    *r = (code & 1u) ? __fadd_rn(*r, s) : __fsub_rn(*r, s);
+                int b = lo;
+                uint32_t next = pre[b + 1];
+                while (i < iend) {
+                    int64_t off[kFixBatch];
+                    uint32_t neg = 0;
+                    float v[kFixBatch];
+#pragma unroll
+                    for (int u = 0; u < kFixBatch; ++u) {
+                        off[u] = -1;
+                        if (i + u < iend) {
+                            while (i + u >= next) next = pre[++b + 1];
+                            const uint32_t code = ly.code_bytes == 1 ? codes[i + u]
+                                                                     : reinterpret_cast<const uint16_t*>(codes)[i + u];
+                            const int64_t o = (int64_t)b * ly.bin_len + (code >> 1);
+                            if (o < tl) off[u] = o;  // always true for codes this call produced
+                            neg |= (code & 1u) << u;
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < kFixBatch; ++u)
+                        if (off[u] >= 0) v[u] = res[off[u]];
+#pragma unroll
+                    for (int u = 0; u < kFixBatch; ++u)
+                        if (off[u] >= 0) res[off[u]] = ((neg >> u) & 1u) ? __fadd_rn(v[u], s) : __fsub_rn(v[u], s);
+                    i += kFixBatch;
                 }
             }
         }
-        if (tid == 0) desc[t] = 0ull;
-        __syncthreads();
+        if (lane == 0) desc[t] = 0ull;
+        __syncwarp();  // pre is rewritten for the next tile
     }
 }
 
@@ -1340,7 +1624,8 @@ __global__ void __launch_bounds__(kFixThreads) fixup_kernel(const __grid_constan
 namespace {
 struct DeviceInfo {
     int sms = 0;
-    uint32_t smem_set = 0;  // largest dynamic shared memory opted in so far
+    uint32_t smem_set[4] = {0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per compress kernel
+    uint32_t fix_smem_set = 0;  // same, fix-up kernel
 };
 DeviceInfo g_dev[64];
 }  // namespace
@@ -1358,13 +1643,16 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
         if (e != cudaSuccess) return e;
     }
     const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf);
-    if (P.total > di.smem_set) {
-        e = cudaFuncSetAttribute(compress_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
+    int paths = 0;
+    for (int l = 0; l < g.num_layers; ++l) paths |= g.layer[l].bpw ? 1 : 2;
+    void (*kern)(KGroup, uint8_t*) = paths == 1 ? compress_kernel<1> : paths == 2 ? compress_kernel<2> : compress_kernel<3>;
+    if (P.total > di.smem_set[paths]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
         if (e != cudaSuccess) return e;
-        di.smem_set = P.total;
+        di.smem_set[paths] = P.total;
     }
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, compress_kernel, kCtaThreads, P.total);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kCtaThreads, P.total);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const long long cap = (long long)di.sms * occ;
@@ -1382,16 +1670,27 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
         attr[0].val.cooperative = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        e = cudaLaunchKernelEx(&cfg, compress_kernel, g, static_cast<uint8_t*>(ws));
+        e = cudaLaunchKernelEx(&cfg, kern, g, static_cast<uint8_t*>(ws));
         if (e != cudaSuccess) return e;
     }
     if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
     finalize_kernel<<<g.num_layers, 32, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long long fcap = (long long)di.sms * 8;
-    const uint32_t fgrid = (uint32_t)((long long)g.total_tiles < fcap ? (long long)g.total_tiles : fcap);
-    fixup_kernel<<<fgrid, kFixThreads, g.num_layers * sizeof(KLayer), stream>>>(g, static_cast<uint8_t*>(ws));
+    const uint32_t fsmem = fix_smem_bytes(g.num_layers, g.max_bins);
+    if (fsmem > 48 * 1024 && fsmem > di.fix_smem_set) {
+        e = cudaFuncSetAttribute(fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
+        if (e != cudaSuccess) return e;
+        di.fix_smem_set = fsmem;
+    }
+    int focc = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&focc, fixup_kernel, kFixThreads, fsmem);
+    if (e != cudaSuccess) return e;
+    if (focc < 1) return cudaErrorInvalidConfiguration;
+    const long long fwarps = (long long)di.sms * focc * kFixWarps;
+    const long long fneed = ((long long)g.total_tiles < fwarps ? (long long)g.total_tiles : fwarps);
+    const uint32_t fgrid = (uint32_t)((fneed + kFixWarps - 1) / kFixWarps);
+    fixup_kernel<<<fgrid, kFixThreads, fsmem, stream>>>(g, static_cast<uint8_t*>(ws));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     if (ev_after) e = cudaEventRecord(ev_after, stream);

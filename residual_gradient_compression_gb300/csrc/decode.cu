@@ -124,109 +124,231 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
     if (tid == 0) ws[16 + l * K + k] = bad ? 1 : 0;
 }
 
-// Grid-stride over tiles; dynamic shared memory = dense tile + count prefix.
+// Persistent over tiles (CTA c takes tiles c, c + grid, ...). The dense tiles
+// stream through a ring of kAccStages shared-memory stages: bulk copies (TMA) load a
+// tile kAccStages - 1 tiles ahead, and the finished tile goes back with a bulk
+// store, so loads, stores and the code scatter overlap.
+// A stage holds the tile from the 16-byte boundary at or before its first element;
+// the bulk store covers the tile's 16-byte-aligned interior and the threads store
+// the (at most three) elements at each end, which neighbouring tiles share a
+// 16-byte line with.
+// Inside a tile, warp w owns a contiguous range of the tile's bins for every
+// learner, so the learners' additions to one element all come from one warp in
+// learner order; warps need no barrier between learners. Each warp finds where its
+// codes start (the tile's offset in the message plus the counts of the tile's bins
+// before its range), and each lane takes a contiguous run of those codes, finds the
+// bin of its first code by binary search and walks forward.
+constexpr int kAccStages = 3;
+
+__host__ __device__ inline uint32_t acc_stage_bytes(uint32_t tile_cap) { return ((tile_cap + 8) * 4 + 127) & ~127u; }
+__host__ __device__ inline uint32_t acc_pre_bytes(uint32_t max_bins)
+{
+    return (uint32_t)(kDecThreads / 32) * ((max_bins + 8) / 8 + 2) * 4;
+}
+__host__ __device__ inline uint32_t acc_smem_bytes(uint32_t tile_cap, uint32_t max_bins)
+{
+    return kAccStages * acc_stage_bytes(tile_cap) + ((acc_pre_bytes(max_bins) + 127) & ~127u) + 128;
+}
+
+struct AccTile {
+    int layer;
+    uint32_t first_bin;
+    int bins;
+    int64_t ts, te;  // element range [ts, te) of the layer
+    int64_t a0;      // 16-byte boundary at or before ts: element a0 is at stage[0]
+};
+
+__device__ __forceinline__ AccTile acc_tile(const KGroup& g, uint32_t t)
+{
+    AccTile A;
+    A.layer = find_layer(g, t);
+    const KLayer& ly = g.layer[A.layer];
+    A.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+    A.bins = (int)min(ly.bins_per_tile, ly.nbins - A.first_bin);
+    A.ts = (int64_t)A.first_bin * ly.bin_len;
+    A.te = min(A.ts + (int64_t)A.bins * ly.bin_len, ly.n);
+    A.a0 = A.ts & ~(int64_t)3;
+    return A;
+}
+
+// Thread 0: start tile t's dense slice into a stage. The copy ends at the 16-byte
+// boundary at or after the tile unless that lies past the array, in which case the
+// last few elements are loaded with plain loads.
+__device__ void acc_issue(const KGroup& g, const DecodeParams& p, uint32_t t, float* st, uint64_t* bar)
+{
+    const AccTile A = acc_tile(g, t);
+    const float* dense = p.dense[A.layer];
+    const int64_t n = g.layer[A.layer].n;
+    int64_t a1 = (A.te + 3) & ~(int64_t)3;
+    if (a1 > n) a1 = A.te & ~(int64_t)3;
+    if (a1 < A.te) {
+        for (int64_t j = max(a1, A.ts); j < A.te; ++j) st[j - A.a0] = dense[j];
+        ptx::fence_proxy_async_smem();
+    }
+    const uint32_t bytes = a1 > A.a0 ? (uint32_t)(a1 - A.a0) * 4u : 0u;
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    if (bytes) ptx::bulk_g2s(st, dense + A.a0, bytes, bar);
+}
+
+__device__ __forceinline__ bool acc_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns)
+{
+    uint64_t start = 0;
+    while (!ptx::mbar_try_wait(bar, parity)) {
+        const uint64_t now = ptx::globaltimer();
+        if (start == 0) start = now;
+        else if (now - start > timeout_ns) return false;
+    }
+    return true;
+}
+
+// Warp `warp` adds learner k's codes for bins [b0, b1) of tile A to the staged
+// dense tile sd (element ts + x at sd[x]). `pre` is the warp's scratch of
+// b1 - b0 + 1 entries.
+__device__ __forceinline__ void acc_learner(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
+                                            int b0, int b1, float* sd, uint32_t* pre, uint8_t* bad, int lane)
+{
+    const float s = *reinterpret_cast<const float*>(msg);
+    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + A.first_bin;
+    // codes of the tile's bins before b0
+    uint32_t before = 0;
+    for (int b = lane; b < b0; b += 32) before += cnt[b];
+#pragma unroll
+    for (int o = 16; o; o >>= 1) before += __shfl_xor_sync(kFull, before, o);
+    // exclusive prefix of the warp's bins
+    uint32_t run = 0;
+    for (int c0 = b0; c0 < b1; c0 += 32) {
+        const int b = c0 + lane;
+        const uint32_t c = b < b1 ? cnt[b] : 0u;
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (b < b1) pre[b - b0] = run + incl - c;
+        run += __shfl_sync(kFull, incl, 31);
+    }
+    if (lane == 0) pre[b1 - b0] = run;
+    __syncwarp();
+    const uint32_t total = run;
+    const uint32_t per = (total + 31) / 32;
+    uint32_t i = min(total, lane * per);
+    const uint32_t iend = min(total, i + per);
+    if (i < iend) {
+        const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * (off + before);
+        const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len;
+        int lo = 0, hi = b1 - b0 - 1;  // last bin whose prefix is <= i
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (pre[mid] <= i) lo = mid;
+            else hi = mid - 1;
+        }
+        int b = lo;
+        uint32_t next = pre[b + 1];
+        for (; i < iend; ++i) {
+            while (i >= next) next = pre[++b + 1];
+            const uint32_t code = ly.code_bytes == 1 ? codes[i] : reinterpret_cast<const uint16_t*>(codes)[i];
+            const uint32_t o = code >> 1;
+            const int bin = b0 + b;
+            const int64_t len = (A.first_bin + bin == ly.nbins - 1) ? last_len : ly.bin_len;
+            if ((int64_t)o < len) {
+                float* x = sd + (int64_t)bin * ly.bin_len + o;
+                *x = __fadd_rn(*x, (code & 1u) ? -s : s);
+            } else {
+                *bad = 1;  // offset outside its bin: ignored, message flagged
+            }
+        }
+    }
+    __syncwarp();  // pre is rewritten for the next learner; this learner's additions are done
+}
+
 __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_constant__ KGroup g,
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
-    extern __shared__ __align__(16) uint8_t smem[];
-    float* sd = reinterpret_cast<float*>(smem);
-    uint32_t* pre = reinterpret_cast<uint32_t*>(smem + ((g.tile_cap + 8) * 4 + 15) / 16 * 16);
-    __shared__ uint32_t wsum[kDecThreads / 32];
-    const uint32_t T = g.total_tiles;
-    const int K = p.K;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const uint32_t stage_bytes = acc_stage_bytes(g.tile_cap);
+    float* stage0 = reinterpret_cast<float*>(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int pre_len = (g.max_bins + 8) / 8 + 2;
+    uint32_t* pre = reinterpret_cast<uint32_t*>(smem + kAccStages * stage_bytes) + warp * pre_len;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kAccStages * stage_bytes +
+                                                ((acc_pre_bytes(g.max_bins) + 127) & ~127u));
+    const uint32_t T = g.total_tiles;
+    const uint32_t G0 = blockIdx.x, GS = gridDim.x;
+    const int K = p.K;
+    auto stage = [&](int i) { return stage0 + (size_t)(i % kAccStages) * (stage_bytes / 4); };
 
-    for (uint32_t t = blockIdx.x; t < T; t += gridDim.x) {
-        const int l = find_layer(g, t);
-        const KLayer& ly = g.layer[l];
-        const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
-        const int bins = (int)min(ly.bins_per_tile, ly.nbins - first_bin);
-        const int64_t ts = (int64_t)first_bin * ly.bin_len;
-        const int tl = (int)min((int64_t)bins * ly.bin_len, ly.n - ts);
-        const int64_t te = ts + tl;
-        const int ph = (int)(ts & 3);
+    if (tid == 0) {
+        for (int k = 0; k < kAccStages; ++k) ptx::mbar_init(&bar[k], 1);
+        ptx::fence_mbar_init();
+        for (int i = 0; i < kAccStages - 1; ++i)
+            if (G0 + (uint32_t)i * GS < T) acc_issue(g, p, G0 + (uint32_t)i * GS, stage(i), &bar[i]);
+    }
+    __syncthreads();
+
+    bool poisoned = false;
+    int i = 0;
+    for (;; ++i) {
+        const uint32_t t = G0 + (uint32_t)i * GS;
+        if (t >= T) break;
+        float* st = stage(i);
+        if (!__syncthreads_and(acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u, g.timeout_ns))) {
+            poisoned = true;
+            break;
+        }
+        const AccTile A = acc_tile(g, t);
+        const KLayer& ly = g.layer[A.layer];
+        const int l = A.layer;
+        float* sd = st + (A.ts - A.a0);  // element ts + x at sd[x]
+        const int bpw = (A.bins + kDecThreads / 32 - 1) / (kDecThreads / 32);
+        const int b0 = min(A.bins, warp * bpw), b1 = min(A.bins, b0 + bpw);
+        if (b0 < b1) {
+            for (int k = 0; k < K; ++k) {
+                const uint64_t off = tile_offsets(ws, k, T)[t];
+                if (off == kBadOffset) continue;
+                acc_learner(ly, A, p.msg[l * K + k], off, b0, b1, sd, pre, ws + 16 + l * K + k, lane);
+            }
+        }
+
+        // write back: ends by the threads, the aligned interior by one bulk store
+        const int64_t c0 = (A.ts + 3) & ~(int64_t)3, c1 = A.te & ~(int64_t)3;
         float* dense = p.dense[l];
-        const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len;
-
-        // stage the dense tile: 16-byte vectors over the aligned interior
-        const int64_t c0 = (ts + 3) & ~(int64_t)3, c1 = te & ~(int64_t)3;
-        if (c1 > c0) {
-            const float4* src = reinterpret_cast<const float4*>(dense + c0);
-            float4* dst = reinterpret_cast<float4*>(sd + ph + (c0 - ts));
-            for (int64_t v = tid; v < (c1 - c0) / 4; v += kDecThreads) dst[v] = src[v];
-            for (int64_t j = ts + tid; j < c0; j += kDecThreads) sd[ph + (j - ts)] = dense[j];
-            for (int64_t j = c1 + tid; j < te; j += kDecThreads) sd[ph + (j - ts)] = dense[j];
-        } else {
-            for (int64_t j = ts + tid; j < te; j += kDecThreads) sd[ph + (j - ts)] = dense[j];
-        }
         __syncthreads();
-
-        for (int k = 0; k < K; ++k) {
-            const uint64_t off = tile_offsets(ws, k, T)[t];
-            if (off == kBadOffset) continue;
-            const uint8_t* msg = p.msg[l * K + k];
-            const float s = *reinterpret_cast<const float*>(msg);
-            // exclusive prefix of the tile's counts (4 bins per thread)
-            const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + first_bin;
-            uint32_t c[4], loc = 0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int b = tid * 4 + q;
-                c[q] = b < bins ? cnt[b] : 0u;
-                loc += c[q];
-            }
-            uint32_t incl = loc;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                uint32_t y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
-            }
-            if (lane == 31) wsum[warp] = incl;
-            __syncthreads();
-            uint32_t woff = 0, total = 0;
-            for (int w = 0; w < kDecThreads / 32; ++w) {
-                if (w < warp) woff += wsum[w];
-                total += wsum[w];
-            }
-            uint32_t run = woff + incl - loc;
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                const int b = tid * 4 + q;
-                if (b < bins) pre[b] = run;
-                run += c[q];
-            }
-            __syncthreads();
-            const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * off;
-            for (uint32_t i = tid; i < total; i += kDecThreads) {
-                int lo = 0, hi = bins - 1;
-                while (lo < hi) {
-                    const int mid = (lo + hi + 1) >> 1;
-                    if (pre[mid] <= i) lo = mid;
-                    else hi = mid - 1;
-                }
-                const uint32_t code = ly.code_bytes == 1 ? codes[i] : reinterpret_cast<const uint16_t*>(codes)[i];
-                const uint32_t o = code >> 1;
-                const int64_t len = (first_bin + lo == ly.nbins - 1) ? last_len : ly.bin_len;
-                if ((int64_t)o < len) {
-                    float* x = sd + ph + (int64_t)lo * ly.bin_len + o;
-                    *x = __fadd_rn(*x, (code & 1u) ? -s : s);
-                } else {
-                    ws[16 + l * K + k] = 1;  // offset outside its bin: ignored, message flagged
-                }
-            }
-            __syncthreads();
-        }
-
         if (c1 > c0) {
-            float4* dst = reinterpret_cast<float4*>(dense + c0);
-            const float4* src = reinterpret_cast<const float4*>(sd + ph + (c0 - ts));
-            for (int64_t v = tid; v < (c1 - c0) / 4; v += kDecThreads) dst[v] = src[v];
-            for (int64_t j = ts + tid; j < c0; j += kDecThreads) dense[j] = sd[ph + (j - ts)];
-            for (int64_t j = c1 + tid; j < te; j += kDecThreads) dense[j] = sd[ph + (j - ts)];
+            if (tid < 8) {
+                const int64_t j = tid < 4 ? A.ts + tid : c1 + (tid - 4);
+                if ((tid < 4 && j < c0) || (tid >= 4 && j < A.te)) dense[j] = st[j - A.a0];
+            }
         } else {
-            for (int64_t j = ts + tid; j < te; j += kDecThreads) dense[j] = sd[ph + (j - ts)];
+            for (int64_t j = A.ts + tid; j < A.te; j += kDecThreads) dense[j] = st[j - A.a0];
         }
+        ptx::fence_proxy_async_smem();  // the threads' shared writes, before the bulk store reads them
         __syncthreads();
+        if (tid == 0) {
+            if (c1 > c0) ptx::bulk_s2g(dense + c0, st + (c0 - A.a0), (uint32_t)(c1 - c0) * 4u);
+            ptx::bulk_commit();
+            // refill the stage whose store was committed one tile ago
+            const uint32_t tn = t + (uint32_t)(kAccStages - 1) * GS;
+            if (tn < T) {
+                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                acc_issue(g, p, tn, stage(i + kAccStages - 1), &bar[(i + kAccStages - 1) % kAccStages]);
+            }
+        }
+    }
+    if (tid == 0) ptx::bulk_wait0();
+    if (poisoned) {
+        // a load never completed: flag every message of this CTA's remaining tiles'
+        // layers, then give the loads still in flight one more bounded wait before
+        // the CTA's shared memory is released
+        for (uint32_t t = G0 + (uint32_t)i * GS; t < T; t += GS) {
+            const int l = find_layer(g, t);
+            for (int k = tid; k < K; k += kDecThreads) ws[16 + l * K + k] = 1;
+        }
+        for (int j = 0; j < kAccStages - 1; ++j) {
+            const int ij = i + j;
+            if (G0 + (uint32_t)ij * GS < T)
+                acc_wait(&bar[ij % kAccStages], (uint32_t)(ij / kAccStages) & 1u, g.timeout_ns);
+        }
     }
 }
 
@@ -260,7 +382,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     tile_scan_kernel<<<(unsigned)(g.num_layers * p.K), 1024, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const uint32_t smem = (uint32_t)(((g.tile_cap + 8) * 4 + 15) / 16 * 16 + (g.max_bins + 1) * 4);
+    const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins);
     if (smem > di.smem_set) {
         if (smem > 48 * 1024) {
             e = cudaFuncSetAttribute(accumulate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
