@@ -18,7 +18,10 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRounds = 4;             // lane-vectors per chunk: chunk <= 32*VEC*kRounds elements
 constexpr int kWarpSliceMax = 509;     // warp-sliced tiles: a warp slice plus its alignment slots fits 512 slots
 constexpr int kWarpScratch = 36;       // per-warp g_max / count scratch entries (bins per slice <= 31)
-constexpr uint32_t kHistBytes = kWarps * 256 * 8;                   // per-warp exponent buckets
+constexpr int kBuffers = 3;            // code staging buffers, one look-back warp each
+constexpr int kHistLo = 64;            // per-warp exponent buckets cover biased exponents [64, 192);
+constexpr int kHistN = 128;            // maxima outside go straight to the layer's accumulator
+constexpr uint32_t kHistBytes = kBuffers * kHistN * 8;  // one set per look-back warp
 constexpr uint32_t kWarpScratchBytes = kWarps * 2 * kWarpScratch * 4;
 
 // ---------------------------------------------------------------- descriptors
@@ -55,11 +58,11 @@ struct KGroup {
 };
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:
-// 2 stages x {residue slice, dW slice}, layer table, G buffer, 2 code staging buffers, g_max, counts,
-// per-warp exponent buckets, per-warp bin scratch, per-stage tile geometry, control block (mbarriers,
+// 2 stages x {residue slice, dW slice}, layer table, G buffer, kBuffers code staging buffers, g_max, counts,
+// exponent buckets per look-back warp, per-warp bin scratch, per-stage tile geometry, control block (mbarriers,
 // counters, hand-off slots).
 struct SmemPlan {
-    uint32_t r_bytes, d_bytes, layer_bytes, g_bytes, stg_bytes, bin_bytes, total;
+    uint32_t r_bytes, d_bytes, layer_bytes, g_bytes, stg_bytes, bin_stride, bin_bytes, total;
 };
 __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size, uint32_t max_bins,
                                               uint32_t num_layers, uint32_t needs_gbuf)
@@ -70,10 +73,11 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
     p.r_bytes = ((tile_cap + 32) * 4 + 127) & ~127u;
     p.d_bytes = ((tile_cap + 48) * d_size + 127) & ~127u;
     p.stg_bytes = (tile_cap * 2 + 127) & ~127u;
-    p.bin_bytes = (2 * (max_bins + 1) * 4 + 127) & ~127u;  // two buffers
+    p.bin_stride = max_bins + 1;                                     // entries per buffer
+    p.bin_bytes = (kBuffers * p.bin_stride * 4 + 127) & ~127u;       // all buffers
     p.layer_bytes = num_layers * 64u;                        // copy of the layer table
     p.g_bytes = needs_gbuf ? p.r_bytes : 0u;
-    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + 2 * p.stg_bytes + 2 * p.bin_bytes +
+    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + kBuffers * p.stg_bytes + 2 * p.bin_bytes +
               kHistBytes + kWarpScratchBytes + 2048 + 512;
     return p;
 }
@@ -194,6 +198,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity)
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
         : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Same, but the thread may be suspended (without issuing) for up to hint_ns while
+// the phase is incomplete; it resumes as soon as the phase completes.
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }

@@ -589,7 +589,7 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
     uint64_t excl = 0;
     int64_t j = (int64_t)t - 1;
     uint64_t start = 0;
-    uint32_t sleep_ns = 64;
+    uint32_t sleep_ns = 32;
     bool ok = true;
     for (;;) {
         uint64_t dv[kLbPerLane];
@@ -634,7 +634,7 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
             if (mstar < kLbPerLane) break;
             j -= 32 * kLbPerLane;
             start = 0;
-            sleep_ns = 64;
+            sleep_ns = 32;
             continue;
         }
         uint64_t now = 0;
@@ -643,7 +643,7 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
         if (start == 0) start = now;
         else if (now - start > timeout_ns) { ok = false; break; }
         __nanosleep(sleep_ns);
-        if (sleep_ns < 512) sleep_ns <<= 1;
+        if (sleep_ns < 256) sleep_ns <<= 1;
     }
     if (lane == 0 && publish) ptx::st_relaxed(&desc[t], ok ? (kFlagIncl | (excl + total)) : kFlagErr);
     *excl_out = excl;
@@ -733,10 +733,10 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint6
 // bpw = floor(509 / L_T) whole bins, warp w owning slice w, so bin maxima, counts
 // and code ranks are all warp-local and the compute warps never wait for one
 // another inside a tile. Other bin lengths use block-wide phases (see above).
-// Bin maxima accumulate per warp in exponent buckets and are flushed to the
-// layer's accumulator when the warp moves to another layer; s is formed by the
-// finalise kernel.
-constexpr int kLookbackWarps = 2;  // one per staging buffer
+// Bin maxima are added to exponent buckets by the look-back warps (one set per
+// look-back warp), which flush them to the layer's accumulator when they move to
+// another layer; s is formed by the finalise kernel.
+constexpr int kLookbackWarps = kBuffers;  // one per staging buffer
 constexpr int kCtaThreads = kThreads + 32 * kLookbackWarps;
 constexpr int kBarCompute = 1;
 constexpr uint32_t kEndTile = 0xffffffffu;
@@ -750,15 +750,16 @@ struct Slot {
 // Shared-memory control block of the compress kernel.
 struct Ctrl {
     uint64_t stage_full[2];   // bulk copies of the tile in each stage have landed
-    uint64_t buf_full[2];     // compute warps -> look-back warp of buffer b (count kWarps)
-    uint64_t buf_empty[2];    // look-back warp of buffer b -> compute warps (count 1)
+    uint64_t buf_full[kBuffers];   // compute warps -> look-back warp of buffer b (count kWarps)
+    uint64_t buf_empty[kBuffers];  // look-back warp of buffer b -> compute warps (count 1)
     uint32_t users[2];        // compute warps done reading each stage
     uint32_t issued[2];       // tiles issued into each stage
     int32_t issue_layer;      // layer of the last tile issued
     uint32_t poisoned;        // a wait ran out: later tiles publish errors only
     uint32_t wsum[kWarps];    // block scan scratch
-    Slot slot[2];
+    Slot slot[kBuffers];
 };
+static_assert(sizeof(Ctrl) <= 512, "control block exceeds its shared-memory allowance");
 
 template <int ID, int N>
 __device__ __forceinline__ void bar_sync() { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
@@ -766,11 +767,15 @@ __device__ __forceinline__ void compute_sync() { bar_sync<kBarCompute, kThreads>
 
 // Bounded wait on an mbarrier phase; skipped (reported as failed) once the CTA is
 // poisoned, so that a lost copy or hand-off costs at most one timeout per CTA.
+// Between checks of the time limit the thread sleeps in the barrier (woken when
+// the phase completes) instead of spinning: spinning warps take issue slots from
+// the compute warps.
+constexpr uint32_t kWaitHintNs = 20000;
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, uint64_t timeout_ns, uint32_t* poisoned)
 {
     if (*reinterpret_cast<volatile uint32_t*>(poisoned)) return false;
     uint64_t start = 0;
-    while (!ptx::mbar_try_wait(bar, parity)) {
+    while (!ptx::mbar_try_wait_sleep(bar, parity, kWaitHintNs)) {
         const uint64_t now = ptx::globaltimer();
         if (start == 0) start = now;
         else if (now - start > timeout_ns) {
@@ -847,8 +852,16 @@ __device__ void issue_tile(const KLayer* lays, uint32_t t, int layer, float* sr,
 // Exponent buckets of 32 bin maxima (one per lane, 0 for none): the largest
 // exponent present and the one below it are summed with one warp reduction each
 // (at most 32 x 2^24 < 2^32); any other exponent is summed in a loop. Lane 0 adds
-// each sum to the warp's shared buckets.
-__device__ __forceinline__ void bucket_group(uint32_t u, unsigned long long* hist, int lane)
+// each sum to the warp's shared buckets, or, for an exponent outside their window,
+// to the layer's accumulator gacc.
+__device__ __forceinline__ void bucket_add(unsigned long long* hist, unsigned long long* gacc, uint32_t E,
+                                           uint32_t v)
+{
+    if (E - kHistLo < (uint32_t)kHistN) hist[E - kHistLo] += (unsigned long long)v;
+    else atomicAdd(&gacc[E], (unsigned long long)v);
+}
+
+__device__ __forceinline__ void bucket_group(uint32_t u, unsigned long long* hist, unsigned long long* gacc, int lane)
 {
     if (__ballot_sync(kFull, u != 0u) == 0u) return;
     const uint32_t E = u >> 23;
@@ -857,15 +870,15 @@ __device__ __forceinline__ void bucket_group(uint32_t u, unsigned long long* his
     const uint32_t s_hi = __reduce_add_sync(kFull, (u && E == Eh) ? M : 0u);
     const uint32_t s_lo = __reduce_add_sync(kFull, (u && Eh > 0 && E == Eh - 1) ? M : 0u);
     if (lane == 0) {
-        if (s_hi) hist[Eh] += (unsigned long long)s_hi;
-        if (s_lo) hist[Eh - 1] += (unsigned long long)s_lo;
+        if (s_hi) bucket_add(hist, gacc, Eh, s_hi);
+        if (s_lo) bucket_add(hist, gacc, Eh - 1, s_lo);
     }
     uint32_t left = __ballot_sync(kFull, u != 0u && E + 1 < Eh);
     while (left) {
         const uint32_t Ek = __shfl_sync(kFull, E, __ffs(left) - 1);
         const bool mine = ((left >> lane) & 1u) && E == Ek;
         const uint32_t sum = __reduce_add_sync(kFull, mine ? M : 0u);
-        if (lane == 0) hist[Ek] += (unsigned long long)sum;
+        if (lane == 0) bucket_add(hist, gacc, Ek, sum);
         left &= ~__ballot_sync(kFull, mine);
     }
     __syncwarp();
@@ -875,26 +888,28 @@ __device__ __forceinline__ void bucket_group(uint32_t u, unsigned long long* his
 __device__ __forceinline__ void flush_buckets(unsigned long long* hist, LayerWs* lw, int lane)
 {
     __syncwarp();
-    for (int e = lane; e < 256; e += 32) {
+    for (int e = lane; e < kHistN; e += 32) {
         const unsigned long long v = hist[e];
         if (v) {
-            atomicAdd(&lw->acc[e], v);
+            atomicAdd(&lw->acc[kHistLo + e], v);
             hist[e] = 0ull;
         }
     }
     __syncwarp();
 }
 
-// Look-back warp that owns staging buffer b, i.e. every other tile of the CTA.
+// Look-back warp that owns staging buffer b, i.e. every kBuffers-th tile of the CTA.
 // For each such tile, in order: it sums the code runs, publishes the tile's
 // AGGREGATE (INCLUSIVE for a layer's first tile), writes the per-bin counts into
-// the message and clears the bin arrays; then it resolves the tile's prefix with
-// the look-back and copies the staged codes into the message.
+// the message, adds the bin maxima to its exponent buckets and clears the bin
+// arrays; then it resolves the tile's prefix with the look-back and copies the
+// staged codes into the message.
 struct LookbackCtx {
     uint16_t* stg;
     uint32_t* gmax;
     uint32_t* cnt;
     uint32_t bin_len;  // entries of gmax / cnt to clear
+    unsigned long long* hist;  // this warp's exponent buckets
 };
 
 __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, Ctrl* ctl, const LookbackCtx& C,
@@ -902,6 +917,7 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
 {
     uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
     uint64_t* texcl = desc + g.total_tiles;
+    int hist_layer = -1;
     for (uint32_t j = 0;; ++j) {
         const bool got = wait_phase(&ctl->buf_full[b], j & 1u, g.timeout_ns, &ctl->poisoned);
         const Slot& sl = ctl->slot[b];
@@ -914,7 +930,8 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
             if (!got) {
                 const uint32_t T = g.total_tiles;
                 int l = 0;
-                for (uint32_t u = (uint32_t)blockIdx.x + (2 * j + b) * gridDim.x; u < T; u += 2 * gridDim.x) {
+                for (uint32_t u = (uint32_t)blockIdx.x + (kBuffers * j + b) * gridDim.x; u < T;
+                     u += kBuffers * gridDim.x) {
                     l = layer_from(lays, g.num_layers, u, l);
                     if (lane == 0) {
                         ptx::st_relaxed(&desc[u], kFlagErr);
@@ -951,6 +968,14 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
             ptx::st_relaxed(&desc[t], (t == ly.tile_begin ? kFlagIncl : kFlagAgg) | total);
         uint16_t* cdst = reinterpret_cast<uint16_t*>(ly.msg + 8) + sl.first_bin;
         for (int bb = lane; bb < bins; bb += 32) cdst[bb] = (uint16_t)C.cnt[bb];
+        // the tile's bin maxima into the exponent buckets (flushed when the layer changes)
+        LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l));
+        if (l != hist_layer) {
+            if (hist_layer >= 0)
+                flush_buckets(C.hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+            hist_layer = l;
+        }
+        for (int b0 = 0; b0 < bins; b0 += 32) bucket_group(b0 + lane < bins ? C.gmax[b0 + lane] : 0u, C.hist, lw->acc, lane);
         __syncwarp();
         for (uint32_t bb = lane; bb < C.bin_len; bb += 32) { C.gmax[bb] = 0u; C.cnt[bb] = 0u; }
         uint64_t excl = 0;
@@ -976,6 +1001,7 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive(&ctl->buf_empty[b]);
     }
+    if (hist_layer >= 0) flush_buckets(C.hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
 }
 
 // Warp-sliced tile: warp `warp` owns bins [wb0, wb1) of the tile, at most 509
@@ -983,14 +1009,14 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
 // 16-byte boundary at or before its first element). Per lane: G = residue + dW,
 // residue := G in global memory, and |H| = |fl32(G + dW)| with the masks of G != 0
 // and G < 0 kept in registers; `release` then gives the stage back. Bin maxima and
-// counts go through the warp's scratch (wg, wc: zero on entry and on return), the
-// counts into the tile's count array, the maxima into the warp's exponent buckets,
-// and the codes, ranked with a warp scan, to stg[we0 + rank], we0 being the warp's
-// first tile element. Returns the warp's code count; *src gets we0.
+// counts go through the warp's scratch (wg, wc: zero on entry and on return) into
+// the tile's maximum and count arrays, and the codes, ranked with a warp scan, to
+// stg[we0 + rank], we0 being the warp's first tile element. Returns the warp's
+// code count; *src gets we0.
 template <bool BF16, class Release>
 __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G, int pr, int pd, const float* sr,
                                               const void* sd, uint32_t* wg, uint32_t* wc, uint32_t* cnt_tile,
-                                              uint16_t* stg, unsigned long long* hist, int warp, int lane,
+                                              uint16_t* stg, uint32_t* gmax_tile, int warp, int lane,
                                               uint32_t* src, Release&& release)
 {
     const int L = ly.bin_len;
@@ -1094,11 +1120,12 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
     {
         // per bin of the slice: count to the tile's array, maximum to the buckets; scratch back to zero
         const int nb = wb1 - wb0;
-        const uint32_t u = lane < nb ? wg[lane] : 0u;
-        if (lane < nb) cnt_tile[wb0 + lane] = wc[lane];
+        if (lane < nb) {
+            cnt_tile[wb0 + lane] = wc[lane];
+            gmax_tile[wb0 + lane] = wg[lane];
+        }
         wg[lane] = 0u;
         wc[lane] = 0u;
-        bucket_group(u, hist, lane);
     }
     const uint32_t c = __popc(f);
     uint32_t incl = c;
@@ -1108,12 +1135,14 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
         if (lane >= o) incl += y;
     }
     const uint32_t total = __shfl_sync(kFull, incl, 31);
-    uint32_t pos = (uint32_t)we0 + incl - c;
+    // code of slot idx: ((slot's offset in its bin) << 1) | sign, i.e. base + 2 idx | sign
+    const uint32_t base_lo = (uint32_t)((e_first - we0) - bin_lo * L) << 1;
+    const uint32_t base_hi = base_lo - 2u * (uint32_t)L;
+    uint16_t* sp = stg + we0 + incl - c;
     while (f) {
         const int idx = __ffs(f) - 1;
         f &= f - 1;
-        const int off = (e_first + idx - we0) - bin_lo * L - (idx < split ? 0 : L);
-        stg[pos++] = (uint16_t)(((uint32_t)off << 1) | ((ng >> idx) & 1u));
+        *sp++ = (uint16_t)((idx < split ? base_lo : base_hi) + 2u * idx + ((ng >> idx) & 1u));
     }
     *src = (uint32_t)we0;
     return total;
@@ -1240,7 +1269,7 @@ __device__ __forceinline__ uint32_t tile_in_registers(const Tile& T, uint32_t* g
 template <class Release>
 __device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int pr, int pd, float* sr_s, void* sd_s,
                                         float* gbuf, uint32_t* gmax_c, uint32_t* cnt_c, uint16_t* stg, Slot& sl,
-                                        uint32_t* wsum, unsigned long long* hist, int tid, Release* release_p)
+                                        uint32_t* wsum, int tid, Release* release_p)
 {
     Release& release = *release_p;
     const int lane = tid & 31, warp = tid >> 5;
@@ -1303,9 +1332,6 @@ __device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int p
         compute_sync();  // phase C was the last reader of the stage
         release();
     }
-    compute_sync();  // every warp's bin maxima are in gmax_c
-    for (int b0 = 32 * warp; b0 < G.bins; b0 += 32 * kWarps)
-        bucket_group(b0 + lane < G.bins ? gmax_c[b0 + lane] : 0u, hist, lane);
 }
 
 // kPaths: 1 = every layer of the launch is warp-sliced, 2 = none is, 3 = mixed.
@@ -1324,12 +1350,12 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
     uint8_t* p = smem + 2 * stage_bytes;
     KLayer* lays = reinterpret_cast<KLayer*>(p); p += P.layer_bytes;
     float* gbuf = reinterpret_cast<float*>(p); p += P.g_bytes;  // G, for tiles processed through shared memory
-    uint16_t* stg0 = reinterpret_cast<uint16_t*>(p); p += 2 * P.stg_bytes;
+    uint16_t* stg0 = reinterpret_cast<uint16_t*>(p); p += kBuffers * P.stg_bytes;
     const uint32_t stg_stride = P.stg_bytes / 2;
-    uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;  // 2 buffers of bin_stride
-    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;   // 2 buffers of bin_stride
-    const uint32_t bin_stride = P.bin_bytes / 8;
-    unsigned long long* hist0 = reinterpret_cast<unsigned long long*>(p); p += kHistBytes;  // [warp][256] buckets
+    uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;  // kBuffers buffers of bin_stride
+    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;   // kBuffers buffers of bin_stride
+    const uint32_t bin_stride = P.bin_stride;
+    unsigned long long* hist0 = reinterpret_cast<unsigned long long*>(p); p += kHistBytes;  // [buffer][kHistN] buckets
     uint32_t* wscr0 = reinterpret_cast<uint32_t*>(p); p += kWarpScratchBytes;  // [warp][2][kWarpScratch]
     TileGeo* info = reinterpret_cast<TileGeo*>(p); p += 2048;  // [2]: geometry of the tile in each stage
     Ctrl* ctl = reinterpret_cast<Ctrl*>(p);
@@ -1346,13 +1372,13 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
         for (int e = tid; e < g.num_layers * (int)(sizeof(KLayer) / 16); e += kCtaThreads) dst[e] = src[e];
     }
     __syncthreads();
-    for (uint32_t e = tid; e < 2 * bin_stride; e += kCtaThreads) { gmax_s[e] = 0u; cnt_s[e] = 0u; }
+    for (uint32_t e = tid; e < kBuffers * bin_stride; e += kCtaThreads) { gmax_s[e] = 0u; cnt_s[e] = 0u; }
     if (tid == 0) {
         ctl->users[0] = ctl->users[1] = 0u;
         ctl->issued[0] = ctl->issued[1] = 0u;
         ctl->poisoned = 0u;
-        for (int k = 0; k < 2; ++k) {
-            ptx::mbar_init(&ctl->stage_full[k], 1);
+        for (int k = 0; k < 2; ++k) ptx::mbar_init(&ctl->stage_full[k], 1);
+        for (int k = 0; k < kBuffers; ++k) {
             ptx::mbar_init(&ctl->buf_full[k], kWarps);
             ptx::mbar_init(&ctl->buf_empty[k], 1);
         }
@@ -1378,49 +1404,47 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
         C.gmax = gmax_s + b * bin_stride;
         C.cnt = cnt_s + b * bin_stride;
         C.bin_len = bin_stride;
+        C.hist = hist0 + b * kHistN;
         lookback_warp(g, lays, ws, ctl, C, b, lane);
     } else {
-        unsigned long long* hist = hist0 + warp * 256;
         uint32_t* wg = wscr0 + warp * 2 * kWarpScratch;
         uint32_t* wc = wg + kWarpScratch;
-        int hist_layer = -1;
         for (;; ++it) {
             const uint32_t t = G0 + it * GS;
             if (t >= T) break;
-            const int s = it & 1;  // stage, staging buffer and bin-array buffer
+            const int s = it & 1;                         // stage
+            const int bf = (int)(it % (uint32_t)kBuffers);  // staging buffer and bin arrays
             // Bounded waits. A copy or hand-off that never completes poisons the CTA:
             // no further copies are issued, and the look-back warps publish only
             // errors from then on; the compute warps still run every tile (from
             // whatever the buffers hold: every index stays inside its buffer) so
             // that the hand-off protocol ends normally.
             wait_phase(&ctl->stage_full[s], (it >> 1) & 1u, g.timeout_ns, &ctl->poisoned);
-            // the look-back warp of this parity has finished tile it-2: the staging
-            // buffer and bin arrays of parity s are free and cleared
-            if (it >= 2) wait_phase(&ctl->buf_empty[s], ((it >> 1) & 1u) ^ 1u, g.timeout_ns, &ctl->poisoned);
+            // the look-back warp of buffer bf has finished tile it - kBuffers: the
+            // staging buffer and bin arrays bf are free and cleared
+            if (it >= (uint32_t)kBuffers)
+                wait_phase(&ctl->buf_empty[bf], (it / kBuffers - 1u) & 1u, g.timeout_ns, &ctl->poisoned);
             __syncwarp();
             const TileGeo G = info[s];
             const KLayer& ly = lays[G.layer];
-            if (G.layer != hist_layer) {  // new layer: hand the buckets to the previous one
-                if (hist_layer >= 0)
-                    flush_buckets(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
-                hist_layer = G.layer;
-            }
-            uint32_t* gmax_c = gmax_s + s * bin_stride;
-            uint32_t* cnt_c = cnt_s + s * bin_stride;
+            uint32_t* gmax_c = gmax_s + bf * bin_stride;
+            uint32_t* cnt_c = cnt_s + bf * bin_stride;
             const int pr = (int)(G.ts & 3), pd = ly.dw_bf16 ? (int)(G.ts & 7) : pr;
             const int64_t te = G.ts + G.tl;
-            uint16_t* stg = stg0 + s * stg_stride;
-            Slot& sl = ctl->slot[s];
+            uint16_t* stg = stg0 + bf * stg_stride;
+            Slot& sl = ctl->slot[bf];
             const uint32_t t_next = t + 2 * GS;
             // every compute warp calls this once per tile when it no longer reads the
-            // stage; the last one starts the CTA's tile after next into it
+            // stage; the last one starts the CTA's tile after next into it. No fence is
+            // needed (and one would wait for this warp's global stores): the warp's
+            // reads of the stage have returned their values, and one warp's shared
+            // memory accesses are performed in order, so they precede its count.
             auto release = [&]() {
                 if (lane == 0) {
-                    __threadfence_block();
+                    asm volatile("" ::: "memory");
                     const uint32_t prev = atomicAdd(&ctl->users[s], 1u);
                     if (prev == kWarps - 1) {
                         ctl->users[s] = 0u;
-                        __threadfence_block();
                         if (t_next < T && !*reinterpret_cast<volatile uint32_t*>(&ctl->poisoned)) {
                             const int il = layer_from(lays, g.num_layers, t_next, ctl->issue_layer);
                             ctl->issue_layer = il;
@@ -1441,11 +1465,11 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
                 // warp-sliced tile: no barrier among the compute warps
                 uint32_t src = 0, cnt;
                 if (ly.dw_bf16)
-                    cnt = warp_tile<true>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, hist, warp, lane, &src,
-                                          release);
+                    cnt = warp_tile<true>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, gmax_c, warp, lane,
+                                          &src, release);
                 else
-                    cnt = warp_tile<false>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, hist, warp, lane, &src,
-                                           release);
+                    cnt = warp_tile<false>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, gmax_c, warp, lane,
+                                           &src, release);
                 if (lane == 0) {
                     sl.src[warp] = src;
                     sl.cnt[warp] = cnt;
@@ -1454,7 +1478,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
                 }
             } else {
                 if constexpr ((kPaths & 2) != 0)
-                    block_tile(ly, G, pr, pd, stage_r(s), stage_d(s), gbuf, gmax_c, cnt_c, stg, sl, ctl->wsum, hist, tid,
+                    block_tile(ly, G, pr, pd, stage_r(s), stage_d(s), gbuf, gmax_c, cnt_c, stg, sl, ctl->wsum, tid,
                                &release);
             }
             if (tid == 0) {
@@ -1464,15 +1488,14 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
                 sl.bins = (uint32_t)G.bins;
             }
             __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&ctl->buf_full[s]);
+            if (lane == 0) ptx::mbar_arrive(&ctl->buf_full[bf]);
         }
-        if (hist_layer >= 0) flush_buckets(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
         // hand each look-back warp the end marker once it has released its buffer:
-        // buffer b carried the tiles it' < it with it' % 2 == b. Every warp waits for
-        // that release before it arrives: an arrival is not tied to a phase, so one
-        // made early would count towards the last tile's hand-off.
-        for (int b = 0; b < 2; ++b) {
-            const uint32_t uses = (it + 1 - b) / 2;  // tiles handed over on buffer b
+        // buffer b carried the tiles it' < it with it' % kBuffers == b. Every warp
+        // waits for that release before it arrives: an arrival is not tied to a
+        // phase, so one made early would count towards the last tile's hand-off.
+        for (int b = 0; b < kBuffers; ++b) {
+            const uint32_t uses = it > (uint32_t)b ? (it - b + kBuffers - 1) / kBuffers : 0u;  // tiles on buffer b
             if (lane == 0) {
                 if (uses >= 1) wait_phase(&ctl->buf_empty[b], (uses - 1) & 1u, g.timeout_ns, &ctl->poisoned);
                 if (warp == 0) ctl->slot[b].t = kEndTile;

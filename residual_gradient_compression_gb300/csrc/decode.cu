@@ -193,7 +193,7 @@ __device__ void acc_issue(const KGroup& g, const DecodeParams& p, uint32_t t, fl
 __device__ __forceinline__ bool acc_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns)
 {
     uint64_t start = 0;
-    while (!ptx::mbar_try_wait(bar, parity)) {
+    while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
         const uint64_t now = ptx::globaltimer();
         if (start == 0) start = now;
         else if (now - start > timeout_ns) return false;
