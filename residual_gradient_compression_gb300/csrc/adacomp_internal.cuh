@@ -18,10 +18,11 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRounds = 4;             // lane-vectors per chunk: chunk <= 32*VEC*kRounds elements
 constexpr int kWarpSliceMax = 509;     // warp-sliced tiles: a warp slice plus its alignment slots fits 512 slots
 constexpr int kWarpScratch = 36;       // per-warp g_max / count scratch entries (bins per slice <= 31)
-constexpr int kBuffers = 3;            // code staging buffers, one look-back warp each
+constexpr int kMaxBuffers = 4;         // code staging buffers (one look-back warp each): 4, or 3 where
+                                       // tiles are long (block-wide tiles of up to 8192 elements)
 constexpr int kHistLo = 64;            // per-warp exponent buckets cover biased exponents [64, 192);
 constexpr int kHistN = 128;            // maxima outside go straight to the layer's accumulator
-constexpr uint32_t kHistBytes = kBuffers * kHistN * 8;  // one set per look-back warp
+constexpr uint32_t kHistBytesPerBuffer = kHistN * 8;  // one set per look-back warp
 constexpr uint32_t kWarpScratchBytes = kWarps * 2 * kWarpScratch * 4;
 
 // ---------------------------------------------------------------- descriptors
@@ -58,14 +59,14 @@ struct KGroup {
 };
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:
-// 2 stages x {residue slice, dW slice}, layer table, G buffer, kBuffers code staging buffers, g_max, counts,
+// 2 stages x {residue slice, dW slice}, layer table, G buffer, nbuf code staging buffers, g_max, counts,
 // exponent buckets per look-back warp, per-warp bin scratch, per-stage tile geometry, control block (mbarriers,
 // counters, hand-off slots).
 struct SmemPlan {
     uint32_t r_bytes, d_bytes, layer_bytes, g_bytes, stg_bytes, bin_stride, bin_bytes, total;
 };
 __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size, uint32_t max_bins,
-                                              uint32_t num_layers, uint32_t needs_gbuf)
+                                              uint32_t num_layers, uint32_t needs_gbuf, uint32_t nbuf)
 {
     SmemPlan p;
     // slack past the tile: the phase slots (< 4 fp32, < 8 bf16) plus segments that
@@ -74,11 +75,11 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
     p.d_bytes = ((tile_cap + 48) * d_size + 127) & ~127u;
     p.stg_bytes = (tile_cap * 2 + 127) & ~127u;
     p.bin_stride = max_bins + 1;                                     // entries per buffer
-    p.bin_bytes = (kBuffers * p.bin_stride * 4 + 127) & ~127u;       // all buffers
+    p.bin_bytes = (nbuf * p.bin_stride * 4 + 127) & ~127u;           // all buffers
     p.layer_bytes = num_layers * 64u;                        // copy of the layer table
     p.g_bytes = needs_gbuf ? p.r_bytes : 0u;
-    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + kBuffers * p.stg_bytes + 2 * p.bin_bytes +
-              kHistBytes + kWarpScratchBytes + 2048 + 512;
+    p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + nbuf * p.stg_bytes + 2 * p.bin_bytes +
+              nbuf * kHistBytesPerBuffer + kWarpScratchBytes + 2048 + 640;
     return p;
 }
 

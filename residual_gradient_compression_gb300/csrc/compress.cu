@@ -736,8 +736,8 @@ __device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint6
 // Bin maxima are added to exponent buckets by the look-back warps (one set per
 // look-back warp), which flush them to the layer's accumulator when they move to
 // another layer; s is formed by the finalise kernel.
-constexpr int kLookbackWarps = kBuffers;  // one per staging buffer
-constexpr int kCtaThreads = kThreads + 32 * kLookbackWarps;
+// Threads of a compress CTA with nb staging buffers (one look-back warp each).
+__host__ __device__ constexpr int cta_threads(int nb) { return kThreads + 32 * nb; }
 constexpr int kBarCompute = 1;
 constexpr uint32_t kEndTile = 0xffffffffu;
 
@@ -750,16 +750,16 @@ struct Slot {
 // Shared-memory control block of the compress kernel.
 struct Ctrl {
     uint64_t stage_full[2];   // bulk copies of the tile in each stage have landed
-    uint64_t buf_full[kBuffers];   // compute warps -> look-back warp of buffer b (count kWarps)
-    uint64_t buf_empty[kBuffers];  // look-back warp of buffer b -> compute warps (count 1)
+    uint64_t buf_full[kMaxBuffers];   // compute warps -> look-back warp of buffer b (count kWarps)
+    uint64_t buf_empty[kMaxBuffers];  // look-back warp of buffer b -> compute warps (count 1)
     uint32_t users[2];        // compute warps done reading each stage
     uint32_t issued[2];       // tiles issued into each stage
     int32_t issue_layer;      // layer of the last tile issued
     uint32_t poisoned;        // a wait ran out: later tiles publish errors only
     uint32_t wsum[kWarps];    // block scan scratch
-    Slot slot[kBuffers];
+    Slot slot[kMaxBuffers];
 };
-static_assert(sizeof(Ctrl) <= 512, "control block exceeds its shared-memory allowance");
+static_assert(sizeof(Ctrl) <= 640, "control block exceeds its shared-memory allowance");
 
 template <int ID, int N>
 __device__ __forceinline__ void bar_sync() { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
@@ -898,7 +898,7 @@ __device__ __forceinline__ void flush_buckets(unsigned long long* hist, LayerWs*
     __syncwarp();
 }
 
-// Look-back warp that owns staging buffer b, i.e. every kBuffers-th tile of the CTA.
+// Look-back warp that owns staging buffer b of nb, i.e. every nb-th tile of the CTA.
 // For each such tile, in order: it sums the code runs, publishes the tile's
 // AGGREGATE (INCLUSIVE for a layer's first tile), writes the per-bin counts into
 // the message, adds the bin maxima to its exponent buckets and clears the bin
@@ -913,7 +913,7 @@ struct LookbackCtx {
 };
 
 __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, Ctrl* ctl, const LookbackCtx& C,
-                              int b, int lane)
+                              int b, int nb, int lane)
 {
     uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
     uint64_t* texcl = desc + g.total_tiles;
@@ -930,8 +930,7 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
             if (!got) {
                 const uint32_t T = g.total_tiles;
                 int l = 0;
-                for (uint32_t u = (uint32_t)blockIdx.x + (kBuffers * j + b) * gridDim.x; u < T;
-                     u += kBuffers * gridDim.x) {
+                for (uint32_t u = (uint32_t)blockIdx.x + (nb * j + b) * gridDim.x; u < T; u += nb * gridDim.x) {
                     l = layer_from(lays, g.num_layers, u, l);
                     if (lane == 0) {
                         ptx::st_relaxed(&desc[u], kFlagErr);
@@ -1337,12 +1336,13 @@ __device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int p
 // kPaths: 1 = every layer of the launch is warp-sliced, 2 = none is, 3 = mixed.
 // The single-path instantiations keep the warp-sliced path's registers free of
 // the block-wide path's needs.
-template <int kPaths>
-__global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_constant__ KGroup g,
+template <int kPaths, int kNB>
+__global__ void __launch_bounds__(cta_threads(kNB), 2) compress_kernel(const __grid_constant__ KGroup g,
                                                                   uint8_t* __restrict__ ws)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf);
+    constexpr int kCtaThreads = cta_threads(kNB);
+    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf, kNB);
     // stage s: residue slice at smem + s * stage_bytes, dW slice r_bytes after it
     const uint32_t stage_bytes = P.r_bytes + P.d_bytes;
     auto stage_r = [&](int s) { return reinterpret_cast<float*>(smem + s * stage_bytes); };
@@ -1350,12 +1350,12 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
     uint8_t* p = smem + 2 * stage_bytes;
     KLayer* lays = reinterpret_cast<KLayer*>(p); p += P.layer_bytes;
     float* gbuf = reinterpret_cast<float*>(p); p += P.g_bytes;  // G, for tiles processed through shared memory
-    uint16_t* stg0 = reinterpret_cast<uint16_t*>(p); p += kBuffers * P.stg_bytes;
+    uint16_t* stg0 = reinterpret_cast<uint16_t*>(p); p += kNB * P.stg_bytes;
     const uint32_t stg_stride = P.stg_bytes / 2;
-    uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;  // kBuffers buffers of bin_stride
-    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;   // kBuffers buffers of bin_stride
+    uint32_t* gmax_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;  // kNB buffers of bin_stride
+    uint32_t* cnt_s = reinterpret_cast<uint32_t*>(p); p += P.bin_bytes;   // kNB buffers of bin_stride
     const uint32_t bin_stride = P.bin_stride;
-    unsigned long long* hist0 = reinterpret_cast<unsigned long long*>(p); p += kHistBytes;  // [buffer][kHistN] buckets
+    unsigned long long* hist0 = reinterpret_cast<unsigned long long*>(p); p += kNB * kHistBytesPerBuffer;  // [buffer][kHistN] buckets
     uint32_t* wscr0 = reinterpret_cast<uint32_t*>(p); p += kWarpScratchBytes;  // [warp][2][kWarpScratch]
     TileGeo* info = reinterpret_cast<TileGeo*>(p); p += 2048;  // [2]: geometry of the tile in each stage
     Ctrl* ctl = reinterpret_cast<Ctrl*>(p);
@@ -1364,7 +1364,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
     const uint32_t G0 = blockIdx.x, GS = gridDim.x;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
-    for (int e = tid; e < kHistBytes / 8; e += kCtaThreads) hist0[e] = 0ull;
+    for (int e = tid; e < kNB * kHistN; e += kCtaThreads) hist0[e] = 0ull;
     for (int e = tid; e < kWarpScratchBytes / 4; e += kCtaThreads) wscr0[e] = 0u;
     {
         const uint4* src = reinterpret_cast<const uint4*>(&g.layer[0]);
@@ -1372,13 +1372,13 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
         for (int e = tid; e < g.num_layers * (int)(sizeof(KLayer) / 16); e += kCtaThreads) dst[e] = src[e];
     }
     __syncthreads();
-    for (uint32_t e = tid; e < kBuffers * bin_stride; e += kCtaThreads) { gmax_s[e] = 0u; cnt_s[e] = 0u; }
+    for (uint32_t e = tid; e < kNB * bin_stride; e += kCtaThreads) { gmax_s[e] = 0u; cnt_s[e] = 0u; }
     if (tid == 0) {
         ctl->users[0] = ctl->users[1] = 0u;
         ctl->issued[0] = ctl->issued[1] = 0u;
         ctl->poisoned = 0u;
         for (int k = 0; k < 2; ++k) ptx::mbar_init(&ctl->stage_full[k], 1);
-        for (int k = 0; k < kBuffers; ++k) {
+        for (int k = 0; k < kNB; ++k) {
             ptx::mbar_init(&ctl->buf_full[k], kWarps);
             ptx::mbar_init(&ctl->buf_empty[k], 1);
         }
@@ -1405,7 +1405,7 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
         C.cnt = cnt_s + b * bin_stride;
         C.bin_len = bin_stride;
         C.hist = hist0 + b * kHistN;
-        lookback_warp(g, lays, ws, ctl, C, b, lane);
+        lookback_warp(g, lays, ws, ctl, C, b, kNB, lane);
     } else {
         uint32_t* wg = wscr0 + warp * 2 * kWarpScratch;
         uint32_t* wc = wg + kWarpScratch;
@@ -1413,17 +1413,16 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
             const uint32_t t = G0 + it * GS;
             if (t >= T) break;
             const int s = it & 1;                         // stage
-            const int bf = (int)(it % (uint32_t)kBuffers);  // staging buffer and bin arrays
+            const int bf = (int)(it % (uint32_t)kNB);  // staging buffer and bin arrays
             // Bounded waits. A copy or hand-off that never completes poisons the CTA:
             // no further copies are issued, and the look-back warps publish only
             // errors from then on; the compute warps still run every tile (from
             // whatever the buffers hold: every index stays inside its buffer) so
             // that the hand-off protocol ends normally.
             wait_phase(&ctl->stage_full[s], (it >> 1) & 1u, g.timeout_ns, &ctl->poisoned);
-            // the look-back warp of buffer bf has finished tile it - kBuffers: the
+            // the look-back warp of buffer bf has finished tile it - kNB: the
             // staging buffer and bin arrays bf are free and cleared
-            if (it >= (uint32_t)kBuffers)
-                wait_phase(&ctl->buf_empty[bf], (it / kBuffers - 1u) & 1u, g.timeout_ns, &ctl->poisoned);
+            if (it >= (uint32_t)kNB) wait_phase(&ctl->buf_empty[bf], (it / kNB - 1u) & 1u, g.timeout_ns, &ctl->poisoned);
             __syncwarp();
             const TileGeo G = info[s];
             const KLayer& ly = lays[G.layer];
@@ -1491,11 +1490,11 @@ __global__ void __launch_bounds__(kCtaThreads, 2) compress_kernel(const __grid_c
             if (lane == 0) ptx::mbar_arrive(&ctl->buf_full[bf]);
         }
         // hand each look-back warp the end marker once it has released its buffer:
-        // buffer b carried the tiles it' < it with it' % kBuffers == b. Every warp
+        // buffer b carried the tiles it' < it with it' % kNB == b. Every warp
         // waits for that release before it arrives: an arrival is not tied to a
         // phase, so one made early would count towards the last tile's hand-off.
-        for (int b = 0; b < kBuffers; ++b) {
-            const uint32_t uses = it > (uint32_t)b ? (it - b + kBuffers - 1) / kBuffers : 0u;  // tiles on buffer b
+        for (int b = 0; b < kNB; ++b) {
+            const uint32_t uses = it > (uint32_t)b ? (it - b + kNB - 1) / kNB : 0u;  // tiles on buffer b
             if (lane == 0) {
                 if (uses >= 1) wait_phase(&ctl->buf_empty[b], (uses - 1) & 1u, g.timeout_ns, &ctl->poisoned);
                 if (warp == 0) ctl->slot[b].t = kEndTile;
@@ -1665,17 +1664,21 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
         e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf);
     int paths = 0;
     for (int l = 0; l < g.num_layers; ++l) paths |= g.layer[l].bpw ? 1 : 2;
-    void (*kern)(KGroup, uint8_t*) = paths == 1 ? compress_kernel<1> : paths == 2 ? compress_kernel<2> : compress_kernel<3>;
+    // four staging buffers where every layer is warp-sliced (short tiles), else three
+    const int nb = paths == 1 ? 4 : 3;
+    const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf, nb);
+    void (*kern)(KGroup, uint8_t*) = paths == 1 ? compress_kernel<1, 4>
+                                   : paths == 2 ? compress_kernel<2, 3> : compress_kernel<3, 3>;
+    const int threads = cta_threads(nb);
     if (P.total > di.smem_set[paths]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
         if (e != cudaSuccess) return e;
         di.smem_set[paths] = P.total;
     }
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kCtaThreads, P.total);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, P.total);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const long long cap = (long long)di.sms * occ;
@@ -1685,7 +1688,7 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
         // all CTAs must be resident together: the look-back waits on other CTAs' tiles
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(grid);
-        cfg.blockDim = dim3(kCtaThreads);
+        cfg.blockDim = dim3(threads);
         cfg.dynamicSmemBytes = P.total;
         cfg.stream = stream;
         cudaLaunchAttribute attr[1];
