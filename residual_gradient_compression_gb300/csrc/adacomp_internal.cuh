@@ -85,11 +85,12 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
 
 // ---------------------------------------------------------------- compress workspace
 // [Ctl 64 B][LayerWs x num_layers][desc u64 x T][tile_excl u64 x T]
-// desc (the look-back descriptors) and each layer's accumulators are zero between
-// calls: the finalise kernel clears the accumulators, the fix-up kernel the
-// descriptors.
+// Each layer's accumulators are zero between calls (the finalise kernel clears
+// them); the look-back descriptors carry the call's epoch instead of being cleared.
 struct Ctl {
-    uint32_t reserved[16];
+    uint32_t epoch;      // epoch of the last completed call (0: none); a call uses epoch % 255 + 1
+    uint32_t fin_done;   // finalise blocks done with this call (the last one advances epoch)
+    uint32_t reserved[14];
 };
 
 struct Result {              // written by each call, kept for adacomp_query
@@ -117,11 +118,22 @@ __host__ __device__ inline size_t compress_ws_bytes(int num_layers, uint64_t tot
     return ws_desc_offset(num_layers) + 16 * (size_t)total_tiles;
 }
 
-// Look-back descriptor: flag in bits 62..63, value in bits 0..61.
+// Look-back descriptor: flag in bits 62..63, the call's epoch in bits 54..61, value
+// in bits 0..53. A descriptor written by an earlier call (another epoch) reads as
+// not yet published, so descriptors need no clearing between calls.
 constexpr uint64_t kFlagAgg = 1ull << 62;
 constexpr uint64_t kFlagIncl = 2ull << 62;
 constexpr uint64_t kFlagErr = 3ull << 62;
-constexpr uint64_t kValueMask = (1ull << 62) - 1;
+constexpr int kEpochShift = 54;
+constexpr uint64_t kEpochMask = 0xffull << kEpochShift;
+constexpr uint64_t kValueMask = (1ull << kEpochShift) - 1;
+// The call's epoch (1..255) from the one stored in the workspace, in descriptor position.
+__host__ __device__ inline uint64_t call_epoch(uint32_t last) { return (uint64_t)(last % 255u + 1u) << kEpochShift; }
+// Flag of descriptor d in the call with epoch bits ep (0: not published in this call).
+__host__ __device__ inline uint32_t desc_flag(uint64_t d, uint64_t ep)
+{
+    return (d & kEpochMask) == ep ? (uint32_t)(d >> 62) : 0u;
+}
 
 // ---------------------------------------------------------------- decode workspace
 // [fixed 2048 B: u32 K, u32 num_layers, u32 pad[2], u8 bad[num_layers * K]]

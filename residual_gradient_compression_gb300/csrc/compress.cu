@@ -579,7 +579,7 @@ __device__ double exact_sum_warp(const unsigned long long* acc, unsigned long lo
 // ERROR and the function returns false.
 constexpr int kLbPerLane = 4;
 
-__device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin, uint32_t total,
+__device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin, uint32_t total, uint64_t ep,
                                  uint64_t timeout_ns, int lane, bool publish, uint64_t* excl_out)
 {
     if (t == tile_begin) {
@@ -596,7 +596,7 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
 #pragma unroll
         for (int m = 0; m < kLbPerLane; ++m) {
             const int64_t idx = j - (m * 32 + lane);
-            dv[m] = idx >= (int64_t)tile_begin ? ptx::ld_relaxed(&desc[idx]) : kFlagIncl;
+            dv[m] = idx >= (int64_t)tile_begin ? ptx::ld_relaxed(&desc[idx]) : (kFlagIncl | ep);
         }
         int mstar = kLbPerLane;
         uint32_t lim = 31;
@@ -604,7 +604,7 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
         uint32_t needed[kLbPerLane];
 #pragma unroll
         for (int m = 0; m < kLbPerLane; ++m) {
-            const uint32_t f = (uint32_t)(dv[m] >> 62);
+            const uint32_t f = desc_flag(dv[m], ep);
             const uint32_t incl = __ballot_sync(kFull, f >= 2u);
             const uint32_t pend = __ballot_sync(kFull, f == 0u);
             const uint32_t err = __ballot_sync(kFull, f == 3u);
@@ -645,7 +645,7 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
         __nanosleep(sleep_ns);
         if (sleep_ns < 256) sleep_ns <<= 1;
     }
-    if (lane == 0 && publish) ptx::st_relaxed(&desc[t], ok ? (kFlagIncl | (excl + total)) : kFlagErr);
+    if (lane == 0 && publish) ptx::st_relaxed(&desc[t], ok ? (kFlagIncl | ep | (excl + total)) : (kFlagErr | ep));
     *excl_out = excl;
     return ok;
 }
@@ -655,8 +655,8 @@ __device__ bool lookback_resolve(uint64_t* desc, uint32_t t, uint32_t tile_begin
 // header, result area; the accumulator and counters are left zeroed for the next
 // call. `tmp` (256 entries) and `words` (kSumWords entries) are shared scratch;
 // `words` must be zero on entry.
-__device__ void finalize_layer(const KLayer& ly, LayerWs* lw, const uint64_t* desc, unsigned long long* tmp,
-                               unsigned long long* words, int lane)
+__device__ void finalize_layer(const KLayer& ly, LayerWs* lw, const uint64_t* desc, uint64_t ep,
+                               unsigned long long* tmp, unsigned long long* words, int lane)
 {
     for (int e = lane; e < 256; e += 32)
         tmp[e] = ptx::ld_relaxed(reinterpret_cast<const uint64_t*>(&lw->acc[e]));
@@ -666,7 +666,7 @@ __device__ void finalize_layer(const KLayer& ly, LayerWs* lw, const uint64_t* de
         const float s = __double2float_rn(__ddiv_rn(S, (double)ly.nbins));
         const uint32_t err = *reinterpret_cast<volatile uint32_t*>(&lw->err);
         const uint64_t last = ptx::ld_relaxed(&desc[ly.tile_begin + ly.num_tiles - 1]);
-        const bool bad = err != 0u || (last >> 62) != 2u;
+        const bool bad = err != 0u || desc_flag(last, ep) != 2u;
         const uint64_t nnz = bad ? 0ull : (last & kValueMask);
         *reinterpret_cast<float*>(ly.msg) = s;
         *reinterpret_cast<uint32_t*>(ly.msg + 4) = ly.nbins;
@@ -756,6 +756,7 @@ struct Ctrl {
     uint32_t issued[2];       // tiles issued into each stage
     int32_t issue_layer;      // layer of the last tile issued
     uint32_t poisoned;        // a wait ran out: later tiles publish errors only
+    uint64_t ep;              // this call's epoch, in descriptor position
     uint32_t wsum[kWarps];    // block scan scratch
     Slot slot[kMaxBuffers];
 };
@@ -933,7 +934,7 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
                 for (uint32_t u = (uint32_t)blockIdx.x + (nb * j + b) * gridDim.x; u < T; u += nb * gridDim.x) {
                     l = layer_from(lays, g.num_layers, u, l);
                     if (lane == 0) {
-                        ptx::st_relaxed(&desc[u], kFlagErr);
+                        ptx::st_relaxed(&desc[u], kFlagErr | ctl->ep);
                         atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
                     }
                 }
@@ -941,7 +942,7 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
             }
             const int l = layer_from(lays, g.num_layers, t, 0);
             if (lane == 0) {
-                ptx::st_relaxed(&desc[t], kFlagErr);
+                ptx::st_relaxed(&desc[t], kFlagErr | ctl->ep);
                 atomicOr(&reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l))->err, kErrTimeout);
             }
             __syncwarp();
@@ -964,7 +965,7 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
         const uint32_t my_dst = incl - v;
         const uint32_t my_src = lane < (int)nrun ? sl.src[lane] : 0u;
         if (lane == 0 && t != g.inject_skip_tile)
-            ptx::st_relaxed(&desc[t], (t == ly.tile_begin ? kFlagIncl : kFlagAgg) | total);
+            ptx::st_relaxed(&desc[t], (t == ly.tile_begin ? kFlagIncl : kFlagAgg) | ctl->ep | total);
         uint16_t* cdst = reinterpret_cast<uint16_t*>(ly.msg + 8) + sl.first_bin;
         for (int bb = lane; bb < bins; bb += 32) cdst[bb] = (uint16_t)C.cnt[bb];
         // the tile's bin maxima into the exponent buckets (flushed when the layer changes)
@@ -978,7 +979,7 @@ __device__ void lookback_warp(const KGroup& g, const KLayer* lays, uint8_t* ws, 
         __syncwarp();
         for (uint32_t bb = lane; bb < C.bin_len; bb += 32) { C.gmax[bb] = 0u; C.cnt[bb] = 0u; }
         uint64_t excl = 0;
-        const bool ok = lookback_resolve(desc, t, ly.tile_begin, total, g.timeout_ns, lane,
+        const bool ok = lookback_resolve(desc, t, ly.tile_begin, total, ctl->ep, g.timeout_ns, lane,
                                          t != g.inject_skip_tile, &excl);
         if (ok) {
             if (lane == 0) texcl[t] = excl;
@@ -1377,6 +1378,7 @@ __global__ void __launch_bounds__(cta_threads(kNB), 2) compress_kernel(const __g
         ctl->users[0] = ctl->users[1] = 0u;
         ctl->issued[0] = ctl->issued[1] = 0u;
         ctl->poisoned = 0u;
+        ctl->ep = call_epoch(*reinterpret_cast<volatile const uint32_t*>(&reinterpret_cast<const Ctl*>(ws)->epoch));
         for (int k = 0; k < 2; ++k) ptx::mbar_init(&ctl->stage_full[k], 1);
         for (int k = 0; k < kNB; ++k) {
             ptx::mbar_init(&ctl->buf_full[k], kWarps);
@@ -1531,7 +1533,19 @@ __global__ void __launch_bounds__(32) finalize_kernel(const __grid_constant__ KG
     if (threadIdx.x < kSumWords) words[threadIdx.x] = 0ull;
     __syncwarp();
     const uint64_t* desc = reinterpret_cast<const uint64_t*>(ws + ws_desc_offset(g.num_layers));
-    finalize_layer(g.layer[l], reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l)), desc, tmp, words, threadIdx.x);
+    Ctl* ctl = reinterpret_cast<Ctl*>(ws);
+    const uint32_t last_epoch = *reinterpret_cast<volatile const uint32_t*>(&ctl->epoch);
+    finalize_layer(g.layer[l], reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l)), desc, call_epoch(last_epoch), tmp,
+                   words, threadIdx.x);
+    // the last block to finish records this call's epoch (every block has read the
+    // previous one by then)
+    if (threadIdx.x == 0) {
+        __threadfence();
+        if (atomicAdd(&ctl->fin_done, 1u) == (uint32_t)g.num_layers - 1u) {
+            ctl->fin_done = 0u;
+            ctl->epoch = last_epoch % 255u + 1u;
+        }
+    }
 }
 
 // ---------------------------------------------------------------- fix-up kernel
@@ -1541,8 +1555,7 @@ __global__ void __launch_bounds__(32) finalize_kernel(const __grid_constant__ KG
 // warp turns the tile's per-bin counts into an exclusive prefix (shared memory,
 // one array per warp); each lane then takes a contiguous run of the tile's codes,
 // finds the bin of its first code by binary search and walks forward, gathering
-// kFixBatch residues before it writes them back. Also returns the look-back
-// descriptors to zero for the next call.
+// kFixBatch residues before it writes them back.
 constexpr int kFixThreads = 256;
 constexpr int kFixWarps = kFixThreads / 32;
 constexpr int kFixBatch = 4;
@@ -1562,8 +1575,7 @@ __global__ void __launch_bounds__(kFixThreads) fixup_kernel(const __grid_constan
     uint32_t* pre = reinterpret_cast<uint32_t*>(reinterpret_cast<uint8_t*>(fix_dyn) + g.num_layers * sizeof(KLayer)) +
                     warp * (g.max_bins + 2);
     __syncthreads();
-    uint64_t* desc = reinterpret_cast<uint64_t*>(ws + ws_desc_offset(g.num_layers));
-    const uint64_t* texcl = desc + g.total_tiles;
+    const uint64_t* texcl = reinterpret_cast<const uint64_t*>(ws + ws_desc_offset(g.num_layers)) + g.total_tiles;
     const uint32_t T = g.total_tiles;
     const uint32_t nw = gridDim.x * kFixWarps;
 
@@ -1635,7 +1647,6 @@ __global__ void __launch_bounds__(kFixThreads) fixup_kernel(const __grid_constan
                 }
             }
         }
-        if (lane == 0) desc[t] = 0ull;
         __syncwarp();  // pre is rewritten for the next tile
     }
 }

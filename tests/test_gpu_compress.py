@@ -56,7 +56,9 @@ def _dw(n, step, seed, bf16, device="cuda"):
 
 SHAPES = [(1, 1), (2, 2), (7, 3), (10, 4), (1000, 1), (5000, 2), (123457, 7), (99999, 6),
           (100003, 50), (200000, 63), (65537, 64), (1000001, 500), (300000, 5000),
-          (250000, 8192), (40000, 4096), (4095, 4097), (8191, 8192)]
+          (250000, 8192), (40000, 4096), (4095, 4097), (8191, 8192),
+          # more warp-slice shapes: 31, 16, 25 and 5 bins per warp
+          (77777, 16), (90001, 30), (33333, 20), (1000003, 100)]
 
 
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
@@ -144,15 +146,18 @@ def test_deterministic_and_workspace_left_clean():
         msg, s = layer.step(r, dw)
         outs.append((msg.tobytes(), s, r.cpu().numpy().tobytes()))
         ws = layer.ws.cpu().numpy()
-        # the layer's exact-sum buckets and counters and every look-back descriptor
-        # are zero again; only the result area and the per-tile offsets (rewritten by
-        # every call) keep data
+        # the layer's exact-sum buckets and counters are zero again; every look-back
+        # descriptor is INCLUSIVE and carries the epoch the workspace records for the
+        # call just made (so the next call reads them all as unpublished)
         hdr = 64
-        assert not ws[:hdr].any()
+        epoch = int(ws[0:4].view(np.uint32)[0])
+        assert 1 <= epoch <= 255 and not ws[4:hdr].any()
         lw = ws[hdr:hdr + 2112]
         assert not lw[:2048 + 16].any()
         tiles = (ws.size - (hdr + 2112)) // 16
-        assert not ws[hdr + 2112:hdr + 2112 + 8 * tiles].any()
+        desc = ws[hdr + 2112:hdr + 2112 + 8 * tiles].view(np.uint64)
+        assert np.all(desc >> np.uint64(62) == 2)
+        assert np.all((desc >> np.uint64(54)) & np.uint64(0xff) == epoch)
     assert outs[0] == outs[1] == outs[2]
 
 
