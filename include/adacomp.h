@@ -226,6 +226,37 @@ adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile
 /* Bound on each device-side wait, in nanoseconds (default 2e9). */
 adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns);
 
+/* Deferred ("lazy") fix-up, the next step after the eager path
+ * ("AdaComp (Adaptive Residual Gradient Compression)", Claims > Mechanism
+ * #r629-local-bin-soft-threshold-and-mean-gmax-quantization: residue = G - G_q for
+ * sent elements; the arithmetic is unchanged, only its time moves).
+ *
+ * With enable != 0, a compress call on this handle leaves the residue of the
+ * elements it sent at G and records, in the compress workspace, one bit per such
+ * element; the next compress call on the same workspace applies
+ * residue = fl32(G - sign(G) * s_prev) to them as it loads them, before forming its
+ * own G, and adacomp_materialize applies them on demand. Messages, s and every
+ * later step are bit-identical to the eager path; the residue buffer holds the
+ * eager residue only after adacomp_materialize. No fix-up kernel runs for layers
+ * whose bins take warp-sliced tiles (16 <= L_T <= 509); other layers are fixed up
+ * eagerly as before.
+ *
+ * The workspace grows by 512 bytes per tile: *compress_ws_bytes receives the new
+ * size, and the workspace must be zero-filled before its first use. Consecutive
+ * calls must use the same workspace; materialise before checkpointing the residue,
+ * before switching the mode off, or after a call that reported an error (then also
+ * zero the workspace). adacomp_compress_static_ws rejects such handles
+ * (ADACOMP_ERR_INVALID_ARG): its workspace is not kept between calls. */
+adacomp_status adacomp_set_lazy_fixup(adacomp_layer_t h, int32_t enable, size_t* compress_ws_bytes);
+
+/* Applies every pending deferred correction to residue[] (layer order of the
+ * handle) and clears it; asynchronous on `stream`. Does nothing when the handle
+ * defers nothing. Same alignment and workspace rules as adacomp_compress. */
+adacomp_status adacomp_materialize(adacomp_layer_t h, float* residue, void* ws, size_t ws_bytes,
+                                   cudaStream_t stream);
+adacomp_status adacomp_materialize_group(adacomp_layer_t h, float* const* residue, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream);
+
 /* Releases the handle. adacomp_free(NULL) does nothing. */
 void adacomp_free(adacomp_layer_t h);
 

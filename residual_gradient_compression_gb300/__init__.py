@@ -57,6 +57,9 @@ def lib() -> ctypes.CDLL:
         L.adacomp_set_timeout_ns.argtypes = [vp, u64]
         L.adacomp_set_timing_events.argtypes = [vp, vp, vp, vp]
         L.adacomp_set_fault_injection.argtypes = [vp, ctypes.c_uint32]
+        L.adacomp_set_lazy_fixup.argtypes = [vp, i32, P(sz)]
+        L.adacomp_materialize.argtypes = [vp, vp, vp, sz, vp]
+        L.adacomp_materialize_group.argtypes = [vp, P(vp), vp, sz, vp]
         L.adacomp_free.argtypes = [vp]
         L.adacomp_free.restype = None
         L.adacomp_status_string.argtypes = [ctypes.c_int]
@@ -65,7 +68,8 @@ def lib() -> ctypes.CDLL:
                      "adacomp_compress_group", "adacomp_decode_accumulate",
                      "adacomp_decode_accumulate_group", "adacomp_query", "adacomp_decode_status",
                      "adacomp_set_timeout_ns", "adacomp_set_timing_events",
-                     "adacomp_set_fault_injection"):
+                     "adacomp_set_fault_injection", "adacomp_set_lazy_fixup", "adacomp_materialize",
+                     "adacomp_materialize_group"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -196,6 +200,26 @@ def adacomp_set_timing_events(h: Handle, before=None, mid=None, after=None):
 def adacomp_set_fault_injection(h: Handle, skip_tile: int = 0xFFFFFFFF):
     """Test hook: the given tile never publishes, so its successors time out."""
     _check(lib().adacomp_set_fault_injection(h.ptr, skip_tile), "adacomp_set_fault_injection")
+
+
+def adacomp_set_lazy_fixup(h: Handle, enable: bool = True) -> int:
+    """Defers the residue fix-up to the next compress call; returns (and records on
+    the handle) the compress workspace size the mode needs."""
+    ws = ctypes.c_size_t()
+    _check(lib().adacomp_set_lazy_fixup(h.ptr, int(bool(enable)), ctypes.byref(ws)), "adacomp_set_lazy_fixup")
+    h.compress_ws_bytes = ws.value
+    return ws.value
+
+
+def adacomp_materialize(h: Handle, residue, ws, stream=None):
+    _check(lib().adacomp_materialize(h.ptr, _ptr(residue), _ptr(ws), _nbytes(ws), _stream(stream)),
+           "adacomp_materialize")
+
+
+def adacomp_materialize_group(h: Handle, residues, ws, stream=None):
+    VP = ctypes.c_void_p * h.num_layers
+    _check(lib().adacomp_materialize_group(h.ptr, VP(*[_ptr(r) for r in residues]), _ptr(ws), _nbytes(ws),
+                                           _stream(stream)), "adacomp_materialize_group")
 
 
 def adacomp_free(h: Handle):

@@ -21,6 +21,7 @@ struct adacomp_layer {
     size_t decode_per_learner = 0;
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // optional timing events
     uint32_t inject_skip_tile = 0xffffffffu;           // test-only fault injection
+    bool lazy = false;                                 // deferred fix-up (adacomp_set_lazy_fixup)
 };
 
 namespace {
@@ -99,6 +100,7 @@ void fill_group(const adacomp_layer* h, KGroup* g)
     g->timeout_ns = h->timeout_ns;
     g->inject_skip_tile = h->inject_skip_tile;
     g->needs_gbuf = 0;
+    g->lazy = h->lazy ? 1u : 0u;
     for (const KLayer& k : h->layers)
         if (k.bin_len < 16 || (uint64_t)k.bins_per_tile * k.bin_len + 3 > 4096) g->needs_gbuf = 1;
     for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];
@@ -254,6 +256,43 @@ adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile
     if (!h) return ADACOMP_ERR_INVALID_ARG;
     h->inject_skip_tile = skip_tile;
     return ADACOMP_OK;
+}
+
+adacomp_status adacomp_set_lazy_fixup(adacomp_layer_t h, int32_t enable, size_t* compress_ws_bytes)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    h->lazy = enable != 0;
+    h->compress_ws = adacomp::compress_ws_bytes((int)h->layers.size(), h->total_tiles, h->lazy);
+    if (compress_ws_bytes) *compress_ws_bytes = h->compress_ws;
+    return ADACOMP_OK;
+}
+
+adacomp_status adacomp_materialize_group(adacomp_layer_t h, float* const* residue, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream)
+{
+    if (!h || !residue || !ws) return ADACOMP_ERR_INVALID_ARG;
+    if (!aligned(ws, 16)) return ADACOMP_ERR_ALIGNMENT;
+    if (ws_bytes < h->compress_ws) return ADACOMP_ERR_WORKSPACE;
+    if (!h->lazy) return ADACOMP_OK;  // nothing is ever deferred
+    KGroup* g = new (std::nothrow) KGroup;
+    if (!g) return ADACOMP_ERR_INVALID_ARG;
+    std::memset(g, 0, sizeof *g);
+    fill_group(h, g);
+    for (size_t i = 0; i < h->layers.size(); ++i) {
+        if (!residue[i]) { delete g; return ADACOMP_ERR_INVALID_ARG; }
+        if (!aligned(residue[i], 16)) { delete g; return ADACOMP_ERR_ALIGNMENT; }
+        g->layer[i].residue = residue[i];
+    }
+    const cudaError_t e = adacomp::launch_materialize(*g, ws, stream);
+    delete g;
+    return cuda_status(e);
+}
+
+adacomp_status adacomp_materialize(adacomp_layer_t h, float* residue, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
+    return adacomp_materialize_group(h, &residue, ws, ws_bytes, stream);
 }
 
 adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns)

@@ -56,6 +56,7 @@ struct KGroup {
     uint64_t timeout_ns;
     uint32_t inject_skip_tile;  // fault injection for tests: this tile never publishes (~0u: none)
     uint32_t needs_gbuf;        // some tile is processed through shared memory (short bins or > 4096 slots)
+    uint32_t lazy;              // deferred fix-up for warp-sliced layers (pending masks in the workspace)
 };
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:
@@ -84,7 +85,7 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
 }
 
 // ---------------------------------------------------------------- compress workspace
-// [Ctl 64 B][LayerWs x num_layers][desc u64 x T][tile_excl u64 x T]
+// [Ctl 64 B][LayerWs x num_layers][desc u64 x T][tile_excl u64 x T][lazy only: pending u16 x 256 x T]
 // Each layer's accumulators are zero between calls (the finalise kernel clears
 // them); the look-back descriptors carry the call's epoch instead of being cleared.
 struct Ctl {
@@ -113,9 +114,17 @@ static_assert(sizeof(LayerWs) % 64 == 0, "LayerWs alignment");
 
 __host__ __device__ inline size_t ws_layer_offset(int l) { return sizeof(Ctl) + (size_t)l * sizeof(LayerWs); }
 __host__ __device__ inline size_t ws_desc_offset(int num_layers) { return sizeof(Ctl) + (size_t)num_layers * sizeof(LayerWs); }
-__host__ __device__ inline size_t compress_ws_bytes(int num_layers, uint64_t total_tiles)
+// Deferred (lazy) fix-up: one 16-bit mask per compute lane and tile, bit 4k + i
+// for the lane's register slot (k, i) of a warp-sliced tile, set when that element
+// was sent and its residue still holds G.
+constexpr size_t kPendBytesPerTile = kWarps * 32 * 2;
+__host__ __device__ inline size_t ws_pend_offset(int num_layers, uint64_t total_tiles)
 {
     return ws_desc_offset(num_layers) + 16 * (size_t)total_tiles;
+}
+__host__ __device__ inline size_t compress_ws_bytes(int num_layers, uint64_t total_tiles, bool lazy = false)
+{
+    return ws_pend_offset(num_layers, total_tiles) + (lazy ? kPendBytesPerTile * (size_t)total_tiles : 0);
 }
 
 // Look-back descriptor: flag in bits 62..63, the call's epoch in bits 54..61, value
@@ -159,6 +168,7 @@ struct DecodeParams {
 cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cudaEvent_t ev_before = nullptr,
                             cudaEvent_t ev_mid = nullptr, cudaEvent_t ev_after = nullptr);
 cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cudaStream_t stream);
+cudaError_t launch_materialize(const KGroup& g, void* ws, cudaStream_t stream);
 }  // namespace adacomp
 
 struct adacomp_layer;

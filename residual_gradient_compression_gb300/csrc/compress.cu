@@ -1017,7 +1017,7 @@ template <bool BF16, class Release>
 __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G, int pr, int pd, const float* sr,
                                               const void* sd, uint32_t* wg, uint32_t* wc, uint32_t* cnt_tile,
                                               uint16_t* stg, uint32_t* gmax_tile, int warp, int lane,
-                                              uint32_t* src, Release&& release)
+                                              uint16_t* pend, float s_prev, uint32_t* src, Release&& release)
 {
     const int L = ly.bin_len;
     const int bpw = ly.bpw;
@@ -1033,7 +1033,11 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
     const int rot = seg_rot(lane);
     float ah[4][4];
     uint32_t nz = 0, ng = 0;
+    uint32_t nzr = 0;  // G != 0 in register order (bit 4k + i)
     float m_lo = 0.0f, m_hi = 0.0f;
+    // deferred fix-up of the previous call: the residue of the slots it sent still
+    // holds G; the correction fl32(G - sign(G) s_prev) is applied as they are loaded
+    const uint32_t pm = pend ? (uint32_t)*pend : 0u;
     if (active) {
         const bool edge = valid != 0xffffu;
         const float* rs = sr + pr + e_first;
@@ -1041,7 +1045,13 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
             const int q0 = 4 * (k ^ rot);
-            const float4 r = *reinterpret_cast<const float4*>(rs + q0);
+            float4 r = *reinterpret_cast<const float4*>(rs + q0);
+            if (pm & (0xfu << (4 * k))) {
+                if (pm & (1u << (4 * k + 0))) r.x = __fsub_rn(r.x, copysignf(s_prev, r.x));
+                if (pm & (1u << (4 * k + 1))) r.y = __fsub_rn(r.y, copysignf(s_prev, r.y));
+                if (pm & (1u << (4 * k + 2))) r.z = __fsub_rn(r.z, copysignf(s_prev, r.z));
+                if (pm & (1u << (4 * k + 3))) r.w = __fsub_rn(r.w, copysignf(s_prev, r.w));
+            }
             float d[4], gv[4];
             if constexpr (BF16) {
                 const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(sd) + pd + e_first + q0);
@@ -1069,7 +1079,9 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
             }
             nz |= nzq << q0;
             ng |= ngq << q0;
-            // residue := G (sent elements are corrected by the fix-up kernel)
+            nzr |= nzq << (4 * k);
+            // residue := G (sent elements are corrected by the fix-up kernel, or by the
+            // next call when the fix-up is deferred)
             float* gp = gres + q0;
             if (vq == 0xfu) {
                 *reinterpret_cast<float4*>(gp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
@@ -1097,7 +1109,7 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
     if (m_lo > 0.0f) atomicMax(&wg[bin_lo], __float_as_uint(m_lo));
     if (m_hi > 0.0f) atomicMax(&wg[bin_lo + 1], __float_as_uint(m_hi));
     __syncwarp();
-    uint32_t f = 0;
+    uint32_t f = 0, fr = 0;  // sent slots, in slot order and in register order
     if (active) {
         const float gm_lo = __uint_as_float(wg[bin_lo]);
         const float gm_hi = split < kSeg ? __uint_as_float(wg[bin_lo + 1]) : 0.0f;
@@ -1109,8 +1121,10 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
             for (int i = 0; i < 4; ++i)
                 nib |= ah[k][i] >= (q0 + i < split ? gm_lo : gm_hi) ? (1u << i) : 0u;
             f |= nib << q0;
+            fr |= nib << (4 * k);
         }
         f &= nz;
+        fr &= nzr;
         const uint32_t lomask = split >= kSeg ? 0xffffu : ((1u << max(split, 0)) - 1u);
         const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
         if (c_lo) atomicAdd(&wc[bin_lo], c_lo);
@@ -1144,6 +1158,7 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
         f &= f - 1;
         *sp++ = (uint16_t)((idx < split ? base_lo : base_hi) + 2u * idx + ((ng >> idx) & 1u));
     }
+    if (pend) *pend = (uint16_t)fr;  // corrections this call leaves to the next one
     *src = (uint32_t)we0;
     return total;
 }
@@ -1337,7 +1352,9 @@ __device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int p
 // kPaths: 1 = every layer of the launch is warp-sliced, 2 = none is, 3 = mixed.
 // The single-path instantiations keep the warp-sliced path's registers free of
 // the block-wide path's needs.
-template <int kPaths, int kNB>
+// kLazy: warp-sliced layers apply the previous call's deferred corrections and
+// record their own instead of leaving them to the fix-up kernel.
+template <int kPaths, int kNB, bool kLazy>
 __global__ void __launch_bounds__(cta_threads(kNB), 2) compress_kernel(const __grid_constant__ KGroup g,
                                                                   uint8_t* __restrict__ ws)
 {
@@ -1465,12 +1482,19 @@ __global__ void __launch_bounds__(cta_threads(kNB), 2) compress_kernel(const __g
                 if constexpr (kPaths & 1) {
                 // warp-sliced tile: no barrier among the compute warps
                 uint32_t src = 0, cnt;
+                uint16_t* pend = nullptr;
+                float s_prev = 0.0f;
+                if constexpr (kLazy) {
+                    pend = reinterpret_cast<uint16_t*>(ws + ws_pend_offset(g.num_layers, T)) +
+                           ((size_t)t * kWarps + warp) * 32 + lane;
+                    s_prev = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(G.layer))->result.s;
+                }
                 if (ly.dw_bf16)
                     cnt = warp_tile<true>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, gmax_c, warp, lane,
-                                          &src, release);
+                                          pend, s_prev, &src, release);
                 else
                     cnt = warp_tile<false>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, gmax_c, warp, lane,
-                                           &src, release);
+                                           pend, s_prev, &src, release);
                 if (lane == 0) {
                     sl.src[warp] = src;
                     sl.cnt[warp] = cnt;
@@ -1588,7 +1612,7 @@ __global__ void __launch_bounds__(kFixThreads) fixup_kernel(const __grid_constan
         const int64_t ts = (int64_t)first_bin * ly.bin_len;
         const int tl = (int)min((int64_t)bins * ly.bin_len, ly.n - ts);
         const LayerWs* lw = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l));
-        if (lw->result.status == 0u) {
+        if (lw->result.status == 0u && !(g.lazy && ly.bpw)) {  // deferred layers are corrected by the next call
             const uint16_t* cnt = reinterpret_cast<const uint16_t*>(ly.msg + 8) + first_bin;
             uint32_t run = 0;
             for (int b0 = 0; b0 < bins; b0 += 32) {
@@ -1651,13 +1675,52 @@ __global__ void __launch_bounds__(kFixThreads) fixup_kernel(const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------- materialise (deferred fix-up)
+// Applies the corrections a compress call with a deferred fix-up left pending:
+// residue = fl32(G - sign(G) s) for every slot whose bit is set in its lane's mask,
+// with s the layer's scale from that call; the masks are cleared. One CTA of
+// 8 x 32 threads per tile, thread (warp, lane) owning the same slots as in the
+// compress kernel's warp-sliced tile.
+__global__ void __launch_bounds__(kThreads) materialize_kernel(const __grid_constant__ KGroup g,
+                                                               uint8_t* __restrict__ ws)
+{
+    const uint32_t T = g.total_tiles;
+    uint16_t* pend0 = reinterpret_cast<uint16_t*>(ws + ws_pend_offset(g.num_layers, T));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (uint32_t t = blockIdx.x; t < T; t += gridDim.x) {
+        const int l = layer_from(g.layer, g.num_layers, t, 0);
+        const KLayer& ly = g.layer[l];
+        if (!ly.bpw) continue;
+        uint16_t* pend = pend0 + ((size_t)t * kWarps + warp) * 32 + lane;
+        const uint32_t pm = *pend;
+        if (!pm) continue;
+        const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+        const int bins = (int)min(ly.bins_per_tile, ly.nbins - first_bin);
+        const int64_t ts = (int64_t)first_bin * ly.bin_len;
+        const int pr = (int)(ts & 3);
+        const int wb0 = min(bins, warp * (int)ly.bpw);
+        const int e_first = (((pr + wb0 * ly.bin_len) & ~3) - pr) + kSeg * lane;
+        const int rot = seg_rot(lane);
+        const float s = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l))->result.s;
+        float* res = ly.residue + ts + e_first;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            const int q0 = 4 * (k ^ rot);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (pm & (1u << (4 * k + i))) res[q0 + i] = __fsub_rn(res[q0 + i], copysignf(s, res[q0 + i]));
+        }
+        *pend = 0;
+    }
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------- host launcher
 namespace {
 struct DeviceInfo {
     int sms = 0;
-    uint32_t smem_set[4] = {0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per compress kernel
+    uint32_t smem_set[5] = {0, 0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per compress kernel
     uint32_t fix_smem_set = 0;  // same, fix-up kernel
 };
 DeviceInfo g_dev[64];
@@ -1680,13 +1743,16 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
     // four staging buffers where every layer is warp-sliced (short tiles), else three
     const int nb = paths == 1 ? 4 : 3;
     const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf, nb);
-    void (*kern)(KGroup, uint8_t*) = paths == 1 ? compress_kernel<1, 4>
-                                   : paths == 2 ? compress_kernel<2, 3> : compress_kernel<3, 3>;
+    void (*kern)(KGroup, uint8_t*);
+    if (paths == 1) kern = g.lazy ? compress_kernel<1, 4, true> : compress_kernel<1, 4, false>;
+    else if (paths == 2) kern = compress_kernel<2, 3, false>;  // no warp-sliced layer: nothing is deferred
+    else kern = g.lazy ? compress_kernel<3, 3, true> : compress_kernel<3, 3, false>;
+    const int kidx = paths == 1 ? (g.lazy ? 1 : 0) : paths == 2 ? 2 : (g.lazy ? 3 : 4);
     const int threads = cta_threads(nb);
-    if (P.total > di.smem_set[paths]) {
+    if (P.total > di.smem_set[kidx]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
         if (e != cudaSuccess) return e;
-        di.smem_set[paths] = P.total;
+        di.smem_set[kidx] = P.total;
     }
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, threads, P.total);
@@ -1714,6 +1780,10 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
     finalize_kernel<<<g.num_layers, 32, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
+    if (g.lazy && paths == 1) {  // every layer's corrections are deferred to the next call
+        if (ev_after) e = cudaEventRecord(ev_after, stream);
+        return e;
+    }
     const uint32_t fsmem = fix_smem_bytes(g.num_layers, g.max_bins);
     if (fsmem > 48 * 1024 && fsmem > di.fix_smem_set) {
         e = cudaFuncSetAttribute(fixup_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)fsmem);
@@ -1732,6 +1802,24 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
     if (e != cudaSuccess) return e;
     if (ev_after) e = cudaEventRecord(ev_after, stream);
     return e;
+}
+
+cudaError_t launch_materialize(const KGroup& g, void* ws, cudaStream_t stream)
+{
+    if (!g.lazy) return cudaSuccess;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    DeviceInfo& di = g_dev[dev];
+    if (di.sms == 0) {
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const long long cap = (long long)di.sms * 8;
+    const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
+    materialize_kernel<<<grid, kThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    return cudaGetLastError();
 }
 
 }  // namespace adacomp
@@ -1763,6 +1851,7 @@ extern "C" adacomp_status adacomp_compress_static_ws(adacomp_layer_t h, float* r
     size_t ws_needed = 0;
     const int chk = prepare_single_compress(h, residue, dW, msg, msg_capacity, &g, &ws_needed);
     if (chk != ADACOMP_OK) return (adacomp_status)chk;
+    if (g.lazy) return ADACOMP_ERR_INVALID_ARG;  // deferred corrections need a workspace kept by the caller
     if (result_out && (reinterpret_cast<uintptr_t>(result_out) & 7u)) return ADACOMP_ERR_ALIGNMENT;
 
     int dev = 0;

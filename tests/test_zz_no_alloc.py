@@ -77,3 +77,16 @@ def test_static_scratch_rejects_layers_that_do_not_fit():
     st = f(h.ptr, tiny.data_ptr(), tiny.data_ptr(), tiny.data_ptr(), 16, None,
            torch.cuda.current_stream().cuda_stream)
     assert st == ac.ERR_WORKSPACE
+
+
+def test_static_scratch_rejects_deferred_fixup_handles():
+    """A deferred fix-up keeps state in the workspace between calls, which the fixed
+    array cannot hold for the caller."""
+    f = _entry()
+    h = ac.adacomp_init_layer(10_000, 50, ac.F32)
+    ac.adacomp_set_lazy_fixup(h, True)
+    r = torch.zeros(10_000, device="cuda")
+    msg = torch.zeros(h.max_msg_bytes[0], dtype=torch.uint8, device="cuda")
+    st = f(h.ptr, r.data_ptr(), r.data_ptr(), msg.data_ptr(), msg.numel(), None,
+           torch.cuda.current_stream().cuda_stream)
+    assert st == ac.ERR_INVALID_ARG
