@@ -53,6 +53,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
+    p.add_argument("--no-lazy", action="store_true", help="skip the deferred fix-up measurement")
     p.add_argument("--min-timed-seconds", type=float, default=1.5,
                    help="repeat the K timed steps until the clock sampler has covered this long")
     return p.parse_args()
@@ -292,8 +293,10 @@ class DeviceRun:
         # compress: streaming kernel, finalise, fix-up; decode: tile sums, scan, accumulate
         return self.K * len(self.gidx) * 3 + len(self.gidx) * 3
 
-    def step(self, i, stream_ptr, k1_events=None, dec_events=None):
-        """Enqueues one step: every learner's compress, then the decode of the step's messages."""
+    def step(self, i, stream_ptr, k1_events=None, dec_events=None, ws_fixed=None):
+        """Enqueues one step: every learner's compress, then the decode of the step's messages.
+        ws_fixed: one workspace per (learner, group) used by every step (a deferred
+        fix-up keeps its pending corrections there), instead of the per-step ring."""
         L, s = self.L, i % self.sets
         for k in range(self.K):
             for gi, h in enumerate(self.h):
@@ -302,7 +305,7 @@ class DeviceRun:
                     L.adacomp_set_timing_events(h.ptr, self.ct.c_void_p(e[0].cuda_event),
                                                 self.ct.c_void_p(e[1].cuda_event),
                                                 self.ct.c_void_p(e[2].cuda_event))
-                ws = self.ws[i % self.ring][k][gi]
+                ws = ws_fixed[k][gi] if ws_fixed is not None else self.ws[i % self.ring][k][gi]
                 st = L.adacomp_compress_group(h.ptr, self.c_res[k][gi], self.c_dw[k][s][gi], self.c_msg[k][gi],
                                               self.c_cap[k][gi], ws.data_ptr(), ws.numel(), stream_ptr)
                 if st:
@@ -439,7 +442,49 @@ def run_device(args, rank, world):
     }
     if not args.no_e2e:
         out["e2e"] = run_e2e(args, run, layers, sp, world)
+    if not args.no_lazy:
+        out["lazy_fixup"] = run_lazy(args, run, sp, world, n_elems)
     return out, run
+
+
+def run_lazy(args, run, sp, world, n_elems):
+    """The same steps with the residue fix-up deferred to the next step
+    (adacomp_set_lazy_fixup): identical messages, no fix-up kernel for warp-sliced
+    layers. Reported beside the eager numbers, not as the headline."""
+    ac = run.ac
+    for h in run.h:
+        ac.adacomp_set_lazy_fixup(h, True)
+    ws = [[torch.zeros(h.compress_ws_bytes, dtype=torch.uint8, device=run.dev) for h in run.h]
+          for _ in range(run.K)]
+    stream = torch.cuda.current_stream()
+    for i in range(max(3, args.warmup)):
+        run.step(i, sp, ws_fixed=ws)
+    start, end = _new_events(2)
+    reps, t0, step_no = [], time.perf_counter(), 0
+    while True:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for i in range(args.steps):
+            run.step(step_no + i, sp, ws_fixed=ws)
+        end.record(stream)
+        torch.cuda.synchronize()
+        reps.append(start.elapsed_time(end))
+        step_no += args.steps
+        if time.perf_counter() - t0 >= args.min_timed_seconds / 2 or len(reps) >= 200:
+            break
+    ms = max_over_ranks(sorted(reps)[len(reps) // 2], world)
+    for k in range(run.K):
+        for gi, h in enumerate(run.h):
+            for li in range(h.num_layers):
+                if ac.adacomp_query(h, ws[k][gi], li)[2] != ac.OK:
+                    raise RuntimeError("device status not OK with the deferred fix-up")
+            ac.adacomp_materialize_group(h, run.res[k][1][run.gidx[gi][0]:run.gidx[gi][-1] + 1], ws[k][gi])
+    for h in run.h:
+        ac.adacomp_set_lazy_fixup(h, False)
+    torch.cuda.synchronize()
+    return {"value": n_elems * args.steps * world / (ms * 1e-3), "unit": "elements/s",
+            "ms_per_step": ms / args.steps, "timed_repetitions": len(reps)}
 
 
 def run_e2e(args, run, layers, sp, world):
