@@ -262,6 +262,85 @@ __device__ __forceinline__ void acc_learner(const KLayer& ly, const AccTile& A, 
     __syncwarp();  // pre is rewritten for the next learner; this learner's additions are done
 }
 
+// Warp `warp` owns one bin of tile A (tiles of at most 8 bins): every learner's
+// codes for that bin. Lane k of a round of 32 learners fetches learner k's tile
+// offset, scale and counts at once; the codes are then prefetched for 8 learners
+// at a time (lane i holding code i of each) and added in learner order.
+constexpr int kAccWindow = 8;
+
+__device__ __forceinline__ void acc_bin_learners(const KLayer& ly, const AccTile& A, const DecodeParams& p,
+                                                 uint8_t* ws, uint32_t T, uint32_t t, int l, int bin, float* sd,
+                                                 int lane)
+{
+    const int K = p.K;
+    const int L = ly.bin_len;
+    const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * L;
+    const uint32_t len = (uint32_t)((A.first_bin + bin == ly.nbins - 1) ? last_len : L);
+    float* x0 = sd + (int64_t)bin * L;
+    const bool wide = ly.code_bytes == 2;
+    for (int kb = 0; kb < K; kb += 32) {
+        // lane k: where learner kb + k's codes for this bin start, how many, its scale
+        const int k = kb + lane;
+        unsigned long long start = 0;
+        uint32_t c = 0;
+        float sk = 0.0f;
+        const uint8_t* codes = nullptr;
+        if (k < K) {
+            const uint64_t off = tile_offsets(ws, k, T)[t];
+            if (off != kBadOffset) {
+                const uint8_t* msg = p.msg[l * K + k];
+                const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + A.first_bin;
+                uint32_t before = 0;
+                for (int b = 0; b < bin; ++b) before += cnt[b];
+                c = cnt[bin];
+                sk = *reinterpret_cast<const float*>(msg);
+                start = off + before;
+                codes = msg + 8 + 2ull * ly.nbins;
+            }
+        }
+        const int kn = min(32, K - kb);
+        for (int k0 = 0; k0 < kn; k0 += kAccWindow) {
+            uint32_t cw[kAccWindow];
+#pragma unroll
+            for (int w = 0; w < kAccWindow; ++w) {
+                const int kk = min(k0 + w, kn - 1);
+                const uint32_t ck = __shfl_sync(kFull, c, kk);
+                const unsigned long long st = __shfl_sync(kFull, start, kk);
+                const uint8_t* cp = reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)codes, kk));
+                cw[w] = 0xffffffffu;
+                if (k0 + w < kn && (uint32_t)lane < ck)
+                    cw[w] = wide ? reinterpret_cast<const uint16_t*>(cp)[st + lane] : cp[st + lane];
+            }
+#pragma unroll
+            for (int w = 0; w < kAccWindow; ++w) {
+                if (k0 + w >= kn) break;
+                const int kk = k0 + w;
+                const uint32_t ck = __shfl_sync(kFull, c, kk);
+                const float s = __shfl_sync(kFull, sk, kk);
+                bool bad = false;
+                if (cw[w] != 0xffffffffu) {
+                    const uint32_t o = cw[w] >> 1;
+                    if (o < len) x0[o] = __fadd_rn(x0[o], (cw[w] & 1u) ? -s : s);
+                    else bad = true;
+                }
+                if (ck > 32u) {  // more codes than lanes in this bin: the rest, in rounds
+                    const unsigned long long st = __shfl_sync(kFull, start, kk);
+                    const uint8_t* cp =
+                        reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)codes, kk));
+                    for (uint32_t i = 32 + lane; i < ck; i += 32) {
+                        const uint32_t code = wide ? reinterpret_cast<const uint16_t*>(cp)[st + i] : cp[st + i];
+                        const uint32_t o = code >> 1;
+                        if (o < len) x0[o] = __fadd_rn(x0[o], (code & 1u) ? -s : s);
+                        else bad = true;
+                    }
+                }
+                if (bad) ws[16 + l * K + kb + kk] = 1;  // offset outside its bin: ignored, message flagged
+                __syncwarp();  // learner kk's additions come before learner kk + 1's
+            }
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_constant__ KGroup g,
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
@@ -302,7 +381,9 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         float* sd = st + (A.ts - A.a0);  // element ts + x at sd[x]
         const int bpw = (A.bins + kDecThreads / 32 - 1) / (kDecThreads / 32);
         const int b0 = min(A.bins, warp * bpw), b1 = min(A.bins, b0 + bpw);
-        if (b0 < b1) {
+        if (bpw == 1) {
+            if (b0 < b1) acc_bin_learners(ly, A, p, ws, T, t, l, b0, sd, lane);
+        } else if (b0 < b1) {
             for (int k = 0; k < K; ++k) {
                 const uint64_t off = tile_offsets(ws, k, T)[t];
                 if (off == kBadOffset) continue;

@@ -53,7 +53,7 @@ def _gpu_decode(h, msgs, dense0):
 
 @pytest.mark.parametrize("n,L,K", [(10, 4, 1), (1, 1, 2), (100_003, 50, 1), (100_003, 50, 3),
                                    (1_000_001, 500, 16), (300_007, 5000, 5), (77_777, 7, 4),
-                                   (65_537, 64, 2)])
+                                   (65_537, 64, 2), (200_003, 500, 40), (123_457, 1000, 3)])
 def test_decode_matches_oracle(n, L, K):
     msgs = _learner_msgs(n, L, K, seed=n + L)
     h = ac.adacomp_init_layer(n, L, ac.F32)
@@ -108,8 +108,9 @@ def test_flat100m_four_learners_end_to_end():
     assert np.array_equal(dense.cpu().numpy().view(np.uint32), ref_dense.view(np.uint32))
 
 
-def test_malformed_messages_are_skipped_and_reported():
-    n, L = 50_000, 50
+@pytest.mark.parametrize("L", [50, 500])
+def test_malformed_messages_are_skipped_and_reported(L):
+    n = 50_000
     msgs = _learner_msgs(n, L, 2, seed=3)
     h = ac.adacomp_init_layer(n, L, ac.F32)
     good = msgs[0][0][:msgs[0][1]].cpu().numpy()
@@ -121,8 +122,9 @@ def test_malformed_messages_are_skipped_and_reported():
         if mutate == "B":
             bad[4] = (int(bad[4]) + 1) % 256
         else:
-            bad[8] = 60  # bin 0 holds 50 elements
-            bad[9] = 0
+            c = L + 10  # more codes than bin 0 has elements
+            bad[8] = c & 0xff
+            bad[9] = c >> 8
         got, st = _gpu_decode(h, [msgs[0], (bad, mb)], dense0)
         assert st == ac.ERR_BAD_MESSAGE, mutate
         assert np.array_equal(got.view(np.uint32), expect.view(np.uint32)), mutate
