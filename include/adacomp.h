@@ -226,6 +226,19 @@ adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile
 /* Bound on each device-side wait, in nanoseconds (default 2e9). */
 adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns);
 
+/* Selection rule. ADACOMP_RULE_ADACOMP (the default) sends an element when
+ * G != 0 and |fl32(G + dW)| >= g_max of its bin ("AdaComp (Adaptive Residual
+ * Gradient Compression)", Claims > Mechanism
+ * #r629-local-bin-soft-threshold-and-mean-gmax-quantization).
+ * ADACOMP_RULE_LOCAL_SELECTION is the hard Local Selection rule that the same entry
+ * contrasts with it (Claims > Mechanism
+ * #r629-self-adjusting-sparsity-prevents-residual-explosion): no soft-threshold
+ * probe, G != 0 and |G| >= g_max, i.e. only the bin maxima (all of them on a tie).
+ * s, the codes, the message format, the residue update and decoding are the same
+ * for both. Returns ADACOMP_ERR_INVALID_ARG for any other value. */
+enum { ADACOMP_RULE_ADACOMP = 0, ADACOMP_RULE_LOCAL_SELECTION = 1 };
+adacomp_status adacomp_set_selection_rule(adacomp_layer_t h, int32_t rule);
+
 /* Deferred ("lazy") fix-up, the next step after the eager path
  * ("AdaComp (Adaptive Residual Gradient Compression)", Claims > Mechanism
  * #r629-local-bin-soft-threshold-and-mean-gmax-quantization: residue = G - G_q for

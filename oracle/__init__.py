@@ -49,7 +49,7 @@ class Oracle:
         lib.adacomp_oracle_exact_sum_f32.argtypes = [vp, i64]
         lib.adacomp_oracle_exact_sum_f32.restype = ctypes.c_double
         lib.adacomp_oracle_compress.argtypes = [i64, i32, ctypes.c_int, vp, vp, vp, u64,
-                                                ctypes.POINTER(u64), vp, vp, vp, ctypes.c_int]
+                                                ctypes.POINTER(u64), vp, vp, vp, ctypes.c_int, ctypes.c_int]
         lib.adacomp_oracle_compress.restype = ctypes.c_int
         lib.adacomp_oracle_decode_accumulate.argtypes = [i64, i32, vp, i32, vp]
         lib.adacomp_oracle_decode_accumulate.restype = ctypes.c_int
@@ -86,11 +86,12 @@ class CompressResult:
 
 
 def compress(residue: np.ndarray, dw: np.ndarray, bin_len: int,
-             literal_zero_select: bool = False, lib=None) -> CompressResult:
+             literal_zero_select: bool = False, lib=None, local_selection: bool = False) -> CompressResult:
     """One step for one layer. ``residue`` (fp32, contiguous) is updated in place.
 
     ``dw`` is fp32, or uint16 holding bf16 bit patterns. Returns the message bytes,
-    s, g_max per bin and the 0/1 selection mask.
+    s, g_max per bin and the 0/1 selection mask. ``local_selection`` selects the hard
+    Local Selection rule (abs(G) >= g_max, no soft-threshold probe) instead of AdaComp's.
     """
     lib = lib or _load()
     assert residue.dtype == np.float32 and residue.flags.c_contiguous
@@ -114,7 +115,7 @@ def compress(residue: np.ndarray, dw: np.ndarray, bin_len: int,
     mlen = ctypes.c_uint64(0)
     rc = lib.adacomp_oracle_compress(n, bin_len, bf16, _ptr(residue), _ptr(dw), _ptr(msg), cap,
                                      ctypes.byref(mlen), _ptr(s), _ptr(gmax), _ptr(sel),
-                                     int(literal_zero_select))
+                                     int(literal_zero_select), int(local_selection))
     if rc != OK:
         raise RuntimeError(f"oracle compress failed: {rc}")
     return CompressResult(msg[: mlen.value].copy(), s[0], gmax, sel.astype(bool))

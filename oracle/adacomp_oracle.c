@@ -132,11 +132,15 @@ static uint32_t get_u32(const uint8_t *p)
  * Mechanism claim). residue is updated in place. Optional outputs: s, g_max[B],
  * sel[n] (1 = sent). literal_zero_select = 1 applies |H| >= g_max without the
  * G != 0 conjunct (documentation only: it sends zeros as +s codes).
+ * local_selection = 1 is the hard Local Selection rule the entry contrasts with
+ * AdaComp (Claims > Mechanism #r629-self-adjusting-sparsity-prevents-residual-
+ * explosion): no soft-threshold probe, so the comparison is |G| >= g_max and only
+ * a bin's maxima are sent; everything else (s, codes, residue) is unchanged.
  */
 int adacomp_oracle_compress(int64_t n, int32_t L, int dw_bf16, float *residue, const void *dw,
                             uint8_t *msg, uint64_t msg_cap, uint64_t *msg_len,
                             float *s_out, float *gmax_out, uint8_t *sel_out,
-                            int literal_zero_select)
+                            int literal_zero_select, int local_selection)
 {
     if (n < 1 || L < 1 || L > 32768 || !residue || !dw || !msg) return ORACLE_ERR_ARG;
     int64_t B = bin_count(n, L);
@@ -154,6 +158,7 @@ int adacomp_oracle_compress(int64_t n, int32_t L, int dw_bf16, float *residue, c
         float d = load_dw(dw, dw_bf16, j);
         G[j] = residue[j] + d;
         H[j] = G[j] + d;
+        if (local_selection) H[j] = G[j]; /* Local Selection: compare G itself */
     }
 
     /* g_max(i): largest |G| in bin i; the last bin may be shorter than L */

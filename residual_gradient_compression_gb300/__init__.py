@@ -22,6 +22,7 @@ from .build import LIB as _LIB_PATH
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, \
     ERR_BAD_MESSAGE = range(8)
 F32, BF16 = 0, 1
+RULE_ADACOMP, RULE_LOCAL_SELECTION = 0, 1
 MAX_GROUP = 128
 MAX_LEARNERS = 256
 DECODE_WS_FIXED = 2048
@@ -58,6 +59,7 @@ def lib() -> ctypes.CDLL:
         L.adacomp_set_timing_events.argtypes = [vp, vp, vp, vp]
         L.adacomp_set_fault_injection.argtypes = [vp, ctypes.c_uint32]
         L.adacomp_set_lazy_fixup.argtypes = [vp, i32, P(sz)]
+        L.adacomp_set_selection_rule.argtypes = [vp, i32]
         L.adacomp_materialize.argtypes = [vp, vp, vp, sz, vp]
         L.adacomp_materialize_group.argtypes = [vp, P(vp), vp, sz, vp]
         L.adacomp_free.argtypes = [vp]
@@ -68,7 +70,8 @@ def lib() -> ctypes.CDLL:
                      "adacomp_compress_group", "adacomp_decode_accumulate",
                      "adacomp_decode_accumulate_group", "adacomp_query", "adacomp_decode_status",
                      "adacomp_set_timeout_ns", "adacomp_set_timing_events",
-                     "adacomp_set_fault_injection", "adacomp_set_lazy_fixup", "adacomp_materialize",
+                     "adacomp_set_fault_injection", "adacomp_set_lazy_fixup", "adacomp_set_selection_rule",
+                     "adacomp_materialize",
                      "adacomp_materialize_group"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -200,6 +203,11 @@ def adacomp_set_timing_events(h: Handle, before=None, mid=None, after=None):
 def adacomp_set_fault_injection(h: Handle, skip_tile: int = 0xFFFFFFFF):
     """Test hook: the given tile never publishes, so its successors time out."""
     _check(lib().adacomp_set_fault_injection(h.ptr, skip_tile), "adacomp_set_fault_injection")
+
+
+def adacomp_set_selection_rule(h: Handle, rule: int):
+    """RULE_ADACOMP (default) or RULE_LOCAL_SELECTION (abs(G) >= g_max, no probe)."""
+    _check(lib().adacomp_set_selection_rule(h.ptr, rule), "adacomp_set_selection_rule")
 
 
 def adacomp_set_lazy_fixup(h: Handle, enable: bool = True) -> int:

@@ -22,6 +22,7 @@ struct adacomp_layer {
     cudaEvent_t ev[3] = {nullptr, nullptr, nullptr};  // optional timing events
     uint32_t inject_skip_tile = 0xffffffffu;           // test-only fault injection
     bool lazy = false;                                 // deferred fix-up (adacomp_set_lazy_fixup)
+    uint32_t rule = ADACOMP_RULE_ADACOMP;              // selection rule (adacomp_set_selection_rule)
 };
 
 namespace {
@@ -101,6 +102,7 @@ void fill_group(const adacomp_layer* h, KGroup* g)
     g->inject_skip_tile = h->inject_skip_tile;
     g->needs_gbuf = 0;
     g->lazy = h->lazy ? 1u : 0u;
+    g->local_selection = h->rule == ADACOMP_RULE_LOCAL_SELECTION ? 1u : 0u;
     for (const KLayer& k : h->layers)
         if (k.bin_len < 16 || (uint64_t)k.bins_per_tile * k.bin_len + 3 > 4096) g->needs_gbuf = 1;
     for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];
@@ -255,6 +257,13 @@ adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile
 {
     if (!h) return ADACOMP_ERR_INVALID_ARG;
     h->inject_skip_tile = skip_tile;
+    return ADACOMP_OK;
+}
+
+adacomp_status adacomp_set_selection_rule(adacomp_layer_t h, int32_t rule)
+{
+    if (!h || (rule != ADACOMP_RULE_ADACOMP && rule != ADACOMP_RULE_LOCAL_SELECTION)) return ADACOMP_ERR_INVALID_ARG;
+    h->rule = (uint32_t)rule;
     return ADACOMP_OK;
 }
 

@@ -57,6 +57,7 @@ struct KGroup {
     uint32_t inject_skip_tile;  // fault injection for tests: this tile never publishes (~0u: none)
     uint32_t needs_gbuf;        // some tile is processed through shared memory (short bins or > 4096 slots)
     uint32_t lazy;              // deferred fix-up for warp-sliced layers (pending masks in the workspace)
+    uint32_t local_selection;   // selection rule: 0 AdaComp (abs(G + dW) >= g_max), 1 Local Selection (abs(G) >= g_max)
 };
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:

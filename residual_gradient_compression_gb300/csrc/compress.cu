@@ -131,7 +131,13 @@ struct Tile {
     int cpb;        // chunks per bin
     int ch;         // chunk length (elements, multiple of VEC)
     uint32_t inv_len;  // ceil(2^32 / L)
+    bool ls;           // Local Selection: the probe is G itself, not G + dW
 };
+
+// The value compared with g_max: H = fl32(G + dW) for AdaComp, G for Local
+// Selection ("AdaComp (Adaptive Residual Gradient Compression)", Claims > Mechanism
+// #r629-self-adjusting-sparsity-prevents-residual-explosion).
+__device__ __forceinline__ float probe(float g, float d, bool ls) { return ls ? g : __fadd_rn(g, d); }
 
 struct ChunkRange {
     int bin, e0, e1;
@@ -206,7 +212,7 @@ __device__ __forceinline__ uint32_t phase_c(const Tile& T, int c_begin, int c_en
                 load_d<VEC, BF16>(T.sd, T.pd + i, d);
 #pragma unroll
                 for (int k = 0; k < VEC; ++k) {
-                    float h = __fadd_rn(g[k], d[k]);
+                    float h = probe(g[k], d[k], T.ls);
                     bool sel = (VEC == 1 || i + k < cr.e1) && g[k] != 0.0f && fabsf(h) >= gm;
                     f |= (sel ? 1u : 0u) << k;
                     code[k] = (uint32_t)((i + k - bs) << 1) | (g[k] < 0.0f ? 1u : 0u);
@@ -368,7 +374,7 @@ __device__ __forceinline__ uint32_t seg_flags(const Tile& T, const SegGeo& G, in
         uint32_t nib = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float h = __fadd_rn(g[i], d[i]);
+            const float h = probe(g[i], d[i], T.ls);
             const float gm = q0 + i < G.split ? gm_lo : gm_hi;
             nib |= (g[i] != 0.0f && fabsf(h) >= gm) ? (1u << i) : 0u;
         }
@@ -1017,7 +1023,8 @@ template <bool BF16, class Release>
 __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G, int pr, int pd, const float* sr,
                                               const void* sd, uint32_t* wg, uint32_t* wc, uint32_t* cnt_tile,
                                               uint16_t* stg, uint32_t* gmax_tile, int warp, int lane,
-                                              uint16_t* pend, float s_prev, uint32_t* src, Release&& release)
+                                              uint16_t* pend, float s_prev, bool ls, uint32_t* src,
+                                              Release&& release)
 {
     const int L = ly.bin_len;
     const int bpw = ly.bpw;
@@ -1073,7 +1080,7 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
             uint32_t nzq = 0, ngq = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                ah[k][i] = fabsf(__fadd_rn(gv[i], d[i]));
+                ah[k][i] = fabsf(probe(gv[i], d[i], ls));
                 nzq |= gv[i] != 0.0f ? (1u << i) : 0u;
                 ngq |= gv[i] < 0.0f ? (1u << i) : 0u;
             }
@@ -1206,7 +1213,7 @@ __device__ __forceinline__ uint32_t tile_in_registers(const Tile& T, uint32_t* g
             uint32_t nzq = 0, ngq = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                ah[k][i] = fabsf(__fadd_rn(g[i], d[i]));
+                ah[k][i] = fabsf(probe(g[i], d[i], T.ls));
                 nzq |= g[i] != 0.0f ? (1u << i) : 0u;
                 ngq |= g[i] < 0.0f ? (1u << i) : 0u;
             }
@@ -1284,7 +1291,7 @@ __device__ __forceinline__ uint32_t tile_in_registers(const Tile& T, uint32_t* g
 template <class Release>
 __device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int pr, int pd, float* sr_s, void* sd_s,
                                         float* gbuf, uint32_t* gmax_c, uint32_t* cnt_c, uint16_t* stg, Slot& sl,
-                                        uint32_t* wsum, int tid, Release* release_p)
+                                        uint32_t* wsum, bool ls, int tid, Release* release_p)
 {
     Release& release = *release_p;
     const int lane = tid & 31, warp = tid >> 5;
@@ -1296,6 +1303,7 @@ __device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int p
     Tl.ch = min(ly.bin_len, 32 * (int)ly.vec * kRounds);
     Tl.cpb = (ly.bin_len + Tl.ch - 1) / Tl.ch;
     Tl.inv_len = ly.inv_len;
+    Tl.ls = ls;
     const bool seg = ly.bin_len >= kSeg;
     const bool one_round = seg && pr + G.tl <= kThreads * kSeg;
     const int nchunks = G.bins * Tl.cpb;
@@ -1489,12 +1497,13 @@ __global__ void __launch_bounds__(cta_threads(kNB), 2) compress_kernel(const __g
                            ((size_t)t * kWarps + warp) * 32 + lane;
                     s_prev = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(G.layer))->result.s;
                 }
+                const bool ls = g.local_selection != 0;
                 if (ly.dw_bf16)
                     cnt = warp_tile<true>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, gmax_c, warp, lane,
-                                          pend, s_prev, &src, release);
+                                          pend, s_prev, ls, &src, release);
                 else
                     cnt = warp_tile<false>(ly, G, pr, pd, stage_r(s), stage_d(s), wg, wc, cnt_c, stg, gmax_c, warp, lane,
-                                           pend, s_prev, &src, release);
+                                           pend, s_prev, ls, &src, release);
                 if (lane == 0) {
                     sl.src[warp] = src;
                     sl.cnt[warp] = cnt;
@@ -1503,8 +1512,8 @@ __global__ void __launch_bounds__(cta_threads(kNB), 2) compress_kernel(const __g
                 }
             } else {
                 if constexpr ((kPaths & 2) != 0)
-                    block_tile(ly, G, pr, pd, stage_r(s), stage_d(s), gbuf, gmax_c, cnt_c, stg, sl, ctl->wsum, tid,
-                               &release);
+                    block_tile(ly, G, pr, pd, stage_r(s), stage_d(s), gbuf, gmax_c, cnt_c, stg, sl, ctl->wsum,
+                               g.local_selection != 0, tid, &release);
             }
             if (tid == 0) {
                 sl.t = t;

@@ -138,7 +138,7 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
 // codes start (the tile's offset in the message plus the counts of the tile's bins
 // before its range), and each lane takes a contiguous run of those codes, finds the
 // bin of its first code by binary search and walks forward.
-constexpr int kAccStages = 3;
+constexpr int kAccStages = 2;
 
 __host__ __device__ inline uint32_t acc_stage_bytes(uint32_t tile_cap) { return ((tile_cap + 8) * 4 + 127) & ~127u; }
 __host__ __device__ inline uint32_t acc_pre_bytes(uint32_t max_bins)
@@ -202,19 +202,20 @@ __device__ __forceinline__ bool acc_wait(uint64_t* bar, uint32_t parity, uint64_
 }
 
 // Warp `warp` adds learner k's codes for bins [b0, b1) of tile A to the staged
-// dense tile sd (element ts + x at sd[x]). `pre` is the warp's scratch of
-// b1 - b0 + 1 entries.
-__device__ __forceinline__ void acc_learner(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
-                                            int b0, int b1, float* sd, uint32_t* pre, uint8_t* bad, int lane)
+// dense tile sd (element ts + x at sd[x]), in two parts so that the first part can
+// run while the dense tile is still loading. acc_prefix: the codes of the tile's
+// bins before b0 and the exclusive prefix of the warp's bins in `pre` (b1 - b0 + 1
+// entries); returns the warp's code count and sets *before. acc_walk: each lane
+// takes a contiguous run of the warp's codes, finds the bin of its first code by
+// binary search and walks forward.
+__device__ __forceinline__ uint32_t acc_prefix(const AccTile& A, const uint8_t* msg, int b0, int b1, uint32_t* pre,
+                                               uint32_t* before_out, int lane)
 {
-    const float s = *reinterpret_cast<const float*>(msg);
     const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + A.first_bin;
-    // codes of the tile's bins before b0
     uint32_t before = 0;
     for (int b = lane; b < b0; b += 32) before += cnt[b];
 #pragma unroll
     for (int o = 16; o; o >>= 1) before += __shfl_xor_sync(kFull, before, o);
-    // exclusive prefix of the warp's bins
     uint32_t run = 0;
     for (int c0 = b0; c0 < b1; c0 += 32) {
         const int b = c0 + lane;
@@ -230,7 +231,15 @@ __device__ __forceinline__ void acc_learner(const KLayer& ly, const AccTile& A, 
     }
     if (lane == 0) pre[b1 - b0] = run;
     __syncwarp();
-    const uint32_t total = run;
+    *before_out = before;
+    return run;
+}
+
+__device__ __forceinline__ void acc_walk(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
+                                         uint32_t before, uint32_t total, int b0, int b1, float* sd,
+                                         const uint32_t* pre, uint8_t* bad, int lane)
+{
+    const float s = *reinterpret_cast<const float*>(msg);
     const uint32_t per = (total + 31) / 32;
     uint32_t i = min(total, lane * per);
     const uint32_t iend = min(total, i + per);
@@ -263,80 +272,93 @@ __device__ __forceinline__ void acc_learner(const KLayer& ly, const AccTile& A, 
 }
 
 // Warp `warp` owns one bin of tile A (tiles of at most 8 bins): every learner's
-// codes for that bin. Lane k of a round of 32 learners fetches learner k's tile
-// offset, scale and counts at once; the codes are then prefetched for 8 learners
-// at a time (lane i holding code i of each) and added in learner order.
+// codes for that bin, learners kb .. kb + 31 per round. acc_bin_prep: lane k
+// fetches learner kb + k's tile offset, scale and counts (independent of the dense
+// tile, so it can run while that is loading). acc_bin_apply: the codes are
+// prefetched for 8 learners at a time (lane i holding code i of each) and added in
+// learner order.
 constexpr int kAccWindow = 8;
 
-__device__ __forceinline__ void acc_bin_learners(const KLayer& ly, const AccTile& A, const DecodeParams& p,
-                                                 uint8_t* ws, uint32_t T, uint32_t t, int l, int bin, float* sd,
-                                                 int lane)
+struct BinPrep {
+    unsigned long long start;  // index of the learner's first code for this bin
+    const uint8_t* codes;      // the learner's code array
+    uint32_t c;                // its codes in this bin
+    float s;                   // its scale
+};
+
+__device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile& A, const DecodeParams& p,
+                                                uint8_t* ws, uint32_t T, uint32_t t, int l, int bin, int kb,
+                                                int lane)
 {
+    BinPrep P;
+    P.start = 0;
+    P.codes = nullptr;
+    P.c = 0;
+    P.s = 0.0f;
     const int K = p.K;
+    const int k = kb + lane;
+    if (k < K) {
+        const uint64_t off = tile_offsets(ws, k, T)[t];
+        if (off != kBadOffset) {
+            const uint8_t* msg = p.msg[l * K + k];
+            const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + A.first_bin;
+            uint32_t before = 0;
+            for (int b = 0; b < bin; ++b) before += cnt[b];
+            P.c = cnt[bin];
+            P.s = *reinterpret_cast<const float*>(msg);
+            P.start = off + before;
+            P.codes = msg + 8 + 2ull * ly.nbins;
+        }
+    }
+    return P;
+}
+
+__device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A, int K, uint8_t* ws, int l, int bin,
+                                              int kb, const BinPrep& P, float* sd, int lane)
+{
     const int L = ly.bin_len;
     const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * L;
     const uint32_t len = (uint32_t)((A.first_bin + bin == ly.nbins - 1) ? last_len : L);
     float* x0 = sd + (int64_t)bin * L;
     const bool wide = ly.code_bytes == 2;
-    for (int kb = 0; kb < K; kb += 32) {
-        // lane k: where learner kb + k's codes for this bin start, how many, its scale
-        const int k = kb + lane;
-        unsigned long long start = 0;
-        uint32_t c = 0;
-        float sk = 0.0f;
-        const uint8_t* codes = nullptr;
-        if (k < K) {
-            const uint64_t off = tile_offsets(ws, k, T)[t];
-            if (off != kBadOffset) {
-                const uint8_t* msg = p.msg[l * K + k];
-                const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + A.first_bin;
-                uint32_t before = 0;
-                for (int b = 0; b < bin; ++b) before += cnt[b];
-                c = cnt[bin];
-                sk = *reinterpret_cast<const float*>(msg);
-                start = off + before;
-                codes = msg + 8 + 2ull * ly.nbins;
-            }
+    const int kn = min(32, K - kb);
+    for (int k0 = 0; k0 < kn; k0 += kAccWindow) {
+        uint32_t cw[kAccWindow];
+#pragma unroll
+        for (int w = 0; w < kAccWindow; ++w) {
+            const int kk = min(k0 + w, kn - 1);
+            const uint32_t ck = __shfl_sync(kFull, P.c, kk);
+            const unsigned long long st = __shfl_sync(kFull, P.start, kk);
+            const uint8_t* cp = reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)P.codes, kk));
+            cw[w] = 0xffffffffu;
+            if (k0 + w < kn && (uint32_t)lane < ck)
+                cw[w] = wide ? reinterpret_cast<const uint16_t*>(cp)[st + lane] : cp[st + lane];
         }
-        const int kn = min(32, K - kb);
-        for (int k0 = 0; k0 < kn; k0 += kAccWindow) {
-            uint32_t cw[kAccWindow];
 #pragma unroll
-            for (int w = 0; w < kAccWindow; ++w) {
-                const int kk = min(k0 + w, kn - 1);
-                const uint32_t ck = __shfl_sync(kFull, c, kk);
-                const unsigned long long st = __shfl_sync(kFull, start, kk);
-                const uint8_t* cp = reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)codes, kk));
-                cw[w] = 0xffffffffu;
-                if (k0 + w < kn && (uint32_t)lane < ck)
-                    cw[w] = wide ? reinterpret_cast<const uint16_t*>(cp)[st + lane] : cp[st + lane];
+        for (int w = 0; w < kAccWindow; ++w) {
+            if (k0 + w >= kn) break;
+            const int kk = k0 + w;
+            const uint32_t ck = __shfl_sync(kFull, P.c, kk);
+            const float s = __shfl_sync(kFull, P.s, kk);
+            bool bad = false;
+            if (cw[w] != 0xffffffffu) {
+                const uint32_t o = cw[w] >> 1;
+                if (o < len) x0[o] = __fadd_rn(x0[o], (cw[w] & 1u) ? -s : s);
+                else bad = true;
             }
-#pragma unroll
-            for (int w = 0; w < kAccWindow; ++w) {
-                if (k0 + w >= kn) break;
-                const int kk = k0 + w;
-                const uint32_t ck = __shfl_sync(kFull, c, kk);
-                const float s = __shfl_sync(kFull, sk, kk);
-                bool bad = false;
-                if (cw[w] != 0xffffffffu) {
-                    const uint32_t o = cw[w] >> 1;
-                    if (o < len) x0[o] = __fadd_rn(x0[o], (cw[w] & 1u) ? -s : s);
+            if (ck > 32u) {  // more codes than lanes in this bin: the rest, in rounds
+                const unsigned long long st = __shfl_sync(kFull, P.start, kk);
+                const uint8_t* cp =
+                    reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)P.codes, kk));
+                for (uint32_t i = 32 + lane; i < ck; i += 32) {
+                    const uint32_t code = wide ? reinterpret_cast<const uint16_t*>(cp)[st + i] : cp[st + i];
+                    const uint32_t o = code >> 1;
+                    if (o < len) x0[o] = __fadd_rn(x0[o], (code & 1u) ? -s : s);
                     else bad = true;
                 }
-                if (ck > 32u) {  // more codes than lanes in this bin: the rest, in rounds
-                    const unsigned long long st = __shfl_sync(kFull, start, kk);
-                    const uint8_t* cp =
-                        reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)codes, kk));
-                    for (uint32_t i = 32 + lane; i < ck; i += 32) {
-                        const uint32_t code = wide ? reinterpret_cast<const uint16_t*>(cp)[st + i] : cp[st + i];
-                        const uint32_t o = code >> 1;
-                        if (o < len) x0[o] = __fadd_rn(x0[o], (code & 1u) ? -s : s);
-                        else bad = true;
-                    }
-                }
-                if (bad) ws[16 + l * K + kb + kk] = 1;  // offset outside its bin: ignored, message flagged
-                __syncwarp();  // learner kk's additions come before learner kk + 1's
             }
+            if (bad) ws[16 + l * K + kb + kk] = 1;  // offset outside its bin: ignored, message flagged
+            __syncwarp();  // learner kk's additions come before learner kk + 1's
         }
     }
 }
@@ -371,23 +393,42 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         const uint32_t t = G0 + (uint32_t)i * GS;
         if (t >= T) break;
         float* st = stage(i);
+        const AccTile A = acc_tile(g, t);
+        const KLayer& ly = g.layer[A.layer];
+        const int l = A.layer;
+        const int bpw = (A.bins + kDecThreads / 32 - 1) / (kDecThreads / 32);
+        const int b0 = min(A.bins, warp * bpw), b1 = min(A.bins, b0 + bpw);
+        // the first learners' offsets and counts do not depend on the dense tile:
+        // fetch them while its copy is in flight
+        BinPrep bp;
+        uint64_t off0 = kBadOffset;
+        uint32_t before0 = 0, total0 = 0;
+        if (bpw == 1) {
+            if (b0 < b1) bp = acc_bin_prep(ly, A, p, ws, T, t, l, b0, 0, lane);
+        } else if (b0 < b1) {
+            off0 = tile_offsets(ws, 0, T)[t];
+            if (off0 != kBadOffset) total0 = acc_prefix(A, p.msg[l * K], b0, b1, pre, &before0, lane);
+        }
         if (!__syncthreads_and(acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u, g.timeout_ns))) {
             poisoned = true;
             break;
         }
-        const AccTile A = acc_tile(g, t);
-        const KLayer& ly = g.layer[A.layer];
-        const int l = A.layer;
         float* sd = st + (A.ts - A.a0);  // element ts + x at sd[x]
-        const int bpw = (A.bins + kDecThreads / 32 - 1) / (kDecThreads / 32);
-        const int b0 = min(A.bins, warp * bpw), b1 = min(A.bins, b0 + bpw);
         if (bpw == 1) {
-            if (b0 < b1) acc_bin_learners(ly, A, p, ws, T, t, l, b0, sd, lane);
+            if (b0 < b1) {
+                for (int kb = 0; kb < K; kb += 32) {
+                    if (kb) bp = acc_bin_prep(ly, A, p, ws, T, t, l, b0, kb, lane);
+                    acc_bin_apply(ly, A, K, ws, l, b0, kb, bp, sd, lane);
+                }
+            }
         } else if (b0 < b1) {
             for (int k = 0; k < K; ++k) {
-                const uint64_t off = tile_offsets(ws, k, T)[t];
+                const uint64_t off = k ? tile_offsets(ws, k, T)[t] : off0;
                 if (off == kBadOffset) continue;
-                acc_learner(ly, A, p.msg[l * K + k], off, b0, b1, sd, pre, ws + 16 + l * K + k, lane);
+                const uint8_t* msg = p.msg[l * K + k];
+                uint32_t before = before0, total = total0;
+                if (k) total = acc_prefix(A, msg, b0, b1, pre, &before, lane);
+                acc_walk(ly, A, msg, off, before, total, b0, b1, sd, pre, ws + 16 + l * K + k, lane);
             }
         }
 

@@ -37,6 +37,8 @@ def test_hand_cases(case):
     else:
         dw_t = torch.from_numpy(dw).cuda()
     layer = GpuLayer(residue.size, case["bin_len"], dtype_code(dw_t))
+    if case.get("local_selection"):
+        ac.adacomp_set_selection_rule(layer.h, ac.RULE_LOCAL_SELECTION)
     msg, s = layer.step(res_t, dw_t)
     exp = case["expect"]
     assert msg.tobytes() == hex_bytes(exp["msg_hex"]).tobytes()

@@ -19,7 +19,8 @@ def test_compress_matches_hand_derivation(case):
     residue, dw = case_inputs(case)
     exp = case["expect"]
     r = oracle.compress(residue, dw, case["bin_len"],
-                        literal_zero_select=case.get("literal_zero_select", False))
+                        literal_zero_select=case.get("literal_zero_select", False),
+                        local_selection=case.get("local_selection", False))
     assert r.msg.tobytes() == hex_bytes(exp["msg_hex"]).tobytes()
     assert np.float32(r.s).view(np.uint32) == np.float32(fval(exp["s"])).view(np.uint32)
     assert r.sel.astype(int).tolist() == exp["sel"]

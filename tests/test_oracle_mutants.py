@@ -33,6 +33,7 @@ MUTANTS = {
     "gmax_ignores_partial_bin": ("for (int64_t j = lo; j < hi; ++j)\n            if (fabsf(G[j]) > m)",
                                  "for (int64_t j = lo; j < hi && hi - lo == L; ++j)\n            if (fabsf(G[j]) > m)"),
     "bf16_truncated_to_15_bits": ("(uint32_t)h << 16", "((uint32_t)h << 16) & 0xfffeffffu"),
+    "local_selection_keeps_probe": ("if (local_selection) H[j] = G[j];", "if (local_selection) H[j] = H[j];"),
     "big_endian_count": ("put_u16(counts + 2 * b, cnt);",
                          "put_u16(counts + 2 * b, ((cnt & 0xff) << 8) | (cnt >> 8));"),
 }
@@ -55,7 +56,8 @@ def _golden_pins(lib):
         residue, dw = case_inputs(case)
         exp = case["expect"]
         r = oracle.compress(residue, dw, case["bin_len"],
-                            literal_zero_select=case.get("literal_zero_select", False), lib=lib)
+                            literal_zero_select=case.get("literal_zero_select", False), lib=lib,
+                            local_selection=case.get("local_selection", False))
         assert r.msg.tobytes() == hex_bytes(exp["msg_hex"]).tobytes(), case["name"]
         assert np.float32(r.s) == np.float32(fval(exp["s"])), case["name"]
         assert np.array_equal(residue, f32_array(exp["residue"])), case["name"]
