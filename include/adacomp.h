@@ -226,6 +226,26 @@ adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile
 /* Bound on each device-side wait, in nanoseconds (default 2e9). */
 adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns);
 
+/* Decode fused with one momentum-SGD step (the optimisers the learners use:
+ * "AdaComp (Adaptive Residual Gradient Compression)", Claims > Application
+ * #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers; the update rule
+ * itself is not on the pages and is read as the usual heavy-ball form without
+ * dampening). For each element j of each layer, with g_j the learners' codes summed
+ * from zero exactly as adacomp_decode_accumulate sums them (learner order, fp32):
+ *     v_j = fl32( fl32(mu * v_j) + fl32(grad_scale * g_j) )
+ *     w_j = fl32( w_j - fl32(lr * v_j) )
+ * (no fused multiply-add). weights and momentum are fp32[n] per layer, in/out,
+ * 16-byte aligned; grad_scale = 1/K averages instead of summing. The gradient is
+ * never written to global memory: it lives only in the tile being updated. Same
+ * messages, workspace and error reporting as adacomp_decode_accumulate (a rejected
+ * message contributes nothing). */
+adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, int32_t K, float* weights,
+                                  float* momentum, float lr, float mu, float grad_scale, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream);
+adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
+                                        float* const* weights, float* const* momentum, float lr, float mu,
+                                        float grad_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
+
 /* Selection rule. ADACOMP_RULE_ADACOMP (the default) sends an element when
  * G != 0 and |fl32(G + dW)| >= g_max of its bin ("AdaComp (Adaptive Residual
  * Gradient Compression)", Claims > Mechanism

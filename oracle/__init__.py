@@ -53,6 +53,9 @@ class Oracle:
         lib.adacomp_oracle_compress.restype = ctypes.c_int
         lib.adacomp_oracle_decode_accumulate.argtypes = [i64, i32, vp, i32, vp]
         lib.adacomp_oracle_decode_accumulate.restype = ctypes.c_int
+        f32 = ctypes.c_float
+        lib.adacomp_oracle_decode_sgd.argtypes = [i64, i32, vp, i32, vp, vp, f32, f32, f32]
+        lib.adacomp_oracle_decode_sgd.restype = ctypes.c_int
         self.lib = lib
 
 
@@ -131,3 +134,14 @@ def decode_accumulate(n: int, bin_len: int, msgs, dense: np.ndarray, lib=None) -
     bufs = [np.ascontiguousarray(m, dtype=np.uint8) for m in msgs]
     arr = (ctypes.c_void_p * len(bufs))(*[b.ctypes.data for b in bufs])
     return int(lib.adacomp_oracle_decode_accumulate(n, bin_len, arr, len(bufs), _ptr(dense)))
+
+
+def decode_sgd(n: int, bin_len: int, msgs, w: np.ndarray, v: np.ndarray, lr: float, mu: float,
+               scale: float = 1.0, lib=None) -> int:
+    """Decodes the messages into a zero gradient and applies one momentum-SGD step to
+    ``w`` and ``v`` (fp32, in place). Returns the oracle status."""
+    lib = lib or _load()
+    assert w.dtype == np.float32 and v.dtype == np.float32 and w.size == n and v.size == n
+    arrs = [np.ascontiguousarray(m, dtype=np.uint8) for m in msgs]
+    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
+    return lib.adacomp_oracle_decode_sgd(n, bin_len, ptrs, len(arrs), _ptr(w), _ptr(v), lr, mu, scale)

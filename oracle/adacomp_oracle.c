@@ -256,3 +256,31 @@ int adacomp_oracle_decode_accumulate(int64_t n, int32_t L, const uint8_t *const 
     }
     return ORACLE_OK;
 }
+
+/*
+ * Decode K messages into the aggregated gradient g (a zero-filled fp32 buffer,
+ * learners in order, exactly as adacomp_oracle_decode_accumulate) and apply one
+ * momentum-SGD step to weights w and momentum v (the optimiser of the entry's
+ * Claims > Application #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers;
+ * the rule is read as the heavy-ball form without dampening):
+ *     v = fl32(fl32(mu * v) + fl32(scale * g));   w = fl32(w - fl32(lr * v)).
+ * A malformed message rejects the call and leaves w and v untouched.
+ */
+int adacomp_oracle_decode_sgd(int64_t n, int32_t L, const uint8_t *const *msgs, int32_t K, float *w, float *v,
+                              float lr, float mu, float scale)
+{
+    if (n < 1 || !w || !v) return ORACLE_ERR_ARG;
+    float *g = (float *)calloc((size_t)n, sizeof(float));
+    if (!g) return ORACLE_ERR_ARG;
+    int rc = adacomp_oracle_decode_accumulate(n, L, msgs, K, g);
+    if (rc != ORACLE_OK) { free(g); return rc; }
+    for (int64_t j = 0; j < n; ++j) {
+        float momentum = mu * v[j];
+        float step = scale * g[j];
+        v[j] = momentum + step;
+        float delta = lr * v[j];
+        w[j] = w[j] - delta;
+    }
+    free(g);
+    return ORACLE_OK;
+}

@@ -60,6 +60,9 @@ def lib() -> ctypes.CDLL:
         L.adacomp_set_fault_injection.argtypes = [vp, ctypes.c_uint32]
         L.adacomp_set_lazy_fixup.argtypes = [vp, i32, P(sz)]
         L.adacomp_set_selection_rule.argtypes = [vp, i32]
+        f32 = ctypes.c_float
+        L.adacomp_decode_sgd.argtypes = [vp, P(vp), i32, vp, vp, f32, f32, f32, vp, sz, vp]
+        L.adacomp_decode_sgd_group.argtypes = [vp, P(vp), i32, P(vp), P(vp), f32, f32, f32, vp, sz, vp]
         L.adacomp_materialize.argtypes = [vp, vp, vp, sz, vp]
         L.adacomp_materialize_group.argtypes = [vp, P(vp), vp, sz, vp]
         L.adacomp_free.argtypes = [vp]
@@ -71,7 +74,7 @@ def lib() -> ctypes.CDLL:
                      "adacomp_decode_accumulate_group", "adacomp_query", "adacomp_decode_status",
                      "adacomp_set_timeout_ns", "adacomp_set_timing_events",
                      "adacomp_set_fault_injection", "adacomp_set_lazy_fixup", "adacomp_set_selection_rule",
-                     "adacomp_materialize",
+                     "adacomp_materialize", "adacomp_decode_sgd", "adacomp_decode_sgd_group",
                      "adacomp_materialize_group"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
@@ -203,6 +206,26 @@ def adacomp_set_timing_events(h: Handle, before=None, mid=None, after=None):
 def adacomp_set_fault_injection(h: Handle, skip_tile: int = 0xFFFFFFFF):
     """Test hook: the given tile never publishes, so its successors time out."""
     _check(lib().adacomp_set_fault_injection(h.ptr, skip_tile), "adacomp_set_fault_injection")
+
+
+def adacomp_decode_sgd(h: Handle, msgs, weights, momentum, lr: float, mu: float, ws, grad_scale: float = 1.0,
+                       stream=None):
+    K = len(msgs)
+    arr = (ctypes.c_void_p * K)(*[_ptr(m) for m in msgs])
+    _check(lib().adacomp_decode_sgd(h.ptr, arr, K, _ptr(weights), _ptr(momentum), lr, mu, grad_scale, _ptr(ws),
+                                    _nbytes(ws), _stream(stream)), "adacomp_decode_sgd")
+
+
+def adacomp_decode_sgd_group(h: Handle, msgs, weights, momentum, lr: float, mu: float, ws,
+                             grad_scale: float = 1.0, stream=None):
+    """msgs: per layer a list of K messages (layer-major, as adacomp_decode_accumulate_group)."""
+    L = h.num_layers
+    K = len(msgs[0])
+    arr = (ctypes.c_void_p * (L * K))(*[_ptr(m) for layer in msgs for m in layer])
+    VP = ctypes.c_void_p * L
+    _check(lib().adacomp_decode_sgd_group(h.ptr, arr, K, VP(*[_ptr(w) for w in weights]),
+                                          VP(*[_ptr(v) for v in momentum]), lr, mu, grad_scale, _ptr(ws),
+                                          _nbytes(ws), _stream(stream)), "adacomp_decode_sgd_group")
 
 
 def adacomp_set_selection_rule(h: Handle, rule: int):

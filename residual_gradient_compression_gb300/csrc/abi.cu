@@ -165,8 +165,13 @@ adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* d
     return adacomp_compress_group(h, &residue, &dW, &msg, &msg_capacity, ws, ws_bytes, stream);
 }
 
-adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
-                                               float* const* dense, void* ws, size_t ws_bytes, cudaStream_t stream)
+}  // extern "C"
+
+namespace {
+// Shared by the plain decode (mom == nullptr) and the fused momentum-SGD decode.
+adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, int32_t K, float* const* dense,
+                            float* const* mom, float lr, float mu, float scale, void* ws, size_t ws_bytes,
+                            cudaStream_t stream)
 {
     if (!h || !msgs || !dense || !ws) return ADACOMP_ERR_INVALID_ARG;
     const int64_t L = (int64_t)h->layers.size();
@@ -181,11 +186,16 @@ adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* co
     std::memset(p, 0, sizeof *p);
     fill_group(h, g);
     p->K = K;
+    p->sgd = mom ? 1 : 0;
+    p->lr = lr;
+    p->mu = mu;
+    p->scale = scale;
     adacomp_status st = ADACOMP_OK;
     for (int64_t l = 0; l < L && st == ADACOMP_OK; ++l) {
-        if (!dense[l]) st = ADACOMP_ERR_INVALID_ARG;
-        else if (!aligned(dense[l], 16)) st = ADACOMP_ERR_ALIGNMENT;
+        if (!dense[l] || (mom && !mom[l])) st = ADACOMP_ERR_INVALID_ARG;
+        else if (!aligned(dense[l], 16) || (mom && !aligned(mom[l], 16))) st = ADACOMP_ERR_ALIGNMENT;
         p->dense[l] = dense[l];
+        if (mom) p->mom[l] = mom[l];
         for (int32_t k = 0; k < K && st == ADACOMP_OK; ++k) {
             const void* m = msgs[l * K + k];
             if (!m) st = ADACOMP_ERR_INVALID_ARG;
@@ -197,6 +207,32 @@ adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* co
     delete g;
     delete p;
     return st;
+}
+}  // namespace
+
+extern "C" {
+
+adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
+                                               float* const* dense, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    return decode_group(h, msgs, K, dense, nullptr, 0.0f, 0.0f, 1.0f, ws, ws_bytes, stream);
+}
+
+adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
+                                        float* const* weights, float* const* momentum, float lr, float mu,
+                                        float grad_scale, void* ws, size_t ws_bytes, cudaStream_t stream)
+{
+    if (!momentum) return ADACOMP_ERR_INVALID_ARG;
+    return decode_group(h, msgs, K, weights, momentum, lr, mu, grad_scale, ws, ws_bytes, stream);
+}
+
+adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, int32_t K, float* weights,
+                                  float* momentum, float lr, float mu, float grad_scale, void* ws, size_t ws_bytes,
+                                  cudaStream_t stream)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
+    return adacomp_decode_sgd_group(h, msgs, K, &weights, &momentum, lr, mu, grad_scale, ws, ws_bytes, stream);
 }
 
 adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs, int32_t K, float* dense,

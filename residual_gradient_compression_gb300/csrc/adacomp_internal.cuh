@@ -160,8 +160,11 @@ constexpr uint32_t kErrTimeout = 1;
 
 struct DecodeParams {
     const uint8_t* msg[kMaxDecodePairs];  // [layer * K + k]
-    float* dense[kMaxGroup];
+    float* dense[kMaxGroup];              // the dense sum, or the weights when sgd != 0
+    float* mom[kMaxGroup];                // momentum buffers (sgd != 0)
     int32_t K;
+    int32_t sgd;                          // fused momentum-SGD step instead of a plain sum
+    float lr, mu, scale;                  // w -= lr * v, v = mu * v + scale * g
     int32_t pad;
 };
 

@@ -140,14 +140,20 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
 // bin of its first code by binary search and walks forward.
 constexpr int kAccStages = 2;
 
-__host__ __device__ inline uint32_t acc_stage_bytes(uint32_t tile_cap) { return ((tile_cap + 8) * 4 + 127) & ~127u; }
+// One tile-sized fp32 array of a stage; a stage holds one (the dense tile) or three
+// (the summed gradient g, the weights w and the momentum v, for the fused SGD step).
+__host__ __device__ inline uint32_t acc_array_bytes(uint32_t tile_cap) { return ((tile_cap + 8) * 4 + 127) & ~127u; }
+__host__ __device__ inline uint32_t acc_stage_bytes(uint32_t tile_cap, bool sgd = false)
+{
+    return (sgd ? 3u : 1u) * acc_array_bytes(tile_cap);
+}
 __host__ __device__ inline uint32_t acc_pre_bytes(uint32_t max_bins)
 {
     return (uint32_t)(kDecThreads / 32) * ((max_bins + 8) / 8 + 2) * 4;
 }
-__host__ __device__ inline uint32_t acc_smem_bytes(uint32_t tile_cap, uint32_t max_bins)
+__host__ __device__ inline uint32_t acc_smem_bytes(uint32_t tile_cap, uint32_t max_bins, bool sgd = false)
 {
-    return kAccStages * acc_stage_bytes(tile_cap) + ((acc_pre_bytes(max_bins) + 127) & ~127u) + 128;
+    return kAccStages * acc_stage_bytes(tile_cap, sgd) + ((acc_pre_bytes(max_bins) + 127) & ~127u) + 128;
 }
 
 struct AccTile {
@@ -174,20 +180,31 @@ __device__ __forceinline__ AccTile acc_tile(const KGroup& g, uint32_t t)
 // Thread 0: start tile t's dense slice into a stage. The copy ends at the 16-byte
 // boundary at or after the tile unless that lies past the array, in which case the
 // last few elements are loaded with plain loads.
-__device__ void acc_issue(const KGroup& g, const DecodeParams& p, uint32_t t, float* st, uint64_t* bar)
+// (For the fused SGD step the weights and the momentum are loaded into the stage's
+// second and third arrays; the first, the gradient sum, is zeroed by the threads.)
+template <bool kSGD>
+__device__ void acc_issue(const KGroup& g, const DecodeParams& p, uint32_t t, float* st, uint32_t arr_floats,
+                          uint64_t* bar)
 {
     const AccTile A = acc_tile(g, t);
-    const float* dense = p.dense[A.layer];
     const int64_t n = g.layer[A.layer].n;
     int64_t a1 = (A.te + 3) & ~(int64_t)3;
     if (a1 > n) a1 = A.te & ~(int64_t)3;
-    if (a1 < A.te) {
-        for (int64_t j = max(a1, A.ts); j < A.te; ++j) st[j - A.a0] = dense[j];
-        ptx::fence_proxy_async_smem();
-    }
     const uint32_t bytes = a1 > A.a0 ? (uint32_t)(a1 - A.a0) * 4u : 0u;
-    ptx::mbar_arrive_expect_tx(bar, bytes);
-    if (bytes) ptx::bulk_g2s(st, dense + A.a0, bytes, bar);
+    const int na = kSGD ? 2 : 1;
+    for (int a = 0; a < na; ++a) {
+        const float* src = kSGD ? (a ? p.mom[A.layer] : p.dense[A.layer]) : p.dense[A.layer];
+        float* dst = st + (kSGD ? (size_t)(a + 1) * arr_floats : 0);
+        for (int64_t j = max(a1, A.ts); j < A.te; ++j) dst[j - A.a0] = src[j];
+    }
+    if (a1 < A.te) ptx::fence_proxy_async_smem();
+    ptx::mbar_arrive_expect_tx(bar, bytes * na);
+    if (bytes) {
+        for (int a = 0; a < na; ++a) {
+            const float* src = kSGD ? (a ? p.mom[A.layer] : p.dense[A.layer]) : p.dense[A.layer];
+            ptx::bulk_g2s(st + (kSGD ? (size_t)(a + 1) * arr_floats : 0), src + A.a0, bytes, bar);
+        }
+    }
 }
 
 __device__ __forceinline__ bool acc_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns)
@@ -363,11 +380,16 @@ __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A
     }
 }
 
+// kSGD: the learners' codes are summed into a zeroed gradient tile g, and one
+// momentum-SGD step is applied to the weights w and momentum v while the tile is in
+// shared memory: v = fl32(fl32(mu * v) + fl32(scale * g)), w = fl32(w - fl32(lr * v)).
+template <bool kSGD>
 __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_constant__ KGroup g,
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
     extern __shared__ __align__(128) uint8_t smem[];
-    const uint32_t stage_bytes = acc_stage_bytes(g.tile_cap);
+    const uint32_t stage_bytes = acc_stage_bytes(g.tile_cap, kSGD);
+    const uint32_t arr_floats = acc_array_bytes(g.tile_cap) / 4;
     float* stage0 = reinterpret_cast<float*>(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int pre_len = (g.max_bins + 8) / 8 + 2;
@@ -383,7 +405,7 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         for (int k = 0; k < kAccStages; ++k) ptx::mbar_init(&bar[k], 1);
         ptx::fence_mbar_init();
         for (int i = 0; i < kAccStages - 1; ++i)
-            if (G0 + (uint32_t)i * GS < T) acc_issue(g, p, G0 + (uint32_t)i * GS, stage(i), &bar[i]);
+            if (G0 + (uint32_t)i * GS < T) acc_issue<kSGD>(g, p, G0 + (uint32_t)i * GS, stage(i), arr_floats, &bar[i]);
     }
     __syncthreads();
 
@@ -400,6 +422,10 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         const int b0 = min(A.bins, warp * bpw), b1 = min(A.bins, b0 + bpw);
         // the first learners' offsets and counts do not depend on the dense tile:
         // fetch them while its copy is in flight
+        if constexpr (kSGD) {  // the gradient sum starts at zero (the array no copy targets)
+            float4* z = reinterpret_cast<float4*>(st);
+            for (int64_t q = tid; q < (A.te - A.a0 + 3) / 4; q += kDecThreads) z[q] = make_float4(0.f, 0.f, 0.f, 0.f);
+        }
         BinPrep bp;
         uint64_t off0 = kBadOffset;
         uint32_t before0 = 0, total0 = 0;
@@ -432,28 +458,49 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
             }
         }
 
-        // write back: ends by the threads, the aligned interior by one bulk store
-        const int64_t c0 = (A.ts + 3) & ~(int64_t)3, c1 = A.te & ~(int64_t)3;
-        float* dense = p.dense[l];
         __syncthreads();
-        if (c1 > c0) {
-            if (tid < 8) {
-                const int64_t j = tid < 4 ? A.ts + tid : c1 + (tid - 4);
-                if ((tid < 4 && j < c0) || (tid >= 4 && j < A.te)) dense[j] = st[j - A.a0];
+        if constexpr (kSGD) {  // the optimiser step on the tile
+            float* gs = st;
+            float* wv = st + arr_floats;
+            float* vv = st + 2 * (size_t)arr_floats;
+            for (int64_t x = (A.ts - A.a0) + tid; x < A.te - A.a0; x += kDecThreads) {
+                const float v = __fadd_rn(__fmul_rn(p.mu, vv[x]), __fmul_rn(p.scale, gs[x]));
+                vv[x] = v;
+                wv[x] = __fsub_rn(wv[x], __fmul_rn(p.lr, v));
             }
-        } else {
-            for (int64_t j = A.ts + tid; j < A.te; j += kDecThreads) dense[j] = st[j - A.a0];
+            __syncthreads();
+        }
+        // write back: ends by the threads, the aligned interior by one bulk store per array
+        const int64_t c0 = (A.ts + 3) & ~(int64_t)3, c1 = A.te & ~(int64_t)3;
+        const int na = kSGD ? 2 : 1;
+        for (int a = 0; a < na; ++a) {
+            float* dst = (kSGD && a) ? p.mom[l] : p.dense[l];
+            const float* src = st + (kSGD ? (size_t)(a + 1) * arr_floats : 0);
+            if (c1 > c0) {
+                if (tid < 8) {
+                    const int64_t j = tid < 4 ? A.ts + tid : c1 + (tid - 4);
+                    if ((tid < 4 && j < c0) || (tid >= 4 && j < A.te)) dst[j] = src[j - A.a0];
+                }
+            } else {
+                for (int64_t j = A.ts + tid; j < A.te; j += kDecThreads) dst[j] = src[j - A.a0];
+            }
         }
         ptx::fence_proxy_async_smem();  // the threads' shared writes, before the bulk store reads them
         __syncthreads();
         if (tid == 0) {
-            if (c1 > c0) ptx::bulk_s2g(dense + c0, st + (c0 - A.a0), (uint32_t)(c1 - c0) * 4u);
+            if (c1 > c0) {
+                for (int a = 0; a < na; ++a) {
+                    float* dst = (kSGD && a) ? p.mom[l] : p.dense[l];
+                    const float* src = st + (kSGD ? (size_t)(a + 1) * arr_floats : 0);
+                    ptx::bulk_s2g(dst + c0, src + (c0 - A.a0), (uint32_t)(c1 - c0) * 4u);
+                }
+            }
             ptx::bulk_commit();
             // refill the stage whose store was committed one tile ago
             const uint32_t tn = t + (uint32_t)(kAccStages - 1) * GS;
             if (tn < T) {
                 asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                acc_issue(g, p, tn, stage(i + kAccStages - 1), &bar[(i + kAccStages - 1) % kAccStages]);
+                acc_issue<kSGD>(g, p, tn, stage(i + kAccStages - 1), arr_floats, &bar[(i + kAccStages - 1) % kAccStages]);
             }
         }
     }
@@ -476,7 +523,7 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
 
 struct DecDeviceInfo {
     int sms = 0;
-    uint32_t smem_set = 0;
+    uint32_t smem_set[2] = {0, 0};  // per accumulate kernel (plain sum, fused SGD)
 };
 DecDeviceInfo g_ddev[64];
 
@@ -504,21 +551,23 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     tile_scan_kernel<<<(unsigned)(g.num_layers * p.K), 1024, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins);
-    if (smem > di.smem_set) {
+    const bool sgd = p.sgd != 0;
+    const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins, sgd);
+    void (*kern)(KGroup, DecodeParams, uint8_t*) = sgd ? accumulate_kernel<true> : accumulate_kernel<false>;
+    if (smem > di.smem_set[sgd]) {
         if (smem > 48 * 1024) {
-            e = cudaFuncSetAttribute(accumulate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
         }
-        di.smem_set = smem;
+        di.smem_set[sgd] = smem;
     }
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, accumulate_kernel, kDecThreads, smem);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecThreads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const long long cap = (long long)di.sms * occ;
     const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
-    accumulate_kernel<<<grid, kDecThreads, smem, stream>>>(g, p, w);
+    kern<<<grid, kDecThreads, smem, stream>>>(g, p, w);
     return cudaGetLastError();
 }
 

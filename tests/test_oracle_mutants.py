@@ -34,6 +34,7 @@ MUTANTS = {
                                  "for (int64_t j = lo; j < hi && hi - lo == L; ++j)\n            if (fabsf(G[j]) > m)"),
     "bf16_truncated_to_15_bits": ("(uint32_t)h << 16", "((uint32_t)h << 16) & 0xfffeffffu"),
     "local_selection_keeps_probe": ("if (local_selection) H[j] = G[j];", "if (local_selection) H[j] = H[j];"),
+    "sgd_steps_with_old_momentum": ("float delta = lr * v[j];", "float delta = lr * (v[j] - step);"),
     "big_endian_count": ("put_u16(counts + 2 * b, cnt);",
                          "put_u16(counts + 2 * b, ((cnt & 0xff) << 8) | (cnt >> 8));"),
 }
@@ -65,6 +66,11 @@ def _golden_pins(lib):
             dense = np.zeros(residue.size, np.float32)
             oracle.decode_accumulate(residue.size, case["bin_len"], [r.msg], dense, lib=lib)
             assert np.array_equal(dense, f32_array(exp["decode_into_zeros"])), case["name"]
+    case = load("hand_decode_sgd")
+    w, v = f32_array(case["w_in"]), f32_array(case["v_in"])
+    oracle.decode_sgd(case["n"], case["bin_len"], [hex_bytes(case["msg_hex"])], w, v, case["lr"], case["mu"],
+                      case["scale"], lib=lib)
+    assert np.array_equal(w, f32_array(case["expect_w"])) and np.array_equal(v, f32_array(case["expect_v"]))
     case = load("hand_decode_learner_order")
     dense = f32_array(case["dense_in"])
     oracle.decode_accumulate(case["n"], case["bin_len"], [hex_bytes(h) for h in case["msgs_hex"]],
