@@ -54,6 +54,7 @@ def parse_args():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-e2e", action="store_true")
     p.add_argument("--no-lazy", action="store_true", help="skip the deferred fix-up measurement")
+    p.add_argument("--no-sgd", action="store_true", help="skip the fused decode + SGD measurement")
     p.add_argument("--min-timed-seconds", type=float, default=1.5,
                    help="repeat the K timed steps until the clock sampler has covered this long")
     return p.parse_args()
@@ -444,7 +445,55 @@ def run_device(args, rank, world):
         out["e2e"] = run_e2e(args, run, layers, sp, world)
     if not args.no_lazy:
         out["lazy_fixup"] = run_lazy(args, run, sp, world, n_elems)
+    if not args.no_sgd:
+        out["decode_sgd"] = run_decode_sgd(args, run, sp, world, layers, res[-1])
     return out, run
+
+
+def run_decode_sgd(args, run, sp, world, layers, step_res):
+    """The decode fused with one momentum-SGD step (adacomp_decode_sgd_group) on the
+    last timed step's messages: weights and momentum read and written once (16 B per
+    element) instead of a dense sum plus a separate optimiser pass."""
+    ac, ct = run.ac, run.ct
+    numels = [l.numel for l in layers]
+    w_buf, w_views = _flat_views(numels, torch.float32, run.dev)
+    v_buf, v_views = _flat_views(numels, torch.float32, run.dev)
+    w_buf.normal_()
+    VP = ct.c_void_p
+    c_w = [(VP * len(g))(*[w_views[i].data_ptr() for i in g]) for g in run.gidx]
+    c_v = [(VP * len(g))(*[v_views[i].data_ptr() for i in g]) for g in run.gidx]
+    stream = torch.cuda.current_stream()
+
+    def once():
+        for gi, h in enumerate(run.h):
+            st = run.L.adacomp_decode_sgd_group(h.ptr, run.c_dec_msgs[gi], run.K, c_w[gi], c_v[gi],
+                                                ct.c_float(1e-3), ct.c_float(0.9), ct.c_float(1.0 / run.K),
+                                                run.dec_ws[gi].data_ptr(), run.dec_ws[gi].numel(), sp)
+            if st:
+                raise RuntimeError(f"adacomp_decode_sgd_group: {st}")
+
+    for _ in range(3):
+        once()
+    start, end = _new_events(2)
+    reps, t0 = [], time.perf_counter()
+    while True:
+        barrier(world)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for _ in range(args.steps):
+            once()
+        end.record(stream)
+        torch.cuda.synchronize()
+        reps.append(start.elapsed_time(end) / args.steps)
+        if time.perf_counter() - t0 >= args.min_timed_seconds / 3 or len(reps) >= 200:
+            break
+    ms = max_over_ranks(sorted(reps)[len(reps) // 2], world)
+    msg_bytes = sum(r[1] for r in step_res)
+    bins = sum(-(-l.numel // l.bin_len) for l in layers) * run.K
+    algo = 16 * sum(numels) + msg_bytes + 2 * bins
+    del w_buf, v_buf
+    return {"ms_per_decode": ms, "algorithmic_bytes": algo, "achieved_gbs": algo / (ms * 1e-3) / 1e9,
+            "optimizer": "momentum SGD, lr 1e-3, mu 0.9, grad_scale 1/K"}
 
 
 def run_lazy(args, run, sp, world, n_elems):
@@ -515,12 +564,14 @@ def run_e2e(args, run, layers, sp, world):
         d2h += sum(len(g) for g in run.gidx) * 2112 * run.K
         j = 0
         for k in range(run.K):
+            # one copy per learner: from the first message to the end of the last one
+            # (the buffer holds every layer's message at a fixed offset)
+            end = 0
             for li in range(len(layers)):
-                mb = res[j][1]
-                o = msg_offs[k][li]
-                host_msg[k][o:o + mb].copy_(run.msg[k][0][o:o + mb], non_blocking=True)
-                d2h += mb
+                end = max(end, msg_offs[k][li] + res[j][1])
                 j += 1
+            host_msg[k][:end].copy_(run.msg[k][0][:end], non_blocking=True)
+            d2h += end
     torch.cuda.synchronize()
     secs = max_over_ranks(time.perf_counter() - t0, world)
     n_elems = sum(numels) * run.K
