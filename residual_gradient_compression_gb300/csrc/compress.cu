@@ -1037,16 +1037,26 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
     const int rel0 = max(e_first, we0) - we0;
     const int bin_lo = active ? (int)__umulhi((uint32_t)rel0, ly.inv_len) : 0;  // warp-relative bin
     const int split = (bin_lo + 1) * L - (e_first - we0);  // first slot of bin_lo + 1
+    const uint32_t lomask = split >= kSeg ? 0xffffu : ((1u << max(split, 0)) - 1u);  // slots of bin_lo
     const int rot = seg_rot(lane);
-    float ah[4][4];
-    uint32_t nz = 0, ng = 0;
-    uint32_t nzr = 0;  // G != 0 in register order (bit 4k + i)
+    // Register order: chunk k of the lane (4 slots) is held at registers 4k..4k+3 and
+    // is slot chunk k ^ rot, so bit 4k + i of a register-order mask is slot
+    // 4 (k ^ rot) + i. Every per-element test below uses a compile-time bit.
+    uint32_t vr = 0, lor = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int q0 = 4 * (k ^ rot);
+        vr |= ((valid >> q0) & 0xfu) << (4 * k);
+        lor |= ((lomask >> q0) & 0xfu) << (4 * k);
+    }
+    lor &= vr;
+    float ah[4][4];            // |probe| per register slot
+    uint32_t nzr = 0, ngr = 0;  // G != 0, G < 0 (register order)
     float m_lo = 0.0f, m_hi = 0.0f;
     // deferred fix-up of the previous call: the residue of the slots it sent still
     // holds G; the correction fl32(G - sign(G) s_prev) is applied as they are loaded
     const uint32_t pm = pend ? (uint32_t)*pend : 0u;
     if (active) {
-        const bool edge = valid != 0xffffu;
         const float* rs = sr + pr + e_first;
         float* gres = ly.residue + G.ts + e_first;
 #pragma unroll
@@ -1071,24 +1081,21 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
             gv[1] = __fadd_rn(r.y, d[1]);
             gv[2] = __fadd_rn(r.z, d[2]);
             gv[3] = __fadd_rn(r.w, d[3]);
-            const uint32_t vq = (valid >> q0) & 0xfu;
-            if (edge) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i)
-                    if (!((vq >> i) & 1u)) gv[i] = 0.0f;
-            }
-            uint32_t nzq = 0, ngq = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
+                const uint32_t bit = 1u << (4 * k + i);
+                if (!(vr & bit)) gv[i] = 0.0f;  // a slot outside the warp's bins
                 ah[k][i] = fabsf(probe(gv[i], d[i], ls));
-                nzq |= gv[i] != 0.0f ? (1u << i) : 0u;
-                ngq |= gv[i] < 0.0f ? (1u << i) : 0u;
+                nzr |= gv[i] != 0.0f ? bit : 0u;
+                ngr |= gv[i] < 0.0f ? bit : 0u;
+                const float a = fabsf(gv[i]);
+                const bool lo = (lor & bit) != 0u;
+                m_lo = fmaxf(m_lo, lo ? a : 0.0f);
+                m_hi = fmaxf(m_hi, lo ? 0.0f : a);
             }
-            nz |= nzq << q0;
-            ng |= ngq << q0;
-            nzr |= nzq << (4 * k);
             // residue := G (sent elements are corrected by the fix-up kernel, or by the
             // next call when the fix-up is deferred)
+            const uint32_t vq = (vr >> (4 * k)) & 0xfu;
             float* gp = gres + q0;
             if (vq == 0xfu) {
                 *reinterpret_cast<float4*>(gp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
@@ -1097,18 +1104,6 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
                 for (int i = 0; i < 4; ++i)
                     if ((vq >> i) & 1u) gp[i] = gv[i];
             }
-            const float cm = fmaxf(fmaxf(fabsf(gv[0]), fabsf(gv[1])), fmaxf(fabsf(gv[2]), fabsf(gv[3])));
-            if (q0 + 4 <= split) {
-                m_lo = fmaxf(m_lo, cm);
-            } else if (q0 >= split) {
-                m_hi = fmaxf(m_hi, cm);
-            } else {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    if (q0 + i < split) m_lo = fmaxf(m_lo, fabsf(gv[i]));
-                    else m_hi = fmaxf(m_hi, fabsf(gv[i]));
-                }
-            }
         }
     }
     __syncwarp();
@@ -1116,30 +1111,26 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
     if (m_lo > 0.0f) atomicMax(&wg[bin_lo], __float_as_uint(m_lo));
     if (m_hi > 0.0f) atomicMax(&wg[bin_lo + 1], __float_as_uint(m_hi));
     __syncwarp();
-    uint32_t f = 0, fr = 0;  // sent slots, in slot order and in register order
+    uint32_t fr = 0;  // sent slots, register order
     if (active) {
         const float gm_lo = __uint_as_float(wg[bin_lo]);
-        const float gm_hi = split < kSeg ? __uint_as_float(wg[bin_lo + 1]) : 0.0f;
+        const float gm_hi = lomask != 0xffffu ? __uint_as_float(wg[bin_lo + 1]) : 0.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
-            const int q0 = 4 * (k ^ rot);
-            uint32_t nib = 0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                nib |= ah[k][i] >= (q0 + i < split ? gm_lo : gm_hi) ? (1u << i) : 0u;
-            f |= nib << q0;
-            fr |= nib << (4 * k);
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t bit = 1u << (4 * k + i);
+                fr |= ah[k][i] >= ((lor & bit) ? gm_lo : gm_hi) ? bit : 0u;
+            }
         }
-        f &= nz;
         fr &= nzr;
-        const uint32_t lomask = split >= kSeg ? 0xffffu : ((1u << max(split, 0)) - 1u);
-        const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
+        const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & ~lor);
         if (c_lo) atomicAdd(&wc[bin_lo], c_lo);
         if (c_hi) atomicAdd(&wc[bin_lo + 1], c_hi);
     }
     __syncwarp();
     {
-        // per bin of the slice: count to the tile's array, maximum to the buckets; scratch back to zero
+        // per bin of the slice: count and maximum to the tile's arrays; scratch back to zero
         const int nb = wb1 - wb0;
         if (lane < nb) {
             cnt_tile[wb0 + lane] = wc[lane];
@@ -1147,6 +1138,14 @@ __device__ __forceinline__ uint32_t warp_tile(const KLayer& ly, const TileGeo& G
         }
         wg[lane] = 0u;
         wc[lane] = 0u;
+    }
+    // codes are emitted in slot order: bring the sent and sign masks back to it
+    uint32_t f = 0, ng = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int q0 = 4 * (k ^ rot);
+        f |= ((fr >> (4 * k)) & 0xfu) << q0;
+        ng |= ((ngr >> (4 * k)) & 0xfu) << q0;
     }
     const uint32_t c = __popc(f);
     uint32_t incl = c;
