@@ -104,7 +104,7 @@ void fill_group(const adacomp_layer* h, KGroup* g)
     g->lazy = h->lazy ? 1u : 0u;
     g->local_selection = h->rule == ADACOMP_RULE_LOCAL_SELECTION ? 1u : 0u;
     for (const KLayer& k : h->layers)
-        if (k.bin_len < 16 || (uint64_t)k.bins_per_tile * k.bin_len + 3 > 4096) g->needs_gbuf = 1;
+        if (k.bin_len < 16) g->needs_gbuf = 1;  // the short-bin path stages G in shared memory
     for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];
 }
 

@@ -55,7 +55,7 @@ struct KGroup {
     uint16_t d_size;         // 4 if any layer has fp32 dW, else 2
     uint64_t timeout_ns;
     uint32_t inject_skip_tile;  // fault injection for tests: this tile never publishes (~0u: none)
-    uint32_t needs_gbuf;        // some tile is processed through shared memory (short bins or > 4096 slots)
+    uint32_t needs_gbuf;        // some layer has bins shorter than 16 (G staged in shared memory)
     uint32_t lazy;              // deferred fix-up for warp-sliced layers (pending masks in the workspace)
     uint32_t local_selection;   // selection rule: 0 AdaComp (abs(G + dW) >= g_max), 1 Local Selection (abs(G) >= g_max)
 };
@@ -81,7 +81,7 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
     p.layer_bytes = num_layers * 64u;                        // copy of the layer table
     p.g_bytes = needs_gbuf ? p.r_bytes : 0u;
     p.total = 2 * (p.r_bytes + p.d_bytes) + p.layer_bytes + p.g_bytes + nbuf * p.stg_bytes + 2 * p.bin_bytes +
-              nbuf * kHistBytesPerBuffer + kWarpScratchBytes + 2048 + 640;
+              nbuf * kHistBytesPerBuffer + kWarpScratchBytes + 2048 + 1152;
     return p;
 }
 

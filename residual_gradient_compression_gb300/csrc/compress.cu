@@ -122,7 +122,7 @@ __device__ __forceinline__ void load_d(const void* sd, int id, float (&d)[VEC])
 struct Tile {
     float* gres;    // global residue at the element held in shared slot 0 (tile start - pr)
     const float* sr;  // residue slice; element i at sr[pr + i]
-    float* gs;        // G, same slot layout as sr (a buffer the bulk copies never target)
+    float* gs;        // G for bins shorter than 16 (a buffer the bulk copies never target)
     const void* sd; // dW slice; element i at sd[pd + i]
     int pr, pd;
     int tl;         // elements in the tile
@@ -295,10 +295,9 @@ __device__ __forceinline__ void seg_load_d(const Tile& T, int s, int q, float (&
     }
 }
 
-// Phase A, segment path: G = residue + dW over the slots, written to the G buffer
-// (for phase C) and to the residue in global memory; bin maxima. *mine gets
-// the geometry of segment `tid` (the thread's only segment when the tile fits one
-// round).
+// Phase A, segment path: G = residue + dW over the slots, written to the residue
+// in global memory; bin maxima. (Phase C forms G again from the stage, which is not
+// released before it.) *mine gets the geometry of segment `tid`.
 template <bool BF16>
 __device__ __forceinline__ void phase_a_seg(const Tile& T, uint32_t* gmax_s, int tid, SegGeo* mine)
 {
@@ -309,7 +308,6 @@ __device__ __forceinline__ void phase_a_seg(const Tile& T, uint32_t* gmax_s, int
         if (s == tid) *mine = G;
         const bool edge = G.valid != 0xffffu;
         const float* rs = T.sr + s * kSeg;
-        float* gsp = T.gs + s * kSeg;
         float m_lo = 0.0f, m_hi = 0.0f;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
@@ -329,7 +327,6 @@ __device__ __forceinline__ void phase_a_seg(const Tile& T, uint32_t* gmax_s, int
                 for (int i = 0; i < 4; ++i)
                     if (!((vq >> i) & 1u)) g[i] = 0.0f;
             }
-            *reinterpret_cast<float4*>(gsp + q0) = make_float4(g[0], g[1], g[2], g[3]);
             // residue := G in global memory (sent elements are corrected by the fix-up kernel)
             float* gp = T.gres + s * kSeg + q0;
             if (vq == 0xfu) {
@@ -356,61 +353,68 @@ __device__ __forceinline__ void phase_a_seg(const Tile& T, uint32_t* gmax_s, int
     }
 }
 
-// Flags of one segment's 16 slots (bit idx): G != 0 && |fl32(G + dW)| >= g_max.
+// Flags of one segment's 16 slots (bit idx): G != 0 && |probe| >= g_max, with G
+// formed again from the stage (the same fp32 addition as in phase A); *ng_out gets
+// the slots with G < 0. Slots outside the tile are never flagged.
 template <bool BF16>
 __device__ __forceinline__ uint32_t seg_flags(const Tile& T, const SegGeo& G, int s, int rot, float gm_lo,
-                                              float gm_hi)
+                                              float gm_hi, uint32_t* ng_out)
 {
-    const float* rs = T.gs + s * kSeg;
-    uint32_t f = 0;
+    const float* rs = T.sr + s * kSeg;
+    uint32_t f = 0, ng = 0;
 #pragma unroll
     for (int k = 0; k < 4; ++k) {
         const int q = k ^ rot;
         const int q0 = 4 * q;
-        const float4 gv = *reinterpret_cast<const float4*>(rs + q0);
-        const float g[4] = {gv.x, gv.y, gv.z, gv.w};
+        const float4 r = *reinterpret_cast<const float4*>(rs + q0);
         float d[4];
         seg_load_d<BF16>(T, s, q, d);
-        uint32_t nib = 0;
+        const float g[4] = {__fadd_rn(r.x, d[0]), __fadd_rn(r.y, d[1]), __fadd_rn(r.z, d[2]), __fadd_rn(r.w, d[3])};
+        uint32_t nib = 0, neg = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const float h = probe(g[i], d[i], T.ls);
             const float gm = q0 + i < G.split ? gm_lo : gm_hi;
             nib |= (g[i] != 0.0f && fabsf(h) >= gm) ? (1u << i) : 0u;
+            neg |= g[i] < 0.0f ? (1u << i) : 0u;
         }
         f |= nib << q0;
+        ng |= neg << q0;
     }
-    return f;
+    *ng_out = ng;
+    return f & G.valid;
 }
 
-// Phase C, segment path: flags and codes per slot, per-bin counts, and a block-wide
-// exclusive scan of the per-segment counts (in element order) that places every
-// code at stg[rank]. For tiles of several rounds. Runs on the 256 compute threads
-// (named barrier 1). Returns the tile's code count (same value in every thread).
+// Phase C, segment path: flags and codes per slot and per-bin counts. Round r of the
+// 256 threads covers segments [256 r, 256 r + 256); each warp ranks its own codes of
+// a round with a warp scan and stages them at stg[wbase + rank], wbase being the
+// tile element of the warp's first segment in that round (a warp never has more
+// codes than elements, so the runs stay disjoint), and records the run in run_src /
+// run_cnt at index 8 r + warp. No barrier among the compute warps. Returns the
+// number of runs (8 per round).
 template <bool BF16>
-__device__ __forceinline__ uint32_t phase_c_seg(const Tile& T, const uint32_t* gmax_s, uint32_t* cnt_s,
-                                                uint16_t* stg, uint32_t* wsum, int tid)
+__device__ __forceinline__ int phase_c_seg(const Tile& T, const uint32_t* gmax_s, uint32_t* cnt_s, uint16_t* stg,
+                                           uint32_t* run_src, uint32_t* run_cnt, int tid)
 {
     const int nseg = (T.pr + T.tl + kSeg - 1) / kSeg;
     const int rot = seg_rot(tid);
     const int lane = tid & 31, warp = tid >> 5;
-    uint32_t carry = 0;
-    for (int base = 0; base < nseg; base += kThreads) {
+    int r = 0;
+    for (int base = 0; base < nseg; base += kThreads, ++r) {
         const int s = base + tid;
-        uint32_t f = 0;
+        uint32_t f = 0, ng = 0;
         SegGeo G;
         G.valid = 0; G.bin_lo = 0; G.split = kSeg; G.off_lo = 0; G.e0 = 0;
         if (s < nseg) {
             G = seg_geo(T, s);
             const float gm_lo = __uint_as_float(gmax_s[G.bin_lo]);
             const float gm_hi = G.split < kSeg ? __uint_as_float(gmax_s[G.bin_lo + 1]) : 0.0f;
-            f = seg_flags<BF16>(T, G, s, rot, gm_lo, gm_hi);
+            f = seg_flags<BF16>(T, G, s, rot, gm_lo, gm_hi, &ng);
             const uint32_t lomask = G.split >= kSeg ? 0xffffu : ((1u << max(G.split, 0)) - 1u);
             const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
             if (c_lo) atomicAdd(&cnt_s[G.bin_lo], c_lo);
             if (c_hi) atomicAdd(&cnt_s[G.bin_lo + 1], c_hi);
         }
-        // block-wide exclusive scan of the per-thread counts
         const uint32_t c = __popc(f);
         uint32_t incl = c;
 #pragma unroll
@@ -418,72 +422,20 @@ __device__ __forceinline__ uint32_t phase_c_seg(const Tile& T, const uint32_t* g
             const uint32_t y = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += y;
         }
-        if (lane == 31) wsum[warp] = incl;
-        asm volatile("bar.sync %0, %1;" ::"n"(1), "n"(kThreads) : "memory");
-        uint32_t woff = 0, tot = 0;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) {
-            const uint32_t v = wsum[w];
-            woff += w < warp ? v : 0u;
-            tot += v;
+        const int wbase = max(kSeg * (base + 32 * warp) - T.pr, 0);
+        if (lane == 31) {
+            run_src[8 * r + warp] = (uint32_t)wbase;
+            run_cnt[8 * r + warp] = incl;
         }
-        uint32_t pos = carry + woff + incl - c;
-        const float* rs = T.gs + s * kSeg;
+        uint32_t pos = (uint32_t)wbase + incl - c;
         while (f) {
             const int idx = __ffs(f) - 1;
             f &= f - 1;
             const int off = G.off_lo + idx - (idx < G.split ? 0 : T.L);
-            stg[pos++] = (uint16_t)(((uint32_t)off << 1) | (rs[idx] < 0.0f ? 1u : 0u));
+            stg[pos++] = (uint16_t)(((uint32_t)off << 1) | ((ng >> idx) & 1u));
         }
-        carry += tot;
-        asm volatile("bar.sync %0, %1;" ::"n"(1), "n"(kThreads) : "memory");  // wsum reuse
     }
-    return carry;
-}
-
-// Phase C, segment path, for tiles of one round (at most 256 segments, one per
-// thread, whose geometry phase A computed): flags per slot and per-bin counts; each
-// warp then ranks its own codes (shuffle scan of the per-thread counts) and stages
-// them at stg[wbase + rank], wbase being the first tile element of the warp's
-// segments (a warp never has more codes than elements, so the warps' ranges stay
-// disjoint). Only the sent slots are visited when the codes are written. Returns
-// the warp's code count.
-template <bool BF16>
-__device__ __forceinline__ uint32_t phase_c_seg_warp(const Tile& T, const SegGeo& G, const uint32_t* gmax_s,
-                                                     uint32_t* cnt_s, uint16_t* stg, int tid, int* wbase_out)
-{
-    const int nseg = (T.pr + T.tl + kSeg - 1) / kSeg;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int s = tid;
-    uint32_t f = 0;
-    if (s < nseg) {
-        const float gm_lo = __uint_as_float(gmax_s[G.bin_lo]);
-        const float gm_hi = G.split < kSeg ? __uint_as_float(gmax_s[G.bin_lo + 1]) : 0.0f;
-        f = seg_flags<BF16>(T, G, s, seg_rot(tid), gm_lo, gm_hi);
-        const uint32_t lomask = G.split >= kSeg ? 0xffffu : ((1u << max(G.split, 0)) - 1u);
-        const uint32_t c_lo = __popc(f & lomask), c_hi = __popc(f & ~lomask);
-        if (c_lo) atomicAdd(&cnt_s[G.bin_lo], c_lo);
-        if (c_hi) atomicAdd(&cnt_s[G.bin_lo + 1], c_hi);
-    }
-    const uint32_t c = __popc(f);
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    const uint32_t total = __shfl_sync(kFull, incl, 31);
-    const int wbase = max(kSeg * 32 * warp - T.pr, 0);
-    uint32_t pos = (uint32_t)wbase + incl - c;
-    const float* rs = T.gs + s * kSeg;
-    while (f) {
-        const int idx = __ffs(f) - 1;
-        f &= f - 1;
-        const int off = G.off_lo + idx - (idx < G.split ? 0 : T.L);
-        stg[pos++] = (uint16_t)(((uint32_t)off << 1) | (rs[idx] < 0.0f ? 1u : 0u));
-    }
-    *wbase_out = wbase;
-    return total;
+    return 8 * r;
 }
 
 // ---------------------------------------------------------------- exact scale sum
@@ -747,10 +699,11 @@ __host__ __device__ constexpr int cta_threads(int nb) { return kThreads + 32 * n
 constexpr int kBarCompute = 1;
 constexpr uint32_t kEndTile = 0xffffffffu;
 
+constexpr int kMaxRuns = 24;  // code runs of a tile: 8 warps x at most 3 rounds of 256 segments
 struct Slot {
     uint32_t t, layer, first_bin, bins;
     uint32_t nrun, pad0, pad1, pad2;
-    uint32_t src[kWarps], cnt[kWarps];  // code runs: staging offset and length, in message order
+    uint32_t src[kMaxRuns], cnt[kMaxRuns];  // code runs: staging offset and length, in message order
 };
 
 // Shared-memory control block of the compress kernel.
@@ -766,7 +719,7 @@ struct Ctrl {
     uint32_t wsum[kWarps];    // block scan scratch
     Slot slot[kMaxBuffers];
 };
-static_assert(sizeof(Ctrl) <= 640, "control block exceeds its shared-memory allowance");
+static_assert(sizeof(Ctrl) <= 1152, "control block exceeds its shared-memory allowance");
 
 template <int ID, int N>
 __device__ __forceinline__ void bar_sync() { asm volatile("bar.sync %0, %1;" ::"n"(ID), "n"(N) : "memory"); }
@@ -1341,15 +1294,11 @@ __device__ __noinline__ void block_tile(const KLayer& ly, const TileGeo G, int p
                 sl.cnt[warp] = wt;
                 if (warp == 0) sl.nrun = kWarps;
             }
-        } else {  // several rounds: block-wide scan (ends with a barrier)
-            uint32_t total;
-            if (ly.dw_bf16) total = phase_c_seg<true>(Tl, gmax_c, cnt_c, stg, wsum, tid);
-            else total = phase_c_seg<false>(Tl, gmax_c, cnt_c, stg, wsum, tid);
-            if (tid == 0) {
-                sl.nrun = 1;
-                sl.src[0] = 0;
-                sl.cnt[0] = total;
-            }
+        } else {  // several rounds: one code run per warp and round
+            int nrun;
+            if (ly.dw_bf16) nrun = phase_c_seg<true>(Tl, gmax_c, cnt_c, stg, sl.src, sl.cnt, tid);
+            else nrun = phase_c_seg<false>(Tl, gmax_c, cnt_c, stg, sl.src, sl.cnt, tid);
+            if (tid == 0) sl.nrun = (uint32_t)nrun;
         }
         compute_sync();  // phase C was the last reader of the stage
         release();
