@@ -34,6 +34,21 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 size_t max_msg_bytes(const KLayer& l) { return 8 + 2 * (size_t)l.nbins + (size_t)l.code_bytes * (size_t)l.n; }
 
+// Every layer warp-sliced: the sliced path and its workspace layout.
+bool handle_is_sliced(const adacomp_layer* h)
+{
+    for (const KLayer& k : h->layers)
+        if (!k.bpw) return false;
+    return !h->layers.empty();
+}
+
+size_t compress_ws_for(const adacomp_layer* h)
+{
+    const int nl = (int)h->layers.size();
+    return handle_is_sliced(h) ? adacomp::sliced_ws_bytes(nl, h->total_tiles)
+                               : adacomp::compress_ws_bytes(nl, h->total_tiles, h->lazy);
+}
+
 adacomp_status make_group(adacomp_layer_t* out, int32_t num_layers, const int64_t* n, const int32_t* bin_len,
                           const int32_t* dtype, size_t* max_msg, size_t* cws, size_t* dws)
 {
@@ -83,7 +98,7 @@ adacomp_status make_group(adacomp_layer_t* out, int32_t num_layers, const int64_
     }
     if (tiles >= (1ull << 31)) { delete h; return ADACOMP_ERR_INVALID_ARG; }
     h->total_tiles = (uint32_t)tiles;
-    h->compress_ws = adacomp::compress_ws_bytes(num_layers, tiles);
+    h->compress_ws = compress_ws_for(h);
     h->decode_per_learner = adacomp::decode_per_learner(tiles);
     if (cws) *cws = h->compress_ws;
     if (dws) *dws = h->decode_per_learner;
@@ -307,7 +322,7 @@ adacomp_status adacomp_set_lazy_fixup(adacomp_layer_t h, int32_t enable, size_t*
 {
     if (!h) return ADACOMP_ERR_INVALID_ARG;
     h->lazy = enable != 0;
-    h->compress_ws = adacomp::compress_ws_bytes((int)h->layers.size(), h->total_tiles, h->lazy);
+    h->compress_ws = compress_ws_for(h);
     if (compress_ws_bytes) *compress_ws_bytes = h->compress_ws;
     return ADACOMP_OK;
 }

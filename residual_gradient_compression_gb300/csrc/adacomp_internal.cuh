@@ -92,7 +92,8 @@ __host__ __device__ inline SmemPlan smem_plan(uint32_t tile_cap, uint32_t d_size
 struct Ctl {
     uint32_t epoch;      // epoch of the last completed call (0: none); a call uses epoch % 255 + 1
     uint32_t fin_done;   // finalise blocks done with this call (the last one advances epoch)
-    uint32_t reserved[14];
+    uint32_t pending;    // sliced path: the sent masks hold corrections a deferred fix-up left to the next call
+    uint32_t reserved[13];
 };
 
 struct Result {              // written by each call, kept for adacomp_query
@@ -126,6 +127,29 @@ __host__ __device__ inline size_t ws_pend_offset(int num_layers, uint64_t total_
 __host__ __device__ inline size_t compress_ws_bytes(int num_layers, uint64_t total_tiles, bool lazy = false)
 {
     return ws_pend_offset(num_layers, total_tiles) + (lazy ? kPendBytesPerTile * (size_t)total_tiles : 0);
+}
+
+// Compress workspace of a launch group whose layers are all warp-sliced (the
+// sliced path: 16 <= L_T <= 509, no look-back):
+// [Ctl][LayerWs x num_layers][tile code offset u64 x T][tile code total u32 x T, padded to 16 B]
+// [per-warp code count u32 x 8 x T][sent mask u16 x 256 x T][sign mask u16 x 256 x T].
+// A mask word belongs to compute lane (warp w, lane) of a tile: bit i is slot i of
+// the lane's 16 consecutive slots. The tile totals are zero between calls; the
+// other arrays are written by each call before they are read.
+constexpr size_t kMaskBytesPerTile = kWarps * 32 * 2;
+__host__ __device__ inline size_t sl_excl_offset(int num_layers) { return ws_desc_offset(num_layers); }
+__host__ __device__ inline size_t sl_tot_offset(int num_layers, uint64_t T) { return sl_excl_offset(num_layers) + 8 * (size_t)T; }
+__host__ __device__ inline size_t sl_wcnt_offset(int num_layers, uint64_t T)
+{
+    return sl_tot_offset(num_layers, T) + ((4 * (size_t)T + 15) & ~(size_t)15);
+}
+__host__ __device__ inline size_t sl_sent_offset(int num_layers, uint64_t T) { return sl_wcnt_offset(num_layers, T) + 4 * kWarps * (size_t)T; }
+__host__ __device__ inline size_t sl_sign_offset(int num_layers, uint64_t T) { return sl_sent_offset(num_layers, T) + kMaskBytesPerTile * (size_t)T; }
+__host__ __device__ inline size_t sliced_ws_bytes(int num_layers, uint64_t T) { return sl_sign_offset(num_layers, T) + kMaskBytesPerTile * (size_t)T; }
+// Bytes at the start of a workspace that must be zero before its first call.
+__host__ __device__ inline size_t ws_zero_prefix(int num_layers, uint64_t T, bool sliced)
+{
+    return sliced ? sl_wcnt_offset(num_layers, T) : ws_desc_offset(num_layers) + 8 * (size_t)T;
 }
 
 // Look-back descriptor: flag in bits 62..63, the call's epoch in bits 54..61, value
@@ -173,6 +197,11 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
                             cudaEvent_t ev_mid = nullptr, cudaEvent_t ev_after = nullptr);
 cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cudaStream_t stream);
 cudaError_t launch_materialize(const KGroup& g, void* ws, cudaStream_t stream);
+// The sliced path (every layer of the group warp-sliced).
+bool group_is_sliced(const KGroup& g);
+cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t stream, cudaEvent_t ev_before,
+                                   cudaEvent_t ev_mid, cudaEvent_t ev_after);
+cudaError_t launch_materialize_sliced(const KGroup& g, void* ws, cudaStream_t stream);
 }  // namespace adacomp
 
 struct adacomp_layer;

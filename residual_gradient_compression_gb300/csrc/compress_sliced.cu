@@ -1,0 +1,730 @@
+// AdaComp compression for launch groups whose layers all have 16 <= L_T <= 509
+// (every conv and FC/LSTM layer of the usual configurations): the sliced path.
+//
+// Method: "AdaComp (Adaptive Residual Gradient Compression)", Claims > Mechanism
+// #r629-local-bin-soft-threshold-and-mean-gmax-quantization (Algorithm 2 restated):
+// G = residue + dW, H = G + dW, g_max(i) = max |G| over bin i, s = mean g_max, send
+// |H| >= g_max(i) as sign(G) * s, residue = G - G_q (sent) or G (kept). Code widths:
+// Claims > Application #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers.
+//
+// Three launches, none of which waits on another CTA:
+//   slice_kernel     streams residue and dW once. A tile is eight warp slices of
+//                    floor(509 / L_T) whole bins; every warp runs its own pipeline of
+//                    bulk copies (cp.async.bulk into per-warp shared-memory stages,
+//                    completion on per-warp mbarriers). Per slice: G, residue := G,
+//                    bin maxima (exact, into exponent buckets), the selection masks
+//                    (which do not depend on s), the per-bin counts, written straight
+//                    into the message, and the warp's code count. The codes' positions
+//                    are not needed yet, so no CTA ever waits for another.
+//   slice_finalize   one CTA per layer: s from the exact sum, the header, and the
+//                    exclusive prefix of the tile code totals.
+//   slice_emit       one warp per (tile, slice), last tiles first: the codes from the
+//                    masks, written at their final positions, and the fix-up
+//                    residue = fl32(G - sign(G) s) of every sent element (skipped when
+//                    the fix-up is deferred to the next call).
+// Only two masks (2 bits per element) pass between the first and the last launch.
+#include "adacomp_internal.cuh"
+#include "compress_common.cuh"
+
+#include <cuda_bf16.h>
+
+namespace adacomp {
+namespace {
+
+constexpr int kSlots = 512;              // slots of a warp slice: 16 per lane
+constexpr int kBkLo = 96, kBkN = 64;     // per-warp exponent buckets: biased exponents [96, 160)
+constexpr uint32_t kRBytes = kSlots * 4;  // residue stage
+constexpr uint32_t kDBytes32 = kSlots * 4;
+constexpr uint32_t kDBytes16 = 1152;      // bf16 dW stage: up to 520 elements from the 16-byte boundary before slot 0
+
+struct SlicePlan {
+    uint32_t d_bytes, stage_bytes, stages_bytes, layer_bytes, total;
+};
+__host__ __device__ inline SlicePlan slice_plan(uint32_t d_size, int stages, int num_layers)
+{
+    SlicePlan p;
+    p.d_bytes = d_size == 4 ? kDBytes32 : kDBytes16;
+    p.stage_bytes = kRBytes + p.d_bytes;
+    p.stages_bytes = kWarps * stages * p.stage_bytes;
+    p.layer_bytes = (uint32_t)num_layers * 64u;
+    p.total = p.stages_bytes + p.layer_bytes + kWarpScratchBytes + kWarps * kBkN * 8 + kWarps * stages * 8;
+    return p;
+}
+
+// One warp slice: bins [wb0, wb0 + nb) of tile t, elements [we0, we1) of the tile.
+struct Slice {
+    int layer;
+    int64_t ts;          // first element of the tile (index in its layer)
+    uint32_t first_bin;  // first bin of the tile
+    int wb0, nb;         // first bin of the slice (tile-relative) and its bin count
+    int we0, we1;        // slice elements, tile-relative
+    int64_t a0;          // layer element held by slot 0 of lane 0: the 16-byte boundary at or before ts + we0
+};
+
+// Slice w of tile t of layer `layer` (whose descriptor is ly).
+__device__ __forceinline__ Slice slice_in(const KLayer& ly, int layer, uint32_t t, int w)
+{
+    Slice S;
+    S.layer = layer;
+    S.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+    const int bins = (int)min(ly.bins_per_tile, ly.nbins - S.first_bin);
+    S.ts = (int64_t)S.first_bin * ly.bin_len;
+    const int tl = (int)min((int64_t)bins * ly.bin_len, ly.n - S.ts);
+    S.wb0 = min(bins, w * (int)ly.bpw);
+    const int wb1 = min(bins, S.wb0 + (int)ly.bpw);
+    S.nb = wb1 - S.wb0;
+    S.we0 = S.wb0 * ly.bin_len;
+    S.we1 = min(wb1 * ly.bin_len, tl);
+    S.a0 = (S.ts + S.we0) & ~(int64_t)3;
+    return S;
+}
+
+// Layer of tile t >= the first tile of layer l (tiles of a warp only move forward).
+__device__ __forceinline__ int advance_layer(const KLayer* lays, int num_layers, uint32_t t, int l)
+{
+    while (l + 1 < num_layers && lays[l + 1].tile_begin <= t) ++l;
+    return l;
+}
+
+// Layer of tile t from a shared-memory array of the layers' first tiles.
+__device__ __forceinline__ int layer_of_tile(const uint32_t* tb, int num_layers, uint32_t t)
+{
+    int lo = 0, hi = num_layers - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (tb[mid] <= t) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// Starts slice S's data into a stage (run by one lane): bulk copies of the
+// 16-byte-aligned spans covering the slice, from the boundary at or before its
+// first element (slot 0 of lane 0) to the one at or after its last; only at the
+// end of the layer's arrays are the last few elements loaded with plain loads.
+// The spans never exceed 512 slots: the slice has at most 509 elements. Returns
+// false when nothing was copied (an empty slice: the phase completes at once).
+__device__ bool issue_slice(const KLayer& ly, const Slice& S, float* rb, void* db, uint64_t* bar)
+{
+    if (S.we1 <= S.we0) {
+        ptx::mbar_arrive(bar);
+        return false;
+    }
+    const int64_t e0 = S.ts + S.we0, e1 = S.ts + S.we1;
+    const int64_t a0 = S.a0;
+    int64_t a1 = (e1 + 3) & ~(int64_t)3;
+    if (a1 > ly.n) a1 = e1 & ~(int64_t)3;
+    const uint32_t rbytes = (uint32_t)(a1 - a0) * 4u;
+    int64_t b0 = a0, b1 = a1;
+    uint32_t dbytes = rbytes;
+    if (ly.dw_bf16) {
+        b0 = e0 & ~(int64_t)7;
+        b1 = (e1 + 7) & ~(int64_t)7;
+        if (b1 > ly.n) b1 = e1 & ~(int64_t)7;
+        dbytes = (uint32_t)(b1 - b0) * 2u;
+    }
+    if (a1 < e1 || b1 < e1) {
+        for (int64_t j = max(a1, e0); j < e1; ++j) rb[j - a0] = ly.residue[j];
+        if (ly.dw_bf16) {
+            for (int64_t j = max(b1, e0); j < e1; ++j)
+                static_cast<uint16_t*>(db)[j - b0] = static_cast<const uint16_t*>(ly.dw)[j];
+        } else {
+            for (int64_t j = max(b1, e0); j < e1; ++j) static_cast<float*>(db)[j - a0] = static_cast<const float*>(ly.dw)[j];
+        }
+        ptx::fence_proxy_async_smem();  // before later bulk copies refill these bytes
+    }
+    ptx::mbar_arrive_expect_tx(bar, rbytes + dbytes);
+    if (rbytes) ptx::bulk_g2s(rb, ly.residue + a0, rbytes, bar);
+    if (dbytes) ptx::bulk_g2s(db, static_cast<const uint8_t*>(ly.dw) + b0 * (ly.dw_bf16 ? 2 : 4), dbytes, bar);
+    return true;
+}
+
+// Bounded wait on an mbarrier phase, the thread sleeping in the barrier between
+// checks of the time limit.
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uint64_t timeout_ns)
+{
+    uint64_t start = 0;
+    while (!ptx::mbar_try_wait_sleep(bar, parity, 20000u)) {
+        const uint64_t now = ptx::globaltimer();
+        if (start == 0) start = now;
+        else if (now - start > timeout_ns) return false;
+    }
+    return true;
+}
+
+// Geometry of one lane's 16 slots within its slice (shared by the streaming and
+// the emitting kernels): slot i holds tile element lane_e + i.
+struct LaneGeo {
+    int lane_e;        // tile element of slot 0
+    uint32_t valid;    // slots holding elements of the slice (slot order)
+    int bin_lo;        // slice-relative bin of the first valid slot
+    int split;         // first slot of bin_lo + 1
+};
+__device__ __forceinline__ LaneGeo lane_geo(const Slice& S, const KLayer& ly, int lane)
+{
+    LaneGeo q;
+    q.lane_e = (int)(S.a0 - S.ts) + kSeg * lane;
+    const bool active = S.we1 > S.we0 && q.lane_e + kSeg > S.we0 && q.lane_e < S.we1;
+    const int vlo = max(0, S.we0 - q.lane_e), vhi = min(kSeg, S.we1 - q.lane_e);
+    q.valid = (active && vhi > vlo) ? (((1u << (vhi - vlo)) - 1u) << vlo) : 0u;
+    const int rel0 = max(q.lane_e, S.we0) - S.we0;  // < 512, so umulhi divides exactly
+    q.bin_lo = q.valid ? (int)__umulhi((uint32_t)rel0, ly.inv_len) : 0;
+    q.split = (q.bin_lo + 1) * ly.bin_len - (q.lane_e - S.we0);
+    return q;
+}
+
+// Slot-order mask <-> register order: register chunk k holds slot chunk k ^ rot.
+__device__ __forceinline__ uint32_t to_reg_order(uint32_t m, int rot)
+{
+    uint32_t r = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) r |= ((m >> (4 * (k ^ rot))) & 0xfu) << (4 * k);
+    return r;
+}
+__device__ __forceinline__ uint32_t to_slot_order(uint32_t r, int rot)
+{
+    uint32_t m = 0;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) m |= ((r >> (4 * k)) & 0xfu) << (4 * (k ^ rot));
+    return m;
+}
+
+// ---------------------------------------------------------------- streaming kernel
+// Warp w of CTA c handles slice w of tiles c, c + grid, c + 2 grid, ...; its S
+// stages hold the data of its next S slices. Per slice, per lane (16 slots in
+// registers, the four 16-byte chunks visited in the bank-conflict-free rotated
+// order): G = fl32(residue + dW), |probe|, masks of G != 0 and G < 0, residue := G
+// with 128-bit stores; the stage is then refilled with the warp's slice S ahead.
+// Bin maxima and counts go through the warp's scratch (shared atomics, at most two
+// bins per lane), the counts into the message and the maxima into the warp's
+// exponent buckets (flushed to the layer's accumulator when the warp moves on to
+// another layer). The sent and sign masks and the warp's code count go to the
+// workspace.
+//
+// kLazy: the corrections the previous call deferred (its sent mask, when the
+// workspace says they are pending) are applied as the residue is loaded,
+// fl32(G - copysign(s_prev, G)), the same rounding the fix-up would have made.
+//
+// Every wait is bounded: a copy that does not land in time marks the layer with
+// ADACOMP_ERR_TIMEOUT and the warp stops (later slices only mark their layers);
+// before the CTA exits the warp waits, bounded again, for its copies in flight.
+template <int S, bool kLazy, bool kLS>
+__global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const SlicePlan P = slice_plan(g.d_size, S, g.num_layers);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint8_t* stages = smem + (size_t)warp * S * P.stage_bytes;
+    KLayer* lays = reinterpret_cast<KLayer*>(smem + P.stages_bytes);
+    uint32_t* wg = reinterpret_cast<uint32_t*>(smem + P.stages_bytes + P.layer_bytes) + warp * 2 * kWarpScratch;
+    uint32_t* wc = wg + kWarpScratch;
+    unsigned long long* hist =
+        reinterpret_cast<unsigned long long*>(smem + P.stages_bytes + P.layer_bytes + kWarpScratchBytes) + warp * kBkN;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + P.stages_bytes + P.layer_bytes + kWarpScratchBytes +
+                                                kWarps * kBkN * 8) + warp * S;
+    auto stage_r = [&](int s) { return reinterpret_cast<float*>(stages + s * P.stage_bytes); };
+    auto stage_d = [&](int s) { return static_cast<void*>(stages + s * P.stage_bytes + kRBytes); };
+
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(&g.layer[0]);
+        uint4* dst = reinterpret_cast<uint4*>(lays);
+        for (int e = tid; e < g.num_layers * (int)(sizeof(KLayer) / 16); e += kThreads) dst[e] = src[e];
+    }
+    wg[lane] = 0u;
+    wc[lane] = 0u;
+    if (lane < kWarpScratch - 32) { wg[32 + lane] = 0u; wc[32 + lane] = 0u; }
+    hist[lane] = 0ull;
+    hist[32 + lane] = 0ull;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) ptx::mbar_init(&bar[s], 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();  // layer table; the only block-wide barrier
+
+    const uint32_t T = g.total_tiles, c = blockIdx.x, GS = gridDim.x;
+    uint32_t* tile_tot = reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T));
+    uint32_t* wcnt = reinterpret_cast<uint32_t*>(ws + sl_wcnt_offset(g.num_layers, T));
+    uint16_t* sent = reinterpret_cast<uint16_t*>(ws + sl_sent_offset(g.num_layers, T));
+    uint16_t* sign = reinterpret_cast<uint16_t*>(ws + sl_sign_offset(g.num_layers, T));
+    const bool pending = kLazy && reinterpret_cast<const volatile Ctl*>(ws)->pending != 0u;
+    const int rot = seg_rot(lane);
+
+    // lane 0 starts the warp's first S slices
+    int iss_lo = 0;
+    uint32_t inflight = 0;  // stages with a copy in flight (lane 0's view)
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) {
+            const uint32_t t = c + s * GS;
+            if (t >= T) break;
+            iss_lo = advance_layer(lays, g.num_layers, t, iss_lo);
+            const Slice Sl = slice_in(lays[iss_lo], iss_lo, t, warp);
+            if (t == g.inject_skip_tile) continue;  // test hook: this copy is never started
+            if (issue_slice(lays[Sl.layer], Sl, stage_r(s), stage_d(s), &bar[s])) inflight |= 1u << s;
+        }
+    }
+    __syncwarp();
+
+    int lo = 0, hist_layer = -1;
+    bool poisoned = false;
+    uint32_t i_poison = 0;
+    for (uint32_t i = 0;; ++i) {
+        const uint32_t t = c + i * GS;
+        if (t >= T) break;
+        const int s = (int)(i % S);
+        lo = advance_layer(lays, g.num_layers, t, lo);
+        const KLayer& ly = lays[lo];
+        const Slice Sl = slice_in(ly, lo, t, warp);
+        LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(Sl.layer));
+        if (!poisoned && !__all_sync(kFull, wait_bounded(&bar[s], (i / S) & 1u, g.timeout_ns))) {
+            poisoned = true;  // warp-uniform
+            i_poison = i;
+        }
+        if (poisoned) {  // the stage's data may be incomplete: report, do not compute
+            if (lane == 0) atomicOr(&lw->err, kErrTimeout);
+            continue;
+        }
+        if (lane == 0) inflight &= ~(1u << s);
+        if (Sl.layer != hist_layer) {
+            if (hist_layer >= 0)
+                flush_buckets<kBkLo, kBkN>(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+            hist_layer = Sl.layer;
+        }
+        const LaneGeo q = lane_geo(Sl, ly, lane);
+        const uint32_t lomask = q.split >= kSeg ? 0xffffu : ((1u << max(q.split, 0)) - 1u);  // slots of bin_lo
+        // register order: chunk k of the lane is held at registers 4k..4k+3 and is
+        // slot chunk k ^ rot; every per-element test below uses a compile-time bit
+        const uint32_t vr = to_reg_order(q.valid, rot);
+        const uint32_t lor = to_reg_order(lomask, rot) & vr;
+        const size_t mi = ((size_t)t * kWarps + warp) * 32 + lane;  // this lane's mask word
+        uint32_t pm = 0;
+        float s_prev = 0.0f;
+        if (kLazy && pending) {
+            pm = sent[mi];
+            s_prev = lw->result.s;
+        }
+        float ah[4][4];             // |probe| per register slot
+        uint32_t nzr = 0, ngr = 0;  // G != 0, G < 0 (register order)
+        float m_lo = 0.0f, m_hi = 0.0f;
+        if (q.valid) {
+            const float* rs = stage_r(s) + kSeg * lane;
+            const int doff = ly.dw_bf16 ? (int)(Sl.a0 - ((Sl.ts + Sl.we0) & ~(int64_t)7)) : 0;
+            float* gres = ly.residue + Sl.a0 + kSeg * lane;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int q0 = 4 * (k ^ rot);
+                float4 r = *reinterpret_cast<const float4*>(rs + q0);
+                if (kLazy && (pm & (0xfu << (4 * k)))) {
+                    if (pm & (1u << (4 * k + 0))) r.x = __fsub_rn(r.x, copysignf(s_prev, r.x));
+                    if (pm & (1u << (4 * k + 1))) r.y = __fsub_rn(r.y, copysignf(s_prev, r.y));
+                    if (pm & (1u << (4 * k + 2))) r.z = __fsub_rn(r.z, copysignf(s_prev, r.z));
+                    if (pm & (1u << (4 * k + 3))) r.w = __fsub_rn(r.w, copysignf(s_prev, r.w));
+                }
+                float d[4], gv[4];
+                if (ly.dw_bf16) {
+                    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(stage_d(s)) + doff +
+                                                                    kSeg * lane + q0);
+                    d[0] = bf16_lo(u.x); d[1] = bf16_hi(u.x); d[2] = bf16_lo(u.y); d[3] = bf16_hi(u.y);
+                } else {
+                    const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(stage_d(s)) + kSeg * lane + q0);
+                    d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+                }
+                gv[0] = __fadd_rn(r.x, d[0]);
+                gv[1] = __fadd_rn(r.y, d[1]);
+                gv[2] = __fadd_rn(r.z, d[2]);
+                gv[3] = __fadd_rn(r.w, d[3]);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t bit = 1u << (4 * k + e);
+                    if (!(vr & bit)) gv[e] = 0.0f;  // a slot outside the slice
+                    ah[k][e] = fabsf(probe(gv[e], d[e], kLS));
+                    nzr |= gv[e] != 0.0f ? bit : 0u;
+                    ngr |= gv[e] < 0.0f ? bit : 0u;
+                    const float a = fabsf(gv[e]);
+                    const bool in_lo = (lor & bit) != 0u;
+                    m_lo = fmaxf(m_lo, in_lo ? a : 0.0f);
+                    m_hi = fmaxf(m_hi, in_lo ? 0.0f : a);
+                }
+                // residue := G (sent elements are corrected once s is known)
+                const uint32_t vq = (vr >> (4 * k)) & 0xfu;
+                float* gp = gres + q0;
+                if (vq == 0xfu) {
+                    *reinterpret_cast<float4*>(gp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                } else if (vq) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if ((vq >> e) & 1u) gp[e] = gv[e];
+                }
+            }
+        }
+        // the stage is not read again: lane 0 refills it with the slice S ahead (one
+        // warp's shared memory accesses are performed in order, so its reads of the
+        // stage precede the copy)
+        __syncwarp();
+        if (lane == 0) {
+            const uint32_t tn = t + S * GS;
+            if (tn < T) {
+                iss_lo = advance_layer(lays, g.num_layers, tn, iss_lo);
+                const Slice Sn = slice_in(lays[iss_lo], iss_lo, tn, warp);
+                if (tn != g.inject_skip_tile &&
+                    issue_slice(lays[Sn.layer], Sn, stage_r(s), stage_d(s), &bar[s]))
+                    inflight |= 1u << s;
+            }
+        }
+        if (m_lo > 0.0f) atomicMax(&wg[q.bin_lo], __float_as_uint(m_lo));
+        if (m_hi > 0.0f) atomicMax(&wg[q.bin_lo + 1], __float_as_uint(m_hi));
+        __syncwarp();
+        uint32_t fr = 0;  // sent slots, register order
+        if (q.valid) {
+            const float gm_lo = __uint_as_float(wg[q.bin_lo]);
+            const float gm_hi = lomask != 0xffffu ? __uint_as_float(wg[q.bin_lo + 1]) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t bit = 1u << (4 * k + e);
+                    fr |= ah[k][e] >= ((lor & bit) ? gm_lo : gm_hi) ? bit : 0u;
+                }
+            }
+            fr &= nzr;
+            const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & ~lor);
+            if (c_lo) atomicAdd(&wc[q.bin_lo], c_lo);
+            if (c_hi) atomicAdd(&wc[q.bin_lo + 1], c_hi);
+        }
+        __syncwarp();
+        // the slice's bins: counts into the message, maxima into the buckets; the
+        // scratch is left zero
+        if (lane < Sl.nb) {
+            const uint32_t u = wg[lane];  // the bin maximum, |G| as fp32 bits
+            reinterpret_cast<uint16_t*>(ly.msg + 8)[Sl.first_bin + Sl.wb0 + lane] = (uint16_t)wc[lane];
+            if (u) {
+                const uint32_t E = u >> 23;
+                const unsigned long long M = E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
+                if (E - kBkLo < (uint32_t)kBkN) atomicAdd(&hist[E - kBkLo], M);
+                else atomicAdd(&lw->acc[E], M);
+            }
+        }
+        __syncwarp();
+        wg[lane] = 0u;
+        wc[lane] = 0u;
+        sent[mi] = (uint16_t)fr;  // register order (the emitting kernel reorders)
+        sign[mi] = (uint16_t)(ngr & fr);
+        const uint32_t total = __reduce_add_sync(kFull, (uint32_t)__popc(fr));
+        if (lane == 0) {
+            wcnt[(size_t)t * kWarps + warp] = total;
+            if (total) atomicAdd(&tile_tot[t], total);
+        }
+    }
+    if (hist_layer >= 0)
+        flush_buckets<kBkLo, kBkN>(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+    if (poisoned && lane == 0) {
+        // copies that may still be in flight get one more bounded wait before the
+        // CTA's shared memory is released
+        for (uint32_t j = i_poison; j < i_poison + S; ++j) {
+            const int s = (int)(j % S);
+            if (c + j * GS < T && (inflight >> s) & 1u) wait_bounded(&bar[s], (j / S) & 1u, g.timeout_ns);
+        }
+    }
+}
+
+// ---------------------------------------------------------------- finalise and scan
+// One CTA per layer: s from the layer's exact sum (fp64, rounded once to fp32),
+// the header {s, B}, the result area, and the exclusive prefix of the layer's tile
+// code totals (which are left zero for the next call).
+constexpr int kFinThreads = 1024;
+
+__global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __grid_constant__ KGroup g,
+                                                                     uint8_t* __restrict__ ws)
+{
+    __shared__ unsigned long long tmp[256];
+    __shared__ unsigned long long words[kSumWords];
+    __shared__ unsigned long long wsum[kFinThreads / 32];
+    __shared__ unsigned long long layer_total;
+    const int l = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const KLayer& ly = g.layer[l];
+    LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l));
+    const uint32_t T = g.total_tiles;
+    uint32_t* tot = reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T)) + ly.tile_begin;
+    uint64_t* excl = reinterpret_cast<uint64_t*>(ws + sl_excl_offset(g.num_layers)) + ly.tile_begin;
+    if (tid < kSumWords) words[tid] = 0ull;
+    if (tid < 256) tmp[tid] = lw->acc[tid];
+
+    // thread tid scans tiles [i0, i1) of the layer
+    const uint32_t nt = ly.num_tiles;
+    const uint32_t per = (nt + kFinThreads - 1) / kFinThreads;
+    const uint32_t i0 = min(nt, tid * per), i1 = min(nt, i0 + per);
+    unsigned long long mine = 0;
+    for (uint32_t i = i0; i < i1; ++i) mine += tot[i];
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long v = wsum[lane], x = v;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const unsigned long long y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
+        }
+        wsum[lane] = x - v;  // exclusive over warps
+    }
+    __syncthreads();
+    unsigned long long run = wsum[warp] + incl - mine;
+    for (uint32_t i = i0; i < i1; ++i) {
+        const uint32_t v = tot[i];
+        excl[i] = run;
+        run += v;
+        tot[i] = 0u;
+    }
+    if (tid == kFinThreads - 1) layer_total = run;  // the last thread's range ends the layer
+    __syncthreads();
+    const unsigned long long nnz = layer_total;
+    if (warp == 0) {
+        const double Ssum = exact_sum_warp(tmp, words, lane);
+        if (lane == 0) {
+            const float s = __double2float_rn(__ddiv_rn(Ssum, (double)ly.nbins));
+            const bool bad = *reinterpret_cast<volatile uint32_t*>(&lw->err) != 0u;
+            *reinterpret_cast<float*>(ly.msg) = s;
+            *reinterpret_cast<uint32_t*>(ly.msg + 4) = ly.nbins;
+            lw->result.s = s;
+            lw->result.status = bad ? 6u /* ADACOMP_ERR_TIMEOUT */ : 0u;
+            lw->result.nnz = bad ? 0ull : nnz;
+            lw->result.msg_bytes = 8ull + 2ull * ly.nbins + (bad ? 0ull : (unsigned long long)ly.code_bytes * nnz);
+            lw->done = 0;
+            lw->err = 0;
+        }
+    }
+    if (tid < 256) lw->acc[tid] = 0ull;
+    if (l == 0 && tid == 0) reinterpret_cast<volatile Ctl*>(ws)->pending = g.lazy ? 1u : 0u;
+}
+
+// ---------------------------------------------------------------- codes and fix-up
+// One warp per tile (no loop: many tiles in flight hide the latencies). Lane l
+// loads the sent and sign masks of compute lane l of all eight slices, the tile's
+// code offset, the slices' code counts and the layer's status in one batch; then,
+// slice by slice (skipping slices that sent nothing), a warp scan places each
+// lane's codes after those of the earlier lanes and slices. Code of slot i:
+// ((offset of its element in its bin) << 1) | sign. The masks are stored in the
+// streaming kernel's register order and are brought back to slot order here.
+// kFix: the sent elements, listed in shared memory in code order as
+// (tile element << 1 | sign), are then corrected by the whole warp, 8 per lane at
+// a time with all loads issued before the stores: residue (still G) becomes
+// fl32(G - s) or fl32(G + s).
+constexpr int kEmitThreads = 256;
+constexpr int kEmitWarps = kEmitThreads / 32;
+constexpr int kFixCap = 1024;  // listed elements per warp before a flush
+constexpr int kFixBatch = 8;
+
+__device__ __forceinline__ void fix_listed(const uint16_t* lst, uint32_t n, float* res, float s, int lane)
+{
+    __syncwarp();
+    for (uint32_t j0 = 0; j0 < n; j0 += 32 * kFixBatch) {
+        uint32_t e[kFixBatch];
+        float v[kFixBatch];
+#pragma unroll
+        for (int k = 0; k < kFixBatch; ++k) {
+            const uint32_t j = j0 + k * 32 + lane;
+            e[k] = j < n ? (uint32_t)lst[j] : 0xffffffffu;
+        }
+#pragma unroll
+        for (int k = 0; k < kFixBatch; ++k)
+            if (e[k] != 0xffffffffu) v[k] = res[e[k] >> 1];
+#pragma unroll
+        for (int k = 0; k < kFixBatch; ++k)
+            if (e[k] != 0xffffffffu) res[e[k] >> 1] = (e[k] & 1u) ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
+    }
+    __syncwarp();
+}
+
+template <bool kFix>
+__global__ void __launch_bounds__(kEmitThreads) slice_emit_kernel(const __grid_constant__ KGroup g,
+                                                                  uint8_t* __restrict__ ws)
+{
+    __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
+    __shared__ uint16_t fix_list[kFix ? kEmitWarps : 1][kFix ? kFixCap : 1];
+    for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) tb[e] = g.layer[e].tile_begin;
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const uint32_t T = g.total_tiles;
+    const uint32_t q = blockIdx.x * kEmitWarps + (threadIdx.x >> 5);
+    if (q >= T) return;
+    const uint32_t t = T - 1u - q;  // last tiles first
+    const int l = layer_of_tile(tb, g.num_layers, t);
+    const KLayer ly = g.layer[l];  // into registers: one layer per warp
+    const LayerWs* lw = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l));
+    const uint16_t* sent = reinterpret_cast<const uint16_t*>(ws + sl_sent_offset(g.num_layers, T)) + (size_t)t * kWarps * 32 + lane;
+    const uint16_t* sign = reinterpret_cast<const uint16_t*>(ws + sl_sign_offset(g.num_layers, T)) + (size_t)t * kWarps * 32 + lane;
+    uint32_t f[kWarps], ng[kWarps];
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) { f[w] = sent[w * 32]; ng[w] = sign[w * 32]; }
+    const uint32_t wc = lane < kWarps ? reinterpret_cast<const uint32_t*>(ws + sl_wcnt_offset(g.num_layers, T))[(size_t)t * kWarps + lane] : 0u;
+    const uint64_t tile_pos = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(g.num_layers))[t];
+    const uint32_t status = lw->result.status;
+    const float s = lw->result.s;
+    if (status != 0u) return;  // a layer whose streaming pass did not complete
+    uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
+    const int rot = seg_rot(lane);
+    uint16_t* lst = fix_list[kFix ? (threadIdx.x >> 5) : 0];
+    const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+    float* res_tile = ly.residue + (int64_t)first_bin * ly.bin_len;
+    uint64_t slice_pos = tile_pos;
+    uint32_t listed = 0;
+#pragma unroll 1
+    for (int w = 0; w < kWarps; ++w) {
+        const uint32_t fw = to_slot_order(f[0], rot), nw_ = to_slot_order(ng[0], rot);
+        // rotate the batch so that f[0] is always the current slice (static indexing)
+#pragma unroll
+        for (int k = 0; k + 1 < kWarps; ++k) { f[k] = f[k + 1]; ng[k] = ng[k + 1]; }
+        const uint32_t cnt_w = __shfl_sync(kFull, wc, w);
+        if (cnt_w == 0u) continue;
+        if (kFix && listed + cnt_w > (uint32_t)kFixCap) {
+            fix_listed(lst, listed, res_tile, s, lane);
+            listed = 0;
+        }
+        const Slice Sl = slice_in(ly, l, t, w);
+        const uint32_t c = __popc(fw);
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        if (fw) {
+            const LaneGeo qg = lane_geo(Sl, ly, lane);
+            const uint32_t base_lo = (uint32_t)((qg.lane_e - Sl.we0) - qg.bin_lo * ly.bin_len) << 1;
+            const uint32_t base_hi = base_lo - 2u * (uint32_t)ly.bin_len;
+            uint64_t pos = slice_pos + incl - c;
+            uint32_t li = listed + incl - c;
+            uint32_t m = fw;
+            while (m) {
+                const int idx = __ffs(m) - 1;
+                m &= m - 1;
+                const uint32_t sg = (nw_ >> idx) & 1u;
+                const uint32_t code = (idx < qg.split ? base_lo : base_hi) + 2u * idx + sg;
+                if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
+                else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
+                ++pos;
+                if (kFix) lst[li++] = (uint16_t)(((uint32_t)(qg.lane_e + idx) << 1) | sg);
+            }
+        }
+        slice_pos += cnt_w;
+        listed += cnt_w;
+    }
+    if (kFix && listed) fix_listed(lst, listed, res_tile, s, lane);
+}
+
+// ---------------------------------------------------------------- materialise (deferred fix-up)
+// Applies the corrections a call with a deferred fix-up left pending: for every
+// slot whose bit is set in its lane's sent mask, residue = fl32(G - sign(G) s) with
+// the layer's s from that call. One warp per (tile, slice).
+__global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const __grid_constant__ KGroup g,
+                                                                         uint8_t* __restrict__ ws)
+{
+    __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
+    for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) tb[e] = g.layer[e].tile_begin;
+    __syncthreads();
+    if (reinterpret_cast<const volatile Ctl*>(ws)->pending == 0u) return;
+    const int lane = threadIdx.x & 31;
+    const uint32_t T = g.total_tiles;
+    const uint16_t* sent = reinterpret_cast<const uint16_t*>(ws + sl_sent_offset(g.num_layers, T));
+    const uint64_t units = (uint64_t)T * kWarps;
+    const uint64_t nw = (uint64_t)gridDim.x * (kEmitThreads / 32);
+    for (uint64_t u = (uint64_t)blockIdx.x * (kEmitThreads / 32) + (threadIdx.x >> 5); u < units; u += nw) {
+        const uint32_t t = (uint32_t)(u / kWarps);
+        const int w = (int)(u % kWarps);
+        const uint32_t f = to_slot_order(sent[((size_t)t * kWarps + w) * 32 + lane], seg_rot(lane));
+        if (!f) continue;
+        const int l = layer_of_tile(tb, g.num_layers, t);
+        const Slice Sl = slice_in(g.layer[l], l, t, w);
+        const float s = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l))->result.s;
+        float* res = g.layer[l].residue + Sl.a0 + kSeg * lane;
+#pragma unroll
+        for (int i = 0; i < kSeg; ++i)
+            if ((f >> i) & 1u) res[i] = __fsub_rn(res[i], copysignf(s, res[i]));
+    }
+}
+
+struct SlicedDevice {
+    int sms = 0;
+    uint32_t smem_set[4] = {0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per variant
+};
+SlicedDevice g_sl_dev[64];
+
+constexpr int kStages = 2;  // per-warp stages; with 3 CTAs per SM (74 registers) measured faster than 3 stages with 2
+
+}  // namespace
+
+bool group_is_sliced(const KGroup& g)
+{
+    for (int l = 0; l < g.num_layers; ++l)
+        if (!g.layer[l].bpw) return false;
+    return g.num_layers > 0;
+}
+
+cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t stream, cudaEvent_t ev_before,
+                                   cudaEvent_t ev_mid, cudaEvent_t ev_after)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    SlicedDevice& di = g_sl_dev[dev];
+    if (di.sms == 0) {
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const SlicePlan P = slice_plan(g.d_size, kStages, g.num_layers);
+    void (*kern)(KGroup, uint8_t*);
+    if (g.local_selection) kern = g.lazy ? slice_kernel<kStages, true, true> : slice_kernel<kStages, false, true>;
+    else kern = g.lazy ? slice_kernel<kStages, true, false> : slice_kernel<kStages, false, false>;
+    const int ki = (g.lazy ? 1 : 0) + (g.local_selection ? 2 : 0);
+    if (P.total > di.smem_set[ki]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
+        if (e != cudaSuccess) return e;
+        di.smem_set[ki] = P.total;
+    }
+    int occ = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, P.total);
+    if (e != cudaSuccess) return e;
+    if (occ < 1) return cudaErrorInvalidConfiguration;
+    const long long cap = (long long)di.sms * occ;
+    const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
+    if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess) return e;
+    kern<<<grid, kThreads, P.total, stream>>>(g, static_cast<uint8_t*>(ws));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
+    slice_finalize_kernel<<<g.num_layers, kFinThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    const uint32_t egrid = (g.total_tiles + kEmitWarps - 1) / kEmitWarps;  // one warp per tile
+    if (g.lazy) slice_emit_kernel<false><<<egrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    else slice_emit_kernel<true><<<egrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (ev_after) e = cudaEventRecord(ev_after, stream);
+    return e;
+}
+
+cudaError_t launch_materialize_sliced(const KGroup& g, void* ws, cudaStream_t stream)
+{
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    SlicedDevice& di = g_sl_dev[dev];
+    if (di.sms == 0) {
+        e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+    }
+    const uint64_t units = (uint64_t)g.total_tiles * kWarps;
+    const uint64_t blocks_needed = (units + kEmitThreads / 32 - 1) / (kEmitThreads / 32);
+    const uint64_t cap = (uint64_t)di.sms * 8;
+    const uint32_t grid = (uint32_t)(blocks_needed < cap ? blocks_needed : cap);
+    slice_materialize_kernel<<<grid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    // the corrections are applied: the next call must not apply them again
+    return cudaMemsetAsync(static_cast<uint8_t*>(ws) + offsetof(Ctl, pending), 0, sizeof(uint32_t), stream);
+}
+
+}  // namespace adacomp
