@@ -303,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
             s_prev = lw->result.s;
         }
         float ah[4][4];             // |probe| per register slot
-        uint32_t nzr = 0, ngr = 0;  // G != 0, G < 0 (register order)
+        uint32_t ngr = 0;  // G < 0 (register order; kept for the deferred fix-up's codes only)
         float m_lo = 0.0f, m_hi = 0.0f;
         if (q.valid) {
             const float* rs = stage_r(s) + kSeg * lane;
@@ -336,9 +336,9 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
                 for (int e = 0; e < 4; ++e) {
                     const uint32_t bit = 1u << (4 * k + e);
                     if (!(vr & bit)) gv[e] = 0.0f;  // a slot outside the slice
-                    ah[k][e] = fabsf(probe(gv[e], d[e], kLS));
-                    nzr |= gv[e] != 0.0f ? bit : 0u;
-                    ngr |= gv[e] < 0.0f ? bit : 0u;
+                    // an element with G == 0 is never sent: its probe is made negative
+                    ah[k][e] = gv[e] != 0.0f ? fabsf(probe(gv[e], d[e], kLS)) : -1.0f;
+                    if (kLazy) ngr |= gv[e] < 0.0f ? bit : 0u;
                     const float a = fabsf(gv[e]);
                     const bool in_lo = (lor & bit) != 0u;
                     m_lo = fmaxf(m_lo, in_lo ? a : 0.0f);
@@ -385,7 +385,6 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
                     fr |= ah[k][e] >= ((lor & bit) ? gm_lo : gm_hi) ? bit : 0u;
                 }
             }
-            fr &= nzr;
             const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & ~lor);
             if (c_lo) atomicAdd(&wc[q.bin_lo], c_lo);
             if (c_hi) atomicAdd(&wc[q.bin_lo + 1], c_hi);
@@ -407,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
         wg[lane] = 0u;
         wc[lane] = 0u;
         sent[mi] = (uint16_t)fr;  // register order (the emitting kernel reorders)
-        sign[mi] = (uint16_t)(ngr & fr);
+        if (kLazy) sign[mi] = (uint16_t)(ngr & fr);  // without the fix-up, the emitting kernel has no G
         const uint32_t total = __reduce_add_sync(kFull, (uint32_t)__popc(fr));
         if (lane == 0) {
             wcnt[(size_t)t * kWarps + warp] = total;
@@ -518,7 +517,12 @@ constexpr int kEmitWarps = kEmitThreads / 32;
 constexpr int kFixCap = 1024;  // listed elements per warp before a flush
 constexpr int kFixBatch = 8;
 
-__device__ __forceinline__ void fix_listed(const uint16_t* lst, uint32_t n, float* res, float s, int lane)
+// The listed elements j = 0..n-1 of a tile (tile element indices, in code order):
+// G is loaded from the residue (8 per lane at a time, all loads issued first), the
+// code ((element - its bin's first element) << 1) | (G < 0) is written at code
+// position pos0 + j, and the residue becomes fl32(G - s) or fl32(G + s).
+__device__ __forceinline__ void fix_listed(const uint16_t* lst, uint32_t n, float* res, float s, uint8_t* codes,
+                                           uint64_t pos0, const KLayer& ly, int lane)
 {
     __syncwarp();
     for (uint32_t j0 = 0; j0 < n; j0 += 32 * kFixBatch) {
@@ -531,10 +535,18 @@ __device__ __forceinline__ void fix_listed(const uint16_t* lst, uint32_t n, floa
         }
 #pragma unroll
         for (int k = 0; k < kFixBatch; ++k)
-            if (e[k] != 0xffffffffu) v[k] = res[e[k] >> 1];
+            if (e[k] != 0xffffffffu) v[k] = res[e[k]];
 #pragma unroll
-        for (int k = 0; k < kFixBatch; ++k)
-            if (e[k] != 0xffffffffu) res[e[k] >> 1] = (e[k] & 1u) ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
+        for (int k = 0; k < kFixBatch; ++k) {
+            if (e[k] == 0xffffffffu) continue;
+            const uint32_t neg = v[k] < 0.0f ? 1u : 0u;
+            const uint32_t off = e[k] - __umulhi(e[k], ly.inv_len) * (uint32_t)ly.bin_len;  // e < 2^16: exact
+            const uint32_t code = (off << 1) | neg;
+            const uint64_t pos = pos0 + j0 + k * 32 + lane;
+            if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
+            else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
+            res[e[k]] = neg ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
+        }
     }
     __syncwarp();
 }
@@ -559,7 +571,7 @@ __global__ void __launch_bounds__(kEmitThreads) slice_emit_kernel(const __grid_c
     const uint16_t* sign = reinterpret_cast<const uint16_t*>(ws + sl_sign_offset(g.num_layers, T)) + (size_t)t * kWarps * 32 + lane;
     uint32_t f[kWarps], ng[kWarps];
 #pragma unroll
-    for (int w = 0; w < kWarps; ++w) { f[w] = sent[w * 32]; ng[w] = sign[w * 32]; }
+    for (int w = 0; w < kWarps; ++w) { f[w] = sent[w * 32]; ng[w] = kFix ? 0u : sign[w * 32]; }
     const uint32_t wc = lane < kWarps ? reinterpret_cast<const uint32_t*>(ws + sl_wcnt_offset(g.num_layers, T))[(size_t)t * kWarps + lane] : 0u;
     const uint64_t tile_pos = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(g.num_layers))[t];
     const uint32_t status = lw->result.status;
@@ -571,6 +583,7 @@ __global__ void __launch_bounds__(kEmitThreads) slice_emit_kernel(const __grid_c
     const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
     float* res_tile = ly.residue + (int64_t)first_bin * ly.bin_len;
     uint64_t slice_pos = tile_pos;
+    uint64_t list_pos = tile_pos;  // code position of the first listed element
     uint32_t listed = 0;
 #pragma unroll 1
     for (int w = 0; w < kWarps; ++w) {
@@ -581,7 +594,8 @@ __global__ void __launch_bounds__(kEmitThreads) slice_emit_kernel(const __grid_c
         const uint32_t cnt_w = __shfl_sync(kFull, wc, w);
         if (cnt_w == 0u) continue;
         if (kFix && listed + cnt_w > (uint32_t)kFixCap) {
-            fix_listed(lst, listed, res_tile, s, lane);
+            fix_listed(lst, listed, res_tile, s, codes, list_pos, ly, lane);
+            list_pos += listed;
             listed = 0;
         }
         const Slice Sl = slice_in(ly, l, t, w);
@@ -593,27 +607,35 @@ __global__ void __launch_bounds__(kEmitThreads) slice_emit_kernel(const __grid_c
             if (lane >= o) incl += y;
         }
         if (fw) {
-            const LaneGeo qg = lane_geo(Sl, ly, lane);
-            const uint32_t base_lo = (uint32_t)((qg.lane_e - Sl.we0) - qg.bin_lo * ly.bin_len) << 1;
-            const uint32_t base_hi = base_lo - 2u * (uint32_t)ly.bin_len;
-            uint64_t pos = slice_pos + incl - c;
-            uint32_t li = listed + incl - c;
-            uint32_t m = fw;
-            while (m) {
-                const int idx = __ffs(m) - 1;
-                m &= m - 1;
-                const uint32_t sg = (nw_ >> idx) & 1u;
-                const uint32_t code = (idx < qg.split ? base_lo : base_hi) + 2u * idx + sg;
-                if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
-                else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
-                ++pos;
-                if (kFix) lst[li++] = (uint16_t)(((uint32_t)(qg.lane_e + idx) << 1) | sg);
+            const int lane_e = (int)(Sl.a0 - Sl.ts) + kSeg * lane;  // tile element of slot 0
+            if constexpr (kFix) {
+                uint32_t li = listed + incl - c;
+                uint32_t m = fw;
+                while (m) {
+                    const int idx = __ffs(m) - 1;
+                    m &= m - 1;
+                    lst[li++] = (uint16_t)(lane_e + idx);
+                }
+            } else {
+                const LaneGeo qg = lane_geo(Sl, ly, lane);
+                const uint32_t base_lo = (uint32_t)((qg.lane_e - Sl.we0) - qg.bin_lo * ly.bin_len) << 1;
+                const uint32_t base_hi = base_lo - 2u * (uint32_t)ly.bin_len;
+                uint64_t pos = slice_pos + incl - c;
+                uint32_t m = fw;
+                while (m) {
+                    const int idx = __ffs(m) - 1;
+                    m &= m - 1;
+                    const uint32_t code = (idx < qg.split ? base_lo : base_hi) + 2u * idx + ((nw_ >> idx) & 1u);
+                    if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
+                    else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
+                    ++pos;
+                }
             }
         }
         slice_pos += cnt_w;
         listed += cnt_w;
     }
-    if (kFix && listed) fix_listed(lst, listed, res_tile, s, lane);
+    if (kFix && listed) fix_listed(lst, listed, res_tile, s, codes, list_pos, ly, lane);
 }
 
 // ---------------------------------------------------------------- materialise (deferred fix-up)
