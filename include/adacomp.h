@@ -106,7 +106,7 @@ adacomp_status adacomp_init_group(adacomp_layer_t* out, int32_t num_layers, cons
 
 #define ADACOMP_MAX_GROUP 128
 #define ADACOMP_MAX_LEARNERS 256
-#define ADACOMP_DECODE_WS_FIXED 2048
+#define ADACOMP_DECODE_WS_FIXED 10240
 
 /*
  * One AdaComp step for one layer (Algorithm 2 as restated in Claims > Mechanism

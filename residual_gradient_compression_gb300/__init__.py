@@ -25,7 +25,7 @@ F32, BF16 = 0, 1
 RULE_ADACOMP, RULE_LOCAL_SELECTION = 0, 1
 MAX_GROUP = 128
 MAX_LEARNERS = 256
-DECODE_WS_FIXED = 2048
+DECODE_WS_FIXED = 10240
 
 _lib = None
 

@@ -278,7 +278,7 @@ adacomp_status adacomp_decode_status(adacomp_layer_t h, const void* ws, cudaStre
                                      int32_t* device_status)
 {
     if (!h || !ws) return ADACOMP_ERR_INVALID_ARG;
-    uint8_t fixed[adacomp::kDecodeFixed];
+    uint8_t fixed[16 + adacomp::kMaxDecodePairs];  // K, layers, one bad-message byte per (layer, learner)
     cudaError_t e = cudaMemcpyAsync(fixed, ws, sizeof fixed, cudaMemcpyDeviceToHost, stream);
     if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
     if (e != cudaSuccess) return ADACOMP_ERR_CUDA;

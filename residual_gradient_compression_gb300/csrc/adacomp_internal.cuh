@@ -170,12 +170,14 @@ __host__ __device__ inline uint32_t desc_flag(uint64_t d, uint64_t ep)
 }
 
 // ---------------------------------------------------------------- decode workspace
-// [fixed 2048 B: u32 K, u32 num_layers, u32 pad[2], u8 bad[num_layers * K]]
+// [fixed 10240 B: u32 K, u32 num_layers, u32 pad[2], u8 bad[num_layers * K] (up to byte 1040);
+//  at byte 2048: u64 codes[num_layers * K], the code count of each (layer, learner) message]
 // [per learner k: tile_off u64 x T]
 // bad[l*K+k] and tile_off are written by every decode call before they are read, so
 // the decode workspace needs no initialisation. tile_off = kBadOffset marks a
 // (layer, learner) message that is skipped.
-constexpr size_t kDecodeFixed = 2048;
+constexpr size_t kDecodeFixed = 10240;
+constexpr size_t kDecodeLayerCodes = 2048;  // offset of the (layer, learner) code counts
 constexpr int kMaxDecodePairs = 1024;  // num_layers * K per launch
 constexpr uint64_t kBadOffset = ~0ull;
 __host__ __device__ inline size_t decode_per_learner(uint64_t total_tiles) { return 8 * (size_t)total_tiles; }

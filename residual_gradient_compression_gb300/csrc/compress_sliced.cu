@@ -294,7 +294,8 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
         // register order: chunk k of the lane is held at registers 4k..4k+3 and is
         // slot chunk k ^ rot; every per-element test below uses a compile-time bit
         const uint32_t vr = to_reg_order(q.valid, rot);
-        const uint32_t lor = to_reg_order(lomask, rot) & vr;
+        const uint32_t lor = to_reg_order(lomask, rot) & vr;  // valid slots of bin_lo
+        const uint32_t hir = vr & ~lor;                        // valid slots of bin_lo + 1
         const size_t mi = ((size_t)t * kWarps + warp) * 32 + lane;  // this lane's mask word
         uint32_t pm = 0;
         float s_prev = 0.0f;
@@ -335,14 +336,14 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const uint32_t bit = 1u << (4 * k + e);
-                    if (!(vr & bit)) gv[e] = 0.0f;  // a slot outside the slice
                     // an element with G == 0 is never sent: its probe is made negative
                     ah[k][e] = gv[e] != 0.0f ? fabsf(probe(gv[e], d[e], kLS)) : -1.0f;
                     if (kLazy) ngr |= gv[e] < 0.0f ? bit : 0u;
                     const float a = fabsf(gv[e]);
-                    const bool in_lo = (lor & bit) != 0u;
-                    m_lo = fmaxf(m_lo, in_lo ? a : 0.0f);
-                    m_hi = fmaxf(m_hi, in_lo ? 0.0f : a);
+                    // slots outside the slice hold stale data: neither maximum takes them,
+                    // and they are dropped from the sent mask below
+                    m_lo = fmaxf(m_lo, (lor & bit) ? a : 0.0f);
+                    m_hi = fmaxf(m_hi, (hir & bit) ? a : 0.0f);
                 }
                 // residue := G (sent elements are corrected once s is known)
                 const uint32_t vq = (vr >> (4 * k)) & 0xfu;
@@ -385,6 +386,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
                     fr |= ah[k][e] >= ((lor & bit) ? gm_lo : gm_hi) ? bit : 0u;
                 }
             }
+            fr &= vr;
             const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & ~lor);
             if (c_lo) atomicAdd(&wc[q.bin_lo], c_lo);
             if (c_hi) atomicAdd(&wc[q.bin_lo + 1], c_hi);

@@ -6,16 +6,18 @@
 // summary paragraph); this library reads the combination as a plain sum in learner
 // order, dense[j] = fl32(dense[j] + sign * s_k) for k = 0..K-1.
 //
-// Three launches:
+// Four launches:
 //   tile_sums   per (learner, tile): validate the header and the tile's per-bin
 //               counts, and sum the counts;
 //   tile_scan   per (layer, learner): exclusive prefix of the tile sums, i.e. where
-//               each tile's codes start in that message;
-//   accumulate  per tile: the dense tile is staged in shared memory, every learner's
-//               codes for the tile are applied in learner order (a barrier between
-//               learners), and the tile is written back. One CTA owns each tile, no
-//               two threads touch one element within a learner, and no float atomics
-//               are used, so the result is deterministic.
+//               each tile's codes start in that message, and the message's total;
+//   accumulate  per tile of the layers that are streamed: the dense tile is staged
+//               in shared memory, every learner's codes for the tile are applied in
+//               learner order, and the tile is written back;
+//   sparse_accumulate  per tile of the layers whose learners sent few codes: the
+//               codes are added in place in global memory, learner by learner.
+// One warp owns each bin range of a tile, no two threads touch one element within a
+// learner, and no float atomics are used, so the result is deterministic.
 #include "adacomp_internal.cuh"
 
 namespace adacomp {
@@ -24,66 +26,82 @@ namespace {
 constexpr unsigned kFull = 0xffffffffu;
 constexpr int kDecThreads = 256;
 
-__device__ __forceinline__ int find_layer(const KGroup& g, uint32_t t)
+// Layer of tile t from a shared-memory array of the layers' first tiles.
+__device__ __forceinline__ int layer_of(const uint32_t* tb, int num_layers, uint32_t t)
 {
-    int lo = 0, hi = g.num_layers - 1;
+    int lo = 0, hi = num_layers - 1;
     while (lo < hi) {
         int mid = (lo + hi + 1) >> 1;
-        if (g.layer[mid].tile_begin <= t) lo = mid;
+        if (tb[mid] <= t) lo = mid;
         else hi = mid - 1;
     }
     return lo;
 }
+
+__device__ __forceinline__ unsigned long long* layer_codes(uint8_t* ws)
+{
+    return reinterpret_cast<unsigned long long*>(ws + kDecodeLayerCodes);
+}
+
+// One byte per layer, set when the layer is summed in place in global memory,
+// without staging its dense tiles: when all learners together sent fewer than
+// n / 16 of its elements, each code costs about one 32-byte sector read and write,
+// against 8 bytes per element for streaming the dense array. (The fused SGD step
+// always streams: every element's weights and momentum change.)
+constexpr size_t kDecodeSparseFlags = 1040;  // after the bad-message bytes
+__device__ __forceinline__ uint8_t* sparse_flags(uint8_t* ws) { return ws + kDecodeSparseFlags; }
 
 __device__ __forceinline__ uint64_t* tile_offsets(uint8_t* ws, int k, uint32_t T)
 {
     return reinterpret_cast<uint64_t*>(ws + kDecodeFixed + (size_t)k * decode_per_learner(T));
 }
 
-// One warp per (learner k, tile t): header B must equal the layer's B, and no
-// count may exceed its bin's length; otherwise the tile sum is kBadOffset.
+// One warp per (learner k, tile t), every task in flight at once: the header's B
+// must equal the layer's B, and no count may exceed its bin's length; otherwise the
+// tile sum is kBadOffset.
 __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_constant__ KGroup g,
                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
+    __shared__ uint32_t tb[kMaxGroup];
+    for (int e = threadIdx.x; e < g.num_layers; e += kDecThreads) tb[e] = g.layer[e].tile_begin;
+    if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<uint32_t*>(ws)[2] = 0u;  // scan blocks done
+    __syncthreads();
     const uint32_t T = g.total_tiles;
     const int K = p.K;
     const int lane = threadIdx.x & 31;
-    const uint64_t nwarps = (uint64_t)gridDim.x * (kDecThreads / 32);
-    for (uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5); task < (uint64_t)K * T;
-         task += nwarps) {
-        const int k = (int)(task / T);
-        const uint32_t t = (uint32_t)(task - (uint64_t)k * T);
-        const int l = find_layer(g, t);
-        const KLayer& ly = g.layer[l];
-        const uint8_t* msg = p.msg[l * K + k];
-        const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
-        const int bins = (int)min(ly.bins_per_tile, ly.nbins - first_bin);
-        bool ok = *reinterpret_cast<const uint32_t*>(msg + 4) == ly.nbins;
-        uint32_t sum = 0;
-        if (ok) {
-            const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + first_bin;
-            const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len;
-            for (int b = lane; b < bins; b += 32) {
-                const uint32_t c = cnt[b];
-                const int64_t len = (first_bin + b == ly.nbins - 1) ? last_len : ly.bin_len;
-                ok = ok && (int64_t)c <= len;
-                sum += c;
-            }
-        }
-        ok = __all_sync(kFull, ok);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) sum += __shfl_xor_sync(kFull, sum, o);
-        if (lane == 0) tile_offsets(ws, k, T)[t] = ok ? (uint64_t)sum : kBadOffset;
+    const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
+    if (task >= (uint64_t)K * T) return;
+    const int k = (int)(task / T);
+    const uint32_t t = (uint32_t)(task - (uint64_t)k * T);
+    const int l = layer_of(tb, g.num_layers, t);
+    const KLayer& ly = g.layer[l];
+    const uint8_t* msg = p.msg[l * K + k];
+    const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+    const int bins = (int)min(ly.bins_per_tile, ly.nbins - first_bin);
+    const uint32_t hdr_b = *reinterpret_cast<const uint32_t*>(msg + 4);
+    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + first_bin;
+    const uint32_t last_len = (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
+    bool ok = true;
+    uint32_t sum = 0;
+    for (int b = lane; b < bins; b += 32) {
+        const uint32_t c = cnt[b];
+        ok = ok && c <= (first_bin + b == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len);
+        sum += c;
     }
+    ok = __all_sync(kFull, ok) && hdr_b == ly.nbins;
+    sum = __reduce_add_sync(kFull, sum);
+    if (lane == 0) tile_offsets(ws, k, T)[t] = ok ? (uint64_t)sum : kBadOffset;
 }
 
-// One CTA per (layer, learner): tile sums -> exclusive offsets, in place. A layer
-// message with any bad tile is marked bad as a whole.
+// One CTA per (layer, learner): the tile sums become exclusive offsets, in place,
+// each thread taking a contiguous run of tiles. A layer message with any bad tile
+// is marked bad as a whole; the message's code count goes to the workspace.
 __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__ KGroup g,
                                                          const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
-    __shared__ uint32_t wsum[32];
+    __shared__ unsigned long long wsum[32];
     __shared__ uint32_t bad_s;
+    __shared__ unsigned long long total_s;
     const int K = p.K;
     const int l = blockIdx.x / K, k = blockIdx.x - (blockIdx.x / K) * K;
     const KLayer& ly = g.layer[l];
@@ -95,33 +113,62 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
     }
     if (tid == 0) bad_s = 0u;
     __syncthreads();
-    uint64_t carry = 0;
-    for (uint32_t base = 0; base < ly.num_tiles; base += 1024) {
-        const uint32_t i = base + tid;
-        const uint64_t v = i < ly.num_tiles ? off[i] : 0ull;
-        if (v == kBadOffset) bad_s = 1u;
-        const uint32_t x = v == kBadOffset ? 0u : (uint32_t)v;
-        uint32_t incl = x;
+    const uint32_t nt = ly.num_tiles;
+    const uint32_t per = (nt + 1023) / 1024;
+    const uint32_t i0 = min(nt, tid * per), i1 = min(nt, i0 + per);
+    unsigned long long mine = 0;
+    bool ok = true;
+#pragma unroll 4
+    for (uint32_t i = i0; i < i1; ++i) {
+        const uint64_t v = off[i];
+        ok = ok && v != kBadOffset;
+        mine += v == kBadOffset ? 0ull : v;
+    }
+    if (!ok) bad_s = 1u;
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        const unsigned long long v = wsum[lane];
+        unsigned long long x = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            uint32_t y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
+            const unsigned long long y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
         }
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        uint64_t woff = 0, tot = 0;
-        for (int w = 0; w < 32; ++w) {
-            if (w < warp) woff += wsum[w];
-            tot += wsum[w];
-        }
-        if (i < ly.num_tiles) off[i] = carry + woff + incl - x;
-        carry += tot;
-        __syncthreads();
+        wsum[lane] = x - v;
+        if (lane == 31) total_s = x;
     }
+    __syncthreads();
     const bool bad = bad_s != 0u;
-    if (bad)
-        for (uint32_t i = tid; i < ly.num_tiles; i += 1024) off[i] = kBadOffset;
-    if (tid == 0) ws[16 + l * K + k] = bad ? 1 : 0;
+    unsigned long long run = wsum[warp] + incl - mine;
+    for (uint32_t i = i0; i < i1; ++i) {
+        const uint64_t v = off[i];
+        off[i] = bad ? kBadOffset : run;
+        run += v == kBadOffset ? 0ull : v;
+    }
+    __shared__ uint32_t last_s;
+    if (tid == 0) {
+        ws[16 + l * K + k] = bad ? 1 : 0;
+        layer_codes(ws)[(size_t)l * K + k] = bad ? 0ull : total_s;
+        __threadfence();
+        last_s = atomicAdd(reinterpret_cast<uint32_t*>(ws) + 2, 1u) == gridDim.x - 1u ? 1u : 0u;
+    }
+    __syncthreads();
+    if (last_s) {  // every message is scanned: decide which layers are summed in place
+        __threadfence();
+        for (int e = tid; e < g.num_layers; e += 1024) {
+            const volatile unsigned long long* c = layer_codes(ws) + (size_t)e * K;
+            unsigned long long sum = 0;
+            for (int j = 0; j < K; ++j) sum += c[j];
+            sparse_flags(ws)[e] = sum * 16ull < (unsigned long long)g.layer[e].n ? 1 : 0;
+        }
+    }
 }
 
 // Persistent over tiles (CTA c takes tiles c, c + grid, ...). The dense tiles
@@ -164,10 +211,25 @@ struct AccTile {
     int64_t a0;      // 16-byte boundary at or before ts: element a0 is at stage[0]
 };
 
-__device__ __forceinline__ AccTile acc_tile(const KGroup& g, uint32_t t)
+// Per-CTA copy of what the accumulate kernels look up per tile: each layer's
+// first tile and whether it is summed in place.
+struct LayerIndex {
+    uint32_t tb[kMaxGroup];
+    uint8_t sparse[kMaxGroup];
+};
+
+__device__ __forceinline__ void load_index(LayerIndex& X, const KGroup& g, uint8_t* ws, int K, bool sgd)
+{
+    for (int e = threadIdx.x; e < g.num_layers; e += blockDim.x) {
+        X.tb[e] = g.layer[e].tile_begin;
+        X.sparse[e] = !sgd && sparse_flags(ws)[e] != 0 ? 1 : 0;
+    }
+}
+
+__device__ __forceinline__ AccTile acc_tile(const KGroup& g, const LayerIndex& X, uint32_t t)
 {
     AccTile A;
-    A.layer = find_layer(g, t);
+    A.layer = layer_of(X.tb, g.num_layers, t);
     const KLayer& ly = g.layer[A.layer];
     A.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
     A.bins = (int)min(ly.bins_per_tile, ly.nbins - A.first_bin);
@@ -183,11 +245,15 @@ __device__ __forceinline__ AccTile acc_tile(const KGroup& g, uint32_t t)
 // (For the fused SGD step the weights and the momentum are loaded into the stage's
 // second and third arrays; the first, the gradient sum, is zeroed by the threads.)
 template <bool kSGD>
-__device__ void acc_issue(const KGroup& g, const DecodeParams& p, uint32_t t, float* st, uint32_t arr_floats,
-                          uint64_t* bar)
+__device__ void acc_issue(const KGroup& g, const LayerIndex& X, const DecodeParams& p, uint32_t t, float* st,
+                          uint32_t arr_floats, uint64_t* bar)
 {
-    const AccTile A = acc_tile(g, t);
+    const AccTile A = acc_tile(g, X, t);
     const int64_t n = g.layer[A.layer].n;
+    if (X.sparse[A.layer]) {  // summed in place by the sparse kernel: nothing to stage
+        ptx::mbar_arrive(bar);
+        return;
+    }
     int64_t a1 = (A.te + 3) & ~(int64_t)3;
     if (a1 > n) a1 = A.te & ~(int64_t)3;
     const uint32_t bytes = a1 > A.a0 ? (uint32_t)(a1 - A.a0) * 4u : 0u;
@@ -400,12 +466,15 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     const uint32_t G0 = blockIdx.x, GS = gridDim.x;
     const int K = p.K;
     auto stage = [&](int i) { return stage0 + (size_t)(i % kAccStages) * (stage_bytes / 4); };
+    __shared__ LayerIndex X;
+    load_index(X, g, ws, p.K, kSGD);
+    __syncthreads();
 
     if (tid == 0) {
         for (int k = 0; k < kAccStages; ++k) ptx::mbar_init(&bar[k], 1);
         ptx::fence_mbar_init();
         for (int i = 0; i < kAccStages - 1; ++i)
-            if (G0 + (uint32_t)i * GS < T) acc_issue<kSGD>(g, p, G0 + (uint32_t)i * GS, stage(i), arr_floats, &bar[i]);
+            if (G0 + (uint32_t)i * GS < T) acc_issue<kSGD>(g, X, p, G0 + (uint32_t)i * GS, stage(i), arr_floats, &bar[i]);
     }
     __syncthreads();
 
@@ -415,7 +484,22 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         const uint32_t t = G0 + (uint32_t)i * GS;
         if (t >= T) break;
         float* st = stage(i);
-        const AccTile A = acc_tile(g, t);
+        const AccTile A = acc_tile(g, X, t);
+        if (X.sparse[A.layer]) {
+            // summed in place by the sparse kernel. Its issue completed the stage's
+            // phase at once, so skipping the wait is safe: the next wait on this
+            // barrier is for the following phase. Keep the ring turning.
+            if (tid == 0) {
+                ptx::bulk_commit();
+                const uint32_t tn = t + (uint32_t)(kAccStages - 1) * GS;
+                if (tn < T) {
+                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+                    acc_issue<kSGD>(g, X, p, tn, stage(i + kAccStages - 1), arr_floats,
+                                    &bar[(i + kAccStages - 1) % kAccStages]);
+                }
+            }
+            continue;
+        }
         const KLayer& ly = g.layer[A.layer];
         const int l = A.layer;
         const int bpw = (A.bins + kDecThreads / 32 - 1) / (kDecThreads / 32);
@@ -500,7 +584,7 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
             const uint32_t tn = t + (uint32_t)(kAccStages - 1) * GS;
             if (tn < T) {
                 asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                acc_issue<kSGD>(g, p, tn, stage(i + kAccStages - 1), arr_floats, &bar[(i + kAccStages - 1) % kAccStages]);
+                acc_issue<kSGD>(g, X, p, tn, stage(i + kAccStages - 1), arr_floats, &bar[(i + kAccStages - 1) % kAccStages]);
             }
         }
     }
@@ -510,7 +594,7 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         // layers, then give the loads still in flight one more bounded wait before
         // the CTA's shared memory is released
         for (uint32_t t = G0 + (uint32_t)i * GS; t < T; t += GS) {
-            const int l = find_layer(g, t);
+            const int l = layer_of(X.tb, g.num_layers, t);
             for (int k = tid; k < K; k += kDecThreads) ws[16 + l * K + k] = 1;
         }
         for (int j = 0; j < kAccStages - 1; ++j) {
@@ -521,9 +605,44 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     }
 }
 
+// Layers summed in place (plain sum only): one warp per tile, no staging. For each
+// learner in order the warp finds where the tile's codes start and the prefix of
+// its bins' counts, then each lane takes a contiguous run of the codes and adds
+// sign * s_k to the dense elements in global memory; the warp's barrier after each
+// learner keeps learner order for every element.
+__global__ void __launch_bounds__(kDecThreads) sparse_accumulate_kernel(const __grid_constant__ KGroup g,
+                                                                        const __grid_constant__ DecodeParams p,
+                                                                        uint8_t* ws)
+{
+    extern __shared__ uint32_t sp_dyn[];  // per warp: the bins' count prefix
+    __shared__ LayerIndex X;
+    for (int e = threadIdx.x; e < g.num_layers; e += kDecThreads) X.tb[e] = g.layer[e].tile_begin;
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t T = g.total_tiles;
+    const uint32_t t = blockIdx.x * (kDecThreads / 32) + warp;
+    if (t >= T) return;
+    const AccTile A = acc_tile(g, X, t);
+    const int l = A.layer;
+    if (!sparse_flags(ws)[l]) return;
+    const KLayer& ly = g.layer[l];
+    uint32_t* pre = sp_dyn + warp * (g.max_bins + 2);
+    float* sd = p.dense[l] + A.ts;
+    const int K = p.K;
+    for (int k = 0; k < K; ++k) {
+        const uint64_t off = tile_offsets(ws, k, T)[t];
+        if (off == kBadOffset) continue;
+        const uint8_t* msg = p.msg[l * K + k];
+        uint32_t before = 0;
+        const uint32_t total = acc_prefix(A, msg, 0, A.bins, pre, &before, lane);
+        acc_walk(ly, A, msg, off, before, total, 0, A.bins, sd, pre, ws + 16 + l * K + k, lane);
+    }
+}
+
 struct DecDeviceInfo {
     int sms = 0;
     uint32_t smem_set[2] = {0, 0};  // per accumulate kernel (plain sum, fused SGD)
+    uint32_t sparse_smem_set = 0;
 };
 DecDeviceInfo g_ddev[64];
 
@@ -543,9 +662,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     uint8_t* w = static_cast<uint8_t*>(ws);
     const uint64_t tasks = (uint64_t)p.K * g.total_tiles;
     const uint64_t wpb = kDecThreads / 32;
-    uint64_t sgrid = (tasks + wpb - 1) / wpb;
-    if (sgrid > (uint64_t)di.sms * 16) sgrid = (uint64_t)di.sms * 16;
-    tile_sums_kernel<<<(unsigned)sgrid, kDecThreads, 0, stream>>>(g, p, w);
+    tile_sums_kernel<<<(unsigned)((tasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     tile_scan_kernel<<<(unsigned)(g.num_layers * p.K), 1024, 0, stream>>>(g, p, w);
@@ -568,6 +685,17 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     const long long cap = (long long)di.sms * occ;
     const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
     kern<<<grid, kDecThreads, smem, stream>>>(g, p, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess || sgd) return e;
+    // the layers summed in place (the kernel skips the others)
+    const uint32_t sp_smem = (kDecThreads / 32) * ((uint32_t)g.max_bins + 2) * 4;
+    if (sp_smem > 48 * 1024 && sp_smem > di.sparse_smem_set) {
+        e = cudaFuncSetAttribute(sparse_accumulate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp_smem);
+        if (e != cudaSuccess) return e;
+        di.sparse_smem_set = sp_smem;
+    }
+    const uint32_t sp_grid = (g.total_tiles + kDecThreads / 32 - 1) / (kDecThreads / 32);
+    sparse_accumulate_kernel<<<sp_grid, kDecThreads, sp_smem, stream>>>(g, p, w);
     return cudaGetLastError();
 }
 
