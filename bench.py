@@ -135,10 +135,23 @@ def algorithmic_bytes(layers, nnz, K):
     return stream, post, dec
 
 
-def source_hash():
+# The source files each profiled kernel is built from (its .cu and the headers it includes).
+KERNEL_SOURCES = {
+    "slice_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
+    "slice_emit_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
+    "compress_kernel": ("compress.cu", "compress_common.cuh", "adacomp_internal.cuh"),
+    "accumulate_kernel": ("decode.cu", "adacomp_internal.cuh"),
+    "sparse_accumulate_kernel": ("decode.cu", "adacomp_internal.cuh"),
+}
+
+
+def source_hash(kernel=None):
+    """sha256 prefix of a kernel's source files (all of csrc/ when kernel is None)."""
+    d = os.path.join(ROOT, "residual_gradient_compression_gb300", "csrc")
+    names = KERNEL_SOURCES.get(kernel) or sorted(os.listdir(d))
     h = hashlib.sha256()
-    for name in sorted(os.listdir(os.path.join(ROOT, "residual_gradient_compression_gb300", "csrc"))):
-        with open(os.path.join(ROOT, "residual_gradient_compression_gb300", "csrc", name), "rb") as f:
+    for name in names:
+        with open(os.path.join(d, name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
@@ -160,7 +173,7 @@ def profiled_traffic(kernel: str, workload: str):
             rec = json.load(f)
     except Exception:
         return None
-    if rec.get("source_sha") != source_hash():
+    if rec.get("source_sha") != source_hash(kernel):
         return None
     return rec.get("dram_bytes_per_launch")
 

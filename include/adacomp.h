@@ -38,12 +38,13 @@
  *   - Argument errors are reported synchronously before anything is enqueued.
  *     ADACOMP_ERR_CUDA reports a failed launch (cudaGetLastError).
  *   - Workspaces: a compress workspace must be zero-filled before its first use
- *     (e.g. torch.zeros); every completed compress call leaves it zero-filled again
- *     except for its result area, so it can be reused by later calls and by other
- *     handles that fit in it. Calls that share a workspace must not overlap on the
+ *     (e.g. torch.zeros); every completed compress call leaves the parts that must
+ *     start at zero zeroed again (the rest is written before it is read), so it can
+ *     be reused by later calls and by other handles that fit in it. Calls that share a workspace must not overlap on the
  *     GPU (use one stream, or order the streams). After any device-side error
  *     status, zero the workspace again before reusing it.
- *   - Device-side waits (the look-back between tiles) are bounded by a timeout
+ *   - Device-side waits (for the bulk copies into shared memory, and, for bin
+ *     lengths outside 16..509, the look-back between tiles) are bounded by a timeout
  *     (default 2 s, adacomp_set_timeout_ns); on expiry the kernel records
  *     ADACOMP_ERR_TIMEOUT in the workspace and returns. Nothing traps.
  *   - L_T (bin_len) is limited to 1..8192 by this implementation (the format itself
@@ -67,7 +68,7 @@ typedef enum {
     ADACOMP_ERR_WORKSPACE = 3,    /* ws is NULL or smaller than the size init returned */
     ADACOMP_ERR_CAPACITY = 4,     /* msg_capacity < max_msg_bytes */
     ADACOMP_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
-    ADACOMP_ERR_TIMEOUT = 6,      /* device: a bounded wait between tiles ran out */
+    ADACOMP_ERR_TIMEOUT = 6,      /* device: a bounded wait (a copy, or the look-back between tiles) ran out */
     ADACOMP_ERR_BAD_MESSAGE = 7   /* device: a message's B, counts or offsets do not fit this layer */
 } adacomp_status;
 
@@ -137,8 +138,10 @@ adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* d
  * Same arguments, checks and results as adacomp_compress, but the compress
  * workspace is a 1 MiB array inside the library (a file-scope __device__ array that
  * every GPU loading the library keeps until the process exits). It therefore
- * takes single-layer handles whose compress_ws_bytes is at most 1 MiB (about
- * 260M elements at L_T = 50 or 500); larger layers get ADACOMP_ERR_WORKSPACE.
+ * takes single-layer handles whose compress_ws_bytes is at most 1 MiB: about 3.9M
+ * elements for 16 <= L_T <= 509 (whose workspace holds two bits per element) and
+ * about 260M elements for other bin lengths; larger layers get
+ * ADACOMP_ERR_WORKSPACE.
  * The call allocates nothing: it zeroes the part of the array it uses
  * (cudaMemsetAsync) and runs the same kernels on `stream`.
  *   result_out  optional device buffer of 32 bytes, 8-byte aligned, that receives
@@ -206,8 +209,9 @@ adacomp_status adacomp_decode_status(adacomp_layer_t h, const void* ws, cudaStre
 /*
  * Measurement hook (not part of the method): when set, every later compress call
  * on this handle records `before` on its stream before the streaming kernel, `mid`
- * between the streaming and the fix-up kernel, and `after` once both are enqueued,
- * so cudaEventElapsedTime gives each kernel's duration. The events are created and
+ * between the streaming kernel and the kernels after it (scale, codes, fix-up), and
+ * `after` once all are enqueued, so cudaEventElapsedTime gives the streaming
+ * kernel's duration and that of the rest. The events are created and
  * owned by the caller; pass NULLs to stop recording.
  */
 adacomp_status adacomp_set_timing_events(adacomp_layer_t h, cudaEvent_t before, cudaEvent_t mid,
@@ -215,10 +219,11 @@ adacomp_status adacomp_set_timing_events(adacomp_layer_t h, cudaEvent_t before, 
 
 /*
  * Fault injection for tests of the device-side timeout (not part of the method):
- * when skip_tile is a valid tile index of this handle's next compress calls, that
- * tile never publishes its look-back descriptor, so the tiles after it in its layer
- * wait for it until the timeout and the layer reports ADACOMP_ERR_TIMEOUT. Nothing
- * faults or hangs. Pass 0xFFFFFFFF to switch it off (the default). After such a
+ * when skip_tile is a valid tile index of this handle's next compress calls, the
+ * bulk copies of that tile are never started when every layer has 16 <= L_T <= 509
+ * (its warps' waits run out), and otherwise the tile never publishes its look-back
+ * descriptor (the tiles after it in its layer wait for it); either way the layer
+ * reports ADACOMP_ERR_TIMEOUT once the timeout has passed. Nothing faults or hangs. Pass 0xFFFFFFFF to switch it off (the default). After such a
  * call, zero the workspace before reusing it.
  */
 adacomp_status adacomp_set_fault_injection(adacomp_layer_t h, uint32_t skip_tile);
@@ -270,12 +275,12 @@ adacomp_status adacomp_set_selection_rule(adacomp_layer_t h, int32_t rule);
  * residue = fl32(G - sign(G) * s_prev) to them as it loads them, before forming its
  * own G, and adacomp_materialize applies them on demand. Messages, s and every
  * later step are bit-identical to the eager path; the residue buffer holds the
- * eager residue only after adacomp_materialize. No fix-up kernel runs for layers
- * whose bins take warp-sliced tiles (16 <= L_T <= 509); other layers are fixed up
- * eagerly as before.
+ * eager residue only after adacomp_materialize. The fix-up is deferred for layers
+ * with 16 <= L_T <= 509; other layers are fixed up eagerly as before.
  *
- * The workspace grows by 512 bytes per tile: *compress_ws_bytes receives the new
- * size, and the workspace must be zero-filled before its first use. Consecutive
+ * *compress_ws_bytes receives the workspace size in this mode (it grows by 512
+ * bytes per tile unless every layer has 16 <= L_T <= 509, whose workspace holds the
+ * masks in both modes), and the workspace must be zero-filled before its first use. Consecutive
  * calls must use the same workspace; materialise before checkpointing the residue,
  * before switching the mode off, or after a call that reported an error (then also
  * zero the workspace). adacomp_compress_static_ws rejects such handles

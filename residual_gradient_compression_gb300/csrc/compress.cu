@@ -1,6 +1,9 @@
-// AdaComp compression for sm_103a: one fused streaming kernel per launch group
-// (G, H, bin maxima, selection, per-bin counts, code compaction with a decoupled
-// look-back across tiles, residue := G) and one sparse fix-up kernel that applies
+// AdaComp compression for sm_103a, the look-back path: launch groups with a layer
+// whose bin length lies outside 16..509 (groups whose layers all have
+// 16 <= L_T <= 509 take the sliced path of compress_sliced.cu). One fused streaming
+// kernel per launch group (G, H, bin maxima, selection, per-bin counts, code
+// compaction with a decoupled look-back across tiles, residue := G), a finalise
+// kernel (s, header) and one sparse fix-up kernel that applies
 // residue -= sign(G) * s once s, the mean of the bin maxima, is known.
 //
 // Method: "AdaComp (Adaptive Residual Gradient Compression)", Claims > Mechanism
@@ -9,18 +12,14 @@
 // |H| >= g_max(i) as sign(G) * s, residue = G - G_q (sent) or G (kept). Code widths:
 // Claims > Application #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers.
 //
-// Data flow per tile (a whole number of bins, about 4K elements):
-//   bulk copy (TMA, cp.async.bulk) residue + dW -> shared memory, double-buffered;
-//   phase A: G = residue + dW written back over the residue slice, per-chunk
-//            max |G| reduced with redux.sync into g_max[bin];
-//   bulk copy G -> residue in global memory (the final value of every kept element);
-//   phase C: H = G + dW, flag = G != 0 && |H| >= g_max[bin]; warp ballots give each
-//            code's rank; codes are staged in shared memory in element order;
-//   look-back: the tile's code count is published and its exclusive prefix is
-//            gathered from predecessor tiles (Merrill & Garland's single-pass scan);
-//   codes and counts are written into the message; the bin maxima are added,
-//   exactly, to the layer's exponent-bucketed integer accumulator.
-// The tile that completes a layer turns the exact sum into s and writes the header.
+// Data flow per tile (a whole number of bins, up to 8192 elements):
+//   bulk copy (cp.async.bulk) residue + dW -> shared memory, double-buffered;
+//   compute warps: G and the bin maxima, then flags, per-bin counts and codes
+//            (warp-sliced tiles of a mixed group: per warp, without block barriers);
+//   a look-back warp per staging buffer publishes the tile's code count, resolves its
+//            exclusive prefix from predecessor tiles (Merrill & Garland's single-pass
+//            scan), writes the counts and copies the staged codes into the message,
+//            and adds the bin maxima, exactly, to the layer's exponent buckets.
 #include "adacomp_internal.cuh"
 #include "compress_common.cuh"
 
@@ -543,18 +542,6 @@ struct TileGeo {
     int bins;
 };
 
-
-// Bounded wait on a stage's mbarrier phase; true when the data has landed.
-__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity, uint64_t timeout_ns)
-{
-    uint64_t start = 0;
-    while (!ptx::mbar_try_wait(bar, parity)) {
-        const uint64_t now = ptx::globaltimer();
-        if (start == 0) start = now;
-        else if (now - start > timeout_ns) return false;
-    }
-    return true;
-}
 
 #define ADACOMP_DISPATCH(V, BF, CALL)                                   \
     switch ((V) * 2 + (BF)) {                                           \
@@ -1236,7 +1223,6 @@ __global__ void __launch_bounds__(cta_threads(kNB), 2) compress_kernel(const __g
             uint32_t* gmax_c = gmax_s + bf * bin_stride;
             uint32_t* cnt_c = cnt_s + bf * bin_stride;
             const int pr = (int)(G.ts & 3), pd = ly.dw_bf16 ? (int)(G.ts & 7) : pr;
-            const int64_t te = G.ts + G.tl;
             uint16_t* stg = stg0 + bf * stg_stride;
             Slot& sl = ctl->slot[bf];
             const uint32_t t_next = t + 2 * GS;
@@ -1530,14 +1516,13 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
     }
     int paths = 0;
     for (int l = 0; l < g.num_layers; ++l) paths |= g.layer[l].bpw ? 1 : 2;
-    // four staging buffers where every layer is warp-sliced (short tiles), else three
-    const int nb = paths == 1 ? 4 : 3;
+    // here some layer is not warp-sliced (paths 2 or 3); three staging buffers
+    const int nb = 3;
     const SmemPlan P = smem_plan(g.tile_cap, g.d_size, g.max_bins, g.num_layers, g.needs_gbuf, nb);
     void (*kern)(KGroup, uint8_t*);
-    if (paths == 1) kern = g.lazy ? compress_kernel<1, 4, true> : compress_kernel<1, 4, false>;
-    else if (paths == 2) kern = compress_kernel<2, 3, false>;  // no warp-sliced layer: nothing is deferred
+    if (paths == 2) kern = compress_kernel<2, 3, false>;  // no warp-sliced layer: nothing is deferred
     else kern = g.lazy ? compress_kernel<3, 3, true> : compress_kernel<3, 3, false>;
-    const int kidx = paths == 1 ? (g.lazy ? 1 : 0) : paths == 2 ? 2 : (g.lazy ? 3 : 4);
+    const int kidx = paths == 2 ? 2 : (g.lazy ? 3 : 4);
     const int threads = cta_threads(nb);
     if (P.total > di.smem_set[kidx]) {
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);

@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
 constexpr int kEmitThreads = 256;
 constexpr int kEmitWarps = kEmitThreads / 32;
 constexpr int kFixCap = 1024;  // listed elements per warp before a flush
-constexpr int kFixBatch = 8;
+constexpr int kFixBatch = 4;
 
 // The listed elements j = 0..n-1 of a tile (tile element indices, in code order):
 // G is loaded from the residue (8 per lane at a time, all loads issued first), the
