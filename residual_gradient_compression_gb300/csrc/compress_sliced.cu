@@ -33,6 +33,7 @@ namespace {
 
 constexpr int kSlots = 512;              // slots of a warp slice: 16 per lane
 constexpr int kBkLo = 96, kBkN = 64;     // per-warp exponent buckets: biased exponents [96, 160)
+constexpr int kBkSlices = 8;             // slices between flushes: 8 x 31 maxima below 2^24 fit 32 bits
 constexpr uint32_t kRBytes = kSlots * 4;  // residue stage
 constexpr uint32_t kDBytes32 = kSlots * 4;
 constexpr uint32_t kDBytes16 = 1152;      // bf16 dW stage: up to 520 elements from the 16-byte boundary before slot 0
@@ -47,7 +48,7 @@ __host__ __device__ inline SlicePlan slice_plan(uint32_t d_size, int stages, int
     p.stage_bytes = kRBytes + p.d_bytes;
     p.stages_bytes = kWarps * stages * p.stage_bytes;
     p.layer_bytes = (uint32_t)num_layers * 64u;
-    p.total = p.stages_bytes + p.layer_bytes + kWarpScratchBytes + kWarps * kBkN * 8 + kWarps * stages * 8;
+    p.total = p.stages_bytes + p.layer_bytes + kWarpScratchBytes + kWarps * kBkN * 4 + kWarps * stages * 8;
     return p;
 }
 
@@ -152,6 +153,21 @@ __device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, uin
     return true;
 }
 
+// Adds a warp's 32-bit exponent buckets to layer lw's exact accumulator and clears them.
+__device__ __forceinline__ void flush_hist(uint32_t* hist, LayerWs* lw, int lane)
+{
+    __syncwarp();
+#pragma unroll
+    for (int e = lane; e < kBkN; e += 32) {
+        const uint32_t v = hist[e];
+        if (v) {
+            atomicAdd(&lw->acc[kBkLo + e], (unsigned long long)v);
+            hist[e] = 0u;
+        }
+    }
+    __syncwarp();
+}
+
 // Geometry of one lane's 16 slots within its slice (shared by the streaming and
 // the emitting kernels): slot i holds tile element lane_e + i.
 struct LaneGeo {
@@ -197,7 +213,7 @@ __device__ __forceinline__ uint32_t to_slot_order(uint32_t r, int rot)
 // with 128-bit stores; the stage is then refilled with the warp's slice S ahead.
 // Bin maxima and counts go through the warp's scratch (shared atomics, at most two
 // bins per lane), the counts into the message and the maxima into the warp's
-// exponent buckets (flushed to the layer's accumulator when the warp moves on to
+// exponent buckets (flushed to the layer's accumulator every 8 slices and when the warp moves on to
 // another layer). The sent and sign masks and the warp's code count go to the
 // workspace.
 //
@@ -218,10 +234,9 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
     KLayer* lays = reinterpret_cast<KLayer*>(smem + P.stages_bytes);
     uint32_t* wg = reinterpret_cast<uint32_t*>(smem + P.stages_bytes + P.layer_bytes) + warp * 2 * kWarpScratch;
     uint32_t* wc = wg + kWarpScratch;
-    unsigned long long* hist =
-        reinterpret_cast<unsigned long long*>(smem + P.stages_bytes + P.layer_bytes + kWarpScratchBytes) + warp * kBkN;
+    uint32_t* hist = reinterpret_cast<uint32_t*>(smem + P.stages_bytes + P.layer_bytes + kWarpScratchBytes) + warp * kBkN;
     uint64_t* bar = reinterpret_cast<uint64_t*>(smem + P.stages_bytes + P.layer_bytes + kWarpScratchBytes +
-                                                kWarps * kBkN * 8) + warp * S;
+                                                kWarps * kBkN * 4) + warp * S;
     auto stage_r = [&](int s) { return reinterpret_cast<float*>(stages + s * P.stage_bytes); };
     auto stage_d = [&](int s) { return static_cast<void*>(stages + s * P.stage_bytes + kRBytes); };
 
@@ -233,8 +248,8 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
     wg[lane] = 0u;
     wc[lane] = 0u;
     if (lane < kWarpScratch - 32) { wg[32 + lane] = 0u; wc[32 + lane] = 0u; }
-    hist[lane] = 0ull;
-    hist[32 + lane] = 0ull;
+    hist[lane] = 0u;
+    hist[32 + lane] = 0u;
     if (lane == 0) {
         for (int s = 0; s < S; ++s) ptx::mbar_init(&bar[s], 1);
         ptx::fence_mbar_init();
@@ -264,7 +279,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
     }
     __syncwarp();
 
-    int lo = 0, hist_layer = -1;
+    int lo = 0, hist_layer = -1, hist_slices = 0;
     bool poisoned = false;
     uint32_t i_poison = 0;
     for (uint32_t i = 0;; ++i) {
@@ -284,11 +299,12 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
             continue;
         }
         if (lane == 0) inflight &= ~(1u << s);
-        if (Sl.layer != hist_layer) {
-            if (hist_layer >= 0)
-                flush_buckets<kBkLo, kBkN>(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+        if (Sl.layer != hist_layer || hist_slices == kBkSlices) {
+            if (hist_layer >= 0) flush_hist(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
             hist_layer = Sl.layer;
+            hist_slices = 0;
         }
+        ++hist_slices;
         const LaneGeo q = lane_geo(Sl, ly, lane);
         const uint32_t lomask = q.split >= kSeg ? 0xffffu : ((1u << max(q.split, 0)) - 1u);  // slots of bin_lo
         // register order: chunk k of the lane is held at registers 4k..4k+3 and is
@@ -400,7 +416,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
             if (u) {
                 const uint32_t E = u >> 23;
                 const unsigned long long M = E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu);
-                if (E - kBkLo < (uint32_t)kBkN) atomicAdd(&hist[E - kBkLo], M);
+                if (E - kBkLo < (uint32_t)kBkN) atomicAdd(&hist[E - kBkLo], (uint32_t)M);
                 else atomicAdd(&lw->acc[E], M);
             }
         }
@@ -415,8 +431,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
             if (total) atomicAdd(&tile_tot[t], total);
         }
     }
-    if (hist_layer >= 0)
-        flush_buckets<kBkLo, kBkN>(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
+    if (hist_layer >= 0) flush_hist(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
     if (poisoned && lane == 0) {
         // copies that may still be in flight get one more bounded wait before the
         // CTA's shared memory is released

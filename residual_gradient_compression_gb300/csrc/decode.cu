@@ -469,37 +469,33 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     __shared__ LayerIndex X;
     load_index(X, g, ws, p.K, kSGD);
     __syncthreads();
+    // The CTA's tiles are G0, G0 + GS, ...; tiles of layers summed in place (by the
+    // sparse kernel) are jumped over a layer at a time.
+    auto next_tile = [&](uint32_t t) -> uint32_t {
+        while (t < T) {
+            const int l = layer_of(X.tb, g.num_layers, t);
+            if (!X.sparse[l]) return t;
+            const uint32_t te = l + 1 < g.num_layers ? X.tb[l + 1] : T;
+            t += ((te - t + GS - 1) / GS) * GS;  // the CTA's first tile at or after te
+        }
+        return T;
+    };
+    static_assert(kAccStages == 2, "the ring below issues one tile ahead");
+    uint32_t t = next_tile(G0);
 
     if (tid == 0) {
         for (int k = 0; k < kAccStages; ++k) ptx::mbar_init(&bar[k], 1);
         ptx::fence_mbar_init();
-        for (int i = 0; i < kAccStages - 1; ++i)
-            if (G0 + (uint32_t)i * GS < T) acc_issue<kSGD>(g, X, p, G0 + (uint32_t)i * GS, stage(i), arr_floats, &bar[i]);
+        if (t < T) acc_issue<kSGD>(g, X, p, t, stage(0), arr_floats, &bar[0]);
     }
     __syncthreads();
 
     bool poisoned = false;
     int i = 0;
-    for (;; ++i) {
-        const uint32_t t = G0 + (uint32_t)i * GS;
-        if (t >= T) break;
+    for (; t < T; ++i) {
+        const uint32_t tn = next_tile(t + GS);  // the CTA's next streamed tile
         float* st = stage(i);
         const AccTile A = acc_tile(g, X, t);
-        if (X.sparse[A.layer]) {
-            // summed in place by the sparse kernel. Its issue completed the stage's
-            // phase at once, so skipping the wait is safe: the next wait on this
-            // barrier is for the following phase. Keep the ring turning.
-            if (tid == 0) {
-                ptx::bulk_commit();
-                const uint32_t tn = t + (uint32_t)(kAccStages - 1) * GS;
-                if (tn < T) {
-                    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                    acc_issue<kSGD>(g, X, p, tn, stage(i + kAccStages - 1), arr_floats,
-                                    &bar[(i + kAccStages - 1) % kAccStages]);
-                }
-            }
-            continue;
-        }
         const KLayer& ly = g.layer[A.layer];
         const int l = A.layer;
         const int bpw = (A.bins + kDecThreads / 32 - 1) / (kDecThreads / 32);
@@ -581,61 +577,71 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
             }
             ptx::bulk_commit();
             // refill the stage whose store was committed one tile ago
-            const uint32_t tn = t + (uint32_t)(kAccStages - 1) * GS;
             if (tn < T) {
                 asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
                 acc_issue<kSGD>(g, X, p, tn, stage(i + kAccStages - 1), arr_floats, &bar[(i + kAccStages - 1) % kAccStages]);
             }
         }
+        t = tn;
     }
     if (tid == 0) ptx::bulk_wait0();
     if (poisoned) {
         // a load never completed: flag every message of this CTA's remaining tiles'
         // layers, then give the loads still in flight one more bounded wait before
         // the CTA's shared memory is released
-        for (uint32_t t = G0 + (uint32_t)i * GS; t < T; t += GS) {
-            const int l = layer_of(X.tb, g.num_layers, t);
+        for (uint32_t u = t; u < T; u += GS) {
+            const int l = layer_of(X.tb, g.num_layers, u);
             for (int k = tid; k < K; k += kDecThreads) ws[16 + l * K + k] = 1;
         }
-        for (int j = 0; j < kAccStages - 1; ++j) {
-            const int ij = i + j;
-            if (G0 + (uint32_t)ij * GS < T)
-                acc_wait(&bar[ij % kAccStages], (uint32_t)(ij / kAccStages) & 1u, g.timeout_ns);
-        }
+        // the load of the tile whose wait ran out (the next one was not issued yet)
+        acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u, g.timeout_ns);
     }
 }
 
-// Layers summed in place (plain sum only): one warp per tile, no staging. For each
-// learner in order the warp finds where the tile's codes start and the prefix of
-// its bins' counts, then each lane takes a contiguous run of the codes and adds
-// sign * s_k to the dense elements in global memory; the warp's barrier after each
-// learner keeps learner order for every element.
+// Layers summed in place (plain sum only), no staging: warp u of the grid takes
+// tiles u, u + warps, ... of those layers (the other layers are jumped over a layer
+// at a time). For each learner in order the warp finds where the tile's codes start
+// and the prefix of its bins' counts, then each lane takes a contiguous run of the
+// codes and adds sign * s_k to the dense elements in global memory; the warp's
+// barrier after each learner keeps learner order for every element.
 __global__ void __launch_bounds__(kDecThreads) sparse_accumulate_kernel(const __grid_constant__ KGroup g,
                                                                         const __grid_constant__ DecodeParams p,
                                                                         uint8_t* ws)
 {
     extern __shared__ uint32_t sp_dyn[];  // per warp: the bins' count prefix
     __shared__ LayerIndex X;
-    for (int e = threadIdx.x; e < g.num_layers; e += kDecThreads) X.tb[e] = g.layer[e].tile_begin;
+    for (int e = threadIdx.x; e < g.num_layers; e += kDecThreads) {
+        X.tb[e] = g.layer[e].tile_begin;
+        X.sparse[e] = sparse_flags(ws)[e];
+    }
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t T = g.total_tiles;
-    const uint32_t t = blockIdx.x * (kDecThreads / 32) + warp;
-    if (t >= T) return;
-    const AccTile A = acc_tile(g, X, t);
-    const int l = A.layer;
-    if (!sparse_flags(ws)[l]) return;
-    const KLayer& ly = g.layer[l];
+    const uint32_t NW = gridDim.x * (kDecThreads / 32);
     uint32_t* pre = sp_dyn + warp * (g.max_bins + 2);
-    float* sd = p.dense[l] + A.ts;
     const int K = p.K;
-    for (int k = 0; k < K; ++k) {
-        const uint64_t off = tile_offsets(ws, k, T)[t];
-        if (off == kBadOffset) continue;
-        const uint8_t* msg = p.msg[l * K + k];
-        uint32_t before = 0;
-        const uint32_t total = acc_prefix(A, msg, 0, A.bins, pre, &before, lane);
-        acc_walk(ly, A, msg, off, before, total, 0, A.bins, sd, pre, ws + 16 + l * K + k, lane);
+    uint32_t t = blockIdx.x * (kDecThreads / 32) + warp;
+    for (;;) {
+        while (t < T) {  // the warp's next tile of a layer summed in place
+            const int l = layer_of(X.tb, g.num_layers, t);
+            if (X.sparse[l]) break;
+            const uint32_t te = l + 1 < g.num_layers ? X.tb[l + 1] : T;
+            t += ((te - t + NW - 1) / NW) * NW;
+        }
+        if (t >= T) break;
+        const AccTile A = acc_tile(g, X, t);
+        const int l = A.layer;
+        const KLayer& ly = g.layer[l];
+        float* sd = p.dense[l] + A.ts;
+        for (int k = 0; k < K; ++k) {
+            const uint64_t off = tile_offsets(ws, k, T)[t];
+            if (off == kBadOffset) continue;
+            const uint8_t* msg = p.msg[l * K + k];
+            uint32_t before = 0;
+            const uint32_t total = acc_prefix(A, msg, 0, A.bins, pre, &before, lane);
+            acc_walk(ly, A, msg, off, before, total, 0, A.bins, sd, pre, ws + 16 + l * K + k, lane);
+        }
+        t += NW;
     }
 }
 
@@ -694,7 +700,9 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
         if (e != cudaSuccess) return e;
         di.sparse_smem_set = sp_smem;
     }
-    const uint32_t sp_grid = (g.total_tiles + kDecThreads / 32 - 1) / (kDecThreads / 32);
+    const uint32_t sp_need = (g.total_tiles + kDecThreads / 32 - 1) / (kDecThreads / 32);
+    const uint32_t sp_cap = (uint32_t)di.sms * 8;  // persistent: eight CTAs of eight warps per SM
+    const uint32_t sp_grid = sp_need < sp_cap ? sp_need : sp_cap;
     sparse_accumulate_kernel<<<sp_grid, kDecThreads, sp_smem, stream>>>(g, p, w);
     return cudaGetLastError();
 }
