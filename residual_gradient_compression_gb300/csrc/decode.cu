@@ -318,28 +318,54 @@ __device__ __forceinline__ uint32_t acc_prefix(const AccTile& A, const uint8_t* 
     return run;
 }
 
-__device__ __forceinline__ void acc_walk(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
-                                         uint32_t before, uint32_t total, int b0, int b1, float* sd,
-                                         const uint32_t* pre, uint8_t* bad, int lane)
+// The first kPrefetch codes of each lane's run and the learner's scale, loaded
+// before the dense tile has landed (they do not depend on it).
+constexpr int kPrefetch = 4;
+struct CodePrefetch {
+    uint32_t c[kPrefetch];
+    float s;
+};
+
+__device__ __forceinline__ void acc_fetch(const KLayer& ly, const uint8_t* msg, uint64_t off, uint32_t before,
+                                          uint32_t total, int lane, CodePrefetch& P)
 {
-    const float s = *reinterpret_cast<const float*>(msg);
+    P.s = *reinterpret_cast<const float*>(msg);
     const uint32_t per = (total + 31) / 32;
-    uint32_t i = min(total, lane * per);
-    const uint32_t iend = min(total, i + per);
-    if (i < iend) {
+    const uint32_t i0 = min(total, lane * per), iend = min(total, i0 + per);
+    const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * (off + before);
+#pragma unroll
+    for (int j = 0; j < kPrefetch; ++j) {
+        P.c[j] = 0u;
+        if (i0 + j < iend)
+            P.c[j] = ly.code_bytes == 1 ? codes[i0 + j] : reinterpret_cast<const uint16_t*>(codes)[i0 + j];
+    }
+}
+
+// Each lane takes a contiguous run of the warp's codes (the first kPrefetch from
+// P when use_prefetch), finds the bin of its first code by binary search in the warp's
+// bin prefix and walks forward, adding sign * s to sd[bin * L_T + offset].
+__device__ __forceinline__ void acc_walk_pf(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
+                                            uint32_t before, uint32_t total, int b0, int b1, float* sd,
+                                            const uint32_t* pre, uint8_t* bad, int lane, const CodePrefetch& P,
+                                            bool use_prefetch)
+{
+    const float s = use_prefetch ? P.s : *reinterpret_cast<const float*>(msg);
+    const uint32_t per = (total + 31) / 32;
+    const uint32_t i0 = min(total, lane * per);
+    const uint32_t iend = min(total, i0 + per);
+    if (i0 < iend) {
         const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * (off + before);
         const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len;
-        int lo = 0, hi = b1 - b0 - 1;  // last bin whose prefix is <= i
+        int lo = 0, hi = b1 - b0 - 1;  // last bin whose prefix is <= i0
         while (lo < hi) {
             const int mid = (lo + hi + 1) >> 1;
-            if (pre[mid] <= i) lo = mid;
+            if (pre[mid] <= i0) lo = mid;
             else hi = mid - 1;
         }
         int b = lo;
         uint32_t next = pre[b + 1];
-        for (; i < iend; ++i) {
+        auto apply = [&](uint32_t i, uint32_t code) {
             while (i >= next) next = pre[++b + 1];
-            const uint32_t code = ly.code_bytes == 1 ? codes[i] : reinterpret_cast<const uint16_t*>(codes)[i];
             const uint32_t o = code >> 1;
             const int bin = b0 + b;
             const int64_t len = (A.first_bin + bin == ly.nbins - 1) ? last_len : ly.bin_len;
@@ -349,9 +375,26 @@ __device__ __forceinline__ void acc_walk(const KLayer& ly, const AccTile& A, con
             } else {
                 *bad = 1;  // offset outside its bin: ignored, message flagged
             }
+        };
+        uint32_t i = i0;
+        if (use_prefetch) {
+#pragma unroll
+            for (int j = 0; j < kPrefetch; ++j)
+                if (i0 + j < iend) apply(i0 + j, P.c[j]);
+            i = min(iend, i0 + kPrefetch);
         }
+        for (; i < iend; ++i)
+            apply(i, ly.code_bytes == 1 ? codes[i] : reinterpret_cast<const uint16_t*>(codes)[i]);
     }
     __syncwarp();  // pre is rewritten for the next learner; this learner's additions are done
+}
+
+__device__ __forceinline__ void acc_walk(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
+                                         uint32_t before, uint32_t total, int b0, int b1, float* sd,
+                                         const uint32_t* pre, uint8_t* bad, int lane)
+{
+    CodePrefetch none;
+    acc_walk_pf(ly, A, msg, off, before, total, b0, b1, sd, pre, bad, lane, none, false);
 }
 
 // Warp `warp` owns one bin of tile A (tiles of at most 8 bins): every learner's
@@ -480,8 +523,13 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         }
         return T;
     };
-    static_assert(kAccStages == 2, "the ring below issues one tile ahead");
+    // Tile window: t (processed now) and t1 (copied into the other stage once the
+    // store of t's predecessor has read it, at the end of this iteration). (Three
+    // stages measured no faster for the plain sum, and the fused SGD step's three
+    // arrays per stage would then leave one CTA per SM.)
+    static_assert(kAccStages == 2, "the ring below holds one tile ahead");
     uint32_t t = next_tile(G0);
+    uint32_t t1 = t < T ? next_tile(t + GS) : T;
 
     if (tid == 0) {
         for (int k = 0; k < kAccStages; ++k) ptx::mbar_init(&bar[k], 1);
@@ -493,7 +541,6 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     bool poisoned = false;
     int i = 0;
     for (; t < T; ++i) {
-        const uint32_t tn = next_tile(t + GS);  // the CTA's next streamed tile
         float* st = stage(i);
         const AccTile A = acc_tile(g, X, t);
         const KLayer& ly = g.layer[A.layer];
@@ -507,13 +554,17 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
             for (int64_t q = tid; q < (A.te - A.a0 + 3) / 4; q += kDecThreads) z[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
         BinPrep bp;
+        CodePrefetch cp0;
         uint64_t off0 = kBadOffset;
         uint32_t before0 = 0, total0 = 0;
         if (bpw == 1) {
             if (b0 < b1) bp = acc_bin_prep(ly, A, p, ws, T, t, l, b0, 0, lane);
         } else if (b0 < b1) {
             off0 = tile_offsets(ws, 0, T)[t];
-            if (off0 != kBadOffset) total0 = acc_prefix(A, p.msg[l * K], b0, b1, pre, &before0, lane);
+            if (off0 != kBadOffset) {
+                total0 = acc_prefix(A, p.msg[l * K], b0, b1, pre, &before0, lane);
+                acc_fetch(ly, p.msg[l * K], off0, before0, total0, lane, cp0);
+            }
         }
         if (!__syncthreads_and(acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u, g.timeout_ns))) {
             poisoned = true;
@@ -534,7 +585,7 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
                 const uint8_t* msg = p.msg[l * K + k];
                 uint32_t before = before0, total = total0;
                 if (k) total = acc_prefix(A, msg, b0, b1, pre, &before, lane);
-                acc_walk(ly, A, msg, off, before, total, b0, b1, sd, pre, ws + 16 + l * K + k, lane);
+                acc_walk_pf(ly, A, msg, off, before, total, b0, b1, sd, pre, ws + 16 + l * K + k, lane, cp0, k == 0);
             }
         }
 
@@ -577,12 +628,13 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
             }
             ptx::bulk_commit();
             // refill the stage whose store was committed one tile ago
-            if (tn < T) {
+            if (t1 < T) {
                 asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                acc_issue<kSGD>(g, X, p, tn, stage(i + kAccStages - 1), arr_floats, &bar[(i + kAccStages - 1) % kAccStages]);
+                acc_issue<kSGD>(g, X, p, t1, stage(i + 1), arr_floats, &bar[(i + 1) % kAccStages]);
             }
         }
-        t = tn;
+        t = t1;
+        t1 = t1 < T ? next_tile(t1 + GS) : T;
     }
     if (tid == 0) ptx::bulk_wait0();
     if (poisoned) {
@@ -678,10 +730,10 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins, sgd);
     void (*kern)(KGroup, DecodeParams, uint8_t*) = sgd ? accumulate_kernel<true> : accumulate_kernel<false>;
     if (smem > di.smem_set[sgd]) {
-        if (smem > 48 * 1024) {
-            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-            if (e != cudaSuccess) return e;
-        }
+        // opted in whenever it grows: the kernel's static shared memory counts
+        // towards the 48 KB available without the opt-in
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
         di.smem_set[sgd] = smem;
     }
     int occ = 0;
@@ -695,7 +747,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     if (e != cudaSuccess || sgd) return e;
     // the layers summed in place (the kernel skips the others)
     const uint32_t sp_smem = (kDecThreads / 32) * ((uint32_t)g.max_bins + 2) * 4;
-    if (sp_smem > 48 * 1024 && sp_smem > di.sparse_smem_set) {
+    if (sp_smem > di.sparse_smem_set) {
         e = cudaFuncSetAttribute(sparse_accumulate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sp_smem);
         if (e != cudaSuccess) return e;
         di.sparse_smem_set = sp_smem;

@@ -80,6 +80,56 @@ def test_decode_group_matches_per_layer():
         assert np.array_equal(d.cpu().numpy().view(np.uint32), ref.view(np.uint32)), l.name
 
 
+def _sparse_learner_msgs(n, L, K, seed, keep=0.01):
+    """K learners' first-step messages (zero residue) for a dW that is zero except
+    for a `keep` fraction of its elements, so that few elements are sent."""
+    msgs = []
+    layer = GpuLayer(n, L, ac.F32)
+    for k in range(K):
+        g = torch.Generator(device="cuda")
+        g.manual_seed(seed + 1000 * k)
+        dw = torch.randn(n, generator=g, device="cuda") * 1e-3
+        dw *= (torch.rand(n, generator=g, device="cuda") < keep).float()
+        res = torch.zeros(n, device="cuda")
+        ac.adacomp_compress(layer.h, res, dw, layer.msg, layer.ws)
+        mb, _, st = ac.adacomp_query(layer.h, layer.ws)
+        assert st == ac.OK
+        buf = torch.zeros(((mb + 15) // 16) * 16, dtype=torch.uint8, device="cuda")
+        buf[:mb] = layer.msg[:mb]
+        msgs.append((buf, mb))
+    return msgs
+
+
+def test_decode_group_mixes_streamed_and_in_place_layers():
+    """One grouped decode over layers of every kind: warp-sliced (L_T = 50, 500) and
+    block-tiled (L_T = 7, 1000) bins, each either streamed through shared memory or,
+    when all learners together sent fewer than n/16 codes, summed in place. The
+    inputs are checked to cover all four combinations; every layer must match the
+    oracle's learner-order sum bit for bit."""
+    K = 3
+    spec = [(200_003, 50, False), (300_001, 500, True), (50_001, 7, False), (123_457, 1000, True),
+            (40_000, 500, False)]
+    per_layer = [(_sparse_learner_msgs if sparse else _learner_msgs)(n, L, K, seed=7 * i + 1)
+                 for i, (n, L, sparse) in enumerate(spec)]
+    kinds = set()
+    for (n, L, _), pl in zip(spec, per_layer):
+        B = -(-n // L)
+        w = 1 if L < 64 else 2
+        codes = sum((mb - 8 - 2 * B) // w for _, mb in pl)
+        kinds.add((16 <= L <= 509, 16 * codes < n))
+    assert kinds == {(True, True), (True, False), (False, True), (False, False)}, kinds
+    h = ac.adacomp_init_group([n for n, _, _ in spec], [L for _, L, _ in spec], [ac.F32] * len(spec))
+    dense0 = [torch.randn(n, device="cuda") * 1e-3 for n, _, _ in spec]
+    dense = [d.clone() for d in dense0]
+    ws = workspace(h.decode_ws_bytes(K))
+    ac.adacomp_decode_accumulate_group(h, [[m for m, _ in pl] for pl in per_layer], dense, ws)
+    assert ac.adacomp_decode_status(h, ws) == ac.OK
+    for (n, L, _), pl, d0, d in zip(spec, per_layer, dense0, dense):
+        ref = d0.cpu().numpy()
+        assert oracle.decode_accumulate(n, L, [m[:mb].cpu().numpy() for m, mb in pl], ref) == oracle.OK
+        assert np.array_equal(d.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (n, L)
+
+
 def test_flat100m_four_learners_end_to_end():
     """Full-size flat layer (10^8 elements, L_T = 500): 4 learners compress their own
     N(0, 1e-3) dW, then one decode sums the 4 messages."""
