@@ -306,18 +306,31 @@ class DeviceRun:
                               for s in range(self.sets)])
         self.c_dec_msgs = [(VP * (len(g) * self.K))(*[self.msg[k][1][i].data_ptr() for i in g
                                                         for k in range(self.K)]) for g in self.gidx]
+        self.msg_sets = [(self.msg, self.c_msg, self.c_dec_msgs)]
         self.c_dense = [(VP * len(g))(*[self.dense[1][i].data_ptr() for i in g]) for g in self.gidx]
+
+    def add_msg_set(self):
+        """A second set of message buffers (and their pointer arrays), so that one
+        step's messages can be copied to the host while the next step writes its own."""
+        VP = self.ct.c_void_p
+        maxmsg = [m for h in self.h for m in h.max_msg_bytes]
+        msg = [_flat_views(maxmsg, torch.uint8, self.dev) for _ in range(self.K)]
+        c_msg = [[(VP * len(g))(*[msg[k][1][i].data_ptr() for i in g]) for g in self.gidx] for k in range(self.K)]
+        c_dec = [(VP * (len(g) * self.K))(*[msg[k][1][i].data_ptr() for i in g for k in range(self.K)])
+                 for g in self.gidx]
+        self.msg_sets.append((msg, c_msg, c_dec))
 
     def launches_per_step(self):
         # compress: streaming kernel, finalise, codes + fix-up; decode: sums, scan, accumulate (staged
         # and in place)
         return self.K * len(self.gidx) * 3 + len(self.gidx) * 4
 
-    def step(self, i, stream_ptr, k1_events=None, dec_events=None, ws_fixed=None):
+    def step(self, i, stream_ptr, k1_events=None, dec_events=None, ws_fixed=None, msg_set=0):
         """Enqueues one step: every learner's compress, then the decode of the step's messages.
         ws_fixed: one workspace per (learner, group) used by every step (a deferred
         fix-up keeps its pending corrections there), instead of the per-step ring."""
         L, s = self.L, i % self.sets
+        _, c_msg, c_dec_msgs = self.msg_sets[msg_set]
         for k in range(self.K):
             for gi, h in enumerate(self.h):
                 if k1_events is not None:
@@ -326,14 +339,14 @@ class DeviceRun:
                                                 self.ct.c_void_p(e[1].cuda_event),
                                                 self.ct.c_void_p(e[2].cuda_event))
                 ws = ws_fixed[k][gi] if ws_fixed is not None else self.ws[i % self.ring][k][gi]
-                st = L.adacomp_compress_group(h.ptr, self.c_res[k][gi], self.c_dw[k][s][gi], self.c_msg[k][gi],
+                st = L.adacomp_compress_group(h.ptr, self.c_res[k][gi], self.c_dw[k][s][gi], c_msg[k][gi],
                                               self.c_cap[k][gi], ws.data_ptr(), ws.numel(), stream_ptr)
                 if st:
                     raise RuntimeError(f"adacomp_compress_group: {st}")
         if dec_events is not None:
             dec_events[0].record()
         for gi, h in enumerate(self.h):
-            st = L.adacomp_decode_accumulate_group(h.ptr, self.c_dec_msgs[gi], self.K, self.c_dense[gi],
+            st = L.adacomp_decode_accumulate_group(h.ptr, c_dec_msgs[gi], self.K, self.c_dense[gi],
                                                    self.dec_ws[gi].data_ptr(), self.dec_ws[gi].numel(),
                                                    stream_ptr)
             if st:
@@ -558,48 +571,114 @@ def run_lazy(args, run, sp, world, n_elems):
             "ms_per_step": ms / args.steps, "timed_repetitions": len(reps)}
 
 
+E2E_UPLOAD_STREAMS = 1  # copy streams for the uploads (four measured no faster than one)
+
+
 def run_e2e(args, run, layers, sp, world):
     """Same steps through the C ABI with host buffers: each step copies its dW from
     pinned host memory, runs the path, reads every message length and copies the
-    messages back to pinned host memory."""
+    messages back to pinned host memory (runs of neighbouring messages).
+
+    The copies overlap the computation of neighbouring steps: the dW of step i goes
+    up on copy streams (into the dW slot step i uses, once the step that last used
+    it is done), the results area of step i comes back on the compute stream, and the
+    messages of step i go down on a second copy stream from one of two message
+    buffer sets while step i + 1 computes into the other."""
     numels = [l.numel for l in layers]
     host_dw = []
     for k in range(run.K):
         buf, views = _flat_views(numels, run.dw_dtype, "cpu", pinned=True)
         buf.copy_(run.dw[k][0][0][:buf.numel()])
         host_dw.append(buf)
+    if len(run.msg_sets) < 2:
+        run.add_msg_set()
     host_msg = [torch.empty(run.msg[k][0].numel(), dtype=torch.uint8, pin_memory=True) for k in range(run.K)]
     msg_offs = [[v.data_ptr() - run.msg[k][0].data_ptr() for v in run.msg[k][1]] for k in range(run.K)]
+    res_bytes = [64 + 2112 * len(g) for g in run.gidx]  # control block and per-layer results of a group
+    host_res = [[[torch.empty(rb, dtype=torch.uint8, pin_memory=True) for rb in res_bytes] for _ in range(run.K)]
+                for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    ups = [torch.cuda.Stream() for _ in range(E2E_UPLOAD_STREAMS)]
+    down = torch.cuda.Stream()
     steps = args.steps
     h2d = d2h = 0
+    slot_free = [None] * run.sets   # compute of the step that last read each dW slot
+    msgs_free = [None, None]        # message copies of the step that last wrote each set
+    res_ready = [None, None]
+
+    def messages_down(j):
+        """Enqueues the message copies of step j (its results area is on the host)."""
+        nonlocal d2h
+        res_ready[j % 2].synchronize()
+        msg = run.msg_sets[j % 2][0]
+        down.wait_event(res_ready[j % 2])
+        with torch.cuda.stream(down):
+            for k in range(run.K):
+                spans = []  # (offset, length) of each message in the learner's buffer
+                li = 0
+                for gi, g in enumerate(run.gidx):
+                    blk = host_res[j % 2][k][gi].numpy()
+                    for jj in range(len(g)):
+                        o = 64 + 2112 * jj + 2064
+                        status = int(blk[o + 4:o + 8].view(np.uint32)[0])
+                        if status != 0:
+                            raise RuntimeError(f"device status {status} in the e2e leg")
+                        spans.append((msg_offs[k][li], int(blk[o + 16:o + 24].view(np.uint64)[0])))
+                        li += 1
+                # one copy per run of messages: neighbours whose gap (the unused tail of
+                # a buffer sized for the worst case) is under 256 KB share a copy
+                runs = []
+                for off, ln in sorted(spans):
+                    if runs and off - runs[-1][1] < (256 << 10):
+                        runs[-1][1] = off + ln
+                    else:
+                        runs.append([off, off + ln])
+                for r0, r1 in runs:
+                    host_msg[k][r0:r1].copy_(msg[k][0][r0:r1], non_blocking=True)
+                    d2h += r1 - r0
+        ev = torch.cuda.Event()
+        ev.record(down)
+        msgs_free[j % 2] = ev
+
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
     for i in range(steps):
         slot = i % run.sets
+        for u, up in enumerate(ups):  # each stream uploads one contiguous part of every learner's dW
+            if slot_free[slot] is not None:
+                up.wait_event(slot_free[slot])
+            with torch.cuda.stream(up):
+                for k in range(run.K):
+                    n = host_dw[k].numel()
+                    a, b = n * u // len(ups), n * (u + 1) // len(ups)
+                    run.dw[k][slot][0][a:b].copy_(host_dw[k][a:b], non_blocking=True)
+                    h2d += (b - a) * host_dw[k].element_size()
+            inputs_up = torch.cuda.Event()
+            inputs_up.record(up)
+            comp.wait_event(inputs_up)
+        if msgs_free[i % 2] is not None:
+            comp.wait_event(msgs_free[i % 2])
+        run.step(i, sp, msg_set=i % 2)
         for k in range(run.K):
-            dst = run.dw[k][slot][0]
-            dst[:host_dw[k].numel()].copy_(host_dw[k], non_blocking=True)
-            h2d += host_dw[k].numel() * host_dw[k].element_size()
-        run.step(i, sp)
-        res = run.step_results(i)  # synchronises: message lengths are on the device
-        d2h += sum(len(g) for g in run.gidx) * 2112 * run.K
-        j = 0
-        for k in range(run.K):
-            # one copy per learner: from the first message to the end of the last one
-            # (the buffer holds every layer's message at a fixed offset)
-            end = 0
-            for li in range(len(layers)):
-                end = max(end, msg_offs[k][li] + res[j][1])
-                j += 1
-            host_msg[k][:end].copy_(run.msg[k][0][:end], non_blocking=True)
-            d2h += end
+            for gi in range(len(run.gidx)):
+                ws = run.ws[i % run.ring][k][gi]
+                host_res[i % 2][k][gi].copy_(ws[:res_bytes[gi]], non_blocking=True)
+        d2h += run.K * sum(res_bytes)
+        done = torch.cuda.Event()
+        done.record(comp)
+        slot_free[slot] = done
+        res_ready[i % 2] = done
+        if i >= 1:
+            messages_down(i - 1)
+    messages_down(steps - 1)
     torch.cuda.synchronize()
     secs = max_over_ranks(time.perf_counter() - t0, world)
     n_elems = sum(numels) * run.K
     return {"value": n_elems * steps * world / secs, "unit": "elements/s",
             "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
-            "ms_per_step": secs * 1e3 / steps}
+            "ms_per_step": secs * 1e3 / steps,
+            "overlap": "dW upload, compute and message download of neighbouring steps overlap"}
 
 
 # ---------------------------------------------------------------- oracle legs
