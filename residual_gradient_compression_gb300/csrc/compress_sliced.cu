@@ -445,11 +445,8 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
 // ---------------------------------------------------------------- finalise and scan
 // One CTA per layer: s from the layer's exact sum (fp64, rounded once to fp32),
 // the header {s, B}, the result area, and the exclusive prefix of the layer's tile
-// code totals (which are left zero for the next call), chunk by chunk through
-// shared memory so that every global access is coalesced.
+// code totals (which are left zero for the next call).
 constexpr int kFinThreads = 1024;
-constexpr int kFinPer = 2;                       // tiles per thread within a chunk (static shared memory < 48 KB)
-constexpr int kFinChunk = kFinThreads * kFinPer;  // tiles per chunk
 
 __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __grid_constant__ KGroup g,
                                                                      uint8_t* __restrict__ ws)
@@ -458,8 +455,6 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
     __shared__ unsigned long long words[kSumWords];
     __shared__ unsigned long long wsum[kFinThreads / 32];
     __shared__ unsigned long long layer_total;
-    __shared__ uint32_t fin_tot[kFinChunk];
-    __shared__ unsigned long long fin_excl[kFinChunk];
     const int l = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const KLayer& ly = g.layer[l];
     LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l));
@@ -469,51 +464,38 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
     if (tid < kSumWords) words[tid] = 0ull;
     if (tid < 256) tmp[tid] = lw->acc[tid];
 
-    // The tile totals go through shared memory in chunks of kFinChunk tiles, loaded
-    // and stored coalesced; within a chunk thread tid scans kFinPer consecutive tiles.
+    // thread tid scans tiles [i0, i1) of the layer
     const uint32_t nt = ly.num_tiles;
-    unsigned long long carry = 0;
-    for (uint32_t base = 0; base < nt; base += kFinChunk) {
-        const uint32_t cn = min((uint32_t)kFinChunk, nt - base);
-        for (uint32_t j = tid; j < cn; j += kFinThreads) {
-            fin_tot[j] = tot[base + j];
-            tot[base + j] = 0u;  // zero for the next call
-        }
-        __syncthreads();
-        const uint32_t j0 = min(cn, tid * (uint32_t)kFinPer), j1 = min(cn, j0 + kFinPer);
-        unsigned long long mine = 0;
-        for (uint32_t j = j0; j < j1; ++j) mine += fin_tot[j];
-        unsigned long long incl = mine;
+    const uint32_t per = (nt + kFinThreads - 1) / kFinThreads;
+    const uint32_t i0 = min(nt, tid * per), i1 = min(nt, i0 + per);
+    unsigned long long mine = 0;
+    for (uint32_t i = i0; i < i1; ++i) mine += tot[i];
+    unsigned long long incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const unsigned long long y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long v = wsum[lane], x = v;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
+            const unsigned long long y = __shfl_up_sync(kFull, x, o);
+            if (lane >= o) x += y;
         }
-        if (lane == 31) wsum[warp] = incl;
-        __syncthreads();
-        if (warp == 0) {
-            const unsigned long long v = wsum[lane];
-            unsigned long long x = v;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(kFull, x, o);
-                if (lane >= o) x += y;
-            }
-            wsum[lane] = x - v;  // exclusive over warps
-            if (lane == 31) layer_total = x;
-        }
-        __syncthreads();
-        unsigned long long run = carry + wsum[warp] + incl - mine;
-        for (uint32_t j = j0; j < j1; ++j) {
-            fin_excl[j] = run;
-            run += fin_tot[j];
-        }
-        __syncthreads();
-        for (uint32_t j = tid; j < cn; j += kFinThreads) excl[base + j] = fin_excl[j];
-        carry += layer_total;
-        __syncthreads();  // the chunk's shared arrays are reused
+        wsum[lane] = x - v;  // exclusive over warps
     }
-    if (tid == 0) layer_total = carry;
+    __syncthreads();
+    unsigned long long run = wsum[warp] + incl - mine;
+    for (uint32_t i = i0; i < i1; ++i) {
+        const uint32_t v = tot[i];
+        excl[i] = run;
+        run += v;
+        tot[i] = 0u;
+    }
+    if (tid == kFinThreads - 1) layer_total = run;  // the last thread's range ends the layer
     __syncthreads();
     const unsigned long long nnz = layer_total;
     if (warp == 0) {
