@@ -290,6 +290,15 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
         const KLayer& ly = lays[lo];
         const Slice Sl = slice_in(ly, lo, t, warp);
         LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(Sl.layer));
+        const size_t mi = ((size_t)t * kWarps + warp) * 32 + lane;  // this lane's mask word
+        // the previous call's deferred corrections (its sent mask and s), loaded while
+        // the stage's copy is still landing
+        uint32_t pm = 0;
+        float s_prev = 0.0f;
+        if (kLazy && pending) {
+            pm = sent[mi];
+            s_prev = lw->result.s;
+        }
         if (!poisoned && !__all_sync(kFull, wait_bounded(&bar[s], (i / S) & 1u, g.timeout_ns))) {
             poisoned = true;  // warp-uniform
             i_poison = i;
@@ -312,13 +321,6 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
         const uint32_t vr = to_reg_order(q.valid, rot);
         const uint32_t lor = to_reg_order(lomask, rot) & vr;  // valid slots of bin_lo
         const uint32_t hir = vr & ~lor;                        // valid slots of bin_lo + 1
-        const size_t mi = ((size_t)t * kWarps + warp) * 32 + lane;  // this lane's mask word
-        uint32_t pm = 0;
-        float s_prev = 0.0f;
-        if (kLazy && pending) {
-            pm = sent[mi];
-            s_prev = lw->result.s;
-        }
         float ah[4][4];             // |probe| per register slot
         uint32_t ngr = 0;  // G < 0 (register order; kept for the deferred fix-up's codes only)
         float m_lo = 0.0f, m_hi = 0.0f;
