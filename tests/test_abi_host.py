@@ -44,6 +44,52 @@ def test_sizes_follow_the_message_format():
         ac.adacomp_free(h)
 
 
+def _tiles(n, L):
+    """Tiles of a single layer: eight warp slices of floor(509 / L) bins for
+    16 <= L <= 509, else about 4096 elements of whole bins (at least one bin)."""
+    B = -(-n // L)
+    bpt = 8 * (509 // L) if 16 <= L <= 509 else max(1, 4096 // L)
+    bpt = min(bpt, 1024, B)
+    return -(-B // bpt)
+
+
+@pytest.mark.parametrize("n,L", [(1_000_000, 500), (777_777, 50), (65_537, 16), (10, 509)])
+def test_sliced_workspace_layout(n, L):
+    """16 <= L_T <= 509: control block, one 2112-byte layer block, then per tile a
+    u64 code offset, a u32 code total (padded to 16 bytes), eight u32 slice counts
+    and two 512-byte masks; the deferred fix-up needs no more."""
+    T = _tiles(n, L)
+    expect = 64 + 2112 + 8 * T + (-(-4 * T // 16) * 16) + 32 * T + 1024 * T
+    h = ac.adacomp_init_layer(n, L, ac.F32)
+    assert h.compress_ws_bytes == expect
+    assert ac.adacomp_set_lazy_fixup(h, True) == expect
+    assert h.decode_ws_bytes(3) == ac.DECODE_WS_FIXED + 3 * 8 * T
+    ac.adacomp_free(h)
+
+
+@pytest.mark.parametrize("n,L", [(1_000_000, 5000), (77_777, 7), (300_007, 510)])
+def test_lookback_workspace_layout(n, L):
+    """Other bin lengths: control block, layer block, a u64 descriptor and a u64
+    code offset per tile; the deferred fix-up adds a 512-byte mask per tile."""
+    T = _tiles(n, L)
+    h = ac.adacomp_init_layer(n, L, ac.F32)
+    assert h.compress_ws_bytes == 64 + 2112 + 16 * T
+    assert ac.adacomp_set_lazy_fixup(h, True) == 64 + 2112 + 16 * T + 512 * T
+    ac.adacomp_free(h)
+
+
+def test_group_workspace_takes_the_lookback_layout_when_mixed():
+    """A group is sliced only when every layer is; one block per layer."""
+    ns, Ls = [40_000, 30_000], [50, 500]
+    T = sum(_tiles(n, L) for n, L in zip(ns, Ls))
+    h = ac.adacomp_init_group(ns, Ls, [ac.F32, ac.F32])
+    assert h.compress_ws_bytes == 64 + 2 * 2112 + 8 * T + (-(-4 * T // 16) * 16) + 32 * T + 1024 * T
+    ns2, Ls2 = ns + [20_000], Ls + [5000]
+    T2 = T + _tiles(20_000, 5000)
+    h2 = ac.adacomp_init_group(ns2, Ls2, [ac.F32] * 3)
+    assert h2.compress_ws_bytes == 64 + 3 * 2112 + 16 * T2
+
+
 @pytest.mark.parametrize("n,L,dt", [(0, 4, 0), (-5, 4, 0), (10, 0, 0), (10, 8193, 0), (10, 4, 2)])
 def test_init_rejects_bad_arguments(n, L, dt):
     with pytest.raises(ac.AdacompError) as e:
