@@ -18,8 +18,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kRounds = 4;             // lane-vectors per chunk: chunk <= 32*VEC*kRounds elements
 constexpr int kWarpSliceMax = 509;     // warp-sliced tiles: a warp slice plus its alignment slots fits 512 slots
 constexpr int kWarpScratch = 36;       // per-warp g_max / count scratch entries (bins per slice <= 31)
-constexpr int kMaxBuffers = 4;         // code staging buffers (one look-back warp each): 4, or 3 where
-                                       // tiles are long (block-wide tiles of up to 8192 elements)
+constexpr int kMaxBuffers = 4;         // look-back path: code staging buffers (one look-back warp each);
+                                       // 3 are used (tiles of up to 8192 elements)
 constexpr int kHistLo = 64;            // per-warp exponent buckets cover biased exponents [64, 192);
 constexpr int kHistN = 128;            // maxima outside go straight to the layer's accumulator
 constexpr uint32_t kHistBytesPerBuffer = kHistN * 8;  // one set per look-back warp

@@ -18,11 +18,13 @@
 //                    are not needed yet, so no CTA ever waits for another.
 //   slice_finalize   one CTA per layer: s from the exact sum, the header, and the
 //                    exclusive prefix of the tile code totals.
-//   slice_emit       one warp per (tile, slice), last tiles first: the codes from the
-//                    masks, written at their final positions, and the fix-up
-//                    residue = fl32(G - sign(G) s) of every sent element (skipped when
-//                    the fix-up is deferred to the next call).
-// Only two masks (2 bits per element) pass between the first and the last launch.
+//   slice_emit       one warp per tile, last tiles first: the codes written at their
+//                    final positions, with the sign of G read back from the residue,
+//                    and the fix-up residue = fl32(G - sign(G) s) of every sent element
+//                    (when the fix-up is deferred to the next call, the signs come
+//                    from a second mask and the residue is not touched).
+// Only the sent mask (1 bit per element; 2 with the deferred fix-up) passes between
+// the first and the last launch.
 #include "adacomp_internal.cuh"
 #include "compress_common.cuh"
 
@@ -209,17 +211,21 @@ __device__ __forceinline__ uint32_t to_slot_order(uint32_t r, int rot)
 // Warp w of CTA c handles slice w of tiles c, c + grid, c + 2 grid, ...; its S
 // stages hold the data of its next S slices. Per slice, per lane (16 slots in
 // registers, the four 16-byte chunks visited in the bank-conflict-free rotated
-// order): G = fl32(residue + dW), |probe|, masks of G != 0 and G < 0, residue := G
-// with 128-bit stores; the stage is then refilled with the warp's slice S ahead.
-// Bin maxima and counts go through the warp's scratch (shared atomics, at most two
-// bins per lane), the counts into the message and the maxima into the warp's
-// exponent buckets (flushed to the layer's accumulator every 8 slices and when the warp moves on to
-// another layer). The sent and sign masks and the warp's code count go to the
-// workspace.
+// order): G = fl32(residue + dW), |probe| (-1 where G == 0, so that such elements
+// are never sent), the mask of G < 0 (deferred fix-up only), residue := G with
+// 128-bit stores, and the maxima of the lane's (at most two) bins; slots outside the
+// slice hold stale data and are masked out of the maxima and the sent mask. The
+// stage is then refilled with the warp's slice S ahead. Bin maxima and counts go
+// through the warp's scratch (shared atomics), the counts into the message and the
+// maxima into the warp's 32-bit exponent buckets (flushed to the layer's exact
+// accumulator every 8 slices and when the warp moves on to another layer). The
+// sent mask (and, deferred fix-up only, the sign mask) and the warp's code count go
+// to the workspace.
 //
 // kLazy: the corrections the previous call deferred (its sent mask, when the
 // workspace says they are pending) are applied as the residue is loaded,
 // fl32(G - copysign(s_prev, G)), the same rounding the fix-up would have made.
+// kLS: the Local Selection rule (the probe is G itself).
 //
 // Every wait is bounded: a copy that does not land in time marks the layer with
 // ADACOMP_ERR_TIMEOUT and the warp stops (later slices only mark their layers);
@@ -521,23 +527,24 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
 
 // ---------------------------------------------------------------- codes and fix-up
 // One warp per tile (no loop: many tiles in flight hide the latencies). Lane l
-// loads the sent and sign masks of compute lane l of all eight slices, the tile's
-// code offset, the slices' code counts and the layer's status in one batch; then,
-// slice by slice (skipping slices that sent nothing), a warp scan places each
-// lane's codes after those of the earlier lanes and slices. Code of slot i:
-// ((offset of its element in its bin) << 1) | sign. The masks are stored in the
-// streaming kernel's register order and are brought back to slot order here.
-// kFix: the sent elements, listed in shared memory in code order as
-// (tile element << 1 | sign), are then corrected by the whole warp, 8 per lane at
-// a time with all loads issued before the stores: residue (still G) becomes
-// fl32(G - s) or fl32(G + s).
+// loads the sent masks (and, without kFix, the sign masks) of compute lane l of all
+// eight slices, the tile's code offset, the slices' code counts and the layer's
+// status in one batch; then, slice by slice (skipping slices that sent nothing), a
+// warp scan places each lane's sent elements after those of the earlier lanes and
+// slices. The masks are stored in the streaming kernel's register order and are
+// brought back to slot order here. Code of an element: ((its offset in its bin)
+// << 1) | sign.
+// kFix: the sent elements are listed in shared memory in code order (their tile
+// element indices) and the whole warp then walks the list (fix_listed): G from the
+// residue, the code, and the corrected residue. Without kFix the codes are written
+// from the masks directly.
 constexpr int kEmitThreads = 256;
 constexpr int kEmitWarps = kEmitThreads / 32;
 constexpr int kFixCap = 1024;  // listed elements per warp before a flush
 constexpr int kFixBatch = 4;
 
 // The listed elements j = 0..n-1 of a tile (tile element indices, in code order):
-// G is loaded from the residue (8 per lane at a time, all loads issued first), the
+// G is loaded from the residue (kFixBatch per lane at a time, all loads issued first), the
 // code ((element - its bin's first element) << 1) | (G < 0) is written at code
 // position pos0 + j, and the residue becomes fl32(G - s) or fl32(G + s).
 __device__ __forceinline__ void fix_listed(const uint16_t* lst, uint32_t n, float* res, float s, uint8_t* codes,
