@@ -2,13 +2,14 @@
 """Benchmark of the AdaComp hot path on GB300: compress + decode-accumulate.
 
 One step = one pass of the whole path over one batch of synthetic gradients: every
-layer of the workload is compressed (fused streaming kernel + sparse fix-up) and
-the step's messages are decoded and accumulated into dense gradients. The default
-workload is the ResNet-50 gradient set (53 conv tensors at L_T = 50 with 8-bit
-codes and the 2048x1000 FC at L_T = 500 with 16-bit codes, 25.5M fp32 elements,
-carried residue), compressed by one grouped launch, with the single learner's
-messages decoded (K = 1). ``--workload flat100m`` runs 16 learners over a 10^8
-element layer and decodes all 16 messages.
+learner compresses every layer of the workload (fused streaming kernel, scale,
+codes and fix-up), the message lengths are read back (what an exchange of the
+variable-length messages would carry), and all learners' messages are decoded and
+accumulated into dense gradients. The default workload is the aggregation
+configuration: 16 learners, each with its own carried residue and N(0, 1e-3) dW
+over one flat 10^8-element fp32 layer at L_T = 500, and one decode of all 16
+messages. ``--workload resnet50 | lstm_fc | gpt1p3b | fc400k`` runs the other
+gradient sets with one learner (``gpt1p3b`` at ``--bin-len`` 50, 500 or 5000).
 
 The JSON line reports gradient elements/s (value), algorithmic HBM GB/s and their
 fraction of the measured copy bandwidth, the dominant kernel's roofline, an
@@ -39,6 +40,7 @@ from residual_gradient_compression_gb300 import workloads as wl  # noqa: E402
 
 METRIC = "gradient elements/s and HBM GB/s (% of GB300 roofline) for compress+decode"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # the GB300's nominal HBM3e bandwidth
 
 
 def parse_args():
@@ -47,7 +49,7 @@ def parse_args():
     p.add_argument("--steps", type=int, default=20)
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["adacomp", "reference"], default="adacomp")
-    p.add_argument("--workload", default="resnet50",
+    p.add_argument("--workload", default="flat100m",
                    choices=["resnet50", "fc400k", "lstm_fc", "gpt1p3b", "flat100m"])
     p.add_argument("--bin-len", type=int, default=500, help="L_T for gpt1p3b")
     p.add_argument("--learners", type=int, default=16, help="K for flat100m")
@@ -324,16 +326,54 @@ class DeviceRun:
         self.msg_sets.append((msg, c_msg, c_dec))
 
     def launches_per_step(self):
-        # compress: streaming kernel, finalise, codes + fix-up; decode: sums, scan, accumulate (staged
-        # and in place)
-        return self.K * len(self.gidx) * 3 + len(self.gidx) * 4
+        # compress: streaming kernel, finalise, codes + fix-up; decode: sums, scan, validation,
+        # accumulate (staged and in place)
+        return self.K * len(self.gidx) * 3 + len(self.gidx) * 5
+
+    RESULT_AT = 2064  # offset of a layer's result {s, status, nnz, msg_bytes} in its 2112-byte block
+
+    def _host_results(self):
+        if not hasattr(self, "host_res"):
+            self.res_bytes = [64 + 2112 * len(g) for g in self.gidx]
+            self.host_res = [[torch.empty(rb, dtype=torch.uint8, pin_memory=True) for rb in self.res_bytes]
+                             for _ in range(self.K)]
+        return self.host_res
+
+    def message_lengths(self, ws_of):
+        """Reads every (learner, group) results area back to the host (one copy each,
+        then one wait on the stream) and returns, per group, the layer-major array
+        of message lengths the decode takes; raises on a device status."""
+        host = self._host_results()
+        for k in range(self.K):
+            for gi in range(len(self.gidx)):
+                host[k][gi].copy_(ws_of(k, gi)[:self.res_bytes[gi]], non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        lens = []
+        for gi, g in enumerate(self.gidx):
+            arr = (self.ct.c_uint64 * (len(g) * self.K))()
+            for k in range(self.K):
+                blk = host[k][gi].numpy()
+                for j in range(len(g)):
+                    o = 64 + 2112 * j + self.RESULT_AT
+                    status = int(blk[o + 4:o + 8].view(np.uint32)[0])
+                    if status != 0:
+                        raise RuntimeError(f"device status {status}")
+                    arr[j * self.K + k] = int(blk[o + 16:o + 24].view(np.uint64)[0])
+            lens.append(arr)
+        return lens
 
     def step(self, i, stream_ptr, k1_events=None, dec_events=None, ws_fixed=None, msg_set=0):
-        """Enqueues one step: every learner's compress, then the decode of the step's messages.
-        ws_fixed: one workspace per (learner, group) used by every step (a deferred
-        fix-up keeps its pending corrections there), instead of the per-step ring."""
+        """One step: every learner's compress, the message lengths read back (the
+        exchange of variable-length messages would carry them), then the decode of
+        the step's messages. ws_fixed: one workspace per (learner, group) used by
+        every step (a deferred fix-up keeps its pending corrections there), instead of
+        the per-step ring."""
         L, s = self.L, i % self.sets
         _, c_msg, c_dec_msgs = self.msg_sets[msg_set]
+
+        def ws_of(k, gi):
+            return ws_fixed[k][gi] if ws_fixed is not None else self.ws[i % self.ring][k][gi]
+
         for k in range(self.K):
             for gi, h in enumerate(self.h):
                 if k1_events is not None:
@@ -341,21 +381,23 @@ class DeviceRun:
                     L.adacomp_set_timing_events(h.ptr, self.ct.c_void_p(e[0].cuda_event),
                                                 self.ct.c_void_p(e[1].cuda_event),
                                                 self.ct.c_void_p(e[2].cuda_event))
-                ws = ws_fixed[k][gi] if ws_fixed is not None else self.ws[i % self.ring][k][gi]
+                ws = ws_of(k, gi)
                 st = L.adacomp_compress_group(h.ptr, self.c_res[k][gi], self.c_dw[k][s][gi], c_msg[k][gi],
                                               self.c_cap[k][gi], ws.data_ptr(), ws.numel(), stream_ptr)
                 if st:
                     raise RuntimeError(f"adacomp_compress_group: {st}")
+        lens = self.message_lengths(ws_of)
         if dec_events is not None:
             dec_events[0].record()
         for gi, h in enumerate(self.h):
-            st = L.adacomp_decode_accumulate_group(h.ptr, c_dec_msgs[gi], self.K, self.c_dense[gi],
+            st = L.adacomp_decode_accumulate_group(h.ptr, c_dec_msgs[gi], lens[gi], self.K, self.c_dense[gi],
                                                    self.dec_ws[gi].data_ptr(), self.dec_ws[gi].numel(),
                                                    stream_ptr)
             if st:
                 raise RuntimeError(f"adacomp_decode_accumulate_group: {st}")
         if dec_events is not None:
             dec_events[1].record()
+        return lens
 
     def clear_timing(self):
         for h in self.h:
@@ -369,7 +411,7 @@ class DeviceRun:
                 ws = self.ws[i % self.ring][k][gi]
                 blk = ws[64:64 + 2112 * len(g)].cpu().numpy()
                 for j in range(len(g)):
-                    o = 2112 * j + 2064
+                    o = 2112 * j + self.RESULT_AT
                     status = int(blk[o + 4:o + 8].view(np.uint32)[0])
                     nnz = int(blk[o + 8:o + 16].view(np.uint64)[0])
                     mb = int(blk[o + 16:o + 24].view(np.uint64)[0])
@@ -382,6 +424,26 @@ def _new_events(n):
     for e in evs:
         e.record()  # creates the underlying CUDA event
     return evs
+
+
+def bench_config(args, layers, K, world):
+    """The workload description both arms print (the reference arm the same dict)."""
+    return {"workload": args.workload, "layers": len(layers),
+            "elements_per_learner": sum(l.numel for l in layers), "learners": K,
+            "bin_len": sorted({l.bin_len for l in layers}),
+            "dw_dtype": layers[0].dw_dtype, "residue_dtype": "f32",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (dW rotates over %d sets)" % (
+                4 if args.workload in ("resnet50", "fc400k", "lstm_fc") else 2)}
+
+
+def residue_range(run):
+    """min and max of every learner's residue after the last step (eager fix-up)."""
+    lo, hi = math.inf, -math.inf
+    for k in range(run.K):
+        mn, mx = torch.aminmax(run.res[k][0])
+        lo, hi = min(lo, float(mn)), max(hi, float(mx))
+    return [lo, hi]
 
 
 def run_device(args, rank, world):
@@ -414,7 +476,7 @@ def run_device(args, rank, world):
         torch.cuda.synchronize()
         start.record()
         for i in range(args.steps):
-            run.step(step_no + i, sp, k1_events[i], dec_events[i])
+            run.last_lens = run.step(step_no + i, sp, k1_events[i], dec_events[i])
         end.record()
         torch.cuda.synchronize()
         barrier(world)
@@ -429,6 +491,7 @@ def run_device(args, rank, world):
             break
     clocks = sampler.stop() if sampler else None
     run.clear_timing()
+    rrange = residue_range(run)
 
     # the median repetition is reported
     order = sorted(range(len(reps)), key=lambda r: reps[r][0])
@@ -455,6 +518,7 @@ def run_device(args, rank, world):
     k1_bytes_per_launch = k1_bytes / len(k1)
     achieved = k1_bytes_per_launch / (k1_ms_per_launch * 1e-3) / 1e9
     step_gbs = total_bytes / (ms * 1e-3) / 1e9
+    dec_gbs = dec_bytes / args.steps / (statistics.mean(dec) * 1e-3) / 1e9
     value = n_elems * args.steps * world / (ms * 1e-3)
 
     out = {
@@ -462,18 +526,21 @@ def run_device(args, rank, world):
         "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f32" if run.dw_dtype == torch.float32 else "bf16+f32",
         "data": "synthetic",
-        "config": {"workload": args.workload, "layers": len(layers), "elements_per_learner": n_elems // run.K,
-                   "learners": run.K, "bin_len": sorted({l.bin_len for l in layers}),
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-                   "l2": "inputs larger than L2 (dW rotates over %d sets)" % run.sets,
-                   "timed_repetitions": len(reps)},
+        "config": bench_config(args, layers, run.K, world),
+        "timed_repetitions": len(reps),
         "hbm_gbs": step_gbs, "hbm_frac": step_gbs / peak, "hbm_peak_gbs": peak, "hbm_peak_kind": peak_kind,
+        "hbm_frac_nominal": step_gbs / NOMINAL_HBM_GBS, "hbm_nominal_gbs": NOMINAL_HBM_GBS,
         "compress_ms_per_step": (sum(k1) + sum(fx)) / args.steps, "decode_ms_per_step": statistics.mean(dec),
+        "decode_gbs": dec_gbs, "decode_frac": dec_gbs / peak,
+        "stream_ms_per_launch": k1_ms_per_launch,
         "finalize_emit_ms_per_launch": statistics.mean(fx),
         "compression_ratio": 4.0 * n_elems * args.steps / msg_bytes,
+        "message_bytes_per_learner": msg_bytes / args.steps / run.K,
         "sent_per_bin": nnz_total / bins_total,
+        "residue_range": rrange,
         "roofline": {"kernel": stream_kernel, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                     "frac_nominal": achieved / NOMINAL_HBM_GBS,
                      "traffic": profiled_traffic(stream_kernel, args.workload),
                      "bytes_per_launch": k1_bytes_per_launch, "ms_per_launch": k1_ms_per_launch},
         "gpu_launches": run.launches_per_step() * args.steps,
@@ -484,11 +551,11 @@ def run_device(args, rank, world):
     if not args.no_lazy:
         out["lazy_fixup"] = run_lazy(args, run, sp, world, n_elems)
     if not args.no_sgd:
-        out["decode_sgd"] = run_decode_sgd(args, run, sp, world, layers, res[-1])
+        out["decode_sgd"] = run_decode_sgd(args, run, sp, world, layers)
     return out, run
 
 
-def run_decode_sgd(args, run, sp, world, layers, step_res):
+def run_decode_sgd(args, run, sp, world, layers):
     """The decode fused with one momentum-SGD step (adacomp_decode_sgd_group) on the
     last timed step's messages: weights and momentum read and written once (16 B per
     element) instead of a dense sum plus a separate optimiser pass."""
@@ -504,7 +571,7 @@ def run_decode_sgd(args, run, sp, world, layers, step_res):
 
     def once():
         for gi, h in enumerate(run.h):
-            st = run.L.adacomp_decode_sgd_group(h.ptr, run.c_dec_msgs[gi], run.K, c_w[gi], c_v[gi],
+            st = run.L.adacomp_decode_sgd_group(h.ptr, run.c_dec_msgs[gi], run.last_lens[gi], run.K, c_w[gi], c_v[gi],
                                                 ct.c_float(1e-3), ct.c_float(0.9), ct.c_float(1.0 / run.K),
                                                 run.dec_ws[gi].data_ptr(), run.dec_ws[gi].numel(), sp)
             if st:
@@ -525,8 +592,11 @@ def run_decode_sgd(args, run, sp, world, layers, step_res):
         reps.append(start.elapsed_time(end) / args.steps)
         if time.perf_counter() - t0 >= args.min_timed_seconds / 3 or len(reps) >= 200:
             break
+    for gi, h in enumerate(run.h):
+        if run.ac.adacomp_decode_status(h, run.dec_ws[gi]) != run.ac.OK:
+            raise RuntimeError("the fused decode + SGD step rejected a message")
     ms = max_over_ranks(sorted(reps)[len(reps) // 2], world)
-    msg_bytes = sum(r[1] for r in step_res)
+    msg_bytes = sum(sum(a) for a in run.last_lens)
     bins = sum(-(-l.numel // l.bin_len) for l in layers) * run.K
     algo = 16 * sum(numels) + msg_bytes + 2 * bins
     del w_buf, v_buf
@@ -545,7 +615,7 @@ def run_lazy(args, run, sp, world, n_elems):
           for _ in range(run.K)]
     stream = torch.cuda.current_stream()
     for i in range(max(3, args.warmup)):
-        run.step(i, sp, ws_fixed=ws)
+        run.last_lens = run.step(i, sp, ws_fixed=ws)
     start, end = _new_events(2)
     reps, t0, step_no = [], time.perf_counter(), 0
     while True:
@@ -553,7 +623,7 @@ def run_lazy(args, run, sp, world, n_elems):
         torch.cuda.synchronize()
         start.record(stream)
         for i in range(args.steps):
-            run.step(step_no + i, sp, ws_fixed=ws)
+            run.last_lens = run.step(step_no + i, sp, ws_fixed=ws)
         end.record(stream)
         torch.cuda.synchronize()
         reps.append(start.elapsed_time(end))
@@ -574,19 +644,18 @@ def run_lazy(args, run, sp, world, n_elems):
             "ms_per_step": ms / args.steps, "timed_repetitions": len(reps)}
 
 
-E2E_UPLOAD_STREAMS = 1  # copy streams for the uploads (four measured no faster than one)
-
-
 def run_e2e(args, run, layers, sp, world):
     """Same steps through the C ABI with host buffers: each step copies its dW from
-    pinned host memory, runs the path, reads every message length and copies the
-    messages back to pinned host memory (runs of neighbouring messages).
+    pinned host memory, runs the path (the message lengths come back to the host
+    before the decode, as an exchange of the messages would need them), and copies
+    the messages back to pinned host memory (runs of neighbouring messages).
 
-    The copies overlap the computation of neighbouring steps: the dW of step i goes
-    up on copy streams (into the dW slot step i uses, once the step that last used
-    it is done), the results area of step i comes back on the compute stream, and the
-    messages of step i go down on a second copy stream from one of two message
-    buffer sets while step i + 1 computes into the other."""
+    The copies overlap the computation of neighbouring steps: the dW of step i + 1
+    goes up on a copy stream (into the dW slot it uses, once the step that last read
+    that slot is done) while step i computes, and the messages of step i go down on
+    a second copy stream from one of two message buffer sets while step i + 1
+    computes into the other. Also reported: the host-to-device rate of the upload
+    alone (every learner's dW, one copy each, timed with events on the copy stream)."""
     numels = [l.numel for l in layers]
     host_dw = []
     for k in range(run.K):
@@ -597,36 +666,38 @@ def run_e2e(args, run, layers, sp, world):
         run.add_msg_set()
     host_msg = [torch.empty(run.msg[k][0].numel(), dtype=torch.uint8, pin_memory=True) for k in range(run.K)]
     msg_offs = [[v.data_ptr() - run.msg[k][0].data_ptr() for v in run.msg[k][1]] for k in range(run.K)]
-    res_bytes = [64 + 2112 * len(g) for g in run.gidx]  # control block and per-layer results of a group
-    host_res = [[[torch.empty(rb, dtype=torch.uint8, pin_memory=True) for rb in res_bytes] for _ in range(run.K)]
-                for _ in range(2)]
     comp = torch.cuda.current_stream()
-    ups = [torch.cuda.Stream() for _ in range(E2E_UPLOAD_STREAMS)]
+    up = torch.cuda.Stream()
     down = torch.cuda.Stream()
     steps = args.steps
     h2d = d2h = 0
     slot_free = [None] * run.sets   # compute of the step that last read each dW slot
     msgs_free = [None, None]        # message copies of the step that last wrote each set
-    res_ready = [None, None]
+    up_done = {}
 
-    def messages_down(j):
-        """Enqueues the message copies of step j (its results area is on the host)."""
+    def upload(j):
+        nonlocal h2d
+        slot = j % run.sets
+        if slot_free[slot] is not None:
+            up.wait_event(slot_free[slot])
+        with torch.cuda.stream(up):
+            for k in range(run.K):
+                run.dw[k][slot][0][:host_dw[k].numel()].copy_(host_dw[k], non_blocking=True)
+                h2d += host_dw[k].numel() * host_dw[k].element_size()
+        ev = torch.cuda.Event()
+        ev.record(up)
+        up_done[j] = ev
+
+    def messages_down(j, lens):
+        """Enqueues the message copies of step j (its compress is complete)."""
         nonlocal d2h
-        res_ready[j % 2].synchronize()
         msg = run.msg_sets[j % 2][0]
-        down.wait_event(res_ready[j % 2])
         with torch.cuda.stream(down):
             for k in range(run.K):
-                spans = []  # (offset, length) of each message in the learner's buffer
-                li = 0
+                spans, li = [], 0
                 for gi, g in enumerate(run.gidx):
-                    blk = host_res[j % 2][k][gi].numpy()
                     for jj in range(len(g)):
-                        o = 64 + 2112 * jj + 2064
-                        status = int(blk[o + 4:o + 8].view(np.uint32)[0])
-                        if status != 0:
-                            raise RuntimeError(f"device status {status} in the e2e leg")
-                        spans.append((msg_offs[k][li], int(blk[o + 16:o + 24].view(np.uint64)[0])))
+                        spans.append((msg_offs[k][li], int(lens[gi][jj * run.K + k])))
                         li += 1
                 # one copy per run of messages: neighbours whose gap (the unused tail of
                 # a buffer sized for the worst case) is under 256 KB share a copy
@@ -646,42 +717,39 @@ def run_e2e(args, run, layers, sp, world):
     torch.cuda.synchronize()
     barrier(world)
     t0 = time.perf_counter()
+    upload(0)
     for i in range(steps):
-        slot = i % run.sets
-        for u, up in enumerate(ups):  # each stream uploads one contiguous part of every learner's dW
-            if slot_free[slot] is not None:
-                up.wait_event(slot_free[slot])
-            with torch.cuda.stream(up):
-                for k in range(run.K):
-                    n = host_dw[k].numel()
-                    a, b = n * u // len(ups), n * (u + 1) // len(ups)
-                    run.dw[k][slot][0][a:b].copy_(host_dw[k][a:b], non_blocking=True)
-                    h2d += (b - a) * host_dw[k].element_size()
-            inputs_up = torch.cuda.Event()
-            inputs_up.record(up)
-            comp.wait_event(inputs_up)
+        if i + 1 < steps:
+            upload(i + 1)
+        comp.wait_event(up_done.pop(i))
         if msgs_free[i % 2] is not None:
             comp.wait_event(msgs_free[i % 2])
-        run.step(i, sp, msg_set=i % 2)
-        for k in range(run.K):
-            for gi in range(len(run.gidx)):
-                ws = run.ws[i % run.ring][k][gi]
-                host_res[i % 2][k][gi].copy_(ws[:res_bytes[gi]], non_blocking=True)
-        d2h += run.K * sum(res_bytes)
+        lens = run.step(i, sp, msg_set=i % 2)
+        d2h += run.K * sum(run.res_bytes)
         done = torch.cuda.Event()
         done.record(comp)
-        slot_free[slot] = done
-        res_ready[i % 2] = done
-        if i >= 1:
-            messages_down(i - 1)
-    messages_down(steps - 1)
+        slot_free[i % run.sets] = done
+        messages_down(i, lens)
     torch.cuda.synchronize()
     secs = max_over_ranks(time.perf_counter() - t0, world)
     n_elems = sum(numels) * run.K
+
+    # the upload alone
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(up):
+        e0.record(up)
+        nb = 0
+        for k in range(run.K):
+            run.dw[k][0][0][:host_dw[k].numel()].copy_(host_dw[k], non_blocking=True)
+            nb += host_dw[k].numel() * host_dw[k].element_size()
+        e1.record(up)
+    torch.cuda.synchronize()
+    up_gbs = nb / (e0.elapsed_time(e1) * 1e-3) / 1e9
     return {"value": n_elems * steps * world / secs, "unit": "elements/s",
             "h2d_bytes_per_step": h2d // steps, "d2h_bytes_per_step": d2h // steps,
-            "ms_per_step": secs * 1e3 / steps,
-            "overlap": "dW upload, compute and message download of neighbouring steps overlap"}
+            "ms_per_step": secs * 1e3 / steps, "h2d_gbs_upload_alone": up_gbs,
+            "overlap": "dW upload of the next step and message download of the previous step overlap "
+                       "the computation; the message lengths come back before each decode"}
 
 
 # ---------------------------------------------------------------- oracle legs
@@ -689,8 +757,10 @@ def oracle_sample_layers(args):
     """The layers one oracle step covers: the whole workload when it is small,
     otherwise a fixed slice of it (said in the JSON's `sample`)."""
     layers = workload_layers(args)
-    if args.workload in ("resnet50", "fc400k", "flat100m"):
+    if args.workload in ("resnet50", "fc400k"):
         return layers, "all layers"
+    if args.workload == "flat100m":
+        return layers, "one learner's 10^8-element layer per step (learners 0..15 in turn, each its own dW)"
     if args.workload == "lstm_fc":
         return [layers[0], layers[4]], "one LSTM tensor + one FC tensor (25.2M elements)"
     sub = [l for l in layers if l.name.startswith("h0.")]
@@ -710,10 +780,11 @@ def oracle_run(args, steps=None, budget_s=None, warmup=0):
     elems = secs = 0.0
     done = 0
     i = 0
+    K = learners(args)
     while True:
         dws = []
         for ly in layers:
-            t = wl.gen_dw(args.workload, names.index(ly.name), ly, i, device="cpu")
+            t = wl.gen_dw(args.workload, names.index(ly.name), ly, i // K, learner=i % K, device="cpu")
             dws.append(t.view(torch.int16).numpy().view(np.uint16) if t.dtype == torch.bfloat16 else t.numpy())
         t0 = time.perf_counter()
         for ly, r, d, dn in zip(layers, res, dws, dense):
@@ -730,7 +801,8 @@ def oracle_run(args, steps=None, budget_s=None, warmup=0):
             break
         if budget_s is not None and secs >= budget_s:
             break
-    what = f"{args.workload}: {sample}, {done} step(s) of oracle compress + K=1 decode, carried residue"
+    what = (f"{args.workload}: {sample}, {done} step(s) of oracle compress + decode of that message, carried "
+            "residue; inputs from the same seeded generators on the host")
     return elems, secs, done, what
 
 
@@ -765,8 +837,7 @@ def run_reference(args):
         "steps": done, "warmup": args.warmup, "ms_per_step": secs * 1e3 / done, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16+f32" if layers[0].dw_dtype == "bf16" else "f32",
         "data": "synthetic", "impl": "reference",
-        "config": {"workload": args.workload, "layers": len(layers), "learners": 1,
-                   "bin_len": sorted({l.bin_len for l in layers})},
+        "config": bench_config(args, layers, learners(args), int(os.environ.get("WORLD_SIZE", "1"))),
         "cpu_baseline": {"value": v, "unit": "elements/s", "cores": 1, "kind": "oracle", "sample": what,
                          "host": _host()},
         "e2e": {"value": v, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

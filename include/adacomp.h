@@ -69,7 +69,7 @@ typedef enum {
     ADACOMP_ERR_CAPACITY = 4,     /* msg_capacity < max_msg_bytes */
     ADACOMP_ERR_CUDA = 5,         /* a CUDA runtime call or launch failed */
     ADACOMP_ERR_TIMEOUT = 6,      /* device: a bounded wait (a copy, or the look-back between tiles) ran out */
-    ADACOMP_ERR_BAD_MESSAGE = 7   /* device: a message's B, counts or offsets do not fit this layer */
+    ADACOMP_ERR_BAD_MESSAGE = 7   /* device: a message's length, B, counts or offsets do not fit this layer */
 } adacomp_status;
 
 typedef enum { ADACOMP_F32 = 0, ADACOMP_BF16 = 1 } adacomp_dtype;
@@ -169,28 +169,39 @@ adacomp_status adacomp_compress_group(adacomp_layer_t h, float* const* residue,
  * The pages only say that learners' quantised gradients are combined in
  * data-parallel training (abstract; summary paragraph); the plain sum is this
  * library's reading, and the caller zeroes dense for a fresh sum.
- *   msgs   host array of K device pointers, each a message of this layer starting
- *          on a 4-byte boundary
- *   dense  device fp32[n], in/out
- *   ws     device decode workspace, ws_bytes >= ADACOMP_DECODE_WS_FIXED
- *          + K * decode_ws_bytes_per_learner; needs no initialisation
+ *   msgs       host array of K device pointers, each a message of this layer
+ *              starting on a 4-byte boundary
+ *   msg_bytes  host array of K lengths in bytes, the length of each message as
+ *              received (messages are variable-length: "AdaComp (Adaptive Residual
+ *              Gradient Compression)", Claims > Limitation
+ *              #r629-minibatch-size-activity-and-variable-message-length). Nothing
+ *              past a message's length is used; the library may read the rest of the
+ *              16-byte block its last byte lies in.
+ *   dense      device fp32[n], in/out
+ *   ws         device decode workspace, ws_bytes >= ADACOMP_DECODE_WS_FIXED
+ *              + K * decode_ws_bytes_per_learner; needs no initialisation
  * One CTA owns each range of bins, so no two threads ever add to one element and
- * no float atomics are used. A message whose header B, counts or code offsets do
- * not fit the layer is skipped entirely and ADACOMP_ERR_BAD_MESSAGE is recorded
- * (adacomp_decode_status); a code whose offset lies outside its bin is ignored and
- * also recorded. Errors: INVALID_ARG (K outside 1..256, NULL pointers), ALIGNMENT
- * (dense not 16-byte or a message not 4-byte aligned), WORKSPACE, CUDA.
+ * no float atomics are used. Every message is checked before anything is added, and
+ * a message that fails a check is skipped entirely (it adds nothing; the others are
+ * summed as usual) and ADACOMP_ERR_BAD_MESSAGE is recorded (adacomp_decode_status).
+ * The checks: the length is at least 8 + 2B, the header's B is the layer's B, no
+ * count exceeds its bin's length, the length is exactly 8 + 2B + w * (sum of the
+ * counts), and within every bin the code offsets rise strictly and stay below the
+ * bin's length (a message gives each element at most one code). Errors:
+ * INVALID_ARG (K outside 1..256, NULL pointers), ALIGNMENT (dense not 16-byte or a
+ * message not 4-byte aligned), WORKSPACE, CUDA.
  */
-adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs, int32_t K,
-                                         float* dense, void* ws, size_t ws_bytes,
-                                         cudaStream_t stream);
+adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs,
+                                         const uint64_t* msg_bytes, int32_t K, float* dense,
+                                         void* ws, size_t ws_bytes, cudaStream_t stream);
 
-/* Decode for every layer of a group: msgs is a host array of num_layers * K device
- * pointers, layer-major (msgs[l * K + k]); dense a host array of num_layers device
- * pointers. K <= ADACOMP_MAX_LEARNERS and K * num_layers <= 1024. */
+/* Decode for every layer of a group: msgs and msg_bytes are host arrays of
+ * num_layers * K entries, layer-major (msgs[l * K + k]); dense a host array of
+ * num_layers device pointers. K <= ADACOMP_MAX_LEARNERS and K * num_layers <= 1024. */
 adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* const* msgs,
-                                               int32_t K, float* const* dense, void* ws,
-                                               size_t ws_bytes, cudaStream_t stream);
+                                               const uint64_t* msg_bytes, int32_t K,
+                                               float* const* dense, void* ws, size_t ws_bytes,
+                                               cudaStream_t stream);
 
 /*
  * Waits for `stream` and reads the result of the last compress call that used `ws`
@@ -244,12 +255,13 @@ adacomp_status adacomp_set_timeout_ns(adacomp_layer_t h, uint64_t timeout_ns);
  * never written to global memory: it lives only in the tile being updated. Same
  * messages, workspace and error reporting as adacomp_decode_accumulate (a rejected
  * message contributes nothing). */
-adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, int32_t K, float* weights,
-                                  float* momentum, float lr, float mu, float grad_scale, void* ws,
-                                  size_t ws_bytes, cudaStream_t stream);
-adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
-                                        float* const* weights, float* const* momentum, float lr, float mu,
-                                        float grad_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
+adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                  int32_t K, float* weights, float* momentum, float lr, float mu,
+                                  float grad_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
+adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                        int32_t K, float* const* weights, float* const* momentum, float lr,
+                                        float mu, float grad_scale, void* ws, size_t ws_bytes,
+                                        cudaStream_t stream);
 
 /* Selection rule. ADACOMP_RULE_ADACOMP (the default) sends an element when
  * G != 0 and |fl32(G + dW)| >= g_max of its bin ("AdaComp (Adaptive Residual

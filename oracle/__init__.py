@@ -51,10 +51,10 @@ class Oracle:
         lib.adacomp_oracle_compress.argtypes = [i64, i32, ctypes.c_int, vp, vp, vp, u64,
                                                 ctypes.POINTER(u64), vp, vp, vp, ctypes.c_int, ctypes.c_int]
         lib.adacomp_oracle_compress.restype = ctypes.c_int
-        lib.adacomp_oracle_decode_accumulate.argtypes = [i64, i32, vp, i32, vp]
+        lib.adacomp_oracle_decode_accumulate.argtypes = [i64, i32, vp, vp, i32, vp, vp]
         lib.adacomp_oracle_decode_accumulate.restype = ctypes.c_int
         f32 = ctypes.c_float
-        lib.adacomp_oracle_decode_sgd.argtypes = [i64, i32, vp, i32, vp, vp, f32, f32, f32]
+        lib.adacomp_oracle_decode_sgd.argtypes = [i64, i32, vp, vp, i32, vp, vp, f32, f32, f32]
         lib.adacomp_oracle_decode_sgd.restype = ctypes.c_int
         self.lib = lib
 
@@ -124,24 +124,41 @@ def compress(residue: np.ndarray, dw: np.ndarray, bin_len: int,
     return CompressResult(msg[: mlen.value].copy(), s[0], gmax, sel.astype(bool))
 
 
-def decode_accumulate(n: int, bin_len: int, msgs, dense: np.ndarray, lib=None) -> int:
-    """Adds every message's sign*s_k into ``dense`` (fp32, in place), k in order.
+def _msg_arrays(msgs, lens):
+    bufs = [np.ascontiguousarray(m, dtype=np.uint8) for m in msgs]
+    if lens is None:
+        lens = [b.size for b in bufs]
+    if len(lens) != len(bufs):
+        raise ValueError("one length per message")
+    ptrs = (ctypes.c_void_p * len(bufs))(*[b.ctypes.data for b in bufs])
+    ln = (ctypes.c_uint64 * len(bufs))(*[int(x) for x in lens])
+    return bufs, ptrs, ln
 
-    Returns the oracle status (0 = OK, 3 = a malformed message, nothing added).
+
+def decode_accumulate(n: int, bin_len: int, msgs, dense: np.ndarray, lib=None, lens=None, bad=None) -> int:
+    """Adds every well-formed message's sign*s_k into ``dense`` (fp32, in place), k in order.
+
+    ``lens``: each message's length in bytes (default: the length of its array).
+    Returns the oracle status (0 = OK, 3 = at least one message was rejected and
+    added nothing). ``bad``: an optional uint8 array of K entries set to 1 for each
+    rejected message.
     """
     lib = lib or _load()
     assert dense.dtype == np.float32 and dense.flags.c_contiguous and dense.size == n
-    bufs = [np.ascontiguousarray(m, dtype=np.uint8) for m in msgs]
-    arr = (ctypes.c_void_p * len(bufs))(*[b.ctypes.data for b in bufs])
-    return int(lib.adacomp_oracle_decode_accumulate(n, bin_len, arr, len(bufs), _ptr(dense)))
+    bufs, ptrs, ln = _msg_arrays(msgs, lens)
+    bad_ptr = None
+    if bad is not None:
+        assert bad.dtype == np.uint8 and bad.size == len(bufs)
+        bad_ptr = _ptr(bad)
+    return int(lib.adacomp_oracle_decode_accumulate(n, bin_len, ptrs, ln, len(bufs), _ptr(dense), bad_ptr))
 
 
 def decode_sgd(n: int, bin_len: int, msgs, w: np.ndarray, v: np.ndarray, lr: float, mu: float,
-               scale: float = 1.0, lib=None) -> int:
+               scale: float = 1.0, lib=None, lens=None) -> int:
     """Decodes the messages into a zero gradient and applies one momentum-SGD step to
-    ``w`` and ``v`` (fp32, in place). Returns the oracle status."""
+    ``w`` and ``v`` (fp32, in place); a rejected message adds nothing. Returns the
+    oracle status."""
     lib = lib or _load()
     assert w.dtype == np.float32 and v.dtype == np.float32 and w.size == n and v.size == n
-    arrs = [np.ascontiguousarray(m, dtype=np.uint8) for m in msgs]
-    ptrs = (ctypes.c_void_p * len(arrs))(*[a.ctypes.data for a in arrs])
-    return lib.adacomp_oracle_decode_sgd(n, bin_len, ptrs, len(arrs), _ptr(w), _ptr(v), lr, mu, scale)
+    bufs, ptrs, ln = _msg_arrays(msgs, lens)
+    return lib.adacomp_oracle_decode_sgd(n, bin_len, ptrs, ln, len(bufs), _ptr(w), _ptr(v), lr, mu, scale)

@@ -215,32 +215,68 @@ int adacomp_oracle_compress(int64_t n, int32_t L, int dw_bf16, float *residue, c
 }
 
 /*
- * Decode-and-accumulate: dense[j] += (sign ? -s_k : +s_k) for every code of
- * message k, k = 0..K-1 in order. Messages are validated (header B, count per
- * bin, code offsets) before anything is added.
+ * Whether one message of length len (bytes) is a well-formed message of a layer of
+ * n elements with bins of L. Messages are variable-length ("AdaComp (Adaptive
+ * Residual Gradient Compression)", Claims > Limitation
+ * #r629-minibatch-size-activity-and-variable-message-length), so the length that
+ * came with the message is checked against what its counts say, and nothing past it
+ * is read. The checks, in order: room for the header and the counts (8 + 2B bytes);
+ * the header's B is the layer's; no count exceeds its bin's length; the length is
+ * exactly 8 + 2B + w * (sum of the counts); within every bin the code offsets rise
+ * strictly (the compressor lists a bin's sent elements once each, in ascending
+ * offset) and stay below the bin's length.
  */
-int adacomp_oracle_decode_accumulate(int64_t n, int32_t L, const uint8_t *const *msgs, int32_t K,
-                                     float *dense)
+static int message_ok(int64_t n, int32_t L, const uint8_t *m, uint64_t len)
 {
-    if (n < 1 || L < 1 || L > 32768 || K < 1 || !msgs || !dense) return ORACLE_ERR_ARG;
     int64_t B = bin_count(n, L);
     int w = code_width(L);
-    for (int32_t k = 0; k < K; ++k) {
-        const uint8_t *m = msgs[k];
-        if (!m || (int64_t)get_u32(m + 4) != B) return ORACLE_ERR_BAD_MESSAGE;
-        uint64_t pos = 8 + 2 * (uint64_t)B;
-        for (int64_t b = 0; b < B; ++b) {
-            int64_t len = (b + 1) * L < n ? L : n - b * L;
-            uint32_t cnt = get_u16(m + 8 + 2 * b);
-            if ((int64_t)cnt > len) return ORACLE_ERR_BAD_MESSAGE;
-            for (uint32_t c = 0; c < cnt; ++c) {
-                uint32_t code = (w == 1) ? m[pos] : get_u16(m + pos);
-                pos += (uint64_t)w;
-                if ((int64_t)(code >> 1) >= len) return ORACLE_ERR_BAD_MESSAGE;
-            }
+    if (!m || len < 8 + 2 * (uint64_t)B) return 0;
+    if ((int64_t)get_u32(m + 4) != B) return 0;
+    uint64_t total = 0;
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t blen = (b + 1) * L < n ? L : n - b * L;
+        uint32_t cnt = get_u16(m + 8 + 2 * b);
+        if ((int64_t)cnt > blen) return 0;
+        total += cnt;
+    }
+    if (len != 8 + 2 * (uint64_t)B + (uint64_t)w * total) return 0;
+    uint64_t pos = 8 + 2 * (uint64_t)B;
+    for (int64_t b = 0; b < B; ++b) {
+        int64_t blen = (b + 1) * L < n ? L : n - b * L;
+        uint32_t cnt = get_u16(m + 8 + 2 * b);
+        int64_t prev = -1;
+        for (uint32_t c = 0; c < cnt; ++c) {
+            uint32_t code = (w == 1) ? m[pos] : get_u16(m + pos);
+            pos += (uint64_t)w;
+            int64_t off = (int64_t)(code >> 1);
+            if (off >= blen || off <= prev) return 0;
+            prev = off;
         }
     }
+    return 1;
+}
+
+/*
+ * Decode-and-accumulate: dense[j] += (sign ? -s_k : +s_k) for every code of
+ * message k, k = 0..K-1 in order. Every message is checked first (message_ok); a
+ * message that fails adds nothing, the others are summed as usual, and the call
+ * returns ORACLE_ERR_BAD_MESSAGE (bad_out[k], when given, marks each rejected
+ * message). lens[k] is message k's length in bytes.
+ */
+int adacomp_oracle_decode_accumulate(int64_t n, int32_t L, const uint8_t *const *msgs, const uint64_t *lens,
+                                     int32_t K, float *dense, uint8_t *bad_out)
+{
+    if (n < 1 || L < 1 || L > 32768 || K < 1 || !msgs || !lens || !dense) return ORACLE_ERR_ARG;
+    int64_t B = bin_count(n, L);
+    int w = code_width(L);
+    int any_bad = 0;
     for (int32_t k = 0; k < K; ++k) {
+        int ok = message_ok(n, L, msgs[k], lens[k]);
+        if (bad_out) bad_out[k] = (uint8_t)!ok;
+        if (!ok) any_bad = 1;
+    }
+    for (int32_t k = 0; k < K; ++k) {
+        if (!message_ok(n, L, msgs[k], lens[k])) continue;
         const uint8_t *m = msgs[k];
         float s = u32_as_f32(get_u32(m));
         uint64_t pos = 8 + 2 * (uint64_t)B;
@@ -254,26 +290,28 @@ int adacomp_oracle_decode_accumulate(int64_t n, int32_t L, const uint8_t *const 
             }
         }
     }
-    return ORACLE_OK;
+    return any_bad ? ORACLE_ERR_BAD_MESSAGE : ORACLE_OK;
 }
 
 /*
  * Decode K messages into the aggregated gradient g (a zero-filled fp32 buffer,
- * learners in order, exactly as adacomp_oracle_decode_accumulate) and apply one
- * momentum-SGD step to weights w and momentum v (the optimiser of the entry's
- * Claims > Application #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers;
- * the rule is read as the heavy-ball form without dampening):
+ * learners in order, exactly as adacomp_oracle_decode_accumulate, a rejected
+ * message adding nothing) and apply one momentum-SGD step to weights w and
+ * momentum v (the optimiser of the entry's Claims > Application
+ * #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers; the rule is read as
+ * the heavy-ball form without dampening):
  *     v = fl32(fl32(mu * v) + fl32(scale * g));   w = fl32(w - fl32(lr * v)).
- * A malformed message rejects the call and leaves w and v untouched.
+ * Returns ORACLE_ERR_BAD_MESSAGE when a message was rejected (the step is still
+ * applied with the others).
  */
-int adacomp_oracle_decode_sgd(int64_t n, int32_t L, const uint8_t *const *msgs, int32_t K, float *w, float *v,
-                              float lr, float mu, float scale)
+int adacomp_oracle_decode_sgd(int64_t n, int32_t L, const uint8_t *const *msgs, const uint64_t *lens, int32_t K,
+                              float *w, float *v, float lr, float mu, float scale)
 {
     if (n < 1 || !w || !v) return ORACLE_ERR_ARG;
     float *g = (float *)calloc((size_t)n, sizeof(float));
     if (!g) return ORACLE_ERR_ARG;
-    int rc = adacomp_oracle_decode_accumulate(n, L, msgs, K, g);
-    if (rc != ORACLE_OK) { free(g); return rc; }
+    int rc = adacomp_oracle_decode_accumulate(n, L, msgs, lens, K, g, NULL);
+    if (rc != ORACLE_OK && rc != ORACLE_ERR_BAD_MESSAGE) { free(g); return rc; }
     for (int64_t j = 0; j < n; ++j) {
         float momentum = mu * v[j];
         float step = scale * g[j];
@@ -282,5 +320,5 @@ int adacomp_oracle_decode_sgd(int64_t n, int32_t L, const uint8_t *const *msgs, 
         w[j] = w[j] - delta;
     }
     free(g);
-    return ORACLE_OK;
+    return rc;
 }

@@ -51,8 +51,8 @@ def lib() -> ctypes.CDLL:
         L.adacomp_init_group.argtypes = [P(vp), i32, P(i64), P(i32), P(i32), P(sz), P(sz), P(sz)]
         L.adacomp_compress.argtypes = [vp, vp, vp, vp, sz, vp, sz, vp]
         L.adacomp_compress_group.argtypes = [vp, P(vp), P(vp), P(vp), P(sz), vp, sz, vp]
-        L.adacomp_decode_accumulate.argtypes = [vp, P(vp), i32, vp, vp, sz, vp]
-        L.adacomp_decode_accumulate_group.argtypes = [vp, P(vp), i32, P(vp), vp, sz, vp]
+        L.adacomp_decode_accumulate.argtypes = [vp, P(vp), P(u64), i32, vp, vp, sz, vp]
+        L.adacomp_decode_accumulate_group.argtypes = [vp, P(vp), P(u64), i32, P(vp), vp, sz, vp]
         L.adacomp_query.argtypes = [vp, vp, i32, vp, P(u64), P(ctypes.c_float), P(i32)]
         L.adacomp_decode_status.argtypes = [vp, vp, vp, P(i32)]
         L.adacomp_set_timeout_ns.argtypes = [vp, u64]
@@ -61,8 +61,8 @@ def lib() -> ctypes.CDLL:
         L.adacomp_set_lazy_fixup.argtypes = [vp, i32, P(sz)]
         L.adacomp_set_selection_rule.argtypes = [vp, i32]
         f32 = ctypes.c_float
-        L.adacomp_decode_sgd.argtypes = [vp, P(vp), i32, vp, vp, f32, f32, f32, vp, sz, vp]
-        L.adacomp_decode_sgd_group.argtypes = [vp, P(vp), i32, P(vp), P(vp), f32, f32, f32, vp, sz, vp]
+        L.adacomp_decode_sgd.argtypes = [vp, P(vp), P(u64), i32, vp, vp, f32, f32, f32, vp, sz, vp]
+        L.adacomp_decode_sgd_group.argtypes = [vp, P(vp), P(u64), i32, P(vp), P(vp), f32, f32, f32, vp, sz, vp]
         L.adacomp_materialize.argtypes = [vp, vp, vp, sz, vp]
         L.adacomp_materialize_group.argtypes = [vp, P(vp), vp, sz, vp]
         L.adacomp_free.argtypes = [vp]
@@ -159,20 +159,30 @@ def adacomp_compress_group(h: Handle, residues, dWs, msgs, ws, stream=None):
         _ptr(ws), _nbytes(ws), _stream(stream)), "adacomp_compress_group")
 
 
-def adacomp_decode_accumulate(h: Handle, msgs, dense, ws, stream=None):
+def _lengths(msg_bytes, count: int):
+    lens = [int(b) for b in msg_bytes]
+    if len(lens) != count:
+        raise ValueError(f"expected {count} message lengths, got {len(lens)}")
+    return (ctypes.c_uint64 * count)(*lens)
+
+
+def adacomp_decode_accumulate(h: Handle, msgs, msg_bytes, dense, ws, stream=None):
+    """msgs: K device buffers; msg_bytes: the K message lengths in bytes."""
     K = len(msgs)
     arr = (ctypes.c_void_p * K)(*[_ptr(m) for m in msgs])
-    _check(lib().adacomp_decode_accumulate(h.ptr, arr, K, _ptr(dense), _ptr(ws), _nbytes(ws),
-                                           _stream(stream)), "adacomp_decode_accumulate")
+    _check(lib().adacomp_decode_accumulate(h.ptr, arr, _lengths(msg_bytes, K), K, _ptr(dense), _ptr(ws),
+                                           _nbytes(ws), _stream(stream)), "adacomp_decode_accumulate")
 
 
-def adacomp_decode_accumulate_group(h: Handle, msgs, denses, ws, stream=None):
-    """msgs[l][k]: learner k's message for layer l; denses[l]: layer l's dense buffer."""
+def adacomp_decode_accumulate_group(h: Handle, msgs, msg_bytes, denses, ws, stream=None):
+    """msgs[l][k]: learner k's message for layer l, msg_bytes[l][k] its length;
+    denses[l]: layer l's dense buffer."""
     L = h.num_layers
     K = len(msgs[0])
     flat = [_ptr(m) for per_layer in msgs for m in per_layer]
+    lens = _lengths([b for per_layer in msg_bytes for b in per_layer], L * K)
     _check(lib().adacomp_decode_accumulate_group(
-        h.ptr, (ctypes.c_void_p * (L * K))(*flat), K, (ctypes.c_void_p * L)(*[_ptr(d) for d in denses]),
+        h.ptr, (ctypes.c_void_p * (L * K))(*flat), lens, K, (ctypes.c_void_p * L)(*[_ptr(d) for d in denses]),
         _ptr(ws), _nbytes(ws), _stream(stream)), "adacomp_decode_accumulate_group")
 
 
@@ -208,22 +218,24 @@ def adacomp_set_fault_injection(h: Handle, skip_tile: int = 0xFFFFFFFF):
     _check(lib().adacomp_set_fault_injection(h.ptr, skip_tile), "adacomp_set_fault_injection")
 
 
-def adacomp_decode_sgd(h: Handle, msgs, weights, momentum, lr: float, mu: float, ws, grad_scale: float = 1.0,
-                       stream=None):
+def adacomp_decode_sgd(h: Handle, msgs, msg_bytes, weights, momentum, lr: float, mu: float, ws,
+                       grad_scale: float = 1.0, stream=None):
     K = len(msgs)
     arr = (ctypes.c_void_p * K)(*[_ptr(m) for m in msgs])
-    _check(lib().adacomp_decode_sgd(h.ptr, arr, K, _ptr(weights), _ptr(momentum), lr, mu, grad_scale, _ptr(ws),
-                                    _nbytes(ws), _stream(stream)), "adacomp_decode_sgd")
+    _check(lib().adacomp_decode_sgd(h.ptr, arr, _lengths(msg_bytes, K), K, _ptr(weights), _ptr(momentum), lr, mu,
+                                    grad_scale, _ptr(ws), _nbytes(ws), _stream(stream)), "adacomp_decode_sgd")
 
 
-def adacomp_decode_sgd_group(h: Handle, msgs, weights, momentum, lr: float, mu: float, ws,
+def adacomp_decode_sgd_group(h: Handle, msgs, msg_bytes, weights, momentum, lr: float, mu: float, ws,
                              grad_scale: float = 1.0, stream=None):
-    """msgs: per layer a list of K messages (layer-major, as adacomp_decode_accumulate_group)."""
+    """msgs, msg_bytes: per layer a list of K messages and their lengths (layer-major, as
+    adacomp_decode_accumulate_group)."""
     L = h.num_layers
     K = len(msgs[0])
     arr = (ctypes.c_void_p * (L * K))(*[_ptr(m) for layer in msgs for m in layer])
+    lens = _lengths([b for layer in msg_bytes for b in layer], L * K)
     VP = ctypes.c_void_p * L
-    _check(lib().adacomp_decode_sgd_group(h.ptr, arr, K, VP(*[_ptr(w) for w in weights]),
+    _check(lib().adacomp_decode_sgd_group(h.ptr, arr, lens, K, VP(*[_ptr(w) for w in weights]),
                                           VP(*[_ptr(v) for v in momentum]), lr, mu, grad_scale, _ptr(ws),
                                           _nbytes(ws), _stream(stream)), "adacomp_decode_sgd_group")
 

@@ -184,11 +184,11 @@ adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* d
 
 namespace {
 // Shared by the plain decode (mom == nullptr) and the fused momentum-SGD decode.
-adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, int32_t K, float* const* dense,
-                            float* const* mom, float lr, float mu, float scale, void* ws, size_t ws_bytes,
-                            cudaStream_t stream)
+adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes, int32_t K,
+                            float* const* dense, float* const* mom, float lr, float mu, float scale, void* ws,
+                            size_t ws_bytes, cudaStream_t stream)
 {
-    if (!h || !msgs || !dense || !ws) return ADACOMP_ERR_INVALID_ARG;
+    if (!h || !msgs || !msg_bytes || !dense || !ws) return ADACOMP_ERR_INVALID_ARG;
     const int64_t L = (int64_t)h->layers.size();
     if (K < 1 || K > ADACOMP_MAX_LEARNERS || (int64_t)K * L > adacomp::kMaxDecodePairs)
         return ADACOMP_ERR_INVALID_ARG;
@@ -202,6 +202,14 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, int32_t 
     fill_group(h, g);
     p->K = K;
     p->sgd = mom ? 1 : 0;
+    uint32_t vt = 0;  // validation tasks per learner, layer by layer
+    for (int64_t l = 0; l < L; ++l) {
+        const KLayer& k = h->layers[(size_t)l];
+        const uint32_t per = adacomp::val_tiles_per_task(k.bins_per_tile);
+        p->val_begin[l] = vt;
+        vt += (k.num_tiles + per - 1) / per;
+    }
+    p->val_begin[L] = vt;
     p->lr = lr;
     p->mu = mu;
     p->scale = scale;
@@ -216,6 +224,7 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, int32_t 
             if (!m) st = ADACOMP_ERR_INVALID_ARG;
             else if (!aligned(m, 4)) st = ADACOMP_ERR_ALIGNMENT;
             p->msg[l * K + k] = static_cast<const uint8_t*>(m);
+            p->len[l * K + k] = msg_bytes[l * K + k];
         }
     }
     if (st == ADACOMP_OK) st = cuda_status(adacomp::launch_decode(*g, *p, ws, stream));
@@ -227,35 +236,37 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, int32_t 
 
 extern "C" {
 
-adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
-                                               float* const* dense, void* ws, size_t ws_bytes, cudaStream_t stream)
+adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                               int32_t K, float* const* dense, void* ws, size_t ws_bytes,
+                                               cudaStream_t stream)
 {
-    return decode_group(h, msgs, K, dense, nullptr, 0.0f, 0.0f, 1.0f, ws, ws_bytes, stream);
+    return decode_group(h, msgs, msg_bytes, K, dense, nullptr, 0.0f, 0.0f, 1.0f, ws, ws_bytes, stream);
 }
 
-adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* msgs, int32_t K,
-                                        float* const* weights, float* const* momentum, float lr, float mu,
+adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                        int32_t K, float* const* weights, float* const* momentum, float lr, float mu,
                                         float grad_scale, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (!momentum) return ADACOMP_ERR_INVALID_ARG;
-    return decode_group(h, msgs, K, weights, momentum, lr, mu, grad_scale, ws, ws_bytes, stream);
+    return decode_group(h, msgs, msg_bytes, K, weights, momentum, lr, mu, grad_scale, ws, ws_bytes, stream);
 }
 
-adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, int32_t K, float* weights,
-                                  float* momentum, float lr, float mu, float grad_scale, void* ws, size_t ws_bytes,
-                                  cudaStream_t stream)
+adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes, int32_t K,
+                                  float* weights, float* momentum, float lr, float mu, float grad_scale, void* ws,
+                                  size_t ws_bytes, cudaStream_t stream)
 {
     if (!h) return ADACOMP_ERR_INVALID_ARG;
     if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
-    return adacomp_decode_sgd_group(h, msgs, K, &weights, &momentum, lr, mu, grad_scale, ws, ws_bytes, stream);
+    return adacomp_decode_sgd_group(h, msgs, msg_bytes, K, &weights, &momentum, lr, mu, grad_scale, ws, ws_bytes,
+                                    stream);
 }
 
-adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs, int32_t K, float* dense,
-                                         void* ws, size_t ws_bytes, cudaStream_t stream)
+adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                         int32_t K, float* dense, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (!h) return ADACOMP_ERR_INVALID_ARG;
     if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
-    return adacomp_decode_accumulate_group(h, msgs, K, &dense, ws, ws_bytes, stream);
+    return adacomp_decode_accumulate_group(h, msgs, msg_bytes, K, &dense, ws, ws_bytes, stream);
 }
 
 adacomp_status adacomp_query(adacomp_layer_t h, const void* ws, int32_t layer, cudaStream_t stream,

@@ -131,25 +131,23 @@ __host__ __device__ inline size_t compress_ws_bytes(int num_layers, uint64_t tot
 
 // Compress workspace of a launch group whose layers are all warp-sliced (the
 // sliced path: 16 <= L_T <= 509, no look-back):
-// [Ctl][LayerWs x num_layers][tile code offset u64 x T][tile code total u32 x T, padded to 16 B]
-// [per-warp code count u32 x 8 x T][sent mask u16 x 256 x T][sign mask u16 x 256 x T].
+// [Ctl][LayerWs x num_layers][tile code offset u64 x T, padded to 16 B]
+// [tile code total u32 x T, padded to 16 B][sent mask u16 x 256 x T][sign mask u16 x 256 x T].
 // A mask word belongs to compute lane (warp w, lane) of a tile: bit i is slot i of
 // the lane's 16 consecutive slots. The tile totals are zero between calls; the
-// other arrays are written by each call before they are read.
+// other arrays are written by each call before they are read. The mask arrays start
+// on 16-byte boundaries (the emitting kernel loads them 16 bytes at a time).
 constexpr size_t kMaskBytesPerTile = kWarps * 32 * 2;
+__host__ __device__ inline size_t pad16(size_t b) { return (b + 15) & ~(size_t)15; }
 __host__ __device__ inline size_t sl_excl_offset(int num_layers) { return ws_desc_offset(num_layers); }
-__host__ __device__ inline size_t sl_tot_offset(int num_layers, uint64_t T) { return sl_excl_offset(num_layers) + 8 * (size_t)T; }
-__host__ __device__ inline size_t sl_wcnt_offset(int num_layers, uint64_t T)
-{
-    return sl_tot_offset(num_layers, T) + ((4 * (size_t)T + 15) & ~(size_t)15);
-}
-__host__ __device__ inline size_t sl_sent_offset(int num_layers, uint64_t T) { return sl_wcnt_offset(num_layers, T) + 4 * kWarps * (size_t)T; }
+__host__ __device__ inline size_t sl_tot_offset(int num_layers, uint64_t T) { return sl_excl_offset(num_layers) + pad16(8 * (size_t)T); }
+__host__ __device__ inline size_t sl_sent_offset(int num_layers, uint64_t T) { return sl_tot_offset(num_layers, T) + pad16(4 * (size_t)T); }
 __host__ __device__ inline size_t sl_sign_offset(int num_layers, uint64_t T) { return sl_sent_offset(num_layers, T) + kMaskBytesPerTile * (size_t)T; }
 __host__ __device__ inline size_t sliced_ws_bytes(int num_layers, uint64_t T) { return sl_sign_offset(num_layers, T) + kMaskBytesPerTile * (size_t)T; }
 // Bytes at the start of a workspace that must be zero before its first call.
 __host__ __device__ inline size_t ws_zero_prefix(int num_layers, uint64_t T, bool sliced)
 {
-    return sliced ? sl_wcnt_offset(num_layers, T) : ws_desc_offset(num_layers) + 8 * (size_t)T;
+    return sliced ? sl_sent_offset(num_layers, T) : ws_desc_offset(num_layers) + 8 * (size_t)T;
 }
 
 // Look-back descriptor: flag in bits 62..63, the call's epoch in bits 54..61, value
@@ -181,13 +179,22 @@ constexpr size_t kDecodeLayerCodes = 2048;  // offset of the (layer, learner) co
 constexpr int kMaxDecodePairs = 1024;  // num_layers * K per launch
 constexpr uint64_t kBadOffset = ~0ull;
 __host__ __device__ inline size_t decode_per_learner(uint64_t total_tiles) { return 8 * (size_t)total_tiles; }
+// Code validation: one task per run of whole tiles of one layer holding at most
+// kValBins bins (one tile when a tile holds more).
+constexpr uint32_t kValBins = 128;
+__host__ __device__ inline uint32_t val_tiles_per_task(uint32_t bins_per_tile)
+{
+    return bins_per_tile >= kValBins ? 1u : kValBins / bins_per_tile;
+}
 
 constexpr uint32_t kErrTimeout = 1;
 
 struct DecodeParams {
     const uint8_t* msg[kMaxDecodePairs];  // [layer * K + k]
+    uint64_t len[kMaxDecodePairs];        // the messages' lengths in bytes, same order
     float* dense[kMaxGroup];              // the dense sum, or the weights when sgd != 0
     float* mom[kMaxGroup];                // momentum buffers (sgd != 0)
+    uint32_t val_begin[kMaxGroup + 1];    // validation tasks per learner: layer l's are [val_begin[l], val_begin[l + 1])
     int32_t K;
     int32_t sgd;                          // fused momentum-SGD step instead of a plain sum
     float lr, mu, scale;                  // w -= lr * v, v = mu * v + scale * g

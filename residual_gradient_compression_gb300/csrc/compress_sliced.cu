@@ -14,15 +14,15 @@
 //                    completion on per-warp mbarriers). Per slice: G, residue := G,
 //                    bin maxima (exact, into exponent buckets), the selection masks
 //                    (which do not depend on s), the per-bin counts, written straight
-//                    into the message, and the warp's code count. The codes' positions
+//                    into the message, and the tile's code total. The codes' positions
 //                    are not needed yet, so no CTA ever waits for another.
 //   slice_finalize   one CTA per layer: s from the exact sum, the header, and the
 //                    exclusive prefix of the tile code totals.
-//   slice_emit       one warp per tile, last tiles first: the codes written at their
-//                    final positions, with the sign of G read back from the residue,
-//                    and the fix-up residue = fl32(G - sign(G) s) of every sent element
-//                    (when the fix-up is deferred to the next call, the signs come
-//                    from a second mask and the residue is not touched).
+//   slice_emit       persistent warps, a run of tiles each, last tiles first: the codes
+//                    written at their final positions, with the sign of G read back
+//                    from the residue, and the fix-up residue = fl32(G - sign(G) s) of
+//                    every sent element (when the fix-up is deferred to the next call,
+//                    the signs come from a second mask and the residue is not touched).
 // Only the sent mask (1 bit per element; 2 with the deferred fix-up) passes between
 // the first and the last launch.
 #include "adacomp_internal.cuh"
@@ -219,8 +219,8 @@ __device__ __forceinline__ uint32_t to_slot_order(uint32_t r, int rot)
 // through the warp's scratch (shared atomics), the counts into the message and the
 // maxima into the warp's 32-bit exponent buckets (flushed to the layer's exact
 // accumulator every 8 slices and when the warp moves on to another layer). The
-// sent mask (and, deferred fix-up only, the sign mask) and the warp's code count go
-// to the workspace.
+// sent mask (and, deferred fix-up only, the sign mask) go to the workspace and the
+// slice's code count is added to its tile's total.
 //
 // kLazy: the corrections the previous call deferred (its sent mask, when the
 // workspace says they are pending) are applied as the residue is loaded,
@@ -264,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
 
     const uint32_t T = g.total_tiles, c = blockIdx.x, GS = gridDim.x;
     uint32_t* tile_tot = reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T));
-    uint32_t* wcnt = reinterpret_cast<uint32_t*>(ws + sl_wcnt_offset(g.num_layers, T));
     uint16_t* sent = reinterpret_cast<uint16_t*>(ws + sl_sent_offset(g.num_layers, T));
     uint16_t* sign = reinterpret_cast<uint16_t*>(ws + sl_sign_offset(g.num_layers, T));
     const bool pending = kLazy && reinterpret_cast<const volatile Ctl*>(ws)->pending != 0u;
@@ -434,10 +433,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
         sent[mi] = (uint16_t)fr;  // register order (the emitting kernel reorders)
         if (kLazy) sign[mi] = (uint16_t)(ngr & fr);  // without the fix-up, the emitting kernel has no G
         const uint32_t total = __reduce_add_sync(kFull, (uint32_t)__popc(fr));
-        if (lane == 0) {
-            wcnt[(size_t)t * kWarps + warp] = total;
-            if (total) atomicAdd(&tile_tot[t], total);
-        }
+        if (lane == 0 && total) atomicAdd(&tile_tot[t], total);
     }
     if (hist_layer >= 0) flush_hist(hist, reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer)), lane);
     if (poisoned && lane == 0) {
@@ -454,15 +450,24 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
 // One CTA per layer: s from the layer's exact sum (fp64, rounded once to fp32),
 // the header {s, B}, the result area, and the exclusive prefix of the layer's tile
 // code totals (which are left zero for the next call).
+//
+// The scan takes the layer's tiles in passes of kFinPer * 1024: thread tid loads
+// tiles pass_base + i * 1024 + tid for i < kFinPer (coalesced, every load of the
+// pass issued before the first is used), the warps scan each of the kFinPer rows
+// with shuffles, one warp scans the row-by-warp totals in row order, and the
+// offsets go back coalesced. A pass costs one global round trip and two barriers.
 constexpr int kFinThreads = 1024;
+constexpr int kFinWarps = kFinThreads / 32;
+constexpr int kFinPer = 8;
 
 __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __grid_constant__ KGroup g,
                                                                      uint8_t* __restrict__ ws)
 {
     __shared__ unsigned long long tmp[256];
     __shared__ unsigned long long words[kSumWords];
-    __shared__ unsigned long long wsum[kFinThreads / 32];
-    __shared__ unsigned long long layer_total;
+    __shared__ uint32_t wt[kFinPer][kFinWarps];              // per row and warp: the warp's total
+    __shared__ unsigned long long wx[kFinPer][kFinWarps];    // per row and warp: exclusive offset
+    __shared__ unsigned long long carry_s;
     const int l = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const KLayer& ly = g.layer[l];
     LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l));
@@ -471,41 +476,55 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
     uint64_t* excl = reinterpret_cast<uint64_t*>(ws + sl_excl_offset(g.num_layers)) + ly.tile_begin;
     if (tid < kSumWords) words[tid] = 0ull;
     if (tid < 256) tmp[tid] = lw->acc[tid];
+    if (tid == 0) carry_s = 0ull;
 
-    // thread tid scans tiles [i0, i1) of the layer
     const uint32_t nt = ly.num_tiles;
-    const uint32_t per = (nt + kFinThreads - 1) / kFinThreads;
-    const uint32_t i0 = min(nt, tid * per), i1 = min(nt, i0 + per);
-    unsigned long long mine = 0;
-    for (uint32_t i = i0; i < i1; ++i) mine += tot[i];
-    unsigned long long incl = mine;
+    for (uint32_t base = 0; base < nt; base += kFinPer * kFinThreads) {
+        uint32_t v[kFinPer], inc[kFinPer];
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        unsigned long long v = wsum[lane], x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += y;
+        for (int i = 0; i < kFinPer; ++i) {
+            const uint32_t j = base + i * kFinThreads + tid;
+            v[i] = j < nt ? tot[j] : 0u;
         }
-        wsum[lane] = x - v;  // exclusive over warps
+#pragma unroll
+        for (int i = 0; i < kFinPer; ++i) {
+            inc[i] = v[i];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, inc[i], o);
+                if (lane >= o) inc[i] += y;
+            }
+            if (lane == 31) wt[i][warp] = inc[i];
+        }
+        __syncthreads();  // also orders carry_s of the previous pass
+        if (warp == 0) {
+            unsigned long long c = carry_s;
+#pragma unroll
+            for (int i = 0; i < kFinPer; ++i) {
+                const uint32_t x = wt[i][lane];
+                uint32_t s = x;  // a row holds at most 1024 tiles of < 2^14 codes: 32 bits suffice
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const uint32_t y = __shfl_up_sync(kFull, s, o);
+                    if (lane >= o) s += y;
+                }
+                wx[i][lane] = c + (s - x);
+                c += __shfl_sync(kFull, s, 31);
+            }
+            if (lane == 0) carry_s = c;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kFinPer; ++i) {
+            const uint32_t j = base + i * kFinThreads + tid;
+            if (j < nt) {
+                excl[j] = wx[i][warp] + (inc[i] - v[i]);
+                if (v[i]) tot[j] = 0u;
+            }
+        }
     }
     __syncthreads();
-    unsigned long long run = wsum[warp] + incl - mine;
-    for (uint32_t i = i0; i < i1; ++i) {
-        const uint32_t v = tot[i];
-        excl[i] = run;
-        run += v;
-        tot[i] = 0u;
-    }
-    if (tid == kFinThreads - 1) layer_total = run;  // the last thread's range ends the layer
-    __syncthreads();
-    const unsigned long long nnz = layer_total;
+    const unsigned long long nnz = carry_s;
     if (warp == 0) {
         const double Ssum = exact_sum_warp(tmp, words, lane);
         if (lane == 0) {
@@ -526,142 +545,164 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
 }
 
 // ---------------------------------------------------------------- codes and fix-up
-// One warp per tile (no loop: many tiles in flight hide the latencies). Lane l
-// loads the sent masks (and, without kFix, the sign masks) of compute lane l of all
-// eight slices, the tile's code offset, the slices' code counts and the layer's
-// status in one batch; then, slice by slice (skipping slices that sent nothing), a
-// warp scan places each lane's sent elements after those of the earlier lanes and
-// slices. The masks are stored in the streaming kernel's register order and are
-// brought back to slot order here. Code of an element: ((its offset in its bin)
-// << 1) | sign.
-// kFix: the sent elements are listed in shared memory in code order (their tile
-// element indices) and the whole warp then walks the list (fix_listed): G from the
-// residue, the code, and the corrected residue. Without kFix the codes are written
-// from the masks directly.
+// Persistent warps take the tiles last first (the residue lines the streaming kernel
+// wrote last are the likeliest to be still in L2); a warp loads its next tile's masks
+// and code offset before it emits the current tile.
+// Emit lane L covers slice L >> 2, compute lanes 8 (L & 3) .. 8 (L & 3) + 7: one
+// 16-byte load of their sent masks (and, with the fix-up deferred, one of their sign
+// masks). The masks are stored in the streaming kernel's register order and are
+// brought back to slot order here. An exclusive warp scan of the lanes' popcounts
+// places each lane's sent elements, in element order (which is code order), in a
+// per-warp list in shared memory; the warp then walks the list with consecutive lanes
+// on consecutive codes:
+//   kFix: kFixBatch elements per lane at a time, all residue loads issued first (with
+//         a 64-byte L2 fill size: a scattered 4-byte load otherwise fills a whole
+//         128-byte line), then the code ((element - its bin's first element) << 1) |
+//         (G < 0) and the residue fl32(G - sign(G) s);
+//   otherwise the list entries carry the sign bit, and only the codes are written.
+// A tile with more than kListCap sent elements is listed and walked in rounds.
 constexpr int kEmitThreads = 256;
 constexpr int kEmitWarps = kEmitThreads / 32;
-constexpr int kFixCap = 1024;  // listed elements per warp before a flush
+constexpr int kListCap = 1024;
 constexpr int kFixBatch = 4;
 
-// The listed elements j = 0..n-1 of a tile (tile element indices, in code order):
-// G is loaded from the residue (kFixBatch per lane at a time, all loads issued first), the
-// code ((element - its bin's first element) << 1) | (G < 0) is written at code
-// position pos0 + j, and the residue becomes fl32(G - s) or fl32(G + s).
-__device__ __forceinline__ void fix_listed(const uint16_t* lst, uint32_t n, float* res, float s, uint8_t* codes,
-                                           uint64_t pos0, const KLayer& ly, int lane)
+__device__ __forceinline__ float ld_fill64(const float* p)
 {
-    __syncwarp();
-    for (uint32_t j0 = 0; j0 < n; j0 += 32 * kFixBatch) {
-        uint32_t e[kFixBatch];
-        float v[kFixBatch];
-#pragma unroll
-        for (int k = 0; k < kFixBatch; ++k) {
-            const uint32_t j = j0 + k * 32 + lane;
-            e[k] = j < n ? (uint32_t)lst[j] : 0xffffffffu;
-        }
-#pragma unroll
-        for (int k = 0; k < kFixBatch; ++k)
-            if (e[k] != 0xffffffffu) v[k] = res[e[k]];
-#pragma unroll
-        for (int k = 0; k < kFixBatch; ++k) {
-            if (e[k] == 0xffffffffu) continue;
-            const uint32_t neg = v[k] < 0.0f ? 1u : 0u;
-            const uint32_t off = e[k] - __umulhi(e[k], ly.inv_len) * (uint32_t)ly.bin_len;  // e < 2^16: exact
-            const uint32_t code = (off << 1) | neg;
-            const uint64_t pos = pos0 + j0 + k * 32 + lane;
-            if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
-            else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
-            res[e[k]] = neg ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
-        }
-    }
-    __syncwarp();
+    float v;
+    asm volatile("ld.global.L2::64B.f32 %0, [%1];" : "=f"(v) : "l"(p));
+    return v;
+}
+
+// The inputs of one tile's emission, loaded a tile ahead.
+struct EmitIn {
+    uint4 f;        // sent masks of the lane's eight compute lanes (register order)
+    uint4 ng;       // their sign masks (deferred fix-up only)
+    uint64_t pos;   // the tile's first code position in its message
+};
+
+template <bool kFix>
+__device__ __forceinline__ EmitIn emit_load(const uint8_t* ws, int num_layers, uint32_t T, uint32_t t, int lane)
+{
+    EmitIn in;
+    const uint4* sent = reinterpret_cast<const uint4*>(ws + sl_sent_offset(num_layers, T));
+    in.f = sent[(size_t)t * 32 + lane];
+    if (!kFix) in.ng = reinterpret_cast<const uint4*>(ws + sl_sign_offset(num_layers, T))[(size_t)t * 32 + lane];
+    else in.ng = make_uint4(0u, 0u, 0u, 0u);
+    in.pos = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(num_layers))[t];
+    return in;
 }
 
 template <bool kFix>
-__global__ void __launch_bounds__(kEmitThreads) slice_emit_kernel(const __grid_constant__ KGroup g,
+__global__ void __launch_bounds__(kEmitThreads, 5) slice_emit_kernel(const __grid_constant__ KGroup g,
                                                                   uint8_t* __restrict__ ws)
 {
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
-    __shared__ uint16_t fix_list[kFix ? kEmitWarps : 1][kFix ? kFixCap : 1];
+    __shared__ uint16_t lists[kEmitWarps][kListCap];
     for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) tb[e] = g.layer[e].tile_begin;
     __syncthreads();
     const int lane = threadIdx.x & 31;
+    uint16_t* lst = lists[threadIdx.x >> 5];
     const uint32_t T = g.total_tiles;
-    const uint32_t q = blockIdx.x * kEmitWarps + (threadIdx.x >> 5);
+    const uint32_t NW = gridDim.x * kEmitWarps;
+    uint32_t q = blockIdx.x * kEmitWarps + (threadIdx.x >> 5);
     if (q >= T) return;
-    const uint32_t t = T - 1u - q;  // last tiles first
-    const int l = layer_of_tile(tb, g.num_layers, t);
-    const KLayer ly = g.layer[l];  // into registers: one layer per warp
-    const LayerWs* lw = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l));
-    const uint16_t* sent = reinterpret_cast<const uint16_t*>(ws + sl_sent_offset(g.num_layers, T)) + (size_t)t * kWarps * 32 + lane;
-    const uint16_t* sign = reinterpret_cast<const uint16_t*>(ws + sl_sign_offset(g.num_layers, T)) + (size_t)t * kWarps * 32 + lane;
-    uint32_t f[kWarps], ng[kWarps];
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) { f[w] = sent[w * 32]; ng[w] = kFix ? 0u : sign[w * 32]; }
-    const uint32_t wc = lane < kWarps ? reinterpret_cast<const uint32_t*>(ws + sl_wcnt_offset(g.num_layers, T))[(size_t)t * kWarps + lane] : 0u;
-    const uint64_t tile_pos = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(g.num_layers))[t];
-    const uint32_t status = lw->result.status;
-    const float s = lw->result.s;
-    if (status != 0u) return;  // a layer whose streaming pass did not complete
-    uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
-    const int rot = seg_rot(lane);
-    uint16_t* lst = fix_list[kFix ? (threadIdx.x >> 5) : 0];
-    const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
-    float* res_tile = ly.residue + (int64_t)first_bin * ly.bin_len;
-    uint64_t slice_pos = tile_pos;
-    uint64_t list_pos = tile_pos;  // code position of the first listed element
-    uint32_t listed = 0;
-#pragma unroll 1
-    for (int w = 0; w < kWarps; ++w) {
-        const uint32_t fw = to_slot_order(f[0], rot), nw_ = to_slot_order(ng[0], rot);
-        // rotate the batch so that f[0] is always the current slice (static indexing)
-#pragma unroll
-        for (int k = 0; k + 1 < kWarps; ++k) { f[k] = f[k + 1]; ng[k] = ng[k + 1]; }
-        const uint32_t cnt_w = __shfl_sync(kFull, wc, w);
-        if (cnt_w == 0u) continue;
-        if (kFix && listed + cnt_w > (uint32_t)kFixCap) {
-            fix_listed(lst, listed, res_tile, s, codes, list_pos, ly, lane);
-            list_pos += listed;
-            listed = 0;
+    const int w = lane >> 2;         // the lane's slice
+    const int cl0 = 8 * (lane & 3);  // its first compute lane
+    EmitIn cur = emit_load<kFix>(ws, g.num_layers, T, T - 1u - q, lane);
+    int l_cached = -1;
+    float s = 0.0f;
+    uint32_t status = 0;
+    for (; q < T; q += NW) {
+        const uint32_t t = T - 1u - q;
+        const EmitIn in = cur;
+        if (q + NW < T) cur = emit_load<kFix>(ws, g.num_layers, T, T - 1u - (q + NW), lane);
+        const int l = layer_of_tile(tb, g.num_layers, t);
+        const KLayer& ly = g.layer[l];
+        if (l != l_cached) {
+            const LayerWs* lw = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l));
+            s = lw->result.s;
+            status = lw->result.status;
+            l_cached = l;
         }
-        const Slice Sl = slice_in(ly, l, t, w);
-        const uint32_t c = __popc(fw);
+        if (status != 0u) continue;  // a layer whose streaming pass did not complete
+        // the lane's eight masks in slot order, and its count
+        uint32_t m[8], ngm[8];
+        const uint32_t fw[4] = {in.f.x, in.f.y, in.f.z, in.f.w};
+        const uint32_t nw4[4] = {in.ng.x, in.ng.y, in.ng.z, in.ng.w};
+        uint32_t c = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rot = seg_rot(cl0 + i);
+            m[i] = to_slot_order((fw[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
+            ngm[i] = kFix ? 0u : to_slot_order((nw4[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
+            c += __popc(m[i]);
+        }
         uint32_t incl = c;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += y;
         }
-        if (fw) {
-            const int lane_e = (int)(Sl.a0 - Sl.ts) + kSeg * lane;  // tile element of slot 0
-            if constexpr (kFix) {
-                uint32_t li = listed + incl - c;
-                uint32_t m = fw;
-                while (m) {
-                    const int idx = __ffs(m) - 1;
-                    m &= m - 1;
-                    lst[li++] = (uint16_t)(lane_e + idx);
-                }
-            } else {
-                const LaneGeo qg = lane_geo(Sl, ly, lane);
-                const uint32_t base_lo = (uint32_t)((qg.lane_e - Sl.we0) - qg.bin_lo * ly.bin_len) << 1;
-                const uint32_t base_hi = base_lo - 2u * (uint32_t)ly.bin_len;
-                uint64_t pos = slice_pos + incl - c;
-                uint32_t m = fw;
-                while (m) {
-                    const int idx = __ffs(m) - 1;
-                    m &= m - 1;
-                    const uint32_t code = (idx < qg.split ? base_lo : base_hi) + 2u * idx + ((nw_ >> idx) & 1u);
-                    if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
-                    else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
-                    ++pos;
+        const uint32_t n = __shfl_sync(kFull, incl, 31);
+        if (n == 0u) continue;
+        const Slice Sl = slice_in(ly, l, t, w);
+        const int x0 = (int)(Sl.a0 - Sl.ts) + kSeg * cl0;  // tile element of slot 0 of compute lane cl0
+        float* res = ly.residue + Sl.ts;
+        uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
+        for (uint32_t r0 = 0; r0 < n; r0 += kListCap) {
+            // list this round's elements: positions r0 .. r0 + kListCap - 1 of the tile
+            uint32_t li = incl - c;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                uint32_t mm = m[i];
+                while (mm) {
+                    const int b = __ffs(mm) - 1;
+                    mm &= mm - 1;
+                    if (li - r0 < (uint32_t)kListCap)
+                        lst[li - r0] = (uint16_t)((x0 + kSeg * i + b) | (((ngm[i] >> b) & 1u) << 15));
+                    ++li;
                 }
             }
+            __syncwarp();
+            const uint32_t nr = min(n - r0, (uint32_t)kListCap);
+            const uint64_t pos0 = in.pos + r0;
+            if constexpr (kFix) {
+                for (uint32_t j0 = 0; j0 < nr; j0 += 32 * kFixBatch) {
+                    uint32_t e[kFixBatch];
+                    float v[kFixBatch];
+#pragma unroll
+                    for (int k = 0; k < kFixBatch; ++k) {
+                        const uint32_t j = j0 + k * 32 + lane;
+                        e[k] = j < nr ? (uint32_t)lst[j] : 0xffffffffu;
+                    }
+#pragma unroll
+                    for (int k = 0; k < kFixBatch; ++k)
+                        if (e[k] != 0xffffffffu) v[k] = ld_fill64(res + e[k]);
+#pragma unroll
+                    for (int k = 0; k < kFixBatch; ++k) {
+                        if (e[k] == 0xffffffffu) continue;
+                        const uint32_t neg = v[k] < 0.0f ? 1u : 0u;
+                        const uint32_t off = e[k] - __umulhi(e[k], ly.inv_len) * (uint32_t)ly.bin_len;  // e < 2^16: exact
+                        const uint32_t code = (off << 1) | neg;
+                        const uint64_t pos = pos0 + j0 + k * 32 + lane;
+                        if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
+                        else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
+                        res[e[k]] = neg ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
+                    }
+                }
+            } else {
+                for (uint32_t j = lane; j < nr; j += 32) {
+                    const uint32_t en = lst[j];
+                    const uint32_t x = en & 0x7fffu;
+                    const uint32_t off = x - __umulhi(x, ly.inv_len) * (uint32_t)ly.bin_len;
+                    const uint32_t code = (off << 1) | (en >> 15);
+                    if (ly.code_bytes == 1) codes[pos0 + j] = (uint8_t)code;
+                    else reinterpret_cast<uint16_t*>(codes)[pos0 + j] = (uint16_t)code;
+                }
+            }
+            __syncwarp();  // the list is rewritten by the next round or tile
         }
-        slice_pos += cnt_w;
-        listed += cnt_w;
     }
-    if (kFix && listed) fix_listed(lst, listed, res_tile, s, codes, list_pos, ly, lane);
 }
 
 // ---------------------------------------------------------------- materialise (deferred fix-up)
@@ -698,6 +739,7 @@ __global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const _
 struct SlicedDevice {
     int sms = 0;
     uint32_t smem_set[4] = {0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per variant
+    int emit_occ[2] = {0, 0};             // resident CTAs per SM of the emitting kernel (deferred, eager)
 };
 SlicedDevice g_sl_dev[64];
 
@@ -746,9 +788,18 @@ cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t strea
     if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
     slice_finalize_kernel<<<g.num_layers, kFinThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    const uint32_t egrid = (g.total_tiles + kEmitWarps - 1) / kEmitWarps;  // one warp per tile
-    if (g.lazy) slice_emit_kernel<false><<<egrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
-    else slice_emit_kernel<true><<<egrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    // persistent: as many CTAs as are resident at once, each warp a run of tiles
+    void (*ekern)(KGroup, uint8_t*) = g.lazy ? slice_emit_kernel<false> : slice_emit_kernel<true>;
+    int& eocc = di.emit_occ[g.lazy ? 0 : 1];
+    if (eocc == 0) {
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eocc, ekern, kEmitThreads, 0);
+        if (e != cudaSuccess) return e;
+        if (eocc < 1) return cudaErrorInvalidConfiguration;
+    }
+    const uint32_t eneed = (g.total_tiles + kEmitWarps - 1) / kEmitWarps;
+    const uint32_t ecap = (uint32_t)di.sms * (uint32_t)eocc;
+    const uint32_t egrid = eneed < ecap ? eneed : ecap;
+    ekern<<<egrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ev_after) e = cudaEventRecord(ev_after, stream);
     return e;

@@ -6,18 +6,24 @@
 // summary paragraph); this library reads the combination as a plain sum in learner
 // order, dense[j] = fl32(dense[j] + sign * s_k) for k = 0..K-1.
 //
-// Four launches:
-//   tile_sums   per (learner, tile): validate the header and the tile's per-bin
+// Five launches:
+//   tile_sums   per (learner, tile): check that the message is long enough to hold
+//               its header and counts, validate the header's B and the tile's per-bin
 //               counts, and sum the counts;
 //   tile_scan   per (layer, learner): exclusive prefix of the tile sums, i.e. where
-//               each tile's codes start in that message, and the message's total;
+//               each tile's codes start in that message, the message's total, and
+//               the check that its length is exactly 8 + 2B + w * total;
+//   validate    per (learner, run of tiles): within every bin the code offsets rise
+//               strictly and stay below the bin's length;
 //   accumulate  per tile of the layers that are streamed: the dense tile is staged
 //               in shared memory, every learner's codes for the tile are applied in
 //               learner order, and the tile is written back;
 //   sparse_accumulate  per tile of the layers whose learners sent few codes: the
 //               codes are added in place in global memory, learner by learner.
-// One warp owns each bin range of a tile, no two threads touch one element within a
-// learner, and no float atomics are used, so the result is deterministic.
+// A message that fails any check is rejected as a whole before anything is added
+// (its flag in the workspace). One warp owns each bin range of a tile, no two threads
+// touch one element within a learner, and no float atomics are used, so the result
+// is deterministic.
 #include "adacomp_internal.cuh"
 
 namespace adacomp {
@@ -56,9 +62,10 @@ __device__ __forceinline__ uint64_t* tile_offsets(uint8_t* ws, int k, uint32_t T
     return reinterpret_cast<uint64_t*>(ws + kDecodeFixed + (size_t)k * decode_per_learner(T));
 }
 
-// One warp per (learner k, tile t), every task in flight at once: the header's B
-// must equal the layer's B, and no count may exceed its bin's length; otherwise the
-// tile sum is kBadOffset.
+// One warp per (learner k, tile t), every task in flight at once: the message must
+// be at least 8 + 2B bytes long (else nothing of it is read), the header's B must
+// equal the layer's B, and no count may exceed its bin's length; otherwise the tile
+// sum is kBadOffset.
 __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_constant__ KGroup g,
                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
@@ -76,6 +83,10 @@ __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_con
     const int l = layer_of(tb, g.num_layers, t);
     const KLayer& ly = g.layer[l];
     const uint8_t* msg = p.msg[l * K + k];
+    if (p.len[l * K + k] < 8ull + 2ull * ly.nbins) {  // too short for its header and counts: read nothing
+        if (lane == 0) tile_offsets(ws, k, T)[t] = kBadOffset;
+        return;
+    }
     const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
     const int bins = (int)min(ly.bins_per_tile, ly.nbins - first_bin);
     const uint32_t hdr_b = *reinterpret_cast<const uint32_t*>(msg + 4);
@@ -94,8 +105,9 @@ __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_con
 }
 
 // One CTA per (layer, learner): the tile sums become exclusive offsets, in place,
-// each thread taking a contiguous run of tiles. A layer message with any bad tile
-// is marked bad as a whole; the message's code count goes to the workspace.
+// each thread taking a contiguous run of tiles. A message with any bad tile, or
+// whose length is not 8 + 2B + w * (its code count), is marked bad as a whole; the
+// message's code count goes to the workspace.
 __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__ KGroup g,
                                                          const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
@@ -145,7 +157,9 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
         if (lane == 31) total_s = x;
     }
     __syncthreads();
-    const bool bad = bad_s != 0u;
+    // the message must end exactly after its last code
+    const bool bad = bad_s != 0u ||
+                     p.len[l * K + k] != 8ull + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * total_s;
     unsigned long long run = wsum[warp] + incl - mine;
     for (uint32_t i = i0; i < i1; ++i) {
         const uint64_t v = off[i];
@@ -169,6 +183,131 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
             sparse_flags(ws)[e] = sum * 16ull < (unsigned long long)g.layer[e].n ? 1 : 0;
         }
     }
+}
+
+// One warp per (learner k, run of whole tiles of one layer with at most kValBins
+// bins, or one tile) of a message not already rejected: within every bin the code
+// offsets must rise strictly (a message gives each element at most one code) and
+// stay below the bin's length; otherwise the message is rejected as a whole, before
+// anything is added. The run's counts are loaded at once (lanes over bins), turned
+// into per-bin code starts in shared memory, and the codes are checked in batches of
+// kValBatch per lane, every load of a batch issued first.
+constexpr int kValBatch = 8;
+
+__global__ void __launch_bounds__(kDecThreads) validate_kernel(const __grid_constant__ KGroup g,
+                                                               const __grid_constant__ DecodeParams p, uint8_t* ws)
+{
+    __shared__ uint32_t vb[kMaxGroup + 1];
+    __shared__ uint32_t pre_s[kDecThreads / 32][kValBins + 2];
+    for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) vb[e] = p.val_begin[e];
+    __syncthreads();
+    const int K = p.K;
+    const int lane = threadIdx.x & 31;
+    const uint32_t per_learner = vb[g.num_layers];
+    const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
+    if (task >= (uint64_t)K * per_learner) return;
+    const int k = (int)(task / per_learner);
+    const uint32_t u = (uint32_t)(task - (uint64_t)k * per_learner);
+    int l = 0, hi = g.num_layers - 1;  // the layer whose tasks hold u
+    while (l < hi) {
+        const int mid = (l + hi + 1) >> 1;
+        if (vb[mid] <= u) l = mid;
+        else hi = mid - 1;
+    }
+    if (ws[16 + l * K + k]) return;  // rejected already: nothing more of it is read
+    const KLayer& ly = g.layer[l];
+    const uint32_t tpt = val_tiles_per_task(ly.bins_per_tile);
+    const uint32_t t0 = ly.tile_begin + (u - vb[l]) * tpt;                       // first tile
+    const uint32_t b0 = (t0 - ly.tile_begin) * ly.bins_per_tile;                 // first bin
+    const uint32_t nb = (uint32_t)min((uint64_t)tpt * ly.bins_per_tile, (uint64_t)(ly.nbins - b0));
+    const uint8_t* msg = p.msg[l * K + k];
+    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + b0;
+    const uint64_t off = tile_offsets(ws, k, g.total_tiles)[t0];
+    uint32_t* pre = pre_s[threadIdx.x >> 5];
+    uint32_t total = 0;
+    if (nb <= kValBins) {
+        uint32_t c[kValBins / 32];
+#pragma unroll
+        for (int i = 0; i < (int)(kValBins / 32); ++i) {
+            const uint32_t b = i * 32 + lane;
+            c[i] = b < nb ? cnt[b] : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < (int)(kValBins / 32); ++i) {
+            uint32_t incl = c[i];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            pre[i * 32 + lane] = total + incl - c[i];
+            total += __shfl_sync(kFull, incl, 31);
+        }
+    } else {
+        // a tile with more bins than the shared prefix holds (bins shorter than 32):
+        // checked bin by bin from the counts, one lane per bin
+        uint64_t start = off;
+        for (uint32_t c0 = 0; c0 < nb; c0 += 32) {
+            const uint32_t b = c0 + lane;
+            const uint32_t c = b < nb ? cnt[b] : 0u;
+            uint32_t incl = c;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            bool ok = true;
+            if (b < nb) {
+                const uint32_t len = (b0 + b == ly.nbins - 1) ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len)
+                                                              : (uint32_t)ly.bin_len;
+                const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * (start + incl - c);
+                uint32_t prev = 0;
+                for (uint32_t i = 0; i < c; ++i) {
+                    const uint32_t o = (ly.code_bytes == 1 ? codes[i] : reinterpret_cast<const uint16_t*>(codes)[i]) >> 1;
+                    ok = ok && o < len && (i == 0 || o > prev);
+                    prev = o;
+                }
+            }
+            if (!__all_sync(kFull, ok)) {
+                if (lane == 0) ws[16 + l * K + k] = 1;
+                return;
+            }
+            start += __shfl_sync(kFull, incl, 31);
+        }
+        return;
+    }
+    if (lane == 0) pre[nb] = total;
+    __syncwarp();
+    const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * off;
+    const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len;
+    bool ok = true;
+    for (uint32_t j0 = 0; j0 < total; j0 += 32 * kValBatch) {
+        uint32_t cur[kValBatch], prv[kValBatch];
+#pragma unroll
+        for (int q = 0; q < kValBatch; ++q) {
+            const uint32_t j = j0 + q * 32 + lane;
+            cur[q] = prv[q] = 0u;
+            if (j < total) {
+                cur[q] = ly.code_bytes == 1 ? codes[j] : reinterpret_cast<const uint16_t*>(codes)[j];
+                if (j) prv[q] = ly.code_bytes == 1 ? codes[j - 1] : reinterpret_cast<const uint16_t*>(codes)[j - 1];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < kValBatch; ++q) {
+            const uint32_t j = j0 + q * 32 + lane;
+            if (j >= total) continue;
+            int lo = 0, hb = (int)nb - 1;  // last bin whose start is <= j
+            while (lo < hb) {
+                const int mid = (lo + hb + 1) >> 1;
+                if (pre[mid] <= j) lo = mid;
+                else hb = mid - 1;
+            }
+            const uint32_t len = (b0 + lo == ly.nbins - 1) ? (uint32_t)last_len : (uint32_t)ly.bin_len;
+            const uint32_t o = cur[q] >> 1;
+            ok = ok && o < len && (j == pre[lo] || o > (prv[q] >> 1));
+        }
+    }
+    if (!__all_sync(kFull, ok) && lane == 0) ws[16 + l * K + k] = 1;
 }
 
 // Persistent over tiles (CTA c takes tiles c, c + grid, ...). The dense tiles
@@ -212,10 +351,12 @@ struct AccTile {
 };
 
 // Per-CTA copy of what the accumulate kernels look up per tile: each layer's
-// first tile and whether it is summed in place.
+// first tile, whether it is summed in place, and which (layer, learner) messages
+// passed every check.
 struct LayerIndex {
     uint32_t tb[kMaxGroup];
     uint8_t sparse[kMaxGroup];
+    uint8_t ok[kMaxDecodePairs];
 };
 
 __device__ __forceinline__ void load_index(LayerIndex& X, const KGroup& g, uint8_t* ws, int K, bool sgd)
@@ -224,6 +365,7 @@ __device__ __forceinline__ void load_index(LayerIndex& X, const KGroup& g, uint8
         X.tb[e] = g.layer[e].tile_begin;
         X.sparse[e] = !sgd && sparse_flags(ws)[e] != 0 ? 1 : 0;
     }
+    for (int e = threadIdx.x; e < g.num_layers * K; e += blockDim.x) X.ok[e] = ws[16 + e] == 0 ? 1 : 0;
 }
 
 __device__ __forceinline__ AccTile acc_tile(const KGroup& g, const LayerIndex& X, uint32_t t)
@@ -346,7 +488,7 @@ __device__ __forceinline__ void acc_fetch(const KLayer& ly, const uint8_t* msg, 
 // bin prefix and walks forward, adding sign * s to sd[bin * L_T + offset].
 __device__ __forceinline__ void acc_walk_pf(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
                                             uint32_t before, uint32_t total, int b0, int b1, float* sd,
-                                            const uint32_t* pre, uint8_t* bad, int lane, const CodePrefetch& P,
+                                            const uint32_t* pre, int lane, const CodePrefetch& P,
                                             bool use_prefetch)
 {
     const float s = use_prefetch ? P.s : *reinterpret_cast<const float*>(msg);
@@ -369,11 +511,9 @@ __device__ __forceinline__ void acc_walk_pf(const KLayer& ly, const AccTile& A, 
             const uint32_t o = code >> 1;
             const int bin = b0 + b;
             const int64_t len = (A.first_bin + bin == ly.nbins - 1) ? last_len : ly.bin_len;
-            if ((int64_t)o < len) {
+            if ((int64_t)o < len) {  // always true for a validated message; keeps every write in the tile
                 float* x = sd + (int64_t)bin * ly.bin_len + o;
                 *x = __fadd_rn(*x, (code & 1u) ? -s : s);
-            } else {
-                *bad = 1;  // offset outside its bin: ignored, message flagged
             }
         };
         uint32_t i = i0;
@@ -391,19 +531,19 @@ __device__ __forceinline__ void acc_walk_pf(const KLayer& ly, const AccTile& A, 
 
 __device__ __forceinline__ void acc_walk(const KLayer& ly, const AccTile& A, const uint8_t* msg, uint64_t off,
                                          uint32_t before, uint32_t total, int b0, int b1, float* sd,
-                                         const uint32_t* pre, uint8_t* bad, int lane)
+                                         const uint32_t* pre, int lane)
 {
     CodePrefetch none;
-    acc_walk_pf(ly, A, msg, off, before, total, b0, b1, sd, pre, bad, lane, none, false);
+    acc_walk_pf(ly, A, msg, off, before, total, b0, b1, sd, pre, lane, none, false);
 }
 
 // Warp `warp` owns one bin of tile A (tiles of at most 8 bins): every learner's
 // codes for that bin, learners kb .. kb + 31 per round. acc_bin_prep: lane k
-// fetches learner kb + k's tile offset, scale and counts (independent of the dense
-// tile, so it can run while that is loading). acc_bin_apply: the codes are
-// prefetched for 8 learners at a time (lane i holding code i of each) and added in
-// learner order.
-constexpr int kAccWindow = 8;
+// fetches learner kb + k's tile offset, scale and the counts of the tile's bins up
+// to this one, every load issued at once (independent of the dense tile, so it runs
+// while that is loading). acc_bin_apply: the codes of kAccWindow learners at a time
+// are loaded at once (lane i holding code i of each) and added in learner order.
+constexpr int kAccWindow = 16;
 
 struct BinPrep {
     unsigned long long start;  // index of the learner's first code for this bin
@@ -413,8 +553,8 @@ struct BinPrep {
 };
 
 __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile& A, const DecodeParams& p,
-                                                uint8_t* ws, uint32_t T, uint32_t t, int l, int bin, int kb,
-                                                int lane)
+                                                const LayerIndex& X, uint8_t* ws, uint32_t T, uint32_t t, int l,
+                                                int bin, int kb, int lane)
 {
     BinPrep P;
     P.start = 0;
@@ -423,24 +563,29 @@ __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile&
     P.s = 0.0f;
     const int K = p.K;
     const int k = kb + lane;
-    if (k < K) {
+    if (k < K && X.ok[l * K + k]) {
+        const uint8_t* msg = p.msg[l * K + k];
+        const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + A.first_bin;
+        uint32_t c[8];
+#pragma unroll
+        for (int b = 0; b < 8; ++b) c[b] = b <= bin ? cnt[b] : 0u;
         const uint64_t off = tile_offsets(ws, k, T)[t];
-        if (off != kBadOffset) {
-            const uint8_t* msg = p.msg[l * K + k];
-            const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + A.first_bin;
-            uint32_t before = 0;
-            for (int b = 0; b < bin; ++b) before += cnt[b];
-            P.c = cnt[bin];
-            P.s = *reinterpret_cast<const float*>(msg);
-            P.start = off + before;
-            P.codes = msg + 8 + 2ull * ly.nbins;
+        P.s = *reinterpret_cast<const float*>(msg);
+        uint32_t before = 0, mine = 0;
+#pragma unroll
+        for (int b = 0; b < 8; ++b) {
+            before += b < bin ? c[b] : 0u;
+            mine += b == bin ? c[b] : 0u;
         }
+        P.c = mine;
+        P.start = off + before;
+        P.codes = msg + 8 + 2ull * ly.nbins;
     }
     return P;
 }
 
-__device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A, int K, uint8_t* ws, int l, int bin,
-                                              int kb, const BinPrep& P, float* sd, int lane)
+__device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A, int K, int bin, int kb,
+                                              const BinPrep& P, float* sd, int lane)
 {
     const int L = ly.bin_len;
     const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * L;
@@ -466,11 +611,9 @@ __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A
             const int kk = k0 + w;
             const uint32_t ck = __shfl_sync(kFull, P.c, kk);
             const float s = __shfl_sync(kFull, P.s, kk);
-            bool bad = false;
             if (cw[w] != 0xffffffffu) {
                 const uint32_t o = cw[w] >> 1;
-                if (o < len) x0[o] = __fadd_rn(x0[o], (cw[w] & 1u) ? -s : s);
-                else bad = true;
+                if (o < len) x0[o] = __fadd_rn(x0[o], (cw[w] & 1u) ? -s : s);  // always in range once validated
             }
             if (ck > 32u) {  // more codes than lanes in this bin: the rest, in rounds
                 const unsigned long long st = __shfl_sync(kFull, P.start, kk);
@@ -480,10 +623,8 @@ __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A
                     const uint32_t code = wide ? reinterpret_cast<const uint16_t*>(cp)[st + i] : cp[st + i];
                     const uint32_t o = code >> 1;
                     if (o < len) x0[o] = __fadd_rn(x0[o], (code & 1u) ? -s : s);
-                    else bad = true;
                 }
             }
-            if (bad) ws[16 + l * K + kb + kk] = 1;  // offset outside its bin: ignored, message flagged
             __syncwarp();  // learner kk's additions come before learner kk + 1's
         }
     }
@@ -523,10 +664,11 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         }
         return T;
     };
-    // Tile window: t (processed now) and t1 (copied into the other stage once the
-    // store of t's predecessor has read it, at the end of this iteration). (Three
-    // stages measured no faster for the plain sum, and the fused SGD step's three
-    // arrays per stage would then leave one CTA per SM.)
+    // Tile window: t (processed now) and t1 (copied into the other stage at the start
+    // of this iteration, as soon as the bulk store of the tile that stage held has
+    // read it, so the copy has the whole iteration to land). (Three stages measured
+    // no faster for the plain sum, and the fused SGD step's three arrays per stage
+    // would then leave one CTA per SM.)
     static_assert(kAccStages == 2, "the ring below holds one tile ahead");
     uint32_t t = next_tile(G0);
     uint32_t t1 = t < T ? next_tile(t + GS) : T;
@@ -542,6 +684,10 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     int i = 0;
     for (; t < T; ++i) {
         float* st = stage(i);
+        if (tid == 0 && t1 < T) {
+            ptx::bulk_wait_read0();  // the store of the tile stage i + 1 held has read it
+            acc_issue<kSGD>(g, X, p, t1, stage(i + 1), arr_floats, &bar[(i + 1) % kAccStages]);
+        }
         const AccTile A = acc_tile(g, X, t);
         const KLayer& ly = g.layer[A.layer];
         const int l = A.layer;
@@ -555,16 +701,14 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         }
         BinPrep bp;
         CodePrefetch cp0;
-        uint64_t off0 = kBadOffset;
+        uint64_t off0 = 0;
         uint32_t before0 = 0, total0 = 0;
         if (bpw == 1) {
-            if (b0 < b1) bp = acc_bin_prep(ly, A, p, ws, T, t, l, b0, 0, lane);
-        } else if (b0 < b1) {
+            if (b0 < b1) bp = acc_bin_prep(ly, A, p, X, ws, T, t, l, b0, 0, lane);
+        } else if (b0 < b1 && X.ok[l * K]) {
             off0 = tile_offsets(ws, 0, T)[t];
-            if (off0 != kBadOffset) {
-                total0 = acc_prefix(A, p.msg[l * K], b0, b1, pre, &before0, lane);
-                acc_fetch(ly, p.msg[l * K], off0, before0, total0, lane, cp0);
-            }
+            total0 = acc_prefix(A, p.msg[l * K], b0, b1, pre, &before0, lane);
+            acc_fetch(ly, p.msg[l * K], off0, before0, total0, lane, cp0);
         }
         if (!__syncthreads_and(acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u, g.timeout_ns))) {
             poisoned = true;
@@ -574,18 +718,18 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         if (bpw == 1) {
             if (b0 < b1) {
                 for (int kb = 0; kb < K; kb += 32) {
-                    if (kb) bp = acc_bin_prep(ly, A, p, ws, T, t, l, b0, kb, lane);
-                    acc_bin_apply(ly, A, K, ws, l, b0, kb, bp, sd, lane);
+                    if (kb) bp = acc_bin_prep(ly, A, p, X, ws, T, t, l, b0, kb, lane);
+                    acc_bin_apply(ly, A, K, b0, kb, bp, sd, lane);
                 }
             }
         } else if (b0 < b1) {
             for (int k = 0; k < K; ++k) {
+                if (!X.ok[l * K + k]) continue;  // a rejected message adds nothing
                 const uint64_t off = k ? tile_offsets(ws, k, T)[t] : off0;
-                if (off == kBadOffset) continue;
                 const uint8_t* msg = p.msg[l * K + k];
                 uint32_t before = before0, total = total0;
                 if (k) total = acc_prefix(A, msg, b0, b1, pre, &before, lane);
-                acc_walk_pf(ly, A, msg, off, before, total, b0, b1, sd, pre, ws + 16 + l * K + k, lane, cp0, k == 0);
+                acc_walk_pf(ly, A, msg, off, before, total, b0, b1, sd, pre, lane, cp0, k == 0);
             }
         }
 
@@ -627,11 +771,6 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
                 }
             }
             ptx::bulk_commit();
-            // refill the stage whose store was committed one tile ago
-            if (t1 < T) {
-                asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
-                acc_issue<kSGD>(g, X, p, t1, stage(i + 1), arr_floats, &bar[(i + 1) % kAccStages]);
-            }
         }
         t = t1;
         t1 = t1 < T ? next_tile(t1 + GS) : T;
@@ -645,8 +784,9 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
             const int l = layer_of(X.tb, g.num_layers, u);
             for (int k = tid; k < K; k += kDecThreads) ws[16 + l * K + k] = 1;
         }
-        // the load of the tile whose wait ran out (the next one was not issued yet)
+        // the load of the tile whose wait ran out, and that of the next tile
         acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u, g.timeout_ns);
+        if (t1 < T) acc_wait(&bar[(i + 1) % kAccStages], (uint32_t)((i + 1) / kAccStages) & 1u, g.timeout_ns);
     }
 }
 
@@ -666,6 +806,7 @@ __global__ void __launch_bounds__(kDecThreads) sparse_accumulate_kernel(const __
         X.tb[e] = g.layer[e].tile_begin;
         X.sparse[e] = sparse_flags(ws)[e];
     }
+    for (int e = threadIdx.x; e < g.num_layers * p.K; e += kDecThreads) X.ok[e] = ws[16 + e] == 0 ? 1 : 0;
     __syncthreads();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t T = g.total_tiles;
@@ -686,12 +827,12 @@ __global__ void __launch_bounds__(kDecThreads) sparse_accumulate_kernel(const __
         const KLayer& ly = g.layer[l];
         float* sd = p.dense[l] + A.ts;
         for (int k = 0; k < K; ++k) {
+            if (!X.ok[l * K + k]) continue;  // a rejected message adds nothing
             const uint64_t off = tile_offsets(ws, k, T)[t];
-            if (off == kBadOffset) continue;
             const uint8_t* msg = p.msg[l * K + k];
             uint32_t before = 0;
             const uint32_t total = acc_prefix(A, msg, 0, A.bins, pre, &before, lane);
-            acc_walk(ly, A, msg, off, before, total, 0, A.bins, sd, pre, ws + 16 + l * K + k, lane);
+            acc_walk(ly, A, msg, off, before, total, 0, A.bins, sd, pre, lane);
         }
         t += NW;
     }
@@ -724,6 +865,10 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     tile_scan_kernel<<<(unsigned)(g.num_layers * p.K), 1024, 0, stream>>>(g, p, w);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const uint64_t vtasks = (uint64_t)p.K * p.val_begin[g.num_layers];
+    validate_kernel<<<(unsigned)((vtasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const bool sgd = p.sgd != 0;

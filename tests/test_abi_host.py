@@ -53,13 +53,17 @@ def _tiles(n, L):
     return -(-B // bpt)
 
 
+def _pad16(b):
+    return -(-b // 16) * 16
+
+
 @pytest.mark.parametrize("n,L", [(1_000_000, 500), (777_777, 50), (65_537, 16), (10, 509)])
 def test_sliced_workspace_layout(n, L):
     """16 <= L_T <= 509: control block, one 2112-byte layer block, then per tile a
-    u64 code offset, a u32 code total (padded to 16 bytes), eight u32 slice counts
-    and two 512-byte masks; the deferred fix-up needs no more."""
+    u64 code offset and a u32 code total (each array padded to 16 bytes) and two
+    512-byte masks; the deferred fix-up needs no more."""
     T = _tiles(n, L)
-    expect = 64 + 2112 + 8 * T + (-(-4 * T // 16) * 16) + 32 * T + 1024 * T
+    expect = 64 + 2112 + _pad16(8 * T) + _pad16(4 * T) + 1024 * T
     h = ac.adacomp_init_layer(n, L, ac.F32)
     assert h.compress_ws_bytes == expect
     assert ac.adacomp_set_lazy_fixup(h, True) == expect
@@ -83,7 +87,7 @@ def test_group_workspace_takes_the_lookback_layout_when_mixed():
     ns, Ls = [40_000, 30_000], [50, 500]
     T = sum(_tiles(n, L) for n, L in zip(ns, Ls))
     h = ac.adacomp_init_group(ns, Ls, [ac.F32, ac.F32])
-    assert h.compress_ws_bytes == 64 + 2 * 2112 + 8 * T + (-(-4 * T // 16) * 16) + 32 * T + 1024 * T
+    assert h.compress_ws_bytes == 64 + 2 * 2112 + _pad16(8 * T) + _pad16(4 * T) + 1024 * T
     ns2, Ls2 = ns + [20_000], Ls + [5000]
     T2 = T + _tiles(20_000, 5000)
     h2 = ac.adacomp_init_group(ns2, Ls2, [ac.F32] * 3)
@@ -131,15 +135,17 @@ def test_decode_argument_checks_return_before_launch():
     A = 1 << 20
     L = ac.lib()
     one = (ctypes.c_void_p * 1)(A)
+    ln = (ctypes.c_uint64 * 1)(h.max_msg_bytes[0])
     wsb = h.decode_ws_bytes(1)
-    assert L.adacomp_decode_accumulate(h.ptr, one, 0, A, A, wsb, None) == ac.ERR_INVALID_ARG
-    assert L.adacomp_decode_accumulate(h.ptr, one, 257, A, A, 1 << 30, None) == ac.ERR_INVALID_ARG
-    assert L.adacomp_decode_accumulate(h.ptr, one, 1, A + 4, A, wsb, None) == ac.ERR_ALIGNMENT
+    assert L.adacomp_decode_accumulate(h.ptr, one, ln, 0, A, A, wsb, None) == ac.ERR_INVALID_ARG
+    assert L.adacomp_decode_accumulate(h.ptr, one, ln, 257, A, A, 1 << 30, None) == ac.ERR_INVALID_ARG
+    assert L.adacomp_decode_accumulate(h.ptr, one, ln, 1, A + 4, A, wsb, None) == ac.ERR_ALIGNMENT
     bad = (ctypes.c_void_p * 1)(A + 2)
-    assert L.adacomp_decode_accumulate(h.ptr, bad, 1, A, A, wsb, None) == ac.ERR_ALIGNMENT
-    assert L.adacomp_decode_accumulate(h.ptr, one, 1, A, A, wsb - 1, None) == ac.ERR_WORKSPACE
+    assert L.adacomp_decode_accumulate(h.ptr, bad, ln, 1, A, A, wsb, None) == ac.ERR_ALIGNMENT
+    assert L.adacomp_decode_accumulate(h.ptr, one, ln, 1, A, A, wsb - 1, None) == ac.ERR_WORKSPACE
     null = (ctypes.c_void_p * 1)(None)
-    assert L.adacomp_decode_accumulate(h.ptr, null, 1, A, A, wsb, None) == ac.ERR_INVALID_ARG
+    assert L.adacomp_decode_accumulate(h.ptr, null, ln, 1, A, A, wsb, None) == ac.ERR_INVALID_ARG
+    assert L.adacomp_decode_accumulate(h.ptr, one, None, 1, A, A, wsb, None) == ac.ERR_INVALID_ARG
     ac.adacomp_free(h)
 
 

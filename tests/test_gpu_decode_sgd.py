@@ -39,7 +39,7 @@ def test_decode_sgd_matches_oracle(n, L, K):
     w_ref, v_ref = w.cpu().numpy().copy(), v.cpu().numpy().copy()
     lr, mu, scale = 0.01, 0.9, 1.0 / K
     ws = workspace(h.decode_ws_bytes(K))
-    ac.adacomp_decode_sgd(h, [m for m, _ in msgs], w, v, lr, mu, ws, grad_scale=scale)
+    ac.adacomp_decode_sgd(h, [m for m, _ in msgs], [mb for _, mb in msgs], w, v, lr, mu, ws, grad_scale=scale)
     assert ac.adacomp_decode_status(h, ws) == ac.OK
     host = [m[:mb].cpu().numpy() for m, mb in msgs]
     assert oracle.decode_sgd(n, L, host, w_ref, v_ref, lr, mu, scale) == oracle.OK
@@ -55,7 +55,8 @@ def test_decode_sgd_group_matches_per_layer():
     ws_ = [_wv(n, i) for i, (n, _) in enumerate(shapes)]
     refs = [(w.cpu().numpy().copy(), v.cpu().numpy().copy()) for w, v in ws_]
     ws = workspace(h.decode_ws_bytes(K))
-    ac.adacomp_decode_sgd_group(h, [[m for m, _ in msgs] for msgs in per_layer], [w for w, _ in ws_],
+    ac.adacomp_decode_sgd_group(h, [[m for m, _ in msgs] for msgs in per_layer],
+                                [[mb for _, mb in msgs] for msgs in per_layer], [w for w, _ in ws_],
                                 [v for _, v in ws_], 0.05, 0.5, ws, grad_scale=1.0)
     assert ac.adacomp_decode_status(h, ws) == ac.OK
     for (n, L), msgs, (w, v), (w_ref, v_ref) in zip(shapes, per_layer, ws_, refs):
@@ -74,7 +75,7 @@ def test_decode_sgd_skips_a_malformed_message():
     w, v = _wv(n, 5)
     w_ref, v_ref = w.cpu().numpy().copy(), v.cpu().numpy().copy()
     ws = workspace(h.decode_ws_bytes(2))
-    ac.adacomp_decode_sgd(h, [msgs[0][0], bad], w, v, 0.1, 0.9, ws)
+    ac.adacomp_decode_sgd(h, [msgs[0][0], bad], [msgs[0][1], mb], w, v, 0.1, 0.9, ws)
     assert ac.adacomp_decode_status(h, ws) == ac.ERR_BAD_MESSAGE
     # the good learner alone, as the oracle sees it
     assert oracle.decode_sgd(n, L, [msgs[0][0][:msgs[0][1]].cpu().numpy()], w_ref, v_ref, 0.1, 0.9) == oracle.OK

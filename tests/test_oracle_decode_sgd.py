@@ -48,7 +48,7 @@ def test_zero_momentum_unit_rate_gives_the_decoded_gradient():
     assert np.array_equal(w.view(np.uint32), (w0 - g).view(np.uint32))
 
 
-def test_zero_rate_leaves_weights_and_a_bad_message_changes_nothing():
+def test_zero_rate_leaves_weights_and_a_bad_message_adds_nothing():
     n, L = 5_003, 500
     msgs = _msgs(n, L, 2, 3)
     w = np.ones(n, np.float32)
@@ -59,4 +59,8 @@ def test_zero_rate_leaves_weights_and_a_bad_message_changes_nothing():
     bad[4] ^= 1  # wrong B
     w2, v2 = w.copy(), v.copy()
     assert oracle.decode_sgd(n, L, [msgs[0], bad], w2, v2, 0.1, 0.9, 1.0) == oracle.ERR_BAD_MESSAGE
-    assert np.array_equal(w2, w) and np.array_equal(v2, v)
+    # the rejected message adds nothing: the step is the one the good message alone gives
+    w3, v3 = w.copy(), v.copy()
+    assert oracle.decode_sgd(n, L, [msgs[0]], w3, v3, 0.1, 0.9, 1.0) == oracle.OK
+    assert np.array_equal(w2, w3) and np.array_equal(v2, v3)
+    assert not np.array_equal(w2, w)

@@ -69,3 +69,41 @@ def test_decode_rejects_malformed_messages():
         dense = np.zeros(10, np.float32)
         assert oracle.decode_accumulate(10, 4, [bad], dense) == oracle.ERR_BAD_MESSAGE
         assert not dense.any()
+
+
+def test_decode_validation_hand_cases():
+    """Every malformed variant of the hand message is rejected and adds nothing; the
+    good message beside it is still added (tests/golden/hand_decode_malformed.json)."""
+    case = load("hand_decode_malformed")
+    n, L = case["n"], case["bin_len"]
+    good = hex_bytes(case["good_hex"])
+    gq = f32_array(case["good_decode"])
+    dense = np.zeros(n, np.float32)
+    assert oracle.decode_accumulate(n, L, [good], dense) == oracle.OK
+    assert np.array_equal(dense, gq)
+    for name, hx in case["bad_hex"].items():
+        bad = hex_bytes(hx)
+        dense = np.zeros(n, np.float32)
+        flags = np.zeros(1, np.uint8)
+        assert oracle.decode_accumulate(n, L, [bad], dense, bad=flags) == oracle.ERR_BAD_MESSAGE, name
+        assert not dense.any() and flags[0] == 1, name
+        dense = np.zeros(n, np.float32)
+        flags = np.zeros(2, np.uint8)
+        assert oracle.decode_accumulate(n, L, [bad, good], dense, bad=flags) == oracle.ERR_BAD_MESSAGE, name
+        assert np.array_equal(dense, gq) and list(flags) == [1, 0], name
+
+
+def test_decode_length_is_the_one_given():
+    """The length that comes with a message decides, not the buffer holding it: the
+    good message inside a longer zeroed buffer is accepted with its own length and
+    rejected with the buffer's."""
+    case = load("hand_decode_malformed")
+    good = hex_bytes(case["good_hex"])
+    buf = np.zeros(64, np.uint8)
+    buf[:good.size] = good
+    dense = np.zeros(10, np.float32)
+    assert oracle.decode_accumulate(10, 4, [buf], dense, lens=[good.size]) == oracle.OK
+    assert np.array_equal(dense, f32_array(case["good_decode"]))
+    dense = np.zeros(10, np.float32)
+    assert oracle.decode_accumulate(10, 4, [buf], dense, lens=[buf.size]) == oracle.ERR_BAD_MESSAGE
+    assert not dense.any()

@@ -2,7 +2,8 @@
 
 A mutant is a copy of oracle/adacomp_oracle.c with one planted mistake, compiled
 into a temporary directory on the CPU. The pins replayed against it are the
-hand-derived fixtures, the first-step closed form and the fsum pin of s; a mutant
+hand-derived fixtures, the first-step closed form, the fsum pin of s and the decoder's
+message checks; a mutant
 that passes them all would mean the pins leave that part of the method unchecked.
 """
 import math
@@ -37,6 +38,10 @@ MUTANTS = {
     "sgd_steps_with_old_momentum": ("float delta = lr * v[j];", "float delta = lr * (v[j] - step);"),
     "big_endian_count": ("put_u16(counts + 2 * b, cnt);",
                          "put_u16(counts + 2 * b, ((cnt & 0xff) << 8) | (cnt >> 8));"),
+    "duplicate_offsets_accepted": ("if (off >= blen || off <= prev) return 0;",
+                                   "if (off >= blen || off < prev) return 0;"),
+    "length_unchecked": ("if (len != 8 + 2 * (uint64_t)B + (uint64_t)w * total) return 0;", "(void)total;"),
+    "rejected_message_still_added": ("        if (!message_ok(n, L, msgs[k], lens[k])) continue;\n", ""),
 }
 
 
@@ -78,6 +83,17 @@ def _golden_pins(lib):
     assert np.array_equal(dense, f32_array(case["expect_dense"]))
 
 
+def _decode_validation_pins(lib):
+    case = load("hand_decode_malformed")
+    n, L = case["n"], case["bin_len"]
+    good = hex_bytes(case["good_hex"])
+    gq = f32_array(case["good_decode"])
+    for name, hx in case["bad_hex"].items():
+        dense = np.zeros(n, np.float32)
+        assert oracle.decode_accumulate(n, L, [hex_bytes(hx), good], dense, lib=lib) == oracle.ERR_BAD_MESSAGE, name
+        assert np.array_equal(dense, gq), name
+
+
 def _closed_form_pins(lib):
     rng = np.random.default_rng(3)
     for n, L, bf16 in ((1003, 50, False), (4097, 64, False), (12345, 500, False),
@@ -106,7 +122,7 @@ def _closed_form_pins(lib):
 def test_mutant_is_caught(tmp_path, name):
     lib = _build_mutant(tmp_path, name)
     failures = 0
-    for pins in (_golden_pins, _closed_form_pins):
+    for pins in (_golden_pins, _closed_form_pins, _decode_validation_pins):
         try:
             pins(lib)
         except AssertionError:
@@ -121,3 +137,4 @@ def test_unmutated_copy_passes(tmp_path):
     lib = oracle.Oracle(str(so)).lib
     _golden_pins(lib)
     _closed_form_pins(lib)
+    _decode_validation_pins(lib)
