@@ -552,30 +552,38 @@ def run_device(args, rank, world):
         out["lazy_fixup"] = run_lazy(args, run, sp, world, n_elems)
     if not args.no_sgd:
         out["decode_sgd"] = run_decode_sgd(args, run, sp, world, layers)
+        out["decode_adam"] = run_decode_sgd(args, run, sp, world, layers, adam=True)
     return out, run
 
 
-def run_decode_sgd(args, run, sp, world, layers):
-    """The decode fused with one momentum-SGD step (adacomp_decode_sgd_group) on the
-    last timed step's messages: weights and momentum read and written once (16 B per
-    element) instead of a dense sum plus a separate optimiser pass."""
-    ac, ct = run.ac, run.ct
+def run_decode_sgd(args, run, sp, world, layers, adam=False):
+    """The decode fused with one optimiser step on the last timed step's messages:
+    momentum SGD (adacomp_decode_sgd_group: weights and momentum read and written
+    once, 16 B per element) or Adam (adacomp_decode_adam_group: weights and both
+    moments, 24 B per element), instead of a dense sum plus a separate optimiser pass."""
+    ct = run.ct
     numels = [l.numel for l in layers]
-    w_buf, w_views = _flat_views(numels, torch.float32, run.dev)
-    v_buf, v_views = _flat_views(numels, torch.float32, run.dev)
-    w_buf.normal_()
+    bufs = [_flat_views(numels, torch.float32, run.dev) for _ in range(3 if adam else 2)]
+    bufs[0][0].normal_()
     VP = ct.c_void_p
-    c_w = [(VP * len(g))(*[w_views[i].data_ptr() for i in g]) for g in run.gidx]
-    c_v = [(VP * len(g))(*[v_views[i].data_ptr() for i in g]) for g in run.gidx]
+    ptrs = [[(VP * len(g))(*[views[i].data_ptr() for i in g]) for g in run.gidx] for _, views in bufs]
     stream = torch.cuda.current_stream()
+    f = ct.c_float
+    lr, b1, b2, eps, t = 1e-3, 0.9, 0.999, 1e-8, 10
 
     def once():
         for gi, h in enumerate(run.h):
-            st = run.L.adacomp_decode_sgd_group(h.ptr, run.c_dec_msgs[gi], run.last_lens[gi], run.K, c_w[gi], c_v[gi],
-                                                ct.c_float(1e-3), ct.c_float(0.9), ct.c_float(1.0 / run.K),
-                                                run.dec_ws[gi].data_ptr(), run.dec_ws[gi].numel(), sp)
+            if adam:
+                st = run.L.adacomp_decode_adam_group(
+                    h.ptr, run.c_dec_msgs[gi], run.last_lens[gi], run.K, ptrs[0][gi], ptrs[1][gi], ptrs[2][gi],
+                    f(lr), f(b1), f(b2), f(eps), f(1 - b1 ** t), f(1 - b2 ** t), f(1.0 / run.K),
+                    run.dec_ws[gi].data_ptr(), run.dec_ws[gi].numel(), sp)
+            else:
+                st = run.L.adacomp_decode_sgd_group(h.ptr, run.c_dec_msgs[gi], run.last_lens[gi], run.K, ptrs[0][gi],
+                                                    ptrs[1][gi], f(lr), f(0.9), f(1.0 / run.K),
+                                                    run.dec_ws[gi].data_ptr(), run.dec_ws[gi].numel(), sp)
             if st:
-                raise RuntimeError(f"adacomp_decode_sgd_group: {st}")
+                raise RuntimeError(f"fused decode: {st}")
 
     for _ in range(3):
         once()
@@ -594,14 +602,17 @@ def run_decode_sgd(args, run, sp, world, layers):
             break
     for gi, h in enumerate(run.h):
         if run.ac.adacomp_decode_status(h, run.dec_ws[gi]) != run.ac.OK:
-            raise RuntimeError("the fused decode + SGD step rejected a message")
+            raise RuntimeError("the fused decode rejected a message")
     ms = max_over_ranks(sorted(reps)[len(reps) // 2], world)
     msg_bytes = sum(sum(a) for a in run.last_lens)
     bins = sum(-(-l.numel // l.bin_len) for l in layers) * run.K
-    algo = 16 * sum(numels) + msg_bytes + 2 * bins
-    del w_buf, v_buf
+    algo = (24 if adam else 16) * sum(numels) + msg_bytes + 2 * bins
+    del bufs
+    peak, _ = measured_hbm_gbs()
     return {"ms_per_decode": ms, "algorithmic_bytes": algo, "achieved_gbs": algo / (ms * 1e-3) / 1e9,
-            "optimizer": "momentum SGD, lr 1e-3, mu 0.9, grad_scale 1/K"}
+            "frac": algo / (ms * 1e-3) / 1e9 / peak,
+            "optimizer": ("Adam, lr 1e-3, betas (0.9, 0.999), eps 1e-8, step 10, grad_scale 1/K" if adam
+                          else "momentum SGD, lr 1e-3, mu 0.9, grad_scale 1/K")}
 
 
 def run_lazy(args, run, sp, world, n_elems):

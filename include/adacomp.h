@@ -170,7 +170,7 @@ adacomp_status adacomp_compress_group(adacomp_layer_t h, float* const* residue,
  * data-parallel training (abstract; summary paragraph); the plain sum is this
  * library's reading, and the caller zeroes dense for a fresh sum.
  *   msgs       host array of K device pointers, each a message of this layer
- *              starting on a 4-byte boundary
+ *              starting on a 16-byte boundary
  *   msg_bytes  host array of K lengths in bytes, the length of each message as
  *              received (messages are variable-length: "AdaComp (Adaptive Residual
  *              Gradient Compression)", Claims > Limitation
@@ -188,8 +188,8 @@ adacomp_status adacomp_compress_group(adacomp_layer_t h, float* const* residue,
  * count exceeds its bin's length, the length is exactly 8 + 2B + w * (sum of the
  * counts), and within every bin the code offsets rise strictly and stay below the
  * bin's length (a message gives each element at most one code). Errors:
- * INVALID_ARG (K outside 1..256, NULL pointers), ALIGNMENT (dense not 16-byte or a
- * message not 4-byte aligned), WORKSPACE, CUDA.
+ * INVALID_ARG (K outside 1..256, NULL pointers), ALIGNMENT (dense or a message not
+ * 16-byte aligned), WORKSPACE, CUDA.
  */
 adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs,
                                          const uint64_t* msg_bytes, int32_t K, float* dense,
@@ -262,6 +262,33 @@ adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* ms
                                         int32_t K, float* const* weights, float* const* momentum, float lr,
                                         float mu, float grad_scale, void* ws, size_t ws_bytes,
                                         cudaStream_t stream);
+
+/* Decode fused with one Adam step, the other optimiser the learners use
+ * ("AdaComp (Adaptive Residual Gradient Compression)", Claims > Application
+ * #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers; the update rule is
+ * not on the pages and is read as Kingma and Ba's Adam with the bias corrections
+ * written out). For each element j of each layer, with s_j the learners' codes summed
+ * from zero exactly as adacomp_decode_accumulate sums them (learner order, fp32):
+ *     g   = fl32(grad_scale * s_j)
+ *     m_j = fl32( fl32(beta1 * m_j) + fl32(fl32(1 - beta1) * g) )
+ *     v_j = fl32( fl32(beta2 * v_j) + fl32(fl32(1 - beta2) * fl32(g * g)) )
+ *     w_j = fl32( w_j - fl32( lr * fl32( fl32(m_j / bias_correction1) /
+ *                                        fl32( sqrt(fl32(v_j / bias_correction2)) + eps ) ) ) )
+ * (IEEE fp32, correctly rounded division and square root, no fused multiply-add).
+ * bias_correction1 = 1 - beta1^t and bias_correction2 = 1 - beta2^t for step t are
+ * the caller's (both > 0; ADACOMP_ERR_INVALID_ARG otherwise). weights, m and v are
+ * fp32[n] per layer, in/out, 16-byte aligned. The gradient lives only in the tile
+ * being updated. Same messages, lengths, workspace and error reporting as
+ * adacomp_decode_accumulate (a rejected message contributes nothing). */
+adacomp_status adacomp_decode_adam(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                   int32_t K, float* weights, float* m, float* v, float lr, float beta1,
+                                   float beta2, float eps, float bias_correction1, float bias_correction2,
+                                   float grad_scale, void* ws, size_t ws_bytes, cudaStream_t stream);
+adacomp_status adacomp_decode_adam_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                         int32_t K, float* const* weights, float* const* m, float* const* v,
+                                         float lr, float beta1, float beta2, float eps, float bias_correction1,
+                                         float bias_correction2, float grad_scale, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream);
 
 /* Selection rule. ADACOMP_RULE_ADACOMP (the default) sends an element when
  * G != 0 and |fl32(G + dW)| >= g_max of its bin ("AdaComp (Adaptive Residual

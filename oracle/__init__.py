@@ -55,6 +55,8 @@ class Oracle:
         lib.adacomp_oracle_decode_accumulate.restype = ctypes.c_int
         f32 = ctypes.c_float
         lib.adacomp_oracle_decode_sgd.argtypes = [i64, i32, vp, vp, i32, vp, vp, f32, f32, f32]
+        lib.adacomp_oracle_decode_adam.argtypes = [i64, i32, vp, vp, i32, vp, vp, vp] + [f32] * 7
+        lib.adacomp_oracle_decode_adam.restype = ctypes.c_int
         lib.adacomp_oracle_decode_sgd.restype = ctypes.c_int
         self.lib = lib
 
@@ -162,3 +164,18 @@ def decode_sgd(n: int, bin_len: int, msgs, w: np.ndarray, v: np.ndarray, lr: flo
     assert w.dtype == np.float32 and v.dtype == np.float32 and w.size == n and v.size == n
     bufs, ptrs, ln = _msg_arrays(msgs, lens)
     return lib.adacomp_oracle_decode_sgd(n, bin_len, ptrs, ln, len(bufs), _ptr(w), _ptr(v), lr, mu, scale)
+
+
+def decode_adam(n: int, bin_len: int, msgs, w: np.ndarray, m: np.ndarray, v: np.ndarray, lr: float,
+                beta1: float, beta2: float, eps: float, bc1: float, bc2: float, scale: float = 1.0, lib=None,
+                lens=None) -> int:
+    """Decodes the messages into a zero gradient and applies one Adam step to ``w``,
+    ``m`` and ``v`` (fp32, in place); bc1 and bc2 are the step's bias corrections
+    1 - beta1^t and 1 - beta2^t. A rejected message adds nothing. Returns the
+    oracle status."""
+    lib = lib or _load()
+    for a in (w, m, v):
+        assert a.dtype == np.float32 and a.size == n and a.flags.c_contiguous
+    bufs, ptrs, ln = _msg_arrays(msgs, lens)
+    return lib.adacomp_oracle_decode_adam(n, bin_len, ptrs, ln, len(bufs), _ptr(w), _ptr(m), _ptr(v), lr, beta1,
+                                          beta2, eps, bc1, bc2, scale)

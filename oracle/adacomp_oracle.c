@@ -322,3 +322,51 @@ int adacomp_oracle_decode_sgd(int64_t n, int32_t L, const uint8_t *const *msgs, 
     free(g);
     return rc;
 }
+
+/*
+ * Decode K messages into the aggregated gradient (a zero-filled fp32 buffer,
+ * learners in order, exactly as adacomp_oracle_decode_accumulate, a rejected message
+ * adding nothing) and apply one Adam step to weights w, first moment m and second
+ * moment v (Adam is the other optimiser of the entry's Claims > Application
+ * #r629-conv-40x-and-fc-lstm-200x-compression-across-optimizers; the pages give no
+ * rule, so it is read as Kingma and Ba's Adam with the bias corrections written
+ * out, each operation an fp32 operation rounded once, no fused multiply-add):
+ *     g  = fl32(scale * sum)
+ *     m  = fl32( fl32(beta1 * m) + fl32(fl32(1 - beta1) * g) )
+ *     v  = fl32( fl32(beta2 * v) + fl32(fl32(1 - beta2) * fl32(g * g)) )
+ *     mh = fl32(m / bc1);   vh = fl32(v / bc2)
+ *     w  = fl32( w - fl32( lr * fl32( mh / fl32(sqrt(vh) + eps) ) ) )
+ * bc1 = 1 - beta1^t and bc2 = 1 - beta2^t (step t's bias corrections) are given by
+ * the caller. Returns ORACLE_ERR_BAD_MESSAGE when a message was rejected (the step
+ * is still applied with the others).
+ */
+int adacomp_oracle_decode_adam(int64_t n, int32_t L, const uint8_t *const *msgs, const uint64_t *lens, int32_t K,
+                               float *w, float *m, float *v, float lr, float beta1, float beta2, float eps,
+                               float bc1, float bc2, float scale)
+{
+    if (n < 1 || !w || !m || !v) return ORACLE_ERR_ARG;
+    float *sum = (float *)calloc((size_t)n, sizeof(float));
+    if (!sum) return ORACLE_ERR_ARG;
+    int rc = adacomp_oracle_decode_accumulate(n, L, msgs, lens, K, sum, NULL);
+    if (rc != ORACLE_OK && rc != ORACLE_ERR_BAD_MESSAGE) { free(sum); return rc; }
+    float one_minus_b1 = 1.0f - beta1;
+    float one_minus_b2 = 1.0f - beta2;
+    for (int64_t j = 0; j < n; ++j) {
+        float g = scale * sum[j];
+        float m_keep = beta1 * m[j];
+        float m_add = one_minus_b1 * g;
+        m[j] = m_keep + m_add;
+        float g2 = g * g;
+        float v_keep = beta2 * v[j];
+        float v_add = one_minus_b2 * g2;
+        v[j] = v_keep + v_add;
+        float m_hat = m[j] / bc1;
+        float v_hat = v[j] / bc2;
+        float denom = sqrtf(v_hat) + eps;
+        float ratio = m_hat / denom;
+        float delta = lr * ratio;
+        w[j] = w[j] - delta;
+    }
+    free(sum);
+    return rc;
+}

@@ -63,6 +63,8 @@ def lib() -> ctypes.CDLL:
         f32 = ctypes.c_float
         L.adacomp_decode_sgd.argtypes = [vp, P(vp), P(u64), i32, vp, vp, f32, f32, f32, vp, sz, vp]
         L.adacomp_decode_sgd_group.argtypes = [vp, P(vp), P(u64), i32, P(vp), P(vp), f32, f32, f32, vp, sz, vp]
+        L.adacomp_decode_adam.argtypes = [vp, P(vp), P(u64), i32, vp, vp, vp] + [f32] * 7 + [vp, sz, vp]
+        L.adacomp_decode_adam_group.argtypes = [vp, P(vp), P(u64), i32, P(vp), P(vp), P(vp)] + [f32] * 7 + [vp, sz, vp]
         L.adacomp_materialize.argtypes = [vp, vp, vp, sz, vp]
         L.adacomp_materialize_group.argtypes = [vp, P(vp), vp, sz, vp]
         L.adacomp_free.argtypes = [vp]
@@ -75,7 +77,7 @@ def lib() -> ctypes.CDLL:
                      "adacomp_set_timeout_ns", "adacomp_set_timing_events",
                      "adacomp_set_fault_injection", "adacomp_set_lazy_fixup", "adacomp_set_selection_rule",
                      "adacomp_materialize", "adacomp_decode_sgd", "adacomp_decode_sgd_group",
-                     "adacomp_materialize_group"):
+                     "adacomp_decode_adam", "adacomp_decode_adam_group", "adacomp_materialize_group"):
             getattr(L, name).restype = ctypes.c_int
         _lib = L
     return _lib
@@ -238,6 +240,32 @@ def adacomp_decode_sgd_group(h: Handle, msgs, msg_bytes, weights, momentum, lr: 
     _check(lib().adacomp_decode_sgd_group(h.ptr, arr, lens, K, VP(*[_ptr(w) for w in weights]),
                                           VP(*[_ptr(v) for v in momentum]), lr, mu, grad_scale, _ptr(ws),
                                           _nbytes(ws), _stream(stream)), "adacomp_decode_sgd_group")
+
+
+def adacomp_decode_adam(h: Handle, msgs, msg_bytes, weights, m, v, lr: float, beta1: float, beta2: float,
+                        eps: float, bias_correction1: float, bias_correction2: float, ws, grad_scale: float = 1.0,
+                        stream=None):
+    K = len(msgs)
+    arr = (ctypes.c_void_p * K)(*[_ptr(x) for x in msgs])
+    _check(lib().adacomp_decode_adam(h.ptr, arr, _lengths(msg_bytes, K), K, _ptr(weights), _ptr(m), _ptr(v), lr,
+                                     beta1, beta2, eps, bias_correction1, bias_correction2, grad_scale, _ptr(ws),
+                                     _nbytes(ws), _stream(stream)), "adacomp_decode_adam")
+
+
+def adacomp_decode_adam_group(h: Handle, msgs, msg_bytes, weights, m, v, lr: float, beta1: float, beta2: float,
+                              eps: float, bias_correction1: float, bias_correction2: float, ws,
+                              grad_scale: float = 1.0, stream=None):
+    """msgs, msg_bytes: per layer a list of K messages and their lengths (layer-major);
+    weights, m, v: one buffer per layer."""
+    L = h.num_layers
+    K = len(msgs[0])
+    arr = (ctypes.c_void_p * (L * K))(*[_ptr(x) for layer in msgs for x in layer])
+    lens = _lengths([b for layer in msg_bytes for b in layer], L * K)
+    VP = ctypes.c_void_p * L
+    _check(lib().adacomp_decode_adam_group(h.ptr, arr, lens, K, VP(*[_ptr(x) for x in weights]),
+                                           VP(*[_ptr(x) for x in m]), VP(*[_ptr(x) for x in v]), lr, beta1, beta2,
+                                           eps, bias_correction1, bias_correction2, grad_scale, _ptr(ws),
+                                           _nbytes(ws), _stream(stream)), "adacomp_decode_adam_group")
 
 
 def adacomp_set_selection_rule(h: Handle, rule: int):

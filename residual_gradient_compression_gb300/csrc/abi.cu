@@ -183,12 +183,21 @@ adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* d
 }  // extern "C"
 
 namespace {
-// Shared by the plain decode (mom == nullptr) and the fused momentum-SGD decode.
+// The optimiser step fused with a decode call (none for the plain sum).
+struct OptArgs {
+    int opt = adacomp::kOptNone;
+    float* const* mom = nullptr;   // momentum (SGD) or first moment (Adam), per layer
+    float* const* mom2 = nullptr;  // second moment (Adam), per layer
+    float lr = 0.0f, mu = 0.0f, scale = 1.0f;
+    float beta1 = 0.0f, beta2 = 0.0f, eps = 0.0f, bc1 = 1.0f, bc2 = 1.0f;
+};
+
+// Shared by the plain decode and the decodes fused with an optimiser step.
 adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes, int32_t K,
-                            float* const* dense, float* const* mom, float lr, float mu, float scale, void* ws,
-                            size_t ws_bytes, cudaStream_t stream)
+                            float* const* dense, const OptArgs& o, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (!h || !msgs || !msg_bytes || !dense || !ws) return ADACOMP_ERR_INVALID_ARG;
+    if ((o.opt != adacomp::kOptNone && !o.mom) || (o.opt == adacomp::kOptAdam && !o.mom2)) return ADACOMP_ERR_INVALID_ARG;
     const int64_t L = (int64_t)h->layers.size();
     if (K < 1 || K > ADACOMP_MAX_LEARNERS || (int64_t)K * L > adacomp::kMaxDecodePairs)
         return ADACOMP_ERR_INVALID_ARG;
@@ -201,7 +210,15 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, const ui
     std::memset(p, 0, sizeof *p);
     fill_group(h, g);
     p->K = K;
-    p->sgd = mom ? 1 : 0;
+    p->opt = o.opt;
+    p->lr = o.lr;
+    p->mu = o.mu;
+    p->scale = o.scale;
+    p->beta1 = o.beta1;
+    p->beta2 = o.beta2;
+    p->eps = o.eps;
+    p->bc1 = o.bc1;
+    p->bc2 = o.bc2;
     uint32_t vt = 0;  // validation tasks per learner, layer by layer
     for (int64_t l = 0; l < L; ++l) {
         const KLayer& k = h->layers[(size_t)l];
@@ -210,19 +227,20 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, const ui
         vt += (k.num_tiles + per - 1) / per;
     }
     p->val_begin[L] = vt;
-    p->lr = lr;
-    p->mu = mu;
-    p->scale = scale;
     adacomp_status st = ADACOMP_OK;
     for (int64_t l = 0; l < L && st == ADACOMP_OK; ++l) {
-        if (!dense[l] || (mom && !mom[l])) st = ADACOMP_ERR_INVALID_ARG;
-        else if (!aligned(dense[l], 16) || (mom && !aligned(mom[l], 16))) st = ADACOMP_ERR_ALIGNMENT;
+        float* m1 = o.mom ? o.mom[l] : nullptr;
+        float* m2 = o.mom2 ? o.mom2[l] : nullptr;
+        if (!dense[l] || (o.mom && !m1) || (o.mom2 && !m2)) st = ADACOMP_ERR_INVALID_ARG;
+        else if (!aligned(dense[l], 16) || (m1 && !aligned(m1, 16)) || (m2 && !aligned(m2, 16)))
+            st = ADACOMP_ERR_ALIGNMENT;
         p->dense[l] = dense[l];
-        if (mom) p->mom[l] = mom[l];
+        p->mom[l] = m1;
+        p->mom2[l] = m2;
         for (int32_t k = 0; k < K && st == ADACOMP_OK; ++k) {
             const void* m = msgs[l * K + k];
             if (!m) st = ADACOMP_ERR_INVALID_ARG;
-            else if (!aligned(m, 4)) st = ADACOMP_ERR_ALIGNMENT;
+            else if (!aligned(m, 16)) st = ADACOMP_ERR_ALIGNMENT;
             p->msg[l * K + k] = static_cast<const uint8_t*>(m);
             p->len[l * K + k] = msg_bytes[l * K + k];
         }
@@ -240,7 +258,7 @@ adacomp_status adacomp_decode_accumulate_group(adacomp_layer_t h, const void* co
                                                int32_t K, float* const* dense, void* ws, size_t ws_bytes,
                                                cudaStream_t stream)
 {
-    return decode_group(h, msgs, msg_bytes, K, dense, nullptr, 0.0f, 0.0f, 1.0f, ws, ws_bytes, stream);
+    return decode_group(h, msgs, msg_bytes, K, dense, OptArgs(), ws, ws_bytes, stream);
 }
 
 adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
@@ -248,7 +266,13 @@ adacomp_status adacomp_decode_sgd_group(adacomp_layer_t h, const void* const* ms
                                         float grad_scale, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (!momentum) return ADACOMP_ERR_INVALID_ARG;
-    return decode_group(h, msgs, msg_bytes, K, weights, momentum, lr, mu, grad_scale, ws, ws_bytes, stream);
+    OptArgs o;
+    o.opt = adacomp::kOptSGD;
+    o.mom = momentum;
+    o.lr = lr;
+    o.mu = mu;
+    o.scale = grad_scale;
+    return decode_group(h, msgs, msg_bytes, K, weights, o, ws, ws_bytes, stream);
 }
 
 adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes, int32_t K,
@@ -259,6 +283,39 @@ adacomp_status adacomp_decode_sgd(adacomp_layer_t h, const void* const* msgs, co
     if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
     return adacomp_decode_sgd_group(h, msgs, msg_bytes, K, &weights, &momentum, lr, mu, grad_scale, ws, ws_bytes,
                                     stream);
+}
+
+adacomp_status adacomp_decode_adam_group(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,
+                                         int32_t K, float* const* weights, float* const* m, float* const* v, float lr,
+                                         float beta1, float beta2, float eps, float bias_correction1,
+                                         float bias_correction2, float grad_scale, void* ws, size_t ws_bytes,
+                                         cudaStream_t stream)
+{
+    if (!m || !v) return ADACOMP_ERR_INVALID_ARG;
+    if (!(bias_correction1 > 0.0f) || !(bias_correction2 > 0.0f)) return ADACOMP_ERR_INVALID_ARG;
+    OptArgs o;
+    o.opt = adacomp::kOptAdam;
+    o.mom = m;
+    o.mom2 = v;
+    o.lr = lr;
+    o.scale = grad_scale;
+    o.beta1 = beta1;
+    o.beta2 = beta2;
+    o.eps = eps;
+    o.bc1 = bias_correction1;
+    o.bc2 = bias_correction2;
+    return decode_group(h, msgs, msg_bytes, K, weights, o, ws, ws_bytes, stream);
+}
+
+adacomp_status adacomp_decode_adam(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes, int32_t K,
+                                   float* weights, float* m, float* v, float lr, float beta1, float beta2, float eps,
+                                   float bias_correction1, float bias_correction2, float grad_scale, void* ws,
+                                   size_t ws_bytes, cudaStream_t stream)
+{
+    if (!h) return ADACOMP_ERR_INVALID_ARG;
+    if (h->layers.size() != 1) return ADACOMP_ERR_INVALID_ARG;
+    return adacomp_decode_adam_group(h, msgs, msg_bytes, K, &weights, &m, &v, lr, beta1, beta2, eps,
+                                     bias_correction1, bias_correction2, grad_scale, ws, ws_bytes, stream);
 }
 
 adacomp_status adacomp_decode_accumulate(adacomp_layer_t h, const void* const* msgs, const uint64_t* msg_bytes,

@@ -189,16 +189,22 @@ __host__ __device__ inline uint32_t val_tiles_per_task(uint32_t bins_per_tile)
 
 constexpr uint32_t kErrTimeout = 1;
 
+// Optimiser step fused with the decode (DecodeParams::opt).
+constexpr int kOptNone = 0;  // plain sum into dense
+constexpr int kOptSGD = 1;   // momentum SGD on weights (dense) and momentum (mom)
+constexpr int kOptAdam = 2;  // Adam on weights (dense), first moment (mom) and second moment (mom2)
+
 struct DecodeParams {
     const uint8_t* msg[kMaxDecodePairs];  // [layer * K + k]
     uint64_t len[kMaxDecodePairs];        // the messages' lengths in bytes, same order
-    float* dense[kMaxGroup];              // the dense sum, or the weights when sgd != 0
-    float* mom[kMaxGroup];                // momentum buffers (sgd != 0)
+    float* dense[kMaxGroup];              // the dense sum, or the weights when opt != kOptNone
+    float* mom[kMaxGroup];                // momentum (SGD) or first moment (Adam)
+    float* mom2[kMaxGroup];               // second moment (Adam)
     uint32_t val_begin[kMaxGroup + 1];    // validation tasks per learner: layer l's are [val_begin[l], val_begin[l + 1])
     int32_t K;
-    int32_t sgd;                          // fused momentum-SGD step instead of a plain sum
-    float lr, mu, scale;                  // w -= lr * v, v = mu * v + scale * g
-    int32_t pad;
+    int32_t opt;                          // kOptNone, kOptSGD or kOptAdam
+    float lr, mu, scale;                  // SGD: w -= lr * v, v = mu * v + scale * g (Adam uses lr and scale)
+    float beta1, beta2, eps, bc1, bc2;    // Adam: decay rates, epsilon, the step's bias corrections
 };
 
 // ---------------------------------------------------------------- host-side launchers

@@ -447,84 +447,88 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
 }
 
 // ---------------------------------------------------------------- finalise and scan
-// One CTA per layer: s from the layer's exact sum (fp64, rounded once to fp32),
-// the header {s, B}, the result area, and the exclusive prefix of the layer's tile
-// code totals (which are left zero for the next call).
-//
-// The scan takes the layer's tiles in passes of kFinPer * 1024: thread tid loads
-// tiles pass_base + i * 1024 + tid for i < kFinPer (coalesced, every load of the
-// pass issued before the first is used), the warps scan each of the kFinPer rows
-// with shuffles, one warp scans the row-by-warp totals in row order, and the
-// offsets go back coalesced. A pass costs one global round trip and two barriers.
+// Grid: x = chunk of kFinThreads tiles, y = layer (CTAs past a layer's last chunk
+// exit at once). The CTA of chunk c sums the totals of the layer's tiles before the
+// chunk itself (coalesced, kFinUnroll loads per thread in flight; the repeated reads
+// are small and hit L2), scans its own chunk with one block scan, and writes the
+// chunk's exclusive tile code offsets. The CTA of the layer's last chunk also forms s
+// from the layer's exact sum (fp64, rounded once to fp32), the header {s, B} and the
+// result area. The tile totals are left for the emitting kernel, which clears them.
 constexpr int kFinThreads = 1024;
 constexpr int kFinWarps = kFinThreads / 32;
-constexpr int kFinPer = 8;
+constexpr int kFinUnroll = 8;
 
 __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __grid_constant__ KGroup g,
                                                                      uint8_t* __restrict__ ws)
 {
     __shared__ unsigned long long tmp[256];
     __shared__ unsigned long long words[kSumWords];
-    __shared__ uint32_t wt[kFinPer][kFinWarps];              // per row and warp: the warp's total
-    __shared__ unsigned long long wx[kFinPer][kFinWarps];    // per row and warp: exclusive offset
-    __shared__ unsigned long long carry_s;
-    const int l = blockIdx.x, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    __shared__ unsigned long long red[kFinWarps];
+    __shared__ uint32_t wt[kFinWarps];
+    const int l = blockIdx.y, tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const KLayer& ly = g.layer[l];
+    const uint32_t nt = ly.num_tiles;
+    const uint32_t c0 = blockIdx.x * kFinThreads;  // the chunk's first tile (layer-relative)
+    if (c0 >= nt) return;
+    const bool last_chunk = c0 + kFinThreads >= nt;
     LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(l));
     const uint32_t T = g.total_tiles;
-    uint32_t* tot = reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T)) + ly.tile_begin;
+    const uint32_t* tot = reinterpret_cast<const uint32_t*>(ws + sl_tot_offset(g.num_layers, T)) + ly.tile_begin;
     uint64_t* excl = reinterpret_cast<uint64_t*>(ws + sl_excl_offset(g.num_layers)) + ly.tile_begin;
-    if (tid < kSumWords) words[tid] = 0ull;
-    if (tid < 256) tmp[tid] = lw->acc[tid];
-    if (tid == 0) carry_s = 0ull;
-
-    const uint32_t nt = ly.num_tiles;
-    for (uint32_t base = 0; base < nt; base += kFinPer * kFinThreads) {
-        uint32_t v[kFinPer], inc[kFinPer];
+    if (last_chunk) {
+        if (tid < kSumWords) words[tid] = 0ull;
+        if (tid < 256) tmp[tid] = lw->acc[tid];
+    }
+    // the codes of the tiles before the chunk
+    unsigned long long before = 0;
+    for (uint32_t i0 = 0; i0 < c0; i0 += kFinUnroll * kFinThreads) {
+        uint32_t v[kFinUnroll];
 #pragma unroll
-        for (int i = 0; i < kFinPer; ++i) {
-            const uint32_t j = base + i * kFinThreads + tid;
-            v[i] = j < nt ? tot[j] : 0u;
+        for (int u = 0; u < kFinUnroll; ++u) {
+            const uint32_t i = i0 + u * kFinThreads + tid;
+            v[u] = i < c0 ? tot[i] : 0u;
         }
 #pragma unroll
-        for (int i = 0; i < kFinPer; ++i) {
-            inc[i] = v[i];
+        for (int u = 0; u < kFinUnroll; ++u) before += v[u];
+    }
+    // the chunk's own tiles: one per thread, scanned
+    const uint32_t j = c0 + tid;
+    const uint32_t mine = j < nt ? tot[j] : 0u;
+    // a warp's share: at most 32 x (tiles before the chunk / 1024) x 4072 codes < 2^32 for
+    // layers below 2^38 elements
+    before = __reduce_add_sync(kFull, (uint32_t)before);
+    uint32_t incl = mine;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, inc[i], o);
-                if (lane >= o) inc[i] += y;
-            }
-            if (lane == 31) wt[i][warp] = inc[i];
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    if (lane == 31) wt[warp] = incl;
+    if (lane == 0) red[warp] = before;
+    __syncthreads();
+    if (warp == 0) {
+        unsigned long long b = red[lane];  // the warps' shares of the codes before the chunk
+#pragma unroll
+        for (int o = 16; o; o >>= 1) b += __shfl_xor_sync(kFull, b, o);
+        const uint32_t x = wt[lane];
+        uint32_t sx = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, sx, o);
+            if (lane >= o) sx += y;
         }
-        __syncthreads();  // also orders carry_s of the previous pass
-        if (warp == 0) {
-            unsigned long long c = carry_s;
-#pragma unroll
-            for (int i = 0; i < kFinPer; ++i) {
-                const uint32_t x = wt[i][lane];
-                uint32_t s = x;  // a row holds at most 1024 tiles of < 2^14 codes: 32 bits suffice
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const uint32_t y = __shfl_up_sync(kFull, s, o);
-                    if (lane >= o) s += y;
-                }
-                wx[i][lane] = c + (s - x);
-                c += __shfl_sync(kFull, s, 31);
-            }
-            if (lane == 0) carry_s = c;
-        }
-        __syncthreads();
-#pragma unroll
-        for (int i = 0; i < kFinPer; ++i) {
-            const uint32_t j = base + i * kFinThreads + tid;
-            if (j < nt) {
-                excl[j] = wx[i][warp] + (inc[i] - v[i]);
-                if (v[i]) tot[j] = 0u;
-            }
-        }
+        __syncwarp();
+        red[lane] = b + (sx - x);  // exclusive offset of warp `lane`'s first tile
     }
     __syncthreads();
-    const unsigned long long nnz = carry_s;
+    const unsigned long long off = red[warp] + (incl - mine);
+    if (j < nt) excl[j] = off;
+    if (!last_chunk) return;
+    // the last chunk's last tile ends the layer
+    __shared__ unsigned long long nnz_s;
+    if (j == nt - 1) nnz_s = off + mine;
+    __syncthreads();
+    const unsigned long long nnz = nnz_s;
     if (warp == 0) {
         const double Ssum = exact_sum_warp(tmp, words, lane);
         if (lane == 0) {
@@ -560,7 +564,9 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
 //         128-byte line), then the code ((element - its bin's first element) << 1) |
 //         (G < 0) and the residue fl32(G - sign(G) s);
 //   otherwise the list entries carry the sign bit, and only the codes are written.
-// A tile with more than kListCap sent elements is listed and walked in rounds.
+// A tile with more than kListCap sent elements is listed and walked in rounds. The
+// tiles' code totals (read by the finalising kernel) are cleared here for the next
+// call.
 constexpr int kEmitThreads = 256;
 constexpr int kEmitWarps = kEmitThreads / 32;
 constexpr int kListCap = 1024;
@@ -612,10 +618,12 @@ __global__ void __launch_bounds__(kEmitThreads, 5) slice_emit_kernel(const __gri
     int l_cached = -1;
     float s = 0.0f;
     uint32_t status = 0;
+    uint32_t* tile_tot = reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T));
     for (; q < T; q += NW) {
         const uint32_t t = T - 1u - q;
         const EmitIn in = cur;
         if (q + NW < T) cur = emit_load<kFix>(ws, g.num_layers, T, T - 1u - (q + NW), lane);
+        if (lane == 0) tile_tot[t] = 0u;  // the tile totals start the next call at zero
         const int l = layer_of_tile(tb, g.num_layers, t);
         const KLayer& ly = g.layer[l];
         if (l != l_cached) {
@@ -786,7 +794,10 @@ cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t strea
     kern<<<grid, kThreads, P.total, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
-    slice_finalize_kernel<<<g.num_layers, kFinThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    uint32_t max_tiles = 0;  // the largest layer sets the chunks per layer
+    for (int l = 0; l < g.num_layers; ++l) max_tiles = g.layer[l].num_tiles > max_tiles ? g.layer[l].num_tiles : max_tiles;
+    const dim3 fgrid((max_tiles + kFinThreads - 1) / kFinThreads, (unsigned)g.num_layers);
+    slice_finalize_kernel<<<fgrid, kFinThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // persistent: as many CTAs as are resident at once, each warp a run of tiles
     void (*ekern)(KGroup, uint8_t*) = g.lazy ? slice_emit_kernel<false> : slice_emit_kernel<true>;

@@ -62,58 +62,125 @@ __device__ __forceinline__ uint64_t* tile_offsets(uint8_t* ws, int k, uint32_t T
     return reinterpret_cast<uint64_t*>(ws + kDecodeFixed + (size_t)k * decode_per_learner(T));
 }
 
-// One warp per (learner k, tile t), every task in flight at once: the message must
-// be at least 8 + 2B bytes long (else nothing of it is read), the header's B must
-// equal the layer's B, and no count may exceed its bin's length; otherwise the tile
-// sum is kBadOffset.
+// Layer of validation task u (tasks of a learner are numbered across the layers).
+__device__ __forceinline__ int layer_of_task(const uint32_t* vb, int num_layers, uint32_t u)
+{
+    int lo = 0, hi = num_layers - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (vb[mid] <= u) lo = mid;
+        else hi = mid - 1;
+    }
+    return lo;
+}
+
+// A run of whole tiles of one layer holding at most kValBins bins (or one tile when
+// a tile holds more): the unit of work of the counting and validation kernels.
+struct Run {
+    int layer;
+    uint32_t t0, ntiles;  // first tile (global index) and tiles
+    uint32_t b0, nb;      // first bin (in the layer) and bins
+};
+
+__device__ __forceinline__ Run run_of(const KGroup& g, const uint32_t* vb, uint32_t u)
+{
+    Run R;
+    R.layer = layer_of_task(vb, g.num_layers, u);
+    const KLayer& ly = g.layer[R.layer];
+    const uint32_t tpt = val_tiles_per_task(ly.bins_per_tile);
+    const uint32_t i0 = (u - vb[R.layer]) * tpt;  // first tile within the layer
+    R.t0 = ly.tile_begin + i0;
+    R.ntiles = min(tpt, ly.num_tiles - i0);
+    R.b0 = i0 * ly.bins_per_tile;
+    R.nb = (uint32_t)min((uint64_t)R.ntiles * ly.bins_per_tile, (uint64_t)(ly.nbins - R.b0));
+    return R;
+}
+
+// One warp per (learner k, run): the message must be at least 8 + 2B bytes long
+// (else nothing of it is read), the header's B must equal the layer's B, and no
+// count may exceed its bin's length; otherwise every tile sum of the run is
+// kBadOffset. Lanes take the run's bins (all loads issued at once, coalesced) and
+// add them into per-tile sums in shared memory.
 __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_constant__ KGroup g,
                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
-    __shared__ uint32_t tb[kMaxGroup];
-    for (int e = threadIdx.x; e < g.num_layers; e += kDecThreads) tb[e] = g.layer[e].tile_begin;
+    __shared__ uint32_t vb[kMaxGroup + 1];
+    __shared__ uint32_t sums_s[kDecThreads / 32][kValBins];
+    for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) vb[e] = p.val_begin[e];
     if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<uint32_t*>(ws)[2] = 0u;  // scan blocks done
     __syncthreads();
     const uint32_t T = g.total_tiles;
     const int K = p.K;
     const int lane = threadIdx.x & 31;
+    const uint32_t per_learner = vb[g.num_layers];
     const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
-    if (task >= (uint64_t)K * T) return;
-    const int k = (int)(task / T);
-    const uint32_t t = (uint32_t)(task - (uint64_t)k * T);
-    const int l = layer_of(tb, g.num_layers, t);
+    if (task >= (uint64_t)K * per_learner) return;
+    const int k = (int)(task / per_learner);
+    const Run R = run_of(g, vb, (uint32_t)(task - (uint64_t)k * per_learner));
+    const int l = R.layer;
     const KLayer& ly = g.layer[l];
+    uint64_t* out = tile_offsets(ws, k, T) + R.t0;
     const uint8_t* msg = p.msg[l * K + k];
     if (p.len[l * K + k] < 8ull + 2ull * ly.nbins) {  // too short for its header and counts: read nothing
-        if (lane == 0) tile_offsets(ws, k, T)[t] = kBadOffset;
+        for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = kBadOffset;
         return;
     }
-    const uint32_t first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
-    const int bins = (int)min(ly.bins_per_tile, ly.nbins - first_bin);
     const uint32_t hdr_b = *reinterpret_cast<const uint32_t*>(msg + 4);
-    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + first_bin;
+    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + R.b0;
     const uint32_t last_len = (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
     bool ok = true;
-    uint32_t sum = 0;
-    for (int b = lane; b < bins; b += 32) {
-        const uint32_t c = cnt[b];
-        ok = ok && c <= (first_bin + b == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len);
-        sum += c;
+    if (R.ntiles == 1) {  // one tile (possibly of more than kValBins bins): a warp sum
+        uint32_t sum = 0;
+        for (uint32_t b = lane; b < R.nb; b += 32) {
+            const uint32_t c = cnt[b];
+            ok = ok && c <= (R.b0 + b == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len);
+            sum += c;
+        }
+        ok = __all_sync(kFull, ok) && hdr_b == ly.nbins;
+        sum = __reduce_add_sync(kFull, sum);
+        if (lane == 0) out[0] = ok ? (uint64_t)sum : kBadOffset;
+        return;
+    }
+    uint32_t* sums = sums_s[threadIdx.x >> 5];
+    for (uint32_t i = lane; i < R.ntiles; i += 32) sums[i] = 0u;
+    __syncwarp();
+    uint32_t c[kValBins / 32];
+#pragma unroll
+    for (int i = 0; i < (int)(kValBins / 32); ++i) {
+        const uint32_t b = i * 32 + lane;
+        c[i] = b < R.nb ? cnt[b] : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < (int)(kValBins / 32); ++i) {
+        const uint32_t b = i * 32 + lane;
+        if (b < R.nb) {
+            ok = ok && c[i] <= (R.b0 + b == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len);
+            if (c[i]) atomicAdd(&sums[b / ly.bins_per_tile], c[i]);
+        }
     }
     ok = __all_sync(kFull, ok) && hdr_b == ly.nbins;
-    sum = __reduce_add_sync(kFull, sum);
-    if (lane == 0) tile_offsets(ws, k, T)[t] = ok ? (uint64_t)sum : kBadOffset;
+    __syncwarp();
+    for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = ok ? (uint64_t)sums[i] : kBadOffset;
 }
 
-// One CTA per (layer, learner): the tile sums become exclusive offsets, in place,
-// each thread taking a contiguous run of tiles. A message with any bad tile, or
-// whose length is not 8 + 2B + w * (its code count), is marked bad as a whole; the
-// message's code count goes to the workspace.
-__global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__ KGroup g,
-                                                         const __grid_constant__ DecodeParams p, uint8_t* ws)
+// One CTA per (layer, learner): the tile sums become exclusive offsets, in place. A
+// message with any bad tile, or whose length is not 8 + 2B + w * (its code count),
+// is marked bad as a whole; the message's code count goes to the workspace.
+// The tiles are taken in passes of kScanPer * 1024: thread tid loads tiles
+// pass_base + i * 1024 + tid for i < kScanPer (coalesced, every load of the pass
+// issued before the first is used), the warps scan each row with shuffles and one
+// warp scans the row-by-warp totals in row order. A first sweep finds the total and
+// whether any tile is bad, the second writes the offsets.
+constexpr int kScanThreads = 1024;
+constexpr int kScanWarps = kScanThreads / 32;
+constexpr int kScanPer = 8;
+
+__global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_constant__ KGroup g,
+                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
-    __shared__ unsigned long long wsum[32];
-    __shared__ uint32_t bad_s;
-    __shared__ unsigned long long total_s;
+    __shared__ unsigned long long wt[kScanPer][kScanWarps];
+    __shared__ unsigned long long wx[kScanPer][kScanWarps];
+    __shared__ unsigned long long carry_s;
     const int K = p.K;
     const int l = blockIdx.x / K, k = blockIdx.x - (blockIdx.x / K) * K;
     const KLayer& ly = g.layer[l];
@@ -123,60 +190,72 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
         reinterpret_cast<uint32_t*>(ws)[0] = (uint32_t)K;
         reinterpret_cast<uint32_t*>(ws)[1] = (uint32_t)g.num_layers;
     }
-    if (tid == 0) bad_s = 0u;
+    if (tid == 0) carry_s = 0ull;
     __syncthreads();
     const uint32_t nt = ly.num_tiles;
-    const uint32_t per = (nt + 1023) / 1024;
-    const uint32_t i0 = min(nt, tid * per), i1 = min(nt, i0 + per);
-    unsigned long long mine = 0;
-    bool ok = true;
-#pragma unroll 4
-    for (uint32_t i = i0; i < i1; ++i) {
-        const uint64_t v = off[i];
-        ok = ok && v != kBadOffset;
-        mine += v == kBadOffset ? 0ull : v;
-    }
-    if (!ok) bad_s = 1u;
-    unsigned long long incl = mine;
+    bool bad = false;
+    for (uint32_t base = 0; base < nt; base += kScanPer * kScanThreads) {
+        uint64_t v[kScanPer], inc[kScanPer];
+        bool mine_bad = false;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const unsigned long long y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    if (lane == 31) wsum[warp] = incl;
-    __syncthreads();
-    if (warp == 0) {
-        const unsigned long long v = wsum[lane];
-        unsigned long long x = v;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const unsigned long long y = __shfl_up_sync(kFull, x, o);
-            if (lane >= o) x += y;
+        for (int i = 0; i < kScanPer; ++i) {
+            const uint32_t j = base + i * kScanThreads + tid;
+            v[i] = j < nt ? off[j] : 0ull;
+            mine_bad = mine_bad || v[i] == kBadOffset;
         }
-        wsum[lane] = x - v;
-        if (lane == 31) total_s = x;
+        if (__syncthreads_or(mine_bad)) {  // a bad tile: the whole message is rejected
+            bad = true;
+            break;
+        }
+#pragma unroll
+        for (int i = 0; i < kScanPer; ++i) {
+            inc[i] = v[i];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const unsigned long long y = __shfl_up_sync(kFull, inc[i], o);
+                if (lane >= o) inc[i] += y;
+            }
+            if (lane == 31) wt[i][warp] = inc[i];
+        }
+        __syncthreads();
+        if (warp == 0) {
+            unsigned long long c = carry_s;
+#pragma unroll
+            for (int i = 0; i < kScanPer; ++i) {
+                const unsigned long long x = wt[i][lane];
+                unsigned long long sx = x;
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(kFull, sx, o);
+                    if (lane >= o) sx += y;
+                }
+                wx[i][lane] = c + (sx - x);
+                c += __shfl_sync(kFull, sx, 31);
+            }
+            if (lane == 0) carry_s = c;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < kScanPer; ++i) {
+            const uint32_t j = base + i * kScanThreads + tid;
+            if (j < nt) off[j] = wx[i][warp] + (inc[i] - v[i]);
+        }
     }
     __syncthreads();
+    const unsigned long long total = carry_s;
     // the message must end exactly after its last code
-    const bool bad = bad_s != 0u ||
-                     p.len[l * K + k] != 8ull + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * total_s;
-    unsigned long long run = wsum[warp] + incl - mine;
-    for (uint32_t i = i0; i < i1; ++i) {
-        const uint64_t v = off[i];
-        off[i] = bad ? kBadOffset : run;
-        run += v == kBadOffset ? 0ull : v;
-    }
+    bad = bad || p.len[l * K + k] != 8ull + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * total;
     __shared__ uint32_t last_s;
     if (tid == 0) {
         ws[16 + l * K + k] = bad ? 1 : 0;
-        layer_codes(ws)[(size_t)l * K + k] = bad ? 0ull : total_s;
+        layer_codes(ws)[(size_t)l * K + k] = bad ? 0ull : total;
         __threadfence();
         last_s = atomicAdd(reinterpret_cast<uint32_t*>(ws) + 2, 1u) == gridDim.x - 1u ? 1u : 0u;
     }
     __syncthreads();
     if (last_s) {  // every message is scanned: decide which layers are summed in place
         __threadfence();
-        for (int e = tid; e < g.num_layers; e += 1024) {
+        for (int e = tid; e < g.num_layers; e += kScanThreads) {
             const volatile unsigned long long* c = layer_codes(ws) + (size_t)e * K;
             unsigned long long sum = 0;
             for (int j = 0; j < K; ++j) sum += c[j];
@@ -185,20 +264,78 @@ __global__ void __launch_bounds__(1024) tile_scan_kernel(const __grid_constant__
     }
 }
 
-// One warp per (learner k, run of whole tiles of one layer with at most kValBins
-// bins, or one tile) of a message not already rejected: within every bin the code
-// offsets must rise strictly (a message gives each element at most one code) and
-// stay below the bin's length; otherwise the message is rejected as a whole, before
-// anything is added. The run's counts are loaded at once (lanes over bins), turned
-// into per-bin code starts in shared memory, and the codes are checked in batches of
-// kValBatch per lane, every load of a batch issued first.
+// One warp per (learner k, run) of a message not already rejected: within every bin
+// the code offsets must rise strictly (a message gives each element at most one code)
+// and stay below the bin's length; otherwise the message is rejected as a whole,
+// before anything is added. The run's counts are loaded at once (lanes over bins) and
+// the first code of every non-empty bin is marked in a per-warp bitmap over the run's
+// codes; the codes are then read coalesced, kValBatch per lane at a time, and each is
+// compared with its neighbour (a shuffle), unless it starts a bin, and with its bin's
+// length (L_T, or the layer's last, shorter bin). A run with more codes than the
+// bitmap holds, or a tile of more than kValBins bins, is checked bin by bin instead.
 constexpr int kValBatch = 8;
+constexpr uint32_t kValBitmapWords = 256;  // codes of a run checked through the bitmap: up to 8192
+
+// The codes [0, total) at `codes` (kCpv codes per 16 bytes: 8 of 16 bits or 16 of 8
+// bits), read as 16-byte vectors from the boundary at or before the first (the
+// message starts on a 16-byte boundary, so no read leaves the 16-byte blocks its
+// bytes lie in). Code j must be below its bin's length (last_len from code last_start
+// on) and, unless bit j of bm marks it as its bin's first, above code j - 1.
+template <int kCpv>
+__device__ __forceinline__ bool check_codes(const uint8_t* codes, uint32_t total, const uint32_t* bm,
+                                            uint32_t last_start, uint32_t last_len, uint32_t bin_len, int lane)
+{
+    constexpr int kBits = 128 / kCpv;  // bits per code: 8 or 16
+    const uintptr_t a = reinterpret_cast<uintptr_t>(codes);
+    const uint4* va = reinterpret_cast<const uint4*>(a & ~(uintptr_t)15);
+    const int delta = (int)((a & 15) / (16 / kCpv));  // codes before the first in its vector
+    const uint32_t nvec = (total + delta + kCpv - 1) / kCpv;
+    bool ok = true;
+    uint32_t carry = 0;  // the last code of the previous batch's last vector
+    for (uint32_t v0 = 0; v0 < nvec; v0 += 32 * kValBatch) {
+        uint4 vec[kValBatch];
+#pragma unroll
+        for (int q = 0; q < kValBatch; ++q) {
+            const uint32_t v = v0 + q * 32 + lane;
+            vec[q] = v < nvec ? va[v] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int q = 0; q < kValBatch; ++q) {
+            const uint32_t v = v0 + q * 32 + lane;
+            const uint32_t wd[4] = {vec[q].x, vec[q].y, vec[q].z, vec[q].w};
+            const uint32_t last_code = (wd[3] >> (32 - kBits)) & ((1u << kBits) - 1u);
+            uint32_t before = __shfl_up_sync(kFull, last_code, 1);
+            const uint32_t next_carry = __shfl_sync(kFull, last_code, 31);
+            if (lane == 0) before = carry;
+            carry = next_carry;
+            if (v >= nvec) continue;
+            const int j0 = (int)(v * kCpv) - delta;  // code index of the vector's first slot
+            // the bin-start bits of codes j0 .. j0 + kCpv - 1
+            const int w0 = j0 >> 5;
+            const uint32_t lo_w = w0 >= 0 ? bm[w0] : 0u;
+            const uint32_t hi_w = (w0 + 1) * 32 < (int)total ? bm[w0 + 1] : 0u;
+            const uint64_t bits = (((uint64_t)hi_w << 32) | lo_w) >> (j0 & 31);
+#pragma unroll
+            for (int i = 0; i < kCpv; ++i) {
+                const int j = j0 + i;
+                const uint32_t c = (wd[i / (32 / kBits)] >> (kBits * (i % (32 / kBits)))) & ((1u << kBits) - 1u);
+                if (j >= 0 && j < (int)total) {
+                    const uint32_t o = c >> 1;
+                    const bool starts = (bits >> i) & 1u;
+                    ok = ok && o < ((uint32_t)j >= last_start ? last_len : bin_len) && (starts || o > (before >> 1));
+                }
+                before = c;
+            }
+        }
+    }
+    return ok;
+}
 
 __global__ void __launch_bounds__(kDecThreads) validate_kernel(const __grid_constant__ KGroup g,
                                                                const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
     __shared__ uint32_t vb[kMaxGroup + 1];
-    __shared__ uint32_t pre_s[kDecThreads / 32][kValBins + 2];
+    __shared__ uint32_t bm_s[kDecThreads / 32][kValBitmapWords];
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) vb[e] = p.val_begin[e];
     __syncthreads();
     const int K = p.K;
@@ -207,30 +344,27 @@ __global__ void __launch_bounds__(kDecThreads) validate_kernel(const __grid_cons
     const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
     if (task >= (uint64_t)K * per_learner) return;
     const int k = (int)(task / per_learner);
-    const uint32_t u = (uint32_t)(task - (uint64_t)k * per_learner);
-    int l = 0, hi = g.num_layers - 1;  // the layer whose tasks hold u
-    while (l < hi) {
-        const int mid = (l + hi + 1) >> 1;
-        if (vb[mid] <= u) l = mid;
-        else hi = mid - 1;
-    }
+    const Run R = run_of(g, vb, (uint32_t)(task - (uint64_t)k * per_learner));
+    const int l = R.layer;
     if (ws[16 + l * K + k]) return;  // rejected already: nothing more of it is read
     const KLayer& ly = g.layer[l];
-    const uint32_t tpt = val_tiles_per_task(ly.bins_per_tile);
-    const uint32_t t0 = ly.tile_begin + (u - vb[l]) * tpt;                       // first tile
-    const uint32_t b0 = (t0 - ly.tile_begin) * ly.bins_per_tile;                 // first bin
-    const uint32_t nb = (uint32_t)min((uint64_t)tpt * ly.bins_per_tile, (uint64_t)(ly.nbins - b0));
     const uint8_t* msg = p.msg[l * K + k];
-    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + b0;
-    const uint64_t off = tile_offsets(ws, k, g.total_tiles)[t0];
-    uint32_t* pre = pre_s[threadIdx.x >> 5];
-    uint32_t total = 0;
-    if (nb <= kValBins) {
-        uint32_t c[kValBins / 32];
+    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + R.b0;
+    const uint64_t off = tile_offsets(ws, k, g.total_tiles)[R.t0];
+    const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * off;
+    const bool wide = ly.code_bytes == 2;
+    const uint32_t last_len = (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
+    const bool has_last = R.b0 + R.nb == ly.nbins;  // the run holds the layer's last bin
+    uint32_t* bm = bm_s[threadIdx.x >> 5];
+    bool ok = true;
+    uint32_t total = 0, last_start = 0xffffffffu;
+    bool fast = R.nb <= kValBins;
+    if (fast) {
+        uint32_t c[kValBins / 32], ex[kValBins / 32];
 #pragma unroll
         for (int i = 0; i < (int)(kValBins / 32); ++i) {
             const uint32_t b = i * 32 + lane;
-            c[i] = b < nb ? cnt[b] : 0u;
+            c[i] = b < R.nb ? cnt[b] : 0u;
         }
 #pragma unroll
         for (int i = 0; i < (int)(kValBins / 32); ++i) {
@@ -240,71 +374,48 @@ __global__ void __launch_bounds__(kDecThreads) validate_kernel(const __grid_cons
                 const uint32_t y = __shfl_up_sync(kFull, incl, o);
                 if (lane >= o) incl += y;
             }
-            pre[i * 32 + lane] = total + incl - c[i];
+            ex[i] = total + incl - c[i];
             total += __shfl_sync(kFull, incl, 31);
         }
-    } else {
-        // a tile with more bins than the shared prefix holds (bins shorter than 32):
-        // checked bin by bin from the counts, one lane per bin
-        uint64_t start = off;
-        for (uint32_t c0 = 0; c0 < nb; c0 += 32) {
+        fast = total <= 32 * kValBitmapWords;
+        if (fast) {
+            for (uint32_t w = lane; w < (total + 31) / 32; w += 32) bm[w] = 0u;
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < (int)(kValBins / 32); ++i) {
+                const uint32_t b = i * 32 + lane;
+                if (b < R.nb && c[i]) atomicOr(&bm[ex[i] >> 5], 1u << (ex[i] & 31));
+                if (has_last && b == R.nb - 1) last_start = ex[i];
+            }
+            last_start = __reduce_min_sync(kFull, last_start);
+            __syncwarp();
+            ok = wide ? check_codes<8>(codes, total, bm, last_start, last_len, (uint32_t)ly.bin_len, lane)
+                      : check_codes<16>(codes, total, bm, last_start, last_len, (uint32_t)ly.bin_len, lane);
+        }
+    }
+    if (!fast) {
+        // bin by bin, one lane per bin, each lane walking its bin's codes
+        uint64_t start = 0;
+        for (uint32_t c0 = 0; c0 < R.nb; c0 += 32) {
             const uint32_t b = c0 + lane;
-            const uint32_t c = b < nb ? cnt[b] : 0u;
+            const uint32_t c = b < R.nb ? cnt[b] : 0u;
             uint32_t incl = c;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t y = __shfl_up_sync(kFull, incl, o);
                 if (lane >= o) incl += y;
             }
-            bool ok = true;
-            if (b < nb) {
-                const uint32_t len = (b0 + b == ly.nbins - 1) ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len)
-                                                              : (uint32_t)ly.bin_len;
-                const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * (start + incl - c);
-                uint32_t prev = 0;
+            if (b < R.nb) {
+                const uint32_t len = (R.b0 + b == ly.nbins - 1) ? last_len : (uint32_t)ly.bin_len;
+                const uint64_t j0 = start + incl - c;
+                uint32_t prev_o = 0;
                 for (uint32_t i = 0; i < c; ++i) {
-                    const uint32_t o = (ly.code_bytes == 1 ? codes[i] : reinterpret_cast<const uint16_t*>(codes)[i]) >> 1;
-                    ok = ok && o < len && (i == 0 || o > prev);
-                    prev = o;
+                    const uint32_t o = (wide ? reinterpret_cast<const uint16_t*>(codes)[j0 + i] : codes[j0 + i]) >> 1;
+                    ok = ok && o < len && (i == 0 || o > prev_o);
+                    prev_o = o;
                 }
             }
-            if (!__all_sync(kFull, ok)) {
-                if (lane == 0) ws[16 + l * K + k] = 1;
-                return;
-            }
             start += __shfl_sync(kFull, incl, 31);
-        }
-        return;
-    }
-    if (lane == 0) pre[nb] = total;
-    __syncwarp();
-    const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * off;
-    const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len;
-    bool ok = true;
-    for (uint32_t j0 = 0; j0 < total; j0 += 32 * kValBatch) {
-        uint32_t cur[kValBatch], prv[kValBatch];
-#pragma unroll
-        for (int q = 0; q < kValBatch; ++q) {
-            const uint32_t j = j0 + q * 32 + lane;
-            cur[q] = prv[q] = 0u;
-            if (j < total) {
-                cur[q] = ly.code_bytes == 1 ? codes[j] : reinterpret_cast<const uint16_t*>(codes)[j];
-                if (j) prv[q] = ly.code_bytes == 1 ? codes[j - 1] : reinterpret_cast<const uint16_t*>(codes)[j - 1];
-            }
-        }
-#pragma unroll
-        for (int q = 0; q < kValBatch; ++q) {
-            const uint32_t j = j0 + q * 32 + lane;
-            if (j >= total) continue;
-            int lo = 0, hb = (int)nb - 1;  // last bin whose start is <= j
-            while (lo < hb) {
-                const int mid = (lo + hb + 1) >> 1;
-                if (pre[mid] <= j) lo = mid;
-                else hb = mid - 1;
-            }
-            const uint32_t len = (b0 + lo == ly.nbins - 1) ? (uint32_t)last_len : (uint32_t)ly.bin_len;
-            const uint32_t o = cur[q] >> 1;
-            ok = ok && o < len && (j == pre[lo] || o > (prv[q] >> 1));
         }
     }
     if (!__all_sync(kFull, ok) && lane == 0) ws[16 + l * K + k] = 1;
@@ -326,20 +437,21 @@ __global__ void __launch_bounds__(kDecThreads) validate_kernel(const __grid_cons
 // bin of its first code by binary search and walks forward.
 constexpr int kAccStages = 2;
 
-// One tile-sized fp32 array of a stage; a stage holds one (the dense tile) or three
-// (the summed gradient g, the weights w and the momentum v, for the fused SGD step).
+// One tile-sized fp32 array: a stage holds the dense tile (plain sum) or the
+// gradient sum (a decode fused with an optimiser step, whose weights and state are
+// read from and written to global memory directly).
 __host__ __device__ inline uint32_t acc_array_bytes(uint32_t tile_cap) { return ((tile_cap + 8) * 4 + 127) & ~127u; }
-__host__ __device__ inline uint32_t acc_stage_bytes(uint32_t tile_cap, bool sgd = false)
+__host__ __device__ inline uint32_t acc_stage_bytes(uint32_t tile_cap, int opt = kOptNone)
 {
-    return (sgd ? 3u : 1u) * acc_array_bytes(tile_cap);
+    return acc_array_bytes(tile_cap);
 }
 __host__ __device__ inline uint32_t acc_pre_bytes(uint32_t max_bins)
 {
     return (uint32_t)(kDecThreads / 32) * ((max_bins + 8) / 8 + 2) * 4;
 }
-__host__ __device__ inline uint32_t acc_smem_bytes(uint32_t tile_cap, uint32_t max_bins, bool sgd = false)
+__host__ __device__ inline uint32_t acc_smem_bytes(uint32_t tile_cap, uint32_t max_bins, int opt = kOptNone)
 {
-    return kAccStages * acc_stage_bytes(tile_cap, sgd) + ((acc_pre_bytes(max_bins) + 127) & ~127u) + 128;
+    return kAccStages * acc_stage_bytes(tile_cap, opt) + ((acc_pre_bytes(max_bins) + 127) & ~127u) + 128;
 }
 
 struct AccTile {
@@ -359,11 +471,11 @@ struct LayerIndex {
     uint8_t ok[kMaxDecodePairs];
 };
 
-__device__ __forceinline__ void load_index(LayerIndex& X, const KGroup& g, uint8_t* ws, int K, bool sgd)
+__device__ __forceinline__ void load_index(LayerIndex& X, const KGroup& g, uint8_t* ws, int K, bool opt)
 {
     for (int e = threadIdx.x; e < g.num_layers; e += blockDim.x) {
         X.tb[e] = g.layer[e].tile_begin;
-        X.sparse[e] = !sgd && sparse_flags(ws)[e] != 0 ? 1 : 0;
+        X.sparse[e] = !opt && sparse_flags(ws)[e] != 0 ? 1 : 0;
     }
     for (int e = threadIdx.x; e < g.num_layers * K; e += blockDim.x) X.ok[e] = ws[16 + e] == 0 ? 1 : 0;
 }
@@ -381,12 +493,10 @@ __device__ __forceinline__ AccTile acc_tile(const KGroup& g, const LayerIndex& X
     return A;
 }
 
-// Thread 0: start tile t's dense slice into a stage. The copy ends at the 16-byte
-// boundary at or after the tile unless that lies past the array, in which case the
-// last few elements are loaded with plain loads.
-// (For the fused SGD step the weights and the momentum are loaded into the stage's
-// second and third arrays; the first, the gradient sum, is zeroed by the threads.)
-template <bool kSGD>
+// Thread 0: start tile t's dense slice into a stage (plain sum only). The copy ends
+// at the 16-byte boundary at or after the tile unless that lies past the array, in
+// which case the last few elements are loaded with plain loads.
+template <int kOpt>
 __device__ void acc_issue(const KGroup& g, const LayerIndex& X, const DecodeParams& p, uint32_t t, float* st,
                           uint32_t arr_floats, uint64_t* bar)
 {
@@ -399,20 +509,11 @@ __device__ void acc_issue(const KGroup& g, const LayerIndex& X, const DecodePara
     int64_t a1 = (A.te + 3) & ~(int64_t)3;
     if (a1 > n) a1 = A.te & ~(int64_t)3;
     const uint32_t bytes = a1 > A.a0 ? (uint32_t)(a1 - A.a0) * 4u : 0u;
-    const int na = kSGD ? 2 : 1;
-    for (int a = 0; a < na; ++a) {
-        const float* src = kSGD ? (a ? p.mom[A.layer] : p.dense[A.layer]) : p.dense[A.layer];
-        float* dst = st + (kSGD ? (size_t)(a + 1) * arr_floats : 0);
-        for (int64_t j = max(a1, A.ts); j < A.te; ++j) dst[j - A.a0] = src[j];
-    }
+    const float* src = p.dense[A.layer];
+    for (int64_t j = max(a1, A.ts); j < A.te; ++j) st[j - A.a0] = src[j];
     if (a1 < A.te) ptx::fence_proxy_async_smem();
-    ptx::mbar_arrive_expect_tx(bar, bytes * na);
-    if (bytes) {
-        for (int a = 0; a < na; ++a) {
-            const float* src = kSGD ? (a ? p.mom[A.layer] : p.dense[A.layer]) : p.dense[A.layer];
-            ptx::bulk_g2s(st + (kSGD ? (size_t)(a + 1) * arr_floats : 0), src + A.a0, bytes, bar);
-        }
-    }
+    ptx::mbar_arrive_expect_tx(bar, bytes);
+    if (bytes) ptx::bulk_g2s(st, src + A.a0, bytes, bar);
 }
 
 __device__ __forceinline__ bool acc_wait(uint64_t* bar, uint32_t parity, uint64_t timeout_ns)
@@ -538,18 +639,18 @@ __device__ __forceinline__ void acc_walk(const KLayer& ly, const AccTile& A, con
 }
 
 // Warp `warp` owns one bin of tile A (tiles of at most 8 bins): every learner's
-// codes for that bin, learners kb .. kb + 31 per round. acc_bin_prep: lane k
-// fetches learner kb + k's tile offset, scale and the counts of the tile's bins up
-// to this one, every load issued at once (independent of the dense tile, so it runs
-// while that is loading). acc_bin_apply: the codes of kAccWindow learners at a time
-// are loaded at once (lane i holding code i of each) and added in learner order.
+// codes for that bin, learners kb .. kb + 31 per round. acc_bin_prep: lane k fetches
+// learner kb + k's code count in the bin, its first code and its scale (the tile
+// offset and the counts of the tile's bins up to this one, every load issued at
+// once; none depends on the dense tile, so this runs while that is loading).
+// acc_bin_apply: the codes of kAccWindow learners at a time are loaded at once (lane
+// i holding code i of each) and added in learner order.
 constexpr int kAccWindow = 16;
 
 struct BinPrep {
-    unsigned long long start;  // index of the learner's first code for this bin
-    const uint8_t* codes;      // the learner's code array
-    uint32_t c;                // its codes in this bin
-    float s;                   // its scale
+    const uint8_t* codes;  // the learner's first code for this bin
+    uint32_t c;            // its codes in this bin
+    float s;               // its scale
 };
 
 __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile& A, const DecodeParams& p,
@@ -557,7 +658,6 @@ __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile&
                                                 int bin, int kb, int lane)
 {
     BinPrep P;
-    P.start = 0;
     P.codes = nullptr;
     P.c = 0;
     P.s = 0.0f;
@@ -578,8 +678,7 @@ __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile&
             mine += b == bin ? c[b] : 0u;
         }
         P.c = mine;
-        P.start = off + before;
-        P.codes = msg + 8 + 2ull * ly.nbins;
+        P.codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * (off + before);
     }
     return P;
 }
@@ -587,10 +686,9 @@ __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile&
 __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A, int K, int bin, int kb,
                                               const BinPrep& P, float* sd, int lane)
 {
-    const int L = ly.bin_len;
-    const int64_t last_len = ly.n - (int64_t)(ly.nbins - 1) * L;
-    const uint32_t len = (uint32_t)((A.first_bin + bin == ly.nbins - 1) ? last_len : L);
-    float* x0 = sd + (int64_t)bin * L;
+    const uint32_t len = (A.first_bin + bin == ly.nbins - 1)
+                             ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len) : (uint32_t)ly.bin_len;
+    float* x0 = sd + (int64_t)bin * ly.bin_len;
     const bool wide = ly.code_bytes == 2;
     const int kn = min(32, K - kb);
     for (int k0 = 0; k0 < kn; k0 += kAccWindow) {
@@ -599,11 +697,9 @@ __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A
         for (int w = 0; w < kAccWindow; ++w) {
             const int kk = min(k0 + w, kn - 1);
             const uint32_t ck = __shfl_sync(kFull, P.c, kk);
-            const unsigned long long st = __shfl_sync(kFull, P.start, kk);
             const uint8_t* cp = reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)P.codes, kk));
             cw[w] = 0xffffffffu;
-            if (k0 + w < kn && (uint32_t)lane < ck)
-                cw[w] = wide ? reinterpret_cast<const uint16_t*>(cp)[st + lane] : cp[st + lane];
+            if (k0 + w < kn && (uint32_t)lane < ck) cw[w] = wide ? reinterpret_cast<const uint16_t*>(cp)[lane] : cp[lane];
         }
 #pragma unroll
         for (int w = 0; w < kAccWindow; ++w) {
@@ -616,11 +712,10 @@ __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A
                 if (o < len) x0[o] = __fadd_rn(x0[o], (cw[w] & 1u) ? -s : s);  // always in range once validated
             }
             if (ck > 32u) {  // more codes than lanes in this bin: the rest, in rounds
-                const unsigned long long st = __shfl_sync(kFull, P.start, kk);
                 const uint8_t* cp =
                     reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)P.codes, kk));
                 for (uint32_t i = 32 + lane; i < ck; i += 32) {
-                    const uint32_t code = wide ? reinterpret_cast<const uint16_t*>(cp)[st + i] : cp[st + i];
+                    const uint32_t code = wide ? reinterpret_cast<const uint16_t*>(cp)[i] : cp[i];
                     const uint32_t o = code >> 1;
                     if (o < len) x0[o] = __fadd_rn(x0[o], (code & 1u) ? -s : s);
                 }
@@ -630,15 +725,86 @@ __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A
     }
 }
 
-// kSGD: the learners' codes are summed into a zeroed gradient tile g, and one
-// momentum-SGD step is applied to the weights w and momentum v while the tile is in
-// shared memory: v = fl32(fl32(mu * v) + fl32(scale * g)), w = fl32(w - fl32(lr * v)).
-template <bool kSGD>
-__global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_constant__ KGroup g,
+// One optimiser step over tile A's elements, the gradient sum in gs (element ts + x at
+// gs[x]): weights and state are read from and written to global memory directly, the
+// 16-byte-aligned interior four elements at a time, the (at most three) elements at
+// each end one at a time (neighbouring tiles share those 16-byte lines).
+template <int kOpt>
+__device__ __forceinline__ void opt_elem(const DecodeParams& p, float gsum, float& w, float& m, float& v)
+{
+    if constexpr (kOpt == kOptSGD) {
+        const float mv = __fadd_rn(__fmul_rn(p.mu, m), __fmul_rn(p.scale, gsum));
+        m = mv;
+        w = __fsub_rn(w, __fmul_rn(p.lr, mv));
+    } else {
+        const float gx = __fmul_rn(p.scale, gsum);
+        const float mm = __fadd_rn(__fmul_rn(p.beta1, m), __fmul_rn(__fsub_rn(1.0f, p.beta1), gx));
+        const float vv = __fadd_rn(__fmul_rn(p.beta2, v), __fmul_rn(__fsub_rn(1.0f, p.beta2), __fmul_rn(gx, gx)));
+        m = mm;
+        v = vv;
+        const float ratio = __fdiv_rn(__fdiv_rn(mm, p.bc1), __fadd_rn(__fsqrt_rn(__fdiv_rn(vv, p.bc2)), p.eps));
+        w = __fsub_rn(w, __fmul_rn(p.lr, ratio));
+    }
+}
+
+template <int kOpt>
+__device__ __forceinline__ void opt_tile(const DecodeParams& p, const AccTile& A, const float* gs, int tid)
+{
+    float* W = p.dense[A.layer];
+    float* M = p.mom[A.layer];
+    float* V = kOpt == kOptAdam ? p.mom2[A.layer] : nullptr;
+    const int64_t c0 = (A.ts + 3) & ~(int64_t)3, c1 = A.te & ~(int64_t)3;
+    if (c1 > c0) {
+        for (int64_t q = c0 / 4 + tid; q < c1 / 4; q += kDecThreads) {
+            float4 w4 = reinterpret_cast<const float4*>(W)[q];
+            float4 m4 = reinterpret_cast<const float4*>(M)[q];
+            float4 v4 = make_float4(0.f, 0.f, 0.f, 0.f);
+            if (kOpt == kOptAdam) v4 = reinterpret_cast<const float4*>(V)[q];
+            const float* g4 = gs + (4 * q - A.ts);
+            opt_elem<kOpt>(p, g4[0], w4.x, m4.x, v4.x);
+            opt_elem<kOpt>(p, g4[1], w4.y, m4.y, v4.y);
+            opt_elem<kOpt>(p, g4[2], w4.z, m4.z, v4.z);
+            opt_elem<kOpt>(p, g4[3], w4.w, m4.w, v4.w);
+            reinterpret_cast<float4*>(W)[q] = w4;
+            reinterpret_cast<float4*>(M)[q] = m4;
+            if (kOpt == kOptAdam) reinterpret_cast<float4*>(V)[q] = v4;
+        }
+        if (tid < 8) {  // the ends
+            const int64_t j = tid < 4 ? A.ts + tid : c1 + (tid - 4);
+            if ((tid < 4 && j < c0) || (tid >= 4 && j < A.te)) {
+                float w = W[j], m = M[j], v = kOpt == kOptAdam ? V[j] : 0.0f;
+                opt_elem<kOpt>(p, gs[j - A.ts], w, m, v);
+                W[j] = w;
+                M[j] = m;
+                if (kOpt == kOptAdam) V[j] = v;
+            }
+        }
+    } else {
+        for (int64_t j = A.ts + tid; j < A.te; j += kDecThreads) {
+            float w = W[j], m = M[j], v = kOpt == kOptAdam ? V[j] : 0.0f;
+            opt_elem<kOpt>(p, gs[j - A.ts], w, m, v);
+            W[j] = w;
+            M[j] = m;
+            if (kOpt == kOptAdam) V[j] = v;
+        }
+    }
+}
+
+// kOpt != kOptNone: the learners' codes are summed into a zeroed gradient tile g in
+// shared memory and one optimiser step is applied to the tile's elements (opt_tile):
+//   kOptSGD   v = fl32(fl32(mu * v) + fl32(scale * g)), w = fl32(w - fl32(lr * v));
+//   kOptAdam  g' = fl32(scale * g), m = fl32(fl32(b1 m) + fl32(fl32(1 - b1) g')),
+//             v = fl32(fl32(b2 v) + fl32(fl32(1 - b2) fl32(g' g'))),
+//             w = fl32(w - fl32(lr fl32(fl32(m / bc1) / fl32(sqrt(fl32(v / bc2)) + eps))))
+//             (correctly rounded division and square root).
+// Plain sum: the dense tile is staged (bulk copies in, bulk store out).
+template <int kOpt>
+__global__ void __launch_bounds__(kDecThreads, 5) accumulate_kernel(const __grid_constant__ KGroup g,
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
+    constexpr bool kFused = kOpt != kOptNone;
     extern __shared__ __align__(128) uint8_t smem[];
-    const uint32_t stage_bytes = acc_stage_bytes(g.tile_cap, kSGD);
+    const uint32_t stage_bytes = acc_stage_bytes(g.tile_cap, kOpt);
     const uint32_t arr_floats = acc_array_bytes(g.tile_cap) / 4;
     float* stage0 = reinterpret_cast<float*>(smem);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -651,7 +817,7 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     const int K = p.K;
     auto stage = [&](int i) { return stage0 + (size_t)(i % kAccStages) * (stage_bytes / 4); };
     __shared__ LayerIndex X;
-    load_index(X, g, ws, p.K, kSGD);
+    load_index(X, g, ws, p.K, kFused);
     __syncthreads();
     // The CTA's tiles are G0, G0 + GS, ...; tiles of layers summed in place (by the
     // sparse kernel) are jumped over a layer at a time.
@@ -664,11 +830,10 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
         }
         return T;
     };
-    // Tile window: t (processed now) and t1 (copied into the other stage at the start
-    // of this iteration, as soon as the bulk store of the tile that stage held has
-    // read it, so the copy has the whole iteration to land). (Three stages measured
-    // no faster for the plain sum, and the fused SGD step's three arrays per stage
-    // would then leave one CTA per SM.)
+    // Plain sum: tile window t (processed now) and t1 (copied into the other stage at
+    // the start of this iteration, as soon as the bulk store of the tile that stage held
+    // has read it, so the copy has the whole iteration to land). (Three stages measured
+    // no faster.)
     static_assert(kAccStages == 2, "the ring below holds one tile ahead");
     uint32_t t = next_tile(G0);
     uint32_t t1 = t < T ? next_tile(t + GS) : T;
@@ -676,7 +841,7 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     if (tid == 0) {
         for (int k = 0; k < kAccStages; ++k) ptx::mbar_init(&bar[k], 1);
         ptx::fence_mbar_init();
-        if (t < T) acc_issue<kSGD>(g, X, p, t, stage(0), arr_floats, &bar[0]);
+        if (!kFused && t < T) acc_issue<kOpt>(g, X, p, t, stage(0), arr_floats, &bar[0]);
     }
     __syncthreads();
 
@@ -684,21 +849,21 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
     int i = 0;
     for (; t < T; ++i) {
         float* st = stage(i);
-        if (tid == 0 && t1 < T) {
+        if (!kFused && tid == 0 && t1 < T) {
             ptx::bulk_wait_read0();  // the store of the tile stage i + 1 held has read it
-            acc_issue<kSGD>(g, X, p, t1, stage(i + 1), arr_floats, &bar[(i + 1) % kAccStages]);
+            acc_issue<kOpt>(g, X, p, t1, stage(i + 1), arr_floats, &bar[(i + 1) % kAccStages]);
         }
         const AccTile A = acc_tile(g, X, t);
         const KLayer& ly = g.layer[A.layer];
         const int l = A.layer;
         const int bpw = (A.bins + kDecThreads / 32 - 1) / (kDecThreads / 32);
         const int b0 = min(A.bins, warp * bpw), b1 = min(A.bins, b0 + bpw);
-        // the first learners' offsets and counts do not depend on the dense tile:
-        // fetch them while its copy is in flight
-        if constexpr (kSGD) {  // the gradient sum starts at zero (the array no copy targets)
+        if constexpr (kFused) {  // the gradient sum starts at zero
             float4* z = reinterpret_cast<float4*>(st);
             for (int64_t q = tid; q < (A.te - A.a0 + 3) / 4; q += kDecThreads) z[q] = make_float4(0.f, 0.f, 0.f, 0.f);
         }
+        // the first learners' offsets and counts do not depend on the dense tile:
+        // fetch them while its copy is in flight
         BinPrep bp;
         CodePrefetch cp0;
         uint64_t off0 = 0;
@@ -710,7 +875,10 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
             total0 = acc_prefix(A, p.msg[l * K], b0, b1, pre, &before0, lane);
             acc_fetch(ly, p.msg[l * K], off0, before0, total0, lane, cp0);
         }
-        if (!__syncthreads_and(acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u, g.timeout_ns))) {
+        if (kFused) {
+            __syncthreads();  // the zeroed gradient tile
+        } else if (!__syncthreads_and(acc_wait(&bar[i % kAccStages], (uint32_t)(i / kAccStages) & 1u,
+                                               g.timeout_ns))) {
             poisoned = true;
             break;
         }
@@ -732,45 +900,28 @@ __global__ void __launch_bounds__(kDecThreads) accumulate_kernel(const __grid_co
                 acc_walk_pf(ly, A, msg, off, before, total, b0, b1, sd, pre, lane, cp0, k == 0);
             }
         }
-
         __syncthreads();
-        if constexpr (kSGD) {  // the optimiser step on the tile
-            float* gs = st;
-            float* wv = st + arr_floats;
-            float* vv = st + 2 * (size_t)arr_floats;
-            for (int64_t x = (A.ts - A.a0) + tid; x < A.te - A.a0; x += kDecThreads) {
-                const float v = __fadd_rn(__fmul_rn(p.mu, vv[x]), __fmul_rn(p.scale, gs[x]));
-                vv[x] = v;
-                wv[x] = __fsub_rn(wv[x], __fmul_rn(p.lr, v));
-            }
-            __syncthreads();
-        }
-        // write back: ends by the threads, the aligned interior by one bulk store per array
-        const int64_t c0 = (A.ts + 3) & ~(int64_t)3, c1 = A.te & ~(int64_t)3;
-        const int na = kSGD ? 2 : 1;
-        for (int a = 0; a < na; ++a) {
-            float* dst = (kSGD && a) ? p.mom[l] : p.dense[l];
-            const float* src = st + (kSGD ? (size_t)(a + 1) * arr_floats : 0);
+        if constexpr (kFused) {
+            opt_tile<kOpt>(p, A, sd, tid);
+            __syncthreads();  // the gradient tile is zeroed again for the next tile
+        } else {
+            // write back: ends by the threads, the aligned interior by one bulk store
+            const int64_t c0 = (A.ts + 3) & ~(int64_t)3, c1 = A.te & ~(int64_t)3;
+            float* dst = p.dense[l];
             if (c1 > c0) {
                 if (tid < 8) {
                     const int64_t j = tid < 4 ? A.ts + tid : c1 + (tid - 4);
-                    if ((tid < 4 && j < c0) || (tid >= 4 && j < A.te)) dst[j] = src[j - A.a0];
+                    if ((tid < 4 && j < c0) || (tid >= 4 && j < A.te)) dst[j] = st[j - A.a0];
                 }
             } else {
-                for (int64_t j = A.ts + tid; j < A.te; j += kDecThreads) dst[j] = src[j - A.a0];
+                for (int64_t j = A.ts + tid; j < A.te; j += kDecThreads) dst[j] = st[j - A.a0];
             }
-        }
-        ptx::fence_proxy_async_smem();  // the threads' shared writes, before the bulk store reads them
-        __syncthreads();
-        if (tid == 0) {
-            if (c1 > c0) {
-                for (int a = 0; a < na; ++a) {
-                    float* dst = (kSGD && a) ? p.mom[l] : p.dense[l];
-                    const float* src = st + (kSGD ? (size_t)(a + 1) * arr_floats : 0);
-                    ptx::bulk_s2g(dst + c0, src + (c0 - A.a0), (uint32_t)(c1 - c0) * 4u);
-                }
+            ptx::fence_proxy_async_smem();  // the threads' shared writes, before the bulk store reads them
+            __syncthreads();
+            if (tid == 0) {
+                if (c1 > c0) ptx::bulk_s2g(dst + c0, st + (c0 - A.a0), (uint32_t)(c1 - c0) * 4u);
+                ptx::bulk_commit();
             }
-            ptx::bulk_commit();
         }
         t = t1;
         t1 = t1 < T ? next_tile(t1 + GS) : T;
@@ -840,7 +991,7 @@ __global__ void __launch_bounds__(kDecThreads) sparse_accumulate_kernel(const __
 
 struct DecDeviceInfo {
     int sms = 0;
-    uint32_t smem_set[2] = {0, 0};  // per accumulate kernel (plain sum, fused SGD)
+    uint32_t smem_set[3] = {0, 0, 0};  // per accumulate kernel (plain sum, fused SGD, fused Adam)
     uint32_t sparse_smem_set = 0;
 };
 DecDeviceInfo g_ddev[64];
@@ -859,27 +1010,28 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
         if (e != cudaSuccess) return e;
     }
     uint8_t* w = static_cast<uint8_t*>(ws);
-    const uint64_t tasks = (uint64_t)p.K * g.total_tiles;
+    const uint64_t vtasks = (uint64_t)p.K * p.val_begin[g.num_layers];  // (learner, run) tasks
     const uint64_t wpb = kDecThreads / 32;
-    tile_sums_kernel<<<(unsigned)((tasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
+    tile_sums_kernel<<<(unsigned)((vtasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    tile_scan_kernel<<<(unsigned)(g.num_layers * p.K), 1024, 0, stream>>>(g, p, w);
+    tile_scan_kernel<<<(unsigned)(g.num_layers * p.K), kScanThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const uint64_t vtasks = (uint64_t)p.K * p.val_begin[g.num_layers];
     validate_kernel<<<(unsigned)((vtasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const bool sgd = p.sgd != 0;
-    const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins, sgd);
-    void (*kern)(KGroup, DecodeParams, uint8_t*) = sgd ? accumulate_kernel<true> : accumulate_kernel<false>;
-    if (smem > di.smem_set[sgd]) {
+    const int opt = p.opt;
+    const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins, opt);
+    void (*kern)(KGroup, DecodeParams, uint8_t*) = opt == kOptAdam  ? accumulate_kernel<kOptAdam>
+                                                   : opt == kOptSGD ? accumulate_kernel<kOptSGD>
+                                                                    : accumulate_kernel<kOptNone>;
+    if (smem > di.smem_set[opt]) {
         // opted in whenever it grows: the kernel's static shared memory counts
         // towards the 48 KB available without the opt-in
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        di.smem_set[sgd] = smem;
+        di.smem_set[opt] = smem;
     }
     int occ = 0;
     e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kDecThreads, smem);
@@ -889,7 +1041,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
     kern<<<grid, kDecThreads, smem, stream>>>(g, p, w);
     e = cudaGetLastError();
-    if (e != cudaSuccess || sgd) return e;
+    if (e != cudaSuccess || opt != kOptNone) return e;
     // the layers summed in place (the kernel skips the others)
     const uint32_t sp_smem = (kDecThreads / 32) * ((uint32_t)g.max_bins + 2) * 4;
     if (sp_smem > di.sparse_smem_set) {

@@ -42,6 +42,11 @@ MUTANTS = {
                                    "if (off >= blen || off < prev) return 0;"),
     "length_unchecked": ("if (len != 8 + 2 * (uint64_t)B + (uint64_t)w * total) return 0;", "(void)total;"),
     "rejected_message_still_added": ("        if (!message_ok(n, L, msgs[k], lens[k])) continue;\n", ""),
+    "adam_beta1_swapped": ("float m_keep = beta1 * m[j];\n        float m_add = one_minus_b1 * g;",
+                           "float m_keep = one_minus_b1 * m[j];\n        float m_add = beta1 * g;"),
+    "adam_no_bias_correction": ("float m_hat = m[j] / bc1;", "float m_hat = m[j];"),
+    "adam_eps_inside_sqrt": ("float denom = sqrtf(v_hat) + eps;", "float denom = sqrtf(v_hat + eps);"),
+    "adam_v_from_g": ("float g2 = g * g;", "float g2 = g;"),
 }
 
 
@@ -76,6 +81,12 @@ def _golden_pins(lib):
     oracle.decode_sgd(case["n"], case["bin_len"], [hex_bytes(case["msg_hex"])], w, v, case["lr"], case["mu"],
                       case["scale"], lib=lib)
     assert np.array_equal(w, f32_array(case["expect_w"])) and np.array_equal(v, f32_array(case["expect_v"]))
+    case = load("hand_decode_adam")
+    w, m, v = f32_array(case["w_in"]), f32_array(case["m_in"]), f32_array(case["v_in"])
+    oracle.decode_adam(case["n"], case["bin_len"], [hex_bytes(h) for h in case["msgs_hex"]], w, m, v, case["lr"],
+                       case["beta1"], case["beta2"], case["eps"], case["bc1"], case["bc2"], case["scale"], lib=lib)
+    assert np.array_equal(w, f32_array(case["expect_w"])) and np.array_equal(m, f32_array(case["expect_m"]))
+    assert np.array_equal(v, f32_array(case["expect_v"]))
     case = load("hand_decode_learner_order")
     dense = f32_array(case["dense_in"])
     oracle.decode_accumulate(case["n"], case["bin_len"], [hex_bytes(h) for h in case["msgs_hex"]],
