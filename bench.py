@@ -60,6 +60,10 @@ def parse_args():
     p.add_argument("--no-sgd", action="store_true", help="skip the fused decode + SGD measurement")
     p.add_argument("--min-timed-seconds", type=float, default=1.5,
                    help="repeat the K timed steps until the clock sampler has covered this long")
+    p.add_argument("--residue-contrast", action="store_true",
+                   help="instead of the benchmark: residue range and compression per carried step of AdaComp "
+                        "and of Local Selection on one 4096x4096 layer at L_T 50, 500 and 5000")
+    p.add_argument("--contrast-steps", type=int, default=25)
     return p.parse_args()
 
 
@@ -348,19 +352,21 @@ class DeviceRun:
             for gi in range(len(self.gidx)):
                 host[k][gi].copy_(ws_of(k, gi)[:self.res_bytes[gi]], non_blocking=True)
         torch.cuda.current_stream().synchronize()
-        lens = []
+        if not hasattr(self, "len_bufs"):
+            self.len_bufs = [np.zeros(len(g) * self.K, np.uint64) for g in self.gidx]
+            self.len_ptrs = [b.ctypes.data_as(self.ct.POINTER(self.ct.c_uint64)) for b in self.len_bufs]
         for gi, g in enumerate(self.gidx):
-            arr = (self.ct.c_uint64 * (len(g) * self.K))()
+            nl = len(g)
             for k in range(self.K):
-                blk = host[k][gi].numpy()
-                for j in range(len(g)):
-                    o = 64 + 2112 * j + self.RESULT_AT
-                    status = int(blk[o + 4:o + 8].view(np.uint32)[0])
-                    if status != 0:
-                        raise RuntimeError(f"device status {status}")
-                    arr[j * self.K + k] = int(blk[o + 16:o + 24].view(np.uint64)[0])
-            lens.append(arr)
-        return lens
+                # the layers' 2112-byte blocks after the 64-byte control block; in each, the
+                # result {s f32, status u32, nnz u64, msg_bytes u64} at RESULT_AT
+                blk = host[k][gi].numpy()[64:64 + 2112 * nl].reshape(nl, 2112)
+                res = blk[:, self.RESULT_AT:self.RESULT_AT + 24]
+                status = res[:, 4:8].copy().view(np.uint32).ravel()
+                if status.any():
+                    raise RuntimeError(f"device status {int(status[status != 0][0])}")
+                self.len_bufs[gi][k::self.K] = res[:, 16:24].copy().view(np.uint64).ravel()
+        return self.len_ptrs
 
     def step(self, i, stream_ptr, k1_events=None, dec_events=None, ws_fixed=None, msg_set=0):
         """One step: every learner's compress, the message lengths read back (the
@@ -604,7 +610,7 @@ def run_decode_sgd(args, run, sp, world, layers, adam=False):
         if run.ac.adacomp_decode_status(h, run.dec_ws[gi]) != run.ac.OK:
             raise RuntimeError("the fused decode rejected a message")
     ms = max_over_ranks(sorted(reps)[len(reps) // 2], world)
-    msg_bytes = sum(sum(a) for a in run.last_lens)
+    msg_bytes = int(sum(int(b.sum()) for b in run.len_bufs))
     bins = sum(-(-l.numel // l.bin_len) for l in layers) * run.K
     algo = (24 if adam else 16) * sum(numels) + msg_bytes + 2 * bins
     del bufs
@@ -708,7 +714,7 @@ def run_e2e(args, run, layers, sp, world):
                 spans, li = [], 0
                 for gi, g in enumerate(run.gidx):
                     for jj in range(len(g)):
-                        spans.append((msg_offs[k][li], int(lens[gi][jj * run.K + k])))
+                        spans.append((msg_offs[k][li], int(run.len_bufs[gi][jj * run.K + k])))
                         li += 1
                 # one copy per run of messages: neighbours whose gap (the unused tail of
                 # a buffer sized for the worst case) is under 256 KB share a copy
@@ -761,6 +767,52 @@ def run_e2e(args, run, layers, sp, world):
             "ms_per_step": secs * 1e3 / steps, "h2d_gbs_upload_alone": up_gbs,
             "overlap": "dW upload of the next step and message download of the previous step overlap "
                        "the computation; the message lengths come back before each decode"}
+
+
+# ---------------------------------------------------------------- residue contrast
+def run_residue_contrast(args):
+    """The contrast of "AdaComp (Adaptive Residual Gradient Compression)", Claims >
+    Mechanism #r629-self-adjusting-sparsity-prevents-residual-explosion, on synthetic
+    gradients: one 4096x4096 layer, dW_t = 1e-3 (m + z_t) with a direction m ~ N(0, 0.25)
+    kept for every step (gradients of a training run keep much of their direction)
+    and fresh noise z_t ~ N(0, 1); the residue is carried for `contrast_steps` steps
+    under AdaComp and under Local Selection (hard threshold, no soft-threshold probe)
+    at L_T = 50, 500 and 5000. Reports, per step, the residue's min and max and the
+    compression ratio (4N / message bytes), all through the C ABI."""
+    import residual_gradient_compression_gb300 as ac
+    from residual_gradient_compression_gb300 import build
+    build.build()
+    dev = torch.device("cuda", torch.cuda.current_device())
+    n = 4096 * 4096
+    g = torch.Generator(device=dev)
+    g.manual_seed(5_000_000)
+    m = torch.randn(n, generator=g, device=dev) * 0.5
+    out = {"mode": "residue_contrast", "layer_elements": n, "steps": args.contrast_steps,
+           "dW": "1e-3 * (m + z_t), m ~ N(0, 0.25) fixed, z_t ~ N(0, 1) fresh each step", "results": []}
+    for L in (50, 500, 5000):
+        for rule in (ac.RULE_ADACOMP, ac.RULE_LOCAL_SELECTION):
+            h = ac.adacomp_init_layer(n, L, ac.F32)
+            ac.adacomp_set_selection_rule(h, rule)
+            msg = torch.zeros(h.max_msg_bytes[0], dtype=torch.uint8, device=dev)
+            ws = torch.zeros(h.compress_ws_bytes, dtype=torch.uint8, device=dev)
+            res = torch.zeros(n, device=dev)
+            lo, hi, comp = [], [], []
+            for t in range(args.contrast_steps):
+                gz = torch.Generator(device=dev)
+                gz.manual_seed(5_000_001 + t)
+                dw = (m + torch.randn(n, generator=gz, device=dev)) * 1e-3
+                ac.adacomp_compress(h, res, dw, msg, ws)
+                mb, s, st = ac.adacomp_query(h, ws)
+                if st != ac.OK:
+                    raise RuntimeError(f"device status {st}")
+                mn, mx = torch.aminmax(res)
+                lo.append(float(mn))
+                hi.append(float(mx))
+                comp.append(4.0 * n / mb)
+            out["results"].append({"bin_len": L, "rule": "adacomp" if rule == ac.RULE_ADACOMP else "local_selection",
+                                   "residue_min": lo, "residue_max": hi, "compression": comp})
+            ac.adacomp_free(h)
+    return out
 
 
 # ---------------------------------------------------------------- oracle legs
@@ -863,6 +915,10 @@ def main():
             print(json.dumps(out), flush=True)
         return 0
     rank, world = dist_init()
+    if args.residue_contrast:
+        if rank == 0:
+            print(json.dumps(run_residue_contrast(args)), flush=True)
+        return 0
     out, run = run_device(args, rank, world)
     del run
     torch.cuda.empty_cache()

@@ -136,22 +136,27 @@ adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* d
  * an interface convenience of this library.
  *
  * Same arguments, checks and results as adacomp_compress, but the compress
- * workspace is a 1 MiB array inside the library (a file-scope __device__ array that
- * every GPU loading the library keeps until the process exits). It therefore
- * takes single-layer handles whose compress_ws_bytes is at most 1 MiB: about 3.9M
- * elements for 16 <= L_T <= 509 (whose workspace holds two bits per element) and
- * about 260M elements for other bin lengths; larger layers get
- * ADACOMP_ERR_WORKSPACE.
+ * workspace is an array of ADACOMP_STATIC_WS_BYTES (1 MiB) inside the library (a
+ * file-scope __device__ array that every GPU loading the library keeps until the
+ * process exits). It therefore takes single-layer handles whose compress_ws_bytes
+ * (from adacomp_init_layer) is at most ADACOMP_STATIC_WS_BYTES; compare the two to
+ * know whether a layer fits (roughly 3.9M elements for 16 <= L_T <= 509, whose
+ * workspace holds two bits per element, and far more for other bin lengths). Larger
+ * layers get ADACOMP_ERR_WORKSPACE.
  * The call allocates nothing: it zeroes the part of the array it uses
  * (cudaMemsetAsync) and runs the same kernels on `stream`.
  *   result_out  optional device buffer of 32 bytes, 8-byte aligned, that receives
  *               {float s; uint32 status; uint64 nnz; uint64 msg_bytes; uint64 pad}
  *               (the values adacomp_query reports for adacomp_compress); NULL skips it.
  * The first call on each device looks up the array's device address with that
- * device current; make that first call before capturing any stream. All calls
- * share the one array, so calls that overlap on a GPU (different streams, or
- * several host threads) race and corrupt each other's results: serialise them.
+ * device current and keeps it for the life of the process; make that first call
+ * before capturing any stream. The kept address belongs to the device's context:
+ * after cudaDeviceReset of that device, do not call this entry point again in the
+ * same process. All calls share the one array, so calls that overlap on a GPU
+ * (different streams, or several host threads) race and corrupt each other's
+ * results: serialise them.
  */
+#define ADACOMP_STATIC_WS_BYTES ((size_t)1 << 20)
 adacomp_status adacomp_compress_static_ws(adacomp_layer_t h, float* residue, const void* dW,
                                           void* msg, size_t msg_capacity, void* result_out,
                                           cudaStream_t stream);

@@ -26,6 +26,7 @@ RULE_ADACOMP, RULE_LOCAL_SELECTION = 0, 1
 MAX_GROUP = 128
 MAX_LEARNERS = 256
 DECODE_WS_FIXED = 10240
+STATIC_WS_BYTES = 1 << 20  # ADACOMP_STATIC_WS_BYTES: the largest workspace adacomp_compress_static_ws holds
 
 _lib = None
 

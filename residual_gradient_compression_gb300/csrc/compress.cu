@@ -1610,7 +1610,7 @@ cudaError_t launch_materialize(const KGroup& g, void* ws, cudaStream_t stream)
 #include "adacomp.h"
 
 namespace {
-constexpr size_t kStaticScratchBytes = size_t(1) << 20;  // 1 MiB
+constexpr size_t kStaticScratchBytes = ADACOMP_STATIC_WS_BYTES;  // 1 MiB
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
 // Device address of g_static_scratch, looked up once per device (index = device id).
 std::atomic<void*> g_static_scratch_addr[64];

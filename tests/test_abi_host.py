@@ -154,3 +154,9 @@ def test_status_strings_and_free_null():
         assert ac.adacomp_status_string(s) not in ("", "unknown status")
     ac.lib().adacomp_free(None)
     assert ac.lib().adacomp_set_timeout_ns(None, 5) == ac.ERR_INVALID_ARG
+
+
+def test_static_workspace_size_constant_matches_the_header():
+    text = open(os.path.join(ROOT, "include", "adacomp.h")).read()
+    m = re.search(r"#define ADACOMP_STATIC_WS_BYTES \(\(size_t\)1 << (\d+)\)", text)
+    assert m and (1 << int(m.group(1))) == ac.STATIC_WS_BYTES

@@ -51,3 +51,26 @@ def test_local_selection_residue_grows_where_adacomp_levels_off():
     assert ada[3] < 1.10 * ada[1]  # AdaComp: bounded
     assert ls[3] > 1.3 * ls[0]     # Local Selection: still growing
     assert ls[3] > 1.5 * ada[3]
+
+
+def test_local_selection_residue_grows_where_adacomp_stays_bounded():
+    """The contrast the entry draws (Claims > Mechanism
+    #r629-self-adjusting-sparsity-prevents-residual-explosion): on a designed input, a
+    bin of 64 elements receiving the same positive gradient every step with slightly
+    different magnitudes (d (1 + j/128)), AdaComp's soft threshold sends every element
+    whose G + dW reaches the bin maximum, so the residues stay within about 1.4 d;
+    Local Selection sends only the bin maximum each step, so the other elements keep
+    accumulating and the largest residue passes 20 d within 50 steps."""
+    L = n = 64
+    d = np.float32(1e-3)
+    dw = (d * (1 + np.arange(n, dtype=np.float32) / 128)).astype(np.float32)
+    peak = {}
+    for ls in (False, True):
+        r = np.zeros(n, np.float32)
+        worst = 0.0
+        for _ in range(50):
+            oracle.compress(r, dw, L, local_selection=ls)
+            worst = max(worst, float(np.abs(r).max()))
+        peak[ls] = worst / float(d)
+    assert peak[False] <= 2.0, peak
+    assert peak[True] >= 20.0, peak
