@@ -42,11 +42,21 @@ bool handle_is_sliced(const adacomp_layer* h)
     return !h->layers.empty();
 }
 
+// Every layer's bins longer than a warp slice (and at most kBigMaxLen): the
+// block-sliced path, with the sliced path's workspace layout and 16 slices per tile.
+bool handle_is_big(const adacomp_layer* h)
+{
+    for (const KLayer& k : h->layers)
+        if (!adacomp::is_big_len(k.bin_len)) return false;
+    return !h->layers.empty();
+}
+
 size_t compress_ws_for(const adacomp_layer* h)
 {
     const int nl = (int)h->layers.size();
-    return handle_is_sliced(h) ? adacomp::sliced_ws_bytes(nl, h->total_tiles)
-                               : adacomp::compress_ws_bytes(nl, h->total_tiles, h->lazy);
+    if (handle_is_sliced(h)) return adacomp::sliced_ws_bytes(nl, h->total_tiles);
+    if (handle_is_big(h)) return adacomp::sliced_ws_bytes(nl, h->total_tiles, true);
+    return adacomp::compress_ws_bytes(nl, h->total_tiles, h->lazy);
 }
 
 adacomp_status make_group(adacomp_layer_t* out, int32_t num_layers, const int64_t* n, const int32_t* bin_len,
@@ -118,6 +128,7 @@ void fill_group(const adacomp_layer* h, KGroup* g)
     g->needs_gbuf = 0;
     g->lazy = h->lazy ? 1u : 0u;
     g->local_selection = h->rule == ADACOMP_RULE_LOCAL_SELECTION ? 1u : 0u;
+    g->big = handle_is_big(h) ? 1u : 0u;
     for (const KLayer& k : h->layers)
         if (k.bin_len < 16) g->needs_gbuf = 1;  // the short-bin path stages G in shared memory
     for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];

@@ -58,7 +58,17 @@ struct KGroup {
     uint32_t needs_gbuf;        // some layer has bins shorter than 16 (G staged in shared memory)
     uint32_t lazy;              // deferred fix-up for warp-sliced layers (pending masks in the workspace)
     uint32_t local_selection;   // selection rule: 0 AdaComp (abs(G + dW) >= g_max), 1 Local Selection (abs(G) >= g_max)
+    uint32_t big;               // every layer has kBigMinLen <= L_T <= kBigMaxLen: the block-sliced path
 };
+
+// Block-sliced path: bins longer than a warp slice. A tile (whole bins, at most
+// max(kTileTarget, L_T) elements) is cut into kBigSlices slices of 512 slots from the
+// 16-byte boundary at or before its first element; the bins that fit (at most 8).
+constexpr int kBigMinLen = 510;
+constexpr int kBigMaxLen = 8189;  // a one-bin tile plus its alignment slots fits 16 slices
+constexpr int kBigSlices = 16;
+constexpr int kBigMaxBins = 8;
+__host__ __device__ inline bool is_big_len(int32_t L) { return L >= kBigMinLen && L <= kBigMaxLen; }
 
 // Dynamic shared memory of the compress kernel (bytes), laid out in this order:
 // 2 stages x {residue slice, dW slice}, layer table, G buffer, nbuf code staging buffers, g_max, counts,
@@ -137,13 +147,21 @@ __host__ __device__ inline size_t compress_ws_bytes(int num_layers, uint64_t tot
 // the lane's 16 consecutive slots. The tile totals are zero between calls; the
 // other arrays are written by each call before they are read. The mask arrays start
 // on 16-byte boundaries (the emitting kernel loads them 16 bytes at a time).
+// (The block-sliced path uses the same layout with kBigSlices slices per tile.)
 constexpr size_t kMaskBytesPerTile = kWarps * 32 * 2;
+__host__ __device__ inline size_t mask_bytes_per_tile(bool big) { return (size_t)(big ? kBigSlices : kWarps) * 32 * 2; }
 __host__ __device__ inline size_t pad16(size_t b) { return (b + 15) & ~(size_t)15; }
 __host__ __device__ inline size_t sl_excl_offset(int num_layers) { return ws_desc_offset(num_layers); }
 __host__ __device__ inline size_t sl_tot_offset(int num_layers, uint64_t T) { return sl_excl_offset(num_layers) + pad16(8 * (size_t)T); }
 __host__ __device__ inline size_t sl_sent_offset(int num_layers, uint64_t T) { return sl_tot_offset(num_layers, T) + pad16(4 * (size_t)T); }
-__host__ __device__ inline size_t sl_sign_offset(int num_layers, uint64_t T) { return sl_sent_offset(num_layers, T) + kMaskBytesPerTile * (size_t)T; }
-__host__ __device__ inline size_t sliced_ws_bytes(int num_layers, uint64_t T) { return sl_sign_offset(num_layers, T) + kMaskBytesPerTile * (size_t)T; }
+__host__ __device__ inline size_t sl_sign_offset(int num_layers, uint64_t T, bool big = false)
+{
+    return sl_sent_offset(num_layers, T) + mask_bytes_per_tile(big) * (size_t)T;
+}
+__host__ __device__ inline size_t sliced_ws_bytes(int num_layers, uint64_t T, bool big = false)
+{
+    return sl_sign_offset(num_layers, T, big) + mask_bytes_per_tile(big) * (size_t)T;
+}
 // Bytes at the start of a workspace that must be zero before its first call.
 __host__ __device__ inline size_t ws_zero_prefix(int num_layers, uint64_t T, bool sliced)
 {

@@ -1504,7 +1504,7 @@ DeviceInfo g_dev[64];
 cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cudaEvent_t ev_before,
                             cudaEvent_t ev_mid, cudaEvent_t ev_after)
 {
-    if (group_is_sliced(g)) return launch_compress_sliced(g, ws, stream, ev_before, ev_mid, ev_after);
+    if (group_is_sliced(g) || g.big) return launch_compress_sliced(g, ws, stream, ev_before, ev_mid, ev_after);
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -1581,7 +1581,7 @@ cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cuda
 
 cudaError_t launch_materialize(const KGroup& g, void* ws, cudaStream_t stream)
 {
-    if (group_is_sliced(g)) return launch_materialize_sliced(g, ws, stream);
+    if (group_is_sliced(g) || g.big) return launch_materialize_sliced(g, ws, stream);
     if (!g.lazy) return cudaSuccess;
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -1641,7 +1641,7 @@ extern "C" adacomp_status adacomp_compress_static_ws(adacomp_layer_t h, float* r
     }
     // The array keeps the previous call's contents: zero the control word, the
     // layer's accumulators and the look-back descriptors this call relies on.
-    const size_t zero_bytes = ws_zero_prefix(1, g.total_tiles, group_is_sliced(g));
+    const size_t zero_bytes = ws_zero_prefix(1, g.total_tiles, group_is_sliced(g) || g.big != 0);
     if (cudaMemsetAsync(scratch, 0, zero_bytes, stream) != cudaSuccess) return ADACOMP_ERR_CUDA;
     if (launch_compress(g, scratch, stream) != cudaSuccess) return ADACOMP_ERR_CUDA;
     if (result_out) {

@@ -101,20 +101,18 @@ __device__ __forceinline__ int layer_of_tile(const uint32_t* tb, int num_layers,
     return lo;
 }
 
-// Starts slice S's data into a stage (run by one lane): bulk copies of the
-// 16-byte-aligned spans covering the slice, from the boundary at or before its
-// first element (slot 0 of lane 0) to the one at or after its last; only at the
-// end of the layer's arrays are the last few elements loaded with plain loads.
-// The spans never exceed 512 slots: the slice has at most 509 elements. Returns
-// false when nothing was copied (an empty slice: the phase completes at once).
-__device__ bool issue_slice(const KLayer& ly, const Slice& S, float* rb, void* db, uint64_t* bar)
+// Starts layer elements [e0, e1) into a stage (run by one lane), slot 0 of the
+// stage holding layer element a0 (a0 <= e0, a multiple of 4, e1 - a0 <= 512): bulk
+// copies of the 16-byte-aligned spans covering the range, from a0 to the boundary
+// at or after e1; only at the end of the layer's arrays are the last few elements
+// loaded with plain loads. Returns false when nothing was copied (an empty range:
+// the phase completes at once).
+__device__ bool issue_range(const KLayer& ly, int64_t e0, int64_t e1, int64_t a0, float* rb, void* db, uint64_t* bar)
 {
-    if (S.we1 <= S.we0) {
+    if (e1 <= e0) {
         ptx::mbar_arrive(bar);
         return false;
     }
-    const int64_t e0 = S.ts + S.we0, e1 = S.ts + S.we1;
-    const int64_t a0 = S.a0;
     int64_t a1 = (e1 + 3) & ~(int64_t)3;
     if (a1 > ly.n) a1 = e1 & ~(int64_t)3;
     const uint32_t rbytes = (uint32_t)(a1 - a0) * 4u;
@@ -140,6 +138,12 @@ __device__ bool issue_slice(const KLayer& ly, const Slice& S, float* rb, void* d
     if (rbytes) ptx::bulk_g2s(rb, ly.residue + a0, rbytes, bar);
     if (dbytes) ptx::bulk_g2s(db, static_cast<const uint8_t*>(ly.dw) + b0 * (ly.dw_bf16 ? 2 : 4), dbytes, bar);
     return true;
+}
+
+// A warp slice's data (at most 509 elements from a 16-byte boundary).
+__device__ __forceinline__ bool issue_slice(const KLayer& ly, const Slice& S, float* rb, void* db, uint64_t* bar)
+{
+    return issue_range(ly, S.ts + S.we0, S.ts + S.we1, S.a0, rb, db, bar);
 }
 
 // Bounded wait on an mbarrier phase, the thread sleeping in the barrier between
@@ -191,6 +195,51 @@ __device__ __forceinline__ LaneGeo lane_geo(const Slice& S, const KLayer& ly, in
     return q;
 }
 
+// ---------------------------------------------------------------- block-sliced tiles
+// Tiles of bins longer than a warp slice (kBigMinLen <= L_T <= kBigMaxLen) keep their
+// whole bins (floor(4096 / L_T), at least one) and are cut into kBigSlices slices of
+// 512 slots, slice w starting at slot 512 w from the 16-byte boundary at or before the
+// tile's first element. A 512-slot slice meets at most three bins of 510 or more.
+// In the returned Slice, wb0 is the tile-relative bin of the slice's first element and
+// nb the tile's bin count; an empty slice (past the tile's end) has we0 == we1.
+__device__ __forceinline__ Slice big_slice(const KLayer& ly, int layer, uint32_t t, int w)
+{
+    Slice S;
+    S.layer = layer;
+    S.first_bin = (t - ly.tile_begin) * ly.bins_per_tile;
+    S.nb = (int)min(ly.bins_per_tile, ly.nbins - S.first_bin);
+    S.ts = (int64_t)S.first_bin * ly.bin_len;
+    const int tl = (int)min((int64_t)S.nb * ly.bin_len, ly.n - S.ts);
+    S.a0 = (S.ts & ~(int64_t)3) + (int64_t)kSlots * w;
+    const int rel = (int)(S.a0 - S.ts);  // tile element of slot 0: -3 .. 0 for slice 0
+    S.we0 = max(0, rel);
+    S.we1 = max(S.we0, min(tl, rel + kSlots));
+    S.wb0 = (int)__umulhi((uint32_t)S.we0, ly.inv_len);  // tile elements are below 2^13: exact
+    return S;
+}
+
+// Slices of a block-sliced tile that hold elements.
+__device__ __forceinline__ int big_slices_used(const KLayer& ly, uint32_t t)
+{
+    const uint32_t fb = (t - ly.tile_begin) * ly.bins_per_tile;
+    const int nb = (int)min(ly.bins_per_tile, ly.nbins - fb);
+    const int64_t ts = (int64_t)fb * ly.bin_len;
+    const int tl = (int)min((int64_t)nb * ly.bin_len, ly.n - ts);
+    return ((int)(ts & 3) + tl + kSlots - 1) / kSlots;
+}
+
+// A lane's 16 slots in a block-sliced slice; bin_lo is tile-relative here.
+__device__ __forceinline__ LaneGeo big_lane_geo(const Slice& S, const KLayer& ly, int lane)
+{
+    LaneGeo q;
+    q.lane_e = (int)(S.a0 - S.ts) + kSeg * lane;
+    const int vlo = max(0, S.we0 - q.lane_e), vhi = min(kSeg, S.we1 - q.lane_e);
+    q.valid = vhi > vlo ? (((1u << (vhi - vlo)) - 1u) << vlo) : 0u;
+    q.bin_lo = q.valid ? (int)__umulhi((uint32_t)max(q.lane_e, S.we0), ly.inv_len) : 0;
+    q.split = (q.bin_lo + 1) * ly.bin_len - q.lane_e;
+    return q;
+}
+
 // Slot-order mask <-> register order: register chunk k holds slot chunk k ^ rot.
 __device__ __forceinline__ uint32_t to_reg_order(uint32_t m, int rot)
 {
@@ -205,6 +254,69 @@ __device__ __forceinline__ uint32_t to_slot_order(uint32_t r, int rot)
 #pragma unroll
     for (int k = 0; k < 4; ++k) m |= ((r >> (4 * k)) & 0xfu) << (4 * (k ^ rot));
     return m;
+}
+
+// One lane's 16 slots of a slice whose data is in a stage (rs: residue, ds: dW;
+// slot 0 of lane 0 holds layer element S.a0), the four 16-byte chunks visited in the
+// bank-conflict-free rotated order: G = fl32(residue + dW) (after the deferred
+// correction fl32(G - copysign(s_prev, G)) of the slots set in pm), |probe| into ah
+// (-1 where G == 0, so that such elements are never sent), the mask of G < 0 (kLazy
+// only), residue := G for the valid slots (vr) with 128-bit stores, and the maxima
+// of |G| over the valid slots of the lane's two bins (lor, hir). Registers are in
+// register order: chunk k is slot chunk k ^ rot.
+template <bool kLazy, bool kLS>
+__device__ __forceinline__ void lane_slots(const KLayer& ly, const Slice& Sl, const float* rs0, const void* ds, int lane,
+                                           int rot, uint32_t pm, float s_prev, uint32_t vr, uint32_t lor, uint32_t hir,
+                                           float (&ah)[4][4], uint32_t& ngr, float& m_lo, float& m_hi)
+{
+    const float* rs = rs0 + kSeg * lane;
+    const int doff = ly.dw_bf16 ? (int)(Sl.a0 - ((Sl.ts + Sl.we0) & ~(int64_t)7)) : 0;
+    float* gres = ly.residue + Sl.a0 + kSeg * lane;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+        const int q0 = 4 * (k ^ rot);
+        float4 r = *reinterpret_cast<const float4*>(rs + q0);
+        if (kLazy && (pm & (0xfu << (4 * k)))) {
+            if (pm & (1u << (4 * k + 0))) r.x = __fsub_rn(r.x, copysignf(s_prev, r.x));
+            if (pm & (1u << (4 * k + 1))) r.y = __fsub_rn(r.y, copysignf(s_prev, r.y));
+            if (pm & (1u << (4 * k + 2))) r.z = __fsub_rn(r.z, copysignf(s_prev, r.z));
+            if (pm & (1u << (4 * k + 3))) r.w = __fsub_rn(r.w, copysignf(s_prev, r.w));
+        }
+        float d[4], gv[4];
+        if (ly.dw_bf16) {
+            const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(ds) + doff + kSeg * lane + q0);
+            d[0] = bf16_lo(u.x); d[1] = bf16_hi(u.x); d[2] = bf16_lo(u.y); d[3] = bf16_hi(u.y);
+        } else {
+            const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(ds) + kSeg * lane + q0);
+            d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+        }
+        gv[0] = __fadd_rn(r.x, d[0]);
+        gv[1] = __fadd_rn(r.y, d[1]);
+        gv[2] = __fadd_rn(r.z, d[2]);
+        gv[3] = __fadd_rn(r.w, d[3]);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t bit = 1u << (4 * k + e);
+            // an element with G == 0 is never sent: its probe is made negative
+            ah[k][e] = gv[e] != 0.0f ? fabsf(probe(gv[e], d[e], kLS)) : -1.0f;
+            if (kLazy) ngr |= gv[e] < 0.0f ? bit : 0u;
+            const float a = fabsf(gv[e]);
+            // slots outside the slice hold stale data: neither maximum takes them,
+            // and they are dropped from the sent mask by the caller
+            m_lo = fmaxf(m_lo, (lor & bit) ? a : 0.0f);
+            m_hi = fmaxf(m_hi, (hir & bit) ? a : 0.0f);
+        }
+        // residue := G (sent elements are corrected once s is known)
+        const uint32_t vq = (vr >> (4 * k)) & 0xfu;
+        float* gp = gres + q0;
+        if (vq == 0xfu) {
+            *reinterpret_cast<float4*>(gp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+        } else if (vq) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if ((vq >> e) & 1u) gp[e] = gv[e];
+        }
+    }
 }
 
 // ---------------------------------------------------------------- streaming kernel
@@ -329,57 +441,9 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
         float ah[4][4];             // |probe| per register slot
         uint32_t ngr = 0;  // G < 0 (register order; kept for the deferred fix-up's codes only)
         float m_lo = 0.0f, m_hi = 0.0f;
-        if (q.valid) {
-            const float* rs = stage_r(s) + kSeg * lane;
-            const int doff = ly.dw_bf16 ? (int)(Sl.a0 - ((Sl.ts + Sl.we0) & ~(int64_t)7)) : 0;
-            float* gres = ly.residue + Sl.a0 + kSeg * lane;
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int q0 = 4 * (k ^ rot);
-                float4 r = *reinterpret_cast<const float4*>(rs + q0);
-                if (kLazy && (pm & (0xfu << (4 * k)))) {
-                    if (pm & (1u << (4 * k + 0))) r.x = __fsub_rn(r.x, copysignf(s_prev, r.x));
-                    if (pm & (1u << (4 * k + 1))) r.y = __fsub_rn(r.y, copysignf(s_prev, r.y));
-                    if (pm & (1u << (4 * k + 2))) r.z = __fsub_rn(r.z, copysignf(s_prev, r.z));
-                    if (pm & (1u << (4 * k + 3))) r.w = __fsub_rn(r.w, copysignf(s_prev, r.w));
-                }
-                float d[4], gv[4];
-                if (ly.dw_bf16) {
-                    const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(stage_d(s)) + doff +
-                                                                    kSeg * lane + q0);
-                    d[0] = bf16_lo(u.x); d[1] = bf16_hi(u.x); d[2] = bf16_lo(u.y); d[3] = bf16_hi(u.y);
-                } else {
-                    const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(stage_d(s)) + kSeg * lane + q0);
-                    d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
-                }
-                gv[0] = __fadd_rn(r.x, d[0]);
-                gv[1] = __fadd_rn(r.y, d[1]);
-                gv[2] = __fadd_rn(r.z, d[2]);
-                gv[3] = __fadd_rn(r.w, d[3]);
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const uint32_t bit = 1u << (4 * k + e);
-                    // an element with G == 0 is never sent: its probe is made negative
-                    ah[k][e] = gv[e] != 0.0f ? fabsf(probe(gv[e], d[e], kLS)) : -1.0f;
-                    if (kLazy) ngr |= gv[e] < 0.0f ? bit : 0u;
-                    const float a = fabsf(gv[e]);
-                    // slots outside the slice hold stale data: neither maximum takes them,
-                    // and they are dropped from the sent mask below
-                    m_lo = fmaxf(m_lo, (lor & bit) ? a : 0.0f);
-                    m_hi = fmaxf(m_hi, (hir & bit) ? a : 0.0f);
-                }
-                // residue := G (sent elements are corrected once s is known)
-                const uint32_t vq = (vr >> (4 * k)) & 0xfu;
-                float* gp = gres + q0;
-                if (vq == 0xfu) {
-                    *reinterpret_cast<float4*>(gp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
-                } else if (vq) {
-#pragma unroll
-                    for (int e = 0; e < 4; ++e)
-                        if ((vq >> e) & 1u) gp[e] = gv[e];
-                }
-            }
-        }
+        if (q.valid)
+            lane_slots<kLazy, kLS>(ly, Sl, stage_r(s), stage_d(s), lane, rot, pm, s_prev, vr, lor, hir, ah, ngr, m_lo,
+                                   m_hi);
         // the stage is not read again: lane 0 refills it with the slice S ahead (one
         // warp's shared memory accesses are performed in order, so its reads of the
         // stage precede the copy)
@@ -446,6 +510,299 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
     }
 }
 
+// ---------------------------------------------------------------- block-sliced streaming kernel
+// One tile at a time per CTA (tiles c, c + grid, ...), warp w streaming slice w of
+// each through its own S-stage pipeline of bulk copies, as in slice_kernel. The CTA
+// has one warp per slice of the group's widest tile (W <= 16; slices past a tile's
+// end are empty). A bin now spans several warps, so its maximum and count meet in
+// shared memory. Per tile, in two passes over the warp's stage:
+//   1. G = fl32(residue + dW), residue := G, and the lanes' bin maxima, folded per
+//      bin (a 512-slot slice meets at most three bins) with warp reductions and one
+//      shared atomicMax per bin; then one block barrier;
+//   2. G and the probe again from the stage (recomputing costs less than keeping
+//      them in registers across the barrier: fewer registers, more resident warps),
+//      the selection against the bins' maxima, the masks, and the per-bin counts
+//      (warp reductions, one shared atomicAdd per bin); then the stage is refilled.
+// The counts of tile i are complete at the barrier of tile i + 1, where the finishing
+// warp (the last) writes them into the message, adds the maxima to the CTA's exponent
+// buckets (64-bit, one per fp32 exponent, flushed to the layer's exact accumulator
+// when the CTA moves to another layer and at the end) and writes the tile's code
+// total. Maxima and counts rotate through three buffers, so one barrier per tile
+// suffices. The sent mask (and with the fix-up deferred, the sign mask) of every
+// slice holding elements goes to the workspace, 16 slices per tile; the finalising
+// and emitting kernels follow. Waits are bounded as in slice_kernel; a warp whose
+// copy did not land marks the layer, computes nothing further, and keeps taking part
+// in the barriers.
+constexpr int kBigMaxRegs = 64;
+
+struct BigPlan {
+    uint32_t d_bytes, stage_bytes, stages_bytes, layer_bytes, total;
+};
+__host__ __device__ inline BigPlan big_plan(uint32_t d_size, int stages, int num_layers, int warps)
+{
+    BigPlan p;
+    p.d_bytes = d_size == 4 ? kDBytes32 : kDBytes16;
+    p.stage_bytes = kRBytes + p.d_bytes;
+    p.stages_bytes = (uint32_t)warps * stages * p.stage_bytes;
+    p.layer_bytes = (uint32_t)num_layers * 64u;
+    // + maxima and counts [3][kBigMaxBins] u32 each, 256 u64 exponent buckets, barriers
+    p.total = p.stages_bytes + p.layer_bytes + 6 * kBigMaxBins * 4 + 256 * 8 + (uint32_t)warps * stages * 8;
+    return p;
+}
+
+// Chunk q0 .. q0 + 3 of a lane's slots from a stage (rs: the lane's residue slots,
+// ds: the stage's dW, doff: the dW stage offset of slot 0 of lane 0): G = fl32(residue
+// + dW) after the deferred correction of the slots set in pmk, and dW.
+template <bool kLazy>
+__device__ __forceinline__ void chunk_g(bool bf16, const float* rs, const void* ds, int doff, int lane, int q0,
+                                        uint32_t pmk, float s_prev, float (&gv)[4], float (&d)[4])
+{
+    float4 r = *reinterpret_cast<const float4*>(rs + q0);
+    if (kLazy && pmk) {
+        if (pmk & 1u) r.x = __fsub_rn(r.x, copysignf(s_prev, r.x));
+        if (pmk & 2u) r.y = __fsub_rn(r.y, copysignf(s_prev, r.y));
+        if (pmk & 4u) r.z = __fsub_rn(r.z, copysignf(s_prev, r.z));
+        if (pmk & 8u) r.w = __fsub_rn(r.w, copysignf(s_prev, r.w));
+    }
+    if (bf16) {
+        const uint2 u = *reinterpret_cast<const uint2*>(static_cast<const uint16_t*>(ds) + doff + kSeg * lane + q0);
+        d[0] = bf16_lo(u.x); d[1] = bf16_hi(u.x); d[2] = bf16_lo(u.y); d[3] = bf16_hi(u.y);
+    } else {
+        const float4 v = *reinterpret_cast<const float4*>(static_cast<const float*>(ds) + kSeg * lane + q0);
+        d[0] = v.x; d[1] = v.y; d[2] = v.z; d[3] = v.w;
+    }
+    gv[0] = __fadd_rn(r.x, d[0]);
+    gv[1] = __fadd_rn(r.y, d[1]);
+    gv[2] = __fadd_rn(r.z, d[2]);
+    gv[3] = __fadd_rn(r.w, d[3]);
+}
+
+template <int S, bool kLazy, bool kLS>
+__global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
+{
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int W = (int)(blockDim.x >> 5);
+    const BigPlan P = big_plan(g.d_size, S, g.num_layers, W);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint8_t* stages = smem + (size_t)warp * S * P.stage_bytes;
+    KLayer* lays = reinterpret_cast<KLayer*>(smem + P.stages_bytes);
+    uint32_t* bmax = reinterpret_cast<uint32_t*>(smem + P.stages_bytes + P.layer_bytes);  // [3][kBigMaxBins]
+    uint32_t* bcnt = bmax + 3 * kBigMaxBins;                                              // [3][kBigMaxBins]
+    unsigned long long* hist = reinterpret_cast<unsigned long long*>(bcnt + 3 * kBigMaxBins);
+    uint64_t* bar = reinterpret_cast<uint64_t*>(hist + 256) + warp * S;
+    auto stage_r = [&](int s) { return reinterpret_cast<float*>(stages + s * P.stage_bytes); };
+    auto stage_d = [&](int s) { return static_cast<void*>(stages + s * P.stage_bytes + kRBytes); };
+
+    {
+        const uint4* src = reinterpret_cast<const uint4*>(&g.layer[0]);
+        uint4* dst = reinterpret_cast<uint4*>(lays);
+        for (int e = tid; e < g.num_layers * (int)(sizeof(KLayer) / 16); e += blockDim.x) dst[e] = src[e];
+    }
+    for (int e = tid; e < 6 * kBigMaxBins; e += blockDim.x) bmax[e] = 0u;
+    for (int e = tid; e < 256; e += blockDim.x) hist[e] = 0ull;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) ptx::mbar_init(&bar[s], 1);
+        ptx::fence_mbar_init();
+    }
+    __syncthreads();
+
+    const uint32_t T = g.total_tiles, c = blockIdx.x, GS = gridDim.x;
+    uint32_t* tile_tot = reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T));
+    uint16_t* sent = reinterpret_cast<uint16_t*>(ws + sl_sent_offset(g.num_layers, T));
+    uint16_t* sign = reinterpret_cast<uint16_t*>(ws + sl_sign_offset(g.num_layers, T, true));
+    const bool pending = kLazy && reinterpret_cast<const volatile Ctl*>(ws)->pending != 0u;
+    const int rot = seg_rot(lane);
+
+    int iss_lo = 0;
+    uint32_t inflight = 0;
+    if (lane == 0) {
+        for (int s = 0; s < S; ++s) {
+            const uint32_t t = c + s * GS;
+            if (t >= T) break;
+            iss_lo = advance_layer(lays, g.num_layers, t, iss_lo);
+            const Slice Sl = big_slice(lays[iss_lo], iss_lo, t, warp);
+            if (t == g.inject_skip_tile) continue;  // test hook: this copy is never started
+            if (issue_slice(lays[iss_lo], Sl, stage_r(s), stage_d(s), &bar[s])) inflight |= 1u << s;
+        }
+    }
+    __syncwarp();
+
+    // the finishing warp: tile tp's counts into the message, its maxima into the
+    // buckets (flushed first if the tile starts another layer), its code total; the
+    // buffers of parity `par` are left zero
+    int hist_layer = -1;
+    auto flush = [&]() {
+        if (hist_layer < 0) return;
+        LayerWs* hw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(hist_layer));
+        __syncwarp();
+        for (int e = lane; e < 256; e += 32) {
+            const unsigned long long v = hist[e];
+            if (v) {
+                atomicAdd(&hw->acc[e], v);
+                hist[e] = 0ull;
+            }
+        }
+        __syncwarp();
+    };
+    auto finish = [&](uint32_t tp, int lp, int par) {
+        if (lp != hist_layer) {
+            flush();
+            hist_layer = lp;
+        }
+        const KLayer& ly = lays[lp];
+        const uint32_t fb = (tp - ly.tile_begin) * ly.bins_per_tile;
+        const int nb = (int)min(ly.bins_per_tile, ly.nbins - fb);
+        uint32_t cnt = 0;
+        if (lane < nb) {
+            cnt = bcnt[par * kBigMaxBins + lane];
+            const uint32_t u = bmax[par * kBigMaxBins + lane];
+            reinterpret_cast<uint16_t*>(ly.msg + 8)[fb + lane] = (uint16_t)cnt;
+            if (u) {
+                const uint32_t E = u >> 23;
+                atomicAdd(&hist[E], (unsigned long long)(E ? ((u & 0x7fffffu) | 0x800000u) : (u & 0x7fffffu)));
+            }
+        }
+        if (lane < kBigMaxBins) {
+            bmax[par * kBigMaxBins + lane] = 0u;
+            bcnt[par * kBigMaxBins + lane] = 0u;
+        }
+        const uint32_t total = __reduce_add_sync(kFull, cnt);
+        if (lane == 0) tile_tot[tp] = total;
+    };
+
+    int lo = 0, l_prev = -1;
+    uint32_t t_prev = 0, i = 0;
+    bool poisoned = false;
+    uint32_t i_poison = 0;
+    for (;; ++i) {
+        const uint32_t t = c + i * GS;
+        if (t >= T) break;  // uniform over the CTA
+        const int s = (int)(i % S), par = (int)(i % 3);
+        lo = advance_layer(lays, g.num_layers, t, lo);
+        const KLayer& ly = lays[lo];
+        const Slice Sl = big_slice(ly, lo, t, warp);
+        LayerWs* lw = reinterpret_cast<LayerWs*>(ws + ws_layer_offset(lo));
+        const size_t mi = ((size_t)t * kBigSlices + warp) * 32 + lane;
+        uint32_t pm = 0;
+        float s_prev = 0.0f;
+        if (kLazy && pending && Sl.we1 > Sl.we0) {
+            pm = sent[mi];
+            s_prev = lw->result.s;
+        }
+        if (!poisoned && !__all_sync(kFull, wait_bounded(&bar[s], (i / S) & 1u, g.timeout_ns))) {
+            poisoned = true;
+            i_poison = i;
+        }
+        if (poisoned && lane == 0) atomicOr(&lw->err, kErrTimeout);
+        if (!poisoned && lane == 0) inflight &= ~(1u << s);
+        LaneGeo q = big_lane_geo(Sl, ly, lane);
+        if (poisoned) q.valid = 0u;  // the stage's data may be incomplete: compute nothing
+        const uint32_t lomask = q.split >= kSeg ? 0xffffu : ((1u << max(q.split, 0)) - 1u);
+        const uint32_t vr = to_reg_order(q.valid, rot);
+        const uint32_t lor = to_reg_order(lomask, rot) & vr;
+        const uint32_t hir = vr & ~lor;
+        const float* rs = stage_r(s) + kSeg * lane;
+        const void* ds = stage_d(s);
+        const int doff = ly.dw_bf16 ? (int)(Sl.a0 - ((Sl.ts + Sl.we0) & ~(int64_t)7)) : 0;
+        // pass 1: G, residue := G, the lane's bin maxima
+        float m_lo = 0.0f, m_hi = 0.0f;
+        if (q.valid) {
+            float* gres = ly.residue + Sl.a0 + kSeg * lane;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int q0 = 4 * (k ^ rot);
+                float gv[4], d[4];
+                chunk_g<kLazy>(ly.dw_bf16, rs, ds, doff, lane, q0, (pm >> (4 * k)) & 0xfu, s_prev, gv, d);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t bit = 1u << (4 * k + e);
+                    const float a = fabsf(gv[e]);
+                    m_lo = fmaxf(m_lo, (lor & bit) ? a : 0.0f);
+                    m_hi = fmaxf(m_hi, (hir & bit) ? a : 0.0f);
+                }
+                const uint32_t vq = (vr >> (4 * k)) & 0xfu;
+                float* gp = gres + q0;
+                if (vq == 0xfu) {
+                    *reinterpret_cast<float4*>(gp) = make_float4(gv[0], gv[1], gv[2], gv[3]);
+                } else if (vq) {
+#pragma unroll
+                    for (int e = 0; e < 4; ++e)
+                        if ((vq >> e) & 1u) gp[e] = gv[e];
+                }
+            }
+        }
+        // the warp's bins (Sl.wb0 + 0, 1, 2): maxima as fp32 bits (non-negative, so
+        // they order as unsigned integers)
+        const int rb = q.bin_lo - Sl.wb0;  // 0, 1 or 2 for lanes holding elements
+        const uint32_t ulo = __float_as_uint(m_lo), uhi = __float_as_uint(m_hi);
+        const uint32_t x0 = __reduce_max_sync(kFull, rb == 0 ? ulo : 0u);
+        const uint32_t x1 = __reduce_max_sync(kFull, max(rb == 1 ? ulo : 0u, rb == 0 ? uhi : 0u));
+        const uint32_t x2 = __reduce_max_sync(kFull, max(rb == 2 ? ulo : 0u, rb == 1 ? uhi : 0u));
+        if (lane < 3) {
+            const uint32_t x = lane == 0 ? x0 : (lane == 1 ? x1 : x2);
+            if (x) atomicMax(&bmax[par * kBigMaxBins + Sl.wb0 + lane], x);
+        }
+        __syncthreads();  // the tile's maxima are complete, and the previous tile's counts
+        if (warp == W - 1 && l_prev >= 0) finish(t_prev, l_prev, (int)((i + 2) % 3));
+        // pass 2: the selection against the bins' maxima
+        uint32_t fr = 0, ngr = 0;
+        if (q.valid) {
+            const float gm_lo = __uint_as_float(bmax[par * kBigMaxBins + q.bin_lo]);
+            const float gm_hi = hir ? __uint_as_float(bmax[par * kBigMaxBins + q.bin_lo + 1]) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int q0 = 4 * (k ^ rot);
+                float gv[4], d[4];
+                chunk_g<kLazy>(ly.dw_bf16, rs, ds, doff, lane, q0, (pm >> (4 * k)) & 0xfu, s_prev, gv, d);
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const uint32_t bit = 1u << (4 * k + e);
+                    // an element with G == 0 is never sent
+                    const float ah = gv[e] != 0.0f ? fabsf(probe(gv[e], d[e], kLS)) : -1.0f;
+                    fr |= ah >= ((lor & bit) ? gm_lo : gm_hi) ? bit : 0u;
+                    if (kLazy) ngr |= gv[e] < 0.0f ? bit : 0u;
+                }
+            }
+            fr &= vr;
+        }
+        __syncwarp();
+        if (lane == 0 && !poisoned) {  // the stage is not read again: refill it with the tile S ahead
+            const uint32_t tn = t + S * GS;
+            if (tn < T) {
+                iss_lo = advance_layer(lays, g.num_layers, tn, iss_lo);
+                const Slice Sn = big_slice(lays[iss_lo], iss_lo, tn, warp);
+                if (tn != g.inject_skip_tile && issue_slice(lays[iss_lo], Sn, stage_r(s), stage_d(s), &bar[s]))
+                    inflight |= 1u << s;
+            }
+        }
+        const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & hir);
+        const uint32_t n0 = __reduce_add_sync(kFull, rb == 0 ? c_lo : 0u);
+        const uint32_t n1 = __reduce_add_sync(kFull, (rb == 1 ? c_lo : 0u) + (rb == 0 ? c_hi : 0u));
+        const uint32_t n2 = __reduce_add_sync(kFull, (rb == 2 ? c_lo : 0u) + (rb == 1 ? c_hi : 0u));
+        if (lane < 3) {
+            const uint32_t x = lane == 0 ? n0 : (lane == 1 ? n1 : n2);
+            if (x) atomicAdd(&bcnt[par * kBigMaxBins + Sl.wb0 + lane], x);
+        }
+        if (Sl.we1 > Sl.we0) {
+            sent[mi] = (uint16_t)fr;  // register order (the emitting kernel reorders)
+            if (kLazy) sign[mi] = (uint16_t)(ngr & fr);
+        }
+        t_prev = t;
+        l_prev = lo;
+    }
+    __syncthreads();  // the last tile's counts
+    if (warp == W - 1) {
+        if (l_prev >= 0) finish(t_prev, l_prev, (int)((i + 2) % 3));
+        flush();
+    }
+    if (poisoned && lane == 0) {
+        for (uint32_t j = i_poison; j < i_poison + S; ++j) {
+            const int s = (int)(j % S);
+            if (c + j * GS < T && (inflight >> s) & 1u) wait_bounded(&bar[s], (j / S) & 1u, g.timeout_ns);
+        }
+    }
+}
+
 // ---------------------------------------------------------------- finalise and scan
 // Grid: x = chunk of kFinThreads tiles, y = layer (CTAs past a layer's last chunk
 // exit at once). The CTA of chunk c sums the totals of the layer's tiles before the
@@ -494,8 +851,8 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
     // the chunk's own tiles: one per thread, scanned
     const uint32_t j = c0 + tid;
     const uint32_t mine = j < nt ? tot[j] : 0u;
-    // a warp's share: at most 32 x (tiles before the chunk / 1024) x 4072 codes < 2^32 for
-    // layers below 2^38 elements
+    // a warp's share: at most 32 x (tiles before the chunk / 1024) x 8189 codes < 2^32 for
+    // layers below 2^36 elements
     before = __reduce_add_sync(kFull, (uint32_t)before);
     uint32_t incl = mine;
 #pragma unroll
@@ -579,29 +936,42 @@ __device__ __forceinline__ float ld_fill64(const float* p)
     return v;
 }
 
-// The inputs of one tile's emission, loaded a tile ahead.
+// The inputs of one tile's emission, loaded a tile ahead: per group of eight slices
+// (one for warp-sliced tiles, two for block-sliced ones) the sent masks of the lane's
+// eight compute lanes (register order) and their sign masks (deferred fix-up only).
+template <int H>
 struct EmitIn {
-    uint4 f;        // sent masks of the lane's eight compute lanes (register order)
-    uint4 ng;       // their sign masks (deferred fix-up only)
+    uint4 f[H];
+    uint4 ng[H];
     uint64_t pos;   // the tile's first code position in its message
+    int used;       // block-sliced tiles: slices holding elements (the others' masks are never written)
 };
 
-template <bool kFix>
-__device__ __forceinline__ EmitIn emit_load(const uint8_t* ws, int num_layers, uint32_t T, uint32_t t, int lane)
+template <bool kFix, bool kBig>
+__device__ __forceinline__ EmitIn<kBig ? 2 : 1> emit_load(const KGroup& g, const uint32_t* tb, const uint8_t* ws,
+                                                         uint32_t T, uint32_t t, int lane)
 {
-    EmitIn in;
-    const uint4* sent = reinterpret_cast<const uint4*>(ws + sl_sent_offset(num_layers, T));
-    in.f = sent[(size_t)t * 32 + lane];
-    if (!kFix) in.ng = reinterpret_cast<const uint4*>(ws + sl_sign_offset(num_layers, T))[(size_t)t * 32 + lane];
-    else in.ng = make_uint4(0u, 0u, 0u, 0u);
-    in.pos = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(num_layers))[t];
+    constexpr int H = kBig ? 2 : 1;
+    EmitIn<H> in;
+    in.used = kBig ? big_slices_used(g.layer[layer_of_tile(tb, g.num_layers, t)], t) : kWarps;
+    const int hs = in.used > kWarps ? 2 : 1;  // groups holding elements
+    const uint4* sent = reinterpret_cast<const uint4*>(ws + sl_sent_offset(g.num_layers, T));
+    const uint4* sign = reinterpret_cast<const uint4*>(ws + sl_sign_offset(g.num_layers, T, kBig));
+#pragma unroll
+    for (int h = 0; h < H; ++h) {
+        const size_t i = ((size_t)t * H + h) * 32 + lane;
+        in.f[h] = h < hs ? sent[i] : make_uint4(0u, 0u, 0u, 0u);
+        in.ng[h] = (!kFix && h < hs) ? sign[i] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    in.pos = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(g.num_layers))[t];
     return in;
 }
 
-template <bool kFix>
-__global__ void __launch_bounds__(kEmitThreads, 5) slice_emit_kernel(const __grid_constant__ KGroup g,
+template <bool kFix, bool kBig>
+__global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(const __grid_constant__ KGroup g,
                                                                   uint8_t* __restrict__ ws)
 {
+    constexpr int H = kBig ? 2 : 1;
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
     __shared__ uint16_t lists[kEmitWarps][kListCap];
     for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) tb[e] = g.layer[e].tile_begin;
@@ -612,17 +982,16 @@ __global__ void __launch_bounds__(kEmitThreads, 5) slice_emit_kernel(const __gri
     const uint32_t NW = gridDim.x * kEmitWarps;
     uint32_t q = blockIdx.x * kEmitWarps + (threadIdx.x >> 5);
     if (q >= T) return;
-    const int w = lane >> 2;         // the lane's slice
-    const int cl0 = 8 * (lane & 3);  // its first compute lane
-    EmitIn cur = emit_load<kFix>(ws, g.num_layers, T, T - 1u - q, lane);
+    const int cl0 = 8 * (lane & 3);  // the lane's first compute lane
+    EmitIn<H> cur = emit_load<kFix, kBig>(g, tb, ws, T, T - 1u - q, lane);
     int l_cached = -1;
     float s = 0.0f;
     uint32_t status = 0;
     uint32_t* tile_tot = reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T));
     for (; q < T; q += NW) {
         const uint32_t t = T - 1u - q;
-        const EmitIn in = cur;
-        if (q + NW < T) cur = emit_load<kFix>(ws, g.num_layers, T, T - 1u - (q + NW), lane);
+        const EmitIn<H> in = cur;
+        if (q + NW < T) cur = emit_load<kFix, kBig>(g, tb, ws, T, T - 1u - (q + NW), lane);
         if (lane == 0) tile_tot[t] = 0u;  // the tile totals start the next call at zero
         const int l = layer_of_tile(tb, g.num_layers, t);
         const KLayer& ly = g.layer[l];
@@ -633,82 +1002,92 @@ __global__ void __launch_bounds__(kEmitThreads, 5) slice_emit_kernel(const __gri
             l_cached = l;
         }
         if (status != 0u) continue;  // a layer whose streaming pass did not complete
-        // the lane's eight masks in slot order, and its count
-        uint32_t m[8], ngm[8];
-        const uint32_t fw[4] = {in.f.x, in.f.y, in.f.z, in.f.w};
-        const uint32_t nw4[4] = {in.ng.x, in.ng.y, in.ng.z, in.ng.w};
-        uint32_t c = 0;
-#pragma unroll
-        for (int i = 0; i < 8; ++i) {
-            const int rot = seg_rot(cl0 + i);
-            m[i] = to_slot_order((fw[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
-            ngm[i] = kFix ? 0u : to_slot_order((nw4[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
-            c += __popc(m[i]);
-        }
-        uint32_t incl = c;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(kFull, incl, o);
-            if (lane >= o) incl += y;
-        }
-        const uint32_t n = __shfl_sync(kFull, incl, 31);
-        if (n == 0u) continue;
-        const Slice Sl = slice_in(ly, l, t, w);
-        const int x0 = (int)(Sl.a0 - Sl.ts) + kSeg * cl0;  // tile element of slot 0 of compute lane cl0
-        float* res = ly.residue + Sl.ts;
-        uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
-        for (uint32_t r0 = 0; r0 < n; r0 += kListCap) {
-            // list this round's elements: positions r0 .. r0 + kListCap - 1 of the tile
-            uint32_t li = incl - c;
+        uint64_t pos_h = in.pos;  // first code position of the group of slices
+#pragma unroll 1
+        for (int h = 0; h < H; ++h) {
+            // the lane's eight masks in slot order, and its count
+            uint32_t m[8], ngm[8];
+            const int w = kWarps * h + (lane >> 2);  // the lane's slice
+            // (selected, not indexed, to stay out of local memory; empty slices hold no codes)
+            const bool live = !kBig || w < in.used;
+            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
+            const uint4 fh = live ? (h ? in.f[H - 1] : in.f[0]) : z, nh = live ? (h ? in.ng[H - 1] : in.ng[0]) : z;
+            const uint32_t fw[4] = {fh.x, fh.y, fh.z, fh.w};
+            const uint32_t nw4[4] = {nh.x, nh.y, nh.z, nh.w};
+            uint32_t c = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                uint32_t mm = m[i];
-                while (mm) {
-                    const int b = __ffs(mm) - 1;
-                    mm &= mm - 1;
-                    if (li - r0 < (uint32_t)kListCap)
-                        lst[li - r0] = (uint16_t)((x0 + kSeg * i + b) | (((ngm[i] >> b) & 1u) << 15));
-                    ++li;
-                }
+                const int rot = seg_rot(cl0 + i);
+                m[i] = to_slot_order((fw[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
+                ngm[i] = kFix ? 0u : to_slot_order((nw4[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
+                c += __popc(m[i]);
             }
-            __syncwarp();
-            const uint32_t nr = min(n - r0, (uint32_t)kListCap);
-            const uint64_t pos0 = in.pos + r0;
-            if constexpr (kFix) {
-                for (uint32_t j0 = 0; j0 < nr; j0 += 32 * kFixBatch) {
-                    uint32_t e[kFixBatch];
-                    float v[kFixBatch];
+            uint32_t incl = c;
 #pragma unroll
-                    for (int k = 0; k < kFixBatch; ++k) {
-                        const uint32_t j = j0 + k * 32 + lane;
-                        e[k] = j < nr ? (uint32_t)lst[j] : 0xffffffffu;
-                    }
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(kFull, incl, o);
+                if (lane >= o) incl += y;
+            }
+            const uint32_t n = __shfl_sync(kFull, incl, 31);
+            if (n == 0u) continue;
+            const Slice Sl = kBig ? big_slice(ly, l, t, w) : slice_in(ly, l, t, w);
+            const int x0 = (int)(Sl.a0 - Sl.ts) + kSeg * cl0;  // tile element of slot 0 of compute lane cl0
+            float* res = ly.residue + Sl.ts;
+            uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
+            for (uint32_t r0 = 0; r0 < n; r0 += kListCap) {
+                // list this round's elements: positions r0 .. r0 + kListCap - 1 of the group
+                uint32_t li = incl - c;
 #pragma unroll
-                    for (int k = 0; k < kFixBatch; ++k)
-                        if (e[k] != 0xffffffffu) v[k] = ld_fill64(res + e[k]);
-#pragma unroll
-                    for (int k = 0; k < kFixBatch; ++k) {
-                        if (e[k] == 0xffffffffu) continue;
-                        const uint32_t neg = v[k] < 0.0f ? 1u : 0u;
-                        const uint32_t off = e[k] - __umulhi(e[k], ly.inv_len) * (uint32_t)ly.bin_len;  // e < 2^16: exact
-                        const uint32_t code = (off << 1) | neg;
-                        const uint64_t pos = pos0 + j0 + k * 32 + lane;
-                        if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
-                        else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
-                        res[e[k]] = neg ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
+                for (int i = 0; i < 8; ++i) {
+                    uint32_t mm = m[i];
+                    while (mm) {
+                        const int b = __ffs(mm) - 1;
+                        mm &= mm - 1;
+                        if (li - r0 < (uint32_t)kListCap)
+                            lst[li - r0] = (uint16_t)((x0 + kSeg * i + b) | (((ngm[i] >> b) & 1u) << 15));
+                        ++li;
                     }
                 }
-            } else {
-                for (uint32_t j = lane; j < nr; j += 32) {
-                    const uint32_t en = lst[j];
-                    const uint32_t x = en & 0x7fffu;
-                    const uint32_t off = x - __umulhi(x, ly.inv_len) * (uint32_t)ly.bin_len;
-                    const uint32_t code = (off << 1) | (en >> 15);
-                    if (ly.code_bytes == 1) codes[pos0 + j] = (uint8_t)code;
-                    else reinterpret_cast<uint16_t*>(codes)[pos0 + j] = (uint16_t)code;
+                __syncwarp();
+                const uint32_t nr = min(n - r0, (uint32_t)kListCap);
+                const uint64_t pos0 = pos_h + r0;
+                if constexpr (kFix) {
+                    for (uint32_t j0 = 0; j0 < nr; j0 += 32 * kFixBatch) {
+                        uint32_t e[kFixBatch];
+                        float v[kFixBatch];
+#pragma unroll
+                        for (int k = 0; k < kFixBatch; ++k) {
+                            const uint32_t j = j0 + k * 32 + lane;
+                            e[k] = j < nr ? (uint32_t)lst[j] : 0xffffffffu;
+                        }
+#pragma unroll
+                        for (int k = 0; k < kFixBatch; ++k)
+                            if (e[k] != 0xffffffffu) v[k] = ld_fill64(res + e[k]);
+#pragma unroll
+                        for (int k = 0; k < kFixBatch; ++k) {
+                            if (e[k] == 0xffffffffu) continue;
+                            const uint32_t neg = v[k] < 0.0f ? 1u : 0u;
+                            const uint32_t off = e[k] - __umulhi(e[k], ly.inv_len) * (uint32_t)ly.bin_len;  // e < 2^16: exact
+                            const uint32_t code = (off << 1) | neg;
+                            const uint64_t pos = pos0 + j0 + k * 32 + lane;
+                            if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
+                            else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
+                            res[e[k]] = neg ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
+                        }
+                    }
+                } else {
+                    for (uint32_t j = lane; j < nr; j += 32) {
+                        const uint32_t en = lst[j];
+                        const uint32_t x = en & 0x7fffu;
+                        const uint32_t off = x - __umulhi(x, ly.inv_len) * (uint32_t)ly.bin_len;
+                        const uint32_t code = (off << 1) | (en >> 15);
+                        if (ly.code_bytes == 1) codes[pos0 + j] = (uint8_t)code;
+                        else reinterpret_cast<uint16_t*>(codes)[pos0 + j] = (uint16_t)code;
+                    }
                 }
+                __syncwarp();  // the list is rewritten by the next round, group or tile
             }
-            __syncwarp();  // the list is rewritten by the next round or tile
+            pos_h += n;
         }
     }
 }
@@ -716,10 +1095,13 @@ __global__ void __launch_bounds__(kEmitThreads, 5) slice_emit_kernel(const __gri
 // ---------------------------------------------------------------- materialise (deferred fix-up)
 // Applies the corrections a call with a deferred fix-up left pending: for every
 // slot whose bit is set in its lane's sent mask, residue = fl32(G - sign(G) s) with
-// the layer's s from that call. One warp per (tile, slice).
+// the layer's s from that call. One warp per (tile, slice); the empty slices of
+// block-sliced tiles (whose masks are not written) are skipped.
+template <bool kBig>
 __global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const __grid_constant__ KGroup g,
                                                                          uint8_t* __restrict__ ws)
 {
+    constexpr int W = kBig ? kBigSlices : kWarps;  // slices per tile
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
     for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) tb[e] = g.layer[e].tile_begin;
     __syncthreads();
@@ -727,15 +1109,16 @@ __global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const _
     const int lane = threadIdx.x & 31;
     const uint32_t T = g.total_tiles;
     const uint16_t* sent = reinterpret_cast<const uint16_t*>(ws + sl_sent_offset(g.num_layers, T));
-    const uint64_t units = (uint64_t)T * kWarps;
+    const uint64_t units = (uint64_t)T * W;
     const uint64_t nw = (uint64_t)gridDim.x * (kEmitThreads / 32);
     for (uint64_t u = (uint64_t)blockIdx.x * (kEmitThreads / 32) + (threadIdx.x >> 5); u < units; u += nw) {
-        const uint32_t t = (uint32_t)(u / kWarps);
-        const int w = (int)(u % kWarps);
-        const uint32_t f = to_slot_order(sent[((size_t)t * kWarps + w) * 32 + lane], seg_rot(lane));
-        if (!f) continue;
+        const uint32_t t = (uint32_t)(u / W);
+        const int w = (int)(u % W);
         const int l = layer_of_tile(tb, g.num_layers, t);
-        const Slice Sl = slice_in(g.layer[l], l, t, w);
+        const Slice Sl = kBig ? big_slice(g.layer[l], l, t, w) : slice_in(g.layer[l], l, t, w);
+        if (kBig && Sl.we1 <= Sl.we0) continue;
+        const uint32_t f = to_slot_order(sent[((size_t)t * W + w) * 32 + lane], seg_rot(lane));
+        if (!f) continue;
         const float s = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(l))->result.s;
         float* res = g.layer[l].residue + Sl.a0 + kSeg * lane;
 #pragma unroll
@@ -746,12 +1129,14 @@ __global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const _
 
 struct SlicedDevice {
     int sms = 0;
-    uint32_t smem_set[4] = {0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per variant
-    int emit_occ[2] = {0, 0};             // resident CTAs per SM of the emitting kernel (deferred, eager)
+    uint32_t smem_set[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per variant
+    int emit_occ[4] = {0, 0, 0, 0};                   // resident CTAs per SM of the emitting kernel variants
 };
 SlicedDevice g_sl_dev[64];
 
 constexpr int kStages = 2;  // per-warp stages; with 3 CTAs per SM (74 registers) measured faster than 3 stages with 2
+constexpr int kBigStages = 2;
+
 
 }  // namespace
 
@@ -774,24 +1159,44 @@ cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t strea
         e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const SlicePlan P = slice_plan(g.d_size, kStages, g.num_layers);
     void (*kern)(KGroup, uint8_t*);
-    if (g.local_selection) kern = g.lazy ? slice_kernel<kStages, true, true> : slice_kernel<kStages, false, true>;
-    else kern = g.lazy ? slice_kernel<kStages, true, false> : slice_kernel<kStages, false, false>;
-    const int ki = (g.lazy ? 1 : 0) + (g.local_selection ? 2 : 0);
-    if (P.total > di.smem_set[ki]) {
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)P.total);
+    uint32_t smem = 0, threads = 0;
+    const int ki = (g.lazy ? 1 : 0) + (g.local_selection ? 2 : 0) + (g.big ? 4 : 0);
+    if (g.big) {
+        // one warp per slice of the widest tile: bins_per_tile bins (or the layer), plus
+        // up to 3 alignment slots unless every tile starts on a 16-byte boundary
+        int W = 1;
+        for (int l = 0; l < g.num_layers; ++l) {
+            const KLayer& ly = g.layer[l];
+            const long long tl = (long long)ly.bins_per_tile * ly.bin_len < ly.n ? (long long)ly.bins_per_tile * ly.bin_len : ly.n;
+            const long long off = (ly.num_tiles > 1 && (ly.bin_len & 3)) ? 3 : 0;
+            const int w = (int)((off + tl + kSlots - 1) / kSlots);
+            W = w > W ? w : W;
+        }
+        if (W > kBigSlices) return cudaErrorInvalidValue;
+        smem = big_plan(g.d_size, kBigStages, g.num_layers, W).total;
+        threads = (uint32_t)W * 32u;
+        if (g.local_selection) kern = g.lazy ? block_kernel<kBigStages, true, true> : block_kernel<kBigStages, false, true>;
+        else kern = g.lazy ? block_kernel<kBigStages, true, false> : block_kernel<kBigStages, false, false>;
+    } else {
+        smem = slice_plan(g.d_size, kStages, g.num_layers).total;
+        threads = kThreads;
+        if (g.local_selection) kern = g.lazy ? slice_kernel<kStages, true, true> : slice_kernel<kStages, false, true>;
+        else kern = g.lazy ? slice_kernel<kStages, true, false> : slice_kernel<kStages, false, false>;
+    }
+    if (smem > di.smem_set[ki]) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        di.smem_set[ki] = P.total;
+        di.smem_set[ki] = smem;
     }
     int occ = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kThreads, P.total);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, (int)threads, smem);
     if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const long long cap = (long long)di.sms * occ;
     const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
     if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess) return e;
-    kern<<<grid, kThreads, P.total, stream>>>(g, static_cast<uint8_t*>(ws));
+    kern<<<grid, threads, smem, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
     uint32_t max_tiles = 0;  // the largest layer sets the chunks per layer
@@ -800,8 +1205,10 @@ cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t strea
     slice_finalize_kernel<<<fgrid, kFinThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // persistent: as many CTAs as are resident at once, each warp a run of tiles
-    void (*ekern)(KGroup, uint8_t*) = g.lazy ? slice_emit_kernel<false> : slice_emit_kernel<true>;
-    int& eocc = di.emit_occ[g.lazy ? 0 : 1];
+    void (*ekern)(KGroup, uint8_t*);
+    if (g.big) ekern = g.lazy ? slice_emit_kernel<false, true> : slice_emit_kernel<true, true>;
+    else ekern = g.lazy ? slice_emit_kernel<false, false> : slice_emit_kernel<true, false>;
+    int& eocc = di.emit_occ[(g.lazy ? 0 : 1) + (g.big ? 2 : 0)];
     if (eocc == 0) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eocc, ekern, kEmitThreads, 0);
         if (e != cudaSuccess) return e;
@@ -827,11 +1234,12 @@ cudaError_t launch_materialize_sliced(const KGroup& g, void* ws, cudaStream_t st
         e = cudaDeviceGetAttribute(&di.sms, cudaDevAttrMultiProcessorCount, dev);
         if (e != cudaSuccess) return e;
     }
-    const uint64_t units = (uint64_t)g.total_tiles * kWarps;
+    const uint64_t units = (uint64_t)g.total_tiles * (g.big ? kBigSlices : kWarps);
     const uint64_t blocks_needed = (units + kEmitThreads / 32 - 1) / (kEmitThreads / 32);
     const uint64_t cap = (uint64_t)di.sms * 8;
     const uint32_t grid = (uint32_t)(blocks_needed < cap ? blocks_needed : cap);
-    slice_materialize_kernel<<<grid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    if (g.big) slice_materialize_kernel<true><<<grid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+    else slice_materialize_kernel<false><<<grid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // the corrections are applied: the next call must not apply them again
     return cudaMemsetAsync(static_cast<uint8_t*>(ws) + offsetof(Ctl, pending), 0, sizeof(uint32_t), stream);

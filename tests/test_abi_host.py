@@ -71,14 +71,26 @@ def test_sliced_workspace_layout(n, L):
     ac.adacomp_free(h)
 
 
-@pytest.mark.parametrize("n,L", [(1_000_000, 5000), (77_777, 7), (300_007, 510)])
+@pytest.mark.parametrize("n,L", [(77_777, 7), (100_003, 4), (8191, 8192), (250_000, 8190)])
 def test_lookback_workspace_layout(n, L):
-    """Other bin lengths: control block, layer block, a u64 descriptor and a u64
-    code offset per tile; the deferred fix-up adds a 512-byte mask per tile."""
+    """L_T < 16 and L_T > 8189: control block, layer block, a u64 descriptor and a
+    u64 code offset per tile; the deferred fix-up adds a 512-byte mask per tile."""
     T = _tiles(n, L)
     h = ac.adacomp_init_layer(n, L, ac.F32)
     assert h.compress_ws_bytes == 64 + 2112 + 16 * T
     assert ac.adacomp_set_lazy_fixup(h, True) == 64 + 2112 + 16 * T + 512 * T
+    ac.adacomp_free(h)
+
+
+@pytest.mark.parametrize("n,L", [(1_000_000, 5000), (300_007, 510), (40_000, 4096), (4095, 4097), (10, 8189)])
+def test_block_sliced_workspace_layout(n, L):
+    """510 <= L_T <= 8189: the sliced layout with sixteen 512-slot slices per tile,
+    i.e. two 1024-byte masks per tile; the deferred fix-up needs no more."""
+    T = _tiles(n, L)
+    expect = 64 + 2112 + _pad16(8 * T) + _pad16(4 * T) + 2048 * T
+    h = ac.adacomp_init_layer(n, L, ac.F32)
+    assert h.compress_ws_bytes == expect
+    assert ac.adacomp_set_lazy_fixup(h, True) == expect
     ac.adacomp_free(h)
 
 
@@ -92,6 +104,11 @@ def test_group_workspace_takes_the_lookback_layout_when_mixed():
     T2 = T + _tiles(20_000, 5000)
     h2 = ac.adacomp_init_group(ns2, Ls2, [ac.F32] * 3)
     assert h2.compress_ws_bytes == 64 + 3 * 2112 + 16 * T2
+    # all bins of 510 .. 8189: the block-sliced layout
+    ns3, Ls3 = [20_000, 50_000], [5000, 600]
+    T3 = sum(_tiles(n, L) for n, L in zip(ns3, Ls3))
+    h3 = ac.adacomp_init_group(ns3, Ls3, [ac.F32] * 2)
+    assert h3.compress_ws_bytes == 64 + 2 * 2112 + _pad16(8 * T3) + _pad16(4 * T3) + 2048 * T3
 
 
 @pytest.mark.parametrize("n,L,dt", [(0, 4, 0), (-5, 4, 0), (10, 0, 0), (10, 8193, 0), (10, 4, 2)])

@@ -60,7 +60,11 @@ SHAPES = [(1, 1), (2, 2), (7, 3), (10, 4), (1000, 1), (5000, 2), (123457, 7), (9
           (100003, 50), (200000, 63), (65537, 64), (1000001, 500), (300000, 5000),
           (250000, 8192), (40000, 4096), (4095, 4097), (8191, 8192),
           # more warp-slice shapes: 31, 16, 25 and 5 bins per warp
-          (77777, 16), (90001, 30), (33333, 20), (1000003, 100)]
+          (77777, 16), (90001, 30), (33333, 20), (1000003, 100),
+          # block-sliced tiles: 8 bins of 510 (the shortest), 3 bins of 1365 (tiles off the
+          # 16-byte grid), one bin of 4094, 6000 and 8189 (the longest: 16 slices with the
+          # alignment slots), ragged ends
+          (300007, 510), (123457, 1365), (99999, 4094), (50001, 6000), (65000, 8189), (2000003, 2048)]
 
 
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
@@ -180,11 +184,12 @@ def test_checkpoint_resume_is_bit_identical(tmp_path):
     assert msg_a.tobytes() == msg_c.tobytes()
 
 
-def test_lookback_wait_times_out_with_a_status():
-    """A tile that never publishes its look-back descriptor: the bounded waits of the
-    tiles after it end, the layer reports ADACOMP_ERR_TIMEOUT, and the context stays
-    usable for a normal call afterwards."""
-    n, L = 400_000, 500
+@pytest.mark.parametrize("L", [7, 500, 5000], ids=["lookback", "warp-sliced", "block-sliced"])
+def test_wait_times_out_with_a_status(L):
+    """A tile whose data is never requested (warp- and block-sliced paths) or whose
+    look-back descriptor is never published: the bounded waits end, the layer reports
+    ADACOMP_ERR_TIMEOUT, and the context stays usable for a normal call afterwards."""
+    n = 400_000
     layer = GpuLayer(n, L, ac.F32)
     ac.adacomp_set_timeout_ns(layer.h, 20_000_000)  # 20 ms
     ac.adacomp_set_fault_injection(layer.h, 3)      # tile 3 never publishes

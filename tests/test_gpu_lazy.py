@@ -59,7 +59,8 @@ def _run(shapes, steps, bf16=False, materialize_at=()):
 
 
 @pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
-@pytest.mark.parametrize("n,L", [(1_000_003, 50), (500_001, 500), (300_007, 100), (77_777, 16), (4_001, 63)])
+@pytest.mark.parametrize("n,L", [(1_000_003, 50), (500_001, 500), (300_007, 100), (77_777, 16), (4_001, 63),
+                                 (500_001, 5000), (123_457, 1365), (65_000, 8189)])
 def test_lazy_single_layer(n, L, bf16):
     _run([(n, L)], steps=4, bf16=bf16, materialize_at=(1,))
 
@@ -67,6 +68,10 @@ def test_lazy_single_layer(n, L, bf16):
 def test_lazy_group_mixes_deferred_and_eager_layers():
     # L_T = 4 and 5000 take block-wide tiles and are fixed up eagerly; the rest defer
     _run([(200_000, 50), (50_003, 4), (123_457, 500), (400_000, 5000), (4_096, 50)], steps=3)
+
+
+def test_block_sliced_group_with_a_materialise_between_steps():
+    _run([(400_000, 5000), (123_457, 1365), (77_777, 600)], steps=4, materialize_at=(1,))
 
 
 def test_resnet50_lazy_full_size():
