@@ -146,6 +146,7 @@ def algorithmic_bytes(layers, nnz, K):
 KERNEL_SOURCES = {
     "slice_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "slice_emit_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
+    "block_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "compress_kernel": ("compress.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "accumulate_kernel": ("decode.cu", "adacomp_internal.cuh"),
     "sparse_accumulate_kernel": ("decode.cu", "adacomp_internal.cuh"),
@@ -519,8 +520,14 @@ def run_device(args, rank, world):
     bins_total = sum(-(-ly.numel // ly.bin_len) for ly in lay_k) * args.steps
 
     peak, peak_kind = measured_hbm_gbs()
-    # the streaming kernel of the launch: the sliced path when every bin length is 16..509
-    stream_kernel = "slice_kernel" if all(16 <= ly.bin_len <= 509 for ly in layers) else "compress_kernel"
+    # the streaming kernel of the launch: warp-sliced when every bin length is 16..509,
+    # block-sliced when every one is 510..8189, else the look-back kernel
+    if all(16 <= ly.bin_len <= 509 for ly in layers):
+        stream_kernel = "slice_kernel"
+    elif all(510 <= ly.bin_len <= 8189 for ly in layers):
+        stream_kernel = "block_kernel"
+    else:
+        stream_kernel = "compress_kernel"
     k1_ms_per_launch = statistics.mean(k1)
     k1_bytes_per_launch = k1_bytes / len(k1)
     achieved = k1_bytes_per_launch / (k1_ms_per_launch * 1e-3) / 1e9

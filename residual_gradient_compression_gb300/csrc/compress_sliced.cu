@@ -910,20 +910,17 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
 // wrote last are the likeliest to be still in L2); a warp loads its next tile's masks
 // and code offset before it emits the current tile.
 // Emit lane L covers slice L >> 2, compute lanes 8 (L & 3) .. 8 (L & 3) + 7: one
-// 16-byte load of their sent masks (and, with the fix-up deferred, one of their sign
-// masks). The masks are stored in the streaming kernel's register order and are
-// brought back to slot order here. An exclusive warp scan of the lanes' popcounts
-// places each lane's sent elements, in element order (which is code order), in a
-// per-warp list in shared memory; the warp then walks the list with consecutive lanes
-// on consecutive codes:
-//   kFix: kFixBatch elements per lane at a time, all residue loads issued first (with
-//         a 64-byte L2 fill size: a scattered 4-byte load otherwise fills a whole
-//         128-byte line), then the code ((element - its bin's first element) << 1) |
-//         (G < 0) and the residue fl32(G - sign(G) s);
-//   otherwise the list entries carry the sign bit, and only the codes are written.
-// A tile with more than kListCap sent elements is listed and walked in rounds. The
-// tiles' code totals (read by the finalising kernel) are cleared here for the next
-// call.
+// 16-byte load of their sent masks. The masks are stored in the streaming kernel's
+// register order and are brought back to slot order here. An exclusive warp scan of
+// the lanes' popcounts places each lane's sent elements, in element order (which is
+// code order), in a per-warp list in shared memory; the warp then walks the list
+// with consecutive lanes on consecutive codes, kFixBatch elements per lane at a time:
+// all residue loads issued first (with a 64-byte L2 fill size: a scattered 4-byte
+// load otherwise fills a whole 128-byte line), then the code ((element - its bin's
+// first element) << 1) | (G < 0) and the residue fl32(G - sign(G) s). A tile with more
+// than kListCap sent elements is listed and walked in rounds. The tiles' code totals
+// (read by the finalising kernel) are cleared here for the next call. (With the
+// fix-up deferred, slice_codes_kernel below writes the codes instead.)
 constexpr int kEmitThreads = 256;
 constexpr int kEmitWarps = kEmitThreads / 32;
 constexpr int kListCap = 1024;
@@ -938,16 +935,15 @@ __device__ __forceinline__ float ld_fill64(const float* p)
 
 // The inputs of one tile's emission, loaded a tile ahead: per group of eight slices
 // (one for warp-sliced tiles, two for block-sliced ones) the sent masks of the lane's
-// eight compute lanes (register order) and their sign masks (deferred fix-up only).
+// eight compute lanes (register order).
 template <int H>
 struct EmitIn {
     uint4 f[H];
-    uint4 ng[H];
     uint64_t pos;   // the tile's first code position in its message
     int used;       // block-sliced tiles: slices holding elements (the others' masks are never written)
 };
 
-template <bool kFix, bool kBig>
+template <bool kBig>
 __device__ __forceinline__ EmitIn<kBig ? 2 : 1> emit_load(const KGroup& g, const uint32_t* tb, const uint8_t* ws,
                                                          uint32_t T, uint32_t t, int lane)
 {
@@ -956,20 +952,16 @@ __device__ __forceinline__ EmitIn<kBig ? 2 : 1> emit_load(const KGroup& g, const
     in.used = kBig ? big_slices_used(g.layer[layer_of_tile(tb, g.num_layers, t)], t) : kWarps;
     const int hs = in.used > kWarps ? 2 : 1;  // groups holding elements
     const uint4* sent = reinterpret_cast<const uint4*>(ws + sl_sent_offset(g.num_layers, T));
-    const uint4* sign = reinterpret_cast<const uint4*>(ws + sl_sign_offset(g.num_layers, T, kBig));
 #pragma unroll
-    for (int h = 0; h < H; ++h) {
-        const size_t i = ((size_t)t * H + h) * 32 + lane;
-        in.f[h] = h < hs ? sent[i] : make_uint4(0u, 0u, 0u, 0u);
-        in.ng[h] = (!kFix && h < hs) ? sign[i] : make_uint4(0u, 0u, 0u, 0u);
-    }
+    for (int h = 0; h < H; ++h)
+        in.f[h] = h < hs ? sent[((size_t)t * H + h) * 32 + lane] : make_uint4(0u, 0u, 0u, 0u);
     in.pos = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(g.num_layers))[t];
     return in;
 }
 
-template <bool kFix, bool kBig>
+template <bool kBig>
 __global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(const __grid_constant__ KGroup g,
-                                                                  uint8_t* __restrict__ ws)
+                                                                             uint8_t* __restrict__ ws)
 {
     constexpr int H = kBig ? 2 : 1;
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
@@ -983,7 +975,7 @@ __global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(
     uint32_t q = blockIdx.x * kEmitWarps + (threadIdx.x >> 5);
     if (q >= T) return;
     const int cl0 = 8 * (lane & 3);  // the lane's first compute lane
-    EmitIn<H> cur = emit_load<kFix, kBig>(g, tb, ws, T, T - 1u - q, lane);
+    EmitIn<H> cur = emit_load<kBig>(g, tb, ws, T, T - 1u - q, lane);
     int l_cached = -1;
     float s = 0.0f;
     uint32_t status = 0;
@@ -991,7 +983,7 @@ __global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(
     for (; q < T; q += NW) {
         const uint32_t t = T - 1u - q;
         const EmitIn<H> in = cur;
-        if (q + NW < T) cur = emit_load<kFix, kBig>(g, tb, ws, T, T - 1u - (q + NW), lane);
+        if (q + NW < T) cur = emit_load<kBig>(g, tb, ws, T, T - 1u - (q + NW), lane);
         if (lane == 0) tile_tot[t] = 0u;  // the tile totals start the next call at zero
         const int l = layer_of_tile(tb, g.num_layers, t);
         const KLayer& ly = g.layer[l];
@@ -1005,21 +997,17 @@ __global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(
         uint64_t pos_h = in.pos;  // first code position of the group of slices
 #pragma unroll 1
         for (int h = 0; h < H; ++h) {
-            // the lane's eight masks in slot order, and its count
-            uint32_t m[8], ngm[8];
             const int w = kWarps * h + (lane >> 2);  // the lane's slice
             // (selected, not indexed, to stay out of local memory; empty slices hold no codes)
             const bool live = !kBig || w < in.used;
-            const uint4 z = make_uint4(0u, 0u, 0u, 0u);
-            const uint4 fh = live ? (h ? in.f[H - 1] : in.f[0]) : z, nh = live ? (h ? in.ng[H - 1] : in.ng[0]) : z;
+            const uint4 fh = live ? (h ? in.f[H - 1] : in.f[0]) : make_uint4(0u, 0u, 0u, 0u);
             const uint32_t fw[4] = {fh.x, fh.y, fh.z, fh.w};
-            const uint32_t nw4[4] = {nh.x, nh.y, nh.z, nh.w};
+            // the lane's eight masks in slot order, and its count
+            uint32_t m[8];
             uint32_t c = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                const int rot = seg_rot(cl0 + i);
-                m[i] = to_slot_order((fw[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
-                ngm[i] = kFix ? 0u : to_slot_order((nw4[i >> 1] >> (16 * (i & 1))) & 0xffffu, rot);
+                m[i] = to_slot_order((fw[i >> 1] >> (16 * (i & 1))) & 0xffffu, seg_rot(cl0 + i));
                 c += __popc(m[i]);
             }
             uint32_t incl = c;
@@ -1043,52 +1031,143 @@ __global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(
                     while (mm) {
                         const int b = __ffs(mm) - 1;
                         mm &= mm - 1;
-                        if (li - r0 < (uint32_t)kListCap)
-                            lst[li - r0] = (uint16_t)((x0 + kSeg * i + b) | (((ngm[i] >> b) & 1u) << 15));
+                        if (li - r0 < (uint32_t)kListCap) lst[li - r0] = (uint16_t)(x0 + kSeg * i + b);
                         ++li;
                     }
                 }
                 __syncwarp();
                 const uint32_t nr = min(n - r0, (uint32_t)kListCap);
                 const uint64_t pos0 = pos_h + r0;
-                if constexpr (kFix) {
-                    for (uint32_t j0 = 0; j0 < nr; j0 += 32 * kFixBatch) {
-                        uint32_t e[kFixBatch];
-                        float v[kFixBatch];
+                for (uint32_t j0 = 0; j0 < nr; j0 += 32 * kFixBatch) {
+                    uint32_t e[kFixBatch];
+                    float v[kFixBatch];
 #pragma unroll
-                        for (int k = 0; k < kFixBatch; ++k) {
-                            const uint32_t j = j0 + k * 32 + lane;
-                            e[k] = j < nr ? (uint32_t)lst[j] : 0xffffffffu;
-                        }
-#pragma unroll
-                        for (int k = 0; k < kFixBatch; ++k)
-                            if (e[k] != 0xffffffffu) v[k] = ld_fill64(res + e[k]);
-#pragma unroll
-                        for (int k = 0; k < kFixBatch; ++k) {
-                            if (e[k] == 0xffffffffu) continue;
-                            const uint32_t neg = v[k] < 0.0f ? 1u : 0u;
-                            const uint32_t off = e[k] - __umulhi(e[k], ly.inv_len) * (uint32_t)ly.bin_len;  // e < 2^16: exact
-                            const uint32_t code = (off << 1) | neg;
-                            const uint64_t pos = pos0 + j0 + k * 32 + lane;
-                            if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
-                            else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
-                            res[e[k]] = neg ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
-                        }
+                    for (int k = 0; k < kFixBatch; ++k) {
+                        const uint32_t j = j0 + k * 32 + lane;
+                        e[k] = j < nr ? (uint32_t)lst[j] : 0xffffffffu;
                     }
-                } else {
-                    for (uint32_t j = lane; j < nr; j += 32) {
-                        const uint32_t en = lst[j];
-                        const uint32_t x = en & 0x7fffu;
-                        const uint32_t off = x - __umulhi(x, ly.inv_len) * (uint32_t)ly.bin_len;
-                        const uint32_t code = (off << 1) | (en >> 15);
-                        if (ly.code_bytes == 1) codes[pos0 + j] = (uint8_t)code;
-                        else reinterpret_cast<uint16_t*>(codes)[pos0 + j] = (uint16_t)code;
+#pragma unroll
+                    for (int k = 0; k < kFixBatch; ++k)
+                        if (e[k] != 0xffffffffu) v[k] = ld_fill64(res + e[k]);
+#pragma unroll
+                    for (int k = 0; k < kFixBatch; ++k) {
+                        if (e[k] == 0xffffffffu) continue;
+                        const uint32_t neg = v[k] < 0.0f ? 1u : 0u;
+                        const uint32_t off = e[k] - __umulhi(e[k], ly.inv_len) * (uint32_t)ly.bin_len;  // e < 2^16: exact
+                        const uint32_t code = (off << 1) | neg;
+                        const uint64_t pos = pos0 + j0 + k * 32 + lane;
+                        if (ly.code_bytes == 1) codes[pos] = (uint8_t)code;
+                        else reinterpret_cast<uint16_t*>(codes)[pos] = (uint16_t)code;
+                        res[e[k]] = neg ? __fadd_rn(v[k], s) : __fsub_rn(v[k], s);
                     }
                 }
                 __syncwarp();  // the list is rewritten by the next round, group or tile
             }
             pos_h += n;
         }
+    }
+}
+
+// ---------------------------------------------------------------- codes only (deferred fix-up)
+// With the fix-up deferred, emitting touches no residue: the codes follow from the
+// sent and sign masks alone. One warp per tile, every tile at once (no persistence:
+// there are no residue lines to find in L2). The tile's masks are read as 32-bit
+// words, a word holding two adjacent compute lanes' 16 slots (so the words, in
+// order, cover the tile's slots in order): in each round lane i takes word
+// 32 r + i, brings its two halves to slot order, and writes the codes of its set
+// slots ((element - its bin's first element) << 1 | sign) at consecutive positions
+// from the tile's offset plus the codes of the words before it (a warp scan).
+// A word of two compute lanes' masks (cl, cl + 1, cl even: both have the same
+// chunk rotation) from register order to slot order: nibble k of each half moves to
+// k ^ rot.
+__device__ __forceinline__ uint32_t word_to_slot_order(uint32_t x, int rot)
+{
+    const uint32_t n = ((x << 4) & 0xf0f0f0f0u) | ((x >> 4) & 0x0f0f0f0fu);  // rot bit 0: swap nibble pairs
+    x = (rot & 1) ? n : x;
+    const uint32_t b = __byte_perm(x, 0u, 0x2301);                         // rot bit 1: swap bytes per half
+    return (rot & 2) ? b : x;
+}
+
+template <bool kBig>
+__global__ void __launch_bounds__(kEmitThreads) slice_codes_kernel(const __grid_constant__ KGroup g,
+                                                                   uint8_t* __restrict__ ws)
+{
+    constexpr int W = kBig ? kBigSlices : kWarps;  // slices per tile
+    constexpr int R = W / 2;                       // rounds: 16 words per slice, 32 per round
+    __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
+    __shared__ uint32_t st[kMaxGroup];  // each layer's status
+    for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) {
+        tb[e] = g.layer[e].tile_begin;
+        st[e] = reinterpret_cast<const LayerWs*>(ws + ws_layer_offset(e))->result.status;
+    }
+    __syncthreads();
+    const int lane = threadIdx.x & 31;
+    const uint32_t T = g.total_tiles;
+    const uint32_t t = blockIdx.x * kEmitWarps + (threadIdx.x >> 5);
+    if (t >= T) return;
+    const uint32_t* sent = reinterpret_cast<const uint32_t*>(ws + sl_sent_offset(g.num_layers, T)) + (size_t)t * W * 16;
+    const uint32_t* sign = reinterpret_cast<const uint32_t*>(ws + sl_sign_offset(g.num_layers, T, kBig)) + (size_t)t * W * 16;
+    const int l = layer_of_tile(tb, g.num_layers, t);
+    const KLayer& ly = g.layer[l];
+    // the tile: its first bin and element, bins and elements
+    const uint32_t fb = (t - ly.tile_begin) * ly.bins_per_tile;
+    const int nb = (int)min(ly.bins_per_tile, ly.nbins - fb);
+    const int64_t ts = (int64_t)fb * ly.bin_len;
+    const int used = kBig ? (int)(((int)(ts & 3) + (int)min((int64_t)nb * ly.bin_len, ly.n - ts) + kSlots - 1) / kSlots) : W;
+    uint32_t f[R], ng[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const bool live = (r * 32 + lane) / 16 < used;  // the masks of empty slices are never written
+        f[r] = live ? sent[r * 32 + lane] : 0u;
+        ng[r] = live ? sign[r * 32 + lane] : 0u;
+    }
+    const uint64_t pos0 = reinterpret_cast<const uint64_t*>(ws + sl_excl_offset(g.num_layers))[t];
+    if (lane == 0) reinterpret_cast<uint32_t*>(ws + sl_tot_offset(g.num_layers, T))[t] = 0u;  // zero for the next call
+    if (st[l] != 0u) return;  // a layer whose streaming pass did not complete
+    const bool wide = ly.code_bytes == 2;
+    uint8_t* codes = ly.msg + 8 + 2ull * ly.nbins;
+    const int cl0 = 2 * (lane & 15);  // the word's first compute lane
+    const int rot = seg_rot(cl0);
+    const uint32_t L = (uint32_t)ly.bin_len, inv = ly.inv_len;
+    const int ts3 = (int)(ts & 3);
+    uint64_t base = pos0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t fs = word_to_slot_order(f[r], rot);
+        const uint32_t c = __popc(fs);
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t n = __shfl_sync(kFull, incl, 31);
+        if (c) {
+            const uint32_t sg = word_to_slot_order(ng[r], rot);
+            const int w = 2 * r + (lane >> 4);  // the word's slice
+            // tile element of slot 0 of the slice: from the 16-byte boundary at or before
+            // its first element (warp slices: bins w * bpw ..; block slices: 512 w slots)
+            int rel;
+            if (kBig) {
+                rel = kSlots * w - ts3;
+            } else {
+                const int we0 = min(nb, w * (int)ly.bpw) * (int)L;
+                rel = we0 - (int)((ts + we0) & 3);
+            }
+            const uint32_t x0 = (uint32_t)(rel + kSeg * cl0);  // tile element of the word's bit 0 (bit 0 set: >= 0)
+            uint8_t* cp = codes + (base + (incl - c)) * (wide ? 2u : 1u);
+            uint32_t mm = fs, j = 0;
+            while (mm) {
+                const int b = __ffs(mm) - 1;
+                mm &= mm - 1;
+                const uint32_t x = x0 + (uint32_t)b;  // tile element, < 2^16
+                const uint32_t code = ((x - __umulhi(x, inv) * L) << 1) | ((sg >> b) & 1u);
+                if (wide) reinterpret_cast<uint16_t*>(cp)[j] = (uint16_t)code;
+                else cp[j] = (uint8_t)code;
+                ++j;
+            }
+        }
+        base += n;
     }
 }
 
@@ -1130,7 +1209,7 @@ __global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const _
 struct SlicedDevice {
     int sms = 0;
     uint32_t smem_set[8] = {0, 0, 0, 0, 0, 0, 0, 0};  // largest dynamic shared memory opted in so far, per variant
-    int emit_occ[4] = {0, 0, 0, 0};                   // resident CTAs per SM of the emitting kernel variants
+    int emit_occ[2] = {0, 0};                         // resident CTAs per SM of the emitting kernel (warp-, block-sliced)
 };
 SlicedDevice g_sl_dev[64];
 
@@ -1204,11 +1283,17 @@ cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t strea
     const dim3 fgrid((max_tiles + kFinThreads - 1) / kFinThreads, (unsigned)g.num_layers);
     slice_finalize_kernel<<<fgrid, kFinThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if (g.lazy) {  // codes only: one warp per tile
+        const uint32_t cgrid = (g.total_tiles + kEmitWarps - 1) / kEmitWarps;
+        if (g.big) slice_codes_kernel<true><<<cgrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+        else slice_codes_kernel<false><<<cgrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
+        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        if (ev_after) e = cudaEventRecord(ev_after, stream);
+        return e;
+    }
     // persistent: as many CTAs as are resident at once, each warp a run of tiles
-    void (*ekern)(KGroup, uint8_t*);
-    if (g.big) ekern = g.lazy ? slice_emit_kernel<false, true> : slice_emit_kernel<true, true>;
-    else ekern = g.lazy ? slice_emit_kernel<false, false> : slice_emit_kernel<true, false>;
-    int& eocc = di.emit_occ[(g.lazy ? 0 : 1) + (g.big ? 2 : 0)];
+    void (*ekern)(KGroup, uint8_t*) = g.big ? slice_emit_kernel<true> : slice_emit_kernel<false>;
+    int& eocc = di.emit_occ[g.big ? 1 : 0];
     if (eocc == 0) {
         e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&eocc, ekern, kEmitThreads, 0);
         if (e != cudaSuccess) return e;
