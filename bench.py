@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--workload", default="flat100m",
                    choices=["resnet50", "fc400k", "lstm_fc", "gpt1p3b", "flat100m"])
     p.add_argument("--bin-len", type=int, default=500, help="L_T for gpt1p3b")
+    p.add_argument("--layers", type=int, default=0,
+                   help="only the first N layers of the workload (a smaller case, for profiling)")
     p.add_argument("--learners", type=int, default=16, help="K for flat100m")
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="oracle sample budget")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -102,9 +104,8 @@ def max_over_ranks(x: float, world: int) -> float:
 
 # ---------------------------------------------------------------- workloads
 def workload_layers(args):
-    if args.workload == "gpt1p3b":
-        return wl.layers("gpt1p3b", args.bin_len)
-    return wl.layers(args.workload)
+    ls = wl.layers("gpt1p3b", args.bin_len) if args.workload == "gpt1p3b" else wl.layers(args.workload)
+    return ls[:args.layers] if args.layers else ls
 
 
 def learners(args):
@@ -146,6 +147,7 @@ def algorithmic_bytes(layers, nnz, K):
 KERNEL_SOURCES = {
     "slice_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "slice_emit_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
+    "slice_codes_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "block_kernel": ("compress_sliced.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "compress_kernel": ("compress.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "accumulate_kernel": ("decode.cu", "adacomp_internal.cuh"),
@@ -173,9 +175,12 @@ def measured_hbm_gbs():
         return FALLBACK_HBM_GBS, "fallback"
 
 
-def profiled_traffic(kernel: str, workload: str):
+def profiled_traffic(kernel: str, workload: str, bytes_per_launch: float):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on the
-    current kernel sources; None otherwise."""
+    current kernel sources; None otherwise. A summary taken on a smaller case of the
+    workload (one whose launch is too large to capture) is scaled to this launch by
+    the ratio of algorithmic bytes, the traffic of a streaming kernel growing in
+    proportion to the elements it streams."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     try:
         with open(path) as f:
@@ -184,7 +189,10 @@ def profiled_traffic(kernel: str, workload: str):
         return None
     if rec.get("source_sha") != source_hash(kernel):
         return None
-    return rec.get("dram_bytes_per_launch")
+    dram = rec.get("dram_bytes_per_launch")
+    if dram is not None and rec.get("scale_by_algorithmic_bytes"):
+        dram *= bytes_per_launch / rec["algorithmic_bytes_per_launch"]
+    return dram
 
 
 # ---------------------------------------------------------------- clocks
@@ -555,7 +563,7 @@ def run_device(args, rank, world):
         "roofline": {"kernel": stream_kernel, "bound": "hbm", "achieved": achieved, "peak": peak,
                      "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                      "frac_nominal": achieved / NOMINAL_HBM_GBS,
-                     "traffic": profiled_traffic(stream_kernel, args.workload),
+                     "traffic": profiled_traffic(stream_kernel, args.workload, k1_bytes_per_launch),
                      "bytes_per_launch": k1_bytes_per_launch, "ms_per_launch": k1_ms_per_launch},
         "gpu_launches": run.launches_per_step() * args.steps,
         "clocks": clocks,

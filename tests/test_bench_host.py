@@ -66,9 +66,21 @@ def test_profiled_traffic_needs_matching_sources(tmp_path, monkeypatch):
     (prof / "slice_kernel_w.json").write_text(json.dumps(rec))
     monkeypatch.setattr(bench, "ROOT", str(tmp_path))
     monkeypatch.setattr(bench, "source_hash", lambda kernel=None: rec["source_sha"])
-    assert bench.profiled_traffic("slice_kernel", "w") == 123.0
+    assert bench.profiled_traffic("slice_kernel", "w", 1000.0) == 123.0
     monkeypatch.setattr(bench, "source_hash", lambda kernel=None: "0" * 16)
-    assert bench.profiled_traffic("slice_kernel", "w") is None
+    assert bench.profiled_traffic("slice_kernel", "w", 1000.0) is None
+
+
+def test_profiled_traffic_of_a_smaller_case_is_scaled(tmp_path, monkeypatch):
+    """A summary taken on a smaller case scales by the ratio of algorithmic bytes."""
+    prof = tmp_path / "profiles"
+    prof.mkdir()
+    rec = {"kernel": "block_kernel", "workload": "w", "source_sha": "a" * 16, "dram_bytes_per_launch": 90.0,
+           "algorithmic_bytes_per_launch": 100.0, "scale_by_algorithmic_bytes": True}
+    (prof / "block_kernel_w.json").write_text(json.dumps(rec))
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    monkeypatch.setattr(bench, "source_hash", lambda kernel=None: "a" * 16)
+    assert bench.profiled_traffic("block_kernel", "w", 1000.0) == 900.0
 
 
 def test_reference_arm_line():
