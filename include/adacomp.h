@@ -43,8 +43,9 @@
  *     be reused by later calls and by other handles that fit in it. Calls that share a workspace must not overlap on the
  *     GPU (use one stream, or order the streams). After any device-side error
  *     status, zero the workspace again before reusing it.
- *   - Device-side waits (for the bulk copies into shared memory, and, for bin
- *     lengths outside 16..509, the look-back between tiles) are bounded by a timeout
+ *   - Device-side waits (for the bulk copies into shared memory, and, for handles
+ *     whose bin lengths are not all 16..509 or all 510..8189, the look-back between
+ *     tiles) are bounded by a timeout
  *     (default 2 s, adacomp_set_timeout_ns); on expiry the kernel records
  *     ADACOMP_ERR_TIMEOUT in the workspace and returns. Nothing traps.
  *   - L_T (bin_len) is limited to 1..8192 by this implementation (the format itself
@@ -141,7 +142,8 @@ adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* d
  * process exits). It therefore takes single-layer handles whose compress_ws_bytes
  * (from adacomp_init_layer) is at most ADACOMP_STATIC_WS_BYTES; compare the two to
  * know whether a layer fits (roughly 3.9M elements for 16 <= L_T <= 509, whose
- * workspace holds two bits per element, and far more for other bin lengths). Larger
+ * workspace holds two bits per element, about 2M at L_T = 510, rising with L_T to
+ * the block-sliced limit of 8189, and far more for other bin lengths). Larger
  * layers get ADACOMP_ERR_WORKSPACE.
  * The call allocates nothing: it zeroes the part of the array it uses
  * (cudaMemsetAsync) and runs the same kernels on `stream`.
@@ -237,7 +239,8 @@ adacomp_status adacomp_set_timing_events(adacomp_layer_t h, cudaEvent_t before, 
  * Fault injection for tests of the device-side timeout (not part of the method):
  * when skip_tile is a valid tile index of this handle's next compress calls, the
  * bulk copies of that tile are never started when every layer has 16 <= L_T <= 509
- * (its warps' waits run out), and otherwise the tile never publishes its look-back
+ * or every layer 510 <= L_T <= 8189 (its warps' waits run out), and otherwise the
+ * tile never publishes its look-back
  * descriptor (the tiles after it in its layer wait for it); either way the layer
  * reports ADACOMP_ERR_TIMEOUT once the timeout has passed. Nothing faults or hangs. Pass 0xFFFFFFFF to switch it off (the default). After such a
  * call, zero the workspace before reusing it.
@@ -319,12 +322,15 @@ adacomp_status adacomp_set_selection_rule(adacomp_layer_t h, int32_t rule);
  * residue = fl32(G - sign(G) * s_prev) to them as it loads them, before forming its
  * own G, and adacomp_materialize applies them on demand. Messages, s and every
  * later step are bit-identical to the eager path; the residue buffer holds the
- * eager residue only after adacomp_materialize. The fix-up is deferred for layers
- * with 16 <= L_T <= 509; other layers are fixed up eagerly as before.
+ * eager residue only after adacomp_materialize. The fix-up is deferred for every
+ * layer when all of the handle's layers have 16 <= L_T <= 509, or all have
+ * 510 <= L_T <= 8189; in a handle that mixes the ranges or holds other bin lengths
+ * it is deferred for the layers with 16 <= L_T <= 509 and the others are fixed up
+ * eagerly as before.
  *
  * *compress_ws_bytes receives the workspace size in this mode (it grows by 512
- * bytes per tile unless every layer has 16 <= L_T <= 509, whose workspace holds the
- * masks in both modes), and the workspace must be zero-filled before its first use. Consecutive
+ * bytes per tile unless all layers lie in one of the two ranges above, whose
+ * workspaces hold the masks in both modes), and the workspace must be zero-filled before its first use. Consecutive
  * calls must use the same workspace; materialise before checkpointing the residue,
  * before switching the mode off, or after a call that reported an error (then also
  * zero the workspace). adacomp_compress_static_ws rejects such handles

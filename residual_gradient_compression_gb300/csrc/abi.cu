@@ -230,14 +230,17 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, const ui
     p->eps = o.eps;
     p->bc1 = o.bc1;
     p->bc2 = o.bc2;
-    uint32_t vt = 0;  // validation tasks per learner, layer by layer
+    uint32_t vt = 0, ct = 0;  // counting and code-check tasks per learner, layer by layer
     for (int64_t l = 0; l < L; ++l) {
         const KLayer& k = h->layers[(size_t)l];
         const uint32_t per = adacomp::val_tiles_per_task(k.bins_per_tile);
         p->val_begin[l] = vt;
         vt += (k.num_tiles + per - 1) / per;
+        p->chk_begin[l] = ct;
+        ct += adacomp::chk_tasks(k.num_tiles, k.bins_per_tile);
     }
     p->val_begin[L] = vt;
+    p->chk_begin[L] = ct;
     adacomp_status st = ADACOMP_OK;
     for (int64_t l = 0; l < L && st == ADACOMP_OK; ++l) {
         float* m1 = o.mom ? o.mom[l] : nullptr;

@@ -196,13 +196,32 @@ constexpr size_t kDecodeFixed = 10240;
 constexpr size_t kDecodeLayerCodes = 2048;  // offset of the (layer, learner) code counts
 constexpr int kMaxDecodePairs = 1024;  // num_layers * K per launch
 constexpr uint64_t kBadOffset = ~0ull;
-__host__ __device__ inline size_t decode_per_learner(uint64_t total_tiles) { return 8 * (size_t)total_tiles; }
+// Per learner: the tiles' code offsets (u64) and, before the scan turns them into
+// offsets, the tiles' code sums (u32, 0xffffffff for a tile whose counts are invalid).
+__host__ __device__ inline size_t decode_sums_offset(uint64_t total_tiles) { return 8 * (size_t)total_tiles; }
+__host__ __device__ inline size_t decode_per_learner(uint64_t total_tiles)
+{
+    return 8 * (size_t)total_tiles + ((4 * (size_t)total_tiles + 15) & ~(size_t)15);
+}
 // Code validation: one task per run of whole tiles of one layer holding at most
 // kValBins bins (one tile when a tile holds more).
 constexpr uint32_t kValBins = 128;
 __host__ __device__ inline uint32_t val_tiles_per_task(uint32_t bins_per_tile)
 {
     return bins_per_tile >= kValBins ? 1u : kValBins / bins_per_tile;
+}
+
+// Code checks: one task per 32 bins, lane b walking bin b's codes: floor(32 / bpt)
+// whole tiles per task, or, for tiles of more than 32 bins, ceil(bpt / 32) tasks per
+// tile.
+constexpr uint32_t kChkBins = 32;
+__host__ __device__ inline uint32_t chk_tasks(uint32_t num_tiles, uint32_t bins_per_tile)
+{
+    if (bins_per_tile <= kChkBins) {
+        const uint32_t tpt = kChkBins / bins_per_tile;
+        return (num_tiles + tpt - 1) / tpt;
+    }
+    return num_tiles * ((bins_per_tile + kChkBins - 1) / kChkBins);
 }
 
 constexpr uint32_t kErrTimeout = 1;
@@ -218,7 +237,8 @@ struct DecodeParams {
     float* dense[kMaxGroup];              // the dense sum, or the weights when opt != kOptNone
     float* mom[kMaxGroup];                // momentum (SGD) or first moment (Adam)
     float* mom2[kMaxGroup];               // second moment (Adam)
-    uint32_t val_begin[kMaxGroup + 1];    // validation tasks per learner: layer l's are [val_begin[l], val_begin[l + 1])
+    uint32_t val_begin[kMaxGroup + 1];    // counting tasks per learner: layer l's are [val_begin[l], val_begin[l + 1])
+    uint32_t chk_begin[kMaxGroup + 1];    // code-check tasks per learner, the same way
     int32_t K;
     int32_t opt;                          // kOptNone, kOptSGD or kOptAdam
     float lr, mu, scale;                  // SGD: w -= lr * v, v = mu * v + scale * g (Adam uses lr and scale)

@@ -62,6 +62,13 @@ __device__ __forceinline__ uint64_t* tile_offsets(uint8_t* ws, int k, uint32_t T
     return reinterpret_cast<uint64_t*>(ws + kDecodeFixed + (size_t)k * decode_per_learner(T));
 }
 
+__device__ __forceinline__ uint32_t* tile_sums_of(uint8_t* ws, int k, uint32_t T)
+{
+    return reinterpret_cast<uint32_t*>(ws + kDecodeFixed + (size_t)k * decode_per_learner(T) + decode_sums_offset(T));
+}
+
+constexpr uint32_t kBadSum = 0xffffffffu;  // the sum of a tile whose counts are invalid
+
 // Layer of validation task u (tasks of a learner are numbered across the layers).
 __device__ __forceinline__ int layer_of_task(const uint32_t* vb, int num_layers, uint32_t u)
 {
@@ -99,8 +106,9 @@ __device__ __forceinline__ Run run_of(const KGroup& g, const uint32_t* vb, uint3
 // One warp per (learner k, run): the message must be at least 8 + 2B bytes long
 // (else nothing of it is read), the header's B must equal the layer's B, and no
 // count may exceed its bin's length; otherwise every tile sum of the run is
-// kBadOffset. Lanes take the run's bins (all loads issued at once, coalesced) and
-// add them into per-tile sums in shared memory.
+// kBadSum. Lanes take the run's bins (all loads issued at once, coalesced) and add
+// them into per-tile sums in shared memory. The warp of a message's first run also
+// clears the message's rejection byte, which the later kernels set.
 __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_constant__ KGroup g,
                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
@@ -119,10 +127,11 @@ __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_con
     const Run R = run_of(g, vb, (uint32_t)(task - (uint64_t)k * per_learner));
     const int l = R.layer;
     const KLayer& ly = g.layer[l];
-    uint64_t* out = tile_offsets(ws, k, T) + R.t0;
+    if (R.t0 == ly.tile_begin && lane == 0) ws[16 + l * K + k] = 0;
+    uint32_t* out = tile_sums_of(ws, k, T) + R.t0;
     const uint8_t* msg = p.msg[l * K + k];
     if (p.len[l * K + k] < 8ull + 2ull * ly.nbins) {  // too short for its header and counts: read nothing
-        for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = kBadOffset;
+        for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = kBadSum;
         return;
     }
     const uint32_t hdr_b = *reinterpret_cast<const uint32_t*>(msg + 4);
@@ -138,7 +147,7 @@ __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_con
         }
         ok = __all_sync(kFull, ok) && hdr_b == ly.nbins;
         sum = __reduce_add_sync(kFull, sum);
-        if (lane == 0) out[0] = ok ? (uint64_t)sum : kBadOffset;
+        if (lane == 0) out[0] = ok ? sum : kBadSum;
         return;
     }
     uint32_t* sums = sums_s[threadIdx.x >> 5];
@@ -160,262 +169,245 @@ __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_con
     }
     ok = __all_sync(kFull, ok) && hdr_b == ly.nbins;
     __syncwarp();
-    for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = ok ? (uint64_t)sums[i] : kBadOffset;
+    for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = ok ? sums[i] : kBadSum;
 }
 
-// One CTA per (layer, learner): the tile sums become exclusive offsets, in place. A
-// message with any bad tile, or whose length is not 8 + 2B + w * (its code count),
-// is marked bad as a whole; the message's code count goes to the workspace.
-// The tiles are taken in passes of kScanPer * 1024: thread tid loads tiles
-// pass_base + i * 1024 + tid for i < kScanPer (coalesced, every load of the pass
-// issued before the first is used), the warps scan each row with shuffles and one
-// warp scans the row-by-warp totals in row order. A first sweep finds the total and
-// whether any tile is bad, the second writes the offsets.
+// Grid (chunk, layer * K + learner): the tile sums of one message become the tiles'
+// exclusive code offsets, a chunk of CH tiles per CTA. The CTA sums the message's
+// tiles before its chunk (coalesced, kScanPer loads per thread in flight; the
+// repeated reads are small and hit L2), then scans its own chunk in passes of
+// kScanPer * 1024 tiles (thread tid loads tiles pass + i * 1024 + tid; the warps scan
+// each row with shuffles and one warp scans the row-by-warp totals in row order). A
+// chunk with a bad tile rejects the message; the CTA of the message's last chunk
+// checks that its length is exactly 8 + 2B + w * (its code count) and records that
+// count. The last CTA of the grid decides, per layer, whether the layer is summed in
+// place (all learners' codes < n / 16).
 constexpr int kScanThreads = 1024;
 constexpr int kScanWarps = kScanThreads / 32;
-constexpr int kScanPer = 8;
+constexpr int kScanPer = 4;
 
 __global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_constant__ KGroup g,
-                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
+                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws,
+                                                                 uint32_t CH)
 {
     __shared__ unsigned long long wt[kScanPer][kScanWarps];
     __shared__ unsigned long long wx[kScanPer][kScanWarps];
+    __shared__ unsigned long long red[kScanWarps];
     __shared__ unsigned long long carry_s;
+    __shared__ uint32_t last_s;
     const int K = p.K;
-    const int l = blockIdx.x / K, k = blockIdx.x - (blockIdx.x / K) * K;
+    const int lk = blockIdx.y;
+    const int l = lk / K, k = lk - (lk / K) * K;
     const KLayer& ly = g.layer[l];
-    uint64_t* off = tile_offsets(ws, k, g.total_tiles) + ly.tile_begin;
+    const uint32_t T = g.total_tiles;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    if (blockIdx.x == 0 && tid == 0) {
+    if (blockIdx.x == 0 && blockIdx.y == 0 && tid == 0) {
         reinterpret_cast<uint32_t*>(ws)[0] = (uint32_t)K;
         reinterpret_cast<uint32_t*>(ws)[1] = (uint32_t)g.num_layers;
     }
-    if (tid == 0) carry_s = 0ull;
-    __syncthreads();
     const uint32_t nt = ly.num_tiles;
-    bool bad = false;
-    for (uint32_t base = 0; base < nt; base += kScanPer * kScanThreads) {
-        uint64_t v[kScanPer], inc[kScanPer];
-        bool mine_bad = false;
+    const uint32_t c0 = blockIdx.x * CH;
+    if (c0 < nt) {
+        const uint32_t c1 = min(nt, c0 + CH);
+        const uint32_t* sum = tile_sums_of(ws, k, T) + ly.tile_begin;
+        uint64_t* off = tile_offsets(ws, k, T) + ly.tile_begin;
+        // the codes of the message's tiles before the chunk
+        unsigned long long before = 0;
+        for (uint32_t i0 = 0; i0 < c0; i0 += kScanPer * kScanThreads) {
+            uint32_t v[kScanPer];
 #pragma unroll
-        for (int i = 0; i < kScanPer; ++i) {
-            const uint32_t j = base + i * kScanThreads + tid;
-            v[i] = j < nt ? off[j] : 0ull;
-            mine_bad = mine_bad || v[i] == kBadOffset;
-        }
-        if (__syncthreads_or(mine_bad)) {  // a bad tile: the whole message is rejected
-            bad = true;
-            break;
-        }
-#pragma unroll
-        for (int i = 0; i < kScanPer; ++i) {
-            inc[i] = v[i];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const unsigned long long y = __shfl_up_sync(kFull, inc[i], o);
-                if (lane >= o) inc[i] += y;
+            for (int u = 0; u < kScanPer; ++u) {
+                const uint32_t i = i0 + u * kScanThreads + tid;
+                v[u] = i < c0 ? sum[i] : 0u;
             }
-            if (lane == 31) wt[i][warp] = inc[i];
+#pragma unroll
+            for (int u = 0; u < kScanPer; ++u) before += v[u];
         }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) before += __shfl_xor_sync(kFull, before, o);
+        if (lane == 0) red[warp] = before;
+        if (tid == 0) carry_s = 0ull;
         __syncthreads();
         if (warp == 0) {
-            unsigned long long c = carry_s;
+            unsigned long long b = red[lane];
 #pragma unroll
-            for (int i = 0; i < kScanPer; ++i) {
-                const unsigned long long x = wt[i][lane];
-                unsigned long long sx = x;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const unsigned long long y = __shfl_up_sync(kFull, sx, o);
-                    if (lane >= o) sx += y;
-                }
-                wx[i][lane] = c + (sx - x);
-                c += __shfl_sync(kFull, sx, 31);
-            }
-            if (lane == 0) carry_s = c;
+            for (int o = 16; o; o >>= 1) b += __shfl_xor_sync(kFull, b, o);
+            if (lane == 0) carry_s = b;
         }
         __syncthreads();
+        bool bad = false;
+        for (uint32_t base = c0; base < c1; base += kScanPer * kScanThreads) {
+            uint64_t v[kScanPer], inc[kScanPer];
+            bool mine_bad = false;
 #pragma unroll
-        for (int i = 0; i < kScanPer; ++i) {
-            const uint32_t j = base + i * kScanThreads + tid;
-            if (j < nt) off[j] = wx[i][warp] + (inc[i] - v[i]);
+            for (int i = 0; i < kScanPer; ++i) {
+                const uint32_t j = base + i * kScanThreads + tid;
+                const uint32_t x = j < c1 ? sum[j] : 0u;
+                mine_bad = mine_bad || x == kBadSum;
+                v[i] = x;
+            }
+            if (__syncthreads_or(mine_bad)) {  // a bad tile: the whole message is rejected
+                bad = true;
+                break;
+            }
+#pragma unroll
+            for (int i = 0; i < kScanPer; ++i) {
+                inc[i] = v[i];
+#pragma unroll
+                for (int o = 1; o < 32; o <<= 1) {
+                    const unsigned long long y = __shfl_up_sync(kFull, inc[i], o);
+                    if (lane >= o) inc[i] += y;
+                }
+                if (lane == 31) wt[i][warp] = inc[i];
+            }
+            __syncthreads();
+            if (warp == 0) {
+                unsigned long long c = carry_s;
+#pragma unroll
+                for (int i = 0; i < kScanPer; ++i) {
+                    const unsigned long long x = wt[i][lane];
+                    unsigned long long sx = x;
+#pragma unroll
+                    for (int o = 1; o < 32; o <<= 1) {
+                        const unsigned long long y = __shfl_up_sync(kFull, sx, o);
+                        if (lane >= o) sx += y;
+                    }
+                    wx[i][lane] = c + (sx - x);
+                    c += __shfl_sync(kFull, sx, 31);
+                }
+                if (lane == 0) carry_s = c;
+            }
+            __syncthreads();
+#pragma unroll
+            for (int i = 0; i < kScanPer; ++i) {
+                const uint32_t j = base + i * kScanThreads + tid;
+                if (j < c1) off[j] = wx[i][warp] + (inc[i] - v[i]);
+            }
+        }
+        __syncthreads();
+        if (tid == 0) {
+            if (c1 == nt) {  // the message's last chunk: its code count and its length
+                const unsigned long long total = carry_s;
+                bad = bad || p.len[lk] != 8ull + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * total;
+                layer_codes(ws)[lk] = total;
+            }
+            if (bad) ws[16 + lk] = 1;
         }
     }
-    __syncthreads();
-    const unsigned long long total = carry_s;
-    // the message must end exactly after its last code
-    bad = bad || p.len[l * K + k] != 8ull + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * total;
-    __shared__ uint32_t last_s;
     if (tid == 0) {
-        ws[16 + l * K + k] = bad ? 1 : 0;
-        layer_codes(ws)[(size_t)l * K + k] = bad ? 0ull : total;
         __threadfence();
-        last_s = atomicAdd(reinterpret_cast<uint32_t*>(ws) + 2, 1u) == gridDim.x - 1u ? 1u : 0u;
+        last_s = atomicAdd(reinterpret_cast<uint32_t*>(ws) + 2, 1u) == gridDim.x * gridDim.y - 1u ? 1u : 0u;
     }
     __syncthreads();
     if (last_s) {  // every message is scanned: decide which layers are summed in place
         __threadfence();
         for (int e = tid; e < g.num_layers; e += kScanThreads) {
             const volatile unsigned long long* c = layer_codes(ws) + (size_t)e * K;
+            const volatile uint8_t* badb = ws + 16 + e * K;
             unsigned long long sum = 0;
-            for (int j = 0; j < K; ++j) sum += c[j];
+            for (int j = 0; j < K; ++j) sum += badb[j] ? 0ull : c[j];
             sparse_flags(ws)[e] = sum * 16ull < (unsigned long long)g.layer[e].n ? 1 : 0;
         }
     }
 }
 
-// One warp per (learner k, run) of a message not already rejected: within every bin
-// the code offsets must rise strictly (a message gives each element at most one code)
-// and stay below the bin's length; otherwise the message is rejected as a whole,
-// before anything is added. The run's counts are loaded at once (lanes over bins) and
-// the first code of every non-empty bin is marked in a per-warp bitmap over the run's
-// codes; the codes are then read coalesced, kValBatch per lane at a time, and each is
-// compared with its neighbour (a shuffle), unless it starts a bin, and with its bin's
-// length (L_T, or the layer's last, shorter bin). A run with more codes than the
-// bitmap holds, or a tile of more than kValBins bins, is checked bin by bin instead.
-constexpr int kValBatch = 8;
-constexpr uint32_t kValBitmapWords = 256;  // codes of a run checked through the bitmap: up to 8192
-
-// The codes [0, total) at `codes` (kCpv codes per 16 bytes: 8 of 16 bits or 16 of 8
-// bits), read as 16-byte vectors from the boundary at or before the first (the
-// message starts on a 16-byte boundary, so no read leaves the 16-byte blocks its
-// bytes lie in). Code j must be below its bin's length (last_len from code last_start
-// on) and, unless bit j of bm marks it as its bin's first, above code j - 1.
-template <int kCpv>
-__device__ __forceinline__ bool check_codes(const uint8_t* codes, uint32_t total, const uint32_t* bm,
-                                            uint32_t last_start, uint32_t last_len, uint32_t bin_len, int lane)
+// One warp per (learner k, task of at most kChkBins bins) of a message not already
+// rejected: within every bin the code offsets must rise strictly (a message gives
+// each element at most one code) and stay below the bin's length (L_T, or the
+// layer's last, shorter bin); otherwise the message is rejected as a whole, before
+// anything is added. Lane b takes bin b of the task: its count, then (a warp scan
+// over the task's bins, plus the offset of the bin's tile) the index of its first
+// code, and walks its codes in order, four loads at a time.
+__device__ __forceinline__ int layer_of_chk(const uint32_t* cb, int num_layers, uint32_t u)
 {
-    constexpr int kBits = 128 / kCpv;  // bits per code: 8 or 16
-    const uintptr_t a = reinterpret_cast<uintptr_t>(codes);
-    const uint4* va = reinterpret_cast<const uint4*>(a & ~(uintptr_t)15);
-    const int delta = (int)((a & 15) / (16 / kCpv));  // codes before the first in its vector
-    const uint32_t nvec = (total + delta + kCpv - 1) / kCpv;
-    bool ok = true;
-    uint32_t carry = 0;  // the last code of the previous batch's last vector
-    for (uint32_t v0 = 0; v0 < nvec; v0 += 32 * kValBatch) {
-        uint4 vec[kValBatch];
-#pragma unroll
-        for (int q = 0; q < kValBatch; ++q) {
-            const uint32_t v = v0 + q * 32 + lane;
-            vec[q] = v < nvec ? va[v] : make_uint4(0u, 0u, 0u, 0u);
-        }
-#pragma unroll
-        for (int q = 0; q < kValBatch; ++q) {
-            const uint32_t v = v0 + q * 32 + lane;
-            const uint32_t wd[4] = {vec[q].x, vec[q].y, vec[q].z, vec[q].w};
-            const uint32_t last_code = (wd[3] >> (32 - kBits)) & ((1u << kBits) - 1u);
-            uint32_t before = __shfl_up_sync(kFull, last_code, 1);
-            const uint32_t next_carry = __shfl_sync(kFull, last_code, 31);
-            if (lane == 0) before = carry;
-            carry = next_carry;
-            if (v >= nvec) continue;
-            const int j0 = (int)(v * kCpv) - delta;  // code index of the vector's first slot
-            // the bin-start bits of codes j0 .. j0 + kCpv - 1
-            const int w0 = j0 >> 5;
-            const uint32_t lo_w = w0 >= 0 ? bm[w0] : 0u;
-            const uint32_t hi_w = (w0 + 1) * 32 < (int)total ? bm[w0 + 1] : 0u;
-            const uint64_t bits = (((uint64_t)hi_w << 32) | lo_w) >> (j0 & 31);
-#pragma unroll
-            for (int i = 0; i < kCpv; ++i) {
-                const int j = j0 + i;
-                const uint32_t c = (wd[i / (32 / kBits)] >> (kBits * (i % (32 / kBits)))) & ((1u << kBits) - 1u);
-                if (j >= 0 && j < (int)total) {
-                    const uint32_t o = c >> 1;
-                    const bool starts = (bits >> i) & 1u;
-                    ok = ok && o < ((uint32_t)j >= last_start ? last_len : bin_len) && (starts || o > (before >> 1));
-                }
-                before = c;
-            }
-        }
+    int lo = 0, hi = num_layers - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (cb[mid] <= u) lo = mid;
+        else hi = mid - 1;
     }
-    return ok;
+    return lo;
 }
 
-__global__ void __launch_bounds__(kDecThreads) validate_kernel(const __grid_constant__ KGroup g,
-                                                               const __grid_constant__ DecodeParams p, uint8_t* ws)
+__global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constant__ KGroup g,
+                                                            const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
-    __shared__ uint32_t vb[kMaxGroup + 1];
-    __shared__ uint32_t bm_s[kDecThreads / 32][kValBitmapWords];
-    for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) vb[e] = p.val_begin[e];
+    __shared__ uint32_t cb[kMaxGroup + 1];
+    for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) cb[e] = p.chk_begin[e];
     __syncthreads();
     const int K = p.K;
     const int lane = threadIdx.x & 31;
-    const uint32_t per_learner = vb[g.num_layers];
+    const uint32_t per_learner = cb[g.num_layers];
     const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
     if (task >= (uint64_t)K * per_learner) return;
     const int k = (int)(task / per_learner);
-    const Run R = run_of(g, vb, (uint32_t)(task - (uint64_t)k * per_learner));
-    const int l = R.layer;
+    const uint32_t u = (uint32_t)(task - (uint64_t)k * per_learner);
+    const int l = layer_of_chk(cb, g.num_layers, u);
     if (ws[16 + l * K + k]) return;  // rejected already: nothing more of it is read
     const KLayer& ly = g.layer[l];
-    const uint8_t* msg = p.msg[l * K + k];
-    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + R.b0;
-    const uint64_t off = tile_offsets(ws, k, g.total_tiles)[R.t0];
-    const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (unsigned long long)ly.code_bytes * off;
-    const bool wide = ly.code_bytes == 2;
-    const uint32_t last_len = (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
-    const bool has_last = R.b0 + R.nb == ly.nbins;  // the run holds the layer's last bin
-    uint32_t* bm = bm_s[threadIdx.x >> 5];
-    bool ok = true;
-    uint32_t total = 0, last_start = 0xffffffffu;
-    bool fast = R.nb <= kValBins;
-    if (fast) {
-        uint32_t c[kValBins / 32], ex[kValBins / 32];
-#pragma unroll
-        for (int i = 0; i < (int)(kValBins / 32); ++i) {
-            const uint32_t b = i * 32 + lane;
-            c[i] = b < R.nb ? cnt[b] : 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < (int)(kValBins / 32); ++i) {
-            uint32_t incl = c[i];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
-            }
-            ex[i] = total + incl - c[i];
-            total += __shfl_sync(kFull, incl, 31);
-        }
-        fast = total <= 32 * kValBitmapWords;
-        if (fast) {
-            for (uint32_t w = lane; w < (total + 31) / 32; w += 32) bm[w] = 0u;
-            __syncwarp();
-#pragma unroll
-            for (int i = 0; i < (int)(kValBins / 32); ++i) {
-                const uint32_t b = i * 32 + lane;
-                if (b < R.nb && c[i]) atomicOr(&bm[ex[i] >> 5], 1u << (ex[i] & 31));
-                if (has_last && b == R.nb - 1) last_start = ex[i];
-            }
-            last_start = __reduce_min_sync(kFull, last_start);
-            __syncwarp();
-            ok = wide ? check_codes<8>(codes, total, bm, last_start, last_len, (uint32_t)ly.bin_len, lane)
-                      : check_codes<16>(codes, total, bm, last_start, last_len, (uint32_t)ly.bin_len, lane);
-        }
+    const uint32_t i = u - cb[l];
+    const uint32_t bpt = ly.bins_per_tile;
+    // the task's bins [b0, b0 + nb) of the layer; lane's tile (layer-relative)
+    uint32_t b0, nb, tile, tb0;
+    if (bpt <= kChkBins) {
+        const uint32_t tpt = kChkBins / bpt;
+        b0 = i * tpt * bpt;
+        nb = min(tpt * bpt, ly.nbins - b0);
+        tile = i * tpt + (uint32_t)lane / bpt;
+        tb0 = tile * bpt;  // the first bin of the lane's tile
+    } else {
+        const uint32_t per = (bpt + kChkBins - 1) / kChkBins;
+        tile = i / per;
+        tb0 = tile * bpt;
+        b0 = tb0 + (i - tile * per) * kChkBins;
+        const uint32_t tend = min(tb0 + bpt, ly.nbins);
+        if (b0 >= tend) return;
+        nb = min(kChkBins, tend - b0);
     }
-    if (!fast) {
-        // bin by bin, one lane per bin, each lane walking its bin's codes
-        uint64_t start = 0;
-        for (uint32_t c0 = 0; c0 < R.nb; c0 += 32) {
-            const uint32_t b = c0 + lane;
-            const uint32_t c = b < R.nb ? cnt[b] : 0u;
-            uint32_t incl = c;
+    const uint8_t* msg = p.msg[l * K + k];
+    const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8);
+    const uint32_t c = (uint32_t)lane < nb ? cnt[b0 + lane] : 0u;
+    uint32_t incl = c;
 #pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const uint32_t y = __shfl_up_sync(kFull, incl, o);
-                if (lane >= o) incl += y;
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(kFull, incl, o);
+        if (lane >= o) incl += y;
+    }
+    // codes of the lane's tile before its bin
+    uint64_t before;
+    if (bpt <= kChkBins) {
+        const uint32_t fl = ((uint32_t)lane / bpt) * bpt;  // the lane of its tile's first bin
+        before = (uint64_t)(incl - c) - __shfl_sync(kFull, incl - c, (int)(fl & 31));
+    } else {
+        uint32_t pre = 0;  // the tile's bins before the task's
+        for (uint32_t b = tb0 + lane; b < b0; b += 32) pre += cnt[b];
+        before = (uint64_t)__reduce_add_sync(kFull, pre) + (incl - c);
+    }
+    bool ok = true;
+    if ((uint32_t)lane < nb && c) {
+        const uint64_t first = tile_offsets(ws, k, g.total_tiles)[ly.tile_begin + tile] + before;
+        const uint32_t len = b0 + lane == ly.nbins - 1 ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len)
+                                                       : (uint32_t)ly.bin_len;
+        const uint8_t* codes = msg + 8 + 2ull * ly.nbins;
+        const bool wide = ly.code_bytes == 2;
+        int64_t prev = -1;
+        uint32_t j = 0;
+        for (; j + 4 <= c; j += 4) {
+            uint32_t q[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                q[e] = wide ? reinterpret_cast<const uint16_t*>(codes)[first + j + e] : codes[first + j + e];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const uint32_t o = q[e] >> 1;
+                ok = ok && o < len && (int64_t)o > prev;
+                prev = o;
             }
-            if (b < R.nb) {
-                const uint32_t len = (R.b0 + b == ly.nbins - 1) ? last_len : (uint32_t)ly.bin_len;
-                const uint64_t j0 = start + incl - c;
-                uint32_t prev_o = 0;
-                for (uint32_t i = 0; i < c; ++i) {
-                    const uint32_t o = (wide ? reinterpret_cast<const uint16_t*>(codes)[j0 + i] : codes[j0 + i]) >> 1;
-                    ok = ok && o < len && (i == 0 || o > prev_o);
-                    prev_o = o;
-                }
-            }
-            start += __shfl_sync(kFull, incl, 31);
+        }
+        for (; j < c; ++j) {
+            const uint32_t o = (wide ? reinterpret_cast<const uint16_t*>(codes)[first + j] : codes[first + j]) >> 1;
+            ok = ok && o < len && (int64_t)o > prev;
+            prev = o;
         }
     }
     if (!__all_sync(kFull, ok) && lane == 0) ws[16 + l * K + k] = 1;
@@ -1015,10 +1007,17 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     tile_sums_kernel<<<(unsigned)((vtasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    tile_scan_kernel<<<(unsigned)(g.num_layers * p.K), kScanThreads, 0, stream>>>(g, p, w);
+    // scan chunks: at least 8192 tiles, at most 64 chunks per message
+    uint32_t max_tiles = 0;
+    for (int l = 0; l < g.num_layers; ++l) max_tiles = g.layer[l].num_tiles > max_tiles ? g.layer[l].num_tiles : max_tiles;
+    uint32_t CH = kScanPer * kScanThreads * 2;
+    while ((max_tiles + CH - 1) / CH > 64u) CH += kScanPer * kScanThreads;
+    const dim3 sgrid((max_tiles + CH - 1) / CH, (unsigned)(g.num_layers * p.K));
+    tile_scan_kernel<<<sgrid, kScanThreads, 0, stream>>>(g, p, w, CH);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    validate_kernel<<<(unsigned)((vtasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
+    const uint64_t ctasks = (uint64_t)p.K * p.chk_begin[g.num_layers];  // (learner, 32 bins) tasks
+    check_kernel<<<(unsigned)((ctasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     const int opt = p.opt;

@@ -67,7 +67,8 @@ def test_sliced_workspace_layout(n, L):
     h = ac.adacomp_init_layer(n, L, ac.F32)
     assert h.compress_ws_bytes == expect
     assert ac.adacomp_set_lazy_fixup(h, True) == expect
-    assert h.decode_ws_bytes(3) == ac.DECODE_WS_FIXED + 3 * 8 * T
+    # per learner: a u64 code offset and a u32 code sum per tile (the sums padded to 16 B)
+    assert h.decode_ws_bytes(3) == ac.DECODE_WS_FIXED + 3 * (8 * T + _pad16(4 * T))
     ac.adacomp_free(h)
 
 
