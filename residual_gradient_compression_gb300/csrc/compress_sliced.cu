@@ -519,10 +519,11 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
 //   1. G = fl32(residue + dW), residue := G, and the lanes' bin maxima, folded per
 //      bin (a 512-slot slice meets at most three bins) with warp reductions and one
 //      shared atomicMax per bin; then one block barrier;
-//   2. G and the probe again from the stage (recomputing costs less than keeping
-//      them in registers across the barrier: fewer registers, more resident warps),
-//      the selection against the bins' maxima, the masks, and the per-bin counts
-//      (warp reductions, one shared atomicAdd per bin); then the stage is refilled.
+//   2. the selection against the bins' maxima, from the probes abs(H) that pass 1
+//      wrote over the lane's residue slots of the stage (cheaper than keeping them in
+//      registers across the barrier: fewer registers, more resident warps), the
+//      masks, and the per-bin counts (warp reductions, one shared atomicAdd per bin);
+//      then the stage is refilled.
 // The counts of tile i are complete at the barrier of tile i + 1, where the finishing
 // warp (the last) writes them into the message, adds the maxima to the CTA's exponent
 // buckets (64-bit, one per fp32 exponent, flushed to the layer's exact accumulator
@@ -701,17 +702,20 @@ __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KG
         const uint32_t vr = to_reg_order(q.valid, rot);
         const uint32_t lor = to_reg_order(lomask, rot) & vr;
         const uint32_t hir = vr & ~lor;
-        const float* rs = stage_r(s) + kSeg * lane;
+        float* rs = stage_r(s) + kSeg * lane;
         const void* ds = stage_d(s);
         const int doff = ly.dw_bf16 ? (int)(Sl.a0 - ((Sl.ts + Sl.we0) & ~(int64_t)7)) : 0;
-        // pass 1: G, residue := G, the lane's bin maxima
+        // pass 1: G, residue := G, the lane's bin maxima; the probe abs(H) (-1 where
+        // G == 0, so that such elements are never sent) replaces the lane's residue
+        // slots in the stage, and the signs of G are kept for the deferred fix-up
         float m_lo = 0.0f, m_hi = 0.0f;
+        uint32_t ngr = 0;
         if (q.valid) {
             float* gres = ly.residue + Sl.a0 + kSeg * lane;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
                 const int q0 = 4 * (k ^ rot);
-                float gv[4], d[4];
+                float gv[4], d[4], ah[4];
                 chunk_g<kLazy>(ly.dw_bf16, rs, ds, doff, lane, q0, (pm >> (4 * k)) & 0xfu, s_prev, gv, d);
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
@@ -719,7 +723,10 @@ __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KG
                     const float a = fabsf(gv[e]);
                     m_lo = fmaxf(m_lo, (lor & bit) ? a : 0.0f);
                     m_hi = fmaxf(m_hi, (hir & bit) ? a : 0.0f);
+                    ah[e] = gv[e] != 0.0f ? fabsf(probe(gv[e], d[e], kLS)) : -1.0f;
+                    if (kLazy) ngr |= gv[e] < 0.0f ? bit : 0u;
                 }
+                *reinterpret_cast<float4*>(rs + q0) = make_float4(ah[0], ah[1], ah[2], ah[3]);
                 const uint32_t vq = (vr >> (4 * k)) & 0xfu;
                 float* gp = gres + q0;
                 if (vq == 0xfu) {
@@ -744,27 +751,26 @@ __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KG
         }
         __syncthreads();  // the tile's maxima are complete, and the previous tile's counts
         if (warp == W - 1 && l_prev >= 0) finish(t_prev, l_prev, (int)((i + 2) % 3));
-        // pass 2: the selection against the bins' maxima
-        uint32_t fr = 0, ngr = 0;
+        // pass 2: the selection against the bins' maxima, from the probes in the stage
+        uint32_t fr = 0;
         if (q.valid) {
             const float gm_lo = __uint_as_float(bmax[par * kBigMaxBins + q.bin_lo]);
             const float gm_hi = hir ? __uint_as_float(bmax[par * kBigMaxBins + q.bin_lo + 1]) : 0.0f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
-                const int q0 = 4 * (k ^ rot);
-                float gv[4], d[4];
-                chunk_g<kLazy>(ly.dw_bf16, rs, ds, doff, lane, q0, (pm >> (4 * k)) & 0xfu, s_prev, gv, d);
+                const float4 a4 = *reinterpret_cast<const float4*>(rs + 4 * (k ^ rot));
+                const float ah[4] = {a4.x, a4.y, a4.z, a4.w};
 #pragma unroll
                 for (int e = 0; e < 4; ++e) {
                     const uint32_t bit = 1u << (4 * k + e);
-                    // an element with G == 0 is never sent
-                    const float ah = gv[e] != 0.0f ? fabsf(probe(gv[e], d[e], kLS)) : -1.0f;
-                    fr |= ah >= ((lor & bit) ? gm_lo : gm_hi) ? bit : 0u;
-                    if (kLazy) ngr |= gv[e] < 0.0f ? bit : 0u;
+                    fr |= ah[e] >= ((lor & bit) ? gm_lo : gm_hi) ? bit : 0u;
                 }
             }
             fr &= vr;
         }
+        // the probes written into the stage (generic proxy) come before the bulk copy
+        // that refills it (async proxy)
+        ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0 && !poisoned) {  // the stage is not read again: refill it with the tile S ahead
             const uint32_t tn = t + S * GS;
