@@ -458,8 +458,14 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
                     inflight |= 1u << s;
             }
         }
-        if (m_lo > 0.0f) atomicMax(&wg[q.bin_lo], __float_as_uint(m_lo));
-        if (m_hi > 0.0f) atomicMax(&wg[q.bin_lo + 1], __float_as_uint(m_hi));
+        const bool one_bin = ly.bpw == 1;  // warp-uniform: the slice is one bin (m_hi and c_hi are 0)
+        if (one_bin) {  // a warp reduction instead of 32 lanes' atomics on one word
+            const uint32_t x = __reduce_max_sync(kFull, __float_as_uint(m_lo));
+            if (lane == 0) wg[0] = x;
+        } else {
+            if (m_lo > 0.0f) atomicMax(&wg[q.bin_lo], __float_as_uint(m_lo));
+            if (m_hi > 0.0f) atomicMax(&wg[q.bin_lo + 1], __float_as_uint(m_hi));
+        }
         __syncwarp();
         uint32_t fr = 0;  // sent slots, register order
         if (q.valid) {
@@ -474,9 +480,15 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
                 }
             }
             fr &= vr;
-            const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & ~lor);
-            if (c_lo) atomicAdd(&wc[q.bin_lo], c_lo);
-            if (c_hi) atomicAdd(&wc[q.bin_lo + 1], c_hi);
+            if (!one_bin) {
+                const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & ~lor);
+                if (c_lo) atomicAdd(&wc[q.bin_lo], c_lo);
+                if (c_hi) atomicAdd(&wc[q.bin_lo + 1], c_hi);
+            }
+        }
+        if (one_bin) {
+            const uint32_t n1 = __reduce_add_sync(kFull, (uint32_t)__popc(fr));
+            if (lane == 0) wc[0] = n1;
         }
         __syncwarp();
         // the slice's bins: counts into the message, maxima into the buckets; the
