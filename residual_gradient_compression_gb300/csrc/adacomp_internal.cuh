@@ -211,10 +211,10 @@ __host__ __device__ inline uint32_t val_tiles_per_task(uint32_t bins_per_tile)
     return bins_per_tile >= kValBins ? 1u : kValBins / bins_per_tile;
 }
 
-// Code checks: one task per 32 bins, lane b walking bin b's codes: floor(32 / bpt)
-// whole tiles per task, or, for tiles of more than 32 bins, ceil(bpt / 32) tasks per
-// tile.
-constexpr uint32_t kChkBins = 32;
+// Code checks: one task per kChkBins bins, lane b walking bins b, b + 32, ...:
+// floor(kChkBins / bpt) whole tiles per task, or, for tiles of more than kChkBins
+// bins, ceil(bpt / kChkBins) tasks per tile.
+constexpr uint32_t kChkBins = 128;
 __host__ __device__ inline uint32_t chk_tasks(uint32_t num_tiles, uint32_t bins_per_tile)
 {
     if (bins_per_tile <= kChkBins) {

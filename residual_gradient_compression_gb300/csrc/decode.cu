@@ -315,9 +315,11 @@ __global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_co
 // rejected: within every bin the code offsets must rise strictly (a message gives
 // each element at most one code) and stay below the bin's length (L_T, or the
 // layer's last, shorter bin); otherwise the message is rejected as a whole, before
-// anything is added. Lane b takes bin b of the task: its count, then (a warp scan
-// over the task's bins, plus the offset of the bin's tile) the index of its first
-// code, and walks its codes in order, four loads at a time.
+// anything is added. Lane b takes bins b, b + 32, ... of the task: the bins' counts
+// (coalesced), the exclusive prefix of the task's counts (warp scans, kept in shared
+// memory), the index of each bin's first code (its tile's offset plus the counts of
+// its tile's bins before it), and then it walks each of its bins' codes in order,
+// four loads at a time.
 __device__ __forceinline__ int layer_of_chk(const uint32_t* cb, int num_layers, uint32_t u)
 {
     int lo = 0, hi = num_layers - 1;
@@ -332,11 +334,14 @@ __device__ __forceinline__ int layer_of_chk(const uint32_t* cb, int num_layers, 
 __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constant__ KGroup g,
                                                             const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
+    constexpr int R = (int)(kChkBins / 32);  // bins per lane
     __shared__ uint32_t cb[kMaxGroup + 1];
+    __shared__ uint32_t ex_s[kDecThreads / 32][kChkBins];
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) cb[e] = p.chk_begin[e];
     __syncthreads();
     const int K = p.K;
     const int lane = threadIdx.x & 31;
+    uint32_t* ex = ex_s[threadIdx.x >> 5];
     const uint32_t per_learner = cb[g.num_layers];
     const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
     if (task >= (uint64_t)K * per_learner) return;
@@ -347,18 +352,18 @@ __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constan
     const KLayer& ly = g.layer[l];
     const uint32_t i = u - cb[l];
     const uint32_t bpt = ly.bins_per_tile;
-    // the task's bins [b0, b0 + nb) of the layer; lane's tile (layer-relative)
-    uint32_t b0, nb, tile, tb0;
-    if (bpt <= kChkBins) {
+    // the task's bins [b0, b0 + nb) of the layer
+    uint32_t b0, nb;
+    uint32_t pre = 0;  // tile-spanning tasks: the codes of the tile's bins before the task's
+    const bool whole = bpt <= kChkBins;  // the task is whole tiles
+    if (whole) {
         const uint32_t tpt = kChkBins / bpt;
         b0 = i * tpt * bpt;
         nb = min(tpt * bpt, ly.nbins - b0);
-        tile = i * tpt + (uint32_t)lane / bpt;
-        tb0 = tile * bpt;  // the first bin of the lane's tile
     } else {
         const uint32_t per = (bpt + kChkBins - 1) / kChkBins;
-        tile = i / per;
-        tb0 = tile * bpt;
+        const uint32_t tile = i / per;
+        const uint32_t tb0 = tile * bpt;
         b0 = tb0 + (i - tile * per) * kChkBins;
         const uint32_t tend = min(tb0 + bpt, ly.nbins);
         if (b0 >= tend) return;
@@ -366,46 +371,63 @@ __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constan
     }
     const uint8_t* msg = p.msg[l * K + k];
     const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8);
-    const uint32_t c = (uint32_t)lane < nb ? cnt[b0 + lane] : 0u;
-    uint32_t incl = c;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(kFull, incl, o);
-        if (lane >= o) incl += y;
-    }
-    // codes of the lane's tile before its bin
-    uint64_t before;
-    if (bpt <= kChkBins) {
-        const uint32_t fl = ((uint32_t)lane / bpt) * bpt;  // the lane of its tile's first bin
-        before = (uint64_t)(incl - c) - __shfl_sync(kFull, incl - c, (int)(fl & 31));
-    } else {
-        uint32_t pre = 0;  // the tile's bins before the task's
+    if (!whole) {
+        const uint32_t tb0 = (b0 / bpt) * bpt;
         for (uint32_t b = tb0 + lane; b < b0; b += 32) pre += cnt[b];
-        before = (uint64_t)__reduce_add_sync(kFull, pre) + (incl - c);
+        pre = __reduce_add_sync(kFull, pre);
     }
+    uint32_t c[R];
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t j = r * 32 + lane;
+        c[r] = j < nb ? cnt[b0 + j] : 0u;
+    }
+    uint32_t run = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        uint32_t incl = c[r];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        ex[r * 32 + lane] = run + incl - c[r];
+        run += __shfl_sync(kFull, incl, 31);
+    }
+    __syncwarp();
+    const uint64_t* toff = tile_offsets(ws, k, g.total_tiles) + ly.tile_begin;
+    const uint8_t* codes = msg + 8 + 2ull * ly.nbins;
+    const bool wide = ly.code_bytes == 2;
+    const uint32_t last_len = (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
     bool ok = true;
-    if ((uint32_t)lane < nb && c) {
-        const uint64_t first = tile_offsets(ws, k, g.total_tiles)[ly.tile_begin + tile] + before;
-        const uint32_t len = b0 + lane == ly.nbins - 1 ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len)
-                                                       : (uint32_t)ly.bin_len;
-        const uint8_t* codes = msg + 8 + 2ull * ly.nbins;
-        const bool wide = ly.code_bytes == 2;
+#pragma unroll
+    for (int r = 0; r < R; ++r) {
+        const uint32_t j = r * 32 + lane;
+        if (j >= nb || c[r] == 0u) continue;
+        const uint32_t gb = b0 + j;          // the bin, in the layer
+        const uint32_t tile = gb / bpt;
+        // first code of the bin: its tile's offset plus its tile's codes before it
+        uint64_t first = toff[tile] + ex[j];
+        if (whole) first -= ex[tile * bpt - b0];
+        else first += pre;
+        const uint32_t len = gb == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len;
+        const uint32_t cn = c[r];
         int64_t prev = -1;
-        uint32_t j = 0;
-        for (; j + 4 <= c; j += 4) {
-            uint32_t q[4];
+        uint32_t q = 0;
+        for (; q + 4 <= cn; q += 4) {
+            uint32_t v[4];
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                q[e] = wide ? reinterpret_cast<const uint16_t*>(codes)[first + j + e] : codes[first + j + e];
+                v[e] = wide ? reinterpret_cast<const uint16_t*>(codes)[first + q + e] : codes[first + q + e];
 #pragma unroll
             for (int e = 0; e < 4; ++e) {
-                const uint32_t o = q[e] >> 1;
+                const uint32_t o = v[e] >> 1;
                 ok = ok && o < len && (int64_t)o > prev;
                 prev = o;
             }
         }
-        for (; j < c; ++j) {
-            const uint32_t o = (wide ? reinterpret_cast<const uint16_t*>(codes)[first + j] : codes[first + j]) >> 1;
+        for (; q < cn; ++q) {
+            const uint32_t o = (wide ? reinterpret_cast<const uint16_t*>(codes)[first + q] : codes[first + q]) >> 1;
             ok = ok && o < len && (int64_t)o > prev;
             prev = o;
         }
@@ -1016,7 +1038,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     tile_scan_kernel<<<sgrid, kScanThreads, 0, stream>>>(g, p, w, CH);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const uint64_t ctasks = (uint64_t)p.K * p.chk_begin[g.num_layers];  // (learner, 32 bins) tasks
+    const uint64_t ctasks = (uint64_t)p.K * p.chk_begin[g.num_layers];  // (learner, kChkBins bins) tasks
     check_kernel<<<(unsigned)((ctasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
