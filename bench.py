@@ -664,6 +664,14 @@ def run_lazy(args, run, sp, world, n_elems):
         if time.perf_counter() - t0 >= args.min_timed_seconds / 2 or len(reps) >= 200:
             break
     ms = max_over_ranks(sorted(reps)[len(reps) // 2], world)
+    # one more step with every launch's events: the streaming kernel (which applies
+    # the previous call's corrections) and the finalise + codes launches
+    ev = [_new_events(3) for _ in range(run.K * len(run.h))]
+    run.last_lens = run.step(step_no, sp, k1_events=ev, ws_fixed=ws)
+    torch.cuda.synchronize()
+    run.clear_timing()
+    k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
+    fx = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
     for k in range(run.K):
         for gi, h in enumerate(run.h):
             for li in range(h.num_layers):
@@ -674,7 +682,9 @@ def run_lazy(args, run, sp, world, n_elems):
         ac.adacomp_set_lazy_fixup(h, False)
     torch.cuda.synchronize()
     return {"value": n_elems * args.steps * world / (ms * 1e-3), "unit": "elements/s",
-            "ms_per_step": ms / args.steps, "timed_repetitions": len(reps)}
+            "ms_per_step": ms / args.steps, "timed_repetitions": len(reps),
+            "stream_ms_per_launch": k1, "finalize_codes_ms_per_launch": fx,
+            "finalize_codes_share_of_stream": fx / k1}
 
 
 def run_e2e(args, run, layers, sp, world):

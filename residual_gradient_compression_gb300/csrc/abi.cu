@@ -237,7 +237,7 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, const ui
         p->val_begin[l] = vt;
         vt += (k.num_tiles + per - 1) / per;
         p->chk_begin[l] = ct;
-        ct += adacomp::chk_tasks(k.num_tiles, k.bins_per_tile);
+        ct += adacomp::chk_tasks(k.num_tiles, k.bins_per_tile, k.bin_len);
     }
     p->val_begin[L] = vt;
     p->chk_begin[L] = ct;

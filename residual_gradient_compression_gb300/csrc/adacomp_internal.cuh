@@ -211,12 +211,15 @@ __host__ __device__ inline uint32_t val_tiles_per_task(uint32_t bins_per_tile)
     return bins_per_tile >= kValBins ? 1u : kValBins / bins_per_tile;
 }
 
-// Code checks: one task per kChkBins bins, lane b walking bins b, b + 32, ...:
-// floor(kChkBins / bpt) whole tiles per task, or, for tiles of more than kChkBins
-// bins, ceil(bpt / kChkBins) tasks per tile.
+// Code checks: bins of kChkLongBin elements or more take one task per tile, the lanes
+// over each bin's codes; shorter bins one task per kChkBins bins, lane b walking bins
+// b, b + 32, ...: floor(kChkBins / bpt) whole tiles per task, or, for tiles of more
+// than kChkBins bins, ceil(bpt / kChkBins) tasks per tile.
 constexpr uint32_t kChkBins = 128;
-__host__ __device__ inline uint32_t chk_tasks(uint32_t num_tiles, uint32_t bins_per_tile)
+constexpr int32_t kChkLongBin = 1024;
+__host__ __device__ inline uint32_t chk_tasks(uint32_t num_tiles, uint32_t bins_per_tile, int32_t bin_len)
 {
+    if (bin_len >= kChkLongBin) return num_tiles;
     if (bins_per_tile <= kChkBins) {
         const uint32_t tpt = kChkBins / bins_per_tile;
         return (num_tiles + tpt - 1) / tpt;

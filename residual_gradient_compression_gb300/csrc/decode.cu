@@ -352,6 +352,41 @@ __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constan
     const KLayer& ly = g.layer[l];
     const uint32_t i = u - cb[l];
     const uint32_t bpt = ly.bins_per_tile;
+    if (ly.bin_len >= kChkLongBin) {  // long bins: task i is tile i, the lanes over each bin's codes
+        const uint32_t tb0 = i * bpt;
+        const uint32_t nbt = min(bpt, ly.nbins - tb0);  // <= 4 bins of 1024 or more
+        const uint8_t* msg = p.msg[l * K + k];
+        const uint32_t c = (uint32_t)lane < nbt ? reinterpret_cast<const uint16_t*>(msg + 8)[tb0 + lane] : 0u;
+        uint32_t incl = c;
+#pragma unroll
+        for (int o = 1; o < 8; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(kFull, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint64_t toff = tile_offsets(ws, k, g.total_tiles)[ly.tile_begin + i];
+        const uint8_t* codes = msg + 8 + 2ull * ly.nbins;
+        const bool wide = ly.code_bytes == 2;
+        bool ok = true;
+        for (uint32_t b = 0; b < nbt; ++b) {
+            const uint32_t cb_ = __shfl_sync(kFull, c, (int)b);
+            const uint64_t first = toff + __shfl_sync(kFull, incl - c, (int)b);
+            const uint32_t len = tb0 + b == ly.nbins - 1 ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len)
+                                                         : (uint32_t)ly.bin_len;
+            int32_t carry = -1;  // the previous round's last offset
+            for (uint32_t j0 = 0; j0 < cb_; j0 += 32) {
+                const uint32_t j = j0 + lane;
+                const int32_t o = j < cb_ ? (int32_t)((wide ? reinterpret_cast<const uint16_t*>(codes)[first + j]
+                                                            : codes[first + j]) >> 1)
+                                          : 0x7fffffff;
+                int32_t prev = __shfl_up_sync(kFull, o, 1);
+                if (lane == 0) prev = carry;
+                ok = ok && (j >= cb_ || ((uint32_t)o < len && o > prev));
+                carry = __shfl_sync(kFull, o, 31);
+            }
+        }
+        if (!__all_sync(kFull, ok) && lane == 0) ws[16 + l * K + k] = 1;
+        return;
+    }
     // the task's bins [b0, b0 + nb) of the layer
     uint32_t b0, nb;
     uint32_t pre = 0;  // tile-spanning tasks: the codes of the tile's bins before the task's
