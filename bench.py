@@ -349,8 +349,10 @@ class DeviceRun:
     def _host_results(self):
         if not hasattr(self, "host_res"):
             self.res_bytes = [64 + 2112 * len(g) for g in self.gidx]
-            self.host_res = [[torch.empty(rb, dtype=torch.uint8, pin_memory=True) for rb in self.res_bytes]
-                             for _ in range(self.K)]
+            # one pinned buffer per group, a row per learner; numpy views made once
+            self.host_buf = [torch.empty((self.K, rb), dtype=torch.uint8, pin_memory=True) for rb in self.res_bytes]
+            self.host_np = [b.numpy() for b in self.host_buf]
+            self.host_res = [[self.host_buf[gi][k] for gi in range(len(self.gidx))] for k in range(self.K)]
         return self.host_res
 
     def message_lengths(self, ws_of):
@@ -365,17 +367,17 @@ class DeviceRun:
         if not hasattr(self, "len_bufs"):
             self.len_bufs = [np.zeros(len(g) * self.K, np.uint64) for g in self.gidx]
             self.len_ptrs = [b.ctypes.data_as(self.ct.POINTER(self.ct.c_uint64)) for b in self.len_bufs]
+        ra = self.RESULT_AT
         for gi, g in enumerate(self.gidx):
             nl = len(g)
-            for k in range(self.K):
-                # the layers' 2112-byte blocks after the 64-byte control block; in each, the
-                # result {s f32, status u32, nnz u64, msg_bytes u64} at RESULT_AT
-                blk = host[k][gi].numpy()[64:64 + 2112 * nl].reshape(nl, 2112)
-                res = blk[:, self.RESULT_AT:self.RESULT_AT + 24]
-                status = res[:, 4:8].copy().view(np.uint32).ravel()
-                if status.any():
-                    raise RuntimeError(f"device status {int(status[status != 0][0])}")
-                self.len_bufs[gi][k::self.K] = res[:, 16:24].copy().view(np.uint64).ravel()
+            # every learner's layer blocks (2112 bytes after the 64-byte control block);
+            # in each, the result {s f32, status u32, nnz u64, msg_bytes u64} at RESULT_AT
+            blk = self.host_np[gi][:, 64:64 + 2112 * nl].reshape(self.K, nl, 2112)
+            status = blk[:, :, ra + 4:ra + 8].copy().view(np.uint32)
+            if status.any():
+                raise RuntimeError(f"device status {int(status[status != 0][0])}")
+            mb = blk[:, :, ra + 16:ra + 24].copy().view(np.uint64)[:, :, 0]  # (K, layers)
+            self.len_bufs[gi][:] = mb.T.ravel()  # layer-major: [layer * K + learner]
         return self.len_ptrs
 
     def step(self, i, stream_ptr, k1_events=None, dec_events=None, ws_fixed=None, msg_set=0):
