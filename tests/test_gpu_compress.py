@@ -131,6 +131,29 @@ def test_gpt1p3b_sampled_tensors(bin_len):
     _group_run("gpt1p3b", 2, layers=lys, bin_len=bin_len)
 
 
+@pytest.mark.parametrize("bf16", [False, True], ids=["f32", "bf16"])
+def test_block_sliced_group_of_mixed_bin_lengths(bf16):
+    """One launch over layers whose bins are all 510..8189 but of different lengths:
+    the CTA is as wide as the widest tile (16 warps for L_T = 8189), so layers with
+    fewer slices per tile leave warps idle; every layer must still match the oracle."""
+    shapes = [(400_000, 5000), (123_457, 1365), (77_777, 600), (65_000, 8189), (3_000, 510)]
+    h = ac.adacomp_init_group([n for n, _ in shapes], [L for _, L in shapes], [ac.BF16 if bf16 else ac.F32] * len(shapes))
+    msgs = [torch.zeros(m, dtype=torch.uint8, device="cuda") for m in h.max_msg_bytes]
+    ws = workspace(h.compress_ws_bytes)
+    res = [torch.zeros(n, device="cuda") for n, _ in shapes]
+    res_np = [np.zeros(n, np.float32) for n, _ in shapes]
+    for step in range(3):
+        dws = [_dw(n, step, 7 * i + 1, bf16) for i, (n, _) in enumerate(shapes)]
+        ac.adacomp_compress_group(h, res, dws, msgs, ws)
+        torch.cuda.synchronize()
+        for i, (n, L) in enumerate(shapes):
+            mb, s, st = ac.adacomp_query(h, ws, i)
+            assert st == ac.OK
+            ref = oracle_step(res_np[i], dw_host(dws[i]), L)
+            assert_same_step(msgs[i][:mb].cpu().numpy(), s, res[i].cpu().numpy(), ref, res_np[i],
+                             f"layer {i} L={L} step {step}")
+
+
 def test_all_zero_layer():
     n, L = 10000, 50
     layer = GpuLayer(n, L, ac.F32)
