@@ -52,6 +52,8 @@ def parse_args():
     p.add_argument("--workload", default="flat100m",
                    choices=["resnet50", "fc400k", "lstm_fc", "gpt1p3b", "flat100m"])
     p.add_argument("--bin-len", type=int, default=500, help="L_T for gpt1p3b")
+    p.add_argument("--streams", type=int, default=2, choices=[1, 2],
+                   help="learners' compress calls alternating between two streams (default) or on one")
     p.add_argument("--layers", type=int, default=0,
                    help="only the first N layers of the workload (a smaller case, for profiling)")
     p.add_argument("--learners", type=int, default=16, help="K for flat100m")
@@ -392,7 +394,18 @@ class DeviceRun:
         def ws_of(k, gi):
             return ws_fixed[k][gi] if ws_fixed is not None else self.ws[i % self.ring][k][gi]
 
+        # learners alternate between the launch stream and a second stream, so that one
+        # learner's short launches (finalise, codes) overlap the next one's streaming
+        # kernel; the second stream starts after everything before the step and the
+        # lengths are read once both are done
+        two = self.args.streams > 1 and self.K > 1
+        if two:
+            if not hasattr(self, "side"):
+                self.side = torch.cuda.Stream()
+                self.side_ptr = self.ct.c_void_p(self.side.cuda_stream)
+            self.side.wait_stream(torch.cuda.current_stream())
         for k in range(self.K):
+            sptr = self.side_ptr if two and k % 2 else stream_ptr
             for gi, h in enumerate(self.h):
                 if k1_events is not None:
                     e = k1_events[k * len(self.h) + gi]
@@ -401,9 +414,11 @@ class DeviceRun:
                                                 self.ct.c_void_p(e[2].cuda_event))
                 ws = ws_of(k, gi)
                 st = L.adacomp_compress_group(h.ptr, self.c_res[k][gi], self.c_dw[k][s][gi], c_msg[k][gi],
-                                              self.c_cap[k][gi], ws.data_ptr(), ws.numel(), stream_ptr)
+                                              self.c_cap[k][gi], ws.data_ptr(), ws.numel(), sptr)
                 if st:
                     raise RuntimeError(f"adacomp_compress_group: {st}")
+        if two:
+            torch.cuda.current_stream().wait_stream(self.side)
         lens = self.message_lengths(ws_of)
         if dec_events is not None:
             dec_events[0].record()
@@ -451,6 +466,7 @@ def bench_config(args, layers, K, world):
             "bin_len": sorted({l.bin_len for l in layers}),
             "dw_dtype": layers[0].dw_dtype, "residue_dtype": "f32",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "compress_streams": args.streams if K > 1 else 1,
             "l2": "inputs larger than L2 (dW rotates over %d sets)" % (
                 4 if args.workload in ("resnet50", "fc400k", "lstm_fc") else 2)}
 
@@ -462,6 +478,36 @@ def residue_range(run):
         mn, mx = torch.aminmax(run.res[k][0])
         lo, hi = min(lo, float(mn)), max(hi, float(mx))
     return [lo, hi]
+
+
+def launch_times(args, run, sp, step_no):
+    """Per-launch times of the streaming kernel and of the finalise + codes launches,
+    each kernel alone: the same steps on one stream with events recorded around every
+    launch (one repetition after a step of warm-up). Returns the repetition's step
+    time and the two lists."""
+    saved = args.streams
+    args.streams = 1
+    try:
+        ncalls = run.K * len(run.h)
+        k1_events = [[_new_events(3) for _ in range(ncalls)] for _ in range(args.steps)]
+        run.last_lens = run.step(step_no, sp)
+        start, end = _new_events(2)
+        torch.cuda.synchronize()
+        start.record()
+        for i in range(args.steps):
+            run.last_lens = run.step(step_no + 1 + i, sp, k1_events[i])
+        end.record()
+        torch.cuda.synchronize()
+        run.clear_timing()
+        for i in range(args.steps):
+            for r in run.step_results(step_no + 1 + i):
+                if r[2] != 0:
+                    raise RuntimeError(f"device status {r[2]} in the one-stream steps")
+        k1 = [e[0].elapsed_time(e[1]) for st in k1_events for e in st]
+        fx = [e[1].elapsed_time(e[2]) for st in k1_events for e in st]
+        return start.elapsed_time(end), k1, fx
+    finally:
+        args.streams = saved
 
 
 def run_device(args, rank, world):
@@ -480,8 +526,6 @@ def run_device(args, rank, world):
             if st != 0:
                 raise RuntimeError(f"device status {st} during warm-up")
 
-    ncalls = run.K * len(run.h)
-    k1_events = [[_new_events(3) for _ in range(ncalls)] for _ in range(args.steps)]
     dec_events = [_new_events(2) for _ in range(args.steps)]
     start, end = _new_events(2)
     sampler = ClockSampler(torch.cuda.current_device()) if rank == 0 else None
@@ -494,26 +538,25 @@ def run_device(args, rank, world):
         torch.cuda.synchronize()
         start.record()
         for i in range(args.steps):
-            run.last_lens = run.step(step_no + i, sp, k1_events[i], dec_events[i])
+            run.last_lens = run.step(step_no + i, sp, None, dec_events[i])
         end.record()
         torch.cuda.synchronize()
         barrier(world)
         ms = start.elapsed_time(end)
-        k1 = [e[0].elapsed_time(e[1]) for st in k1_events for e in st]
-        fx = [e[1].elapsed_time(e[2]) for st in k1_events for e in st]
         dec = [e[0].elapsed_time(e[1]) for e in dec_events]
         res = [run.step_results(step_no + i) for i in range(args.steps)]
-        reps.append((ms, k1, fx, dec, res))
+        reps.append((ms, dec, res))
         step_no += args.steps
         if time.perf_counter() - t0 >= args.min_timed_seconds or len(reps) >= 500:
             break
     clocks = sampler.stop() if sampler else None
-    run.clear_timing()
     rrange = residue_range(run)
+    # each kernel's launch time alone: the same steps on one stream, events on every launch
+    one_ms, k1, fx = launch_times(args, run, sp, step_no)
 
     # the median repetition is reported
     order = sorted(range(len(reps)), key=lambda r: reps[r][0])
-    ms, k1, fx, dec, res = reps[order[len(order) // 2]]
+    ms, dec, res = reps[order[len(order) // 2]]
     ms = max_over_ranks(ms, world)
     for step_res in res:
         for nnz, mb, st in step_res:
@@ -539,7 +582,7 @@ def run_device(args, rank, world):
     else:
         stream_kernel = "compress_kernel"
     k1_ms_per_launch = statistics.mean(k1)
-    k1_bytes_per_launch = k1_bytes / len(k1)
+    k1_bytes_per_launch = k1_bytes / (args.steps * run.K * len(run.h))
     achieved = k1_bytes_per_launch / (k1_ms_per_launch * 1e-3) / 1e9
     step_gbs = total_bytes / (ms * 1e-3) / 1e9
     dec_gbs = dec_bytes / args.steps / (statistics.mean(dec) * 1e-3) / 1e9
@@ -574,6 +617,9 @@ def run_device(args, rank, world):
         out["e2e"] = run_e2e(args, run, layers, sp, world)
     if not args.no_lazy:
         out["lazy_fixup"] = run_lazy(args, run, sp, world, n_elems)
+    if run.K > 1 and args.streams == 2:  # the same steps with every learner on one stream
+        out["one_stream"] = {"value": n_elems * args.steps * world / (one_ms * 1e-3), "unit": "elements/s",
+                             "ms_per_step": one_ms / args.steps}
     if not args.no_sgd:
         out["decode_sgd"] = run_decode_sgd(args, run, sp, world, layers)
         out["decode_adam"] = run_decode_sgd(args, run, sp, world, layers, adam=True)
@@ -669,8 +715,12 @@ def run_lazy(args, run, sp, world, n_elems):
     # one more step with every launch's events: the streaming kernel (which applies
     # the previous call's corrections) and the finalise + codes launches
     ev = [_new_events(3) for _ in range(run.K * len(run.h))]
-    run.last_lens = run.step(step_no, sp, k1_events=ev, ws_fixed=ws)
-    torch.cuda.synchronize()
+    saved, args.streams = args.streams, 1  # each kernel alone
+    try:
+        run.last_lens = run.step(step_no, sp, k1_events=ev, ws_fixed=ws)
+        torch.cuda.synchronize()
+    finally:
+        args.streams = saved
     run.clear_timing()
     k1 = statistics.mean(e[0].elapsed_time(e[1]) for e in ev)
     fx = statistics.mean(e[1].elapsed_time(e[2]) for e in ev)
