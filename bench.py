@@ -154,7 +154,7 @@ KERNEL_SOURCES = {
     "compress_kernel": ("compress.cu", "compress_common.cuh", "adacomp_internal.cuh"),
     "accumulate_kernel": ("decode.cu", "adacomp_internal.cuh"),
     "sparse_accumulate_kernel": ("decode.cu", "adacomp_internal.cuh"),
-    "validate_kernel": ("decode.cu", "adacomp_internal.cuh"),
+    "check_kernel": ("decode.cu", "adacomp_internal.cuh"),
 }
 
 
