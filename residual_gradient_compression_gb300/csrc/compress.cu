@@ -1,6 +1,6 @@
-// AdaComp compression for sm_103a, the look-back path: launch groups with a layer
-// whose bin length lies outside 16..509 (groups whose layers all have
-// 16 <= L_T <= 509 take the sliced path of compress_sliced.cu). One fused streaming
+// AdaComp compression for sm_103a, the look-back path: launch groups whose bin
+// lengths are neither all 16..509 nor all 510..8189 (those take the warp-sliced and
+// block-sliced paths of compress_sliced.cu). One fused streaming
 // kernel per launch group (G, H, bin maxima, selection, per-bin counts, code
 // compaction with a decoupled look-back across tiles, residue := G), a finalise
 // kernel (s, header) and one sparse fix-up kernel that applies

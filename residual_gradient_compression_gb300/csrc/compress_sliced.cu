@@ -1,5 +1,7 @@
 // AdaComp compression for launch groups whose layers all have 16 <= L_T <= 509
-// (every conv and FC/LSTM layer of the usual configurations): the sliced path.
+// (every conv and FC/LSTM layer of the usual configurations): the warp-sliced path;
+// and for groups whose layers all have 510 <= L_T <= 8189: the block-sliced path
+// (block_kernel below), which shares the finalise, emitting and codes kernels.
 //
 // Method: "AdaComp (Adaptive Residual Gradient Compression)", Claims > Mechanism
 // #r629-local-bin-soft-threshold-and-mean-gmax-quantization (Algorithm 2 restated):
@@ -16,13 +18,15 @@
 //                    (which do not depend on s), the per-bin counts, written straight
 //                    into the message, and the tile's code total. The codes' positions
 //                    are not needed yet, so no CTA ever waits for another.
-//   slice_finalize   one CTA per layer: s from the exact sum, the header, and the
-//                    exclusive prefix of the tile code totals.
+//   slice_finalize   one CTA per (layer, chunk of 1024 tiles): the exclusive prefix of
+//                    the tile code totals; the layer's last chunk also forms s from
+//                    the exact sum and writes the header.
 //   slice_emit       persistent warps, a run of tiles each, last tiles first: the codes
 //                    written at their final positions, with the sign of G read back
 //                    from the residue, and the fix-up residue = fl32(G - sign(G) s) of
-//                    every sent element (when the fix-up is deferred to the next call,
-//                    the signs come from a second mask and the residue is not touched).
+//                    every sent element. When the fix-up is deferred to the next call,
+//                    slice_codes takes its place: the signs come from a second mask
+//                    and the residue is not touched.
 // Only the sent mask (1 bit per element; 2 with the deferred fix-up) passes between
 // the first and the last launch.
 #include "adacomp_internal.cuh"

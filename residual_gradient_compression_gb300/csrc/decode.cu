@@ -7,14 +7,14 @@
 // order, dense[j] = fl32(dense[j] + sign * s_k) for k = 0..K-1.
 //
 // Five launches:
-//   tile_sums   per (learner, tile): check that the message is long enough to hold
-//               its header and counts, validate the header's B and the tile's per-bin
-//               counts, and sum the counts;
-//   tile_scan   per (layer, learner): exclusive prefix of the tile sums, i.e. where
-//               each tile's codes start in that message, the message's total, and
-//               the check that its length is exactly 8 + 2B + w * total;
-//   validate    per (learner, run of tiles): within every bin the code offsets rise
-//               strictly and stay below the bin's length;
+//   tile_sums   per (learner, run of tiles): check that the message is long enough to
+//               hold its header and counts, check the header's B and the tiles'
+//               per-bin counts, and sum the counts of each tile;
+//   tile_scan   per (message, chunk of tiles): exclusive prefix of the tile sums, i.e.
+//               where each tile's codes start in that message, the message's total,
+//               and the check that its length is exactly 8 + 2B + w * total;
+//   check       per (learner, 128 bins, or one tile of long bins): within every bin
+//               the code offsets rise strictly and stay below the bin's length;
 //   accumulate  per tile of the layers that are streamed: the dense tile is staged
 //               in shared memory, every learner's codes for the tile are applied in
 //               learner order, and the tile is written back;
