@@ -394,19 +394,20 @@ class DeviceRun:
         def ws_of(k, gi):
             return ws_fixed[k][gi] if ws_fixed is not None else self.ws[i % self.ring][k][gi]
 
-        # learners alternate between the launch stream and a second stream, so that one
-        # learner's short launches (finalise, codes) overlap the next one's streaming
-        # kernel; the second stream starts after everything before the step and the
-        # lengths are read once both are done
-        two = self.args.streams > 1 and self.K > 1
+        # the compress calls (learner by learner, launch group by launch group) alternate
+        # between the launch stream and a second stream, so that one call's short
+        # launches (finalise, codes) overlap the next one's streaming kernel; the second
+        # stream starts after everything before the step and the lengths are read once
+        # both are done
+        two = self.args.streams > 1 and self.K * len(self.h) > 1
         if two:
             if not hasattr(self, "side"):
                 self.side = torch.cuda.Stream()
                 self.side_ptr = self.ct.c_void_p(self.side.cuda_stream)
             self.side.wait_stream(torch.cuda.current_stream())
         for k in range(self.K):
-            sptr = self.side_ptr if two and k % 2 else stream_ptr
             for gi, h in enumerate(self.h):
+                sptr = self.side_ptr if two and (k * len(self.h) + gi) % 2 else stream_ptr
                 if k1_events is not None:
                     e = k1_events[k * len(self.h) + gi]
                     L.adacomp_set_timing_events(h.ptr, self.ct.c_void_p(e[0].cuda_event),
@@ -466,7 +467,7 @@ def bench_config(args, layers, K, world):
             "bin_len": sorted({l.bin_len for l in layers}),
             "dw_dtype": layers[0].dw_dtype, "residue_dtype": "f32",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "compress_streams": args.streams if K > 1 else 1,
+            "compress_streams": args.streams if K * (-(-len(layers) // 128)) > 1 else 1,
             "l2": "inputs larger than L2 (dW rotates over %d sets)" % (
                 4 if args.workload in ("resnet50", "fc400k", "lstm_fc") else 2)}
 
@@ -617,7 +618,7 @@ def run_device(args, rank, world):
         out["e2e"] = run_e2e(args, run, layers, sp, world)
     if not args.no_lazy:
         out["lazy_fixup"] = run_lazy(args, run, sp, world, n_elems)
-    if run.K > 1 and args.streams == 2:  # the same steps with every learner on one stream
+    if run.K * len(run.h) > 1 and args.streams == 2:  # the same steps with every call on one stream
         out["one_stream"] = {"value": n_elems * args.steps * world / (one_ms * 1e-3), "unit": "elements/s",
                              "ms_per_step": one_ms / args.steps}
     if not args.no_sgd:
