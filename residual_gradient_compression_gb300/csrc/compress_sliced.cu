@@ -712,12 +712,28 @@ __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KG
         }
         if (poisoned && lane == 0) atomicOr(&lw->err, kErrTimeout);
         if (!poisoned && lane == 0) inflight &= ~(1u << s);
-        LaneGeo q = big_lane_geo(Sl, ly, lane);
-        if (poisoned) q.valid = 0u;  // the stage's data may be incomplete: compute nothing
-        const uint32_t lomask = q.split >= kSeg ? 0xffffu : ((1u << max(q.split, 0)) - 1u);
-        const uint32_t vr = to_reg_order(q.valid, rot);
-        const uint32_t lor = to_reg_order(lomask, rot) & vr;
-        const uint32_t hir = vr & ~lor;
+        // a tile of one bin (L_T > 2048): every slot of the slice belongs to bin 0
+        const bool one_bin = Sl.nb == 1;  // uniform over the CTA
+        LaneGeo q;
+        uint32_t vr, lor, hir;
+        if (one_bin) {
+            q.lane_e = (int)(Sl.a0 - Sl.ts) + kSeg * lane;
+            const int vlo = max(0, Sl.we0 - q.lane_e), vhi = min(kSeg, Sl.we1 - q.lane_e);
+            q.valid = vhi > vlo ? (((1u << (vhi - vlo)) - 1u) << vlo) : 0u;
+            q.bin_lo = 0;
+            q.split = kSeg;
+            if (poisoned) q.valid = 0u;  // the stage's data may be incomplete: compute nothing
+            vr = to_reg_order(q.valid, rot);
+            lor = vr;
+            hir = 0u;
+        } else {
+            q = big_lane_geo(Sl, ly, lane);
+            if (poisoned) q.valid = 0u;
+            const uint32_t lomask = q.split >= kSeg ? 0xffffu : ((1u << max(q.split, 0)) - 1u);
+            vr = to_reg_order(q.valid, rot);
+            lor = to_reg_order(lomask, rot) & vr;
+            hir = vr & ~lor;
+        }
         float* rs = stage_r(s) + kSeg * lane;
         const void* ds = stage_d(s);
         const int doff = ly.dw_bf16 ? (int)(Sl.a0 - ((Sl.ts + Sl.we0) & ~(int64_t)7)) : 0;
@@ -757,13 +773,18 @@ __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KG
         // the warp's bins (Sl.wb0 + 0, 1, 2): maxima as fp32 bits (non-negative, so
         // they order as unsigned integers)
         const int rb = q.bin_lo - Sl.wb0;  // 0, 1 or 2 for lanes holding elements
-        const uint32_t ulo = __float_as_uint(m_lo), uhi = __float_as_uint(m_hi);
-        const uint32_t x0 = __reduce_max_sync(kFull, rb == 0 ? ulo : 0u);
-        const uint32_t x1 = __reduce_max_sync(kFull, max(rb == 1 ? ulo : 0u, rb == 0 ? uhi : 0u));
-        const uint32_t x2 = __reduce_max_sync(kFull, max(rb == 2 ? ulo : 0u, rb == 1 ? uhi : 0u));
-        if (lane < 3) {
-            const uint32_t x = lane == 0 ? x0 : (lane == 1 ? x1 : x2);
-            if (x) atomicMax(&bmax[par * kBigMaxBins + Sl.wb0 + lane], x);
+        if (one_bin) {
+            const uint32_t x0 = __reduce_max_sync(kFull, __float_as_uint(m_lo));
+            if (lane == 0 && x0) atomicMax(&bmax[par * kBigMaxBins], x0);
+        } else {
+            const uint32_t ulo = __float_as_uint(m_lo), uhi = __float_as_uint(m_hi);
+            const uint32_t x0 = __reduce_max_sync(kFull, rb == 0 ? ulo : 0u);
+            const uint32_t x1 = __reduce_max_sync(kFull, max(rb == 1 ? ulo : 0u, rb == 0 ? uhi : 0u));
+            const uint32_t x2 = __reduce_max_sync(kFull, max(rb == 2 ? ulo : 0u, rb == 1 ? uhi : 0u));
+            if (lane < 3) {
+                const uint32_t x = lane == 0 ? x0 : (lane == 1 ? x1 : x2);
+                if (x) atomicMax(&bmax[par * kBigMaxBins + Sl.wb0 + lane], x);
+            }
         }
         __syncthreads();  // the tile's maxima are complete, and the previous tile's counts
         if (warp == W - 1 && l_prev >= 0) finish(t_prev, l_prev, (int)((i + 2) % 3));
@@ -797,13 +818,18 @@ __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KG
                     inflight |= 1u << s;
             }
         }
-        const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & hir);
-        const uint32_t n0 = __reduce_add_sync(kFull, rb == 0 ? c_lo : 0u);
-        const uint32_t n1 = __reduce_add_sync(kFull, (rb == 1 ? c_lo : 0u) + (rb == 0 ? c_hi : 0u));
-        const uint32_t n2 = __reduce_add_sync(kFull, (rb == 2 ? c_lo : 0u) + (rb == 1 ? c_hi : 0u));
-        if (lane < 3) {
-            const uint32_t x = lane == 0 ? n0 : (lane == 1 ? n1 : n2);
-            if (x) atomicAdd(&bcnt[par * kBigMaxBins + Sl.wb0 + lane], x);
+        if (one_bin) {
+            const uint32_t n0 = __reduce_add_sync(kFull, (uint32_t)__popc(fr));
+            if (lane == 0 && n0) atomicAdd(&bcnt[par * kBigMaxBins], n0);
+        } else {
+            const uint32_t c_lo = __popc(fr & lor), c_hi = __popc(fr & hir);
+            const uint32_t n0 = __reduce_add_sync(kFull, rb == 0 ? c_lo : 0u);
+            const uint32_t n1 = __reduce_add_sync(kFull, (rb == 1 ? c_lo : 0u) + (rb == 0 ? c_hi : 0u));
+            const uint32_t n2 = __reduce_add_sync(kFull, (rb == 2 ? c_lo : 0u) + (rb == 1 ? c_hi : 0u));
+            if (lane < 3) {
+                const uint32_t x = lane == 0 ? n0 : (lane == 1 ? n1 : n2);
+                if (x) atomicAdd(&bcnt[par * kBigMaxBins + Sl.wb0 + lane], x);
+            }
         }
         if (Sl.we1 > Sl.we0) {
             sent[mi] = (uint16_t)fr;  // register order (the emitting kernel reorders)
