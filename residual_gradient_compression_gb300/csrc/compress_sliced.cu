@@ -435,13 +435,27 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
             hist_slices = 0;
         }
         ++hist_slices;
-        const LaneGeo q = lane_geo(Sl, ly, lane);
-        const uint32_t lomask = q.split >= kSeg ? 0xffffu : ((1u << max(q.split, 0)) - 1u);  // slots of bin_lo
+        const bool one_bin = ly.bpw == 1;  // warp-uniform: the slice is one bin (m_hi and c_hi are 0)
+        LaneGeo q;
+        uint32_t vr, lor, hir;
         // register order: chunk k of the lane is held at registers 4k..4k+3 and is
         // slot chunk k ^ rot; every per-element test below uses a compile-time bit
-        const uint32_t vr = to_reg_order(q.valid, rot);
-        const uint32_t lor = to_reg_order(lomask, rot) & vr;  // valid slots of bin_lo
-        const uint32_t hir = vr & ~lor;                        // valid slots of bin_lo + 1
+        if (one_bin) {  // every valid slot belongs to the slice's only bin
+            q.lane_e = (int)(Sl.a0 - Sl.ts) + kSeg * lane;
+            const int vlo = max(0, Sl.we0 - q.lane_e), vhi = min(kSeg, Sl.we1 - q.lane_e);
+            q.valid = vhi > vlo ? (((1u << (vhi - vlo)) - 1u) << vlo) : 0u;
+            q.bin_lo = 0;
+            q.split = kSeg;
+            vr = to_reg_order(q.valid, rot);
+            lor = vr;
+            hir = 0u;
+        } else {
+            q = lane_geo(Sl, ly, lane);
+            const uint32_t lomask = q.split >= kSeg ? 0xffffu : ((1u << max(q.split, 0)) - 1u);  // slots of bin_lo
+            vr = to_reg_order(q.valid, rot);
+            lor = to_reg_order(lomask, rot) & vr;  // valid slots of bin_lo
+            hir = vr & ~lor;                        // valid slots of bin_lo + 1
+        }
         float ah[4][4];             // |probe| per register slot
         uint32_t ngr = 0;  // G < 0 (register order; kept for the deferred fix-up's codes only)
         float m_lo = 0.0f, m_hi = 0.0f;
@@ -462,7 +476,6 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
                     inflight |= 1u << s;
             }
         }
-        const bool one_bin = ly.bpw == 1;  // warp-uniform: the slice is one bin (m_hi and c_hi are 0)
         if (one_bin) {  // a warp reduction instead of 32 lanes' atomics on one word
             const uint32_t x = __reduce_max_sync(kFull, __float_as_uint(m_lo));
             if (lane == 0) wg[0] = x;
@@ -474,7 +487,7 @@ __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constan
         uint32_t fr = 0;  // sent slots, register order
         if (q.valid) {
             const float gm_lo = __uint_as_float(wg[q.bin_lo]);
-            const float gm_hi = lomask != 0xffffu ? __uint_as_float(wg[q.bin_lo + 1]) : 0.0f;
+            const float gm_hi = hir ? __uint_as_float(wg[q.bin_lo + 1]) : 0.0f;
 #pragma unroll
             for (int k = 0; k < 4; ++k) {
 #pragma unroll
