@@ -732,14 +732,12 @@ __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile&
     return P;
 }
 
-__device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A, int K, int bin, int kb,
-                                              const BinPrep& P, float* sd, int lane)
+template <bool kWide>
+__device__ __forceinline__ void acc_bin_apply_t(const KLayer& ly, int K, int kb, const BinPrep& P, float* x0,
+                                                uint32_t len, int lane)
 {
-    const uint32_t len = (A.first_bin + bin == ly.nbins - 1)
-                             ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len) : (uint32_t)ly.bin_len;
-    float* x0 = sd + (int64_t)bin * ly.bin_len;
-    const bool wide = ly.code_bytes == 2;
     const int kn = min(32, K - kb);
+    const uint32_t big = __ballot_sync(kFull, P.c > 32u);  // learners with more codes than lanes in the bin
     for (int k0 = 0; k0 < kn; k0 += kAccWindow) {
         uint32_t cw[kAccWindow];
 #pragma unroll
@@ -748,30 +746,40 @@ __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A
             const uint32_t ck = __shfl_sync(kFull, P.c, kk);
             const uint8_t* cp = reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)P.codes, kk));
             cw[w] = 0xffffffffu;
-            if (k0 + w < kn && (uint32_t)lane < ck) cw[w] = wide ? reinterpret_cast<const uint16_t*>(cp)[lane] : cp[lane];
+            if (k0 + w < kn && (uint32_t)lane < ck)
+                cw[w] = kWide ? (uint32_t)reinterpret_cast<const uint16_t*>(cp)[lane] : (uint32_t)cp[lane];
         }
 #pragma unroll
         for (int w = 0; w < kAccWindow; ++w) {
             if (k0 + w >= kn) break;
             const int kk = k0 + w;
-            const uint32_t ck = __shfl_sync(kFull, P.c, kk);
             const float s = __shfl_sync(kFull, P.s, kk);
-            if (cw[w] != 0xffffffffu) {
-                const uint32_t o = cw[w] >> 1;
-                if (o < len) x0[o] = __fadd_rn(x0[o], (cw[w] & 1u) ? -s : s);  // always in range once validated
-            }
-            if (ck > 32u) {  // more codes than lanes in this bin: the rest, in rounds
+            const uint32_t o = cw[w] >> 1;  // 0x7fffffff for no code: never below a bin length
+            // sign * s by flipping the sign bit of s
+            if (o < len) x0[o] = __fadd_rn(x0[o], __int_as_float(__float_as_int(s) ^ (int)(cw[w] << 31)));
+            if ((big >> kk) & 1u) {  // more codes than lanes in this bin: the rest, in rounds
+                const uint32_t ck = __shfl_sync(kFull, P.c, kk);
                 const uint8_t* cp =
                     reinterpret_cast<const uint8_t*>(__shfl_sync(kFull, (unsigned long long)P.codes, kk));
                 for (uint32_t i = 32 + lane; i < ck; i += 32) {
-                    const uint32_t code = wide ? reinterpret_cast<const uint16_t*>(cp)[i] : cp[i];
-                    const uint32_t o = code >> 1;
-                    if (o < len) x0[o] = __fadd_rn(x0[o], (code & 1u) ? -s : s);
+                    const uint32_t code = kWide ? (uint32_t)reinterpret_cast<const uint16_t*>(cp)[i] : (uint32_t)cp[i];
+                    const uint32_t o2 = code >> 1;
+                    if (o2 < len) x0[o2] = __fadd_rn(x0[o2], __int_as_float(__float_as_int(s) ^ (int)(code << 31)));
                 }
             }
             __syncwarp();  // learner kk's additions come before learner kk + 1's
         }
     }
+}
+
+__device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A, int K, int bin, int kb,
+                                              const BinPrep& P, float* sd, int lane)
+{
+    const uint32_t len = (A.first_bin + bin == ly.nbins - 1)
+                             ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len) : (uint32_t)ly.bin_len;
+    float* x0 = sd + (int64_t)bin * ly.bin_len;
+    if (ly.code_bytes == 2) acc_bin_apply_t<true>(ly, K, kb, P, x0, len, lane);
+    else acc_bin_apply_t<false>(ly, K, kb, P, x0, len, lane);
 }
 
 // One optimiser step over tile A's elements, the gradient sum in gs (element ts + x at
