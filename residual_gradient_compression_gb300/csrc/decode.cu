@@ -542,6 +542,21 @@ __device__ __forceinline__ AccTile acc_tile(const KGroup& g, const LayerIndex& X
     return A;
 }
 
+// Thread 0, fused optimiser steps: prefetch tile t's weights and optimiser state
+// (the 16-byte-aligned interior of the tile) into L2 a tile ahead, so that the
+// optimiser step's loads of them hit L2.
+template <int kOpt>
+__device__ __forceinline__ void opt_prefetch(const KGroup& g, const LayerIndex& X, const DecodeParams& p, uint32_t t)
+{
+    const AccTile A = acc_tile(g, X, t);
+    const int64_t c0 = (A.ts + 3) & ~(int64_t)3, c1 = A.te & ~(int64_t)3;
+    if (c1 <= c0) return;
+    const uint32_t bytes = (uint32_t)(c1 - c0) * 4u;
+    ptx::bulk_prefetch_l2(p.dense[A.layer] + c0, bytes);
+    ptx::bulk_prefetch_l2(p.mom[A.layer] + c0, bytes);
+    if (kOpt == kOptAdam) ptx::bulk_prefetch_l2(p.mom2[A.layer] + c0, bytes);
+}
+
 // Thread 0: start tile t's dense slice into a stage (plain sum only). The copy ends
 // at the 16-byte boundary at or after the tile unless that lies past the array, in
 // which case the last few elements are loaded with plain loads.
@@ -899,6 +914,7 @@ __global__ void __launch_bounds__(kDecThreads, 5) accumulate_kernel(const __grid
         for (int k = 0; k < kAccStages; ++k) ptx::mbar_init(&bar[k], 1);
         ptx::fence_mbar_init();
         if (!kFused && t < T) acc_issue<kOpt>(g, X, p, t, stage(0), arr_floats, &bar[0]);
+        if (kFused && t < T) opt_prefetch<kOpt>(g, X, p, t);
     }
     __syncthreads();
 
@@ -910,6 +926,7 @@ __global__ void __launch_bounds__(kDecThreads, 5) accumulate_kernel(const __grid
             ptx::bulk_wait_read0();  // the store of the tile stage i + 1 held has read it
             acc_issue<kOpt>(g, X, p, t1, stage(i + 1), arr_floats, &bar[(i + 1) % kAccStages]);
         }
+        if (kFused && tid == 0 && t1 < T) opt_prefetch<kOpt>(g, X, p, t1);
         const AccTile A = acc_tile(g, X, t);
         const KLayer& ly = g.layer[A.layer];
         const int l = A.layer;
