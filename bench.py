@@ -635,7 +635,12 @@ def run_decode_sgd(args, run, sp, world, layers, adam=False):
     ct = run.ct
     numels = [l.numel for l in layers]
     bufs = [_flat_views(numels, torch.float32, run.dev) for _ in range(3 if adam else 2)]
+    # weights, and optimiser state as it stands some steps into training (nonzero
+    # nearly everywhere: every element has received codes in some earlier step)
     bufs[0][0].normal_()
+    bufs[1][0].normal_(0.0, 1e-4)
+    if adam:
+        bufs[2][0].uniform_(1e-9, 1e-8)
     VP = ct.c_void_p
     ptrs = [[(VP * len(g))(*[views[i].data_ptr() for i in g]) for g in run.gidx] for _, views in bufs]
     stream = torch.cuda.current_stream()
@@ -682,8 +687,9 @@ def run_decode_sgd(args, run, sp, world, layers, adam=False):
     peak, _ = measured_hbm_gbs()
     return {"ms_per_decode": ms, "algorithmic_bytes": algo, "achieved_gbs": algo / (ms * 1e-3) / 1e9,
             "frac": algo / (ms * 1e-3) / 1e9 / peak,
-            "optimizer": ("Adam, lr 1e-3, betas (0.9, 0.999), eps 1e-8, step 10, grad_scale 1/K" if adam
-                          else "momentum SGD, lr 1e-3, mu 0.9, grad_scale 1/K")}
+            "optimizer": ("Adam, lr 1e-3, betas (0.9, 0.999), eps 1e-8, step 10, grad_scale 1/K, "
+                          "moments m ~ N(0, 1e-4), v ~ U(1e-9, 1e-8)" if adam
+                          else "momentum SGD, lr 1e-3, mu 0.9, grad_scale 1/K, momentum ~ N(0, 1e-4)")}
 
 
 def run_lazy(args, run, sp, world, n_elems):

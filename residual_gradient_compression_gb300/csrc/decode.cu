@@ -814,7 +814,12 @@ __device__ __forceinline__ void opt_elem(const DecodeParams& p, float gsum, floa
         const float vv = __fadd_rn(__fmul_rn(p.beta2, v), __fmul_rn(__fsub_rn(1.0f, p.beta2), __fmul_rn(gx, gx)));
         m = mm;
         v = vv;
-        const float ratio = __fdiv_rn(__fdiv_rn(mm, p.bc1), __fadd_rn(__fsqrt_rn(__fdiv_rn(vv, p.bc2)), p.eps));
+        // both moments zero (an element no learner has sent yet) and eps > 0: m/bc1 is
+        // mm itself (a signed zero), sqrt(v/bc2) + eps is eps, and so the ratio is mm
+        // exactly; the divisions and the square root are skipped
+        const float ratio = (mm == 0.0f && vv == 0.0f && p.eps > 0.0f)
+                                ? mm
+                                : __fdiv_rn(__fdiv_rn(mm, p.bc1), __fadd_rn(__fsqrt_rn(__fdiv_rn(vv, p.bc2)), p.eps));
         w = __fsub_rn(w, __fmul_rn(p.lr, ratio));
     }
 }
