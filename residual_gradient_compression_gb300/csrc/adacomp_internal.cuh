@@ -212,9 +212,9 @@ __host__ __device__ inline uint32_t val_tiles_per_task(uint32_t bins_per_tile)
 }
 
 // Code checks: bins of kChkLongBin elements or more take one task per tile, the lanes
-// over each bin's codes; shorter bins one task per kChkBins bins, lane b walking bins
-// b, b + 32, ...: floor(kChkBins / bpt) whole tiles per task, or, for tiles of more
-// than kChkBins bins, ceil(bpt / kChkBins) tasks per tile.
+// over each bin's codes; shorter bins one task per kChkBins bins, the lanes over the
+// task's contiguous run of codes: floor(kChkBins / bpt) whole tiles per task, or, for
+// tiles of more than kChkBins bins, ceil(bpt / kChkBins) tasks per tile.
 constexpr uint32_t kChkBins = 128;
 constexpr int32_t kChkLongBin = 1024;
 __host__ __device__ inline uint32_t chk_tasks(uint32_t num_tiles, uint32_t bins_per_tile, int32_t bin_len)

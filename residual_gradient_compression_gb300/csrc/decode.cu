@@ -315,11 +315,12 @@ __global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_co
 // rejected: within every bin the code offsets must rise strictly (a message gives
 // each element at most one code) and stay below the bin's length (L_T, or the
 // layer's last, shorter bin); otherwise the message is rejected as a whole, before
-// anything is added. Lane b takes bins b, b + 32, ... of the task: the bins' counts
-// (coalesced), the exclusive prefix of the task's counts (warp scans, kept in shared
-// memory), the index of each bin's first code (its tile's offset plus the counts of
-// its tile's bins before it), and then it walks each of its bins' codes in order,
-// four loads at a time.
+// anything is added. Bins shorter than kChkLongBin: lane b takes the counts of bins
+// b, b + 32, ... of the task (coalesced) and their exclusive prefix (warp scans); the
+// task's codes are one contiguous run, which the lanes read 32 at a time (coalesced),
+// each offset compared with the one before it (a shuffle) and with its bin's length;
+// the descents found are matched against those at the bins' first codes. Longer
+// bins: one task per tile, the lanes over each bin's codes.
 __device__ __forceinline__ int layer_of_chk(const uint32_t* cb, int num_layers, uint32_t u)
 {
     int lo = 0, hi = num_layers - 1;
@@ -331,17 +332,79 @@ __device__ __forceinline__ int layer_of_chk(const uint32_t* cb, int num_layers, 
     return lo;
 }
 
-__global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constant__ KGroup g,
+// The lanes over a run of `run` codes of kW bytes from `codes` (a message whose start
+// is 16-byte aligned, so every 16-byte block that holds one of its bytes may be read):
+// 16 bytes per lane, i.e. 16 / kW codes, 32 lanes a round, kChkDepth rounds loaded
+// at once. Counts the descents (a
+// code whose offset is not above that of the code before it; the first code has none
+// before it) and the largest offset of the lane's codes.
+constexpr int kChkDepth = 4;
+
+template <int kW>
+__device__ __forceinline__ void chk_run(const uint8_t* codes, uint32_t run, uint32_t& descents, int32_t& omax,
+                                        int lane)
+{
+    constexpr int E = 16 / kW;
+    const uintptr_t a = reinterpret_cast<uintptr_t>(codes);
+    const uint4* ch = reinterpret_cast<const uint4*>(a & ~uintptr_t(15));
+    const int32_t skip = (int32_t)((a & 15u) / kW);  // codes of the first block before position 0
+    const uint32_t nch = (uint32_t)(skip + (int64_t)run + E - 1) / E;
+    int32_t carry = -1;  // the offset before the lane's first code, from the previous round
+    // kChkDepth rounds' loads are issued before the first of them is used
+    for (uint32_t g0 = 0; g0 < nch; g0 += 32 * kChkDepth) {
+        uint4 v[kChkDepth];
+#pragma unroll
+        for (int d = 0; d < kChkDepth; ++d) {
+            const uint32_t ci = g0 + 32 * d + (uint32_t)lane;
+            v[d] = ci < nch ? ch[ci] : make_uint4(0u, 0u, 0u, 0u);
+        }
+#pragma unroll
+        for (int d = 0; d < kChkDepth; ++d) {
+            const uint32_t ci = g0 + 32 * d + (uint32_t)lane;
+            if (g0 + 32 * d >= nch) break;
+            const int64_t q0 = (int64_t)ci * E - skip;  // position of the block's first code
+            const uint32_t wv[4] = {v[d].x, v[d].y, v[d].z, v[d].w};
+            int32_t o[E];
+#pragma unroll
+            for (int e = 0; e < E; ++e) {
+                const uint32_t code =
+                    kW == 2 ? (wv[e >> 1] >> ((e & 1) * 16)) & 0xffffu : (wv[e >> 2] >> ((e & 3) * 8)) & 0xffu;
+                o[e] = q0 + e < 0 ? -1 : (int32_t)(code >> 1);
+            }
+            int32_t prev = __shfl_up_sync(kFull, o[E - 1], 1);
+            if (lane == 0) prev = carry;
+            carry = __shfl_sync(kFull, o[E - 1], 31);
+            if (q0 >= 0 && q0 + E <= (int64_t)run) {  // every code of the block is in the run
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    descents += o[e] <= prev ? 1u : 0u;
+                    omax = max(omax, o[e]);
+                    prev = o[e];
+                }
+            } else if (ci < nch) {  // the run's first or last block
+#pragma unroll
+                for (int e = 0; e < E; ++e) {
+                    const int64_t q = q0 + e;
+                    if (q >= 0 && q < (int64_t)run) {
+                        descents += o[e] <= prev ? 1u : 0u;
+                        omax = max(omax, o[e]);
+                    }
+                    prev = o[e];
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kDecThreads, 4) check_kernel(const __grid_constant__ KGroup g,
                                                             const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
     constexpr int R = (int)(kChkBins / 32);  // bins per lane
     __shared__ uint32_t cb[kMaxGroup + 1];
-    __shared__ uint32_t ex_s[kDecThreads / 32][kChkBins];
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) cb[e] = p.chk_begin[e];
     __syncthreads();
     const int K = p.K;
     const int lane = threadIdx.x & 31;
-    uint32_t* ex = ex_s[threadIdx.x >> 5];
     const uint32_t per_learner = cb[g.num_layers];
     const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
     if (task >= (uint64_t)K * per_learner) return;
@@ -411,7 +474,7 @@ __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constan
         for (uint32_t b = tb0 + lane; b < b0; b += 32) pre += cnt[b];
         pre = __reduce_add_sync(kFull, pre);
     }
-    uint32_t c[R];
+    uint32_t c[R], ex[R];  // bin r * 32 + lane: its count and the task's codes before it
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const uint32_t j = r * 32 + lane;
@@ -426,47 +489,37 @@ __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constan
             const uint32_t y = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += y;
         }
-        ex[r * 32 + lane] = run + incl - c[r];
+        ex[r] = run + incl - c[r];
         run += __shfl_sync(kFull, incl, 31);
     }
-    __syncwarp();
-    const uint64_t* toff = tile_offsets(ws, k, g.total_tiles) + ly.tile_begin;
-    const uint8_t* codes = msg + 8 + 2ull * ly.nbins;
+    // The task's codes are contiguous: positions 0 .. run - 1 from its first code.
+    const uint64_t first = tile_offsets(ws, k, g.total_tiles)[ly.tile_begin + b0 / bpt] + pre;
     const bool wide = ly.code_bytes == 2;
-    const uint32_t last_len = (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
-    bool ok = true;
+    const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (uint64_t)ly.code_bytes * first;
+    auto off_at = [&](uint32_t q) -> int32_t {
+        return (int32_t)((wide ? reinterpret_cast<const uint16_t*>(codes)[q] : codes[q]) >> 1);
+    };
+    // A descent is a position q >= 1 whose offset is not above the one before it. The
+    // offsets rise strictly within every bin exactly when every descent is the first
+    // code of a bin, i.e. when the descents number as many as the first codes (of the
+    // nonempty bins, past position 0) that are descents.
+    uint32_t at_starts = 0;
 #pragma unroll
-    for (int r = 0; r < R; ++r) {
-        const uint32_t j = r * 32 + lane;
-        if (j >= nb || c[r] == 0u) continue;
-        const uint32_t gb = b0 + j;          // the bin, in the layer
-        const uint32_t tile = gb / bpt;
-        // first code of the bin: its tile's offset plus its tile's codes before it
-        uint64_t first = toff[tile] + ex[j];
-        if (whole) first -= ex[tile * bpt - b0];
-        else first += pre;
-        const uint32_t len = gb == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len;
-        const uint32_t cn = c[r];
-        int64_t prev = -1;
-        uint32_t q = 0;
-        for (; q + 4 <= cn; q += 4) {
-            uint32_t v[4];
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                v[e] = wide ? reinterpret_cast<const uint16_t*>(codes)[first + q + e] : codes[first + q + e];
-#pragma unroll
-            for (int e = 0; e < 4; ++e) {
-                const uint32_t o = v[e] >> 1;
-                ok = ok && o < len && (int64_t)o > prev;
-                prev = o;
-            }
-        }
-        for (; q < cn; ++q) {
-            const uint32_t o = (wide ? reinterpret_cast<const uint16_t*>(codes)[first + q] : codes[first + q]) >> 1;
-            ok = ok && o < len && (int64_t)o > prev;
-            prev = o;
-        }
+    for (int r = 0; r < R; ++r)
+        if (c[r] != 0u && ex[r] != 0u) at_starts += off_at(ex[r]) <= off_at(ex[r] - 1u) ? 1u : 0u;
+    uint32_t descents = 0;
+    int32_t omax = -1;
+    if (run) {
+        if (wide) chk_run<2>(codes, run, descents, omax, lane);
+        else chk_run<1>(codes, run, descents, omax, lane);
     }
+    // Every offset is below its bin's length: L_T, except in the layer's last bin, whose
+    // codes end the task when the task holds that bin; once the offsets rise within it,
+    // its last code is its largest.
+    bool ok = __reduce_max_sync(kFull, (uint32_t)(omax + 1)) <= (uint32_t)ly.bin_len &&
+              __reduce_add_sync(kFull, descents) == __reduce_add_sync(kFull, at_starts);
+    if (ok && b0 + nb == ly.nbins && cnt[ly.nbins - 1] != 0u)
+        ok = off_at(run - 1u) < (int32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
     if (!__all_sync(kFull, ok) && lane == 0) ws[16 + l * K + k] = 1;
 }
 
