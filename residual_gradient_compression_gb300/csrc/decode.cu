@@ -762,7 +762,7 @@ __device__ __forceinline__ void acc_walk(const KLayer& ly, const AccTile& A, con
 // once; none depends on the dense tile, so this runs while that is loading).
 // acc_bin_apply: the codes of kAccWindow learners at a time are loaded at once (lane
 // i holding code i of each) and added in learner order.
-constexpr int kAccWindow = 16;
+constexpr int kAccWindow = 8;
 
 struct BinPrep {
     const uint8_t* codes;  // the learner's first code for this bin
@@ -800,14 +800,43 @@ __device__ __forceinline__ BinPrep acc_bin_prep(const KLayer& ly, const AccTile&
     return P;
 }
 
+// Per warp, one 16-byte entry per learner of the round: its first code's address,
+// its code count in the bin and its scale, read back as warp-wide broadcasts.
+struct alignas(16) LearnerBin {
+    const uint8_t* codes;
+    uint32_t c;
+    float s;
+};
+
 template <bool kWide>
 __device__ __forceinline__ void acc_bin_apply_t(const KLayer& ly, int K, int kb, const BinPrep& P, float* x0,
-                                                uint32_t len, int lane)
+                                                uint32_t len, LearnerBin* lb, int lane)
 {
     const int kn = min(32, K - kb);
     const uint32_t big = __ballot_sync(kFull, P.c > 32u);  // learners with more codes than lanes in the bin
+    lb[lane] = LearnerBin{P.codes, P.c, P.s};
+    __syncwarp();
     for (int k0 = 0; k0 < kn; k0 += kAccWindow) {
         uint32_t cw[kAccWindow];
+        if (kn - k0 >= kAccWindow && ((big >> k0) & ((1u << kAccWindow) - 1u)) == 0u) {
+            // a whole window of learners with at most 32 codes each in the bin (warp-uniform)
+#pragma unroll
+            for (int w = 0; w < kAccWindow; ++w) {
+                const LearnerBin e = lb[k0 + w];
+                cw[w] = 0xffffffffu;
+                if ((uint32_t)lane < e.c)
+                    cw[w] = kWide ? (uint32_t)reinterpret_cast<const uint16_t*>(e.codes)[lane] : (uint32_t)e.codes[lane];
+            }
+#pragma unroll
+            for (int w = 0; w < kAccWindow; ++w) {
+                const uint32_t sb = __float_as_uint(lb[k0 + w].s);
+                const uint32_t o = cw[w] >> 1;
+                // sign * s: adding the code's low bit at bit 31 flips the sign bit of s
+                if (o < len) x0[o] = __fadd_rn(x0[o], __uint_as_float(sb + (cw[w] << 31)));
+                __syncwarp();
+            }
+            continue;
+        }
 #pragma unroll
         for (int w = 0; w < kAccWindow; ++w) {
             const int kk = min(k0 + w, kn - 1);
@@ -841,13 +870,13 @@ __device__ __forceinline__ void acc_bin_apply_t(const KLayer& ly, int K, int kb,
 }
 
 __device__ __forceinline__ void acc_bin_apply(const KLayer& ly, const AccTile& A, int K, int bin, int kb,
-                                              const BinPrep& P, float* sd, int lane)
+                                              const BinPrep& P, float* sd, LearnerBin* lb, int lane)
 {
     const uint32_t len = (A.first_bin + bin == ly.nbins - 1)
                              ? (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len) : (uint32_t)ly.bin_len;
     float* x0 = sd + (int64_t)bin * ly.bin_len;
-    if (ly.code_bytes == 2) acc_bin_apply_t<true>(ly, K, kb, P, x0, len, lane);
-    else acc_bin_apply_t<false>(ly, K, kb, P, x0, len, lane);
+    if (ly.code_bytes == 2) acc_bin_apply_t<true>(ly, K, kb, P, x0, len, lb, lane);
+    else acc_bin_apply_t<false>(ly, K, kb, P, x0, len, lb, lane);
 }
 
 // One optimiser step over tile A's elements, the gradient sum in gs (element ts + x at
@@ -947,6 +976,8 @@ __global__ void __launch_bounds__(kDecThreads, 5) accumulate_kernel(const __grid
     const int K = p.K;
     auto stage = [&](int i) { return stage0 + (size_t)(i % kAccStages) * (stage_bytes / 4); };
     __shared__ LayerIndex X;
+    __shared__ LearnerBin lb_s[kDecThreads / 32][32];
+    LearnerBin* lbw = lb_s[warp];
     load_index(X, g, ws, p.K, kFused);
     __syncthreads();
     // The CTA's tiles are G0, G0 + GS, ...; tiles of layers summed in place (by the
@@ -1019,7 +1050,7 @@ __global__ void __launch_bounds__(kDecThreads, 5) accumulate_kernel(const __grid
             if (b0 < b1) {
                 for (int kb = 0; kb < K; kb += 32) {
                     if (kb) bp = acc_bin_prep(ly, A, p, X, ws, T, t, l, b0, kb, lane);
-                    acc_bin_apply(ly, A, K, b0, kb, bp, sd, lane);
+                    acc_bin_apply(ly, A, K, b0, kb, bp, sd, lbw, lane);
                 }
             }
         } else if (b0 < b1) {
