@@ -5,6 +5,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <utility>
 
 namespace adacomp {
 
@@ -387,6 +388,13 @@ __device__ __forceinline__ uint64_t globaltimer()
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
     return t;
 }
+
+// Programmatic dependent launch: a kernel launched with the programmatic stream
+// serialisation attribute may start before the kernel ahead of it in the stream has
+// finished; griddep_wait blocks until that kernel has completed and its writes are
+// visible, and griddep_launch lets the next such kernel start early.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void griddep_launch() { asm volatile("griddepcontrol.launch_dependents;" :::); }
 
 }  // namespace ptx
 }  // namespace adacomp

@@ -112,6 +112,7 @@ __device__ __forceinline__ Run run_of(const KGroup& g, const uint32_t* vb, uint3
 __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_constant__ KGroup g,
                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
+    ptx::griddep_launch();  // the scan's launch may start; it waits for these sums
     __shared__ uint32_t vb[kMaxGroup + 1];
     __shared__ uint32_t sums_s[kDecThreads / 32][kValBins];
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) vb[e] = p.val_begin[e];
@@ -190,6 +191,8 @@ __global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_co
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws,
                                                                  uint32_t CH)
 {
+    ptx::griddep_wait();  // the tile sums
+    ptx::griddep_launch();
     __shared__ unsigned long long wt[kScanPer][kScanWarps];
     __shared__ unsigned long long wx[kScanPer][kScanWarps];
     __shared__ unsigned long long red[kScanWarps];
@@ -399,6 +402,8 @@ __device__ __forceinline__ void chk_run(const uint8_t* codes, uint32_t run, uint
 __global__ void __launch_bounds__(kDecThreads, 4) check_kernel(const __grid_constant__ KGroup g,
                                                             const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
+    ptx::griddep_wait();  // the offsets and the rejections so far
+    ptx::griddep_launch();
     constexpr int R = (int)(kChkBins / 32);  // bins per lane
     __shared__ uint32_t cb[kMaxGroup + 1];
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) cb[e] = p.chk_begin[e];
@@ -961,6 +966,8 @@ template <int kOpt>
 __global__ void __launch_bounds__(kDecThreads, 5) accumulate_kernel(const __grid_constant__ KGroup g,
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
+    ptx::griddep_wait();  // every check
+    ptx::griddep_launch();
     constexpr bool kFused = kOpt != kOptNone;
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t stage_bytes = acc_stage_bytes(g.tile_cap, kOpt);
@@ -1114,6 +1121,7 @@ __global__ void __launch_bounds__(kDecThreads) sparse_accumulate_kernel(const __
                                                                         const __grid_constant__ DecodeParams p,
                                                                         uint8_t* ws)
 {
+    ptx::griddep_wait();  // the layers that were streamed are done
     extern __shared__ uint32_t sp_dyn[];  // per warp: the bins' count prefix
     __shared__ LayerIndex X;
     for (int e = threadIdx.x; e < g.num_layers; e += kDecThreads) {
@@ -1161,6 +1169,26 @@ DecDeviceInfo g_ddev[64];
 
 }  // namespace
 
+// Launches a kernel that begins with ptx::griddep_wait() behind the previous kernel of
+// the stream with programmatic dependent launch: its blocks may be scheduled while
+// that kernel's last blocks run, and wait there until its writes are visible.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                         Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cudaStream_t stream)
 {
     int dev = 0;
@@ -1184,12 +1212,10 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     uint32_t CH = kScanPer * kScanThreads * 2;
     while ((max_tiles + CH - 1) / CH > 64u) CH += kScanPer * kScanThreads;
     const dim3 sgrid((max_tiles + CH - 1) / CH, (unsigned)(g.num_layers * p.K));
-    tile_scan_kernel<<<sgrid, kScanThreads, 0, stream>>>(g, p, w, CH);
-    e = cudaGetLastError();
+    e = launch_after(tile_scan_kernel, sgrid, dim3(kScanThreads), 0, stream, g, p, w, CH);
     if (e != cudaSuccess) return e;
     const uint64_t ctasks = (uint64_t)p.K * p.chk_begin[g.num_layers];  // (learner, kChkBins bins) tasks
-    check_kernel<<<(unsigned)((ctasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
-    e = cudaGetLastError();
+    e = launch_after(check_kernel, dim3((unsigned)((ctasks + wpb - 1) / wpb)), dim3(kDecThreads), 0, stream, g, p, w);
     if (e != cudaSuccess) return e;
     const int opt = p.opt;
     const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins, opt);
@@ -1209,8 +1235,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const long long cap = (long long)di.sms * occ;
     const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
-    kern<<<grid, kDecThreads, smem, stream>>>(g, p, w);
-    e = cudaGetLastError();
+    e = launch_after(kern, dim3(grid), dim3(kDecThreads), smem, stream, g, p, w);
     if (e != cudaSuccess || opt != kOptNone) return e;
     // the layers summed in place (the kernel skips the others)
     const uint32_t sp_smem = (kDecThreads / 32) * ((uint32_t)g.max_bins + 2) * 4;
@@ -1222,8 +1247,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     const uint32_t sp_need = (g.total_tiles + kDecThreads / 32 - 1) / (kDecThreads / 32);
     const uint32_t sp_cap = (uint32_t)di.sms * 8;  // persistent: eight CTAs of eight warps per SM
     const uint32_t sp_grid = sp_need < sp_cap ? sp_need : sp_cap;
-    sparse_accumulate_kernel<<<sp_grid, kDecThreads, sp_smem, stream>>>(g, p, w);
-    return cudaGetLastError();
+    return launch_after(sparse_accumulate_kernel, dim3(sp_grid), dim3(kDecThreads), sp_smem, stream, g, p, w);
 }
 
 }  // namespace adacomp
