@@ -250,6 +250,26 @@ struct DecodeParams {
 };
 
 // ---------------------------------------------------------------- host-side launchers
+// Launches a kernel that begins with ptx::griddep_wait() behind the previous kernel of
+// the stream with programmatic dependent launch: its blocks may be scheduled while
+// that kernel's last blocks run, and wait there until its writes are visible.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                         Args&&... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
 cudaError_t launch_compress(const KGroup& g, void* ws, cudaStream_t stream, cudaEvent_t ev_before = nullptr,
                             cudaEvent_t ev_mid = nullptr, cudaEvent_t ev_after = nullptr);
 cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cudaStream_t stream);

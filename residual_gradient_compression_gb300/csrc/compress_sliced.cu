@@ -349,6 +349,8 @@ __device__ __forceinline__ void lane_slots(const KLayer& ly, const Slice& Sl, co
 template <int S, bool kLazy, bool kLS>
 __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
 {
+    ptx::griddep_wait();  // the kernel ahead in the stream
+    ptx::griddep_launch();
     extern __shared__ __align__(128) uint8_t smem[];
     const SlicePlan P = slice_plan(g.d_size, S, g.num_layers);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -610,6 +612,8 @@ __device__ __forceinline__ void chunk_g(bool bf16, const float* rs, const void* 
 template <int S, bool kLazy, bool kLS>
 __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
 {
+    ptx::griddep_wait();  // the kernel ahead in the stream
+    ptx::griddep_launch();
     extern __shared__ __align__(128) uint8_t smem[];
     const int W = (int)(blockDim.x >> 5);
     const BigPlan P = big_plan(g.d_size, S, g.num_layers, W);
@@ -879,6 +883,8 @@ constexpr int kFinUnroll = 8;
 __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __grid_constant__ KGroup g,
                                                                      uint8_t* __restrict__ ws)
 {
+    ptx::griddep_wait();  // the kernel ahead in the stream
+    ptx::griddep_launch();
     __shared__ unsigned long long tmp[256];
     __shared__ unsigned long long words[kSumWords];
     __shared__ unsigned long long red[kFinWarps];
@@ -1024,6 +1030,8 @@ template <bool kBig>
 __global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(const __grid_constant__ KGroup g,
                                                                              uint8_t* __restrict__ ws)
 {
+    ptx::griddep_wait();  // the kernel ahead in the stream
+    ptx::griddep_launch();
     constexpr int H = kBig ? 2 : 1;
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
     __shared__ uint16_t lists[kEmitWarps][kListCap];
@@ -1153,6 +1161,8 @@ template <bool kBig>
 __global__ void __launch_bounds__(kEmitThreads) slice_codes_kernel(const __grid_constant__ KGroup g,
                                                                    uint8_t* __restrict__ ws)
 {
+    ptx::griddep_wait();  // the kernel ahead in the stream
+    ptx::griddep_launch();
     constexpr int W = kBig ? kBigSlices : kWarps;  // slices per tile
     constexpr int R = W / 2;                       // rounds: 16 words per slice, 32 per round
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
@@ -1241,6 +1251,8 @@ template <bool kBig>
 __global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const __grid_constant__ KGroup g,
                                                                          uint8_t* __restrict__ ws)
 {
+    ptx::griddep_wait();  // the kernel ahead in the stream
+    ptx::griddep_launch();
     constexpr int W = kBig ? kBigSlices : kWarps;  // slices per tile
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
     for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) tb[e] = g.layer[e].tile_begin;
@@ -1336,19 +1348,20 @@ cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t strea
     const long long cap = (long long)di.sms * occ;
     const uint32_t grid = (uint32_t)((long long)g.total_tiles < cap ? (long long)g.total_tiles : cap);
     if (ev_before && (e = cudaEventRecord(ev_before, stream)) != cudaSuccess) return e;
-    kern<<<grid, threads, smem, stream>>>(g, static_cast<uint8_t*>(ws));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_after(kern, dim3(grid), dim3(threads), smem, stream, g, static_cast<uint8_t*>(ws))) != cudaSuccess)
+        return e;
     if (ev_mid && (e = cudaEventRecord(ev_mid, stream)) != cudaSuccess) return e;
     uint32_t max_tiles = 0;  // the largest layer sets the chunks per layer
     for (int l = 0; l < g.num_layers; ++l) max_tiles = g.layer[l].num_tiles > max_tiles ? g.layer[l].num_tiles : max_tiles;
     const dim3 fgrid((max_tiles + kFinThreads - 1) / kFinThreads, (unsigned)g.num_layers);
-    slice_finalize_kernel<<<fgrid, kFinThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_after(slice_finalize_kernel, fgrid, dim3(kFinThreads), 0, stream, g, static_cast<uint8_t*>(ws))) !=
+        cudaSuccess)
+        return e;
     if (g.lazy) {  // codes only: one warp per tile
         const uint32_t cgrid = (g.total_tiles + kEmitWarps - 1) / kEmitWarps;
-        if (g.big) slice_codes_kernel<true><<<cgrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
-        else slice_codes_kernel<false><<<cgrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
-        if ((e = cudaGetLastError()) != cudaSuccess) return e;
+        e = launch_after(g.big ? slice_codes_kernel<true> : slice_codes_kernel<false>, dim3(cgrid), dim3(kEmitThreads), 0,
+                         stream, g, static_cast<uint8_t*>(ws));
+        if (e != cudaSuccess) return e;
         if (ev_after) e = cudaEventRecord(ev_after, stream);
         return e;
     }
@@ -1363,8 +1376,8 @@ cudaError_t launch_compress_sliced(const KGroup& g, void* ws, cudaStream_t strea
     const uint32_t eneed = (g.total_tiles + kEmitWarps - 1) / kEmitWarps;
     const uint32_t ecap = (uint32_t)di.sms * (uint32_t)eocc;
     const uint32_t egrid = eneed < ecap ? eneed : ecap;
-    ekern<<<egrid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    if ((e = launch_after(ekern, dim3(egrid), dim3(kEmitThreads), 0, stream, g, static_cast<uint8_t*>(ws))) != cudaSuccess)
+        return e;
     if (ev_after) e = cudaEventRecord(ev_after, stream);
     return e;
 }
@@ -1384,9 +1397,9 @@ cudaError_t launch_materialize_sliced(const KGroup& g, void* ws, cudaStream_t st
     const uint64_t blocks_needed = (units + kEmitThreads / 32 - 1) / (kEmitThreads / 32);
     const uint64_t cap = (uint64_t)di.sms * 8;
     const uint32_t grid = (uint32_t)(blocks_needed < cap ? blocks_needed : cap);
-    if (g.big) slice_materialize_kernel<true><<<grid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
-    else slice_materialize_kernel<false><<<grid, kEmitThreads, 0, stream>>>(g, static_cast<uint8_t*>(ws));
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
+    e = launch_after(g.big ? slice_materialize_kernel<true> : slice_materialize_kernel<false>, dim3(grid),
+                     dim3(kEmitThreads), 0, stream, g, static_cast<uint8_t*>(ws));
+    if (e != cudaSuccess) return e;
     // the corrections are applied: the next call must not apply them again
     return cudaMemsetAsync(static_cast<uint8_t*>(ws) + offsetof(Ctl, pending), 0, sizeof(uint32_t), stream);
 }

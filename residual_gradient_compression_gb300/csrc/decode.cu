@@ -112,7 +112,8 @@ __device__ __forceinline__ Run run_of(const KGroup& g, const uint32_t* vb, uint3
 __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_constant__ KGroup g,
                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
-    ptx::griddep_launch();  // the scan's launch may start; it waits for these sums
+    ptx::griddep_wait();  // whatever the stream ran before
+    ptx::griddep_launch();
     __shared__ uint32_t vb[kMaxGroup + 1];
     __shared__ uint32_t sums_s[kDecThreads / 32][kValBins];
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) vb[e] = p.val_begin[e];
@@ -1169,26 +1170,6 @@ DecDeviceInfo g_ddev[64];
 
 }  // namespace
 
-// Launches a kernel that begins with ptx::griddep_wait() behind the previous kernel of
-// the stream with programmatic dependent launch: its blocks may be scheduled while
-// that kernel's last blocks run, and wait there until its writes are visible.
-template <typename... KArgs, typename... Args>
-cudaError_t launch_after(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
-                         Args&&... args)
-{
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = grid;
-    cfg.blockDim = block;
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-}
-
 cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cudaStream_t stream)
 {
     int dev = 0;
@@ -1203,8 +1184,7 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     uint8_t* w = static_cast<uint8_t*>(ws);
     const uint64_t vtasks = (uint64_t)p.K * p.val_begin[g.num_layers];  // (learner, run) tasks
     const uint64_t wpb = kDecThreads / 32;
-    tile_sums_kernel<<<(unsigned)((vtasks + wpb - 1) / wpb), kDecThreads, 0, stream>>>(g, p, w);
-    e = cudaGetLastError();
+    e = launch_after(tile_sums_kernel, dim3((unsigned)((vtasks + wpb - 1) / wpb)), dim3(kDecThreads), 0, stream, g, p, w);
     if (e != cudaSuccess) return e;
     // scan chunks: at least 8192 tiles, at most 64 chunks per message
     uint32_t max_tiles = 0;
