@@ -400,7 +400,34 @@ __device__ __forceinline__ void chk_run(const uint8_t* codes, uint32_t run, uint
     }
 }
 
-__global__ void __launch_bounds__(kDecThreads, 4) check_kernel(const __grid_constant__ KGroup g,
+// Loads that the compiler keeps where they are written (ahead of a branch that could
+// make them unneeded), so that they are in flight together.
+__device__ __forceinline__ uint32_t ld_early_u8(const uint8_t* a)
+{
+    unsigned short v;
+    asm volatile("ld.global.u8 %0, [%1];" : "=h"(v) : "l"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_early_u8_nc(const uint8_t* a)
+{
+    unsigned short v;
+    asm volatile("ld.global.nc.u8 %0, [%1];" : "=h"(v) : "l"(a));
+    return v;
+}
+__device__ __forceinline__ uint32_t ld_early_u16(const uint16_t* a)
+{
+    unsigned short v;
+    asm volatile("ld.global.nc.u16 %0, [%1];" : "=h"(v) : "l"(a));
+    return v;
+}
+__device__ __forceinline__ uint64_t ld_early_u64(const uint64_t* a)
+{
+    uint64_t v;
+    asm volatile("ld.global.nc.u64 %0, [%1];" : "=l"(v) : "l"(a));
+    return v;
+}
+
+__global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constant__ KGroup g,
                                                             const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
     ptx::griddep_wait();  // the offsets and the rejections so far
@@ -417,22 +444,28 @@ __global__ void __launch_bounds__(kDecThreads, 4) check_kernel(const __grid_cons
     const int k = (int)(task / per_learner);
     const uint32_t u = (uint32_t)(task - (uint64_t)k * per_learner);
     const int l = layer_of_chk(cb, g.num_layers, u);
-    if (ws[16 + l * K + k]) return;  // rejected already: nothing more of it is read
     const KLayer& ly = g.layer[l];
+    // A message too short for its counts was rejected by the counting kernel and
+    // nothing of it is read; otherwise its rejection byte (set by the counting or the
+    // scan kernel), its counts and its tile offset are loaded together, and a
+    // rejected message is left there.
+    if (p.len[l * K + k] < 8ull + 2ull * ly.nbins) return;
+    const uint32_t rejected = ld_early_u8(ws + 16 + l * K + k);
     const uint32_t i = u - cb[l];
     const uint32_t bpt = ly.bins_per_tile;
     if (ly.bin_len >= kChkLongBin) {  // long bins: task i is tile i, the lanes over each bin's codes
         const uint32_t tb0 = i * bpt;
         const uint32_t nbt = min(bpt, ly.nbins - tb0);  // <= 4 bins of 1024 or more
         const uint8_t* msg = p.msg[l * K + k];
-        const uint32_t c = (uint32_t)lane < nbt ? reinterpret_cast<const uint16_t*>(msg + 8)[tb0 + lane] : 0u;
+        const uint32_t c = (uint32_t)lane < nbt ? ld_early_u16(reinterpret_cast<const uint16_t*>(msg + 8) + tb0 + lane) : 0u;
+        const uint64_t toff = ld_early_u64(tile_offsets(ws, k, g.total_tiles) + ly.tile_begin + i);
+        if (rejected) return;
         uint32_t incl = c;
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) {
             const uint32_t y = __shfl_up_sync(kFull, incl, o);
             if (lane >= o) incl += y;
         }
-        const uint64_t toff = tile_offsets(ws, k, g.total_tiles)[ly.tile_begin + i];
         const uint8_t* codes = msg + 8 + 2ull * ly.nbins;
         const bool wide = ly.code_bytes == 2;
         bool ok = true;
@@ -475,16 +508,18 @@ __global__ void __launch_bounds__(kDecThreads, 4) check_kernel(const __grid_cons
     }
     const uint8_t* msg = p.msg[l * K + k];
     const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8);
-    if (!whole) {
-        const uint32_t tb0 = (b0 / bpt) * bpt;
-        for (uint32_t b = tb0 + lane; b < b0; b += 32) pre += cnt[b];
-        pre = __reduce_add_sync(kFull, pre);
-    }
     uint32_t c[R], ex[R];  // bin r * 32 + lane: its count and the task's codes before it
 #pragma unroll
     for (int r = 0; r < R; ++r) {
         const uint32_t j = r * 32 + lane;
-        c[r] = j < nb ? cnt[b0 + j] : 0u;
+        c[r] = j < nb ? ld_early_u16(cnt + b0 + j) : 0u;
+    }
+    const uint64_t toff = ld_early_u64(tile_offsets(ws, k, g.total_tiles) + ly.tile_begin + b0 / bpt);
+    if (rejected) return;
+    if (!whole) {
+        const uint32_t tb0 = (b0 / bpt) * bpt;
+        for (uint32_t b = tb0 + lane; b < b0; b += 32) pre += cnt[b];
+        pre = __reduce_add_sync(kFull, pre);
     }
     uint32_t run = 0;
 #pragma unroll
@@ -499,7 +534,7 @@ __global__ void __launch_bounds__(kDecThreads, 4) check_kernel(const __grid_cons
         run += __shfl_sync(kFull, incl, 31);
     }
     // The task's codes are contiguous: positions 0 .. run - 1 from its first code.
-    const uint64_t first = tile_offsets(ws, k, g.total_tiles)[ly.tile_begin + b0 / bpt] + pre;
+    const uint64_t first = toff + pre;
     const bool wide = ly.code_bytes == 2;
     const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (uint64_t)ly.code_bytes * first;
     auto off_at = [&](uint32_t q) -> int32_t {
@@ -509,16 +544,32 @@ __global__ void __launch_bounds__(kDecThreads, 4) check_kernel(const __grid_cons
     // offsets rise strictly within every bin exactly when every descent is the first
     // code of a bin, i.e. when the descents number as many as the first codes (of the
     // nonempty bins, past position 0) that are descents.
-    uint32_t at_starts = 0;
+    // (the codes at the bins' first codes are loaded before the run's, so that both
+    // are in flight at once)
+    uint32_t at_cur[R], at_prev[R];
 #pragma unroll
-    for (int r = 0; r < R; ++r)
-        if (c[r] != 0u && ex[r] != 0u) at_starts += off_at(ex[r]) <= off_at(ex[r] - 1u) ? 1u : 0u;
+    for (int r = 0; r < R; ++r) {
+        at_cur[r] = at_prev[r] = 0u;
+        if (c[r] != 0u && ex[r] != 0u) {
+            if (wide) {
+                at_cur[r] = ld_early_u16(reinterpret_cast<const uint16_t*>(codes) + ex[r]);
+                at_prev[r] = ld_early_u16(reinterpret_cast<const uint16_t*>(codes) + ex[r] - 1u);
+            } else {
+                at_cur[r] = ld_early_u8_nc(codes + ex[r]);
+                at_prev[r] = ld_early_u8_nc(codes + ex[r] - 1u);
+            }
+        }
+    }
     uint32_t descents = 0;
     int32_t omax = -1;
     if (run) {
         if (wide) chk_run<2>(codes, run, descents, omax, lane);
         else chk_run<1>(codes, run, descents, omax, lane);
     }
+    uint32_t at_starts = 0;
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+        if (c[r] != 0u && ex[r] != 0u) at_starts += (at_cur[r] >> 1) <= (at_prev[r] >> 1) ? 1u : 0u;
     // Every offset is below its bin's length: L_T, except in the layer's last bin, whose
     // codes end the task when the task holds that bin; once the offsets rise within it,
     // its last code is its largest.
