@@ -197,17 +197,15 @@ constexpr size_t kDecodeFixed = 10240;
 constexpr size_t kDecodeLayerCodes = 2048;  // offset of the (layer, learner) code counts
 constexpr int kMaxDecodePairs = 1024;  // num_layers * K per launch
 constexpr uint64_t kBadOffset = ~0ull;
-// Per learner: the tiles' code offsets (u64; the scan writes those of the runs' first
-// tiles, the check kernel the others) and the runs' code sums (u32, 0xffffffff for a
-// run whose counts are invalid; a run is at most one task of kValBins bins, so there
-// are no more runs than tiles).
+// Per learner: the tiles' code offsets (u64) and, before the scan turns them into
+// offsets, the tiles' code sums (u32, 0xffffffff for a tile whose counts are invalid).
 __host__ __device__ inline size_t decode_sums_offset(uint64_t total_tiles) { return 8 * (size_t)total_tiles; }
 __host__ __device__ inline size_t decode_per_learner(uint64_t total_tiles)
 {
     return 8 * (size_t)total_tiles + ((4 * (size_t)total_tiles + 15) & ~(size_t)15);
 }
-// Counting and scanning: one run per kValBins bins of whole tiles of one layer (one
-// tile when a tile holds more).
+// Code validation: one task per run of whole tiles of one layer holding at most
+// kValBins bins (one tile when a tile holds more).
 constexpr uint32_t kValBins = 128;
 __host__ __device__ inline uint32_t val_tiles_per_task(uint32_t bins_per_tile)
 {

@@ -350,7 +350,6 @@ template <int S, bool kLazy, bool kLS>
 __global__ void __launch_bounds__(kThreads, 3) slice_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
 {
     ptx::griddep_wait();  // the kernel ahead in the stream
-    ptx::griddep_launch();
     extern __shared__ __align__(128) uint8_t smem[];
     const SlicePlan P = slice_plan(g.d_size, S, g.num_layers);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -613,7 +612,6 @@ template <int S, bool kLazy, bool kLS>
 __global__ void __maxnreg__(kBigMaxRegs) block_kernel(const __grid_constant__ KGroup g, uint8_t* __restrict__ ws)
 {
     ptx::griddep_wait();  // the kernel ahead in the stream
-    ptx::griddep_launch();
     extern __shared__ __align__(128) uint8_t smem[];
     const int W = (int)(blockDim.x >> 5);
     const BigPlan P = big_plan(g.d_size, S, g.num_layers, W);
@@ -884,7 +882,6 @@ __global__ void __launch_bounds__(kFinThreads) slice_finalize_kernel(const __gri
                                                                      uint8_t* __restrict__ ws)
 {
     ptx::griddep_wait();  // the kernel ahead in the stream
-    ptx::griddep_launch();
     __shared__ unsigned long long tmp[256];
     __shared__ unsigned long long words[kSumWords];
     __shared__ unsigned long long red[kFinWarps];
@@ -1031,7 +1028,6 @@ __global__ void __launch_bounds__(kEmitThreads, kBig ? 4 : 5) slice_emit_kernel(
                                                                              uint8_t* __restrict__ ws)
 {
     ptx::griddep_wait();  // the kernel ahead in the stream
-    ptx::griddep_launch();
     constexpr int H = kBig ? 2 : 1;
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
     __shared__ uint16_t lists[kEmitWarps][kListCap];
@@ -1162,7 +1158,6 @@ __global__ void __launch_bounds__(kEmitThreads) slice_codes_kernel(const __grid_
                                                                    uint8_t* __restrict__ ws)
 {
     ptx::griddep_wait();  // the kernel ahead in the stream
-    ptx::griddep_launch();
     constexpr int W = kBig ? kBigSlices : kWarps;  // slices per tile
     constexpr int R = W / 2;                       // rounds: 16 words per slice, 32 per round
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
@@ -1252,7 +1247,6 @@ __global__ void __launch_bounds__(kEmitThreads) slice_materialize_kernel(const _
                                                                          uint8_t* __restrict__ ws)
 {
     ptx::griddep_wait();  // the kernel ahead in the stream
-    ptx::griddep_launch();
     constexpr int W = kBig ? kBigSlices : kWarps;  // slices per tile
     __shared__ uint32_t tb[kMaxGroup];  // first tile of each layer
     for (int e = threadIdx.x; e < g.num_layers; e += kEmitThreads) tb[e] = g.layer[e].tile_begin;

@@ -7,16 +7,14 @@
 // order, dense[j] = fl32(dense[j] + sign * s_k) for k = 0..K-1.
 //
 // Five launches:
-//   tile_sums   per (learner, run of tiles of up to 128 bins): check that the message
-//               is long enough to hold its header and counts, check the header's B
-//               and the run's per-bin counts, and sum them;
-//   tile_scan   per (message, chunk of runs): exclusive prefix of the run sums, i.e.
-//               where each run's codes start in that message (its first tile's
-//               offset), the message's total, and the check that its length is
-//               exactly 8 + 2B + w * total;
-//   check       per (learner, 128 bins, or one tile of long bins): the offsets of the
-//               task's other tiles, and within every bin the code offsets rise
-//               strictly and stay below the bin's length;
+//   tile_sums   per (learner, run of tiles): check that the message is long enough to
+//               hold its header and counts, check the header's B and the tiles'
+//               per-bin counts, and sum the counts of each tile;
+//   tile_scan   per (message, chunk of tiles): exclusive prefix of the tile sums, i.e.
+//               where each tile's codes start in that message, the message's total,
+//               and the check that its length is exactly 8 + 2B + w * total;
+//   check       per (learner, 128 bins, or one tile of long bins): within every bin
+//               the code offsets rise strictly and stay below the bin's length;
 //   accumulate  per tile of the layers that are streamed: the dense tile is staged
 //               in shared memory, every learner's codes for the tile are applied in
 //               learner order, and the tile is written back;
@@ -107,17 +105,16 @@ __device__ __forceinline__ Run run_of(const KGroup& g, const uint32_t* vb, uint3
 
 // One warp per (learner k, run): the message must be at least 8 + 2B bytes long
 // (else nothing of it is read), the header's B must equal the layer's B, and no
-// count may exceed its bin's length; otherwise the run's sum is kBadSum. Lanes take
-// the run's bins (all loads issued at once, coalesced) and the warp sums their
-// counts into the run's entry of the sums array (run u of learner k at [u]). The
-// warp of a message's first run also clears the message's rejection byte, which the
-// later kernels set.
+// count may exceed its bin's length; otherwise every tile sum of the run is
+// kBadSum. Lanes take the run's bins (all loads issued at once, coalesced) and add
+// them into per-tile sums in shared memory. The warp of a message's first run also
+// clears the message's rejection byte, which the later kernels set.
 __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_constant__ KGroup g,
                                                                 const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
     ptx::griddep_wait();  // whatever the stream ran before
-    ptx::griddep_launch();
     __shared__ uint32_t vb[kMaxGroup + 1];
+    __shared__ uint32_t sums_s[kDecThreads / 32][kValBins];
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) vb[e] = p.val_begin[e];
     if (blockIdx.x == 0 && threadIdx.x == 0) reinterpret_cast<uint32_t*>(ws)[2] = 0u;  // scan blocks done
     __syncthreads();
@@ -128,55 +125,61 @@ __global__ void __launch_bounds__(kDecThreads) tile_sums_kernel(const __grid_con
     const uint64_t task = (uint64_t)blockIdx.x * (kDecThreads / 32) + (threadIdx.x >> 5);
     if (task >= (uint64_t)K * per_learner) return;
     const int k = (int)(task / per_learner);
-    const uint32_t u = (uint32_t)(task - (uint64_t)k * per_learner);
-    const Run R = run_of(g, vb, u);
+    const Run R = run_of(g, vb, (uint32_t)(task - (uint64_t)k * per_learner));
     const int l = R.layer;
     const KLayer& ly = g.layer[l];
     if (R.t0 == ly.tile_begin && lane == 0) ws[16 + l * K + k] = 0;
-    uint32_t* out = tile_sums_of(ws, k, T) + u;
+    uint32_t* out = tile_sums_of(ws, k, T) + R.t0;
     const uint8_t* msg = p.msg[l * K + k];
     if (p.len[l * K + k] < 8ull + 2ull * ly.nbins) {  // too short for its header and counts: read nothing
-        if (lane == 0) *out = kBadSum;
+        for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = kBadSum;
         return;
     }
     const uint32_t hdr_b = *reinterpret_cast<const uint32_t*>(msg + 4);
     const uint16_t* cnt = reinterpret_cast<const uint16_t*>(msg + 8) + R.b0;
     const uint32_t last_len = (uint32_t)(ly.n - (int64_t)(ly.nbins - 1) * ly.bin_len);
     bool ok = true;
-    uint32_t sum = 0;
-    if (R.nb <= kValBins) {
-        uint32_t c[kValBins / 32];
-#pragma unroll
-        for (int i = 0; i < (int)(kValBins / 32); ++i) {
-            const uint32_t b = i * 32 + lane;
-            c[i] = b < R.nb ? cnt[b] : 0u;
-        }
-#pragma unroll
-        for (int i = 0; i < (int)(kValBins / 32); ++i) {
-            const uint32_t b = i * 32 + lane;
-            ok = ok && c[i] <= (R.b0 + b == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len);
-            sum += c[i];
-        }
-    } else {  // one tile of more than kValBins bins
+    if (R.ntiles == 1) {  // one tile (possibly of more than kValBins bins): a warp sum
+        uint32_t sum = 0;
         for (uint32_t b = lane; b < R.nb; b += 32) {
             const uint32_t c = cnt[b];
             ok = ok && c <= (R.b0 + b == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len);
             sum += c;
         }
+        ok = __all_sync(kFull, ok) && hdr_b == ly.nbins;
+        sum = __reduce_add_sync(kFull, sum);
+        if (lane == 0) out[0] = ok ? sum : kBadSum;
+        return;
+    }
+    uint32_t* sums = sums_s[threadIdx.x >> 5];
+    for (uint32_t i = lane; i < R.ntiles; i += 32) sums[i] = 0u;
+    __syncwarp();
+    uint32_t c[kValBins / 32];
+#pragma unroll
+    for (int i = 0; i < (int)(kValBins / 32); ++i) {
+        const uint32_t b = i * 32 + lane;
+        c[i] = b < R.nb ? cnt[b] : 0u;
+    }
+#pragma unroll
+    for (int i = 0; i < (int)(kValBins / 32); ++i) {
+        const uint32_t b = i * 32 + lane;
+        if (b < R.nb) {
+            ok = ok && c[i] <= (R.b0 + b == ly.nbins - 1 ? last_len : (uint32_t)ly.bin_len);
+            if (c[i]) atomicAdd(&sums[b / ly.bins_per_tile], c[i]);
+        }
     }
     ok = __all_sync(kFull, ok) && hdr_b == ly.nbins;
-    sum = __reduce_add_sync(kFull, sum);
-    if (lane == 0) *out = ok ? sum : kBadSum;
+    __syncwarp();
+    for (uint32_t i = lane; i < R.ntiles; i += 32) out[i] = ok ? sums[i] : kBadSum;
 }
 
-// Grid (chunk, layer * K + learner): the run sums of one message become the runs'
-// exclusive code offsets, written as the code offsets of the runs' first tiles (the
-// check kernel fills in the other tiles' offsets), a chunk of CH runs per CTA. The
-// CTA sums the message's runs before its chunk (coalesced, kScanPer loads per thread
-// in flight; the repeated reads are small and hit L2), then scans its own chunk in
-// passes of kScanPer * 1024 runs (thread tid loads runs pass + i * 1024 + tid; the
-// warps scan each row with shuffles and one warp scans the row-by-warp totals in row
-// order). A chunk with a bad run rejects the message; the CTA of the message's last chunk
+// Grid (chunk, layer * K + learner): the tile sums of one message become the tiles'
+// exclusive code offsets, a chunk of CH tiles per CTA. The CTA sums the message's
+// tiles before its chunk (coalesced, kScanPer loads per thread in flight; the
+// repeated reads are small and hit L2), then scans its own chunk in passes of
+// kScanPer * 1024 tiles (thread tid loads tiles pass + i * 1024 + tid; the warps scan
+// each row with shuffles and one warp scans the row-by-warp totals in row order). A
+// chunk with a bad tile rejects the message; the CTA of the message's last chunk
 // checks that its length is exactly 8 + 2B + w * (its code count) and records that
 // count. The last CTA of the grid decides, per layer, whether the layer is summed in
 // place (all learners' codes < n / 16).
@@ -188,8 +191,7 @@ __global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_co
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws,
                                                                  uint32_t CH)
 {
-    ptx::griddep_wait();  // the run sums
-    ptx::griddep_launch();
+    ptx::griddep_wait();  // the tile sums
     __shared__ unsigned long long wt[kScanPer][kScanWarps];
     __shared__ unsigned long long wx[kScanPer][kScanWarps];
     __shared__ unsigned long long red[kScanWarps];
@@ -205,12 +207,11 @@ __global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_co
         reinterpret_cast<uint32_t*>(ws)[0] = (uint32_t)K;
         reinterpret_cast<uint32_t*>(ws)[1] = (uint32_t)g.num_layers;
     }
-    const uint32_t nt = p.val_begin[l + 1] - p.val_begin[l];  // the layer's runs
-    const uint32_t tpr = val_tiles_per_task(ly.bins_per_tile);  // tiles per run
+    const uint32_t nt = ly.num_tiles;
     const uint32_t c0 = blockIdx.x * CH;
     if (c0 < nt) {
         const uint32_t c1 = min(nt, c0 + CH);
-        const uint32_t* sum = tile_sums_of(ws, k, T) + p.val_begin[l];
+        const uint32_t* sum = tile_sums_of(ws, k, T) + ly.tile_begin;
         uint64_t* off = tile_offsets(ws, k, T) + ly.tile_begin;
         // the codes of the message's tiles before the chunk
         unsigned long long before = 0;
@@ -282,7 +283,7 @@ __global__ void __launch_bounds__(kScanThreads) tile_scan_kernel(const __grid_co
 #pragma unroll
             for (int i = 0; i < kScanPer; ++i) {
                 const uint32_t j = base + i * kScanThreads + tid;
-                if (j < c1) off[(size_t)j * tpr] = wx[i][warp] + (inc[i] - v[i]);
+                if (j < c1) off[j] = wx[i][warp] + (inc[i] - v[i]);
             }
         }
         __syncthreads();
@@ -424,14 +425,16 @@ __device__ __forceinline__ uint64_t ld_early_u64(const uint64_t* a)
     return v;
 }
 
-__global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constant__ KGroup g,
+// kLongOnly: every layer's bins have kChkLongBin elements or more. Those walks are
+// bound by load latency and run best with four CTAs per SM; the short-bin path runs
+// best unconstrained (74 registers, no spills).
+template <bool kLongOnly>
+__global__ void __launch_bounds__(kDecThreads, kLongOnly ? 4 : 1) check_kernel(const __grid_constant__ KGroup g,
                                                             const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
     ptx::griddep_wait();  // the offsets and the rejections so far
-    ptx::griddep_launch();
     constexpr int R = (int)(kChkBins / 32);  // bins per lane
     __shared__ uint32_t cb[kMaxGroup + 1];
-    __shared__ uint32_t ex_s[kDecThreads / 32][kChkBins];  // per warp: the task's count prefix
     for (int e = threadIdx.x; e <= g.num_layers; e += kDecThreads) cb[e] = p.chk_begin[e];
     __syncthreads();
     const int K = p.K;
@@ -451,20 +454,13 @@ __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constan
     const uint32_t rejected = ld_early_u8(ws + 16 + l * K + k);
     const uint32_t i = u - cb[l];
     const uint32_t bpt = ly.bins_per_tile;
-    if (ly.bin_len >= kChkLongBin) {  // long bins: task i is tile i, the lanes over each bin's codes
+    if (kLongOnly || ly.bin_len >= kChkLongBin) {  // long bins: task i is tile i, the lanes over each bin's codes
         const uint32_t tb0 = i * bpt;
         const uint32_t nbt = min(bpt, ly.nbins - tb0);  // <= 4 bins of 1024 or more
         const uint8_t* msg = p.msg[l * K + k];
         const uint32_t c = (uint32_t)lane < nbt ? ld_early_u16(reinterpret_cast<const uint16_t*>(msg + 8) + tb0 + lane) : 0u;
-        // the tile's run: its offset (the scan's) plus the codes of the run's tiles before this one
-        const uint32_t r0 = i - i % val_tiles_per_task(bpt);
-        uint64_t* toffs = tile_offsets(ws, k, g.total_tiles) + ly.tile_begin;
-        const uint64_t roff = ld_early_u64(toffs + r0);
+        const uint64_t toff = ld_early_u64(tile_offsets(ws, k, g.total_tiles) + ly.tile_begin + i);
         if (rejected) return;
-        uint32_t rpre = 0;
-        for (uint32_t b = r0 * bpt + lane; b < tb0; b += 32) rpre += reinterpret_cast<const uint16_t*>(msg + 8)[b];
-        const uint64_t toff = roff + __reduce_add_sync(kFull, rpre);
-        if (i != r0 && lane == 0) toffs[i] = toff;
         uint32_t incl = c;
 #pragma unroll
         for (int o = 1; o < 8; o <<= 1) {
@@ -538,19 +534,8 @@ __global__ void __launch_bounds__(kDecThreads) check_kernel(const __grid_constan
         ex[r] = run + incl - c[r];
         run += __shfl_sync(kFull, incl, 31);
     }
-    // The task's codes are contiguous: positions 0 .. run - 1 from its first code. The
-    // scan wrote the offset of the run's (for whole tiles: the task's) first tile; the
-    // offsets of the task's other tiles are written here.
+    // The task's codes are contiguous: positions 0 .. run - 1 from its first code.
     const uint64_t first = toff + pre;
-    if (whole && nb > bpt) {
-        uint32_t* exw = ex_s[threadIdx.x >> 5];
-#pragma unroll
-        for (int r = 0; r < R; ++r) exw[r * 32 + lane] = ex[r];
-        __syncwarp();
-        const uint32_t ntl = (nb + bpt - 1) / bpt;  // the task's tiles
-        uint64_t* toffs = tile_offsets(ws, k, g.total_tiles) + ly.tile_begin + b0 / bpt;
-        for (uint32_t m = 1 + lane; m < ntl; m += 32) toffs[m] = first + exw[m * bpt];
-    }
     const bool wide = ly.code_bytes == 2;
     const uint8_t* codes = msg + 8 + 2ull * ly.nbins + (uint64_t)ly.code_bytes * first;
     auto off_at = [&](uint32_t q) -> int32_t {
@@ -1035,7 +1020,6 @@ __global__ void __launch_bounds__(kDecThreads, 5) accumulate_kernel(const __grid
                                                                  const __grid_constant__ DecodeParams p, uint8_t* ws)
 {
     ptx::griddep_wait();  // every check
-    ptx::griddep_launch();
     constexpr bool kFused = kOpt != kOptNone;
     extern __shared__ __align__(128) uint8_t smem[];
     const uint32_t stage_bytes = acc_stage_bytes(g.tile_cap, kOpt);
@@ -1254,18 +1238,18 @@ cudaError_t launch_decode(const KGroup& g, const DecodeParams& p, void* ws, cuda
     e = launch_after(tile_sums_kernel, dim3((unsigned)((vtasks + wpb - 1) / wpb)), dim3(kDecThreads), 0, stream, g, p, w);
     if (e != cudaSuccess) return e;
     // scan chunks: at least 8192 tiles, at most 64 chunks per message
-    uint32_t max_runs = 0;
-    for (int l = 0; l < g.num_layers; ++l) {
-        const uint32_t r = p.val_begin[l + 1] - p.val_begin[l];
-        max_runs = r > max_runs ? r : max_runs;
-    }
+    uint32_t max_tiles = 0;
+    for (int l = 0; l < g.num_layers; ++l) max_tiles = g.layer[l].num_tiles > max_tiles ? g.layer[l].num_tiles : max_tiles;
     uint32_t CH = kScanPer * kScanThreads * 2;
-    while ((max_runs + CH - 1) / CH > 64u) CH += kScanPer * kScanThreads;
-    const dim3 sgrid((max_runs + CH - 1) / CH, (unsigned)(g.num_layers * p.K));
+    while ((max_tiles + CH - 1) / CH > 64u) CH += kScanPer * kScanThreads;
+    const dim3 sgrid((max_tiles + CH - 1) / CH, (unsigned)(g.num_layers * p.K));
     e = launch_after(tile_scan_kernel, sgrid, dim3(kScanThreads), 0, stream, g, p, w, CH);
     if (e != cudaSuccess) return e;
     const uint64_t ctasks = (uint64_t)p.K * p.chk_begin[g.num_layers];  // (learner, kChkBins bins) tasks
-    e = launch_after(check_kernel, dim3((unsigned)((ctasks + wpb - 1) / wpb)), dim3(kDecThreads), 0, stream, g, p, w);
+    bool long_only = true;
+    for (int l = 0; l < g.num_layers; ++l) long_only = long_only && g.layer[l].bin_len >= kChkLongBin;
+    e = launch_after(long_only ? check_kernel<true> : check_kernel<false>, dim3((unsigned)((ctasks + wpb - 1) / wpb)),
+                     dim3(kDecThreads), 0, stream, g, p, w);
     if (e != cudaSuccess) return e;
     const int opt = p.opt;
     const uint32_t smem = acc_smem_bytes(g.tile_cap, g.max_bins, opt);
