@@ -35,6 +35,11 @@
  *   - Work is enqueued on `stream` and returns before it runs; results, the message
  *     length and the device-side status are read back with adacomp_query /
  *     adacomp_decode_status. Every call is deterministic: same inputs, same bits.
+ *   - A debug build of the library (compiled with ADACOMP_DEBUG_CHECKS defined)
+ *     makes every compress, decode and materialise call wait for `stream` after its
+ *     launches, unless the stream is being captured, and return ADACOMP_ERR_CUDA
+ *     when its kernels raised an error, so that the error is reported by the call
+ *     that caused it.
  *   - Argument errors are reported synchronously before anything is enqueued.
  *     ADACOMP_ERR_CUDA reports a failed launch (cudaGetLastError).
  *   - Workspaces: a compress workspace must be zero-filled before its first use

@@ -17,7 +17,10 @@ from typing import Sequence
 
 import torch
 
-from .build import LIB as _LIB_PATH
+from .build import lib_path as _lib_path
+
+# libadacomp.so, or libadacomp_debug.so when ADACOMP_DEBUG_CHECKS=1 (a debug build)
+_LIB_PATH = _lib_path()
 
 OK, ERR_INVALID_ARG, ERR_ALIGNMENT, ERR_WORKSPACE, ERR_CAPACITY, ERR_CUDA, ERR_TIMEOUT, \
     ERR_BAD_MESSAGE = range(8)

@@ -26,6 +26,26 @@ struct adacomp_layer {
     uint32_t rule = ADACOMP_RULE_ADACOMP;              // selection rule (adacomp_set_selection_rule)
 };
 
+namespace adacomp {
+// The status of a call's launches. Built with ADACOMP_DEBUG_CHECKS (a debug build),
+// the call also waits for its stream, unless the stream is being captured, so that an
+// error raised while its kernels run is returned by the call that launched them
+// rather than by a later one.
+adacomp_status launch_result(cudaError_t e, cudaStream_t stream)
+{
+    if (e != cudaSuccess) return ADACOMP_ERR_CUDA;
+#ifdef ADACOMP_DEBUG_CHECKS
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) return ADACOMP_ERR_CUDA;
+    if (cap == cudaStreamCaptureStatusNone && cudaStreamSynchronize(stream) != cudaSuccess) return ADACOMP_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return ADACOMP_ERR_CUDA;
+#else
+    (void)stream;
+#endif
+    return ADACOMP_OK;
+}
+}  // namespace adacomp
+
 namespace {
 // A named range on the host timeline around an entry point's launches (a no-op
 // unless a profiler that records NVTX ranges is attached), so that a trace shows
@@ -147,7 +167,8 @@ void fill_group(const adacomp_layer* h, KGroup* g)
     for (size_t i = 0; i < h->layers.size(); ++i) g->layer[i] = h->layers[i];
 }
 
-adacomp_status cuda_status(cudaError_t e) { return e == cudaSuccess ? ADACOMP_OK : ADACOMP_ERR_CUDA; }
+
+adacomp_status launched(cudaError_t e, cudaStream_t stream) { return adacomp::launch_result(e, stream); }
 
 }  // namespace
 
@@ -194,7 +215,7 @@ adacomp_status adacomp_compress_group(adacomp_layer_t h, float* const* residue, 
     }
     const cudaError_t e = adacomp::launch_compress(*g, ws, stream, h->ev[0], h->ev[1], h->ev[2]);
     delete g;
-    return cuda_status(e);
+    return launched(e, stream);
 }
 
 adacomp_status adacomp_compress(adacomp_layer_t h, float* residue, const void* dW, void* msg, size_t msg_capacity,
@@ -276,7 +297,7 @@ adacomp_status decode_group(adacomp_layer_t h, const void* const* msgs, const ui
             p->len[l * K + k] = msg_bytes[l * K + k];
         }
     }
-    if (st == ADACOMP_OK) st = cuda_status(adacomp::launch_decode(*g, *p, ws, stream));
+    if (st == ADACOMP_OK) st = launched(adacomp::launch_decode(*g, *p, ws, stream), stream);
     delete g;
     delete p;
     return st;
@@ -445,7 +466,7 @@ adacomp_status adacomp_materialize_group(adacomp_layer_t h, float* const* residu
     }
     const cudaError_t e = adacomp::launch_materialize(*g, ws, stream);
     delete g;
-    return cuda_status(e);
+    return launched(e, stream);
 }
 
 adacomp_status adacomp_materialize(adacomp_layer_t h, float* residue, void* ws, size_t ws_bytes, cudaStream_t stream)

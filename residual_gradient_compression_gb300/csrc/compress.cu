@@ -1609,6 +1609,10 @@ cudaError_t launch_materialize(const KGroup& g, void* ws, cudaStream_t stream)
 
 #include "adacomp.h"
 
+namespace adacomp {
+adacomp_status launch_result(cudaError_t e, cudaStream_t stream);  // abi.cu
+}
+
 namespace {
 constexpr size_t kStaticScratchBytes = ADACOMP_STATIC_WS_BYTES;  // 1 MiB
 static __device__ __align__(256) uint8_t g_static_scratch[kStaticScratchBytes];
@@ -1649,5 +1653,5 @@ extern "C" adacomp_status adacomp_compress_static_ws(adacomp_layer_t h, float* r
         if (cudaMemcpyAsync(result_out, res, sizeof(Result), cudaMemcpyDeviceToDevice, stream) != cudaSuccess)
             return ADACOMP_ERR_CUDA;
     }
-    return ADACOMP_OK;
+    return launch_result(cudaSuccess, stream);
 }
