@@ -52,8 +52,8 @@ def parse_args():
     p.add_argument("--workload", default="flat100m",
                    choices=["resnet50", "fc400k", "lstm_fc", "gpt1p3b", "flat100m"])
     p.add_argument("--bin-len", type=int, default=500, help="L_T for gpt1p3b")
-    p.add_argument("--streams", type=int, default=2, choices=[1, 2],
-                   help="learners' compress calls alternating between two streams (default) or on one")
+    p.add_argument("--streams", type=int, default=3, choices=[1, 2, 3, 4],
+                   help="learners' compress calls taking turns on this many streams (default three)")
     p.add_argument("--layers", type=int, default=0,
                    help="only the first N layers of the workload (a smaller case, for profiling)")
     p.add_argument("--learners", type=int, default=16, help="K for flat100m")
@@ -394,20 +394,22 @@ class DeviceRun:
         def ws_of(k, gi):
             return ws_fixed[k][gi] if ws_fixed is not None else self.ws[i % self.ring][k][gi]
 
-        # the compress calls (learner by learner, launch group by launch group) alternate
-        # between the launch stream and a second stream, so that one call's short
-        # launches (finalise, codes) overlap the next one's streaming kernel; the second
-        # stream starts after everything before the step and the lengths are read once
-        # both are done
-        two = self.args.streams > 1 and self.K * len(self.h) > 1
-        if two:
-            if not hasattr(self, "side"):
-                self.side = torch.cuda.Stream()
-                self.side_ptr = self.ct.c_void_p(self.side.cuda_stream)
-            self.side.wait_stream(torch.cuda.current_stream())
+        # the compress calls (learner by learner, launch group by launch group) take turns
+        # on the launch stream and args.streams - 1 side streams, so that one call's
+        # short launches (finalise, codes) overlap the next one's streaming kernel; the
+        # side streams start after everything before the step and the lengths are read
+        # once all are done
+        nstreams = self.args.streams if self.K * len(self.h) > 1 else 1
+        if nstreams > 1:
+            if len(getattr(self, "sides", [])) < nstreams - 1:
+                self.sides = [torch.cuda.Stream() for _ in range(nstreams - 1)]
+                self.side_ptrs = [self.ct.c_void_p(x.cuda_stream) for x in self.sides]
+            for x in self.sides[:nstreams - 1]:
+                x.wait_stream(torch.cuda.current_stream())
         for k in range(self.K):
             for gi, h in enumerate(self.h):
-                sptr = self.side_ptr if two and (k * len(self.h) + gi) % 2 else stream_ptr
+                turn = (k * len(self.h) + gi) % nstreams
+                sptr = self.side_ptrs[turn - 1] if turn else stream_ptr
                 if k1_events is not None:
                     e = k1_events[k * len(self.h) + gi]
                     L.adacomp_set_timing_events(h.ptr, self.ct.c_void_p(e[0].cuda_event),
@@ -418,8 +420,9 @@ class DeviceRun:
                                               self.c_cap[k][gi], ws.data_ptr(), ws.numel(), sptr)
                 if st:
                     raise RuntimeError(f"adacomp_compress_group: {st}")
-        if two:
-            torch.cuda.current_stream().wait_stream(self.side)
+        if nstreams > 1:
+            for x in self.sides[:nstreams - 1]:
+                torch.cuda.current_stream().wait_stream(x)
         lens = self.message_lengths(ws_of)
         if dec_events is not None:
             dec_events[0].record()
@@ -618,7 +621,7 @@ def run_device(args, rank, world):
         out["e2e"] = run_e2e(args, run, layers, sp, world)
     if not args.no_lazy:
         out["lazy_fixup"] = run_lazy(args, run, sp, world, n_elems)
-    if run.K * len(run.h) > 1 and args.streams == 2:  # the same steps with every call on one stream
+    if run.K * len(run.h) > 1 and args.streams > 1:  # the same steps with every call on one stream
         out["one_stream"] = {"value": n_elems * args.steps * world / (one_ms * 1e-3), "unit": "elements/s",
                              "ms_per_step": one_ms / args.steps}
     if not args.no_sgd:
