@@ -133,6 +133,40 @@ def test_decode_group_mixes_streamed_and_in_place_layers():
         assert np.array_equal(d.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (n, L)
 
 
+def test_decode_group_mixes_long_and_short_bins():
+    """A grouped decode whose layers have bins of 1024 elements or more (L_T = 2048,
+    5000: one check task per tile, the lanes over each bin's codes) beside shorter ones
+    (L_T = 50, 500: 128-bin tasks over contiguous code runs), so the general check
+    kernel takes both branches in one launch; one learner's message of the L_T = 5000
+    layer carries a duplicated offset and is rejected alone. Every layer matches the
+    oracle's learner-order sum bit for bit."""
+    K = 3
+    spec = [(200_003, 50, False), (123_457, 5000, False), (80_000, 2048, True), (60_001, 500, False)]
+    per_layer = [(_sparse_learner_msgs if sparse else _learner_msgs)(n, L, K, seed=11 * i + 5)
+                 for i, (n, L, sparse) in enumerate(spec)]
+    # learner 1 of the L_T = 5000 layer: its second code repeats its first
+    n5, L5 = spec[1][0], spec[1][1]
+    m, mb = per_layer[1][1]
+    bad_np, bad_len = _malformed(m[:mb].cpu().numpy(), n5, L5, "duplicate")
+    big = torch.zeros(bad_np.size + (1 << 16), dtype=torch.uint8, device="cuda")
+    big[:bad_np.size] = torch.from_numpy(bad_np).cuda()
+    per_layer[1][1] = (big, bad_len)
+    h = ac.adacomp_init_group([n for n, _, _ in spec], [L for _, L, _ in spec], [ac.F32] * len(spec))
+    dense0 = [torch.randn(n, device="cuda") * 1e-3 for n, _, _ in spec]
+    dense = [d.clone() for d in dense0]
+    ws = workspace(h.decode_ws_bytes(K))
+    ac.adacomp_decode_accumulate_group(h, [[m for m, _ in pl] for pl in per_layer],
+                                       [[mb for _, mb in pl] for pl in per_layer], dense, ws)
+    assert ac.adacomp_decode_status(h, ws) == ac.ERR_BAD_MESSAGE
+    for i, ((n, L, _), pl, d0, d) in enumerate(zip(spec, per_layer, dense0, dense)):
+        ref = d0.cpu().numpy()
+        flags = np.zeros(K, np.uint8)
+        st = oracle.decode_accumulate(n, L, [m[:mb].cpu().numpy() for m, mb in pl], ref, bad=flags)
+        assert list(flags) == ([0, 1, 0] if i == 1 else [0, 0, 0]), (L, list(flags))
+        assert st == (oracle.ERR_BAD_MESSAGE if i == 1 else oracle.OK)
+        assert np.array_equal(d.cpu().numpy().view(np.uint32), ref.view(np.uint32)), (n, L)
+
+
 def test_flat100m_sixteen_learners_full_size():
     """The aggregation workload at full size: a flat layer of 10^8 elements at
     L_T = 500, 16 learners each compressing its own N(0, 1e-3) dW (the launch
